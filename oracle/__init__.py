@@ -1,0 +1,16 @@
+"""CPU oracle (test infrastructure only; see loglinear_oracle's header)."""
+from .loglinear_oracle import (  # noqa: F401
+    decay_rows,
+    decode_step,
+    fenwick_partition,
+    forward_chunked,
+    forward_direct,
+    hier_rows,
+    level,
+    level_matrix,
+    level_row,
+    linear_attention_recurrent,
+    lssb,
+    recurrence,
+    states_from_buckets,
+)
