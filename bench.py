@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Benchmark of the log-linear attention hot path on GB300; prints ONE JSON line.
+
+A step is one pass of the whole hot path on synthetic seeded inputs resident in HBM:
+the chunked forward on B1 H16 T16384 dk=dv=128 C64 L15 (bf16 q/k/v/out, fp32 log a and
+lambda) followed by one decode step of B128 H16 d128 L15 fp32 states at t = 12345.
+``value`` is forward tokens/s (B*T per forward); decode tokens/s is reported beside it.
+L2 is flushed (a 512 MiB write) between timed steps, outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same per-GPU workload (weak scaling, no collective on
+the data path); the max step time over ranks is used and rank 0 prints the line.
+``--impl reference`` times the CPU oracle (the only reference this method has) on a
+bounded sample of the same forward workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "fwd tokens/s at T=16K,H=16,d=128 bf16 + % of roofline; decode tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return dict(hbm=pk["hbm_gbs"], bf16=pk["bf16_tflops"],
+                    bf16_sus=pk.get("bf16_tflops_sustained", pk["bf16_tflops"]), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+
+def fwd_algorithmic(cfg):
+    """Bytes the forward must move (inputs once, output once) and the FLOPs it must do
+    (causal half of each chunk's C x C products, per-chunk states, one readout GEMM per
+    non-empty inter-chunk level)."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    BH = cfg.B * cfg.H
+    tok = cfg.B * cfg.T * cfg.H
+    bytes_ = tok * (2 * cfg.dk + cfg.dv) * e + tok * 4 + tok * cfg.L * 4 + tok * cfg.dv * e
+    C = cfg.C
+    N = cfg.T // C
+    intra = C * (C + 1) / 2 * 2 * (cfg.dk + cfg.dv) * N
+    states = 2 * C * cfg.dk * cfg.dv * N
+    readout = 2 * C * cfg.dk * cfg.dv * sum(bin(j).count("1") for j in range(N))
+    flops = BH * (intra + states + readout)
+    return bytes_, flops
+
+
+def decode_algorithmic(cfg):
+    """Bytes of the levels the step must read (non-empty after t-1) and write (every
+    level that changes), fp32."""
+    lvl_bytes = cfg.dk * cfg.dv * 4
+    t = cfg.t
+    pre = W.nonempty_levels_before(t, cfg.L)
+    l = (t & -t).bit_length() - 1
+    written = set(pre) | {l + 1}            # decayed, merged, cleared or new
+    return cfg.B * cfg.H * lvl_bytes * (len(pre) + len(written))
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+
+
+def oracle_sample(cfg, seconds, seed=0):
+    """Times the oracle's direct forward on sampled query rows of one head, until about
+    `seconds` of CPU time; returns (tokens/s extrapolated to the whole workload, sample
+    description, threads used)."""
+    import oracle
+    T = cfg.T
+    # one head drawn with the workload's recipe
+    x = W.make_fwd_inputs(cfg.with_(B=1, H=1))
+    rng = np.random.default_rng(seed)
+    rows_done, pairs_done, t0 = 0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        rows = np.sort(rng.choice(T, 64, replace=False))
+        oracle.forward_direct(x["q"], x["k"], x["v"], x["log_a"], x["lam"], rows=rows,
+                              heads=[(0, 0)])
+        rows_done += len(rows)
+        pairs_done += int((rows + 1).sum())
+    el = time.perf_counter() - t0
+    pairs_total = cfg.B * cfg.H * T * (T + 1) / 2
+    t_total = el * pairs_total / pairs_done
+    tok_s = cfg.B * T / t_total
+    threads = torch.get_num_threads()
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        threads = max([i.get("num_threads", 1) for i in info] + [1])
+    except Exception:
+        threads = os.cpu_count()
+    desc = (f"oracle forward_direct (fp64 NumPy) on {rows_done} random query rows of one head "
+            f"of {cfg.name} in {el:.1f} s, extrapolated by (query, source) pair count to "
+            f"B{cfg.B} H{cfg.H} T{T}")
+    return tok_s, desc, threads
+
+
+# ---------------------------------------------------------------- our implementation
+
+
+def run_ours(args, rank, world, local_rank):
+    import log_linear_attention_fwd_gb300 as LL
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = W.FWD_CONFIGS[W.HEADLINE_FWD]
+    dcfg = W.DECODE_CONFIG
+    peaks = load_peaks()
+    x = W.make_fwd_inputs(cfg)
+    d = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
+    out = torch.empty(cfg.B, cfg.T, cfg.H, cfg.dv, device=dev, dtype=d["q"].dtype)
+    in_code = 1 if cfg.dtype == "bf16" else 0
+    path = LL.resolve_path(cfg.dk, cfg.dv, cfg.C, in_code)
+    ws = torch.empty(LL.fwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv, cfg.C, in_code),
+                     device=dev, dtype=torch.uint8)
+    # decode inputs: state generated on the device from a seeded generator (timing only)
+    gen = torch.Generator(device=dev).manual_seed(1234)
+    state = torch.zeros(dcfg.B, dcfg.H, dcfg.L, dcfg.dk, dcfg.dv, device=dev)
+    for lv in W.nonempty_levels_before(dcfg.t, dcfg.L):
+        state[:, :, lv].normal_(0.0, 0.05, generator=gen)
+    dinp = {k: (None if v is None else v.to(dev)) for k, v in W.make_decode_step_inputs(dcfg).items()}
+    dout = torch.empty(dcfg.B, dcfg.H, dcfg.dv, device=dev, dtype=torch.float32)
+    flush = torch.empty(512 << 20, device=dev, dtype=torch.uint8)
+    n_ev = 5
+    stream = torch.cuda.current_stream()
+
+    def one_step(ev_f, ev_d):
+        n_k = LL.loglinear_fwd_with_events(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C,
+                                           ev_f, out, ws)
+        ev_d[0].record(stream)
+        LL.loglinear_decode_step(state, dinp["q"], dinp["k"], dinp["v"], dinp["log_a"],
+                                 dinp["lam"], dcfg.t, out=dout)
+        ev_d[1].record(stream)
+        return n_k
+
+    mk = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        one_step(mk(n_ev), mk(2))
+    torch.cuda.synchronize()
+    evs = [(mk(n_ev), mk(2)) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    n_kernels = 0
+    for ef, ed in evs:
+        flush.zero_()
+        n_kernels = one_step(ef, ed)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    t_fwd = [ef[0].elapsed_time(ef[n_kernels]) * 1e-3 for ef, _ in evs]
+    t_stage = [[ef[i].elapsed_time(ef[i + 1]) * 1e-3 for ef, _ in evs] for i in range(n_kernels)]
+    t_dec = [ed[0].elapsed_time(ed[1]) * 1e-3 for _, ed in evs]
+    fwd_mean, dec_mean = sum(t_fwd) / len(t_fwd), sum(t_dec) / len(t_dec)
+    stage_mean = [sum(s) / len(s) for s in t_stage]
+    if world > 1:
+        tt = torch.tensor([fwd_mean, dec_mean], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        fwd_mean, dec_mean = tt.tolist()
+    fwd_tok_s = world * cfg.B * cfg.T / fwd_mean
+    dec_tok_s = world * dcfg.B / dec_mean
+    fbytes, fflops = fwd_algorithmic(cfg)
+    dbytes = decode_algorithmic(dcfg)
+    t_hbm = fbytes / (peaks["hbm"] * 1e9)
+    t_tc = fflops / (peaks["bf16"] * 1e12)
+    stage_names = {"simt": ["simt_chunk_state", "simt_level_scan", "simt_intra_readout"],
+                   "tc": ["tc_chunk_state", "tc_level_scan", "tc_intra_readout"]}[path][-n_kernels:]
+    dom = int(np.argmax(stage_mean))
+    # achieved numbers for the forward pass as a whole and for its dominant kernel
+    roofline_fwd = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+                    "achieved": fbytes / fwd_mean / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
+                    "frac": (fbytes / fwd_mean / 1e9) / peaks["hbm"],
+                    "frac_of_binding_roofline": max(t_hbm, t_tc) / fwd_mean,
+                    "tensor_frac": (fflops / fwd_mean / 1e12) / peaks["bf16"],
+                    "algorithmic_bytes": fbytes, "algorithmic_flops": fflops,
+                    "peak_source": peaks["src"], "traffic": None}
+    dom_bytes = stage_bytes(cfg, path, stage_names[dom])
+    roofline = {"kernel": stage_names[dom], "bound": "hbm",
+                "achieved": dom_bytes / stage_mean[dom] / 1e9, "peak": peaks["hbm"],
+                "unit": "GB/s", "frac": dom_bytes / stage_mean[dom] / 1e9 / peaks["hbm"],
+                "traffic": None, "algorithmic_bytes": dom_bytes, "peak_source": peaks["src"],
+                "us_per_launch": stage_mean[dom] * 1e6}
+    decode = {"tokens_per_s": dec_tok_s, "us_per_step": dec_mean * 1e6,
+              "roofline": {"kernel": "decode_step_kernel", "bound": "hbm",
+                           "achieved": dbytes / dec_mean / 1e9, "peak": peaks["hbm"],
+                           "unit": "GB/s", "frac": dbytes / dec_mean / 1e9 / peaks["hbm"],
+                           "algorithmic_bytes": dbytes, "peak_source": peaks["src"],
+                           "traffic": None},
+              "config": {"workload": dcfg.name, "B": dcfg.B, "H": dcfg.H, "dk": dcfg.dk,
+                         "dv": dcfg.dv, "L": dcfg.L, "t": dcfg.t, "state": "fp32"}}
+    e2e = measure_e2e(LL, cfg, x, dev, ws, args)
+    res = {"metric": METRIC, "value": fwd_tok_s, "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": (fwd_mean + dec_mean) * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": f"{cfg.name}: loglinear_fwd B{cfg.B} H{cfg.H} T{cfg.T} "
+                                  f"dk=dv={cfg.dk} C{cfg.C} L{cfg.L} bf16, + decode "
+                                  f"B{dcfg.B} H{dcfg.H} d{dcfg.dk} L{dcfg.L} t={dcfg.t}",
+                      "B": cfg.B, "H": cfg.H, "T": cfg.T, "dk": cfg.dk, "dv": cfg.dv,
+                      "chunk": cfg.C, "L": cfg.L, "path": path,
+                      "l2": "flushed (512 MiB write) between timed steps",
+                      "parallelism": f"replicas x{world} (independent (b,h) work, no collective)"},
+           "fwd_ms": fwd_mean * 1e3, "fwd_stage_us": dict(zip(stage_names, [s * 1e6 for s in stage_mean])),
+           "roofline": roofline, "roofline_fwd": roofline_fwd, "decode": decode, "e2e": e2e,
+           "gpu_launches": args.steps * (n_kernels + 1), "clocks": clk,
+           "wall_s_timed_region": wall}
+    return res
+
+
+def stage_bytes(cfg, path, name):
+    """Bytes each forward kernel of this design must move (its inputs and outputs)."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    tok = cfg.B * cfg.T * cfg.H
+    tile = 128 if path == "tc" else cfg.C
+    N = -(-cfg.T // tile)
+    st = cfg.B * cfg.H * N * cfg.dk * cfg.dv
+    node_e = 2 if path == "tc" else 4
+    qkv = tok * (2 * cfg.dk + cfg.dv) * e
+    if name.endswith("chunk_state"):
+        return tok * (cfg.dk + cfg.dv) * e + tok * 4 + st * 4
+    if name.endswith("level_scan"):
+        return st * 4 + st * node_e
+    return qkv + tok * 4 + tok * cfg.L * 4 + st * node_e + tok * cfg.dv * e
+
+
+def measure_e2e(LL, cfg, x, dev, ws, args):
+    """Forward through the public API with inputs in pinned host memory: each timed
+    iteration copies the inputs to the device, runs loglinear_fwd and copies the output
+    back (all on the current stream)."""
+    host = {k: (None if v is None else v.pin_memory()) for k, v in x.items()}
+    dbuf = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in x.items()}
+    out_h = torch.empty(cfg.B, cfg.T, cfg.H, cfg.dv, dtype=x["q"].dtype).pin_memory()
+    out_d = torch.empty(cfg.B, cfg.T, cfg.H, cfg.dv, dtype=x["q"].dtype, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def it():
+        for k, v in host.items():
+            if v is not None:
+                dbuf[k].copy_(v, non_blocking=True)
+        LL.loglinear_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["log_a"], dbuf["lam"], cfg.C,
+                         out=out_d, workspace=ws)
+        out_h.copy_(out_d, non_blocking=True)
+
+    for _ in range(max(2, args.warmup)):
+        it()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        it()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / n
+    return {"value": cfg.B * cfg.T / t, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": t * 1e3}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = W.FWD_CONFIGS[W.HEADLINE_FWD]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = []
+        per = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+        for i in range(args.warmup + args.steps):
+            tok_s, desc, thr = oracle_sample(cfg, per, seed=i)
+            if i >= args.warmup:
+                steps.append(tok_s)
+        v = statistics.median(steps)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": cfg.B * cfg.T / v * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": f"{cfg.name}: direct O(T^2) oracle, B{cfg.B} H{cfg.H} "
+                                       f"T{cfg.T} dk=dv={cfg.dk} L{cfg.L}"},
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok_s, desc, thr = oracle_sample(cfg, args.cpu_seconds)
+        res["cpu_baseline"] = {"value": tok_s, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                               "sample": desc}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

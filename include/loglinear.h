@@ -1,0 +1,174 @@
+/*
+ * loglinear.h — C ABI of the log-linear attention library (sm_103a).
+ *
+ * The operation (page "论文阅读：Log-Linear Attention — 基于 Fenwick 树与层次矩阵的对数线性
+ * 复杂度注意力机制", sections 并行形式 and 与已有模型的组合; page "算力终结者来了！…", section
+ * 结构矩阵):
+ *
+ *     O = (Q K^T ⊙ M^S ⊙ M^H) V,
+ *     M^S[t,s] = prod_{r=s+1..t} a_r        (Mamba-2 scalar decay; all ones without it)
+ *     M^H[t,s] = lambda[t, l(t,s)]           (Fenwick level l(t,s) of source s from query t)
+ *
+ * and its recurrent decode step with the lssb rule (first page, section 解码：基于 lssb 的
+ * 状态更新).  l(t,t) = 0; for s < t, l(t,s) is the level of the Fenwick bucket of t holding s
+ * (first page, section 层级判定算法), equal to the bit length of (t XOR s).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor arguments are DEVICE pointers to dense row-major arrays (no strides),
+ *     owned by the caller.  The library never allocates, frees or synchronises; all work
+ *     is enqueued on `stream` (NULL = the legacy default stream) and is asynchronous.
+ *   - Sizes are element counts.  Positions t are 0-based and must fit in int32.
+ *   - Every call validates its arguments on the host before launching anything and
+ *     returns an ll_status code; on a non-zero status nothing has been enqueued, except
+ *     LL_ERR_CUDA, which reports a failed launch (the message is in
+ *     loglinear_last_cuda_error()).
+ *   - `out` must not alias any input.  Calls are thread-safe.
+ */
+#ifndef LOGLINEAR_H
+#define LOGLINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LL_API __attribute__((visibility("default")))
+#else
+#define LL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* ll_stream_t;
+
+typedef enum {
+  LL_OK = 0,
+  LL_ERR_INVALID = 1,      /* a required pointer is NULL, a size is negative, unknown enum */
+  LL_ERR_SHAPE = 2,        /* sizes violate the method: chunk not a power of two, too few levels */
+  LL_ERR_DTYPE = 3,        /* unknown dtype code */
+  LL_ERR_UNSUPPORTED = 4,  /* valid problem outside this build's kernels (e.g. head dim > 128) */
+  LL_ERR_CUDA = 5,         /* a CUDA call or kernel launch failed */
+  LL_ERR_WORKSPACE = 6,    /* workspace NULL or smaller than loglinear_fwd_workspace_size() */
+  LL_ERR_ALIGN = 7         /* a pointer is not aligned as the chosen kernel path requires */
+} ll_status;
+
+typedef enum { LL_F32 = 0, LL_BF16 = 1 } ll_dtype;
+
+/* Kernel path of the forward.  AUTO takes the tensor-core path when it applies (bf16
+ * inputs, dk = dv = 128) and the fp32 CUDA-core path otherwise. */
+typedef enum { LL_PATH_AUTO = 0, LL_PATH_SIMT = 1, LL_PATH_TC = 2 } ll_path;
+
+/* Library version, (major << 16) | minor. */
+LL_API int loglinear_version(void);
+
+/* Human-readable name of a status code (static string). */
+LL_API const char* loglinear_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread (static per-thread buffer). */
+LL_API const char* loglinear_last_cuda_error(void);
+
+/* Path the forward would take for these arguments (LL_PATH_SIMT or LL_PATH_TC), or a
+ * negative ll_status if the request is invalid. */
+LL_API int loglinear_fwd_resolve_path(int64_t dk, int64_t dv, int chunk, int in_dtype, int path);
+
+/*
+ * Workspace bytes loglinear_fwd needs (written to *bytes).  The workspace holds the
+ * per-chunk states U_i (chunk-local decayed sums of k v^T), the Fenwick block states the
+ * inter-chunk readout uses, and the per-chunk log decays.  It is scratch: its content on
+ * entry does not matter and is not meaningful on exit.
+ */
+LL_API int loglinear_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                 int chunk, int in_dtype, int path, size_t* bytes);
+
+/*
+ * Chunked-parallel forward (first page, sections 矩阵分解 and 两阶段计算; second page,
+ * section 高效训练算法): intra-chunk masked attention for the levels inside a chunk, per-
+ * chunk states, a level scan over Fenwick block pairs of chunks, and a lambda-weighted
+ * readout of the block states fused into the output epilogue.
+ *
+ *   q, k    [B, T, H, dk]   in_dtype (LL_F32 or LL_BF16)
+ *   v       [B, T, H, dv]   in_dtype
+ *   log_a   [B, T, H]       fp32, log of the decay a_t (<= 0 expected); NULL = no decay
+ *   lambda  [B, T, H, L]    fp32 level weights lambda[t, l]; L >= bit_length(T-1) + 1;
+ *                           levels above bit_length(T-1) are not read
+ *   out     [B, T, H, dv]   out_dtype (LL_F32 or LL_BF16), fully overwritten
+ *   chunk   C, a power of two.  The result does not depend on C: the decomposition into
+ *           an intra-chunk block D plus inter-chunk levels is exact for any C.  The fp32
+ *           path works on chunks of min(C, 64) tokens; the tensor-core path on 128-token
+ *           tiles (levels <= 7 in the dense intra-tile product, the rest through block
+ *           states).
+ *   T need not be a multiple of C (the last chunk is partial).  B, T or H = 0 is a no-op.
+ *   workspace: device scratch of at least loglinear_fwd_workspace_size() bytes, 256-byte
+ *           aligned.  Two calls that run concurrently need two workspaces.
+ * Errors: LL_ERR_INVALID, LL_ERR_SHAPE, LL_ERR_DTYPE, LL_ERR_UNSUPPORTED (dk or dv > 128;
+ * LL_PATH_TC forced on a shape other than bf16 with dk = dv = 128), LL_ERR_WORKSPACE, LL_ERR_ALIGN (tensor-core
+ * path: q, k, v, out not 16-byte aligned), LL_ERR_CUDA.
+ */
+LL_API int loglinear_fwd(const void* q, const void* k, const void* v, const float* log_a,
+                  const float* lambda, void* out, int64_t B, int64_t T, int64_t H,
+                  int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype,
+                  int path, void* workspace, size_t workspace_bytes, ll_stream_t stream);
+
+/*
+ * loglinear_fwd with per-kernel timing: identical work and results, plus cudaEventRecord
+ * of stage_events[0] before the first kernel and of stage_events[i+1] after kernel i, on
+ * `stream`.  stage_events is a host array of n_events cudaEvent_t handles created by the
+ * caller; events past the number of kernels launched are recorded after the last one.
+ * *n_kernels (if not NULL) receives the number of kernels launched.
+ */
+LL_API int loglinear_fwd_with_events(const void* q, const void* k, const void* v,
+                                     const float* log_a, const float* lambda, void* out,
+                                     int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                     int64_t L, int chunk, int in_dtype, int out_dtype, int path,
+                                     void* workspace, size_t workspace_bytes, ll_stream_t stream,
+                                     void* const* stage_events, int n_events, int* n_kernels);
+
+/*
+ * One decode step at position t for every (b, h) (first page, section 解码：基于 lssb 的
+ * 状态更新; slide deck "論文紹介：Log Linear Attention", slide 21).  With l = lssb(t) (index of
+ * the lowest set bit of t > 0):
+ *   S^(l+1) <- a_t * sum_{j<=l} S^(j);  S^(1..l) <- 0;  S^(j) <- a_t * S^(j) for j > l+1;
+ *   S^(0) <- k_t v_t^T;  out = sum_j lambda[j] * S^(j)^T q_t   (non-empty levels only).
+ * At t = 0 the state is (re)initialised: S^(0) <- k_0 v_0^T, every other level <- 0.
+ * For t > 0 the state must hold the Fenwick states after position t-1: the levels that
+ * are empty after t-1 (bit j-1 of t-1 clear, j >= 1) are neither read nor written.
+ *
+ *   state   [B, H, L, dk, dv] fp32, updated in place, 16-byte aligned
+ *   q, k    [B, H, dk]   in_dtype;   v [B, H, dv] in_dtype
+ *   log_a   [B, H] fp32 or NULL (no decay);   lambda [B, H, L] fp32
+ *   out     [B, H, dv]   out_dtype, overwritten
+ *   t       >= 0, same for every (b, h); L >= bit_length(t) + 1
+ * Supported: 1 <= dk <= 128; dv a power of two in [4, 128].
+ * Errors: LL_ERR_INVALID, LL_ERR_SHAPE, LL_ERR_DTYPE, LL_ERR_UNSUPPORTED, LL_ERR_ALIGN,
+ * LL_ERR_CUDA.
+ */
+LL_API int loglinear_decode_step(float* state, const void* q, const void* k, const void* v,
+                          const float* log_a, const float* lambda, int64_t t, void* out,
+                          int64_t B, int64_t H, int64_t dk, int64_t dv, int64_t L,
+                          int in_dtype, int out_dtype, ll_stream_t stream);
+
+/*
+ * Reads and clears the device error word of the tensor-core path (synchronises `stream`).
+ * *flags = 0 when every mbarrier wait of the kernels run so far completed; bit 0 set when
+ * a wait ran out of time (the CTA then skipped its remaining work, its output tile is not
+ * valid, and the launch itself still reported success).
+ */
+LL_API int loglinear_device_error(ll_stream_t stream, unsigned* flags);
+
+/*
+ * Debug view of the forward's level indexing (first page, sections 层级判定算法 and 矩阵
+ * 分解): writes levels[t * T + s] (int8, device) for 0 <= s, t < T: the Fenwick level the
+ * given path assigns to the pair (query t, source s) through its intra-chunk formula or
+ * its inter-chunk block pairing, and -1 for s > t.  chunk and path as in loglinear_fwd
+ * (path AUTO resolves as for bf16, dk = dv = 128).  T <= 16384.
+ */
+LL_API int loglinear_debug_level_map(int64_t T, int chunk, int path, int8_t* levels,
+                              ll_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOGLINEAR_H */

@@ -1,0 +1,208 @@
+"""ctypes binding of libloglinear.so: argument marshalling only.
+
+Every step of the forward and of the decode step runs in the library's CUDA kernels;
+this module checks tensor placement / dtype / contiguity, allocates outputs and the
+forward's workspace with PyTorch (device memory is PyTorch's job here), passes raw
+pointers and sizes to the C ABI on the current CUDA stream, and turns a non-zero status
+into an exception.  If the library is missing the import fails loudly: there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libloglinear.so")
+
+LL_OK, LL_ERR_INVALID, LL_ERR_SHAPE, LL_ERR_DTYPE, LL_ERR_UNSUPPORTED, LL_ERR_CUDA, \
+    LL_ERR_WORKSPACE, LL_ERR_ALIGN = range(8)
+LL_F32, LL_BF16 = 0, 1
+LL_PATH_AUTO, LL_PATH_SIMT, LL_PATH_TC = 0, 1, 2
+PATHS = {"auto": LL_PATH_AUTO, "simt": LL_PATH_SIMT, "tc": LL_PATH_TC}
+
+# Every symbol include/loglinear.h declares, with its ctypes signature.
+_i64, _int, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+SIGNATURES = {
+    "loglinear_version": (_int, []),
+    "loglinear_status_string": (ctypes.c_char_p, [_int]),
+    "loglinear_last_cuda_error": (ctypes.c_char_p, []),
+    "loglinear_fwd_resolve_path": (_int, [_i64, _i64, _int, _int, _int]),
+    "loglinear_fwd_workspace_size": (_int, [_i64, _i64, _i64, _i64, _i64, _int, _int, _int,
+                                            ctypes.POINTER(_sz)]),
+    "loglinear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
+                             _int, _int, _int, _int, _vp, _sz, _vp]),
+    "loglinear_fwd_with_events": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                         _i64, _i64, _int, _int, _int, _int, _vp, _sz, _vp,
+                                         ctypes.POINTER(_vp), _int, ctypes.POINTER(_int)]),
+    "loglinear_decode_step": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _i64,
+                                     _i64, _i64, _int, _int, _vp]),
+    "loglinear_debug_level_map": (_int, [_i64, _int, _int, _vp, _vp]),
+    "loglinear_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),
+}
+
+
+class LoglinearError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = f"{where}: {status_string(status)}"
+        if status == LL_ERR_CUDA:
+            msg += f" ({_lib.loglinear_last_cuda_error().decode()})"
+        super().__init__(msg)
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = load_library()
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.loglinear_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LL_F32
+    if t.dtype == torch.bfloat16:
+        return LL_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_dev(name, t, dtype=None, shape=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def resolve_path(dk, dv, chunk, in_dtype, path="auto") -> str:
+    r = _lib.loglinear_fwd_resolve_path(dk, dv, chunk, in_dtype, PATHS[path])
+    if r < 0:
+        raise LoglinearError(-r, "loglinear_fwd_resolve_path")
+    return {LL_PATH_SIMT: "simt", LL_PATH_TC: "tc"}[r]
+
+
+def fwd_workspace_size(B, T, H, dk, dv, chunk, in_dtype, path="auto") -> int:
+    out = ctypes.c_size_t(0)
+    st = _lib.loglinear_fwd_workspace_size(B, T, H, dk, dv, chunk, in_dtype, PATHS[path],
+                                           ctypes.byref(out))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_fwd_workspace_size")
+    return int(out.value)
+
+
+def loglinear_fwd(q, k, v, log_a, lam, chunk, out=None, out_dtype=None, workspace=None,
+                  path="auto", stream=None):
+    """O = (Q K^T ⊙ M^S ⊙ M^H) V through the C ABI (q, k [B,T,H,dk]; v [B,T,H,dv];
+    log_a [B,T,H] fp32 or None; lam [B,T,H,L] fp32).  Returns out [B,T,H,dv]."""
+    B, T, H, dk = q.shape
+    dv, L = v.shape[-1], lam.shape[-1]
+    _check_dev("q", q, shape=(B, T, H, dk))
+    _check_dev("k", k, q.dtype, (B, T, H, dk))
+    _check_dev("v", v, q.dtype, (B, T, H, dv))
+    _check_dev("log_a", log_a, torch.float32, (B, T, H))
+    _check_dev("lam", lam, torch.float32, (B, T, H, L))
+    in_dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty(B, T, H, dv, device=q.device, dtype=out_dtype or q.dtype)
+    _check_dev("out", out, shape=(B, T, H, dv))
+    ws_bytes = fwd_workspace_size(B, T, H, dk, dv, chunk, in_dt, path)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), device=q.device, dtype=torch.uint8)
+    _check_dev("workspace", workspace, torch.uint8)
+    st = _lib.loglinear_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
+                            B, T, H, dk, dv, L, chunk, in_dt, _dtype_code(out), PATHS[path],
+                            _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_fwd")
+    return out
+
+
+def loglinear_fwd_with_events(q, k, v, log_a, lam, chunk, events, out, workspace, path="auto",
+                              stream=None):
+    """loglinear_fwd plus torch.cuda.Event records between its kernels (events are
+    created with enable_timing=True by the caller).  Returns the number of kernels."""
+    B, T, H, dk = q.shape
+    dv, L = v.shape[-1], lam.shape[-1]
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    nk = ctypes.c_int(0)
+    st = _lib.loglinear_fwd_with_events(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam),
+                                        _ptr(out), B, T, H, dk, dv, L, chunk, _dtype_code(q),
+                                        _dtype_code(out), PATHS[path], _ptr(workspace),
+                                        workspace.numel(), _stream(stream), arr, len(events),
+                                        ctypes.byref(nk))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_fwd_with_events")
+    return nk.value
+
+
+def loglinear_decode_step(state, q, k, v, log_a, lam, t, out=None, out_dtype=None, stream=None):
+    """One lssb decode step at position t; updates state [B,H,L,dk,dv] (fp32) in place
+    and returns out [B,H,dv]."""
+    B, H, L, dk, dv = state.shape
+    _check_dev("state", state, torch.float32)
+    _check_dev("q", q, shape=(B, H, dk))
+    _check_dev("k", k, q.dtype, (B, H, dk))
+    _check_dev("v", v, q.dtype, (B, H, dv))
+    _check_dev("log_a", log_a, torch.float32, (B, H))
+    _check_dev("lam", lam, torch.float32, (B, H, L))
+    if out is None:
+        out = torch.empty(B, H, dv, device=q.device, dtype=out_dtype or q.dtype)
+    _check_dev("out", out, shape=(B, H, dv))
+    st = _lib.loglinear_decode_step(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_a),
+                                    _ptr(lam), int(t), _ptr(out), B, H, dk, dv, L, _dtype_code(q),
+                                    _dtype_code(out), _stream(stream))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_decode_step")
+    return out
+
+
+def device_error(stream=None) -> int:
+    """Reads and clears the tensor-core path's device error word (0 = no bounded wait
+    ran out of time).  Synchronises the stream."""
+    flags = ctypes.c_uint(0)
+    st = _lib.loglinear_device_error(_stream(stream), ctypes.byref(flags))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_device_error")
+    return int(flags.value)
+
+
+def debug_level_map(T, chunk, path="auto", stream=None):
+    """[T, T] int8 map of the level the forward's decomposition gives each (t, s)."""
+    out = torch.empty(T, T, device="cuda", dtype=torch.int8)
+    st = _lib.loglinear_debug_level_map(T, chunk, PATHS[path], _ptr(out), _stream(stream))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_debug_level_map")
+    return out

@@ -1,0 +1,117 @@
+// Internal declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "loglinear.h"
+
+namespace ll {
+
+// ---------------------------------------------------------------- element access
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// ---------------------------------------------------------------- Fenwick indexing
+//
+// Level of source s seen from query t (s <= t): the Fenwick bucket of t that holds s is
+// the one cut at the highest bit where s and t differ, so the level is the bit length of
+// t XOR s; s == t gives 0, the sentinel bucket (page "论文阅读：Log-Linear Attention",
+// sections 前缀的层次化分解 and 层级判定算法).
+__host__ __device__ __forceinline__ int fenwick_level(uint32_t t, uint32_t s) {
+#ifdef __CUDA_ARCH__
+  return 32 - __clz(t ^ s);
+#else
+  uint32_t x = t ^ s;
+  int n = 0;
+  while (x) { ++n; x >>= 1; }
+  return n;
+#endif
+}
+
+// Inter-chunk block pairing.  Chunk j reads, at chunk level m (token level lc + m), the
+// aligned block of 2^(m-1) chunks just below c = j with its low m-1 bits cleared; that
+// block exists iff bit m-1 of j is set.  The block state is stored under index c, which
+// is unique per (m, block) since ctz(c) = m-1.
+__host__ __device__ __forceinline__ bool inter_block(int64_t j, int m, int64_t* c_out) {
+  if (!((j >> (m - 1)) & 1)) return false;
+  *c_out = (j >> (m - 1)) << (m - 1);
+  return true;
+}
+
+// ---------------------------------------------------------------- forward arguments
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* log_a;  // may be null
+  const float* lam;
+  void* out;
+  int B, T, H, dk, dv, L;
+  int C, lc;  // tile length and log2(tile)
+  int N;      // tiles per (b, h)
+  // workspace
+  float* U;       // [B*H][N][dk*dv] chunk states (layout per path)
+  void* nodes;    // [B*H][N][dk*dv] Fenwick block states, slot c = first reader chunk
+  float* lg;      // [B*H][N] log decay of each whole chunk
+};
+
+// Workspace carving (identical on host for size queries and for launches).
+struct FwdWorkspace {
+  size_t off_U, off_nodes, off_lg, total;
+};
+FwdWorkspace fwd_workspace_layout(int64_t B, int64_t H, int64_t N, int64_t dk, int64_t dv,
+                                  size_t node_elem_bytes);
+
+// Optional per-kernel event recording by the launchers (instrumentation only).
+struct StageEvents {
+  cudaEvent_t* ev = nullptr;
+  int n = 0;
+  int recorded = 0;
+  cudaError_t record(cudaStream_t s) {
+    if (recorded < n) return cudaEventRecord(ev[recorded++], s);
+    return cudaSuccess;
+  }
+  cudaError_t finish(cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    const int kernels = recorded > 0 ? recorded - 1 : 0;
+    launched = kernels;
+    while (recorded < n && e == cudaSuccess) e = cudaEventRecord(ev[recorded++], s);
+    return e;
+  }
+  int launched = 0;
+};
+
+// Launchers (return cudaError_t of the launches).
+cudaError_t launch_simt_forward(const FwdArgs& a, int in_dtype, int out_dtype, cudaStream_t s,
+                                StageEvents* ev);
+cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev);
+cudaError_t launch_level_scan(const FwdArgs& a, bool bf16_nodes, cudaStream_t s);
+// Reads and clears the tensor-core path's device error word (synchronises the stream).
+cudaError_t tc_take_error(cudaStream_t s, unsigned* flags);
+bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int chunk);
+constexpr int kTcTile = 128;
+
+struct DecodePlan {
+  int t_zero;      // 1 if t == 0 (initialise)
+  int l;           // lssb(t) for t > 0
+  int n_hi;        // number of levels > l+1 holding data after t-1
+  int lv[64];      // touched levels: 0..l, then the n_hi levels above l+1
+};
+cudaError_t launch_decode(float* state, const void* q, const void* k, const void* v,
+                          const float* log_a, const float* lam, void* out, int B, int H,
+                          int dk, int dv, int L, const DecodePlan& plan, int in_dtype,
+                          int out_dtype, cudaStream_t s);
+
+cudaError_t launch_level_map(int T, int tile, int lc, int8_t* levels, cudaStream_t s);
+
+}  // namespace ll

@@ -1,0 +1,260 @@
+// C ABI of the library: argument validation, workspace carving and kernel dispatch.
+// Nothing here allocates device memory or synchronises; every check happens on the host
+// before the first launch.
+#include <cstdio>
+#include <cstring>
+
+#include "ll_internal.cuh"
+
+namespace ll {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+FwdWorkspace fwd_workspace_layout(int64_t B, int64_t H, int64_t N, int64_t dk, int64_t dv,
+                                  size_t node_elem_bytes) {
+  FwdWorkspace w;
+  const size_t states = (size_t)(B * H * N) * (size_t)(dk * dv);
+  w.off_U = 0;
+  w.off_nodes = align_up(w.off_U + states * sizeof(float), 256);
+  w.off_lg = align_up(w.off_nodes + states * node_elem_bytes, 256);
+  w.total = align_up(w.off_lg + (size_t)(B * H * N) * sizeof(float), 256);
+  return w;
+}
+
+// Fills levels[t*T + s] with the level the forward's decomposition gives the pair: the
+// intra-tile formula when s and t share a tile, else the chunk level of the block pairing
+// that contains s's tile, offset by lc; -1 above the diagonal; 127 if no block matched.
+__global__ void level_map_kernel(int T, int tile, int lc, int8_t* levels) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)T * T) return;
+  const int t = (int)(idx / T), s = (int)(idx - (int64_t)t * T);
+  int8_t out = -1;
+  if (s <= t) {
+    const int j = t / tile, i = s / tile;
+    if (i == j) {
+      out = (int8_t)fenwick_level((uint32_t)t, (uint32_t)s);
+    } else {
+      out = 127;
+      for (int m = 1; (int64_t(1) << (m - 1)) <= j; ++m) {
+        int64_t c;
+        if (inter_block(j, m, &c) && i >= c - (int64_t(1) << (m - 1)) && i < c)
+          out = (int8_t)(lc + m);
+      }
+    }
+  }
+  levels[idx] = out;
+}
+
+cudaError_t launch_level_map(int T, int tile, int lc, int8_t* levels, cudaStream_t s) {
+  const int64_t n = (int64_t)T * T;
+  if (n == 0) return cudaSuccess;
+  level_map_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(T, tile, lc, levels);
+  return cudaGetLastError();
+}
+
+}  // namespace ll
+
+using namespace ll;
+
+namespace {
+
+thread_local char g_cuda_err[256] = "no error";
+
+int cuda_fail(cudaError_t e) {
+  snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return LL_ERR_CUDA;
+}
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+int log2_exact(int64_t x) {
+  int n = 0;
+  while ((int64_t(1) << n) < x) ++n;
+  return n;
+}
+int bit_length(int64_t x) {
+  int n = 0;
+  while (x > 0) { ++n; x >>= 1; }
+  return n;
+}
+bool dtype_ok(int d) { return d == LL_F32 || d == LL_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kSimtMaxChunk = 64;
+constexpr int64_t kMaxHeadDim = 128;
+
+// Shared validation of the forward's sizes; fills the resolved path and tile geometry.
+int check_fwd_sizes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv, int chunk,
+                    int in_dtype, int path, int* path_out, int* tile, int64_t* N) {
+  if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1) return LL_ERR_INVALID;
+  if (!dtype_ok(in_dtype)) return LL_ERR_DTYPE;
+  if (path != LL_PATH_AUTO && path != LL_PATH_SIMT && path != LL_PATH_TC) return LL_ERR_INVALID;
+  if (!is_pow2(chunk)) return LL_ERR_SHAPE;
+  if (T > INT32_MAX || B * H > INT32_MAX / 2) return LL_ERR_UNSUPPORTED;
+  if (dk > kMaxHeadDim || dv > kMaxHeadDim) return LL_ERR_UNSUPPORTED;
+  int p = path;
+  if (p == LL_PATH_AUTO)
+    p = tc_forward_supported(dk, dv, in_dtype, chunk) ? LL_PATH_TC : LL_PATH_SIMT;
+  if (p == LL_PATH_TC && !tc_forward_supported(dk, dv, in_dtype, chunk)) return LL_ERR_UNSUPPORTED;
+  *path_out = p;
+  // The result does not depend on the chunk length: each path evaluates the same sum on
+  // its own tile (CUDA cores: min(C, 64); tensor cores: 128).
+  *tile = p == LL_PATH_TC ? kTcTile : (chunk < kSimtMaxChunk ? chunk : kSimtMaxChunk);
+  *N = (T + *tile - 1) / *tile;
+  return LL_OK;
+}
+
+size_t node_bytes(int path) { return path == LL_PATH_TC ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+int loglinear_version(void) { return (0 << 16) | 1; }
+
+const char* loglinear_status_string(int status) {
+  switch (status) {
+    case LL_OK: return "LL_OK";
+    case LL_ERR_INVALID: return "LL_ERR_INVALID: null pointer, negative size or unknown enum";
+    case LL_ERR_SHAPE: return "LL_ERR_SHAPE: sizes violate the method (chunk, levels)";
+    case LL_ERR_DTYPE: return "LL_ERR_DTYPE: unknown dtype code";
+    case LL_ERR_UNSUPPORTED: return "LL_ERR_UNSUPPORTED: no kernel for this shape or path";
+    case LL_ERR_CUDA: return "LL_ERR_CUDA: CUDA call or launch failed";
+    case LL_ERR_WORKSPACE: return "LL_ERR_WORKSPACE: workspace missing or too small";
+    case LL_ERR_ALIGN: return "LL_ERR_ALIGN: pointer alignment";
+    default: return "unknown status";
+  }
+}
+
+const char* loglinear_last_cuda_error(void) { return g_cuda_err; }
+
+int loglinear_fwd_resolve_path(int64_t dk, int64_t dv, int chunk, int in_dtype, int path) {
+  int p, tile;
+  int64_t N;
+  const int st = check_fwd_sizes(1, 1, 1, dk, dv, chunk, in_dtype, path, &p, &tile, &N);
+  return st == LL_OK ? p : -st;
+}
+
+int loglinear_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                 int chunk, int in_dtype, int path, size_t* bytes) {
+  if (!bytes) return LL_ERR_INVALID;
+  int p, tile;
+  int64_t N;
+  const int st = check_fwd_sizes(B, T, H, dk, dv, chunk, in_dtype, path, &p, &tile, &N);
+  if (st != LL_OK) return st;
+  *bytes = fwd_workspace_layout(B, H, N, dk, dv, node_bytes(p)).total;
+  return LL_OK;
+}
+
+static int fwd_impl(const void* q, const void* k, const void* v, const float* log_a,
+                    const float* lambda, void* out, int64_t B, int64_t T, int64_t H, int64_t dk,
+                    int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype, int path,
+                    void* workspace, size_t workspace_bytes, ll_stream_t stream,
+                    StageEvents* ev) {
+  int p, tile;
+  int64_t N;
+  int st = check_fwd_sizes(B, T, H, dk, dv, chunk, in_dtype, path, &p, &tile, &N);
+  if (st != LL_OK) return st;
+  if (!dtype_ok(out_dtype)) return LL_ERR_DTYPE;
+  if (L < 1) return LL_ERR_INVALID;
+  if (B == 0 || T == 0 || H == 0) return LL_OK;
+  if (!q || !k || !v || !lambda || !out) return LL_ERR_INVALID;
+  if (L < bit_length(T - 1) + 1) return LL_ERR_SHAPE;
+  if (L > 64) return LL_ERR_UNSUPPORTED;
+  const FwdWorkspace w = fwd_workspace_layout(B, H, N, dk, dv, node_bytes(p));
+  if (!workspace || workspace_bytes < w.total) return LL_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_ALIGN;
+  if (p == LL_PATH_TC && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out)))
+    return LL_ERR_ALIGN;
+  FwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_a = log_a; a.lam = lambda; a.out = out;
+  a.B = (int)B; a.T = (int)T; a.H = (int)H; a.dk = (int)dk; a.dv = (int)dv; a.L = (int)L;
+  a.C = tile; a.lc = log2_exact(tile); a.N = (int)N;
+  char* ws = static_cast<char*>(workspace);
+  a.U = reinterpret_cast<float*>(ws + w.off_U);
+  a.nodes = ws + w.off_nodes;
+  a.lg = reinterpret_cast<float*>(ws + w.off_lg);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = p == LL_PATH_TC ? launch_tc_forward(a, out_dtype, s, ev)
+                                        : launch_simt_forward(a, in_dtype, out_dtype, s, ev);
+  return e == cudaSuccess ? LL_OK : cuda_fail(e);
+}
+
+int loglinear_fwd(const void* q, const void* k, const void* v, const float* log_a,
+                  const float* lambda, void* out, int64_t B, int64_t T, int64_t H, int64_t dk,
+                  int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype, int path,
+                  void* workspace, size_t workspace_bytes, ll_stream_t stream) {
+  return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, dk, dv, L, chunk, in_dtype, out_dtype,
+                  path, workspace, workspace_bytes, stream, nullptr);
+}
+
+int loglinear_fwd_with_events(const void* q, const void* k, const void* v, const float* log_a,
+                              const float* lambda, void* out, int64_t B, int64_t T, int64_t H,
+                              int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
+                              int out_dtype, int path, void* workspace, size_t workspace_bytes,
+                              ll_stream_t stream, void* const* stage_events, int n_events,
+                              int* n_kernels) {
+  if (n_events < 0 || (n_events > 0 && !stage_events)) return LL_ERR_INVALID;
+  StageEvents ev;
+  ev.ev = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events));
+  ev.n = n_events;
+  if (n_kernels) *n_kernels = 0;
+  const int st = fwd_impl(q, k, v, log_a, lambda, out, B, T, H, dk, dv, L, chunk, in_dtype,
+                          out_dtype, path, workspace, workspace_bytes, stream, &ev);
+  if (n_kernels) *n_kernels = ev.launched;
+  return st;
+}
+
+int loglinear_decode_step(float* state, const void* q, const void* k, const void* v,
+                          const float* log_a, const float* lambda, int64_t t, void* out,
+                          int64_t B, int64_t H, int64_t dk, int64_t dv, int64_t L,
+                          int in_dtype, int out_dtype, ll_stream_t stream) {
+  if (B < 0 || H < 0 || dk < 1 || dv < 1 || t < 0 || L < 1) return LL_ERR_INVALID;
+  if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return LL_ERR_DTYPE;
+  if (t > INT32_MAX) return LL_ERR_UNSUPPORTED;
+  if (L < bit_length(t) + 1) return LL_ERR_SHAPE;
+  if (dk > kMaxHeadDim || !is_pow2(dv) || dv < 4 || dv > kMaxHeadDim || L > 64)
+    return LL_ERR_UNSUPPORTED;
+  if (B * H > INT32_MAX) return LL_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0) return LL_OK;
+  if (!state || !q || !k || !v || !lambda || !out) return LL_ERR_INVALID;
+  if (!aligned16(state)) return LL_ERR_ALIGN;
+  DecodePlan plan;
+  memset(&plan, 0, sizeof(plan));
+  if (t == 0) {
+    plan.t_zero = 1;
+  } else {
+    int l = 0;
+    while (!((t >> l) & 1)) ++l;
+    plan.l = l;
+    int n = 0;
+    for (int i = 0; i <= l; ++i) plan.lv[n++] = i;
+    for (int lv = l + 2; lv < L; ++lv)
+      if (((t - 1) >> (lv - 1)) & 1) plan.lv[n++] = lv;
+    plan.n_hi = n - (l + 1);
+  }
+  const cudaError_t e = launch_decode(state, q, k, v, log_a, lambda, out, (int)B, (int)H, (int)dk,
+                                      (int)dv, (int)L, plan, in_dtype, out_dtype,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LL_OK : cuda_fail(e);
+}
+
+int loglinear_device_error(ll_stream_t stream, unsigned* flags) {
+  if (!flags) return LL_ERR_INVALID;
+  const cudaError_t e = tc_take_error(reinterpret_cast<cudaStream_t>(stream), flags);
+  return e == cudaSuccess ? LL_OK : cuda_fail(e);
+}
+
+int loglinear_debug_level_map(int64_t T, int chunk, int path, int8_t* levels,
+                              ll_stream_t stream) {
+  if (T < 0 || T > 16384) return LL_ERR_INVALID;
+  if (T > 0 && !levels) return LL_ERR_INVALID;
+  int p, tile;
+  int64_t N;
+  const int st = check_fwd_sizes(1, T, 1, 128, 128, chunk, LL_BF16, path, &p, &tile, &N);
+  if (st != LL_OK) return st;
+  const cudaError_t e = launch_level_map((int)T, tile, log2_exact(tile), levels,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LL_OK : cuda_fail(e);
+}
+
+}  // extern "C"

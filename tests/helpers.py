@@ -1,0 +1,31 @@
+"""Shared helpers of the parity tests (comparison metrics and tolerances)."""
+import numpy as np
+import torch
+
+# Tolerances: rel-L2 <= 1e-5 for fp32 inputs; <= 2e-2 for bf16 inputs with fp32
+# accumulation (max-abs reported next to it); level indexing exact.
+TOL_F32 = 1e-5
+TOL_BF16 = 2e-2
+
+
+def to64(x):
+    if isinstance(x, torch.Tensor):
+        return x.detach().float().cpu().double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def rel_l2(got, want):
+    got, want = to64(got), to64(want)
+    return float(np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-300))
+
+
+def max_abs(got, want):
+    return float(np.max(np.abs(to64(got) - to64(want)))) if to64(want).size else 0.0
+
+
+def cuda(d):
+    return {k: (None if v is None else v.cuda()) for k, v in d.items()}
+
+
+def tol_for(dtype):
+    return TOL_F32 if dtype in ("f32", torch.float32) else TOL_BF16

@@ -1,0 +1,143 @@
+"""C ABI checks that need no GPU: the library loads, exports every function the header
+declares, and rejects bad arguments with the documented status before any launch.
+
+Every call below is built to fail host-side validation (or to be a documented no-op),
+so none of them reaches a kernel launch even on a machine with a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "loglinear.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from log_linear_attention_fwd_gb300 import _binding
+    return _binding
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(loglinear_\w+)\s*\(", text)))
+
+
+def test_header_symbols_exported(L):
+    names = header_functions()
+    assert len(names) >= 7
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in L.SIGNATURES, f"{n} has no ctypes signature"
+
+
+def test_version_and_status_strings(L):
+    lib = L.lib()
+    assert lib.loglinear_version() >= 1
+    for st in range(8):
+        s = lib.loglinear_status_string(st).decode()
+        assert s.startswith("LL_")
+    assert lib.loglinear_status_string(99).decode() == "unknown status"
+
+
+FAKE = ctypes.c_void_p(0x1000)   # never dereferenced: every call here fails validation first
+
+
+def fwd(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, out=FAKE, B=1, T=64, H=2, dk=16, dv=16,
+             Lv=7, chunk=16, ind=L.LL_F32, outd=L.LL_F32, path=L.LL_PATH_SIMT, ws=None, wsb=0,
+             stream=None)
+    a.update(kw)
+    return L.lib().loglinear_fwd(a["q"], a["k"], a["v"], a["log_a"], a["lam"], a["out"], a["B"],
+                                 a["T"], a["H"], a["dk"], a["dv"], a["Lv"], a["chunk"], a["ind"],
+                                 a["outd"], a["path"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_fwd_validation_codes(L):
+    assert fwd(L, chunk=3) == L.LL_ERR_SHAPE
+    assert fwd(L, chunk=0) == L.LL_ERR_SHAPE
+    assert fwd(L, Lv=6) == L.LL_ERR_SHAPE             # T=64 needs L >= 7
+    assert fwd(L, T=65, Lv=7) == L.LL_ERR_SHAPE       # T=65 needs L >= 8
+    assert fwd(L, ind=7) == L.LL_ERR_DTYPE
+    assert fwd(L, outd=-1) == L.LL_ERR_DTYPE
+    assert fwd(L, dk=129) == L.LL_ERR_UNSUPPORTED
+    assert fwd(L, dv=0) == L.LL_ERR_INVALID
+    assert fwd(L, B=-1) == L.LL_ERR_INVALID
+    assert fwd(L, path=9) == L.LL_ERR_INVALID
+    assert fwd(L, q=None) == L.LL_ERR_INVALID
+    assert fwd(L, lam=None) == L.LL_ERR_INVALID
+    assert fwd(L, ws=None, wsb=0) == L.LL_ERR_WORKSPACE
+    assert fwd(L, ws=FAKE, wsb=16) == L.LL_ERR_WORKSPACE
+    # tensor-core path: misaligned q (after every size check passed) -> LL_ERR_ALIGN
+    assert fwd(L, dk=128, dv=128, ind=L.LL_BF16, outd=L.LL_BF16, path=L.LL_PATH_TC,
+               q=ctypes.c_void_p(0x1002), ws=FAKE, wsb=1 << 40) == L.LL_ERR_ALIGN
+    assert fwd(L, dk=64, dv=64, ind=L.LL_BF16, path=L.LL_PATH_TC) == L.LL_ERR_UNSUPPORTED
+    assert fwd(L, dk=128, dv=128, ind=L.LL_F32, path=L.LL_PATH_TC) == L.LL_ERR_UNSUPPORTED
+    # empty problems are no-ops, even with null pointers
+    for kw in (dict(B=0), dict(T=0), dict(H=0)):
+        assert fwd(L, q=None, k=None, v=None, lam=None, out=None, **kw) == L.LL_OK
+
+
+def test_workspace_size_and_paths(L):
+    sz = L.fwd_workspace_size(1, 64, 2, 16, 16, 16, L.LL_F32, "simt")
+    n_states = 1 * 2 * 4 * 16 * 16
+    assert sz >= 2 * n_states * 4
+    with pytest.raises(L.LoglinearError):
+        L.fwd_workspace_size(1, 64, 2, 16, 16, 24, L.LL_F32, "simt")
+    assert L.resolve_path(64, 64, 64, L.LL_F32) == "simt"
+    assert L.resolve_path(128, 128, 64, L.LL_F32) == "simt"
+    assert L.resolve_path(128, 128, 64, L.LL_BF16) == "tc"
+    assert L.resolve_path(128, 128, 128, L.LL_BF16) == "tc"
+    assert L.resolve_path(128, 128, 256, L.LL_BF16) == "tc"
+    assert L.resolve_path(64, 64, 256, L.LL_F32) == "simt"
+    # the fp32 path tiles at min(C, 64): C = 256 needs the workspace of C = 64
+    assert L.fwd_workspace_size(1, 1000, 2, 16, 16, 256, L.LL_F32) == \
+        L.fwd_workspace_size(1, 1000, 2, 16, 16, 64, L.LL_F32)
+    assert L.resolve_path(64, 64, 64, L.LL_BF16) == "simt"
+    with pytest.raises(L.LoglinearError):
+        L.resolve_path(64, 64, 64, L.LL_BF16, "tc")
+    # tensor-core workspace: fp32 chunk states + bf16 block states, 128-token tiles
+    tc = L.fwd_workspace_size(1, 16384, 16, 128, 128, 64, L.LL_BF16, "tc")
+    assert tc >= 16 * 128 * 128 * 128 * (4 + 2)
+
+
+def dec(L, **kw):
+    a = dict(state=FAKE, q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, t=5, out=FAKE, B=2, H=2,
+             dk=16, dv=16, Lv=4, ind=L.LL_F32, outd=L.LL_F32, stream=None)
+    a.update(kw)
+    return L.lib().loglinear_decode_step(a["state"], a["q"], a["k"], a["v"], a["log_a"], a["lam"],
+                                         a["t"], a["out"], a["B"], a["H"], a["dk"], a["dv"],
+                                         a["Lv"], a["ind"], a["outd"], a["stream"])
+
+
+def test_decode_validation_codes(L):
+    assert dec(L, t=-1) == L.LL_ERR_INVALID
+    assert dec(L, t=8, Lv=4) == L.LL_ERR_SHAPE       # t=8 reaches level 4 -> L >= 5
+    assert dec(L, dv=12) == L.LL_ERR_UNSUPPORTED     # dv must be a power of two
+    assert dec(L, dv=2) == L.LL_ERR_UNSUPPORTED
+    assert dec(L, dk=200) == L.LL_ERR_UNSUPPORTED
+    assert dec(L, ind=5) == L.LL_ERR_DTYPE
+    assert dec(L, state=None) == L.LL_ERR_INVALID
+    assert dec(L, out=None) == L.LL_ERR_INVALID
+    assert dec(L, state=ctypes.c_void_p(0x1004)) == L.LL_ERR_ALIGN
+    assert dec(L, B=0, state=None) == L.LL_OK
+
+
+def test_level_map_validation(L):
+    lib = L.lib()
+    assert lib.loglinear_debug_level_map(-1, 16, 0, FAKE, None) == L.LL_ERR_INVALID
+    assert lib.loglinear_debug_level_map(16, 16, 0, None, None) == L.LL_ERR_INVALID
+    assert lib.loglinear_debug_level_map(16, 12, 0, FAKE, None) == L.LL_ERR_SHAPE
+    assert lib.loglinear_debug_level_map(0, 16, 0, None, None) == L.LL_OK
+    assert lib.loglinear_device_error(None, None) == L.LL_ERR_INVALID
+
+
+def test_binding_rejects_host_tensors(L):
+    import torch
+    q = torch.zeros(1, 8, 1, 4)
+    with pytest.raises(ValueError):
+        L.loglinear_fwd(q, q, q, None, torch.zeros(1, 8, 1, 4), 4)

@@ -1,0 +1,188 @@
+"""Parity of the CUDA forward with the CPU oracle, through the C ABI (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.helpers import TOL_BF16, TOL_F32, cuda, max_abs, rel_l2, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def LL():
+    import log_linear_attention_fwd_gb300 as m
+    return m
+
+
+def run(LL, x, chunk, path="auto", out_dtype=None):
+    d = cuda(x)
+    out = LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], chunk, path=path,
+                           out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def oracle_fwd(x, rows=None, heads=None):
+    return oracle.forward_direct(x["q"], x["k"], x["v"], x["log_a"], x["lam"], rows=rows, heads=heads)
+
+
+# ------------------------------------------------------------------ the workloads
+
+
+@pytest.mark.parametrize("name", ["linear_T64", "mamba2_T1024"])
+def test_fp32_workloads_full(LL, name):
+    cfg = W.FWD_CONFIGS[name]
+    x = W.make_fwd_inputs(cfg)
+    got = run(LL, x, cfg.C)
+    want = oracle_fwd(x)
+    err = rel_l2(got, want)
+    print(f"{name}: rel_l2={err:.3e} max_abs={max_abs(got, want):.3e}")
+    assert err <= TOL_F32
+
+
+def _sample_rows(T, n, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 63, 64, 127, 128, 129, T // 2, T // 2 - 1, T - 129, T - 128, T - 2, T - 1]
+    pw = [(1 << p) for p in range(1, T.bit_length()) if (1 << p) < T]
+    rows = set(fixed + pw + [p - 1 for p in pw] + list(rng.integers(0, T, n)))
+    return np.array(sorted(r for r in rows if 0 <= r < T))
+
+
+@pytest.mark.parametrize("name", ["mamba2_T4096", "mamba2_T16384"])
+def test_bf16_workloads_sampled(LL, name):
+    cfg = W.FWD_CONFIGS[name]
+    x = W.make_fwd_inputs(cfg)
+    got = run(LL, x, cfg.C)
+    assert torch.isfinite(got.float()).all()
+    # one whole head, plus sampled rows of every head
+    full = [(cfg.B - 1, cfg.H - 1)]
+    want = oracle_fwd(x, heads=full)
+    b, h = full[0]
+    err_full = rel_l2(got[b, :, h], want[b, :, h])
+    rows = _sample_rows(cfg.T, 96, 1)
+    heads = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
+    want_s = oracle_fwd(x, rows=rows, heads=heads)
+    err_s = rel_l2(got[:, rows], want_s[:, rows])
+    print(f"{name}: rel_l2(full head)={err_full:.3e} rel_l2(sampled rows)={err_s:.3e} "
+          f"max_abs={max_abs(got[:, rows], want_s[:, rows]):.3e}")
+    assert err_full <= TOL_BF16 and err_s <= TOL_BF16
+
+
+# ------------------------------------------------------------------ edge cases
+
+
+@pytest.mark.parametrize("T,C,decay", [(1, 16, True), (2, 16, False), (15, 16, True), (17, 16, True),
+                                       (53, 16, True), (200, 8, True), (333, 64, True),
+                                       (64, 1, True), (40, 2, False), (1000, 32, True),
+                                       (4096, 16, True), (130, 64, False), (700, 256, True)])
+def test_ragged_and_chunk_sizes_simt(LL, T, C, decay):
+    L = max((T - 1).bit_length() + 1, 1)
+    cfg = W.FwdConfig("e", 2, 3, T, 16, 8, C, L, "f32", decay, "softplus", seed=T * 7 + C)
+    x = W.make_fwd_inputs(cfg)
+    got = run(LL, x, C, path="simt")
+    want = oracle_fwd(x)
+    assert rel_l2(got, want) <= TOL_F32, (T, C)
+
+
+@pytest.mark.parametrize("dk,dv", [(1, 4), (7, 3), (32, 16), (128, 128), (96, 64)])
+def test_head_dims_simt(LL, dk, dv):
+    cfg = W.FwdConfig("e", 1, 2, 150, dk, dv, 32, 9, "f32", True, "softplus", seed=dk + dv)
+    x = W.make_fwd_inputs(cfg)
+    got = run(LL, x, 32, path="simt")
+    assert rel_l2(got, oracle_fwd(x)) <= TOL_F32
+
+
+def test_extra_levels_strong_and_zero_decay(LL):
+    cfg = W.FwdConfig("e", 1, 2, 300, 16, 16, 16, 20, "f32", True, "softplus", seed=9)
+    x = W.make_fwd_inputs(cfg)
+    for la in (torch.full_like(x["log_a"], -6.0), torch.zeros_like(x["log_a"]),
+               x["log_a"] * 30):
+        y = dict(x, log_a=la.contiguous())
+        got = run(LL, y, 16, path="simt")
+        assert torch.isfinite(got).all()
+        assert rel_l2(got, oracle_fwd(y)) <= TOL_F32
+
+
+def test_dtype_combinations_simt(LL):
+    cfg = W.FwdConfig("e", 1, 2, 257, 32, 32, 32, 10, "bf16", True, "softplus", seed=4)
+    x = W.make_fwd_inputs(cfg)
+    want = oracle_fwd(x)
+    got32 = run(LL, x, 32, path="simt", out_dtype=torch.float32)
+    assert got32.dtype == torch.float32 and rel_l2(got32, want) <= TOL_F32
+    got16 = run(LL, x, 32, path="simt")
+    assert got16.dtype == torch.bfloat16 and rel_l2(got16, want) <= TOL_BF16
+    xf = dict(x, q=x["q"].float(), k=x["k"].float(), v=x["v"].float())
+    gotf = run(LL, xf, 32, path="simt", out_dtype=torch.bfloat16)
+    assert rel_l2(gotf, want) <= TOL_BF16
+
+
+def test_empty_problems(LL):
+    q = torch.zeros(1, 0, 2, 16, device="cuda")
+    lam = torch.zeros(1, 0, 2, 1, device="cuda")
+    out = LL.loglinear_fwd(q, q, torch.zeros(1, 0, 2, 8, device="cuda"), None, lam, 16)
+    assert out.shape == (1, 0, 2, 8)
+
+
+# ------------------------------------------------------------------ exact indexing
+
+
+@pytest.mark.parametrize("T,C,path", [(64, 16, "simt"), (1000, 64, "simt"), (300, 4, "simt"),
+                                      (2048, 1, "simt")])
+def test_level_map_bit_exact(LL, T, C, path):
+    got = LL.debug_level_map(T, C, path=path).cpu().numpy().astype(np.int64)
+    want = oracle.level_matrix(T)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("path,C,T,dtype", [("simt", 16, 200, "f32"), ("simt", 8, 517, "f32"),
+                                            ("simt", 64, 1024, "bf16")])
+def test_onehot_lambda_bit_exact(LL, path, C, T, dtype):
+    """Small-integer q, k, v, no decay, lambda = e_l: every level's contribution is an
+    exact integer sum in fp32, so the CUDA result must equal the oracle exactly."""
+    L = (T - 1).bit_length() + 1
+    for lvl in range(L):
+        x = W.make_int_inputs(1, T, 2, 8, 8, L, lvl, seed=lvl, dtype=dtype)
+        got = run(LL, x, C, path=path, out_dtype=torch.float32)
+        want = oracle_fwd(x)
+        assert np.array_equal(got.double().numpy(), want), (path, lvl)
+
+
+# ------------------------------------------------------------------ tensor-core path
+
+
+@pytest.mark.parametrize("T,C,decay", [(128, 64, True), (300, 64, True), (1000, 128, True),
+                                       (2125, 64, True), (4096, 64, False), (77, 64, True)])
+def test_tc_path_matches_oracle(LL, T, C, decay):
+    L = (T - 1).bit_length() + 1
+    cfg = W.FwdConfig("tc", 2, 3, T, 128, 128, C, L, "bf16", decay, "softplus", seed=T + C)
+    x = W.make_fwd_inputs(cfg)
+    assert LL.resolve_path(128, 128, C, 1) == "tc"
+    want = oracle_fwd(x)
+    got = run(LL, x, C, path="tc")
+    got32 = run(LL, x, C, path="tc", out_dtype=torch.float32)
+    assert LL.device_error() == 0
+    e16, e32 = rel_l2(got, want), rel_l2(got32, want)
+    print(f"tc T={T} C={C}: rel_l2 bf16-out={e16:.3e} f32-out={e32:.3e} "
+          f"max_abs={max_abs(got32, want):.3e}")
+    assert e16 <= TOL_BF16 and e32 <= TOL_BF16
+
+
+def test_tc_level_map_bit_exact(LL):
+    for T in (128, 1000, 4096):
+        got = LL.debug_level_map(T, 64, path="tc").cpu().numpy().astype(np.int64)
+        assert np.array_equal(got, oracle.level_matrix(T)), T
+
+
+@pytest.mark.parametrize("T", [256, 1151])
+def test_tc_onehot_lambda_bit_exact(LL, T):
+    """Integer inputs that stay exact through bf16 states: the tensor-core result must
+    equal the oracle bit for bit at every level, intra-tile and inter-tile."""
+    L = (T - 1).bit_length() + 1
+    for lvl in range(L):
+        x = W.make_sparse_int_inputs(1, T, 2, 128, L, lvl, seed=lvl)
+        got = run(LL, x, 64, path="tc", out_dtype=torch.float32)
+        want = oracle_fwd(x)
+        assert np.array_equal(got.double().numpy(), want), lvl
+    assert LL.device_error() == 0

@@ -117,6 +117,24 @@ def make_int_inputs(B, T, H, dk, dv, L, onehot_level: int, seed: int = 0, dtype=
     return dict(q=q.to(dt), k=k.to(dt), v=v.to(dt), log_a=None, lam=lam)
 
 
+def make_sparse_int_inputs(B, T, H, d, L, onehot_level: int, seed: int = 0):
+    """bf16 inputs whose every intermediate stays an exactly representable integer even
+    through bf16 storage of the chunk states: q, v in {-1, 0, 1}, each k a signed one-hot
+    vector (so q.k is in {-1, 0, 1} and a state entry counts the tokens of a block whose k
+    hits that feature), no decay, one-hot lambda."""
+    g = _gen(seed)
+    q = torch.randint(-1, 2, (B, T, H, d), generator=g).float()
+    v = torch.randint(-1, 2, (B, T, H, d), generator=g).float()
+    hot = torch.randint(0, d, (B, T, H), generator=g)
+    sign = torch.randint(0, 2, (B, T, H), generator=g).float() * 2 - 1
+    k = torch.zeros(B, T, H, d)
+    k.scatter_(3, hot[..., None], sign[..., None])
+    lam = torch.zeros(B, T, H, L)
+    lam[..., onehot_level] = 1.0
+    bf = torch.bfloat16
+    return dict(q=q.to(bf), k=k.to(bf), v=v.to(bf), log_a=None, lam=lam)
+
+
 def make_decode_tokens(cfg: DecodeConfig, b: int, h: int, T: int):
     """Prefill stream of one (b, h): k [T,dk], v [T,dv] (cfg dtype), log_a [T] fp32.
 
