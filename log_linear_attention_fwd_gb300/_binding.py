@@ -156,6 +156,10 @@ def loglinear_fwd_with_events(q, k, v, log_a, lam, chunk, events, out, workspace
     created with enable_timing=True by the caller).  Returns the number of kernels."""
     B, T, H, dk = q.shape
     dv, L = v.shape[-1], lam.shape[-1]
+    st_ = stream if stream is not None else torch.cuda.current_stream()
+    for e in events:          # torch creates the CUDA event lazily, on its first record
+        if not e.cuda_event:
+            e.record(st_)
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     nk = ctypes.c_int(0)
     st = _lib.loglinear_fwd_with_events(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam),
