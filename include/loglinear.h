@@ -158,6 +158,33 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
 LL_API int loglinear_device_error(ll_stream_t stream, unsigned* flags);
 
 /*
+ * loglinear_fwd for callers that cannot allocate device memory.  The paper has no
+ * counterpart to this entry point: it exists for callers such as a plugin inside a host
+ * application that owns all device memory and hands extensions no allocator, or a
+ * real-time loop where cudaMalloc (which may synchronise the device) is not allowed.
+ *
+ * Same arguments and result as loglinear_fwd, minus the workspace.  The scratch lives in
+ * one fixed device array of LL_FWD_NOALLOC_SCRATCH_BYTES that the library declares; every
+ * GPU that loads the library's device code holds it until the process exits.  This call
+ * allocates nothing (no cudaMalloc, no allocating library routine).
+ *   - The first call on a device (with that device current) looks up the array's device
+ *     address and caches it; make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents.  Nothing in it
+ *     needs clearing between calls, but calls whose work overlaps on the GPU (another
+ *     stream, another host thread) race on it: serialise them.
+ *   - A problem whose scratch (loglinear_fwd_workspace_size) exceeds the array is
+ *     rejected with LL_ERR_WORKSPACE before any launch.
+ * Errors: those of loglinear_fwd; LL_ERR_WORKSPACE for problems too large; LL_ERR_CUDA if
+ * the array's address cannot be obtained.
+ */
+#define LL_FWD_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+LL_API int loglinear_fwd_noalloc(const void* q, const void* k, const void* v,
+                                 const float* log_a, const float* lambda, void* out,
+                                 int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                 int64_t L, int chunk, int in_dtype, int out_dtype, int path,
+                                 ll_stream_t stream);
+
+/*
  * Debug view of the forward's level indexing (first page, sections 层级判定算法 and 矩阵
  * 分解): writes levels[t * T + s] (int8, device) for 0 <= s, t < T: the Fenwick level the
  * given path assigns to the pair (query t, source s) through its intra-chunk formula or

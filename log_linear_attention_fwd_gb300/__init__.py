@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     lib,
     loglinear_decode_step,
     loglinear_fwd,
+    loglinear_fwd_noalloc,
     loglinear_fwd_with_events,
     resolve_path,
     status_string,

@@ -41,6 +41,8 @@ SIGNATURES = {
                                      _i64, _i64, _int, _int, _vp]),
     "loglinear_debug_level_map": (_int, [_i64, _int, _int, _vp, _vp]),
     "loglinear_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),
+    "loglinear_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                     _i64, _int, _int, _int, _int, _vp]),
 }
 
 
@@ -190,6 +192,22 @@ def loglinear_decode_step(state, q, k, v, log_a, lam, t, out=None, out_dtype=Non
                                     _dtype_code(out), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_decode_step")
+    return out
+
+
+def loglinear_fwd_noalloc(q, k, v, log_a, lam, chunk, out, path="auto", stream=None):
+    """loglinear_fwd without a workspace, for callers that cannot allocate device memory:
+    the scratch is the library's fixed device array (see include/loglinear.h).  `out` is
+    caller-provided; nothing is allocated here either."""
+    B, T, H, dk = q.shape
+    dv, L = v.shape[-1], lam.shape[-1]
+    for name, t in (("q", q), ("k", k), ("v", v), ("log_a", log_a), ("lam", lam), ("out", out)):
+        _check_dev(name, t)
+    st = _lib.loglinear_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
+                                    B, T, H, dk, dv, L, chunk, _dtype_code(q), _dtype_code(out),
+                                    PATHS[path], _stream(stream))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_fwd_noalloc")
     return out
 
 

@@ -114,4 +114,7 @@ cudaError_t launch_decode(float* state, const void* q, const void* k, const void
 
 cudaError_t launch_level_map(int T, int tile, int lc, int8_t* levels, cudaStream_t s);
 
+// Records a CUDA error for loglinear_last_cuda_error() and returns LL_ERR_CUDA.
+int report_cuda_error(cudaError_t e);
+
 }  // namespace ll

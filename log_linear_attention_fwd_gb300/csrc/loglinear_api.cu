@@ -107,6 +107,8 @@ size_t node_bytes(int path) { return path == LL_PATH_TC ? 2 : 4; }
 
 }  // namespace
 
+int ll::report_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 extern "C" {
 
 int loglinear_version(void) { return (0 << 16) | 1; }
