@@ -88,6 +88,25 @@ def decode_algorithmic(cfg):
     return cfg.B * cfg.H * lvl_bytes * (len(pre) + len(written))
 
 
+# ---------------------------------------------------------------- ranks
+
+
+def max_over_ranks(values, world, device):
+    """Per-rank step times -> their maximum over all ranks (the job is as slow as its
+    slowest rank).  One all-reduce of a small tensor; a no-op at world size 1."""
+    if world <= 1:
+        return list(values)
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world, units_per_rank, seconds):
+    """Units all ranks processed (each rank runs the same per-GPU workload: weak
+    scaling) divided by the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 # ---------------------------------------------------------------- clocks
 
 
@@ -107,8 +126,11 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
+            t0 = time.time()  # wait for the first sample so the window really starts here
+            while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.02)
         except Exception:
             self.proc = None
 
@@ -137,7 +159,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "warm-up + timed region, every 20 ms"}
 
 
 # ---------------------------------------------------------------- CPU oracle sample
@@ -214,13 +236,14 @@ def run_ours(args, rank, world, local_rank):
         return n_k
 
     mk = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    evs = [(mk(n_ev), mk(2)) for _ in range(args.steps)]
+    # clocks are sampled from the start of the warm-up to the end of the timed region
+    clocks = ClockSampler(local_rank)
+    clocks.start()
     for _ in range(args.warmup):
         flush.zero_()
         one_step(mk(n_ev), mk(2))
     torch.cuda.synchronize()
-    evs = [(mk(n_ev), mk(2)) for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank)
-    clocks.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -239,12 +262,9 @@ def run_ours(args, rank, world, local_rank):
     t_dec = [ed[0].elapsed_time(ed[1]) * 1e-3 for _, ed in evs]
     fwd_mean, dec_mean = sum(t_fwd) / len(t_fwd), sum(t_dec) / len(t_dec)
     stage_mean = [sum(s) / len(s) for s in t_stage]
-    if world > 1:
-        tt = torch.tensor([fwd_mean, dec_mean], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        fwd_mean, dec_mean = tt.tolist()
-    fwd_tok_s = world * cfg.B * cfg.T / fwd_mean
-    dec_tok_s = world * dcfg.B / dec_mean
+    fwd_mean, dec_mean = max_over_ranks([fwd_mean, dec_mean], world, dev)
+    fwd_tok_s = whole_job_rate(world, cfg.B * cfg.T, fwd_mean)
+    dec_tok_s = whole_job_rate(world, dcfg.B, dec_mean)
     fbytes, fflops = fwd_algorithmic(cfg)
     dbytes = decode_algorithmic(dcfg)
     t_hbm = fbytes / (peaks["hbm"] * 1e9)

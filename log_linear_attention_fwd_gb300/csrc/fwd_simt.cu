@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_state(FwdArgs a) {
   for (int r = threadIdx.x; r < n; r += kThreads) w[r] = expf(lgi - cs[r]);
   __syncthreads();
   const int64_t bh = (int64_t)b * a.H + h;
-  float* U = a.U + (bh * a.N + i) * (int64_t)dk * dv;
+  float* U = reinterpret_cast<float*>(a.U) + (bh * a.N + i) * (int64_t)dk * dv;
   for (int idx = threadIdx.x; idx < dk * dv; idx += kThreads) {
     const int d = idx / dv, e = idx - d * dv;
     float acc = 0.f;
@@ -204,7 +204,7 @@ cudaError_t launch_typed(const FwdArgs& a, cudaStream_t s, StageEvents* ev) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   if (a.N > 1) {
-    if ((e = launch_level_scan(a, /*bf16_nodes=*/false, s)) != cudaSuccess) return e;
+    if ((e = launch_level_scan(a, /*bf16_states=*/false, s)) != cudaSuccess) return e;
     if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   }
   simt_intra_readout<InT, OutT><<<grid_c, kThreads, sm3, s>>>(a);

@@ -5,27 +5,29 @@
 // and 两阶段计算; page "算力终结者来了！…", section 高效训练算法) with the tile as the chunk:
 //
 //   tc_chunk_state    per tile i: U_i^T = (w ⊙ V)^T K on tcgen05 (w_s = exp(cs_end - cs_s),
-//                     cs = tile-local prefix sums of log a), written fp32 [d_v][d_k], plus the
-//                     tile's log decay lg_i.
-//   level_scan        (level_scan.cu) Fenwick block totals of tiles, stored bf16 [d_v][d_k]
-//                     under the index of their first reader tile.
-//   tc_intra_readout  per tile j: S = Q K^T (tcgen05, TMEM), P = S ⊙ exp(cs_t - cs_s) ⊙
-//                     lambda[t, l(t,s)] on the causal half (CUDA cores, written back to shared
-//                     memory as bf16), O = P V (tcgen05); then for every set bit m-1 of j one
-//                     more MMA accumulates (r ⊙ Q) Tot into the same TMEM accumulator, with
-//                     r_t = lambda[t, 7+m] exp(cs_t + D), D the log decay from the block's end
-//                     to the tile's start.  The lambda-weighted per-level readout is thus
-//                     fused into the output accumulator: no per-level output reaches memory.
+//                     cs = tile-local prefix sums of log a), stored bf16 [d_v][d_k] through a
+//                     TMA store, plus the tile's log decay lg_i.
+//   level_scan        (level_scan.cu) Fenwick block totals of tiles in fp32, stored bf16
+//                     [d_v][d_k] under the index of their first reader tile.
+//   tc_intra_readout  per tile j: S = Q K^T (tcgen05, TMEM); P = S ⊙ exp(cs_t - cs_s) ⊙
+//                     lambda[t, l(t,s)] on the causal half (CUDA cores, bf16 into shared
+//                     memory); O = P V (tcgen05), moved to registers.  Then, for every set
+//                     bit m-1 of j, one MMA Q Tot_m into one of two TMEM buffers while the
+//                     previous level's product is added to O with the row weights
+//                     r_t = lambda[t, 7+m] exp(cs_t + D_m) (D_m = log decay from the
+//                     block's end to the tile's start).  The lambda-weighted per-level
+//                     readout is thus fused into the output epilogue; no per-level output
+//                     reaches memory.  bf16 output leaves through a TMA store.
 //
 // With 128-token tiles the chunk-pair level log2(C)+1 of a requested C = 64 lies inside a
 // tile and is taken in the dense masked product; the sum is the same.
 //
 // Shared-memory tiles are 128 rows x 128 bf16 stored as two 64-column panels with the
-// 128-byte swizzle TMA produces; K-major operands (Q, K, P, scaled Q, block states) and
-// MN-major ones (V as the B of P V, V and K in the state GEMM) are described to tcgen05
-// with the matching descriptors.  Every mbarrier wait is bounded (see tc_ptx.cuh); a CTA
-// whose wait times out raises g_tc_error, skips its remaining MMAs and stores, frees its
-// TMEM and exits.
+// 128-byte swizzle TMA produces; K-major operands (Q, K, P, block states) and MN-major
+// ones (V as the B of P V; V and K in the state GEMM) are described to tcgen05 with the
+// matching descriptors.  Every mbarrier wait is bounded (see tc_ptx.cuh); a CTA whose
+// wait times out raises g_tc_error, skips its remaining MMAs and stores, frees its TMEM
+// and exits.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -49,14 +51,13 @@ constexpr int kThreads = 128;               // one thread per tile row / TMEM la
 constexpr int kLamStride = 9;               // intra lambdas per row in smem (levels 0..7)
 constexpr int kIntraLevels = 8;             // levels inside a 128-token tile: 0..7
 constexpr int kTileLc = 7;                  // log2(kTile)
-constexpr int kMaxChunkLevels = 32;
+constexpr int kMaxChunkLevels = 32;         // chunk levels m = 1..31 (positions < 2^31)
 
 struct TcParams {
   int B, T, H, L, N;
   const float* log_a;
   const float* lam;
   void* out;
-  float* U;
   float* lg;
   int out_f32;
 };
@@ -66,13 +67,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return p + (((a + 1023u) & ~1023u) - a);
 }
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
-// Inclusive prefix sum over the 128 threads of the CTA; red holds 4 floats.
+// Inclusive prefix sum over the 128 threads of the CTA; red holds 4 floats and must not
+// be reused before the next __syncthreads.
 __device__ __forceinline__ float block_scan128(float x, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -92,31 +88,51 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Multiplies row r of a 128 x 128 swizzled bf16 tile by s, from src into dst (same
-// physical positions: the swizzle only permutes 16-byte chunks inside a row).
-__device__ __forceinline__ void scale_row(const uint8_t* src, uint8_t* dst, int r, float s) {
+// Multiplies row r of a 128 x 128 swizzled bf16 tile by s in place.  The swizzle only
+// permutes the 16-byte chunks inside a row; walking them from chunk (r mod 8) makes the
+// eight rows of a 1 KiB swizzle atom touch eight different bank groups at each step.
+__device__ __forceinline__ void scale_row_inplace(uint8_t* buf, int r, float s) {
 #pragma unroll
   for (int pnl = 0; pnl < 2; ++pnl) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t off = pnl * kPanel + r * 128 + c * 16;
-      uint4 u = *reinterpret_cast<const uint4*>(src + off);
+    for (int cc = 0; cc < 8; ++cc) {
+      const int c = (cc + r) & 7;
+      uint4* ptr = reinterpret_cast<uint4*>(buf + pnl * kPanel + r * 128 + c * 16);
+      uint4 u = *ptr;
       uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[k]));
         w[k] = pack_bf16(f.x * s, f.y * s);
       }
-      *reinterpret_cast<uint4*>(dst + off) = make_uint4(w[0], w[1], w[2], w[3]);
+      *ptr = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+}
+
+// Writes 32 fp32 values as bf16 into columns [32c, 32c+32) of row r of a swizzled tile.
+__device__ __forceinline__ void put_row32_bf16(uint8_t* buf, int r, int c, const float* v) {
+  uint8_t* panel = buf + (c >> 1) * kPanel;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(panel + sw128_offset(r, (c & 1) * 4 + q)) =
+        make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                   pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+__device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
+  uint8_t* panel = buf + (c >> 1) * kPanel;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(panel + sw128_offset(r, (c & 1) * 4 + q)) = make_uint4(0, 0, 0, 0);
 }
 
 // ------------------------------------------------------------------ K1: chunk states
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc_chunk_state_kernel(const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV, TcParams p) {
+                          const __grid_constant__ CUtensorMap tmV,
+                          const __grid_constant__ CUtensorMap tmU, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* Kb = smem;
@@ -138,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
+    prefetch_tensormap(&tmU);
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
     fence_mbar_init();
@@ -161,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float w = tid < n ? expf(lg - cs) : 0.f;
 
   bool ok = mbar_wait(&bars[0], 0);
-  if (ok) scale_row(Vb, Vb, tid, w);
+  if (ok) scale_row_inplace(Vb, tid, w);
   fence_proxy_async_smem();
   const bool all_ok = __syncthreads_and(ok);
   if (all_ok && tid == 0) {
@@ -176,20 +193,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mma_commit(&bars[1]);
   }
-  bool ok2 = all_ok && mbar_wait(&bars[1], 0);
+  const bool ok2 = all_ok && mbar_wait(&bars[1], 0);
   tc_fence_after();
   if (__syncthreads_and(ok2)) {
-    float* U = p.U + (((int64_t)b * p.H + h) * p.N + i) * (int64_t)(kD * kD) + (int64_t)tid * kD;
-#pragma unroll
+    // row tid of U^T (d_v index) -> bf16 into Kb (free since the MMA completed) -> TMA store
+#pragma unroll 1
     for (int c = 0; c < kD / 32; ++c) {
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, v);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        reinterpret_cast<float4*>(U + c * 32)[q] =
-            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      put_row32_bf16(Kb, tid, c, v);
     }
-    if (tid == 0) p.lg[((int64_t)b * p.H + h) * p.N + i] = lg;
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      const int row0 = (int)((((int64_t)b * p.H + h) * p.N + i) * kD);
+      tma_store_2d(&tmU, Kb, 0, row0);
+      tma_store_2d(&tmU, Kb + kPanel, 64, row0);
+      tma_store_commit();
+      p.lg[((int64_t)b * p.H + h) * p.N + i] = lg;
+      tma_store_wait_read();
+    }
   } else if (tid == 0) {
     atomicOr(&g_tc_error, 1u);
   }
@@ -200,29 +223,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ K3: intra + readout
 
+struct K3Smem {
+  // byte offsets from the 1024-aligned base
+  static constexpr int kQ = 0, kK = kOperand, kV = 2 * kOperand;
+  static constexpr int kBars = 3 * kOperand;                   // 7 mbarriers
+  static constexpr int kTslot = kBars + 7 * 8;
+  static constexpr int kRed = kTslot + 16;                     // 4 floats
+  static constexpr int kCarry = kRed + 16;                     // 4 floats
+  static constexpr int kCs = kCarry + 16;                      // 128 floats
+  static constexpr int kLam = kCs + 4 * kTile;                 // 128 x kLamStride floats
+  static constexpr int kDm = kLam + 4 * kTile * kLamStride;    // kMaxChunkLevels floats
+  static constexpr int kRs = kDm + 4 * kMaxChunkLevels;        // [levels][128] floats
+};
+
 __global__ void __launch_bounds__(kThreads, 2)
     tc_intra_readout_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
-                            const __grid_constant__ CUtensorMap tmNode, TcParams p) {
+                            const __grid_constant__ CUtensorMap tmNode,
+                            const __grid_constant__ CUtensorMap tmOut, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* Qb = smem;
-  uint8_t* Kb = smem + kOperand;      // K, then P, then the scaled Q of each level
-  uint8_t* Vb = smem + 2 * kOperand;  // V, then the block state of each level
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 3 * kOperand);  // load, mma, node
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
-  float* red = reinterpret_cast<float*>(tslot + 4);
-  float* cs_s = red + 4;                       // [128]
-  float* lam_s = cs_s + kTile;                 // [128][kLamStride]
-  float* Dm = lam_s + kTile * kLamStride;      // [kMaxChunkLevels]
+  uint8_t* Qb = smem + K3Smem::kQ;
+  uint8_t* Kb = smem + K3Smem::kK;   // K, then P, then the block states of odd levels
+  uint8_t* Vb = smem + K3Smem::kV;   // V, then the block states of even levels
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K3Smem::kBars);
+  uint64_t* bar_load = &bars[0];
+  uint64_t* bar_s = &bars[1];
+  uint64_t* bar_o = &bars[2];
+  uint64_t* bar_node = &bars[3];     // [2]
+  uint64_t* bar_lvl = &bars[5];      // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + K3Smem::kTslot);
+  float* red = reinterpret_cast<float*>(smem + K3Smem::kRed);
+  float* carry_s = reinterpret_cast<float*>(smem + K3Smem::kCarry);
+  float* cs_s = reinterpret_cast<float*>(smem + K3Smem::kCs);
+  float* lam_s = reinterpret_cast<float*>(smem + K3Smem::kLam);
+  float* Dm = reinterpret_cast<float*>(smem + K3Smem::kDm);
+  float* rs = reinterpret_cast<float*>(smem + K3Smem::kRs);
 
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int t0 = j * kTile;
   const int n = min(kTile, p.T - t0);
   const int64_t bh = (int64_t)b * p.H + h;
   const int64_t row = ((int64_t)b * p.T + t0 + tid) * p.H + h;  // (b, t, h) of this thread
+  const int nlev = __popc((unsigned)j);                          // inter-chunk levels read
 
   if (warp == 0) {
     tmem_alloc(tslot, 256);
@@ -233,9 +278,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmNode);
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    mbar_init(&bars[2], 1);
+    prefetch_tensormap(&tmOut);
+    for (int q = 0; q < 7; ++q) mbar_init(&bars[q], 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -244,38 +288,66 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t tmem = *tslot;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   if (tid == 0) {
-    mbar_arrive_expect_tx(&bars[0], 3 * kOperand);
-    tma_load_4d(&tmQ, &bars[0], Qb, 0, h, t0, b);
-    tma_load_4d(&tmQ, &bars[0], Qb + kPanel, 64, h, t0, b);
-    tma_load_4d(&tmK, &bars[0], Kb, 0, h, t0, b);
-    tma_load_4d(&tmK, &bars[0], Kb + kPanel, 64, h, t0, b);
-    tma_load_4d(&tmV, &bars[0], Vb, 0, h, t0, b);
-    tma_load_4d(&tmV, &bars[0], Vb + kPanel, 64, h, t0, b);
+    mbar_arrive_expect_tx(bar_load, 3 * kOperand);
+    tma_load_4d(&tmQ, bar_load, Qb, 0, h, t0, b);
+    tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, h, t0, b);
+    tma_load_4d(&tmK, bar_load, Kb, 0, h, t0, b);
+    tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, h, t0, b);
+    tma_load_4d(&tmV, bar_load, Vb, 0, h, t0, b);
+    tma_load_4d(&tmV, bar_load, Vb + kPanel, 64, h, t0, b);
+    // warm L2 with every block state this tile will read
+    for (int m = 1; m < kMaxChunkLevels; ++m) {
+      int64_t c;
+      if (!inter_block(j, m, &c)) continue;
+      const int r0 = (int)((bh * p.N + c) * kD);
+      tma_prefetch_2d(&tmNode, 0, r0);
+      tma_prefetch_2d(&tmNode, 64, r0);
+    }
   }
-  // per-row decay prefix and intra-tile lambdas, while the tiles are in flight
+  // ---- per-row data while the tiles are in flight
   const float la = (p.log_a && tid < n) ? p.log_a[row] : 0.f;
   const float cs = block_scan128(la, red);
   cs_s[tid] = cs;
 #pragma unroll
   for (int l = 0; l < kIntraLevels; ++l)
     lam_s[tid * kLamStride + l] = (tid < n && l < p.L) ? p.lam[row * p.L + l] : 0.f;
-  // log decay from the end of each inter-chunk block to the start of this tile
-  if (warp == 0) {
+  // D_m = sum of lg over tiles [c_m, j), from inclusive prefix sums of lg[j-1], lg[j-2], ..
+  if (nlev > 0) {
     const float* lgp = p.lg + bh * p.N;
-    for (int m = 1; m < kMaxChunkLevels && (1 << (m - 1)) <= j; ++m) {
-      if (!((j >> (m - 1)) & 1)) continue;
-      const int c = (j >> (m - 1)) << (m - 1);
-      float s = 0.f;
-      for (int i = c + lane; i < j; i += 32) s += lgp[i];
-      s = warp_sum(s);
-      if (lane == 0) Dm[m] = s;
+    const int top = 31 - __clz((unsigned)j);
+    const int span = j - (1 << top);  // the longest range j - c_m over every level
+    if (tid == 0) {
+      carry_s[0] = 0.f;
+      for (int m = 1; m <= top + 1; ++m)
+        if (((j >> (m - 1)) & 1) && ((j >> (m - 1)) << (m - 1)) == j) Dm[m] = 0.f;
+    }
+    for (int base = 0; base < span; base += kThreads) {
+      __syncthreads();
+      const int idx = base + tid;
+      const float x = idx < span ? lgp[j - 1 - idx] : 0.f;
+      const float incl = block_scan128(x, red) + carry_s[0];
+      for (int m = 1; m <= top + 1; ++m) {
+        if (!((j >> (m - 1)) & 1)) continue;
+        const int c = (j >> (m - 1)) << (m - 1);
+        if (j - c - 1 == idx) Dm[m] = incl;
+      }
+      __syncthreads();
+      if (tid == kThreads - 1) carry_s[0] = incl;
     }
   }
   __syncthreads();
+  {  // per-level row weights r_t = lambda[t, 7+m] exp(cs_t + D_m), level-major in smem
+    int k = 0;
+    for (int m = 1; m < kMaxChunkLevels; ++m) {
+      if (!((j >> (m - 1)) & 1)) continue;
+      rs[k * kTile + tid] = tid < n ? p.lam[row * p.L + kTileLc + m] * __expf(cs + Dm[m]) : 0.f;
+      ++k;
+    }
+  }
 
-  bool ok = mbar_wait(&bars[0], 0);
+  // ---- S = Q K^T
+  bool ok = mbar_wait(bar_load, 0);
   bool all_ok = __syncthreads_and(ok);
-  // S = Q K^T
   if (all_ok && tid == 0) {
     tc_fence_after();
     constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
@@ -286,48 +358,41 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_bf16(tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
                idesc, kk > 0);
     }
-    mma_commit(&bars[1]);
+    mma_commit(bar_s);
   }
-  uint32_t mma_phase = 0;
-  ok = all_ok && mbar_wait(&bars[1], mma_phase);
-  mma_phase ^= 1;
+  ok = all_ok && mbar_wait(bar_s, 0);
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
-  // P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t, s)] on s <= t, as bf16 into Kb (K-major)
+  // ---- P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t, s)] on s <= t, bf16 into Kb (K-major).
+  // Column chunk c of warp w lies entirely above the diagonal when c > w.
   if (all_ok) {
     const uint32_t tq = (uint32_t)(t0 + tid);
     const float* lam_r = lam_s + tid * kLamStride;
 #pragma unroll 1
     for (int c = 0; c < kTile / 32; ++c) {
+      if (c > warp) {
+        put_row32_zero(Kb, tid, c);
+        continue;
+      }
       float sv[32];
       tmem_ld32(tmem + lane_base + c * 32, sv);
-      uint32_t pk[16];
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        float pr[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int s = c * 32 + k + u;
-          float v = 0.f;
-          if (s <= tid && tid < n) {
-            const int lvl = fenwick_level(tq, (uint32_t)(t0 + s));
-            v = sv[k + u] * lam_r[lvl] * __expf(cs - cs_s[s]);
-          }
-          pr[u] = v;
+      for (int k = 0; k < 32; ++k) {
+        const int s = c * 32 + k;
+        float v = 0.f;
+        if (s <= tid && tid < n) {
+          const int lvl = fenwick_level(tq, (uint32_t)(t0 + s));
+          v = sv[k] * lam_r[lvl] * __expf(cs - cs_s[s]);
         }
-        pk[k >> 1] = pack_bf16(pr[0], pr[1]);
+        sv[k] = v;
       }
-      uint8_t* panel = Kb + (c >> 1) * kPanel;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(panel + sw128_offset(tid, (c & 1) * 4 + q)) =
-            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      put_row32_bf16(Kb, tid, c, sv);
     }
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
-  // O = P V  (V MN-major as B)
+  // ---- O = P V  (V MN-major as B)
   if (all_ok && tid == 0) {
     tc_fence_after();
     constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
@@ -338,73 +403,126 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_bf16(tmem + 128, smem_desc_sw128(pa + aoff, 16, 1024),
                smem_desc_sw128(va + kk * 2048, kPanel, 1024), idesc, kk > 0);
     }
-    mma_commit(&bars[1]);
+    mma_commit(bar_o);
   }
-  // inter-chunk levels: O += (r ⊙ Q) Tot for every set bit m-1 of j
-  uint32_t node_phase = 0;
-  for (int m = 1; m < kMaxChunkLevels && (1 << (m - 1)) <= j; ++m) {
-    if (!((j >> (m - 1)) & 1)) continue;
-    ok = all_ok && mbar_wait(&bars[1], mma_phase);  // previous MMA released Kb and Vb
-    mma_phase ^= 1;
-    all_ok = __syncthreads_and(ok);
-    if (!all_ok) break;
-    const int c = (j >> (m - 1)) << (m - 1);
-    if (tid == 0) {
-      const int r0 = (int)((bh * p.N + c) * kD);
-      mbar_arrive_expect_tx(&bars[2], kOperand);
-      tma_load_2d(&tmNode, &bars[2], Vb, 0, r0);
-      tma_load_2d(&tmNode, &bars[2], Vb + kPanel, 64, r0);
-    }
-    const float r = tid < n ? p.lam[row * p.L + kTileLc + m] * __expf(cs + Dm[m]) : 0.f;
-    scale_row(Qb, Kb, tid, r);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    ok = mbar_wait(&bars[2], node_phase);
-    node_phase ^= 1;
-    all_ok = __syncthreads_and(ok);
-    if (!all_ok) break;
-    if (tid == 0) {
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
-      const uint32_t aa = smem_u32(Kb), sa = smem_u32(Vb);
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-        mma_bf16(tmem + 128, smem_desc_sw128(aa + off, 16, 1024),
-                 smem_desc_sw128(sa + off, 16, 1024), idesc, 1);
-      }
-      mma_commit(&bars[1]);
-    }
-  }
-  ok = all_ok && mbar_wait(&bars[1], mma_phase);
+  ok = all_ok && mbar_wait(bar_o, 0);
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
+  float o[kD];
+#pragma unroll
+  for (int q = 0; q < kD; ++q) o[q] = 0.f;
   if (all_ok) {
-    // every lane executes the warp-wide TMEM loads; padding rows skip only the stores
-    const int64_t obase = row * kD;
-#pragma unroll 1
+#pragma unroll
     for (int c = 0; c < kD / 32; ++c) {
       float v[32];
       tmem_ld32(tmem + lane_base + 128 + c * 32, v);
-      if (tid >= n) continue;
-      if (p.out_f32) {
-        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + obase + c * 32);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      } else {
-        uint4* o =
-            reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + obase + c * 32);
+      for (int q = 0; q < 32; ++q) o[c * 32 + q] = v[q];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();  // Kb, Vb and all 256 TMEM columns are free from here on
+
+  // ---- inter-chunk levels: MMA into alternating TMEM buffers, weighted adds into o.
+  // Level k uses shared buffer (k odd ? Kb : Vb), TMEM columns [128 (k&1), +128),
+  // mbarriers bar_node[k&1] (its block state arrived) and bar_lvl[k&1] (its MMA finished).
+  if (all_ok && tid == 0) {
+    int k = 0;
+    for (int m = 1; m < kMaxChunkLevels && k < 2; ++m) {
+      int64_t c;
+      if (!inter_block(j, m, &c)) continue;
+      const int r0 = (int)((bh * p.N + c) * kD);
+      uint8_t* dst = (k & 1) ? Kb : Vb;
+      mbar_arrive_expect_tx(&bar_node[k], kOperand);
+      tma_load_2d(&tmNode, &bar_node[k], dst, 0, r0);
+      tma_load_2d(&tmNode, &bar_node[k], dst + kPanel, 64, r0);
+      ++k;
+    }
+  }
+  uint32_t node_ph[2] = {0, 0}, lvl_ph[2] = {0, 0};
+  int m_next = 1;  // scan position of the next block state to load (after the first two)
+  if (tid == 0) {
+    int seen = 0;
+    for (; m_next < kMaxChunkLevels; ++m_next) {
+      if (!((j >> (m_next - 1)) & 1)) continue;
+      if (++seen > 2) break;
+    }
+  }
+  for (int k = 0; k <= nlev && all_ok; ++k) {
+    if (k < nlev) {  // issue level k
+      const int bf = k & 1;
+      ok = mbar_wait(&bar_node[bf], node_ph[bf]);
+      node_ph[bf] ^= 1;
+      all_ok = __syncthreads_and(ok);
+      if (!all_ok) break;
+      if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+        const uint32_t qa = smem_u32(Qb), sa = smem_u32(bf ? Kb : Vb);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          o[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
-                            pack_bf16(v[8 * q + 4], v[8 * q + 5]),
-                            pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+          mma_bf16(tmem + bf * 128, smem_desc_sw128(qa + off, 16, 1024),
+                   smem_desc_sw128(sa + off, 16, 1024), idesc, kk > 0);
+        }
+        mma_commit(&bar_lvl[bf]);
+      }
+    }
+    if (k >= 1) {  // finish level k-1 while level k runs
+      const int bf = (k - 1) & 1;
+      ok = mbar_wait(&bar_lvl[bf], lvl_ph[bf]);
+      lvl_ph[bf] ^= 1;
+      tc_fence_after();
+      all_ok = __syncthreads_and(ok);
+      if (!all_ok) break;
+      const float r = rs[(k - 1) * kTile + tid];
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + bf * 128 + c * 32, v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) o[c * 32 + q] = fmaf(r, v[q], o[c * 32 + q]);
+      }
+      tc_fence_before();
+      __syncthreads();  // buffer bf (TMEM and shared) is free again
+      if (tid == 0 && k + 1 < nlev) {  // block state of level k+1 into buffer bf
+        int64_t c = 0;
+        while (m_next < kMaxChunkLevels && !inter_block(j, m_next, &c)) ++m_next;
+        const int r0 = (int)((bh * p.N + c) * kD);
+        ++m_next;
+        uint8_t* dst = bf ? Kb : Vb;
+        mbar_arrive_expect_tx(&bar_node[bf], kOperand);
+        tma_load_2d(&tmNode, &bar_node[bf], dst, 0, r0);
+        tma_load_2d(&tmNode, &bar_node[bf], dst + kPanel, 64, r0);
       }
     }
   }
-  if (!all_ok && tid == 0) atomicOr(&g_tc_error, 1u);
+
+  // ---- epilogue
+  if (all_ok) {
+    if (p.out_f32) {
+      if (tid < n) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * kD);
+#pragma unroll
+        for (int q = 0; q < kD / 4; ++q)
+          dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      }
+    } else {
+      // no MMA reads Q any more: stage the bf16 tile there and store it with TMA
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) put_row32_bf16(Qb, tid, c, o + c * 32);
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tma_store_4d(&tmOut, Qb, 0, h, t0, b);
+        tma_store_4d(&tmOut, Qb + kPanel, 64, h, t0, b);
+        tma_store_commit();
+        tma_store_wait_read();
+      }
+    }
+  } else if (tid == 0) {
+    atomicOr(&g_tc_error, 1u);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
@@ -426,7 +544,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [B, T, H, 128] bf16, boxes of 128 tokens x 64 features of one (b, h); rows past T read 0.
+// [B, T, H, 128] bf16, boxes of 128 tokens x 64 features of one (b, h); rows past T read
+// as 0 and are not written.
 bool make_tokens_map(CUtensorMap* m, const void* base, int B, int T, int H) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -440,8 +559,8 @@ bool make_tokens_map(CUtensorMap* m, const void* base, int B, int T, int H) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Block states [rows = B*H*N*128][128] bf16, boxes of 128 rows x 64 columns.
-bool make_nodes_map(CUtensorMap* m, const void* base, int64_t rows) {
+// [rows][128] bf16 matrices (chunk states, block states), boxes of 128 rows x 64 columns.
+bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
@@ -454,8 +573,7 @@ bool make_nodes_map(CUtensorMap* m, const void* base, int64_t rows) {
 }
 
 constexpr size_t kSmemK1 = 2 * kOperand + 1024 + 256;
-constexpr size_t kSmemK3 =
-    3 * kOperand + 1024 + 64 + 4 * (4 + kTile + kTile * kLamStride + kMaxChunkLevels);
+size_t smem_k3(int levels) { return (size_t)K3Smem::kRs + 4 * kTile * levels + 1024; }
 
 }  // namespace
 
@@ -464,15 +582,19 @@ bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int /*chunk*/) {
 }
 
 cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev) {
-  CUtensorMap tmQ, tmK, tmV, tmNode;
+  const int64_t rows = (int64_t)a.B * a.H * a.N * kD;
+  CUtensorMap tmQ, tmK, tmV, tmOut, tmNode, tmU;
   if (!make_tokens_map(&tmQ, a.q, a.B, a.T, a.H) || !make_tokens_map(&tmK, a.k, a.B, a.T, a.H) ||
       !make_tokens_map(&tmV, a.v, a.B, a.T, a.H) ||
-      !make_nodes_map(&tmNode, a.nodes, (int64_t)a.B * a.H * a.N * kD))
+      !make_tokens_map(&tmOut, a.out, a.B, a.T, a.H) || !make_rows_map(&tmNode, a.nodes, rows) ||
+      !make_rows_map(&tmU, a.U, rows))
     return cudaErrorInvalidValue;
   TcParams p;
   p.B = a.B; p.T = a.T; p.H = a.H; p.L = a.L; p.N = a.N;
-  p.log_a = a.log_a; p.lam = a.lam; p.out = a.out; p.U = a.U; p.lg = a.lg;
+  p.log_a = a.log_a; p.lam = a.lam; p.out = a.out; p.lg = a.lg;
   p.out_f32 = out_dtype == LL_F32;
+  int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
+  while ((int64_t(1) << levels) < a.N) ++levels;
   cudaError_t e;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -481,19 +603,21 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemK1);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(tc_intra_readout_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemK3);
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem_k3(kMaxChunkLevels - 1));
   });
   if (attr_err != cudaSuccess) return attr_err;
   const dim3 grid(a.N, a.H, a.B);
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
-  tc_chunk_state_kernel<<<grid, kThreads, kSmemK1, s>>>(tmK, tmV, p);
+  tc_chunk_state_kernel<<<grid, kThreads, kSmemK1, s>>>(tmK, tmV, tmU, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   if (a.N > 1) {
-    if ((e = launch_level_scan(a, /*bf16_nodes=*/true, s)) != cudaSuccess) return e;
+    if ((e = launch_level_scan(a, /*bf16_states=*/true, s)) != cudaSuccess) return e;
     if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   }
-  tc_intra_readout_kernel<<<grid, kThreads, kSmemK3, s>>>(tmQ, tmK, tmV, tmNode, p);
+  tc_intra_readout_kernel<<<grid, kThreads, smem_k3(levels), s>>>(tmQ, tmK, tmV, tmNode, tmOut,
+                                                                    p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   return ev ? ev->finish(s) : cudaSuccess;

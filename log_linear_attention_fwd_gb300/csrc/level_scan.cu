@@ -3,6 +3,8 @@
 // section 高效训练算法).
 //
 // Input: per-chunk states U_i (decayed to the chunk's end) and per-chunk log decays lg_i.
+// States are read and written in one storage type (fp32 on the CUDA-core path, bf16 on
+// the tensor-core path); the block totals are always accumulated in fp32.
 // At chunk level m the chunks form aligned blocks of 2^(m-1); each odd block reads the
 // total of its even sibling,
 //     Tot(m, p) = sum_{i in block p} exp(sum_{i' in block p, i' > i} lg_i') U_i,
@@ -39,6 +41,21 @@ __device__ __forceinline__ Vec<VW> load_v(const float* p) {
 }
 
 template <int VW>
+__device__ __forceinline__ Vec<VW> load_v(const __nv_bfloat16* p) {
+  Vec<VW> r;
+  if constexpr (VW == 4) {
+    const uint2 t = __ldcs(reinterpret_cast<const uint2*>(p));
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
+    r.x[0] = lo.x; r.x[1] = lo.y; r.x[2] = hi.x; r.x[3] = hi.y;
+  } else {
+#pragma unroll
+    for (int k = 0; k < VW; ++k) r.x[k] = __bfloat162float(p[k]);
+  }
+  return r;
+}
+
+template <int VW>
 __device__ __forceinline__ void store_v(float* p, const Vec<VW>& v) {
   if constexpr (VW == 4) {
     *reinterpret_cast<float4*>(p) = make_float4(v.x[0], v.x[1], v.x[2], v.x[3]);
@@ -63,13 +80,14 @@ __device__ __forceinline__ void store_v(__nv_bfloat16* p, const Vec<VW>& v) {
   }
 }
 
-template <typename NodeT, int VW>
+template <typename StateT, int VW>
 __global__ void __launch_bounds__(kThreads) level_scan_kernel(FwdArgs a) {
+  using NodeT = StateT;
   const int64_t elems = (int64_t)a.dk * a.dv;
   const int64_t e = VW * ((int64_t)blockIdx.x * kThreads + threadIdx.x);
   if (e >= elems) return;
   const int64_t bh = (int64_t)blockIdx.z * a.H + blockIdx.y;
-  const float* U = a.U + bh * a.N * elems + e;
+  const StateT* U = reinterpret_cast<const StateT*>(a.U) + bh * a.N * elems + e;
   NodeT* nodes = reinterpret_cast<NodeT*>(a.nodes) + bh * a.N * elems + e;
   const float* lg = a.lg + bh * a.N;
   Vec<VW> stk[kMaxLevels];
@@ -106,17 +124,17 @@ __global__ void __launch_bounds__(kThreads) level_scan_kernel(FwdArgs a) {
 
 }  // namespace
 
-cudaError_t launch_level_scan(const FwdArgs& a, bool bf16_nodes, cudaStream_t s) {
+cudaError_t launch_level_scan(const FwdArgs& a, bool bf16_states, cudaStream_t s) {
   const int64_t elems = (int64_t)a.dk * a.dv;
   if (elems % 4 == 0) {
     const dim3 grid((unsigned)((elems / 4 + kThreads - 1) / kThreads), a.H, a.B);
-    if (bf16_nodes)
+    if (bf16_states)
       level_scan_kernel<__nv_bfloat16, 4><<<grid, kThreads, 0, s>>>(a);
     else
       level_scan_kernel<float, 4><<<grid, kThreads, 0, s>>>(a);
   } else {
     const dim3 grid((unsigned)((elems + kThreads - 1) / kThreads), a.H, a.B);
-    if (bf16_nodes)
+    if (bf16_states)
       level_scan_kernel<__nv_bfloat16, 1><<<grid, kThreads, 0, s>>>(a);
     else
       level_scan_kernel<float, 1><<<grid, kThreads, 0, s>>>(a);

@@ -60,7 +60,7 @@ struct FwdArgs {
   int C, lc;  // tile length and log2(tile)
   int N;      // tiles per (b, h)
   // workspace
-  float* U;       // [B*H][N][dk*dv] chunk states (layout per path)
+  void* U;        // [B*H][N][dk*dv] chunk states (fp32 on CUDA cores, bf16 on tensor cores)
   void* nodes;    // [B*H][N][dk*dv] Fenwick block states, slot c = first reader chunk
   float* lg;      // [B*H][N] log decay of each whole chunk
 };
@@ -70,7 +70,7 @@ struct FwdWorkspace {
   size_t off_U, off_nodes, off_lg, total;
 };
 FwdWorkspace fwd_workspace_layout(int64_t B, int64_t H, int64_t N, int64_t dk, int64_t dv,
-                                  size_t node_elem_bytes);
+                                  size_t state_elem_bytes);
 
 // Optional per-kernel event recording by the launchers (instrumentation only).
 struct StageEvents {
@@ -95,7 +95,7 @@ struct StageEvents {
 cudaError_t launch_simt_forward(const FwdArgs& a, int in_dtype, int out_dtype, cudaStream_t s,
                                 StageEvents* ev);
 cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev);
-cudaError_t launch_level_scan(const FwdArgs& a, bool bf16_nodes, cudaStream_t s);
+cudaError_t launch_level_scan(const FwdArgs& a, bool bf16_states, cudaStream_t s);
 // Reads and clears the tensor-core path's device error word (synchronises the stream).
 cudaError_t tc_take_error(cudaStream_t s, unsigned* flags);
 bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int chunk);

@@ -11,12 +11,12 @@ namespace ll {
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 FwdWorkspace fwd_workspace_layout(int64_t B, int64_t H, int64_t N, int64_t dk, int64_t dv,
-                                  size_t node_elem_bytes) {
+                                  size_t state_elem_bytes) {
   FwdWorkspace w;
   const size_t states = (size_t)(B * H * N) * (size_t)(dk * dv);
   w.off_U = 0;
-  w.off_nodes = align_up(w.off_U + states * sizeof(float), 256);
-  w.off_lg = align_up(w.off_nodes + states * node_elem_bytes, 256);
+  w.off_nodes = align_up(w.off_U + states * state_elem_bytes, 256);
+  w.off_lg = align_up(w.off_nodes + states * state_elem_bytes, 256);
   w.total = align_up(w.off_lg + (size_t)(B * H * N) * sizeof(float), 256);
   return w;
 }
@@ -172,7 +172,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* lo
   a.B = (int)B; a.T = (int)T; a.H = (int)H; a.dk = (int)dk; a.dv = (int)dv; a.L = (int)L;
   a.C = tile; a.lc = log2_exact(tile); a.N = (int)N;
   char* ws = static_cast<char*>(workspace);
-  a.U = reinterpret_cast<float*>(ws + w.off_U);
+  a.U = ws + w.off_U;
   a.nodes = ws + w.off_nodes;
   a.lg = reinterpret_cast<float*>(ws + w.off_lg);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -100,9 +100,9 @@ def test_workspace_size_and_paths(L):
     assert L.resolve_path(64, 64, 64, L.LL_BF16) == "simt"
     with pytest.raises(L.LoglinearError):
         L.resolve_path(64, 64, 64, L.LL_BF16, "tc")
-    # tensor-core workspace: fp32 chunk states + bf16 block states, 128-token tiles
+    # tensor-core workspace: bf16 chunk states + bf16 block states, 128-token tiles
     tc = L.fwd_workspace_size(1, 16384, 16, 128, 128, 64, L.LL_BF16, "tc")
-    assert tc >= 16 * 128 * 128 * 128 * (4 + 2)
+    assert tc >= 16 * 128 * 128 * 128 * (2 + 2)
 
 
 def dec(L, **kw):
