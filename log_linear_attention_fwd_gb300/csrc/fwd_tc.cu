@@ -28,6 +28,10 @@
 // matching descriptors.  Every mbarrier wait is bounded (see tc_ptx.cuh); a CTA whose
 // wait times out raises g_tc_error, skips its remaining MMAs and stores, frees its TMEM
 // and exits.
+//
+// Single-lane issue blocks (TMA, MMA) are followed by __syncwarp(): otherwise the other
+// lanes of warp 0 reach the next mbarrier spin first and keep the issuing lane from
+// being scheduled for microseconds.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -170,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_4d(&tmV, &bars[0], Vb, 0, h, t0, b);
     tma_load_4d(&tmV, &bars[0], Vb + kPanel, 64, h, t0, b);
   }
+  __syncwarp();
   const float la = (p.log_a && tid < n) ? p.log_a[((int64_t)b * p.T + t0 + tid) * p.H + h] : 0.f;
   const float cs = block_scan128(la, red);
   if (tid == kThreads - 1) lg_s[0] = cs;  // padding rows add 0: the last prefix is the total
@@ -193,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mma_commit(&bars[1]);
   }
+  __syncwarp();  // lane 0 must finish issuing before its warp spins on the barrier
   const bool ok2 = all_ok && mbar_wait(&bars[1], 0);
   tc_fence_after();
   if (__syncthreads_and(ok2)) {
@@ -223,20 +229,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ K3: intra + readout
 
+// 8 warps: warps w and w+4 share TMEM lane quarter w mod 4 (tile rows 32(w mod 4)..+31).
+// They split that quarter's causal chunks of P between them, and the output columns
+// (64 each) of O and of every level epilogue.
+constexpr int kThreads3 = 256;
+
 struct K3Smem {
   // byte offsets from the 1024-aligned base
   static constexpr int kQ = 0, kK = kOperand, kV = 2 * kOperand;
   static constexpr int kBars = 3 * kOperand;                   // 7 mbarriers
   static constexpr int kTslot = kBars + 7 * 8;
-  static constexpr int kRed = kTslot + 16;                     // 4 floats
-  static constexpr int kCarry = kRed + 16;                     // 4 floats
+  static constexpr int kRed = kTslot + 16;                     // 8 floats
+  static constexpr int kCarry = kRed + 32;                     // 4 floats
   static constexpr int kCs = kCarry + 16;                      // 128 floats
   static constexpr int kLam = kCs + 4 * kTile;                 // 128 x kLamStride floats
   static constexpr int kDm = kLam + 4 * kTile * kLamStride;    // kMaxChunkLevels floats
   static constexpr int kRs = kDm + 4 * kMaxChunkLevels;        // [levels][128] floats
 };
 
-__global__ void __launch_bounds__(kThreads, 2)
+// Inclusive prefix sum over the 256 threads of the CTA; red holds 8 floats and must not
+// be reused before the next __syncthreads.
+__device__ __forceinline__ float block_scan256(float x, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  float pre = 0.f;
+  for (int w = 0; w < warp; ++w) pre += red[w];
+  return x + pre;
+}
+
+__global__ void __launch_bounds__(kThreads3, 2)
     tc_intra_readout_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
@@ -263,11 +290,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int qt = warp & 3;           // row quarter (TMEM lane quarter) of this warp
+  const int hh = warp >> 2;          // which of the quarter's two warps
+  const int r = tid & (kTile - 1);   // tile row of this thread
   const int t0 = j * kTile;
   const int n = min(kTile, p.T - t0);
   const int64_t bh = (int64_t)b * p.H + h;
-  const int64_t row = ((int64_t)b * p.T + t0 + tid) * p.H + h;  // (b, t, h) of this thread
-  const int nlev = __popc((unsigned)j);                          // inter-chunk levels read
+  const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;  // (b, t, h) of row r
+  const int nlev = __popc((unsigned)j);                        // inter-chunk levels read
 
   if (warp == 0) {
     tmem_alloc(tslot, 256);
@@ -286,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_load, 3 * kOperand);
     tma_load_4d(&tmQ, bar_load, Qb, 0, h, t0, b);
@@ -304,43 +334,65 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_prefetch_2d(&tmNode, 64, r0);
     }
   }
-  // ---- per-row data while the tiles are in flight
-  const float la = (p.log_a && tid < n) ? p.log_a[row] : 0.f;
-  const float cs = block_scan128(la, red);
-  cs_s[tid] = cs;
+  __syncwarp();
+  // ---- per-row data while the tiles are in flight.  Every global load of this phase is
+  // issued first (log a, the intra- and inter-level lambdas, the tile log decays D_m
+  // sums over) so that their latencies overlap; the scans and exponentials follow.  The
+  // two threads of a row split the loads.
+  const float* lgp = p.lg + bh * p.N;
+  const int top = nlev > 0 ? 31 - __clz((unsigned)j) : 0;
+  const int span = nlev > 0 ? j - (1 << top) : 0;  // the longest range j - c_m
+  const bool row_live = r < n;
+  const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
+  float lam_in[kIntraLevels / 2];
 #pragma unroll
-  for (int l = 0; l < kIntraLevels; ++l)
-    lam_s[tid * kLamStride + l] = (tid < n && l < p.L) ? p.lam[row * p.L + l] : 0.f;
+  for (int i = 0; i < kIntraLevels / 2; ++i) {
+    const int l = hh * (kIntraLevels / 2) + i;
+    lam_in[i] = (row_live && l < p.L) ? p.lam[row * p.L + l] : 0.f;
+  }
+  const float lg_first = tid < span ? lgp[j - 1 - tid] : 0.f;
+  {  // raw inter-level lambdas, level-major in smem (weighted below); levels alternate
+    int k = 0;  // between the two threads of a row
+#pragma unroll 4
+    for (int m = 1; m < kMaxChunkLevels; ++m) {
+      if (!((j >> (m - 1)) & 1)) continue;
+      if ((k & 1) == hh) rs[k * kTile + r] = row_live ? p.lam[row * p.L + kTileLc + m] : 0.f;
+      ++k;
+    }
+  }
+  const float cs_scan = block_scan256(la, red);  // threads 0..127 hold row prefixes
+  if (hh == 0) cs_s[r] = cs_scan;
+#pragma unroll
+  for (int i = 0; i < kIntraLevels / 2; ++i)
+    lam_s[r * kLamStride + hh * (kIntraLevels / 2) + i] = lam_in[i];
   // D_m = sum of lg over tiles [c_m, j), from inclusive prefix sums of lg[j-1], lg[j-2], ..
   if (nlev > 0) {
-    const float* lgp = p.lg + bh * p.N;
-    const int top = 31 - __clz((unsigned)j);
-    const int span = j - (1 << top);  // the longest range j - c_m over every level
     if (tid == 0) {
       carry_s[0] = 0.f;
       for (int m = 1; m <= top + 1; ++m)
         if (((j >> (m - 1)) & 1) && ((j >> (m - 1)) << (m - 1)) == j) Dm[m] = 0.f;
     }
-    for (int base = 0; base < span; base += kThreads) {
+    for (int base = 0; base < span; base += kThreads3) {
       __syncthreads();
       const int idx = base + tid;
-      const float x = idx < span ? lgp[j - 1 - idx] : 0.f;
-      const float incl = block_scan128(x, red) + carry_s[0];
+      const float x = base == 0 ? lg_first : (idx < span ? lgp[j - 1 - idx] : 0.f);
+      const float incl = block_scan256(x, red) + carry_s[0];
       for (int m = 1; m <= top + 1; ++m) {
         if (!((j >> (m - 1)) & 1)) continue;
         const int c = (j >> (m - 1)) << (m - 1);
         if (j - c - 1 == idx) Dm[m] = incl;
       }
       __syncthreads();
-      if (tid == kThreads - 1) carry_s[0] = incl;
+      if (tid == kThreads3 - 1) carry_s[0] = incl;
     }
   }
   __syncthreads();
-  {  // per-level row weights r_t = lambda[t, 7+m] exp(cs_t + D_m), level-major in smem
+  const float cs = cs_s[r];
+  {  // per-level row weights r_t = lambda[t, 7+m] exp(cs_t + D_m)
     int k = 0;
     for (int m = 1; m < kMaxChunkLevels; ++m) {
       if (!((j >> (m - 1)) & 1)) continue;
-      rs[k * kTile + tid] = tid < n ? p.lam[row * p.L + kTileLc + m] * __expf(cs + Dm[m]) : 0.f;
+      if ((k & 1) == hh) rs[k * kTile + r] *= __expf(cs + Dm[m]);
       ++k;
     }
   }
@@ -360,33 +412,38 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     mma_commit(bar_s);
   }
+  __syncwarp();  // lane 0 must finish issuing before its warp spins on the barrier
   ok = all_ok && mbar_wait(bar_s, 0);
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
   // ---- P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t, s)] on s <= t, bf16 into Kb (K-major).
-  // Column chunk c of warp w lies entirely above the diagonal when c > w.
+  // The two warps of quarter qt take the 32-column chunks of their parity.  Chunks
+  // c > qt lie above the diagonal (zero); chunks c < qt lie below it, where every pair
+  // has the same level 5 + bit_length(qt XOR c); chunk qt holds the diagonal.
   if (all_ok) {
-    const uint32_t tq = (uint32_t)(t0 + tid);
-    const float* lam_r = lam_s + tid * kLamStride;
-#pragma unroll 1
-    for (int c = 0; c < kTile / 32; ++c) {
-      if (c > warp) {
-        put_row32_zero(Kb, tid, c);
+    const float* lam_r = lam_s + r * kLamStride;
+    for (int c = hh; c < kTile / 32; c += 2) {
+      if (c > qt) {
+        put_row32_zero(Kb, r, c);
         continue;
       }
       float sv[32];
       tmem_ld32(tmem + lane_base + c * 32, sv);
+      if (c < qt) {
+        const float wl = lam_r[5 + (32 - __clz((unsigned)(qt ^ c)))];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const int s = c * 32 + k;
-        float v = 0.f;
-        if (s <= tid && tid < n) {
-          const int lvl = fenwick_level(tq, (uint32_t)(t0 + s));
-          v = sv[k] * lam_r[lvl] * __expf(cs - cs_s[s]);
+        for (int k = 0; k < 32; ++k) sv[k] *= wl * __expf(cs - cs_s[c * 32 + k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int s = c * 32 + k;
+          float v = 0.f;
+          if (s <= r && row_live)
+            v = sv[k] * lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * __expf(cs - cs_s[s]);
+          sv[k] = v;
         }
-        sv[k] = v;
       }
-      put_row32_bf16(Kb, tid, c, sv);
+      put_row32_bf16(Kb, r, c, sv);
     }
   }
   fence_proxy_async_smem();
@@ -405,17 +462,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     mma_commit(bar_o);
   }
+  __syncwarp();
   ok = all_ok && mbar_wait(bar_o, 0);
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
-  float o[kD];
+  // this thread's half of the output row: columns [64 hh, 64 hh + 64)
+  float o[kD / 2];
 #pragma unroll
-  for (int q = 0; q < kD; ++q) o[q] = 0.f;
+  for (int q = 0; q < kD / 2; ++q) o[q] = 0.f;
+  const uint32_t col0 = 64u * hh;
   if (all_ok) {
 #pragma unroll
-    for (int c = 0; c < kD / 32; ++c) {
+    for (int c = 0; c < 2; ++c) {
       float v[32];
-      tmem_ld32(tmem + lane_base + 128 + c * 32, v);
+      tmem_ld32(tmem + lane_base + 128 + col0 + c * 32, v);
 #pragma unroll
       for (int q = 0; q < 32; ++q) o[c * 32 + q] = v[q];
     }
@@ -448,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (++seen > 2) break;
     }
   }
+  __syncwarp();
   for (int k = 0; k <= nlev && all_ok; ++k) {
     if (k < nlev) {  // issue level k
       const int bf = k & 1;
@@ -467,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mma_commit(&bar_lvl[bf]);
       }
+      __syncwarp();
     }
     if (k >= 1) {  // finish level k-1 while level k runs
       const int bf = (k - 1) & 1;
@@ -475,13 +537,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       tc_fence_after();
       all_ok = __syncthreads_and(ok);
       if (!all_ok) break;
-      const float r = rs[(k - 1) * kTile + tid];
+      const float wr = rs[(k - 1) * kTile + r];
 #pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float v[32];
-        tmem_ld32(tmem + lane_base + bf * 128 + c * 32, v);
+        tmem_ld32(tmem + lane_base + bf * 128 + col0 + c * 32, v);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) o[c * 32 + q] = fmaf(r, v[q], o[c * 32 + q]);
+        for (int q = 0; q < 32; ++q) o[c * 32 + q] = fmaf(wr, v[q], o[c * 32 + q]);
       }
       tc_fence_before();
       __syncthreads();  // buffer bf (TMEM and shared) is free again
@@ -495,22 +557,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(&tmNode, &bar_node[bf], dst, 0, r0);
         tma_load_2d(&tmNode, &bar_node[bf], dst + kPanel, 64, r0);
       }
+      __syncwarp();
     }
   }
 
   // ---- epilogue
   if (all_ok) {
     if (p.out_f32) {
-      if (tid < n) {
-        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * kD);
+      if (row_live) {
+        float4* dst =
+            reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * kD + col0);
 #pragma unroll
-        for (int q = 0; q < kD / 4; ++q)
+        for (int q = 0; q < kD / 8; ++q)
           dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
       }
     } else {
       // no MMA reads Q any more: stage the bf16 tile there and store it with TMA
 #pragma unroll
-      for (int c = 0; c < kD / 32; ++c) put_row32_bf16(Qb, tid, c, o + c * 32);
+      for (int c = 0; c < 2; ++c) put_row32_bf16(Qb, r, 2 * hh + c, o + c * 32);
       fence_proxy_async_smem();
       __syncthreads();
       if (tid == 0) {
@@ -519,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_store_commit();
         tma_store_wait_read();
       }
+      __syncwarp();
     }
   } else if (tid == 0) {
     atomicOr(&g_tc_error, 1u);
@@ -616,8 +681,8 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
     if ((e = launch_level_scan(a, /*bf16_states=*/true, s)) != cudaSuccess) return e;
     if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   }
-  tc_intra_readout_kernel<<<grid, kThreads, smem_k3(levels), s>>>(tmQ, tmK, tmV, tmNode, tmOut,
-                                                                    p);
+  tc_intra_readout_kernel<<<grid, kThreads3, smem_k3(levels), s>>>(tmQ, tmK, tmV, tmNode,
+                                                                     tmOut, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   return ev ? ev->finish(s) : cudaSuccess;

@@ -9,18 +9,21 @@
 // total of its even sibling,
 //     Tot(m, p) = sum_{i in block p} exp(sum_{i' in block p, i' > i} lg_i') U_i,
 // built bottom-up with Tot(m+1, q) = exp(LG(m, 2q+1)) Tot(m, 2q) + Tot(m, 2q+1).
-// Every thread owns 4 (or, if d_k*d_v is not a multiple of 4, 1) consecutive state elements of one (b, h) and walks the chunks in
-// order with a binary counter (one pending even block per level), so each block total is
-// formed once, in fp32, and every even block is stored under the index c of its first
-// reader chunk, c = (p+1) 2^(m-1).  The state layout inside a chunk is opaque here.
+// A thread owns 8 (bf16) or 4 (fp32) consecutive state elements of one (b, h) (1 if
+// d_k*d_v is not a multiple of 4) and walks chunks in order with a binary counter (one
+// pending even block per level), so each block total is formed once, in fp32, and every
+// even block is stored under the index c of its first reader chunk, c = (p+1) 2^(m-1).
+// Loads run kPrefetch chunks ahead.  The state layout inside a chunk is opaque here.
 #include "ll_internal.cuh"
 
 namespace ll {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kMaxLevels = 40;  // chunk levels of the counter (N < 2^39)
-constexpr int kPrefetch = 4;
+constexpr int kSegs = 16;                 // segments per (b, h), one thread each
+constexpr int kGroups = 8;                // element groups per CTA
+constexpr int kThreads = kSegs * kGroups;
+constexpr int kMaxSegLevels = 32;         // levels inside a segment (seg_len < 2^31)
+constexpr int kPrefetch = 8;
 
 template <int VW>
 struct Vec {
@@ -43,7 +46,16 @@ __device__ __forceinline__ Vec<VW> load_v(const float* p) {
 template <int VW>
 __device__ __forceinline__ Vec<VW> load_v(const __nv_bfloat16* p) {
   Vec<VW> r;
-  if constexpr (VW == 4) {
+  if constexpr (VW == 8) {
+    const uint4 t = __ldcs(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      r.x[2 * k] = f.x;
+      r.x[2 * k + 1] = f.y;
+    }
+  } else if constexpr (VW == 4) {
     const uint2 t = __ldcs(reinterpret_cast<const uint2*>(p));
     const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
     const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
@@ -67,7 +79,15 @@ __device__ __forceinline__ void store_v(float* p, const Vec<VW>& v) {
 
 template <int VW>
 __device__ __forceinline__ void store_v(__nv_bfloat16* p, const Vec<VW>& v) {
-  if constexpr (VW == 4) {
+  if constexpr (VW == 8) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v.x[2 * k], v.x[2 * k + 1]);
+      w[k] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if constexpr (VW == 4) {
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x[0], v.x[1]);
     __nv_bfloat162 hi = __floats2bfloat162_rn(v.x[2], v.x[3]);
     uint2 u;
@@ -80,41 +100,86 @@ __device__ __forceinline__ void store_v(__nv_bfloat16* p, const Vec<VW>& v) {
   }
 }
 
+// One CTA covers kGroups element groups (VW elements each) of one (b, h) with kSegs
+// threads per group: thread (s, g) first walks segment s, an aligned run of seg_len
+// chunks, and stores every block inside it; the complete segments' totals then meet in
+// shared memory, where one thread per group walks them to form the blocks of a segment
+// or longer.  The sequential depth is seg_len + N/seg_len instead of N.
 template <typename StateT, int VW>
-__global__ void __launch_bounds__(kThreads) level_scan_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(kThreads) level_scan_kernel(FwdArgs a, int seg_lc) {
   using NodeT = StateT;
+  __shared__ Vec<VW> seg_tot[kSegs][kGroups];
+  __shared__ float seg_lg[kSegs];
+  const int g = threadIdx.x % kGroups, sg = threadIdx.x / kGroups;
   const int64_t elems = (int64_t)a.dk * a.dv;
-  const int64_t e = VW * ((int64_t)blockIdx.x * kThreads + threadIdx.x);
-  if (e >= elems) return;
+  const int64_t e = VW * ((int64_t)blockIdx.x * kGroups + g);
+  const bool live = e < elems;
   const int64_t bh = (int64_t)blockIdx.z * a.H + blockIdx.y;
   const StateT* U = reinterpret_cast<const StateT*>(a.U) + bh * a.N * elems + e;
   NodeT* nodes = reinterpret_cast<NodeT*>(a.nodes) + bh * a.N * elems + e;
   const float* lg = a.lg + bh * a.N;
-  Vec<VW> stk[kMaxLevels];
-  float stk_lg[kMaxLevels];
-  Vec<VW> pre[kPrefetch];
+  const int64_t seg_len = int64_t(1) << seg_lc;
+  const int64_t i_lo = sg * seg_len;
+  const int64_t i_hi = i_lo + seg_len < (int64_t)a.N ? i_lo + seg_len : (int64_t)a.N;
+
+  // phase 1: blocks of fewer than seg_len chunks, inside segment sg
+  if (live && i_lo < a.N) {
+    Vec<VW> stk[kMaxSegLevels];
+    float stk_lg[kMaxSegLevels];
+    Vec<VW> pre[kPrefetch];
 #pragma unroll
-  for (int u = 0; u < kPrefetch; ++u)
-    if (u < a.N) pre[u] = load_v<VW>(U + (int64_t)u * elems);
-  for (int64_t i0 = 0; i0 < a.N; i0 += kPrefetch) {
+    for (int u = 0; u < kPrefetch; ++u)
+      if (i_lo + u < i_hi) pre[u] = load_v<VW>(U + (i_lo + u) * elems);
+    for (int64_t i0 = i_lo; i0 < i_hi; i0 += kPrefetch) {
 #pragma unroll
-    for (int u = 0; u < kPrefetch; ++u) {
-      const int64_t i = i0 + u;
-      if (i >= a.N) break;
-      Vec<VW> cur = pre[u];
-      if (i + kPrefetch < a.N) pre[u] = load_v<VW>(U + (i + kPrefetch) * elems);
-      float cur_lg = lg[i];
-      int64_t p = i;
-      int m = 1;
-      while (p & 1) {  // odd block: merge with the pending even sibling one level up
-        const float g = expf(cur_lg);
+      for (int u = 0; u < kPrefetch; ++u) {
+        const int64_t i = i0 + u;
+        if (i >= i_hi) break;
+        Vec<VW> cur = pre[u];
+        if (i + kPrefetch < i_hi) pre[u] = load_v<VW>(U + (i + kPrefetch) * elems);
+        float cur_lg = lg[i];
+        int64_t p = i;
+        int m = 1;
+        while ((p & 1) && m <= seg_lc) {  // odd block: merge with its pending even sibling
+          const float gl = expf(cur_lg);
 #pragma unroll
-        for (int k = 0; k < VW; ++k) cur.x[k] = fmaf(g, stk[m - 1].x[k], cur.x[k]);
+          for (int k = 0; k < VW; ++k) cur.x[k] = fmaf(gl, stk[m - 1].x[k], cur.x[k]);
+          cur_lg += stk_lg[m - 1];
+          p >>= 1;
+          ++m;
+        }
+        if (m <= seg_lc) {  // an even block shorter than a segment
+          const int64_t c = (p + 1) << (m - 1);
+          if (c < a.N) store_v<VW>(nodes + c * elems, cur);
+          stk[m - 1] = cur;
+          stk_lg[m - 1] = cur_lg;
+        } else {            // the whole segment: hand it to phase 2
+          seg_tot[sg][g] = cur;
+          if (g == 0) seg_lg[sg] = cur_lg;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // phase 2: blocks of one segment or more, over the complete segments
+  if (live && sg == 0) {
+    const int64_t nfull = a.N >> seg_lc;
+    Vec<VW> stk[kSegs];
+    float stk_lg[kSegs];
+    for (int64_t q = 0; q < nfull; ++q) {
+      Vec<VW> cur = seg_tot[q][g];
+      float cur_lg = seg_lg[q];
+      int64_t p = q;
+      int m = 1;  // level above the segment level
+      while (p & 1) {
+        const float gl = expf(cur_lg);
+#pragma unroll
+        for (int k = 0; k < VW; ++k) cur.x[k] = fmaf(gl, stk[m - 1].x[k], cur.x[k]);
         cur_lg += stk_lg[m - 1];
         p >>= 1;
         ++m;
       }
-      const int64_t c = (p + 1) << (m - 1);
+      const int64_t c = (p + 1) << (seg_lc + m - 1);
       if (c < a.N) store_v<VW>(nodes + c * elems, cur);
       stk[m - 1] = cur;
       stk_lg[m - 1] = cur_lg;
@@ -126,19 +191,21 @@ __global__ void __launch_bounds__(kThreads) level_scan_kernel(FwdArgs a) {
 
 cudaError_t launch_level_scan(const FwdArgs& a, bool bf16_states, cudaStream_t s) {
   const int64_t elems = (int64_t)a.dk * a.dv;
-  if (elems % 4 == 0) {
-    const dim3 grid((unsigned)((elems / 4 + kThreads - 1) / kThreads), a.H, a.B);
-    if (bf16_states)
-      level_scan_kernel<__nv_bfloat16, 4><<<grid, kThreads, 0, s>>>(a);
-    else
-      level_scan_kernel<float, 4><<<grid, kThreads, 0, s>>>(a);
-  } else {
-    const dim3 grid((unsigned)((elems + kThreads - 1) / kThreads), a.H, a.B);
-    if (bf16_states)
-      level_scan_kernel<__nv_bfloat16, 1><<<grid, kThreads, 0, s>>>(a);
-    else
-      level_scan_kernel<float, 1><<<grid, kThreads, 0, s>>>(a);
-  }
+  int seg_lc = 0;  // segments of 2^seg_lc chunks, at most kSegs of them
+  while (((int64_t)kSegs << seg_lc) < a.N) ++seg_lc;
+  auto grid = [&](int vw) {
+    return dim3((unsigned)((elems / vw + kGroups - 1) / kGroups), a.H, a.B);
+  };
+  if (bf16_states && elems % 8 == 0)  // 16-byte loads of 8 bf16
+    level_scan_kernel<__nv_bfloat16, 8><<<grid(8), kThreads, 0, s>>>(a, seg_lc);
+  else if (elems % 4 == 0 && bf16_states)
+    level_scan_kernel<__nv_bfloat16, 4><<<grid(4), kThreads, 0, s>>>(a, seg_lc);
+  else if (elems % 4 == 0)
+    level_scan_kernel<float, 4><<<grid(4), kThreads, 0, s>>>(a, seg_lc);
+  else if (bf16_states)
+    level_scan_kernel<__nv_bfloat16, 1><<<grid(1), kThreads, 0, s>>>(a, seg_lc);
+  else
+    level_scan_kernel<float, 1><<<grid(1), kThreads, 0, s>>>(a, seg_lc);
   return cudaGetLastError();
 }
 
