@@ -593,6 +593,135 @@ __global__ void __launch_bounds__(kThreads3, 2)
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// ------------------------------------------------------------------ level scan (bulk)
+//
+// The level scan of level_scan.cu for bf16 chunk states of d_k = d_v = 128 and at most
+// 256 tiles per (b, h), with all global traffic in two TMA transfers per CTA: one load
+// of the CTA's [N tiles][64 columns] slice of chunk states into shared memory and one
+// store of the [N][64] block states it produces.  The binary counter runs as in
+// level_scan.cu: 16 aligned segments of tiles walked in parallel (8 threads of 8 columns
+// each), then the segment totals combined by one thread per column group.
+
+constexpr int kScanSegs = 16, kScanGroups = 8, kScanCols = 64;
+constexpr int kScanThreads = kScanSegs * kScanGroups;
+constexpr int kScanMaxTiles = 256;
+
+__device__ __forceinline__ void ld_bf16x8(const uint8_t* p, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+    x[2 * k] = f.x;
+    x[2 * k + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ void st_bf16x8(uint8_t* p, const float* x) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                                            pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+    tc_level_scan_kernel(const __grid_constant__ CUtensorMap tmU,
+                         const __grid_constant__ CUtensorMap tmNodes, const float* lg_all,
+                         int N, int seg_lc) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* Ub = smem;                           // [N][64] bf16 chunk states
+  uint8_t* Nb = smem + N * 128;                 // [N][64] bf16 block states (row 0 unused)
+  float* seg_tot = reinterpret_cast<float*>(Nb + N * 128);   // [16][8][8]
+  float* seg_lg = seg_tot + kScanSegs * kScanGroups * 8;     // [16]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(seg_lg + kScanSegs);
+  const int tid = threadIdx.x, g = tid % kScanGroups, sg = tid / kScanGroups;
+  const int col0 = blockIdx.x * kScanCols;
+  const int64_t bh = blockIdx.y;
+  const int row0 = (int)(bh * N);
+  const float* lg = lg_all + bh * N;
+  if (tid == 0) {
+    prefetch_tensormap(&tmU);
+    prefetch_tensormap(&tmNodes);
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();  // the barrier is initialised before anyone waits on it
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)N * 128u);
+    tma_load_2d(&tmU, bar, Ub, col0, row0);
+  }
+  __syncwarp();
+  if (tid < 8) *reinterpret_cast<uint4*>(Nb + tid * 16) = make_uint4(0, 0, 0, 0);
+  const bool ok = __syncthreads_and(mbar_wait(bar, 0));
+  if (ok) {
+    const int seg_len = 1 << seg_lc;
+    const int i_lo = sg * seg_len, i_hi = min(N, i_lo + seg_len);
+    float stk[16][8];       // pending even blocks inside the segment (levels 1..seg_lc)
+    float stk_lg[16];
+    for (int i = i_lo; i < i_hi; ++i) {
+      float cur[8];
+      ld_bf16x8(Ub + i * 128 + g * 16, cur);
+      float cur_lg = lg[i];
+      int p = i, m = 1;
+      while ((p & 1) && m <= seg_lc) {  // odd block: merge with its pending even sibling
+        const float gl = expf(cur_lg);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) cur[k] = fmaf(gl, stk[m - 1][k], cur[k]);
+        cur_lg += stk_lg[m - 1];
+        p >>= 1;
+        ++m;
+      }
+      if (m <= seg_lc) {
+        const int c = (p + 1) << (m - 1);
+        if (c < N) st_bf16x8(Nb + c * 128 + g * 16, cur);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) stk[m - 1][k] = cur[k];
+        stk_lg[m - 1] = cur_lg;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) seg_tot[(sg * kScanGroups + g) * 8 + k] = cur[k];
+        if (g == 0) seg_lg[sg] = cur_lg;
+      }
+    }
+  }
+  __syncthreads();
+  if (ok && sg == 0) {  // blocks of one segment or more
+    const int nfull = N >> seg_lc;
+    float stk[kScanSegs][8];
+    float stk_lg[kScanSegs];
+    for (int q = 0; q < nfull; ++q) {
+      float cur[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) cur[k] = seg_tot[(q * kScanGroups + g) * 8 + k];
+      float cur_lg = seg_lg[q];
+      int p = q, m = 1;
+      while (p & 1) {
+        const float gl = expf(cur_lg);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) cur[k] = fmaf(gl, stk[m - 1][k], cur[k]);
+        cur_lg += stk_lg[m - 1];
+        p >>= 1;
+        ++m;
+      }
+      const int c = (p + 1) << (seg_lc + m - 1);
+      if (c < N) st_bf16x8(Nb + c * 128 + g * 16, cur);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) stk[m - 1][k] = cur[k];
+      stk_lg[m - 1] = cur_lg;
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    if (ok) {
+      tma_store_2d(&tmNodes, Nb, col0, row0);
+      tma_store_commit();
+      tma_store_wait_read();
+    } else {
+      atomicOr(&g_tc_error, 1u);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -637,6 +766,24 @@ bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows][16384] bf16 chunk or block states viewed as rows of one tile's 128 x 128 state,
+// boxes of `box_rows` states x 64 columns, no swizzle.
+bool make_scan_map(CUtensorMap* m, const void* base, int64_t states, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kD * kD, (cuuint64_t)states};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * kD * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kScanCols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t smem_scan(int N) {
+  return (size_t)N * 256 + 4 * (kScanSegs * kScanGroups * 8 + kScanSegs) + 16 + 1024;
+}
+
 constexpr size_t kSmemK1 = 2 * kOperand + 1024 + 256;
 size_t smem_k3(int levels) { return (size_t)K3Smem::kRs + 4 * kTile * levels + 1024; }
 
@@ -678,7 +825,24 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   if (a.N > 1) {
-    if ((e = launch_level_scan(a, /*bf16_states=*/true, s)) != cudaSuccess) return e;
+    if (a.N <= kScanMaxTiles) {  // bulk scan: the whole tile range of a slice in one TMA box
+      CUtensorMap tmUs, tmNs;
+      const int64_t states = (int64_t)a.B * a.H * a.N;
+      if (!make_scan_map(&tmUs, a.U, states, a.N) || !make_scan_map(&tmNs, a.nodes, states, a.N))
+        return cudaErrorInvalidValue;
+      int seg_lc = 0;
+      while ((kScanSegs << seg_lc) < a.N) ++seg_lc;
+      const size_t sms = smem_scan(a.N);
+      if ((e = cudaFuncSetAttribute(tc_level_scan_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms)) !=
+          cudaSuccess)
+        return e;
+      tc_level_scan_kernel<<<dim3(kD * kD / kScanCols, (unsigned)(a.B * a.H)), kScanThreads, sms,
+                             s>>>(tmUs, tmNs, a.lg, a.N, seg_lc);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    } else if ((e = launch_level_scan(a, /*bf16_states=*/true, s)) != cudaSuccess) {
+      return e;
+    }
     if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   }
   tc_intra_readout_kernel<<<grid, kThreads3, smem_k3(levels), s>>>(tmQ, tmK, tmV, tmNode,
