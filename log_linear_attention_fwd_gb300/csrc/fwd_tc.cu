@@ -299,6 +299,31 @@ __global__ void __launch_bounds__(kThreads3, 2)
   const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;  // (b, t, h) of row r
   const int nlev = __popc((unsigned)j);                        // inter-chunk levels read
 
+  // ---- per-row data.  Every global load of the prologue is issued first, before the
+  // TMEM allocation and the tile loads (log a, the intra- and inter-level lambdas, the
+  // tile log decays D_m sums over), so that their latencies overlap; the scans and
+  // exponentials follow.  The two threads of a row split the loads.
+  const float* lgp = p.lg + bh * p.N;
+  const int top = nlev > 0 ? 31 - __clz((unsigned)j) : 0;
+  const int span = nlev > 0 ? j - (1 << top) : 0;  // the longest range j - c_m
+  const bool row_live = r < n;
+  const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
+  float lam_in[kIntraLevels / 2];
+#pragma unroll
+  for (int i = 0; i < kIntraLevels / 2; ++i) {
+    const int l = hh * (kIntraLevels / 2) + i;
+    lam_in[i] = (row_live && l < p.L) ? p.lam[row * p.L + l] : 0.f;
+  }
+  const float lg_first = tid < span ? lgp[j - 1 - tid] : 0.f;
+  {  // raw inter-level lambdas, level-major in smem (weighted below); levels alternate
+    int k = 0;  // between the two threads of a row
+#pragma unroll 4
+    for (int m = 1; m < kMaxChunkLevels; ++m) {
+      if (!((j >> (m - 1)) & 1)) continue;
+      if ((k & 1) == hh) rs[k * kTile + r] = row_live ? p.lam[row * p.L + kTileLc + m] : 0.f;
+      ++k;
+    }
+  }
   if (warp == 0) {
     tmem_alloc(tslot, 256);
     tmem_relinquish();
@@ -325,7 +350,8 @@ __global__ void __launch_bounds__(kThreads3, 2)
     tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, h, t0, b);
     tma_load_4d(&tmV, bar_load, Vb, 0, h, t0, b);
     tma_load_4d(&tmV, bar_load, Vb + kPanel, 64, h, t0, b);
-    // warm L2 with every block state this tile will read
+  }
+  if (tid == 32) {  // another warp warms L2 with every block state this tile will read
     for (int m = 1; m < kMaxChunkLevels; ++m) {
       int64_t c;
       if (!inter_block(j, m, &c)) continue;
@@ -335,31 +361,6 @@ __global__ void __launch_bounds__(kThreads3, 2)
     }
   }
   __syncwarp();
-  // ---- per-row data while the tiles are in flight.  Every global load of this phase is
-  // issued first (log a, the intra- and inter-level lambdas, the tile log decays D_m
-  // sums over) so that their latencies overlap; the scans and exponentials follow.  The
-  // two threads of a row split the loads.
-  const float* lgp = p.lg + bh * p.N;
-  const int top = nlev > 0 ? 31 - __clz((unsigned)j) : 0;
-  const int span = nlev > 0 ? j - (1 << top) : 0;  // the longest range j - c_m
-  const bool row_live = r < n;
-  const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
-  float lam_in[kIntraLevels / 2];
-#pragma unroll
-  for (int i = 0; i < kIntraLevels / 2; ++i) {
-    const int l = hh * (kIntraLevels / 2) + i;
-    lam_in[i] = (row_live && l < p.L) ? p.lam[row * p.L + l] : 0.f;
-  }
-  const float lg_first = tid < span ? lgp[j - 1 - tid] : 0.f;
-  {  // raw inter-level lambdas, level-major in smem (weighted below); levels alternate
-    int k = 0;  // between the two threads of a row
-#pragma unroll 4
-    for (int m = 1; m < kMaxChunkLevels; ++m) {
-      if (!((j >> (m - 1)) & 1)) continue;
-      if ((k & 1) == hh) rs[k * kTile + r] = row_live ? p.lam[row * p.L + kTileLc + m] : 0.f;
-      ++k;
-    }
-  }
   const float cs_scan = block_scan256(la, red);  // threads 0..127 hold row prefixes
   if (hh == 0) cs_s[r] = cs_scan;
 #pragma unroll
