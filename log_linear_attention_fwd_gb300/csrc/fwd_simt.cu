@@ -204,7 +204,7 @@ cudaError_t launch_typed(const FwdArgs& a, cudaStream_t s, StageEvents* ev) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   if (a.N > 1) {
-    if ((e = launch_level_scan(a, /*bf16_states=*/false, s)) != cudaSuccess) return e;
+    if ((e = launch_level_scan(a, s)) != cudaSuccess) return e;
     if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   }
   simt_intra_readout<InT, OutT><<<grid_c, kThreads, sm3, s>>>(a);

@@ -5,10 +5,11 @@
 // and 两阶段计算; page "算力终结者来了！…", section 高效训练算法) with the tile as the chunk:
 //
 //   tc_chunk_state    per tile i: U_i^T = (w ⊙ V)^T K on tcgen05 (w_s = exp(cs_end - cs_s),
-//                     cs = tile-local prefix sums of log a), stored bf16 [d_v][d_k] through a
-//                     TMA store, plus the tile's log decay lg_i.
-//   level_scan        (level_scan.cu) Fenwick block totals of tiles in fp32, stored bf16
-//                     [d_v][d_k] under the index of their first reader tile.
+//                     cs = tile-local prefix sums of log a) into TMEM, and the tile's log
+//                     decay lg_i.  The Fenwick block totals of tiles are merged in the same
+//                     kernel as the tiles finish (fp32 in TMEM; the CTA that completes a
+//                     sibling pair forms the parent) and stored bf16 [d_v][d_k] under the
+//                     index of their first reader tile.
 //   tc_intra_readout  per tile j: S = Q K^T (tcgen05, TMEM); P = S ⊙ exp(cs_t - cs_s) ⊙
 //                     lambda[t, l(t,s)] on the causal half (CUDA cores, bf16 into shared
 //                     memory); O = P V (tcgen05), moved to registers.  Then, for every set
@@ -62,7 +63,11 @@ struct TcParams {
   const float* log_a;
   const float* lam;
   void* out;
-  float* lg;
+  float* lg;         // [B*H][N] log decay of each tile
+  uint8_t* nodes;    // [B*H][N] block states, bf16 [d_v][d_k], slot = first reader tile
+  uint8_t* odd;      // [B*H][N] totals of odd blocks left for their sibling, slot = first tile
+  float* blg;        // [B*H][N] log decays of the blocks left behind, slot = first tile
+  uint32_t* cnt;     // [B*H][N] arrival counters of the sibling pairs, slot = midpoint tile
   int out_f32;
 };
 
@@ -131,25 +136,86 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
     *reinterpret_cast<uint4*>(panel + sw128_offset(r, (c & 1) * 4 + q)) = make_uint4(0, 0, 0, 0);
 }
 
-// ------------------------------------------------------------------ K1: chunk states
+// A held block total: the 16-byte pieces q = it * 128 + tid (it = 0..15) of a row-major
+// [128][128] bf16 matrix, 8 bf16 each, so that every warp moves 512 contiguous bytes per
+// step.  Generic-proxy global accesses, so that another CTA can read the data after a
+// release/acquire on a counter; the loads bypass L1 (the data was written by another SM
+// during this launch).
+constexpr int kPieces = kOperand / 16 / kThreads;  // 16 per thread
 
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void store_pieces(const uint4 (&x)[kPieces], uint8_t* dst, int tid) {
+#pragma unroll
+  for (int it = 0; it < kPieces; ++it) reinterpret_cast<uint4*>(dst)[it * kThreads + tid] = x[it];
+}
+
+// x <- bf16(g * left + right) elementwise, left/right = (x, the sibling's pieces) in the
+// order `x_is_left` gives.  Both CTAs of a pair would compute the same bits.
+__device__ __forceinline__ void merge_pieces(uint4 (&x)[kPieces], const uint8_t* sib, float g,
+                                             bool x_is_left, int tid) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {  // 8 loads in flight per thread, bounded registers
+    uint4 y[kPieces / 2];
+#pragma unroll
+    for (int u = 0; u < kPieces / 2; ++u)
+      y[u] = __ldcg(reinterpret_cast<const uint4*>(sib) + (half * kPieces / 2 + u) * kThreads + tid);
+#pragma unroll
+    for (int u = 0; u < kPieces / 2; ++u) {
+      const int it = half * kPieces / 2 + u;
+      uint32_t a[4] = {x[it].x, x[it].y, x[it].z, x[it].w};
+      const uint32_t c[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a[k]));
+        const float2 fc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c[k]));
+        const float2 l = x_is_left ? fa : fc, r = x_is_left ? fc : fa;
+        a[k] = pack_bf16(fmaf(g, l.x, r.x), fmaf(g, l.y, r.y));
+      }
+      x[it] = make_uint4(a[0], a[1], a[2], a[3]);
+    }
+  }
+}
+
+// Whether the total of block pb at chunk level m (tiles [pb 2^(m-1), (pb+1) 2^(m-1))) is
+// needed: an even block is the block state of its first reader tile (pb+1) 2^(m-1), if
+// that tile exists; an odd block only feeds its parent.
+__device__ __forceinline__ bool block_needed(int m, int64_t pb, int64_t N) {
+  for (; m <= kMaxChunkLevels; ++m, pb >>= 1)
+    if (!(pb & 1)) return ((pb + 1) << (m - 1)) < N;
+  return false;
+}
+
+// ------------------------------------------------------------------ K1: chunk states
+//
+// Per tile i: U_i^T = (w ⊙ V)^T K into TMEM (fp32), then the Fenwick block states.  The
+// block totals Tot(m+1, q) = exp(LG(2q+1)) Tot(m, 2q) + Tot(m, 2q+1) are merged as the
+// tiles finish, without a separate scan and without waiting: each CTA holds the total of
+// one block (first its own tile), stores it as a block state if the block is even (slot
+// = its first reader tile), and counts itself in at the arrival counter of the block's
+// sibling pair (keyed by the pair's midpoint tile, unique per pair).  The first of the two
+// CTAs leaves its total for the other one (the block state of an even block; a scratch
+// slot keyed by its first tile for an odd one, with the block's log decay) and exits; the
+// second reads it, forms the parent and carries on one level up.  Only blocks some block
+// state depends on are formed.  Totals cross CTAs in bf16, the format of the block states
+// themselves, and both CTAs of a pair would compute the same bits.
+
+__global__ void __launch_bounds__(kThreads, 3)
     tc_chunk_state_kernel(const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV,
-                          const __grid_constant__ CUtensorMap tmU, TcParams p) {
+                          const __grid_constant__ CUtensorMap tmV, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* Kb = smem;
-  uint8_t* Vb = smem + kOperand;
+  uint8_t* Kb = smem;                // K, then U_i^T in bf16
+  uint8_t* Vb = smem + kOperand;     // V
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kOperand);  // [0] load, [1] mma
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
   float* red = reinterpret_cast<float*>(tslot + 4);
   float* lg_s = red + 4;
+  uint32_t* flag_s = reinterpret_cast<uint32_t*>(lg_s + 1);  // 2 per chunk level
 
   const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int t0 = i * kTile;
   const int n = min(kTile, p.T - t0);
+  const int64_t bh = (int64_t)b * p.H + h;
 
   if (warp == 0) {
     tmem_alloc(tslot, 128);
@@ -158,7 +224,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
-    prefetch_tensormap(&tmU);
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
     fence_mbar_init();
@@ -167,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  const uint32_t lane = (uint32_t)(warp * 32) << 16;
   if (tid == 0) {
     mbar_arrive_expect_tx(&bars[0], 2 * kOperand);
     tma_load_4d(&tmK, &bars[0], Kb, 0, h, t0, b);
@@ -202,22 +268,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool ok2 = all_ok && mbar_wait(&bars[1], 0);
   tc_fence_after();
   if (__syncthreads_and(ok2)) {
-    // row tid of U^T (d_v index) -> bf16 into Kb (free since the MMA completed) -> TMA store
+    if (tid == 0) p.lg[bh * p.N + i] = lg;
+    // row tid of U^T (d_v index) -> bf16 into Kb (free since the MMA completed), then
+    // re-read in the piece layout
 #pragma unroll 1
     for (int c = 0; c < kD / 32; ++c) {
       float v[32];
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, v);
+      tmem_ld32(tmem + lane + c * 32, v);
       put_row32_bf16(Kb, tid, c, v);
     }
-    fence_proxy_async_smem();
     __syncthreads();
-    if (tid == 0) {
-      const int row0 = (int)((((int64_t)b * p.H + h) * p.N + i) * kD);
-      tma_store_2d(&tmU, Kb, 0, row0);
-      tma_store_2d(&tmU, Kb + kPanel, 64, row0);
-      tma_store_commit();
-      p.lg[((int64_t)b * p.H + h) * p.N + i] = lg;
-      tma_store_wait_read();
+    uint4 x[kPieces];
+#pragma unroll
+    for (int it = 0; it < kPieces; ++it) {
+      const int q = it * kThreads + tid, row = q >> 4, c16 = q & 15;
+      x[it] = *reinterpret_cast<const uint4*>(Kb + (c16 >> 3) * kPanel + sw128_offset(row, c16 & 7));
+    }
+    const int64_t N = p.N;
+    uint8_t* nodes = p.nodes + bh * N * kOperand;
+    uint8_t* odd = p.odd + bh * N * kOperand;
+    float* blg = p.blg + bh * N;
+    uint32_t* cnt = p.cnt + bh * N;
+    float LGb = lg;  // log decay of the held block
+    int64_t pb = i;  // the held block: index pb at chunk level m
+    for (int m = 1; m <= kMaxChunkLevels; ++m, pb >>= 1) {
+      const bool even = !(pb & 1);
+      const int64_t start = pb << (m - 1), end = (pb + 1) << (m - 1);
+      if (even) {
+        if (end >= N) break;  // no reader tile and no sibling
+        store_pieces(x, nodes + end * kOperand, tid);
+      }
+      if (!block_needed(m + 1, pb >> 1, N)) break;
+      // Arrival at the pair (midpoint tile as key).  Publication protocol: every thread's
+      // stores, then a block barrier, then thread 0 fences and counts in (the fence is
+      // cumulative over the barrier); the CTA that finds the count at 1 fences again and
+      // the barrier hands the acquire to every thread before the sibling is read.
+      uint32_t* pair = cnt + (even ? end : start);
+      uint32_t* fl = flag_s + 2 * m;
+      bool second = false;
+      if (!even) {  // a right half often finds its left sibling in already
+        if (tid == 0) fl[0] = ld_acquire_gpu(pair);
+        __syncthreads();
+        second = fl[0] != 0;
+      }
+      if (!second) {
+        if (!even) store_pieces(x, odd + start * kOperand, tid);
+        if (tid == 0) blg[start] = LGb;
+        __syncthreads();
+        if (tid == 0) {
+          __threadfence();
+          fl[1] = atomicAdd(pair, 1u);
+          __threadfence();
+        }
+        __syncthreads();
+        second = fl[1] != 0;
+        if (!second) break;  // the sibling's CTA forms the parent
+      }
+      const int64_t len = int64_t(1) << (m - 1);
+      const float sib_lg = __ldcg(blg + (even ? end : start - len));
+      const float g = expf(even ? sib_lg : LGb);  // decay across the right half
+      merge_pieces(x, even ? odd + end * kOperand : nodes + start * kOperand, g, even, tid);
+      LGb = even ? LGb + sib_lg : sib_lg + LGb;
     }
   } else if (tid == 0) {
     atomicOr(&g_tc_error, 1u);
@@ -594,135 +705,6 @@ __global__ void __launch_bounds__(kThreads3, 2)
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// ------------------------------------------------------------------ level scan (bulk)
-//
-// The level scan of level_scan.cu for bf16 chunk states of d_k = d_v = 128 and at most
-// 256 tiles per (b, h), with all global traffic in two TMA transfers per CTA: one load
-// of the CTA's [N tiles][64 columns] slice of chunk states into shared memory and one
-// store of the [N][64] block states it produces.  The binary counter runs as in
-// level_scan.cu: 16 aligned segments of tiles walked in parallel (8 threads of 8 columns
-// each), then the segment totals combined by one thread per column group.
-
-constexpr int kScanSegs = 16, kScanGroups = 8, kScanCols = 64;
-constexpr int kScanThreads = kScanSegs * kScanGroups;
-constexpr int kScanMaxTiles = 256;
-
-__device__ __forceinline__ void ld_bf16x8(const uint8_t* p, float* x) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-    x[2 * k] = f.x;
-    x[2 * k + 1] = f.y;
-  }
-}
-
-__device__ __forceinline__ void st_bf16x8(uint8_t* p, const float* x) {
-  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                                            pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-}
-
-__global__ void __launch_bounds__(kScanThreads)
-    tc_level_scan_kernel(const __grid_constant__ CUtensorMap tmU,
-                         const __grid_constant__ CUtensorMap tmNodes, const float* lg_all,
-                         int N, int seg_lc) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint8_t* Ub = smem;                           // [N][64] bf16 chunk states
-  uint8_t* Nb = smem + N * 128;                 // [N][64] bf16 block states (row 0 unused)
-  float* seg_tot = reinterpret_cast<float*>(Nb + N * 128);   // [16][8][8]
-  float* seg_lg = seg_tot + kScanSegs * kScanGroups * 8;     // [16]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(seg_lg + kScanSegs);
-  const int tid = threadIdx.x, g = tid % kScanGroups, sg = tid / kScanGroups;
-  const int col0 = blockIdx.x * kScanCols;
-  const int64_t bh = blockIdx.y;
-  const int row0 = (int)(bh * N);
-  const float* lg = lg_all + bh * N;
-  if (tid == 0) {
-    prefetch_tensormap(&tmU);
-    prefetch_tensormap(&tmNodes);
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();  // the barrier is initialised before anyone waits on it
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, (uint32_t)N * 128u);
-    tma_load_2d(&tmU, bar, Ub, col0, row0);
-  }
-  __syncwarp();
-  if (tid < 8) *reinterpret_cast<uint4*>(Nb + tid * 16) = make_uint4(0, 0, 0, 0);
-  const bool ok = __syncthreads_and(mbar_wait(bar, 0));
-  if (ok) {
-    const int seg_len = 1 << seg_lc;
-    const int i_lo = sg * seg_len, i_hi = min(N, i_lo + seg_len);
-    float stk[16][8];       // pending even blocks inside the segment (levels 1..seg_lc)
-    float stk_lg[16];
-    for (int i = i_lo; i < i_hi; ++i) {
-      float cur[8];
-      ld_bf16x8(Ub + i * 128 + g * 16, cur);
-      float cur_lg = lg[i];
-      int p = i, m = 1;
-      while ((p & 1) && m <= seg_lc) {  // odd block: merge with its pending even sibling
-        const float gl = expf(cur_lg);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) cur[k] = fmaf(gl, stk[m - 1][k], cur[k]);
-        cur_lg += stk_lg[m - 1];
-        p >>= 1;
-        ++m;
-      }
-      if (m <= seg_lc) {
-        const int c = (p + 1) << (m - 1);
-        if (c < N) st_bf16x8(Nb + c * 128 + g * 16, cur);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) stk[m - 1][k] = cur[k];
-        stk_lg[m - 1] = cur_lg;
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) seg_tot[(sg * kScanGroups + g) * 8 + k] = cur[k];
-        if (g == 0) seg_lg[sg] = cur_lg;
-      }
-    }
-  }
-  __syncthreads();
-  if (ok && sg == 0) {  // blocks of one segment or more
-    const int nfull = N >> seg_lc;
-    float stk[kScanSegs][8];
-    float stk_lg[kScanSegs];
-    for (int q = 0; q < nfull; ++q) {
-      float cur[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) cur[k] = seg_tot[(q * kScanGroups + g) * 8 + k];
-      float cur_lg = seg_lg[q];
-      int p = q, m = 1;
-      while (p & 1) {
-        const float gl = expf(cur_lg);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) cur[k] = fmaf(gl, stk[m - 1][k], cur[k]);
-        cur_lg += stk_lg[m - 1];
-        p >>= 1;
-        ++m;
-      }
-      const int c = (p + 1) << (seg_lc + m - 1);
-      if (c < N) st_bf16x8(Nb + c * 128 + g * 16, cur);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) stk[m - 1][k] = cur[k];
-      stk_lg[m - 1] = cur_lg;
-    }
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) {
-    if (ok) {
-      tma_store_2d(&tmNodes, Nb, col0, row0);
-      tma_store_commit();
-      tma_store_wait_read();
-    } else {
-      atomicOr(&g_tc_error, 1u);
-    }
-  }
-}
-
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -767,25 +749,7 @@ bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][16384] bf16 chunk or block states viewed as rows of one tile's 128 x 128 state,
-// boxes of `box_rows` states x 64 columns, no swizzle.
-bool make_scan_map(CUtensorMap* m, const void* base, int64_t states, int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kD * kD, (cuuint64_t)states};
-  cuuint64_t strides[1] = {(cuuint64_t)kD * kD * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kScanCols, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-size_t smem_scan(int N) {
-  return (size_t)N * 256 + 4 * (kScanSegs * kScanGroups * 8 + kScanSegs) + 16 + 1024;
-}
-
-constexpr size_t kSmemK1 = 2 * kOperand + 1024 + 256;
+constexpr size_t kSmemK1 = 2 * kOperand + 1024 + 512;
 size_t smem_k3(int levels) { return (size_t)K3Smem::kRs + 4 * kTile * levels + 1024; }
 
 }  // namespace
@@ -796,15 +760,18 @@ bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int /*chunk*/) {
 
 cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev) {
   const int64_t rows = (int64_t)a.B * a.H * a.N * kD;
-  CUtensorMap tmQ, tmK, tmV, tmOut, tmNode, tmU;
+  CUtensorMap tmQ, tmK, tmV, tmOut, tmNode;
   if (!make_tokens_map(&tmQ, a.q, a.B, a.T, a.H) || !make_tokens_map(&tmK, a.k, a.B, a.T, a.H) ||
       !make_tokens_map(&tmV, a.v, a.B, a.T, a.H) ||
-      !make_tokens_map(&tmOut, a.out, a.B, a.T, a.H) || !make_rows_map(&tmNode, a.nodes, rows) ||
-      !make_rows_map(&tmU, a.U, rows))
+      !make_tokens_map(&tmOut, a.out, a.B, a.T, a.H) || !make_rows_map(&tmNode, a.nodes, rows))
     return cudaErrorInvalidValue;
   TcParams p;
   p.B = a.B; p.T = a.T; p.H = a.H; p.L = a.L; p.N = a.N;
   p.log_a = a.log_a; p.lam = a.lam; p.out = a.out; p.lg = a.lg;
+  p.nodes = static_cast<uint8_t*>(a.nodes);
+  p.odd = static_cast<uint8_t*>(a.U);
+  p.blg = a.blg;
+  p.cnt = a.cnt;
   p.out_f32 = out_dtype == LL_F32;
   int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
   while ((int64_t(1) << levels) < a.N) ++levels;
@@ -822,30 +789,13 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   if (attr_err != cudaSuccess) return attr_err;
   const dim3 grid(a.N, a.H, a.B);
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
-  tc_chunk_state_kernel<<<grid, kThreads, kSmemK1, s>>>(tmK, tmV, tmU, p);
+  // the pair arrival counters start at zero in every call
+  if ((e = cudaMemsetAsync(a.cnt, 0, sizeof(uint32_t) * (size_t)a.B * a.H * a.N, s)) !=
+      cudaSuccess)
+    return e;
+  tc_chunk_state_kernel<<<grid, kThreads, kSmemK1, s>>>(tmK, tmV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
-  if (a.N > 1) {
-    if (a.N <= kScanMaxTiles) {  // bulk scan: the whole tile range of a slice in one TMA box
-      CUtensorMap tmUs, tmNs;
-      const int64_t states = (int64_t)a.B * a.H * a.N;
-      if (!make_scan_map(&tmUs, a.U, states, a.N) || !make_scan_map(&tmNs, a.nodes, states, a.N))
-        return cudaErrorInvalidValue;
-      int seg_lc = 0;
-      while ((kScanSegs << seg_lc) < a.N) ++seg_lc;
-      const size_t sms = smem_scan(a.N);
-      if ((e = cudaFuncSetAttribute(tc_level_scan_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms)) !=
-          cudaSuccess)
-        return e;
-      tc_level_scan_kernel<<<dim3(kD * kD / kScanCols, (unsigned)(a.B * a.H)), kScanThreads, sms,
-                             s>>>(tmUs, tmNs, a.lg, a.N, seg_lc);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    } else if ((e = launch_level_scan(a, /*bf16_states=*/true, s)) != cudaSuccess) {
-      return e;
-    }
-    if (ev && (e = ev->record(s)) != cudaSuccess) return e;
-  }
   tc_intra_readout_kernel<<<grid, kThreads3, smem_k3(levels), s>>>(tmQ, tmK, tmV, tmNode,
                                                                      tmOut, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -2,15 +2,14 @@
 // Attention", section 两阶段计算, the worked four-chunk example; page "算力终结者来了！…",
 // section 高效训练算法).
 //
-// Input: per-chunk states U_i (decayed to the chunk's end) and per-chunk log decays lg_i.
-// States are read and written in one storage type (fp32 on the CUDA-core path, bf16 on
-// the tensor-core path); the block totals are always accumulated in fp32.
+// Input: per-chunk fp32 states U_i (decayed to the chunk's end) and per-chunk log decays
+// lg_i.  (The tensor-core path forms its block states inside its chunk-state kernel.)
 // At chunk level m the chunks form aligned blocks of 2^(m-1); each odd block reads the
 // total of its even sibling,
 //     Tot(m, p) = sum_{i in block p} exp(sum_{i' in block p, i' > i} lg_i') U_i,
 // built bottom-up with Tot(m+1, q) = exp(LG(m, 2q+1)) Tot(m, 2q) + Tot(m, 2q+1).
-// A thread owns 8 (bf16) or 4 (fp32) consecutive state elements of one (b, h) (1 if
-// d_k*d_v is not a multiple of 4) and walks chunks in order with a binary counter (one
+// A thread owns 4 consecutive state elements of one (b, h) (1 if d_k*d_v is not a
+// multiple of 4) and walks chunks in order with a binary counter (one
 // pending even block per level), so each block total is formed once, in fp32, and every
 // even block is stored under the index c of its first reader chunk, c = (p+1) 2^(m-1).
 // Loads run kPrefetch chunks ahead.  The state layout inside a chunk is opaque here.
@@ -44,30 +43,6 @@ __device__ __forceinline__ Vec<VW> load_v(const float* p) {
 }
 
 template <int VW>
-__device__ __forceinline__ Vec<VW> load_v(const __nv_bfloat16* p) {
-  Vec<VW> r;
-  if constexpr (VW == 8) {
-    const uint4 t = __ldcs(reinterpret_cast<const uint4*>(p));
-    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-      r.x[2 * k] = f.x;
-      r.x[2 * k + 1] = f.y;
-    }
-  } else if constexpr (VW == 4) {
-    const uint2 t = __ldcs(reinterpret_cast<const uint2*>(p));
-    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
-    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
-    r.x[0] = lo.x; r.x[1] = lo.y; r.x[2] = hi.x; r.x[3] = hi.y;
-  } else {
-#pragma unroll
-    for (int k = 0; k < VW; ++k) r.x[k] = __bfloat162float(p[k]);
-  }
-  return r;
-}
-
-template <int VW>
 __device__ __forceinline__ void store_v(float* p, const Vec<VW>& v) {
   if constexpr (VW == 4) {
     *reinterpret_cast<float4*>(p) = make_float4(v.x[0], v.x[1], v.x[2], v.x[3]);
@@ -77,37 +52,13 @@ __device__ __forceinline__ void store_v(float* p, const Vec<VW>& v) {
   }
 }
 
-template <int VW>
-__device__ __forceinline__ void store_v(__nv_bfloat16* p, const Vec<VW>& v) {
-  if constexpr (VW == 8) {
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(v.x[2 * k], v.x[2 * k + 1]);
-      w[k] = *reinterpret_cast<uint32_t*>(&b);
-    }
-    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-  } else if constexpr (VW == 4) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x[0], v.x[1]);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v.x[2], v.x[3]);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&lo);
-    u.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(p) = u;
-  } else {
-#pragma unroll
-    for (int k = 0; k < VW; ++k) p[k] = __float2bfloat16_rn(v.x[k]);
-  }
-}
-
 // One CTA covers kGroups element groups (VW elements each) of one (b, h) with kSegs
 // threads per group: thread (s, g) first walks segment s, an aligned run of seg_len
 // chunks, and stores every block inside it; the complete segments' totals then meet in
 // shared memory, where one thread per group walks them to form the blocks of a segment
 // or longer.  The sequential depth is seg_len + N/seg_len instead of N.
-template <typename StateT, int VW>
+template <int VW>
 __global__ void __launch_bounds__(kThreads) level_scan_kernel(FwdArgs a, int seg_lc) {
-  using NodeT = StateT;
   __shared__ Vec<VW> seg_tot[kSegs][kGroups];
   __shared__ float seg_lg[kSegs];
   const int g = threadIdx.x % kGroups, sg = threadIdx.x / kGroups;
@@ -115,8 +66,8 @@ __global__ void __launch_bounds__(kThreads) level_scan_kernel(FwdArgs a, int seg
   const int64_t e = VW * ((int64_t)blockIdx.x * kGroups + g);
   const bool live = e < elems;
   const int64_t bh = (int64_t)blockIdx.z * a.H + blockIdx.y;
-  const StateT* U = reinterpret_cast<const StateT*>(a.U) + bh * a.N * elems + e;
-  NodeT* nodes = reinterpret_cast<NodeT*>(a.nodes) + bh * a.N * elems + e;
+  const float* U = reinterpret_cast<const float*>(a.U) + bh * a.N * elems + e;
+  float* nodes = reinterpret_cast<float*>(a.nodes) + bh * a.N * elems + e;
   const float* lg = a.lg + bh * a.N;
   const int64_t seg_len = int64_t(1) << seg_lc;
   const int64_t i_lo = sg * seg_len;
@@ -189,23 +140,17 @@ __global__ void __launch_bounds__(kThreads) level_scan_kernel(FwdArgs a, int seg
 
 }  // namespace
 
-cudaError_t launch_level_scan(const FwdArgs& a, bool bf16_states, cudaStream_t s) {
+cudaError_t launch_level_scan(const FwdArgs& a, cudaStream_t s) {
   const int64_t elems = (int64_t)a.dk * a.dv;
   int seg_lc = 0;  // segments of 2^seg_lc chunks, at most kSegs of them
   while (((int64_t)kSegs << seg_lc) < a.N) ++seg_lc;
   auto grid = [&](int vw) {
     return dim3((unsigned)((elems / vw + kGroups - 1) / kGroups), a.H, a.B);
   };
-  if (bf16_states && elems % 8 == 0)  // 16-byte loads of 8 bf16
-    level_scan_kernel<__nv_bfloat16, 8><<<grid(8), kThreads, 0, s>>>(a, seg_lc);
-  else if (elems % 4 == 0 && bf16_states)
-    level_scan_kernel<__nv_bfloat16, 4><<<grid(4), kThreads, 0, s>>>(a, seg_lc);
-  else if (elems % 4 == 0)
-    level_scan_kernel<float, 4><<<grid(4), kThreads, 0, s>>>(a, seg_lc);
-  else if (bf16_states)
-    level_scan_kernel<__nv_bfloat16, 1><<<grid(1), kThreads, 0, s>>>(a, seg_lc);
+  if (elems % 4 == 0)  // 16-byte loads of 4 fp32
+    level_scan_kernel<4><<<grid(4), kThreads, 0, s>>>(a, seg_lc);
   else
-    level_scan_kernel<float, 1><<<grid(1), kThreads, 0, s>>>(a, seg_lc);
+    level_scan_kernel<1><<<grid(1), kThreads, 0, s>>>(a, seg_lc);
   return cudaGetLastError();
 }
 

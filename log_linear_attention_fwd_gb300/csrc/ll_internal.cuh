@@ -60,14 +60,17 @@ struct FwdArgs {
   int C, lc;  // tile length and log2(tile)
   int N;      // tiles per (b, h)
   // workspace
-  void* U;        // [B*H][N][dk*dv] chunk states (fp32 on CUDA cores, bf16 on tensor cores)
+  void* U;        // [B*H][N][dk*dv] chunk states (fp32, CUDA cores); on the tensor cores
+                  // the totals of odd blocks left for their sibling (bf16)
   void* nodes;    // [B*H][N][dk*dv] Fenwick block states, slot c = first reader chunk
   float* lg;      // [B*H][N] log decay of each whole chunk
+  float* blg;     // [B*H][N] log decays of the blocks left for a sibling (tensor cores)
+  uint32_t* cnt;  // [B*H][N] sibling-pair arrival counters (tensor cores)
 };
 
 // Workspace carving (identical on host for size queries and for launches).
 struct FwdWorkspace {
-  size_t off_U, off_nodes, off_lg, total;
+  size_t off_U, off_nodes, off_lg, off_blg, off_cnt, total;
 };
 FwdWorkspace fwd_workspace_layout(int64_t B, int64_t H, int64_t N, int64_t dk, int64_t dv,
                                   size_t state_elem_bytes);
@@ -95,7 +98,7 @@ struct StageEvents {
 cudaError_t launch_simt_forward(const FwdArgs& a, int in_dtype, int out_dtype, cudaStream_t s,
                                 StageEvents* ev);
 cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev);
-cudaError_t launch_level_scan(const FwdArgs& a, bool bf16_states, cudaStream_t s);
+cudaError_t launch_level_scan(const FwdArgs& a, cudaStream_t s);
 // Reads and clears the tensor-core path's device error word (synchronises the stream).
 cudaError_t tc_take_error(cudaStream_t s, unsigned* flags);
 bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int chunk);

@@ -186,3 +186,36 @@ def test_tc_onehot_lambda_bit_exact(LL, T):
         want = oracle_fwd(x)
         assert np.array_equal(got.double().numpy(), want), lvl
     assert LL.device_error() == 0
+
+
+@pytest.mark.parametrize("T", [40000])
+def test_tc_many_tiles_sampled(LL, T):
+    """A deep block tree (313 tiles, not a power of two): the block states of every level
+    are merged across many CTAs; sampled rows of every head against the oracle."""
+    L = (T - 1).bit_length() + 1
+    cfg = W.FwdConfig("tc_deep", 1, 2, T, 128, 128, 64, L, "bf16", True, "softplus", seed=11)
+    x = W.make_fwd_inputs(cfg)
+    got = run(LL, x, 64, path="tc", out_dtype=torch.float32)
+    assert LL.device_error() == 0
+    rows = _sample_rows(T, 48, 2)
+    want = oracle_fwd(x, rows=rows, heads=[(0, 0), (0, 1)])
+    err = rel_l2(got[:, rows], want[:, rows])
+    print(f"tc T={T}: rel_l2(sampled rows)={err:.3e}")
+    assert err <= TOL_BF16
+
+
+def test_tc_repeated_calls_same_workspace(LL):
+    """The pair counters of the block tree are reset by every call: two calls on one
+    workspace give identical results."""
+    cfg = W.FwdConfig("tc_rep", 1, 2, 3000, 128, 128, 64, 13, "bf16", True, "softplus", seed=5)
+    x = cuda(W.make_fwd_inputs(cfg))
+    ws = torch.empty(LL.fwd_workspace_size(1, cfg.T, cfg.H, 128, 128, 64, 1), device="cuda",
+                     dtype=torch.uint8)
+    outs = []
+    for _ in range(3):
+        o = LL.loglinear_fwd(x["q"], x["k"], x["v"], x["log_a"], x["lam"], 64, path="tc",
+                             workspace=ws)
+        torch.cuda.synchronize()
+        outs.append(o.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    assert LL.device_error() == 0
