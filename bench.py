@@ -270,7 +270,7 @@ def run_ours(args, rank, world, local_rank):
     t_hbm = fbytes / (peaks["hbm"] * 1e9)
     t_tc = fflops / (peaks["bf16"] * 1e12)
     stage_names = {"simt": ["simt_chunk_state", "simt_level_scan", "simt_intra_readout"],
-                   "tc": ["tc_chunk_state", "tc_intra_readout"]}[path][-n_kernels:]
+                   "tc": ["tc_forward"]}[path][-n_kernels:]
     dom = int(np.argmax(stage_mean))
     # achieved numbers for the forward pass as a whole and for its dominant kernel
     roofline_fwd = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
@@ -322,8 +322,8 @@ def stage_bytes(cfg, path, name):
     st = cfg.B * cfg.H * N * cfg.dk * cfg.dv
     node_e = 2 if path == "tc" else 4
     qkv = tok * (2 * cfg.dk + cfg.dv) * e
-    if name == "tc_chunk_state":  # k, v, log a in; the block states out (tree in-kernel)
-        return tok * (cfg.dk + cfg.dv) * e + tok * 4 + st * node_e
+    if name == "tc_forward":  # one kernel: q, k, v, log a, lambda in, out out
+        return qkv + tok * 4 + tok * cfg.L * 4 + tok * cfg.dv * e
     if name.endswith("chunk_state"):
         return tok * (cfg.dk + cfg.dv) * e + tok * 4 + st * 4
     if name.endswith("level_scan"):

@@ -60,17 +60,19 @@ struct FwdArgs {
   int C, lc;  // tile length and log2(tile)
   int N;      // tiles per (b, h)
   // workspace
-  void* U;        // [B*H][N][dk*dv] chunk states (fp32, CUDA cores); on the tensor cores
-                  // the totals of odd blocks left for their sibling (bf16)
+  void* U;        // [B*H][N][dk*dv] chunk states (fp32 on CUDA cores, bf16 on tensor cores)
   void* nodes;    // [B*H][N][dk*dv] Fenwick block states, slot c = first reader chunk
   float* lg;      // [B*H][N] log decay of each whole chunk
-  float* blg;     // [B*H][N] log decays of the blocks left for a sibling (tensor cores)
-  uint32_t* cnt;  // [B*H][N] sibling-pair arrival counters (tensor cores)
+  // tensor cores only (block states published between CTAs of one launch):
+  float* nlg;     // [B*H][N] log decay of the block in each even block-state slot
+  uint32_t* rdy_u;  // [B*H][N] ready flags of U; followed in memory by
+  uint32_t* rdy_n;  // [B*H][N] ready flags of the block states, and by
+  uint32_t* tick;   // one tile ticket counter (the three are zeroed together)
 };
 
 // Workspace carving (identical on host for size queries and for launches).
 struct FwdWorkspace {
-  size_t off_U, off_nodes, off_lg, off_blg, off_cnt, total;
+  size_t off_U, off_nodes, off_lg, off_nlg, off_rdy_u, off_rdy_n, off_tick, total;
 };
 FwdWorkspace fwd_workspace_layout(int64_t B, int64_t H, int64_t N, int64_t dk, int64_t dv,
                                   size_t state_elem_bytes);

@@ -17,9 +17,12 @@ FwdWorkspace fwd_workspace_layout(int64_t B, int64_t H, int64_t N, int64_t dk, i
   w.off_U = 0;
   w.off_nodes = align_up(w.off_U + states * state_elem_bytes, 256);
   w.off_lg = align_up(w.off_nodes + states * state_elem_bytes, 256);
-  w.off_blg = align_up(w.off_lg + (size_t)(B * H * N) * sizeof(float), 256);
-  w.off_cnt = align_up(w.off_blg + (size_t)(B * H * N) * sizeof(float), 256);
-  w.total = align_up(w.off_cnt + (size_t)(B * H * N) * sizeof(uint32_t), 256);
+  const size_t tiles = (size_t)(B * H * N);
+  w.off_nlg = align_up(w.off_lg + tiles * sizeof(float), 256);
+  w.off_rdy_u = align_up(w.off_nlg + tiles * sizeof(float), 256);
+  w.off_rdy_n = w.off_rdy_u + tiles * sizeof(uint32_t);  // contiguous: zeroed by one memset
+  w.off_tick = w.off_rdy_n + tiles * sizeof(uint32_t);
+  w.total = align_up(w.off_tick + sizeof(uint32_t), 256);
   return w;
 }
 
@@ -177,8 +180,10 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* lo
   a.U = ws + w.off_U;
   a.nodes = ws + w.off_nodes;
   a.lg = reinterpret_cast<float*>(ws + w.off_lg);
-  a.blg = reinterpret_cast<float*>(ws + w.off_blg);
-  a.cnt = reinterpret_cast<uint32_t*>(ws + w.off_cnt);
+  a.nlg = reinterpret_cast<float*>(ws + w.off_nlg);
+  a.rdy_u = reinterpret_cast<uint32_t*>(ws + w.off_rdy_u);
+  a.rdy_n = reinterpret_cast<uint32_t*>(ws + w.off_rdy_n);
+  a.tick = reinterpret_cast<uint32_t*>(ws + w.off_tick);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = p == LL_PATH_TC ? launch_tc_forward(a, out_dtype, s, ev)
                                         : launch_simt_forward(a, in_dtype, out_dtype, s, ev);

@@ -180,6 +180,40 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   return v;
 }
 
+// Release store of a flag.  After a block barrier, thread 0's release also covers the
+// stores of every thread of the block (release is cumulative).
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *flag is non-zero, with acquire semantics.  Returns false if that takes
+// longer than kWaitLimitNs (the caller records the error and carries on).
+__device__ __forceinline__ bool wait_flag_acquire(const uint32_t* flag) {
+  if (ld_acquire_gpu(flag) != 0) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(100);
+    if (ld_acquire_gpu(flag) != 0) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---------------------------------------------------------------- cp.async (16 bytes)
+
+// Global -> shared, cached in L2 only.  Commit the issued copies as a group and wait for
+// them with cp_async_wait_all(); a tcgen05.mma that reads the data needs
+// fence_proxy_async_smem() and a block barrier after that.
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- MMA
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D, dense.
