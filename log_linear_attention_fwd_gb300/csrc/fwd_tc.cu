@@ -102,25 +102,29 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
 //      128..255 (the tile's chunk state, d_v x d_k).
 //   4. P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t,s)] on the causal half, bf16 into the
 //      K buffer once the state MMA is done with it; O = P V into columns 0..127.
-//   5. While P V runs: U_j is published; for even j the CTA forms the block state of
-//      slot j (below) and publishes it.
-//   6. For every set bit m-1 of j, in increasing m: wait for the block state of slot c_m,
-//      copy it into shared memory, MMA Q Tot into one of two TMEM buffers, and add the
-//      previous level's product to O with the row weights lambda[t, 7+m] exp(cs_t + D_m).
-//      D_m, the log decay from the block's end to the tile's start, is the sum of the
-//      log decays of the lower levels' blocks, which their producers store next to them.
+//   5. U_j is published (staged bf16 in the K buffer, stored coalesced); for odd j the
+//      CTA then forms the block state of slot j+1 (below) and publishes it.
+//   6. For every set bit m-1 of j, in increasing m: the block state of slot c_m by TMA
+//      into shared memory (two buffers), MMA Q Tot into one of two TMEM buffers, and the
+//      previous level's product added to O with the row weights
+//      lambda[t, 7+m] exp(cs_t + D_m).  D_m, the log decay from the block's end to the
+//      tile's start, is the sum of the log decays of the lower levels' blocks, which
+//      their producers store next to them.  All block states are warmed in L2 at start.
 //   7. O to bf16 through a TMA store, or fp32 stores.
 //
 // Block states.  Slot c holds the decayed total of the 2^z tiles before c, z = ctz(c):
-// for odd c that is U_{c-1} itself; for even c it is formed by tile c from
+// for odd c that is U_{c-1} itself; for even c it is formed by tile c-1 from
 //     [c - 2^z, c) = [c - 2^z, c - 2^(z-1)) + ... + [c - 4, c - 2) + [c - 2, c - 1) + [c - 1, c)
-// whose parts are the block states of slots c - 2^(k-1) (k = z..1; slot c - 1 is odd and
-// holds U_{c-2}) and U_{c-1}: Tot = sum_k exp(LG of the parts to its right) part_k, in
-// fp32, rounded once to bf16.  All the parts come from tiles that started earlier and
-// publish them early, so there is no chain of merges.  Publication: every thread's
-// stores, a block barrier, then thread 0 raises the ready flag with a release store; a
-// reader's thread 0 acquires the flag, and a block barrier hands that on to every
-// thread.
+// whose parts are the block states of slots c - 2^(k-1) (k = z..2), U_{c-2} (slot c-1)
+// and U_{c-1}, tile c-1's own state: Tot = sum_k exp(LG of the parts to its right)
+// part_k, in fp32, rounded once to bf16.  All the parts come from tiles that started
+// earlier and publish them early, so there is no chain of merges, and a tile publishes
+// what it forms before it waits for the block states it reads.
+//
+// Publication: every thread's generic stores, a block barrier, then thread 0 raises the
+// ready flag with a release store.  Readers: one thread acquires the flag; generic loads
+// by the others follow a block barrier; a TMA load is issued by the acquiring thread
+// itself after a global proxy fence.
 
 constexpr int kThreadsF = 256;
 
@@ -143,8 +147,8 @@ __device__ __forceinline__ float block_scan256(float x, float* red) {
 struct FSmem {
   // byte offsets from the 1024-aligned base
   static constexpr int kQ = 0, kK = kOperand, kV = 2 * kOperand;
-  static constexpr int kBars = 3 * kOperand;                   // 6 mbarriers
-  static constexpr int kTslot = kBars + 6 * 8;
+  static constexpr int kBars = 3 * kOperand;                   // 8 mbarriers
+  static constexpr int kTslot = kBars + 8 * 8;
   static constexpr int kInt = kTslot + 16;                     // ticket: 4 u32
   static constexpr int kRed = kInt + 16;                       // 8 floats
   static constexpr int kLg = kRed + 32;                        // 4 floats
@@ -183,21 +187,13 @@ __device__ __forceinline__ uint32_t piece_offset(int q) {
   return (uint32_t)((c16 >> 3) * kPanel) + sw128_offset(row, c16 & 7);
 }
 
-// Copies a row-major [128][128] bf16 block state into a swizzled K-major tile (two
-// 64-column panels), 8 pieces of 16 bytes per thread, coalesced on the global side.
-__device__ __forceinline__ void cp_async_state(uint8_t* buf, const uint8_t* src, int tid) {
-#pragma unroll
-  for (int it = 0; it < kStatePieces; ++it) {
-    const int q = it * kThreadsF + tid;
-    cp_async_16(buf + piece_offset(q), src + q * 16);
-  }
-}
-
 __global__ void __launch_bounds__(kThreadsF, 2)
     tc_forward_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV,
-                      const __grid_constant__ CUtensorMap tmOut, TcParams p) {
+                      const __grid_constant__ CUtensorMap tmOut,
+                      const __grid_constant__ CUtensorMap tmU,
+                      const __grid_constant__ CUtensorMap tmNode, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* Qb = smem + FSmem::kQ;
@@ -208,7 +204,8 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint64_t* bar_s = &bars[1];
   uint64_t* bar_u = &bars[2];
   uint64_t* bar_o = &bars[3];
-  uint64_t* bar_lvl = &bars[4];      // [2]
+  uint64_t* bar_lvl = &bars[4];      // [2]: level MMAs
+  uint64_t* bar_node = &bars[6];     // [2]: block-state loads
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + FSmem::kTslot);
   uint32_t* ints = reinterpret_cast<uint32_t*>(smem + FSmem::kInt);  // [0] ticket
   float* red = reinterpret_cast<float*>(smem + FSmem::kRed);
@@ -234,7 +231,9 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmOut);
-    for (int q = 0; q < 6; ++q) mbar_init(&bars[q], 1);
+    prefetch_tensormap(&tmU);
+    prefetch_tensormap(&tmNode);
+    for (int q = 0; q < 8; ++q) mbar_init(&bars[q], 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -261,6 +260,14 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, h, t0, b);
     tma_load_4d(&tmV, bar_load, Vb, 0, h, t0, b);
     tma_load_4d(&tmV, bar_load, Vb + kPanel, 64, h, t0, b);
+  }
+  if (tid == 32) {  // warm L2 with the block states the levels will read
+    for (int m = 1; m < kMaxChunkLevels; ++m) {
+      if (!((j >> (m - 1)) & 1)) continue;
+      const int64_t c = ((int64_t)j >> (m - 1)) << (m - 1);
+      prefetch_l2_bulk((c & 1) ? p.U + (bh * N + c - 1) * kOperand : p.nodes + (bh * N + c) * kOperand,
+                       kOperand);
+    }
   }
   __syncwarp();
 
@@ -385,9 +392,9 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   __syncwarp();
 
   // ---- O = P V is done: publish the tile's state U_j (staged bf16 in Kb, which P no
-  // longer needs, then stored coalesced), and for even j form the block state of slot j
-  // (below), straight into Vb for level 0 and out to its slot.  Published states are
-  // row-major [d_v][d_k] bf16; thread tid moves the 16-byte pieces q = it * 256 + tid.
+  // longer needs, then stored coalesced), and for odd j form the block state of slot
+  // j+1 (below) and publish it.  Published states are row-major [d_v][d_k] bf16; thread
+  // tid moves the 16-byte pieces q = it * 256 + tid.
   ok = all_ok && mbar_wait(bar_o, 0);
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
@@ -397,9 +404,6 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   float* nlg = p.nlg + bh * N;
   uint32_t* rdy_u = p.rdy_u + bh * N;
   uint32_t* rdy_n = p.rdy_n + bh * N;
-  const int zj = j > 0 ? __ffs(j) - 1 : 0;  // trailing zeros of j
-  const bool own_level = j > 0 && !(j & 1);
-  float own_lg = 0.f;                       // log decay of the block in slot j (j even)
 #pragma unroll
   for (int c = 0; c < 2; ++c) {  // U^T row r, columns [64 hh, 64 hh + 64) -> Kb
     float v[32];
@@ -407,36 +411,39 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     put_row32_bf16(Kb, r, 2 * hh + c, v);
   }
   __syncthreads();
+  const bool forms = (j & 1) && j + 1 < N;  // odd j forms the block state of slot j+1
+  float acc[8 * kStatePieces];              // that sum, fp32, in this thread's pieces
 #pragma unroll
   for (int it = 0; it < kStatePieces; ++it) {
     const int q = it * kThreadsF + tid;
-    reinterpret_cast<uint4*>(const_cast<uint8_t*>(Ug) + (int64_t)j * kOperand)[q] =
-        *reinterpret_cast<const uint4*>(Kb + piece_offset(q));
+    const uint4 w = *reinterpret_cast<const uint4*>(Kb + piece_offset(q));
+    reinterpret_cast<uint4*>(const_cast<uint8_t*>(Ug) + (int64_t)j * kOperand)[q] = w;
+    const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+      acc[8 * it + 2 * e] = f.x;
+      acc[8 * it + 2 * e + 1] = f.y;
+    }
   }
   if (tid == 0) p.lgu[bh * N + j] = lg;
   __syncthreads();
   if (tid == 0) st_release_gpu(&rdy_u[j], 1u);
-  if (own_level) {
-    // slot j holds [j - 2^z, j) = the block states of slots j - 2^(k-1), k = z..1 (an odd
-    // slot c holds U_{c-1}), then U_{j-1}; summed right to left with the decay across
-    // what lies to the right, in fp32, rounded once to bf16
-    bool got = true;
-    if (tid == 0) {
-      got = wait_flag_acquire(&rdy_u[j - 1]) && wait_flag_acquire(&rdy_u[j - 2]);
-      for (int k = 2; k <= zj && got; ++k) got = wait_flag_acquire(&rdy_n[j - (1 << (k - 1))]);
-    }
-    got = __syncthreads_and(got);
-    if (!got && tid == 0) atomicOr(&g_tc_error, 2u);
-    float acc[8 * kStatePieces];
-#pragma unroll
-    for (int q = 0; q < 8 * kStatePieces; ++q) acc[q] = 0.f;
-    float G = 0.f;  // log decay of what has been summed so far
-    for (int k = 0; k <= zj; ++k) {  // k = 0: U_{j-1}; k >= 1: slot j - 2^(k-1)
-      const int c = k == 0 ? j : j - (1 << (k - 1));
-      const bool is_u = (c & 1) != 0 || k == 0;
+  if (forms) {
+    // Slot c = j+1 holds [c - 2^z, c), z = ctz(c): the block states of slots c - 2^(k-1)
+    // (k = z..2), then U_{j-1}, then U_j; summed right to left, each weighted by the
+    // decay across what lies to its right, in fp32, rounded once to bf16.
+    const int c = j + 1, zc = __ffs(c) - 1;
+    bool fl = true;
+    if (tid < zc)  // thread 0: U_{j-1}; thread t >= 1: slot c - 2^t
+      fl = wait_flag_acquire(tid == 0 ? &rdy_u[j - 1] : &rdy_n[c - (1 << tid)]);
+    if (!__syncthreads_and(fl) && tid == 0) atomicOr(&g_tc_error, 2u);
+    float G = lg;  // log decay of what has been summed so far
+    for (int k = 1; k <= zc; ++k) {  // k = 1: U_{j-1}; k >= 2: slot c - 2^(k-1)
+      const int cs_k = c - (1 << (k - 1));
       const uint4* src = reinterpret_cast<const uint4*>(
-          is_u ? Ug + (int64_t)(c - 1) * kOperand : nodes + (int64_t)c * kOperand);
-      const float L = __ldcg(is_u ? &lgu[c - 1] : &nlg[c]);
+          k == 1 ? Ug + (int64_t)(j - 1) * kOperand : nodes + (int64_t)cs_k * kOperand);
+      const float L = __ldcg(k == 1 ? &lgu[j - 1] : &nlg[cs_k]);
       const float g = __expf(G);
       uint4 y[kStatePieces];
 #pragma unroll
@@ -453,21 +460,52 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       }
       G += L;
     }
-    own_lg = G;
 #pragma unroll
-    for (int it = 0; it < kStatePieces; ++it) {
-      const int q = it * kThreadsF + tid;
-      const uint4 w = make_uint4(pack_bf16(acc[8 * it], acc[8 * it + 1]),
-                                 pack_bf16(acc[8 * it + 2], acc[8 * it + 3]),
-                                 pack_bf16(acc[8 * it + 4], acc[8 * it + 5]),
-                                 pack_bf16(acc[8 * it + 6], acc[8 * it + 7]));
-      reinterpret_cast<uint4*>(nodes + (int64_t)j * kOperand)[q] = w;
-      if (all_ok) *reinterpret_cast<uint4*>(Vb + piece_offset(q)) = w;
-    }
-    if (tid == 0) nlg[j] = G;
+    for (int it = 0; it < kStatePieces; ++it)
+      reinterpret_cast<uint4*>(nodes + (int64_t)c * kOperand)[it * kThreadsF + tid] =
+          make_uint4(pack_bf16(acc[8 * it], acc[8 * it + 1]), pack_bf16(acc[8 * it + 2], acc[8 * it + 3]),
+                     pack_bf16(acc[8 * it + 4], acc[8 * it + 5]),
+                     pack_bf16(acc[8 * it + 6], acc[8 * it + 7]));
+    if (tid == 0) nlg[c] = G;
     __syncthreads();
-    if (tid == 0) st_release_gpu(&rdy_n[j], 1u);
+    if (tid == 0) st_release_gpu(&rdy_n[c], 1u);
   }
+
+  // ---- the levels' block states: thread k acquires level k's ready flag now and later
+  // issues its TMA load itself (after a proxy fence), so the acquire and the async-proxy
+  // read are ordered in one thread.  The block state of slot c is U_{c-1} for odd c.
+  int my_c = 0;  // thread k < nlev: the slot of level k
+  {
+    bool fl = true;
+    if (tid < nlev) {
+      int m = 0;
+      for (int seen = -1; seen < tid;) {
+        ++m;
+        if ((j >> (m - 1)) & 1) ++seen;
+      }
+      my_c = (j >> (m - 1)) << (m - 1);
+      const bool is_u = (my_c & 1) != 0;
+      fl = wait_flag_acquire(is_u ? &rdy_u[my_c - 1] : &rdy_n[my_c]);
+      nl_s[tid] = fl ? __ldcg(is_u ? &lgu[my_c - 1] : &nlg[my_c]) : 0.f;
+      fence_proxy_async_global();
+    }
+    if (!__syncthreads_and(fl) && tid == 0) atomicOr(&g_tc_error, 2u);
+  }
+  auto fetch = [&](int k) {  // thread k: TMA of level k's block state into (k odd ? Kb : Vb)
+    if (tid == k) {
+      uint8_t* dst = (k & 1) ? Kb : Vb;
+      const bool is_u = (my_c & 1) != 0;
+      const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
+      mbar_arrive_expect_tx(&bar_node[k & 1], kOperand);
+      tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[k & 1], dst, 0, row0);
+      tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[k & 1], dst + kPanel, 64, row0);
+    }
+  };
+  if (all_ok) {  // Kb (U staging) and Vb are free
+    if (nlev > 0) fetch(0);
+    if (nlev > 1) fetch(1);
+  }
+  __syncwarp();
 
   // ---- O from TMEM into registers: this thread's half row, columns [64 hh, 64 hh + 64)
   float o[kD / 2];
@@ -483,48 +521,21 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       for (int q = 0; q < 32; ++q) o[c * 32 + q] = v[q];
     }
   }
-  fence_proxy_async_smem();
   tc_fence_before();
-  __syncthreads();  // TMEM is free; Vb holds level 0 for even j, Kb is free
+  __syncthreads();  // TMEM is free
 
   // ---- inter-chunk levels.  Level k (the k-th set bit of j, from the lowest) uses
-  // shared buffer (k odd ? Kb : Vb) and TMEM columns [128 (k&1), +128); bar_lvl[k&1]
-  // signals its MMA.  Block state k+1 is fetched once level k's MMA is issued and
-  // level k-1 has been added to O, so one copy is outstanding at each MMA issue.  The
-  // block state of slot c is U_{c-1} for odd c, else the one tile c formed.
-  int m_next = 1;  // scan position of the next set bit of j
-  auto fetch = [&](int k) {
-    while (!((j >> (m_next - 1)) & 1)) ++m_next;
-    const int c = (j >> (m_next - 1)) << (m_next - 1);
-    ++m_next;
-    if (k == 0 && own_level) {  // already in Vb
-      if (tid == 0) nl_s[0] = own_lg;
-      __syncthreads();
-      return true;
-    }
-    const bool is_u = (c & 1) != 0;
-    bool got = true;
-    if (tid == 0) {
-      got = wait_flag_acquire(is_u ? &rdy_u[c - 1] : &rdy_n[c]);
-      nl_s[k] = got ? __ldcg(is_u ? &lgu[c - 1] : &nlg[c]) : 0.f;
-    }
-    got = __syncthreads_and(got);  // thread 0's acquire now covers every thread's reads
-    if (got)
-      cp_async_state((k & 1) ? Kb : Vb,
-                     is_u ? Ug + (int64_t)(c - 1) * kOperand : nodes + (int64_t)c * kOperand, tid);
-    cp_async_commit();
-    return got;
-  };
-  uint32_t lvl_ph[2] = {0, 0};
+  // shared buffer (k odd ? Kb : Vb) and TMEM columns [128 (k&1), +128); bar_node[k&1]
+  // signals its block state, bar_lvl[k&1] its MMA.  The load of level k+1 starts once
+  // level k-1 has been added to O (levels 0 and 1 were started above).
+  uint32_t lvl_ph[2] = {0, 0}, node_ph[2] = {0, 0};
   float D = 0.f;  // log decay from block k's end to the tile's start
-  bool fetched = nlev > 0 && all_ok ? fetch(0) : true;
   for (int k = 0; k <= nlev && all_ok; ++k) {
     if (k < nlev) {  // issue level k
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (!fetched && tid == 0) atomicOr(&g_tc_error, 2u);
+      ok = mbar_wait(&bar_node[k & 1], node_ph[k & 1]);
+      node_ph[k & 1] ^= 1;
+      all_ok = __syncthreads_and(ok);
+      if (!all_ok) break;
       if (tid == 0) {
         tc_fence_after();
         constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
@@ -557,8 +568,9 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       }
       tc_fence_before();
       __syncthreads();  // buffer bf (TMEM and shared) is free again
+      if (k + 1 < nlev) fetch(k + 1);
+      __syncwarp();
     }
-    if (k + 1 < nlev) fetched = fetch(k + 1);  // into the buffer level k-1 used
   }
 
   // ---- epilogue
@@ -588,7 +600,6 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   } else if (tid == 0) {
     atomicOr(&g_tc_error, 1u);
   }
-  cp_async_wait_all();  // no copy may land after the CTA is gone (error paths)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 256);
@@ -625,6 +636,20 @@ bool make_tokens_map(CUtensorMap* m, const void* base, int B, int T, int H) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows][128] bf16 matrices (published tile and block states), boxes of 128 rows x 64
+// columns with the 128-byte swizzle.
+bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTile};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int /*chunk*/) {
@@ -632,9 +657,12 @@ bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int /*chunk*/) {
 }
 
 cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev) {
-  CUtensorMap tmQ, tmK, tmV, tmOut;
+  const int64_t rows = (int64_t)a.B * a.H * a.N * kD;  // TMA row coordinates are int32
+  if (rows > INT32_MAX) return cudaErrorInvalidValue;
+  CUtensorMap tmQ, tmK, tmV, tmOut, tmU, tmNode;
   if (!make_tokens_map(&tmQ, a.q, a.B, a.T, a.H) || !make_tokens_map(&tmK, a.k, a.B, a.T, a.H) ||
-      !make_tokens_map(&tmV, a.v, a.B, a.T, a.H) || !make_tokens_map(&tmOut, a.out, a.B, a.T, a.H))
+      !make_tokens_map(&tmV, a.v, a.B, a.T, a.H) || !make_tokens_map(&tmOut, a.out, a.B, a.T, a.H) ||
+      !make_rows_map(&tmU, a.U, rows) || !make_rows_map(&tmNode, a.nodes, rows))
     return cudaErrorInvalidValue;
   TcParams p;
   p.B = a.B; p.T = a.T; p.H = a.H; p.L = a.L; p.N = a.N;
@@ -664,7 +692,7 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
       cudaSuccess)
     return e;
   tc_forward_kernel<<<dim3((unsigned)tiles), kThreadsF, smem_fused(levels), s>>>(tmQ, tmK, tmV,
-                                                                               tmOut, p);
+                                                                               tmOut, tmU, tmNode, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   return ev ? ev->finish(s) : cudaSuccess;
