@@ -97,13 +97,14 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
 // done, and they publish what others wait for before they wait on anything themselves.
 //
 //   1. Q, K, V by TMA; per-row log a and lambda; cs = tile-local prefix sums of log a.
-//   2. S = Q K^T (tcgen05) into TMEM columns 0..127.
+//   2. S = Q K^T (tcgen05) into TMEM columns 0..127, issued as soon as Q and K land.
 //   3. K rows scaled in place by w_s = exp(lg - cs_s); U^T = V^T (w ⊙ K) into columns
 //      128..255 (the tile's chunk state, d_v x d_k).
-//   4. P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t,s)] on the causal half, bf16 into the
-//      K buffer once the state MMA is done with it; O = P V into columns 0..127.
-//   5. U_j is published (staged bf16 in the K buffer, stored coalesced); for odd j the
-//      CTA then forms the block state of slot j+1 (below) and publishes it.
+//   4. (after 5) P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t,s)] on the causal half, bf16
+//      into the K buffer; O = P V into columns 0..127.
+//   5. Right after the state MMA (before P): U_j is published (staged bf16 in the Q
+//      buffer, stored coalesced); for odd j the CTA then forms the block state of slot
+//      j+1 (below) and publishes it; Q is loaded again by TMA for the levels.
 //   6. For every set bit m-1 of j, in increasing m: the block state of slot c_m by TMA
 //      into shared memory (two buffers), MMA Q Tot into one of two TMEM buffers, and the
 //      previous level's product added to O with the row weights
@@ -147,8 +148,8 @@ __device__ __forceinline__ float block_scan256(float x, float* red) {
 struct FSmem {
   // byte offsets from the 1024-aligned base
   static constexpr int kQ = 0, kK = kOperand, kV = 2 * kOperand;
-  static constexpr int kBars = 3 * kOperand;                   // 8 mbarriers
-  static constexpr int kTslot = kBars + 8 * 8;
+  static constexpr int kBars = 3 * kOperand;                   // 9 mbarriers
+  static constexpr int kTslot = kBars + 10 * 8;
   static constexpr int kInt = kTslot + 16;                     // ticket: 4 u32
   static constexpr int kRed = kInt + 16;                       // 8 floats
   static constexpr int kLg = kRed + 32;                        // 4 floats
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
                       const __grid_constant__ CUtensorMap tmNode, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* Qb = smem + FSmem::kQ;
+  uint8_t* Qb = smem + FSmem::kQ;    // Q, then U^T in bf16, then Q again, then the output
   uint8_t* Kb = smem + FSmem::kK;    // K, then w ⊙ K, then P, then block states
   uint8_t* Vb = smem + FSmem::kV;    // V, then block states
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FSmem::kBars);
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint64_t* bar_o = &bars[3];
   uint64_t* bar_lvl = &bars[4];      // [2]: level MMAs
   uint64_t* bar_node = &bars[6];     // [2]: block-state loads
+  uint64_t* bar_q = &bars[8];        // Q loaded again for the levels
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + FSmem::kTslot);
   uint32_t* ints = reinterpret_cast<uint32_t*>(smem + FSmem::kInt);  // [0] ticket
   float* red = reinterpret_cast<float*>(smem + FSmem::kRed);
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     prefetch_tensormap(&tmOut);
     prefetch_tensormap(&tmU);
     prefetch_tensormap(&tmNode);
-    for (int q = 0; q < 8; ++q) mbar_init(&bars[q], 1);
+    for (int q = 0; q < 9; ++q) mbar_init(&bars[q], 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;  // (b, t, h) of row r
   const int nlev = __popc((unsigned)j);                        // inter-chunk levels read
   const bool row_live = r < n;
+  bool landed = true;  // thread 0: Q, K and V arrived
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_load, 3 * kOperand);
     tma_load_4d(&tmQ, bar_load, Qb, 0, h, t0, b);
@@ -289,6 +292,21 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       ++k;
     }
   }
+  if (tid == 0) {  // S = Q K^T as soon as the tiles land, before the scan needs log a
+    landed = mbar_wait(bar_load, 0);
+    if (landed) {
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+      const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+        mma_bf16(tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                 idesc, kk > 0);
+      }
+      mma_commit(bar_s);
+    }
+  }
   const float cs_scan = block_scan256(la, red);  // threads 0..127 hold row prefixes
   if (hh == 0) cs_s[r] = cs_scan;
   if (tid == kTile - 1) lg_s[0] = cs_scan;       // padding rows add 0: the tile's log decay
@@ -299,23 +317,9 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   const float cs = cs_s[r];
   const float lg = lg_s[0];
 
-  // ---- S = Q K^T
-  bool ok = mbar_wait(bar_load, 0);
-  bool all_ok = __syncthreads_and(ok);
-  if (all_ok && tid == 0) {
-    tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
-    const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb);
-#pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-      mma_bf16(tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-               idesc, kk > 0);
-    }
-    mma_commit(bar_s);
-  }
-  __syncwarp();
-  ok = all_ok && mbar_wait(bar_s, 0);
+  // ---- S = Q K^T (issued by thread 0 above)
+  bool all_ok = __syncthreads_and(landed);
+  bool ok = all_ok && mbar_wait(bar_s, 0);
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
 
@@ -336,68 +340,15 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   }
   __syncwarp();
 
-  // ---- P, bf16 into Kb once the state MMA has finished reading it.  The two warps of
-  // quarter qt take the 32-column chunks of their parity: chunks c > qt lie above the
-  // diagonal (zero), chunks c < qt below it (level 5 + bit_length(qt XOR c) for every
-  // pair), chunk qt holds the diagonal.
-  bool u_done = false;
-  if (all_ok) {
-    const float* lam_r = lam_s + r * kLamStride;
-    for (int c = hh; c < kTile / 32; c += 2) {
-      float sv[32];
-      if (c <= qt) {
-        tmem_ld32(tmem + lane_base + c * 32, sv);
-        if (c < qt) {
-          const float wl = lam_r[5 + (32 - __clz((unsigned)(qt ^ c)))];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) sv[k] *= wl * __expf(cs - cs_s[c * 32 + k]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int s = c * 32 + k;
-            float v = 0.f;
-            if (s <= r && row_live)
-              v = sv[k] * lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * __expf(cs - cs_s[s]);
-            sv[k] = v;
-          }
-        }
-      }
-      if (!u_done) {
-        ok = ok && mbar_wait(bar_u, 0);
-        u_done = true;
-      }
-      if (c > qt)
-        put_row32_zero(Kb, r, c);
-      else
-        put_row32_bf16(Kb, r, c, sv);
-    }
-  }
+  ok = all_ok && mbar_wait(bar_u, 0);
   tc_fence_after();
-  fence_proxy_async_smem();
-  tc_fence_before();
   all_ok = __syncthreads_and(ok);
-  // ---- O = P V into columns 0..127 (V MN-major as B)
-  if (all_ok && tid == 0) {
-    tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
-    const uint32_t pa = smem_u32(Kb), va = smem_u32(Vb);
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk) {
-      const uint32_t aoff = (kk >> 2) * kPanel + (kk & 3) * 32;
-      mma_bf16(tmem, smem_desc_sw128(pa + aoff, 16, 1024),
-               smem_desc_sw128(va + kk * 2048, kPanel, 1024), idesc, kk > 0);
-    }
-    mma_commit(bar_o);
-  }
-  __syncwarp();
 
-  // ---- O = P V is done: publish the tile's state U_j (staged bf16 in Kb, which P no
-  // longer needs, then stored coalesced), and for odd j form the block state of slot
-  // j+1 (below) and publish it.  Published states are row-major [d_v][d_k] bf16; thread
-  // tid moves the 16-byte pieces q = it * 256 + tid.
-  ok = all_ok && mbar_wait(bar_o, 0);
-  tc_fence_after();
-  all_ok = __syncthreads_and(ok);
+  // ---- publish U_j (staged bf16 in Qb, which S no longer reads, then stored coalesced)
+  // and, for odd j, form the block state of slot j+1 and publish it; then Q comes back
+  // by TMA for the levels.  Published states are row-major [d_v][d_k] bf16; thread tid
+  // moves the 16-byte pieces q = it * 256 + tid.  This runs even after an error, so that
+  // no reader waits for a flag that is never raised.
   const uint8_t* Ug = p.U + bh * N * kOperand;
   uint8_t* nodes = p.nodes + bh * N * kOperand;
   const float* lgu = p.lgu + bh * N;
@@ -405,10 +356,10 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint32_t* rdy_u = p.rdy_u + bh * N;
   uint32_t* rdy_n = p.rdy_n + bh * N;
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {  // U^T row r, columns [64 hh, 64 hh + 64) -> Kb
+  for (int c = 0; c < 2; ++c) {  // U^T row r, columns [64 hh, 64 hh + 64) -> Qb
     float v[32];
     tmem_ld32(tmem + lane_base + 128 + 64 * hh + 32 * c, v);
-    put_row32_bf16(Kb, r, 2 * hh + c, v);
+    put_row32_bf16(Qb, r, 2 * hh + c, v);
   }
   __syncthreads();
   const bool forms = (j & 1) && j + 1 < N;  // odd j forms the block state of slot j+1
@@ -416,7 +367,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
 #pragma unroll
   for (int it = 0; it < kStatePieces; ++it) {
     const int q = it * kThreadsF + tid;
-    const uint4 w = *reinterpret_cast<const uint4*>(Kb + piece_offset(q));
+    const uint4 w = *reinterpret_cast<const uint4*>(Qb + piece_offset(q));
     reinterpret_cast<uint4*>(const_cast<uint8_t*>(Ug) + (int64_t)j * kOperand)[q] = w;
     const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -471,6 +422,69 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     if (tid == 0) st_release_gpu(&rdy_n[c], 1u);
   }
 
+  __syncthreads();  // Qb is no longer read
+  if (tid == 0 && nlev > 0) {
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar_q, kOperand);
+    tma_load_4d(&tmQ, bar_q, Qb, 0, h, t0, b);
+    tma_load_4d(&tmQ, bar_q, Qb + kPanel, 64, h, t0, b);
+  }
+  __syncwarp();
+
+  // ---- P, bf16 into Kb (the state MMA is done with it).  The two warps of
+  // quarter qt take the 32-column chunks of their parity: chunks c > qt lie above the
+  // diagonal (zero), chunks c < qt below it (level 5 + bit_length(qt XOR c) for every
+  // pair), chunk qt holds the diagonal.
+  if (all_ok) {
+    const float* lam_r = lam_s + r * kLamStride;
+    for (int c = hh; c < kTile / 32; c += 2) {
+      float sv[32];
+      if (c <= qt) {
+        tmem_ld32(tmem + lane_base + c * 32, sv);
+        if (c < qt) {
+          const float wl = lam_r[5 + (32 - __clz((unsigned)(qt ^ c)))];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) sv[k] *= wl * __expf(cs - cs_s[c * 32 + k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int s = c * 32 + k;
+            float v = 0.f;
+            if (s <= r && row_live)
+              v = sv[k] * lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * __expf(cs - cs_s[s]);
+            sv[k] = v;
+          }
+        }
+      }
+      if (c > qt)
+        put_row32_zero(Kb, r, c);
+      else
+        put_row32_bf16(Kb, r, c, sv);
+    }
+  }
+  tc_fence_after();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  all_ok = __syncthreads_and(ok);
+  // ---- O = P V into columns 0..127 (V MN-major as B)
+  if (all_ok && tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+    const uint32_t pa = smem_u32(Kb), va = smem_u32(Vb);
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk) {
+      const uint32_t aoff = (kk >> 2) * kPanel + (kk & 3) * 32;
+      mma_bf16(tmem, smem_desc_sw128(pa + aoff, 16, 1024),
+               smem_desc_sw128(va + kk * 2048, kPanel, 1024), idesc, kk > 0);
+    }
+    mma_commit(bar_o);
+  }
+  __syncwarp();
+
+  // ---- O = P V is done: Kb and Vb are free
+  ok = all_ok && mbar_wait(bar_o, 0);
+  tc_fence_after();
+  all_ok = __syncthreads_and(ok);
   // ---- the levels' block states: thread k acquires level k's ready flag now and later
   // issues its TMA load itself (after a proxy fence), so the acquire and the async-proxy
   // read are ordered in one thread.  The block state of slot c is U_{c-1} for odd c.
@@ -528,6 +542,10 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   // shared buffer (k odd ? Kb : Vb) and TMEM columns [128 (k&1), +128); bar_node[k&1]
   // signals its block state, bar_lvl[k&1] its MMA.  The load of level k+1 starts once
   // level k-1 has been added to O (levels 0 and 1 were started above).
+  if (nlev > 0 && all_ok) {  // Q is back
+    ok = mbar_wait(bar_q, 0);
+    all_ok = __syncthreads_and(ok);
+  }
   uint32_t lvl_ph[2] = {0, 0}, node_ph[2] = {0, 0};
   float D = 0.f;  // log decay from block k's end to the tile's start
   for (int k = 0; k <= nlev && all_ok; ++k) {
