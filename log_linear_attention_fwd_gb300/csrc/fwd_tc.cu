@@ -155,7 +155,8 @@ struct FSmem {
   static constexpr int kLg = kRed + 32;                        // 4 floats
   static constexpr int kNl = kLg + 16;                         // kMaxChunkLevels floats
   static constexpr int kCs = kNl + 4 * kMaxChunkLevels;        // 128 floats
-  static constexpr int kLam = kCs + 4 * kTile;                 // 128 x kLamStride floats
+  static constexpr int kFcol = kCs + 4 * kTile;                // 128 floats
+  static constexpr int kLam = kFcol + 4 * kTile;               // 128 x kLamStride floats
   static constexpr int kLamX = kLam + 4 * kTile * kLamStride;  // [levels][128] floats
 };
 
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   float* lg_s = reinterpret_cast<float*>(smem + FSmem::kLg);
   float* nl_s = reinterpret_cast<float*>(smem + FSmem::kNl);
   float* cs_s = reinterpret_cast<float*>(smem + FSmem::kCs);
+  float* fcol = reinterpret_cast<float*>(smem + FSmem::kFcol);  // exp(cs_e - cs_s), e = s | 31
   float* lam_s = reinterpret_cast<float*>(smem + FSmem::kLam);
   float* lamx = reinterpret_cast<float*>(smem + FSmem::kLamX);
 
@@ -263,6 +265,12 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, h, t0, b);
     tma_load_4d(&tmV, bar_load, Vb, 0, h, t0, b);
     tma_load_4d(&tmV, bar_load, Vb + kPanel, 64, h, t0, b);
+  }
+  if (tid == 64 && h == 0 && j + 2 < N) {  // warm L2 with tile j+2's log a and lambda (all heads)
+    const int64_t tok0 = (int64_t)b * p.T + (int64_t)(j + 2) * kTile;
+    const int64_t ntok = min(kTile, p.T - (j + 2) * kTile);
+    prefetch_l2_range(p.lam + tok0 * p.H * p.L, ntok * p.H * p.L * 4);
+    if (p.log_a) prefetch_l2_range(p.log_a + tok0 * p.H, ntok * p.H * 4);
   }
   if (tid == 32) {  // warm L2 with the block states the levels will read
     for (int m = 1; m < kMaxChunkLevels; ++m) {
@@ -316,6 +324,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   __syncthreads();
   const float cs = cs_s[r];
   const float lg = lg_s[0];
+  if (hh == 1) fcol[r] = __expf(cs_s[r | 31] - cs);  // <= 1: cs does not increase
 
   // ---- S = Q K^T (issued by thread 0 above)
   bool all_ok = __syncthreads_and(landed);
@@ -441,10 +450,11 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       float sv[32];
       if (c <= qt) {
         tmem_ld32(tmem + lane_base + c * 32, sv);
-        if (c < qt) {
-          const float wl = lam_r[5 + (32 - __clz((unsigned)(qt ^ c)))];
+        if (c < qt) {  // exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s), both <= 1
+          const float wl = lam_r[5 + (32 - __clz((unsigned)(qt ^ c)))] *
+                           __expf(cs - cs_s[c * 32 + 31]);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) sv[k] *= wl * __expf(cs - cs_s[c * 32 + k]);
+          for (int k = 0; k < 32; ++k) sv[k] *= wl * fcol[c * 32 + k];
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) {

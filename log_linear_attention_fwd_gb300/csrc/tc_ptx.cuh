@@ -133,6 +133,17 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Warms L2 with the 16-byte-aligned part of [p, p + bytes) (a hint: nothing outside the
+// range is touched).
+__device__ __forceinline__ void prefetch_l2_range(const void* p, int64_t bytes) {
+  const uint64_t a = reinterpret_cast<uint64_t>(p);
+  const uint64_t lo = (a + 15) & ~uint64_t(15), hi = (a + (uint64_t)bytes) & ~uint64_t(15);
+  for (uint64_t x = lo; x + 16 <= hi; x += 65536) {
+    const uint64_t n = hi - x < 65536 ? hi - x : 65536;
+    prefetch_l2_bulk(reinterpret_cast<const void*>(x), (uint32_t)n);
+  }
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
