@@ -148,8 +148,8 @@ __device__ __forceinline__ float block_scan256(float x, float* red) {
 struct FSmem {
   // byte offsets from the 1024-aligned base
   static constexpr int kQ = 0, kK = kOperand, kV = 2 * kOperand;
-  static constexpr int kBars = 3 * kOperand;                   // 9 mbarriers
-  static constexpr int kTslot = kBars + 10 * 8;
+  static constexpr int kBars = 3 * kOperand;                   // 11 mbarriers
+  static constexpr int kTslot = kBars + 12 * 8;
   static constexpr int kInt = kTslot + 16;                     // ticket: 4 u32
   static constexpr int kRed = kInt + 16;                       // 8 floats
   static constexpr int kLg = kRed + 32;                        // 4 floats
@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint64_t* bar_lvl = &bars[4];      // [2]: level MMAs
   uint64_t* bar_node = &bars[6];     // [2]: block-state loads
   uint64_t* bar_q = &bars[8];        // Q loaded again for the levels
+  uint64_t* bar_free = &bars[9];     // [2]: every warp has read a level's TMEM buffer
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + FSmem::kTslot);
   uint32_t* ints = reinterpret_cast<uint32_t*>(smem + FSmem::kInt);  // [0] ticket
   float* red = reinterpret_cast<float*>(smem + FSmem::kRed);
@@ -238,6 +239,8 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     prefetch_tensormap(&tmU);
     prefetch_tensormap(&tmNode);
     for (int q = 0; q < 9; ++q) mbar_init(&bars[q], 1);
+    mbar_init(&bar_free[0], kThreadsF / 32);
+    mbar_init(&bar_free[1], kThreadsF / 32);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -491,32 +494,34 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   }
   __syncwarp();
 
-  // ---- O = P V is done: Kb and Vb are free
-  ok = all_ok && mbar_wait(bar_o, 0);
-  tc_fence_after();
-  all_ok = __syncthreads_and(ok);
-  // ---- the levels' block states: thread k acquires level k's ready flag now and later
-  // issues its TMA load itself (after a proxy fence), so the acquire and the async-proxy
-  // read are ordered in one thread.  The block state of slot c is U_{c-1} for odd c.
-  int my_c = 0;  // thread k < nlev: the slot of level k
+  // ---- while P V runs, the levels' block states: thread 32+k (warp 1) acquires level
+  // k's ready flag now and later issues its TMA load itself (after a proxy fence), so the
+  // acquire and the async-proxy read are ordered in one thread.  The block state of slot
+  // c is U_{c-1} for odd c.
+  int my_c = 0;  // thread 32+k, k < nlev: the slot of level k
   {
     bool fl = true;
-    if (tid < nlev) {
+    const int k = tid - 32;
+    if (k >= 0 && k < nlev) {
       int m = 0;
-      for (int seen = -1; seen < tid;) {
+      for (int seen = -1; seen < k;) {
         ++m;
         if ((j >> (m - 1)) & 1) ++seen;
       }
       my_c = (j >> (m - 1)) << (m - 1);
       const bool is_u = (my_c & 1) != 0;
       fl = wait_flag_acquire(is_u ? &rdy_u[my_c - 1] : &rdy_n[my_c]);
-      nl_s[tid] = fl ? __ldcg(is_u ? &lgu[my_c - 1] : &nlg[my_c]) : 0.f;
+      nl_s[k] = fl ? __ldcg(is_u ? &lgu[my_c - 1] : &nlg[my_c]) : 0.f;
       fence_proxy_async_global();
     }
     if (!__syncthreads_and(fl) && tid == 0) atomicOr(&g_tc_error, 2u);
   }
-  auto fetch = [&](int k) {  // thread k: TMA of level k's block state into (k odd ? Kb : Vb)
-    if (tid == k) {
+  // ---- O = P V is done: Kb and Vb are free
+  ok = all_ok && mbar_wait(bar_o, 0);
+  tc_fence_after();
+  all_ok = __syncthreads_and(ok);
+  auto fetch = [&](int k) {  // thread 32+k: TMA of level k's block state into (k odd ? Kb : Vb)
+    if (tid == 32 + k) {
       uint8_t* dst = (k & 1) ? Kb : Vb;
       const bool is_u = (my_c & 1) != 0;
       const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
@@ -548,23 +553,27 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   tc_fence_before();
   __syncthreads();  // TMEM is free
 
-  // ---- inter-chunk levels.  Level k (the k-th set bit of j, from the lowest) uses
-  // shared buffer (k odd ? Kb : Vb) and TMEM columns [128 (k&1), +128); bar_node[k&1]
-  // signals its block state, bar_lvl[k&1] its MMA.  The load of level k+1 starts once
-  // level k-1 has been added to O (levels 0 and 1 were started above).
-  if (nlev > 0 && all_ok) {  // Q is back
-    ok = mbar_wait(bar_q, 0);
-    all_ok = __syncthreads_and(ok);
-  }
-  uint32_t lvl_ph[2] = {0, 0}, node_ph[2] = {0, 0};
+  // ---- inter-chunk levels, without block barriers.  Level k (the k-th set bit of j,
+  // from the lowest) uses shared buffer (k odd ? Kb : Vb) and TMEM columns
+  // [128 (k&1), +128).  Thread 0 issues MMA k once its block state has landed
+  // (bar_node[k&1]) and every warp has added level k-2 to O (bar_free[k&1]); each warp
+  // adds level k-1 to O once MMA k-1 is done (bar_lvl), then releases that TMEM buffer.
+  // The load of level k+1 starts as soon as MMA k-1 is done with its shared buffer
+  // (levels 0 and 1 were started above).
+  const int lane = tid & 31;
+  uint32_t lvl_ph[2] = {0, 0}, node_ph[2] = {0, 0}, free_ph[2] = {0, 0};
   float D = 0.f;  // log decay from block k's end to the tile's start
+  bool lv_ok = all_ok;
+  if (tid == 0 && nlev > 0 && lv_ok) lv_ok = mbar_wait(bar_q, 0);  // Q is back
   for (int k = 0; k <= nlev && all_ok; ++k) {
-    if (k < nlev) {  // issue level k
-      ok = mbar_wait(&bar_node[k & 1], node_ph[k & 1]);
+    if (tid == 0 && k < nlev) {  // issue level k
+      bool go = lv_ok && mbar_wait(&bar_node[k & 1], node_ph[k & 1]);
       node_ph[k & 1] ^= 1;
-      all_ok = __syncthreads_and(ok);
-      if (!all_ok) break;
-      if (tid == 0) {
+      if (k >= 2) {
+        go = go && mbar_wait(&bar_free[k & 1], free_ph[k & 1]);
+        free_ph[k & 1] ^= 1;
+      }
+      if (go) {
         tc_fence_after();
         constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
         const uint32_t qa = smem_u32(Qb), sa = smem_u32((k & 1) ? Kb : Vb);
@@ -576,15 +585,19 @@ __global__ void __launch_bounds__(kThreadsF, 2)
         }
         mma_commit(&bar_lvl[k & 1]);
       }
-      __syncwarp();
+      lv_ok = go;
     }
-    if (k >= 1) {  // finish level k-1 while level k runs
+    __syncwarp();
+    if (k >= 1) {  // level k-1 into O
       const int bf = (k - 1) & 1;
-      ok = mbar_wait(&bar_lvl[bf], lvl_ph[bf]);
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_lvl[bf], lvl_ph[bf]));
       lvl_ph[bf] ^= 1;
+      if (!got) {
+        lv_ok = false;
+        break;
+      }
       tc_fence_after();
-      all_ok = __syncthreads_and(ok);
-      if (!all_ok) break;
+      if (k + 1 < nlev) fetch(k + 1);  // thread 33+k, into the buffer MMA k-1 read
       const float wr = lamx[(k - 1) * kTile + r] * __expf(cs + D);
       D += nl_s[k - 1];
 #pragma unroll
@@ -595,11 +608,11 @@ __global__ void __launch_bounds__(kThreadsF, 2)
         for (int q = 0; q < 32; ++q) o[c * 32 + q] = fmaf(wr, v[q], o[c * 32 + q]);
       }
       tc_fence_before();
-      __syncthreads();  // buffer bf (TMEM and shared) is free again
-      if (k + 1 < nlev) fetch(k + 1);
       __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_free[bf]);
     }
   }
+  all_ok = __syncthreads_and(all_ok && lv_ok);
 
   // ---- epilogue
   if (all_ok) {
