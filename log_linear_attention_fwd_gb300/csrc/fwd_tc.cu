@@ -110,7 +110,7 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
 //      previous level's product added to O with the row weights
 //      lambda[t, 7+m] exp(cs_t + D_m).  D_m, the log decay from the block's end to the
 //      tile's start, is the sum of the log decays of the lower levels' blocks, which
-//      their producers store next to them.  All block states are warmed in L2 at start.
+//      their producers store next to them.
 //   7. O to bf16 through a TMA store, or fp32 stores.
 //
 // Block states.  Slot c holds the decayed total of the 2^z tiles before c, z = ctz(c):
@@ -274,14 +274,6 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     const int64_t ntok = min(kTile, p.T - (j + 2) * kTile);
     prefetch_l2_range(p.lam + tok0 * p.H * p.L, ntok * p.H * p.L * 4);
     if (p.log_a) prefetch_l2_range(p.log_a + tok0 * p.H, ntok * p.H * 4);
-  }
-  if (tid == 32) {  // warm L2 with the block states the levels will read
-    for (int m = 1; m < kMaxChunkLevels; ++m) {
-      if (!((j >> (m - 1)) & 1)) continue;
-      const int64_t c = ((int64_t)j >> (m - 1)) << (m - 1);
-      prefetch_l2_bulk((c & 1) ? p.U + (bh * N + c - 1) * kOperand : p.nodes + (bh * N + c) * kOperand,
-                       kOperand);
-    }
   }
   __syncwarp();
 
