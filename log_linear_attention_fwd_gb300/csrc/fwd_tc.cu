@@ -450,6 +450,17 @@ __global__ void __launch_bounds__(kThreadsF, 2)
                            __expf(cs - cs_s[c * 32 + 31]);
 #pragma unroll
           for (int k = 0; k < 32; ++k) sv[k] *= wl * fcol[c * 32 + k];
+        } else if (cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f) {
+          // the diagonal chunk with a decay range that keeps exp(cs_t - cs_e) <= e^80:
+          // exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s)
+          const float gt = __expf(cs - cs_s[c * 32 + 31]);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int s = c * 32 + k;
+            sv[k] = (s <= r && row_live)
+                        ? sv[k] * lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * (gt * fcol[s])
+                        : 0.f;
+          }
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
