@@ -126,6 +126,26 @@ LL_API int loglinear_fwd_with_events(const void* q, const void* k, const void* v
                                      void* const* stage_events, int n_events, int* n_kernels);
 
 /*
+ * Prefill for decoding: loglinear_fwd over positions 0..T-1, plus the per-level decode
+ * state at position T-1, so that loglinear_decode_step can continue at t = T (first page,
+ * sections 循环形式与输出计算 (one state per Fenwick bucket) and 两阶段计算 (block states
+ * of chunks)).  Level l of the state is the sum over the level-l Fenwick bucket of T-1 of
+ * exp(cum_{T-1} - cum_s) k_s v_s^T.  Levels above the last chunk are the forward's block
+ * states of chunks, decayed to T-1; the levels inside the last chunk (and level 0) are
+ * summed from k and v; the other levels are zero.
+ *   state_out [B, H, L, dk, dv] fp32, fully overwritten (all zero when T = 0).  On the
+ *           tensor-core path the levels taken from block states carry their bf16
+ *           rounding.
+ * The other arguments, the workspace and the errors are those of loglinear_fwd; state_out
+ * NULL or not 4-byte aligned is LL_ERR_INVALID / LL_ERR_ALIGN.
+ */
+LL_API int loglinear_prefill(const void* q, const void* k, const void* v, const float* log_a,
+                             const float* lambda, void* out, float* state_out, int64_t B,
+                             int64_t T, int64_t H, int64_t dk, int64_t dv, int64_t L, int chunk,
+                             int in_dtype, int out_dtype, int path, void* workspace,
+                             size_t workspace_bytes, ll_stream_t stream);
+
+/*
  * One decode step at position t for every (b, h) (first page, section 解码：基于 lssb 的
  * 状态更新; slide deck "論文紹介：Log Linear Attention", slide 21).  With l = lssb(t) (index of
  * the lowest set bit of t > 0):
@@ -151,9 +171,10 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
 
 /*
  * Reads and clears the device error word of the tensor-core path (synchronises `stream`).
- * *flags = 0 when every mbarrier wait of the kernels run so far completed; bit 0 set when
- * a wait ran out of time (the CTA then skipped its remaining work, its output tile is not
- * valid, and the launch itself still reported success).
+ * *flags = 0 when every wait of the kernels run so far completed.  Bit 0: an mbarrier
+ * wait ran out of time (the CTA then skipped its remaining work and its output tile is
+ * not valid).  Bit 1: a wait for another tile's published state ran out of time (the
+ * output of that tile is not valid).  The launch itself still reported success.
  */
 LL_API int loglinear_device_error(ll_stream_t stream, unsigned* flags);
 

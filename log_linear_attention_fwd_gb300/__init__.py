@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     loglinear_fwd,
     loglinear_fwd_noalloc,
     loglinear_fwd_with_events,
+    loglinear_prefill,
     resolve_path,
     status_string,
 )

@@ -43,6 +43,8 @@ SIGNATURES = {
     "loglinear_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "loglinear_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                      _i64, _int, _int, _int, _int, _vp]),
+    "loglinear_prefill": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                 _i64, _int, _int, _int, _int, _vp, _sz, _vp]),
 }
 
 
@@ -193,6 +195,37 @@ def loglinear_decode_step(state, q, k, v, log_a, lam, t, out=None, out_dtype=Non
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_decode_step")
     return out
+
+
+def loglinear_prefill(q, k, v, log_a, lam, chunk, out=None, state=None, out_dtype=None,
+                      workspace=None, path="auto", stream=None):
+    """loglinear_fwd over the prompt plus the per-level decode state at its last position
+    (fp32 [B, H, L, dk, dv]), ready for loglinear_decode_step at t = T.
+    Returns (out, state)."""
+    B, T, H, dk = q.shape
+    dv, L = v.shape[-1], lam.shape[-1]
+    _check_dev("q", q, shape=(B, T, H, dk))
+    _check_dev("k", k, q.dtype, (B, T, H, dk))
+    _check_dev("v", v, q.dtype, (B, T, H, dv))
+    _check_dev("log_a", log_a, torch.float32, (B, T, H))
+    _check_dev("lam", lam, torch.float32, (B, T, H, L))
+    in_dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty(B, T, H, dv, device=q.device, dtype=out_dtype or q.dtype)
+    if state is None:
+        state = torch.empty(B, H, L, dk, dv, device=q.device, dtype=torch.float32)
+    _check_dev("out", out, shape=(B, T, H, dv))
+    _check_dev("state", state, torch.float32, (B, H, L, dk, dv))
+    ws_bytes = fwd_workspace_size(B, T, H, dk, dv, chunk, in_dt, path) if T > 0 else 0
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), device=q.device, dtype=torch.uint8)
+    _check_dev("workspace", workspace, torch.uint8)
+    st = _lib.loglinear_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
+                                _ptr(state), B, T, H, dk, dv, L, chunk, in_dt, _dtype_code(out),
+                                PATHS[path], _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_prefill")
+    return out, state
 
 
 def loglinear_fwd_noalloc(q, k, v, log_a, lam, chunk, out, path="auto", stream=None):

@@ -101,6 +101,10 @@ cudaError_t launch_simt_forward(const FwdArgs& a, int in_dtype, int out_dtype, c
                                 StageEvents* ev);
 cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev);
 cudaError_t launch_level_scan(const FwdArgs& a, cudaStream_t s);
+// The decode state at position T-1 from a completed forward's workspace (tc_layout: the
+// tensor-core path's bf16 [d_v][d_k] block states).
+cudaError_t launch_prefill_state(const FwdArgs& a, bool tc_layout, int in_dtype, float* state,
+                                 cudaStream_t s);
 // Reads and clears the tensor-core path's device error word (synchronises the stream).
 cudaError_t tc_take_error(cudaStream_t s, unsigned* flags);
 bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int chunk);

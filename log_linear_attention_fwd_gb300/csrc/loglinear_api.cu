@@ -156,7 +156,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* lo
                     const float* lambda, void* out, int64_t B, int64_t T, int64_t H, int64_t dk,
                     int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype, int path,
                     void* workspace, size_t workspace_bytes, ll_stream_t stream,
-                    StageEvents* ev) {
+                    StageEvents* ev, float* state_out = nullptr) {
   int p, tile;
   int64_t N;
   int st = check_fwd_sizes(B, T, H, dk, dv, chunk, in_dtype, path, &p, &tile, &N);
@@ -185,8 +185,10 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* lo
   a.rdy_n = reinterpret_cast<uint32_t*>(ws + w.off_rdy_n);
   a.tick = reinterpret_cast<uint32_t*>(ws + w.off_tick);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = p == LL_PATH_TC ? launch_tc_forward(a, out_dtype, s, ev)
-                                        : launch_simt_forward(a, in_dtype, out_dtype, s, ev);
+  cudaError_t e = p == LL_PATH_TC ? launch_tc_forward(a, out_dtype, s, ev)
+                                  : launch_simt_forward(a, in_dtype, out_dtype, s, ev);
+  if (e == cudaSuccess && state_out)
+    e = launch_prefill_state(a, p == LL_PATH_TC, in_dtype, state_out, s);
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 
@@ -196,6 +198,22 @@ int loglinear_fwd(const void* q, const void* k, const void* v, const float* log_
                   void* workspace, size_t workspace_bytes, ll_stream_t stream) {
   return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, dk, dv, L, chunk, in_dtype, out_dtype,
                   path, workspace, workspace_bytes, stream, nullptr);
+}
+
+int loglinear_prefill(const void* q, const void* k, const void* v, const float* log_a,
+                      const float* lambda, void* out, float* state_out, int64_t B, int64_t T,
+                      int64_t H, int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
+                      int out_dtype, int path, void* workspace, size_t workspace_bytes,
+                      ll_stream_t stream) {
+  if (!state_out) return LL_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(state_out) & 3u) != 0) return LL_ERR_ALIGN;
+  if (B > 0 && H > 0 && T == 0 && L >= 1 && dk >= 1 && dv >= 1) {  // no prefix: empty state
+    const cudaError_t e = cudaMemsetAsync(state_out, 0, sizeof(float) * (size_t)(B * H * L * dk * dv),
+                                          reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LL_OK : cuda_fail(e);
+  }
+  return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, dk, dv, L, chunk, in_dtype, out_dtype,
+                  path, workspace, workspace_bytes, stream, nullptr, state_out);
 }
 
 int loglinear_fwd_with_events(const void* q, const void* k, const void* v, const float* log_a,

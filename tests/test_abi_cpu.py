@@ -82,6 +82,25 @@ def test_fwd_validation_codes(L):
         assert fwd(L, q=None, k=None, v=None, lam=None, out=None, **kw) == L.LL_OK
 
 
+def test_prefill_validation_codes(L):
+    def pre(state, **kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, out=FAKE, B=1, T=64, H=2, dk=16,
+                 dv=16, Lv=7, chunk=16, ind=L.LL_F32, outd=L.LL_F32, path=L.LL_PATH_SIMT,
+                 ws=None, wsb=0, stream=None)
+        a.update(kw)
+        return L.lib().loglinear_prefill(a["q"], a["k"], a["v"], a["log_a"], a["lam"], a["out"],
+                                         state, a["B"], a["T"], a["H"], a["dk"], a["dv"], a["Lv"],
+                                         a["chunk"], a["ind"], a["outd"], a["path"], a["ws"],
+                                         a["wsb"], a["stream"])
+    assert pre(None) == L.LL_ERR_INVALID
+    assert pre(ctypes.c_void_p(0x1002)) == L.LL_ERR_ALIGN
+    # the forward's own validation applies unchanged
+    assert pre(FAKE, chunk=3) == L.LL_ERR_SHAPE
+    assert pre(FAKE, Lv=6) == L.LL_ERR_SHAPE
+    assert pre(FAKE, ws=None, wsb=0) == L.LL_ERR_WORKSPACE
+    assert pre(FAKE, B=0, q=None, k=None, v=None, lam=None, out=None) == L.LL_OK
+
+
 def test_workspace_size_and_paths(L):
     sz = L.fwd_workspace_size(1, 64, 2, 16, 16, 16, L.LL_F32, "simt")
     n_states = 1 * 2 * 4 * 16 * 16

@@ -1,0 +1,110 @@
+"""Prefill -> decode handoff on the GPU: the per-level decode state after a prompt,
+checked against the oracle's bucket definition, and decode steps that continue from it,
+checked against the oracle's direct form over the longer sequence."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.helpers import TOL_BF16, TOL_F32, cuda, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def LL():
+    import log_linear_attention_fwd_gb300 as m
+    return m
+
+
+def oracle_state(x, T):
+    """[B, H, L, dk, dv] per-level states at position T-1 (bucket definition)."""
+    B, _, H, dk = x["q"].shape
+    dv, L = x["v"].shape[-1], x["lam"].shape[-1]
+    S = np.zeros((B, H, L, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            la = None if x["log_a"] is None else x["log_a"][b, :T, h]
+            S[b, h] = oracle.states_from_buckets(x["k"][b, :T, h], x["v"][b, :T, h], la, T - 1, L)
+    return S
+
+
+def check_state(got, want, tol):
+    err = rel_l2(got, want)
+    # each non-empty level on its own, relative to its own size
+    B, H, L = want.shape[:3]
+    for lv in range(L):
+        w = want[:, :, lv]
+        if np.linalg.norm(w) > 0:
+            assert rel_l2(got[:, :, lv], w) <= tol, lv
+        else:
+            assert float(np.abs(got[:, :, lv].double().numpy()).max()) == 0.0, lv
+    return err
+
+
+@pytest.mark.parametrize("T,C", [(1, 16), (2, 16), (17, 16), (64, 16), (100, 8), (257, 32),
+                                 (1000, 64)])
+def test_prefill_state_simt(LL, T, C):
+    L = max((T - 1).bit_length() + 1, 1)
+    cfg = W.FwdConfig("p", 2, 3, T, 16, 8, C, L, "f32", True, "softplus", seed=T + 3)
+    x = W.make_fwd_inputs(cfg)
+    d = cuda(x)
+    out, state = LL.loglinear_prefill(d["q"], d["k"], d["v"], d["log_a"], d["lam"], C, path="simt")
+    torch.cuda.synchronize()
+    err = check_state(state.cpu(), oracle_state(x, T), TOL_F32)
+    assert rel_l2(out.cpu(), oracle.forward_direct(x["q"], x["k"], x["v"], x["log_a"], x["lam"])) <= TOL_F32
+    print(f"simt T={T}: state rel_l2={err:.2e}")
+
+
+@pytest.mark.parametrize("T", [1, 128, 300, 1000, 2049])
+def test_prefill_state_tc(LL, T):
+    L = max((T - 1).bit_length() + 1, 1)
+    cfg = W.FwdConfig("p", 2, 3, T, 128, 128, 64, L, "bf16", True, "softplus", seed=T + 5)
+    x = W.make_fwd_inputs(cfg)
+    d = cuda(x)
+    assert LL.resolve_path(128, 128, 64, 1) == "tc"
+    out, state = LL.loglinear_prefill(d["q"], d["k"], d["v"], d["log_a"], d["lam"], 64, path="tc")
+    torch.cuda.synchronize()
+    assert LL.device_error() == 0
+    err = check_state(state.cpu(), oracle_state(x, T), TOL_BF16)
+    print(f"tc T={T}: state rel_l2={err:.2e}")
+
+
+@pytest.mark.parametrize("path,T,dk,dtype", [("simt", 300, 16, "f32"), ("tc", 1151, 128, "bf16")])
+def test_decode_continues_from_prefill(LL, path, T, dk, dtype):
+    """Prefill T positions, then decode positions T..T+n-1 from the handed-over state; the
+    outputs must match the direct form over the whole T+n sequence."""
+    n = 6
+    L = (T + n - 1).bit_length() + 1
+    cfg = W.FwdConfig("pd", 2, 2, T + n, dk, dk, 64, L, dtype, True, "softplus", seed=11)
+    x = W.make_fwd_inputs(cfg)
+    d = cuda(x)
+    pre = {k: (None if v is None else v[:, :T].contiguous()) for k, v in d.items()}
+    _, state = LL.loglinear_prefill(pre["q"], pre["k"], pre["v"], pre["log_a"], pre["lam"], 64,
+                                    path=path)
+    outs = []
+    for t in range(T, T + n):
+        o = LL.loglinear_decode_step(state, d["q"][:, t].contiguous(), d["k"][:, t].contiguous(),
+                                     d["v"][:, t].contiguous(), d["log_a"][:, t].contiguous(),
+                                     d["lam"][:, t].contiguous(), t, out_dtype=torch.float32)
+        outs.append(o)
+    torch.cuda.synchronize()
+    got = torch.stack(outs, dim=1).cpu()  # [B, n, H, dv]
+    rows = np.arange(T, T + n)
+    want = oracle.forward_direct(x["q"], x["k"], x["v"], x["log_a"], x["lam"], rows=rows)[:, rows]
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    err = rel_l2(got, want)
+    print(f"{path}: continuation rel_l2={err:.2e}")
+    assert err <= tol
+
+
+def test_prefill_empty_prompt(LL):
+    B, H, L, d = 2, 3, 4, 8
+    q = torch.zeros(B, 0, H, d, device="cuda")
+    lam = torch.zeros(B, 0, H, L, device="cuda")
+    la = torch.zeros(B, 0, H, device="cuda")
+    state = torch.full((B, H, L, d, d), 7.0, device="cuda")
+    _, state = LL.loglinear_prefill(q, q, q, la, lam, 16, state=state, path="simt")
+    torch.cuda.synchronize()
+    assert float(state.abs().max()) == 0.0
