@@ -321,6 +321,7 @@ def run_ours(args, rank, world, local_rank):
               "config": {"workload": dcfg.name, "B": dcfg.B, "H": dcfg.H, "dk": dcfg.dk,
                          "dv": dcfg.dv, "L": dcfg.L, "t": dcfg.t, "state": "fp32"}}
     e2e = measure_e2e(LL, cfg, x, dev, ws, args)
+    prefill = measure_prefill(LL, cfg, d, out, ws, flush, peaks)
     res = {"metric": METRIC, "value": fwd_tok_s, "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": (fwd_mean + dec_mean) * 1e3, "higher_is_better": True,
@@ -334,6 +335,7 @@ def run_ours(args, rank, world, local_rank):
                       "parallelism": f"replicas x{world} (independent (b,h) work, no collective)"},
            "fwd_ms": fwd_mean * 1e3, "fwd_stage_us": dict(zip(stage_names, [s * 1e6 for s in stage_mean])),
            "roofline": roofline, "roofline_fwd": roofline_fwd, "decode": decode, "e2e": e2e,
+           "prefill": prefill,
            "gpu_launches": args.steps * (n_kernels + 1), "clocks": clk,
            "wall_s_timed_region": wall}
     return res
@@ -355,6 +357,43 @@ def stage_bytes(cfg, path, name):
     if name.endswith("level_scan"):
         return st * 4 + st * node_e
     return qkv + tok * 4 + tok * cfg.L * 4 + st * node_e + tok * cfg.dv * e
+
+
+def measure_prefill(LL, cfg, d, out, ws, flush, peaks, reps=10):
+    """The prefill -> decode handoff on the headline prompt: loglinear_prefill (forward
+    plus the per-level decode state at T-1) against loglinear_fwd alone, medians of
+    `reps` calls each (L2 flushed before every call, outside the events).  The
+    difference is the state kernel; its bytes are the fp32 state it writes plus the
+    block states it reads."""
+    state = torch.empty(cfg.B, cfg.H, cfg.L, cfg.dk, cfg.dv, device=out.device,
+                        dtype=torch.float32)
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts)
+
+    t_pre = timed(lambda: LL.loglinear_prefill(d["q"], d["k"], d["v"], d["log_a"], d["lam"],
+                                               cfg.C, out=out, state=state, workspace=ws))
+    t_fwd = timed(lambda: LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C,
+                                           out=out, workspace=ws))
+    t = cfg.T - 1
+    j = t >> 7
+    state_bytes = cfg.B * cfg.H * cfg.L * cfg.dk * cfg.dv * 4
+    read_bytes = cfg.B * cfg.H * bin(j).count("1") * cfg.dk * cfg.dv * 2
+    t_state = max(t_pre - t_fwd, 1e-9)
+    return {"prefill_us": t_pre * 1e6, "fwd_us": t_fwd * 1e6, "state_kernel_us": t_state * 1e6,
+            "state_bytes": state_bytes + read_bytes,
+            "state_kernel_gbs": (state_bytes + read_bytes) / t_state / 1e9,
+            "note": "state kernel = prefill - forward (medians); bytes = fp32 state written "
+                    "+ bf16 block states read"}
 
 
 def measure_e2e(LL, cfg, x, dev, ws, args):
