@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxTile = 128;   // largest tile of either forward path
+constexpr int kMaxDim = 128;    // d_k, d_v <= 128 (16 x 16 threads of 8 x 8 outputs)
 
 template <typename InT>
 __device__ __forceinline__ float ld(const void* p, int64_t i) {
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
   float* red = sm;                  // [32]
   float* cs = sm + 32;              // [kMaxTile]
   float* w = cs + kMaxTile;         // [kMaxTile] weights of the bucket's positions
-  float* ks = w + kMaxTile;         // [bucket][dk]
+  float* ks = w + kMaxTile;         // [bucket][128] (then v, or the transpose tile)
   const int n = t - t0 + 1;         // positions of tile j up to t
   {
     const float la = (a.log_a && (int)threadIdx.x < n)
@@ -102,36 +103,64 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
   const float cs_t = cs[n - 1];
 
   if (lvl <= lc) {
-    // a range of positions inside tile j: sum_s exp(cs_t - cs_s) k_s v_s^T
+    // a range of positions inside tile j: sum_s exp(cs_t - cs_s) k_s v_s^T, as outer
+    // products accumulated in registers: thread (td, te) owns the 8 x 8 block of rows
+    // [8 td, 8 td + 8) and columns [8 te, 8 te + 8); rows of k (scaled by the decay) and
+    // of v are staged zero-padded to 128 columns.
     const int nb = hi - lo;
-    float* vs = ks + nb * dk;
+    float* vs = ks + nb * kMaxDim;
     for (int i = threadIdx.x; i < nb; i += kThreads) w[i] = __expf(cs_t - cs[lo - t0 + i]);
-    for (int i = threadIdx.x; i < nb * dk; i += kThreads) {
-      const int r = i / dk, d = i - r * dk;
-      ks[i] = ld<InT>(a.k, (((int64_t)b * a.T + lo + r) * a.H + h) * dk + d);
-    }
-    for (int i = threadIdx.x; i < nb * dv; i += kThreads) {
-      const int r = i / dv, e = i - r * dv;
-      vs[i] = ld<InT>(a.v, (((int64_t)b * a.T + lo + r) * a.H + h) * dv + e);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nb * kMaxDim; i += kThreads) {
+      const int r = i / kMaxDim, d = i - r * kMaxDim;
+      const int64_t tok = ((int64_t)b * a.T + lo + r) * a.H + h;
+      ks[i] = d < dk ? w[r] * ld<InT>(a.k, tok * dk + d) : 0.f;
+      vs[i] = d < dv ? ld<InT>(a.v, tok * dv + d) : 0.f;
     }
     __syncthreads();
-    for (int64_t i = threadIdx.x; i < elems; i += kThreads) {
-      const int d = (int)(i / dv), e = (int)(i - (int64_t)d * dv);
-      float acc = 0.f;
-      for (int r = 0; r < nb; ++r) acc = fmaf(w[r] * ks[r * dk + d], vs[r * dv + e], acc);
-      S[i] = acc;
+    const int td = threadIdx.x >> 4, te = threadIdx.x & 15;
+    float acc[8][8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+#pragma unroll
+      for (int y = 0; y < 8; ++y) acc[x][y] = 0.f;
+    for (int r = 0; r < nb; ++r) {
+      const float4* kr = reinterpret_cast<const float4*>(ks + r * kMaxDim + 8 * td);
+      const float4* vr = reinterpret_cast<const float4*>(vs + r * kMaxDim + 8 * te);
+      const float4 k0 = kr[0], k1 = kr[1], v0 = vr[0], v1 = vr[1];
+      const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+      const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int x = 0; x < 8; ++x)
+#pragma unroll
+        for (int y = 0; y < 8; ++y) acc[x][y] = fmaf(kk[x], vv[y], acc[x][y]);
+    }
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const int d = 8 * td + x;
+      if (d >= dk) break;
+      float* row = S + (int64_t)d * dv;
+      if ((dv & 7) == 0 && 8 * te < dv) {  // two aligned 16-byte stores
+        reinterpret_cast<float4*>(row + 8 * te)[0] =
+            make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+        reinterpret_cast<float4*>(row + 8 * te)[1] =
+            make_float4(acc[x][4], acc[x][5], acc[x][6], acc[x][7]);
+      } else {
+#pragma unroll
+        for (int y = 0; y < 8; ++y)
+          if (8 * te + y < dv) row[8 * te + y] = acc[x][y];
+      }
     }
     return;
   }
 
-  // a block of tiles [c - 2^(m-1), c): the block state of slot c, decayed to t
-  const int m = lvl - lc;
+  // a block of 2^(lvl - lc - 1) tiles ending at tile c: the block state of slot c,
+  // decayed to t
   const int c = hi >> lc;
   float D = 0.f;  // sum of the tile log decays over [c, j)
   for (int i = c + (int)threadIdx.x; i < j; i += kThreads) D += a.lg[bh * a.N + i];
   D = block_sum(D, red);
   const float g = __expf(D + cs_t);
-  (void)m;
   if (kTcLayout) {
     const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(
         (c & 1) ? a.U : a.nodes) + (bh * a.N + ((c & 1) ? c - 1 : c)) * elems;
@@ -163,10 +192,10 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
 cudaError_t launch_prefill_state(const FwdArgs& a, bool tc_layout, int in_dtype, float* state,
                                  cudaStream_t s) {
   if (a.C > kMaxTile) return cudaErrorInvalidValue;
+  if (a.dk > kMaxDim || a.dv > kMaxDim) return cudaErrorInvalidValue;
   const int nb_max = a.C / 2 > 1 ? a.C / 2 : 1;  // largest bucket inside a tile
   const size_t smem =
-      sizeof(float) * (32 + 2 * kMaxTile + (size_t)nb_max * (a.dk + a.dv) +
-                       (tc_layout ? 32 * 33 : 0));
+      sizeof(float) * (32 + 2 * kMaxTile + (size_t)nb_max * 2 * kMaxDim + 32 * 33);
   const dim3 grid((unsigned)a.L, (unsigned)(a.B * a.H));
   cudaError_t e = cudaSuccess;
   if (in_dtype == LL_BF16) {
