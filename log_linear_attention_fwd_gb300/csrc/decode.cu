@@ -77,35 +77,50 @@ __global__ void __launch_bounds__(kThreads, kFew == 16 ? 1 : 2) decode_step_kern
     const int n_low = l + 1;
     const int cnt = n_low + plan.n_hi;
     const float lam_m = lam_s[l + 1];
-    for (int r = row0; r < dk; r += row_step) {
-      const int64_t off = (int64_t)r * groups + cg;
-      float4 x[kFew > 0 ? kFew : 1];
+    // Two rows per pass, every load of both in flight before either is used: with 2
+    // CTAs of 256 threads per SM that keeps ~100 KB of state reads outstanding per SM.
+    for (int r2 = row0; r2 < dk; r2 += 2 * row_step) {
+      float4 x2[2][kFew > 0 ? kFew : 1];
 #pragma unroll
-      for (int i = 0; i < kFew; ++i)
-        if (i < cnt) x[i] = __ldcs(S + plan.lv[i] * l4 + off);
-      float4 merged = zero;
+      for (int p2 = 0; p2 < 2; ++p2) {
+        const int r = r2 + p2 * row_step;
+        if (r < dk) {
+          const int64_t off = (int64_t)r * groups + cg;
 #pragma unroll
-      for (int i = 0; i < kFew; ++i)
-        if (i < n_low) merged = f4_add(merged, x[i]);
-      merged = f4_scale(a, merged);
-      const float4 kv = f4_scale(ks[r], vv);
-      __stcs(S + off, kv);
-      __stcs(S + (l + 1) * l4 + off, merged);
-      float4 ro = f4_fma(lam_s[0], kv, f4_scale(lam_m, merged));
-#pragma unroll
-      for (int i = 1; i < kFew; ++i) {
-        if (i < n_low) {
-          __stcs(S + i * l4 + off, zero);
-        } else if (i < cnt) {
-          float4 y = x[i];
-          if (decay) {
-            y = f4_scale(a, y);
-            __stcs(S + plan.lv[i] * l4 + off, y);
-          }
-          ro = f4_fma(lam_s[plan.lv[i]], y, ro);
+          for (int i = 0; i < kFew; ++i)
+            if (i < cnt) x2[p2][i] = __ldcs(S + plan.lv[i] * l4 + off);
         }
       }
-      acc = f4_fma(qs[r], ro, acc);
+#pragma unroll
+      for (int p2 = 0; p2 < 2; ++p2) {
+        const int r = r2 + p2 * row_step;
+        if (r >= dk) break;
+        const int64_t off = (int64_t)r * groups + cg;
+        const float4* x = x2[p2];
+        float4 merged = zero;
+#pragma unroll
+        for (int i = 0; i < kFew; ++i)
+          if (i < n_low) merged = f4_add(merged, x[i]);
+        merged = f4_scale(a, merged);
+        const float4 kv = f4_scale(ks[r], vv);
+        __stcs(S + off, kv);
+        __stcs(S + (l + 1) * l4 + off, merged);
+        float4 ro = f4_fma(lam_s[0], kv, f4_scale(lam_m, merged));
+#pragma unroll
+        for (int i = 1; i < kFew; ++i) {
+          if (i < n_low) {
+            __stcs(S + i * l4 + off, zero);
+          } else if (i < cnt) {
+            float4 y = x[i];
+            if (decay) {
+              y = f4_scale(a, y);
+              __stcs(S + plan.lv[i] * l4 + off, y);
+            }
+            ro = f4_fma(lam_s[plan.lv[i]], y, ro);
+          }
+        }
+        acc = f4_fma(qs[r], ro, acc);
+      }
     }
   } else {
     // any number of levels: same update, one level at a time
