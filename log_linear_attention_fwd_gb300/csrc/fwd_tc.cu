@@ -50,8 +50,8 @@ struct TcParams {
   const float* log_a;
   const float* lam;
   void* out;
-  uint8_t* U;        // [B*H][N] tile states U_i^T, bf16 [d_v][d_k]
-  uint8_t* nodes;    // [B*H][N] block states of the even slots, bf16 [d_v][d_k]
+  uint8_t* U;        // [B*H][N] tile states U_i, bf16 [d_k][d_v]
+  uint8_t* nodes;    // [B*H][N] block states of the even slots, bf16 [d_k][d_v]
   float* lgu;        // [B*H][N] log decay of each tile
   float* nlg;        // [B*H][N] log decay of the block in each even slot
   uint32_t* rdy_u;   // [B*H][N] ready flags of U
@@ -98,8 +98,8 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
 //
 //   1. Q, K, V by TMA; per-row log a and lambda; cs = tile-local prefix sums of log a.
 //   2. S = Q K^T (tcgen05) into TMEM columns 0..127, issued as soon as Q and K land.
-//   3. K rows scaled in place by w_s = exp(lg - cs_s); U^T = V^T (w ⊙ K) into columns
-//      128..255 (the tile's chunk state, d_v x d_k).
+//   3. K rows scaled in place by w_s = exp(lg - cs_s); U = (w ⊙ K)^T V into columns
+//      128..255 (the tile's chunk state, d_k x d_v).
 //   4. (after 5) P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t,s)] on the causal half, bf16
 //      into the K buffer; O = P V into columns 0..127.
 //   5. Right after the state MMA (before P): U_j is published (staged bf16 in the Q
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
                       const __grid_constant__ CUtensorMap tmNode, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* Qb = smem + FSmem::kQ;    // Q, then U^T in bf16, then Q again, then the output
+  uint8_t* Qb = smem + FSmem::kQ;    // Q, then U in bf16, then Q again, then the output
   uint8_t* Kb = smem + FSmem::kK;    // K, then w ⊙ K, then P, then block states
   uint8_t* Vb = smem + FSmem::kV;    // V, then block states
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FSmem::kBars);
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
 
-  // ---- U^T = V^T (w ⊙ K): K rows scaled in place (S no longer reads K)
+  // ---- U = (w ⊙ K)^T V, d_k x d_v: K rows scaled in place (S no longer reads K)
   if (all_ok) scale_half_row_inplace(Kb, r, hh, row_live ? expf(lg - cs) : 0.f);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -338,8 +338,8 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     const uint32_t va = smem_u32(Vb), ka = smem_u32(Kb);
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk)
-      mma_bf16(tmem + 128, smem_desc_sw128(va + kk * 2048, kPanel, 1024),
-               smem_desc_sw128(ka + kk * 2048, kPanel, 1024), idesc, kk > 0);
+      mma_bf16(tmem + 128, smem_desc_sw128(ka + kk * 2048, kPanel, 1024),
+               smem_desc_sw128(va + kk * 2048, kPanel, 1024), idesc, kk > 0);
     mma_commit(bar_u);
   }
   __syncwarp();
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
 
   // ---- publish U_j (staged bf16 in Qb, which S no longer reads, then stored coalesced)
   // and, for odd j, form the block state of slot j+1 and publish it; then Q comes back
-  // by TMA for the levels.  Published states are row-major [d_v][d_k] bf16; thread tid
+  // by TMA for the levels.  Published states are row-major [d_k][d_v] bf16; thread tid
   // moves the 16-byte pieces q = it * 256 + tid.  This runs even after an error, so that
   // no reader waits for a flag that is never raised.
   const uint8_t* Ug = p.U + bh * N * kOperand;
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint32_t* rdy_u = p.rdy_u + bh * N;
   uint32_t* rdy_n = p.rdy_n + bh * N;
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {  // U^T row r, columns [64 hh, 64 hh + 64) -> Qb
+  for (int c = 0; c < 2; ++c) {  // U row r (d_k), columns [64 hh, 64 hh + 64) (d_v) -> Qb
     float v[32];
     tmem_ld32(tmem + lane_base + 128 + 64 * hh + 32 * c, v);
     put_row32_bf16(Qb, r, 2 * hh + c, v);
@@ -578,13 +578,14 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       }
       if (go) {
         tc_fence_after();
-        constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+        // A = Q (K-major), B = the block state [d_k][d_v] (MN-major, like V in P V)
+        constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
         const uint32_t qa = smem_u32(Qb), sa = smem_u32((k & 1) ? Kb : Vb);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
           mma_bf16(tmem + (k & 1) * 128, smem_desc_sw128(qa + off, 16, 1024),
-                   smem_desc_sw128(sa + off, 16, 1024), idesc, kk > 0);
+                   smem_desc_sw128(sa + kk * 2048, kPanel, 1024), idesc, kk > 0);
         }
         mma_commit(&bar_lvl[k & 1]);
       }

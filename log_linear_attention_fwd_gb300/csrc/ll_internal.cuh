@@ -60,7 +60,7 @@ struct FwdArgs {
   int C, lc;  // tile length and log2(tile)
   int N;      // tiles per (b, h)
   // workspace
-  void* U;        // [B*H][N][dk*dv] chunk states (fp32 on CUDA cores, bf16 on tensor cores)
+  void* U;        // [B*H][N][dk][dv] chunk states (fp32 on CUDA cores, bf16 on tensor cores)
   void* nodes;    // [B*H][N][dk*dv] Fenwick block states, slot c = first reader chunk
   float* lg;      // [B*H][N] log decay of each whole chunk
   // tensor cores only (block states published between CTAs of one launch):
@@ -102,7 +102,7 @@ cudaError_t launch_simt_forward(const FwdArgs& a, int in_dtype, int out_dtype, c
 cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev);
 cudaError_t launch_level_scan(const FwdArgs& a, cudaStream_t s);
 // The decode state at position T-1 from a completed forward's workspace (tc_layout: the
-// tensor-core path's bf16 [d_v][d_k] block states).
+// tensor-core path's bf16 block states; both paths store them [d_k][d_v]).
 cudaError_t launch_prefill_state(const FwdArgs& a, bool tc_layout, int in_dtype, float* state,
                                  cudaStream_t s);
 // Reads and clears the tensor-core path's device error word (synchronises the stream).

@@ -56,8 +56,8 @@ __device__ float block_sum(float x, float* sh) {
   return s;
 }
 
-// tc_layout: block states are bf16 [d_v][d_k] (tensor-core path; odd slots are U_{c-1});
-// otherwise fp32 [d_k][d_v] for every slot.
+// tc_layout: block states are bf16 (tensor-core path; odd slots are U_{c-1}); otherwise
+// fp32 for every slot.  Both are row-major [d_k][d_v], the layout of the state.
 template <typename InT, bool kTcLayout>
 __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, float* state) {
   extern __shared__ float sm[];
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
   float* red = sm;                  // [32]
   float* cs = sm + 32;              // [kMaxTile]
   float* w = cs + kMaxTile;         // [kMaxTile] weights of the bucket's positions
-  float* ks = w + kMaxTile;         // [bucket][128] (then v, or the transpose tile)
+  float* ks = w + kMaxTile;         // [bucket][128], then v
   const int n = t - t0 + 1;         // positions of tile j up to t
   {
     const float la = (a.log_a && (int)threadIdx.x < n)
@@ -164,23 +164,7 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
   if (kTcLayout) {
     const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(
         (c & 1) ? a.U : a.nodes) + (bh * a.N + ((c & 1) ? c - 1 : c)) * elems;
-    // [d_v][d_k] -> [d_k][d_v] through 32 x 32 shared tiles
-    float* tt = ks;  // [32][33]
-    for (int e0 = 0; e0 < dv; e0 += 32)
-      for (int d0 = 0; d0 < dk; d0 += 32) {
-        for (int i = threadIdx.x; i < 32 * 32; i += kThreads) {
-          const int er = i >> 5, dc = i & 31;
-          if (e0 + er < dv && d0 + dc < dk)
-            tt[er * 33 + dc] = __bfloat162float(src[(int64_t)(e0 + er) * dk + d0 + dc]);
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < 32 * 32; i += kThreads) {
-          const int dr = i >> 5, ec = i & 31;
-          if (d0 + dr < dk && e0 + ec < dv)
-            S[(int64_t)(d0 + dr) * dv + e0 + ec] = g * tt[ec * 33 + dr];
-        }
-        __syncthreads();
-      }
+    for (int64_t i = threadIdx.x; i < elems; i += kThreads) S[i] = g * __bfloat162float(src[i]);
   } else {
     const float* src = reinterpret_cast<const float*>(a.nodes) + (bh * a.N + c) * elems;
     for (int64_t i = threadIdx.x; i < elems; i += kThreads) S[i] = g * src[i];
@@ -195,7 +179,7 @@ cudaError_t launch_prefill_state(const FwdArgs& a, bool tc_layout, int in_dtype,
   if (a.dk > kMaxDim || a.dv > kMaxDim) return cudaErrorInvalidValue;
   const int nb_max = a.C / 2 > 1 ? a.C / 2 : 1;  // largest bucket inside a tile
   const size_t smem =
-      sizeof(float) * (32 + 2 * kMaxTile + (size_t)nb_max * 2 * kMaxDim + 32 * 33);
+      sizeof(float) * (32 + 2 * kMaxTile + (size_t)nb_max * 2 * kMaxDim);
   const dim3 grid((unsigned)a.L, (unsigned)(a.B * a.H));
   cudaError_t e = cudaSuccess;
   if (in_dtype == LL_BF16) {
