@@ -57,7 +57,7 @@ typedef enum {
 typedef enum { LL_F32 = 0, LL_BF16 = 1 } ll_dtype;
 
 /* Kernel path of the forward.  AUTO takes the tensor-core path when it applies (bf16
- * inputs, dk = dv = 128) and the fp32 CUDA-core path otherwise. */
+ * inputs, dk = 128, dv = 64 or 128) and the fp32 CUDA-core path otherwise. */
 typedef enum { LL_PATH_AUTO = 0, LL_PATH_SIMT = 1, LL_PATH_TC = 2 } ll_path;
 
 /* Library version, (major << 16) | minor. */
@@ -103,7 +103,7 @@ LL_API int loglinear_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t
  *   workspace: device scratch of at least loglinear_fwd_workspace_size() bytes, 256-byte
  *           aligned.  Two calls that run concurrently need two workspaces.
  * Errors: LL_ERR_INVALID, LL_ERR_SHAPE, LL_ERR_DTYPE, LL_ERR_UNSUPPORTED (dk or dv > 128;
- * LL_PATH_TC forced on a shape other than bf16 with dk = dv = 128), LL_ERR_WORKSPACE, LL_ERR_ALIGN (tensor-core
+ * LL_PATH_TC forced on a shape other than bf16 with dk = 128, dv in {64, 128}), LL_ERR_WORKSPACE, LL_ERR_ALIGN (tensor-core
  * path: q, k, v, out not 16-byte aligned), LL_ERR_CUDA.
  */
 LL_API int loglinear_fwd(const void* q, const void* k, const void* v, const float* log_a,
@@ -210,7 +210,7 @@ LL_API int loglinear_fwd_noalloc(const void* q, const void* k, const void* v,
  * 分解): writes levels[t * T + s] (int8, device) for 0 <= s, t < T: the Fenwick level the
  * given path assigns to the pair (query t, source s) through its intra-chunk formula or
  * its inter-chunk block pairing, and -1 for s > t.  chunk and path as in loglinear_fwd
- * (path AUTO resolves as for bf16, dk = dv = 128).  T <= 16384.
+ * (path AUTO resolves as for bf16, dk = dv = 128; the level map does not depend on dv).  T <= 16384.
  */
 LL_API int loglinear_debug_level_map(int64_t T, int chunk, int path, int8_t* levels,
                               ll_stream_t stream);

@@ -1,5 +1,6 @@
 // Forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), bf16 inputs with
-// fp32 accumulation, d_k = d_v = 128, 128-token tiles (the M = 128 datapath of one SM).
+// fp32 accumulation, d_k = 128, d_v = 64 or 128, 128-token tiles (the M = 128 datapath of
+// one SM).
 //
 // The chunked two-stage algorithm (page "论文阅读：Log-Linear Attention", sections 矩阵分解
 // and 两阶段计算; page "算力终结者来了！…", section 高效训练算法) with the tile as the chunk, in
@@ -11,7 +12,7 @@
 // With 128-token tiles the chunk-pair level log2(C)+1 of a requested C = 64 lies inside a
 // tile and is taken in the dense masked product; the sum is the same.
 //
-// Shared-memory tiles are 128 rows x 128 bf16 stored as two 64-column panels with the
+// Shared-memory tiles are 128 rows x 64 or 128 bf16 stored as 64-column panels with the
 // 128-byte swizzle TMA produces; K-major operands (Q, K, P, block states) and MN-major
 // ones (V as the B of P V; V and K in the state GEMM) are described to tcgen05 with the
 // matching descriptors.  Every wait (mbarriers, block-state flags) is bounded (see
@@ -37,7 +38,7 @@ namespace {
 using namespace tc;
 
 constexpr int kTile = 128;                  // tokens per tile (= MMA M)
-constexpr int kD = 128;                     // d_k = d_v
+constexpr int kD = 128;                     // d_k; d_v is the kernel's template argument
 constexpr int kPanel = kTile * 64 * 2;      // one [128][64] bf16 panel: 16 KiB
 constexpr int kOperand = 2 * kPanel;        // a 128 x 128 bf16 tile: 32 KiB
 constexpr int kLamStride = 9;               // intra lambdas per row in smem (levels 0..7)
@@ -90,7 +91,7 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
 // ------------------------------------------------------------------ the forward kernel
 //
 // One CTA per 128-token tile; 8 warps: warps w and w+4 share TMEM lane quarter w mod 4
-// (tile rows 32(w mod 4)..+31) and split its columns (64 each) and its P chunks.
+// (tile rows 32(w mod 4)..+31) and split its d_v columns (half each) and its P chunks.
 //
 // Tiles are taken in ticket order (an atomic counter; tile j of every (b,h) before tile
 // j+1), so a CTA only waits for tiles with smaller tickets: those CTAs are resident or
@@ -99,14 +100,15 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
 //   1. Q, K, V by TMA; per-row log a and lambda; cs = tile-local prefix sums of log a.
 //   2. S = Q K^T (tcgen05) into TMEM columns 0..127, issued as soon as Q and K land.
 //   3. K rows scaled in place by w_s = exp(lg - cs_s); U = (w ⊙ K)^T V into columns
-//      128..255 (the tile's chunk state, d_k x d_v).
+//      128..128+d_v (the tile's chunk state, d_k x d_v).
 //   4. (after 5) P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t,s)] on the causal half, bf16
-//      into the K buffer; O = P V into columns 0..127.
+//      into the K buffer; O = P V into columns 0..d_v.
 //   5. Right after the state MMA (before P): U_j is published (staged bf16 in the Q
 //      buffer, stored coalesced); for odd j the CTA then forms the block state of slot
 //      j+1 (below) and publishes it; Q is loaded again by TMA for the levels.
 //   6. For every set bit m-1 of j, in increasing m: the block state of slot c_m by TMA
-//      into shared memory (two buffers), MMA Q Tot into one of two TMEM buffers, and the
+//      into shared memory (two buffers), MMA Q Tot into one of two TMEM buffers (columns
+//      0.. and 128..), and the
 //      previous level's product added to O with the row weights
 //      lambda[t, 7+m] exp(cs_t + D_m).  D_m, the log decay from the block's end to the
 //      tile's start, is the sum of the log decays of the lower levels' blocks, which
@@ -179,16 +181,26 @@ __device__ __forceinline__ void scale_half_row_inplace(uint8_t* buf, int r, int 
   }
 }
 
-// Pieces of a 128 x 128 bf16 state: piece q (16 bytes) is row q / 16, columns
-// 8 (q mod 16) .. +7 of the row-major matrix; each thread of the CTA moves the pieces
-// it * 256 + tid.  piece_offset is where a piece sits in a swizzled K-major smem tile.
-constexpr int kStatePieces = kOperand / 16 / 256;  // 8 per thread
+// Pieces of a 128 x DV bf16 state: piece q (16 bytes) is row q / (DV/8), columns
+// 8 (q mod DV/8) .. +7 of the row-major matrix; each thread of the CTA moves the pieces
+// it * 256 + tid.  piece_offset is where a piece sits in a swizzled smem tile of 64-column
+// panels.
+template <int DV>
+struct Dv {
+  static constexpr int kStateBytes = kD * DV * 2;             // one published state
+  static constexpr int kVBytes = kTile * DV * 2;              // one V (or output) tile
+  static constexpr int kPanels = DV / 64;                     // 64-column panels of d_v
+  static constexpr int kStatePieces = kStateBytes / 16 / 256; // per thread: 8 or 4
+  static constexpr int kHalf = DV / 2;                        // d_v columns per thread
+};
 
-__device__ __forceinline__ uint32_t piece_offset(int q) {
-  const int row = q >> 4, c16 = q & 15;
-  return (uint32_t)((c16 >> 3) * kPanel) + sw128_offset(row, c16 & 7);
+template <int DV>
+__device__ __forceinline__ uint32_t piece_offset(uint32_t q) {
+  const uint32_t row = q / (DV / 8), c16 = q % (DV / 8);
+  return (c16 >> 3) * kPanel + sw128_offset(row, c16 & 7);
 }
 
+template <int DV>
 __global__ void __launch_bounds__(kThreadsF, 2)
     tc_forward_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -201,6 +213,8 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint8_t* Qb = smem + FSmem::kQ;    // Q, then U in bf16, then Q again, then the output
   uint8_t* Kb = smem + FSmem::kK;    // K, then w ⊙ K, then P, then block states
   uint8_t* Vb = smem + FSmem::kV;    // V, then block states
+  using G = Dv<DV>;
+  constexpr int kStatePieces = G::kStatePieces;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FSmem::kBars);
   uint64_t* bar_load = &bars[0];
   uint64_t* bar_s = &bars[1];
@@ -261,13 +275,14 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   const bool row_live = r < n;
   bool landed = true;  // thread 0: Q, K and V arrived
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar_load, 3 * kOperand);
+    mbar_arrive_expect_tx(bar_load, 2 * kOperand + G::kVBytes);
     tma_load_4d(&tmQ, bar_load, Qb, 0, h, t0, b);
     tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, h, t0, b);
     tma_load_4d(&tmK, bar_load, Kb, 0, h, t0, b);
     tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, h, t0, b);
-    tma_load_4d(&tmV, bar_load, Vb, 0, h, t0, b);
-    tma_load_4d(&tmV, bar_load, Vb + kPanel, 64, h, t0, b);
+#pragma unroll
+    for (int pv = 0; pv < G::kPanels; ++pv)
+      tma_load_4d(&tmV, bar_load, Vb + pv * kPanel, 64 * pv, h, t0, b);
   }
   if (tid == 64 && h == 0 && j + 2 < N) {  // warm L2 with tile j+2's log a and lambda (all heads)
     const int64_t tok0 = (int64_t)b * p.T + (int64_t)(j + 2) * kTile;
@@ -334,7 +349,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   __syncthreads();
   if (all_ok && tid == 0) {
     tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16(128, 128, /*A MN-major*/ 1, /*B MN-major*/ 1);
+    constexpr uint32_t idesc = idesc_bf16(128, DV, /*A MN-major*/ 1, /*B MN-major*/ 1);
     const uint32_t va = smem_u32(Vb), ka = smem_u32(Kb);
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk)
@@ -353,17 +368,17 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   // by TMA for the levels.  Published states are row-major [d_k][d_v] bf16; thread tid
   // moves the 16-byte pieces q = it * 256 + tid.  This runs even after an error, so that
   // no reader waits for a flag that is never raised.
-  const uint8_t* Ug = p.U + bh * N * kOperand;
-  uint8_t* nodes = p.nodes + bh * N * kOperand;
+  const uint8_t* Ug = p.U + bh * N * G::kStateBytes;
+  uint8_t* nodes = p.nodes + bh * N * G::kStateBytes;
   const float* lgu = p.lgu + bh * N;
   float* nlg = p.nlg + bh * N;
   uint32_t* rdy_u = p.rdy_u + bh * N;
   uint32_t* rdy_n = p.rdy_n + bh * N;
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {  // U row r (d_k), columns [64 hh, 64 hh + 64) (d_v) -> Qb
+  for (int c = 0; c < G::kPanels; ++c) {  // U row r (d_k), this thread's half of d_v -> Qb
     float v[32];
-    tmem_ld32(tmem + lane_base + 128 + 64 * hh + 32 * c, v);
-    put_row32_bf16(Qb, r, 2 * hh + c, v);
+    tmem_ld32(tmem + lane_base + 128 + G::kHalf * hh + 32 * c, v);
+    put_row32_bf16(Qb, r, G::kPanels * hh + c, v);
   }
   __syncthreads();
   const bool forms = (j & 1) && j + 1 < N;  // odd j forms the block state of slot j+1
@@ -371,8 +386,8 @@ __global__ void __launch_bounds__(kThreadsF, 2)
 #pragma unroll
   for (int it = 0; it < kStatePieces; ++it) {
     const int q = it * kThreadsF + tid;
-    const uint4 w = *reinterpret_cast<const uint4*>(Qb + piece_offset(q));
-    reinterpret_cast<uint4*>(const_cast<uint8_t*>(Ug) + (int64_t)j * kOperand)[q] = w;
+    const uint4 w = *reinterpret_cast<const uint4*>(Qb + piece_offset<DV>(q));
+    reinterpret_cast<uint4*>(const_cast<uint8_t*>(Ug) + (int64_t)j * G::kStateBytes)[q] = w;
     const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -397,7 +412,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     for (int k = 1; k <= zc; ++k) {  // k = 1: U_{j-1}; k >= 2: slot c - 2^(k-1)
       const int cs_k = c - (1 << (k - 1));
       const uint4* src = reinterpret_cast<const uint4*>(
-          k == 1 ? Ug + (int64_t)(j - 1) * kOperand : nodes + (int64_t)cs_k * kOperand);
+          k == 1 ? Ug + (int64_t)(j - 1) * G::kStateBytes : nodes + (int64_t)cs_k * G::kStateBytes);
       const float L = __ldcg(k == 1 ? &lgu[j - 1] : &nlg[cs_k]);
       const float g = __expf(G);
       uint4 y[kStatePieces];
@@ -417,7 +432,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     }
 #pragma unroll
     for (int it = 0; it < kStatePieces; ++it)
-      reinterpret_cast<uint4*>(nodes + (int64_t)c * kOperand)[it * kThreadsF + tid] =
+      reinterpret_cast<uint4*>(nodes + (int64_t)c * G::kStateBytes)[it * kThreadsF + tid] =
           make_uint4(pack_bf16(acc[8 * it], acc[8 * it + 1]), pack_bf16(acc[8 * it + 2], acc[8 * it + 3]),
                      pack_bf16(acc[8 * it + 4], acc[8 * it + 5]),
                      pack_bf16(acc[8 * it + 6], acc[8 * it + 7]));
@@ -482,10 +497,10 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   fence_proxy_async_smem();
   tc_fence_before();
   all_ok = __syncthreads_and(ok);
-  // ---- O = P V into columns 0..127 (V MN-major as B)
+  // ---- O = P V into columns 0..DV (V MN-major as B)
   if (all_ok && tid == 0) {
     tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+    constexpr uint32_t idesc = idesc_bf16(128, DV, 0, 1);
     const uint32_t pa = smem_u32(Kb), va = smem_u32(Vb);
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -528,9 +543,10 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       uint8_t* dst = (k & 1) ? Kb : Vb;
       const bool is_u = (my_c & 1) != 0;
       const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
-      mbar_arrive_expect_tx(&bar_node[k & 1], kOperand);
-      tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[k & 1], dst, 0, row0);
-      tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[k & 1], dst + kPanel, 64, row0);
+      mbar_arrive_expect_tx(&bar_node[k & 1], G::kStateBytes);
+#pragma unroll
+      for (int pv = 0; pv < G::kPanels; ++pv)
+        tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[k & 1], dst + pv * kPanel, 64 * pv, row0);
     }
   };
   if (all_ok) {  // Kb (U staging) and Vb are free
@@ -539,14 +555,14 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   }
   __syncwarp();
 
-  // ---- O from TMEM into registers: this thread's half row, columns [64 hh, 64 hh + 64)
-  float o[kD / 2];
+  // ---- O from TMEM into registers: this thread's half row, columns [DV/2 hh, +DV/2)
+  float o[G::kHalf];
 #pragma unroll
-  for (int q = 0; q < kD / 2; ++q) o[q] = 0.f;
-  const uint32_t col0 = 64u * hh;
+  for (int q = 0; q < G::kHalf; ++q) o[q] = 0.f;
+  const uint32_t col0 = (uint32_t)G::kHalf * hh;
   if (all_ok) {
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < G::kPanels; ++c) {
       float v[32];
       tmem_ld32(tmem + lane_base + col0 + c * 32, v);
 #pragma unroll
@@ -558,7 +574,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
 
   // ---- inter-chunk levels, without block barriers.  Level k (the k-th set bit of j,
   // from the lowest) uses shared buffer (k odd ? Kb : Vb) and TMEM columns
-  // [128 (k&1), +128).  Thread 0 issues MMA k once its block state has landed
+  // [128 (k&1), +DV).  Thread 0 issues MMA k once its block state has landed
   // (bar_node[k&1]) and every warp has added level k-2 to O (bar_free[k&1]); each warp
   // adds level k-1 to O once MMA k-1 is done (bar_lvl), then releases that TMEM buffer.
   // The load of level k+1 starts as soon as MMA k-1 is done with its shared buffer
@@ -579,7 +595,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       if (go) {
         tc_fence_after();
         // A = Q (K-major), B = the block state [d_k][d_v] (MN-major, like V in P V)
-        constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+        constexpr uint32_t idesc = idesc_bf16(128, DV, 0, 1);
         const uint32_t qa = smem_u32(Qb), sa = smem_u32((k & 1) ? Kb : Vb);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -605,7 +621,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       const float wr = lamx[(k - 1) * kTile + r] * __expf(cs + D);
       D += nl_s[k - 1];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < G::kPanels; ++c) {
         float v[32];
         tmem_ld32(tmem + lane_base + bf * 128 + col0 + c * 32, v);
 #pragma unroll
@@ -623,20 +639,21 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     if (p.out_f32) {
       if (row_live) {
         float4* dst =
-            reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * kD + col0);
+            reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * DV + col0);
 #pragma unroll
-        for (int q = 0; q < kD / 8; ++q)
+        for (int q = 0; q < G::kHalf / 4; ++q)
           dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
       }
     } else {
       // no MMA reads Q any more: stage the bf16 tile there and store it with TMA
 #pragma unroll
-      for (int c = 0; c < 2; ++c) put_row32_bf16(Qb, r, 2 * hh + c, o + c * 32);
+      for (int c = 0; c < G::kPanels; ++c) put_row32_bf16(Qb, r, G::kPanels * hh + c, o + c * 32);
       fence_proxy_async_smem();
       __syncthreads();
       if (tid == 0) {
-        tma_store_4d(&tmOut, Qb, 0, h, t0, b);
-        tma_store_4d(&tmOut, Qb + kPanel, 64, h, t0, b);
+#pragma unroll
+        for (int pv = 0; pv < G::kPanels; ++pv)
+          tma_store_4d(&tmOut, Qb + pv * kPanel, 64 * pv, h, t0, b);
         tma_store_commit();
         tma_store_wait_read();
       }
@@ -666,14 +683,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [B, T, H, 128] bf16, boxes of 128 tokens x 64 features of one (b, h); rows past T read
-// as 0 and are not written.
-bool make_tokens_map(CUtensorMap* m, const void* base, int B, int T, int H) {
+// [B, T, H, width] bf16 (width 64 or 128), boxes of 128 tokens x 64 features of one
+// (b, h); rows past T read as 0 and are not written.
+bool make_tokens_map(CUtensorMap* m, const void* base, int B, int T, int H, int width) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2,
-                           (cuuint64_t)T * H * kD * 2};
+  cuuint64_t dims[4] = {(cuuint64_t)width, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)width * 2, (cuuint64_t)H * width * 2,
+                           (cuuint64_t)T * H * width * 2};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
@@ -681,13 +698,13 @@ bool make_tokens_map(CUtensorMap* m, const void* base, int B, int T, int H) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][128] bf16 matrices (published tile and block states), boxes of 128 rows x 64
-// columns with the 128-byte swizzle.
-bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows) {
+// [rows][width] bf16 matrices (published tile and block states, width = d_v), boxes of
+// 128 rows x 64 columns with the 128-byte swizzle.
+bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows, int width) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)width * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)kTile};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
@@ -698,16 +715,20 @@ bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows) {
 }  // namespace
 
 bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int /*chunk*/) {
-  return in_dtype == LL_BF16 && dk == kD && dv == kD;
+  return in_dtype == LL_BF16 && dk == kD && (dv == 64 || dv == 128);
 }
 
 cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev) {
   const int64_t rows = (int64_t)a.B * a.H * a.N * kD;  // TMA row coordinates are int32
   if (rows > INT32_MAX) return cudaErrorInvalidValue;
+  if (a.dk != kD || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
+  const int dv = (int)a.dv;
   CUtensorMap tmQ, tmK, tmV, tmOut, tmU, tmNode;
-  if (!make_tokens_map(&tmQ, a.q, a.B, a.T, a.H) || !make_tokens_map(&tmK, a.k, a.B, a.T, a.H) ||
-      !make_tokens_map(&tmV, a.v, a.B, a.T, a.H) || !make_tokens_map(&tmOut, a.out, a.B, a.T, a.H) ||
-      !make_rows_map(&tmU, a.U, rows) || !make_rows_map(&tmNode, a.nodes, rows))
+  if (!make_tokens_map(&tmQ, a.q, a.B, a.T, a.H, kD) ||
+      !make_tokens_map(&tmK, a.k, a.B, a.T, a.H, kD) ||
+      !make_tokens_map(&tmV, a.v, a.B, a.T, a.H, dv) ||
+      !make_tokens_map(&tmOut, a.out, a.B, a.T, a.H, dv) || !make_rows_map(&tmU, a.U, rows, dv) ||
+      !make_rows_map(&tmNode, a.nodes, rows, dv))
     return cudaErrorInvalidValue;
   TcParams p;
   p.B = a.B; p.T = a.T; p.H = a.H; p.L = a.L; p.N = a.N;
@@ -725,8 +746,13 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(tc_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(tc_forward_kernel<128>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem_fused(kMaxChunkLevels - 1));
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(tc_forward_kernel<64>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem_fused(kMaxChunkLevels - 1));
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles = (int64_t)a.B * a.H * a.N;
@@ -736,8 +762,12 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   if ((e = cudaMemsetAsync(a.rdy_u, 0, sizeof(uint32_t) * (size_t)(2 * tiles + 1), s)) !=
       cudaSuccess)
     return e;
-  tc_forward_kernel<<<dim3((unsigned)tiles), kThreadsF, smem_fused(levels), s>>>(tmQ, tmK, tmV,
-                                                                               tmOut, tmU, tmNode, p);
+  if (dv == 128)
+    tc_forward_kernel<128><<<dim3((unsigned)tiles), kThreadsF, smem_fused(levels), s>>>(
+        tmQ, tmK, tmV, tmOut, tmU, tmNode, p);
+  else
+    tc_forward_kernel<64><<<dim3((unsigned)tiles), kThreadsF, smem_fused(levels), s>>>(
+        tmQ, tmK, tmV, tmOut, tmU, tmNode, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   return ev ? ev->finish(s) : cudaSuccess;

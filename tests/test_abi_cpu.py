@@ -112,6 +112,9 @@ def test_workspace_size_and_paths(L):
     assert L.resolve_path(128, 128, 64, L.LL_BF16) == "tc"
     assert L.resolve_path(128, 128, 128, L.LL_BF16) == "tc"
     assert L.resolve_path(128, 128, 256, L.LL_BF16) == "tc"
+    assert L.resolve_path(128, 64, 64, L.LL_BF16) == "tc"      # the d_v = 64 instance
+    assert L.resolve_path(128, 96, 64, L.LL_BF16) == "simt"
+    assert L.resolve_path(64, 128, 64, L.LL_BF16) == "simt"
     assert L.resolve_path(64, 64, 256, L.LL_F32) == "simt"
     # the fp32 path tiles at min(C, 64): C = 256 needs the workspace of C = 64
     assert L.fwd_workspace_size(1, 1000, 2, 16, 16, 256, L.LL_F32) == \

@@ -152,19 +152,22 @@ def test_onehot_lambda_bit_exact(LL, path, C, T, dtype):
 # ------------------------------------------------------------------ tensor-core path
 
 
-@pytest.mark.parametrize("T,C,decay", [(128, 64, True), (300, 64, True), (1000, 128, True),
-                                       (2125, 64, True), (4096, 64, False), (77, 64, True)])
-def test_tc_path_matches_oracle(LL, T, C, decay):
+@pytest.mark.parametrize("T,C,decay,dv", [(128, 64, True, 128), (300, 64, True, 128),
+                                          (1000, 128, True, 128), (2125, 64, True, 128),
+                                          (4096, 64, False, 128), (77, 64, True, 128),
+                                          (77, 64, True, 64), (1000, 64, True, 64),
+                                          (2125, 64, True, 64), (4096, 64, False, 64)])
+def test_tc_path_matches_oracle(LL, T, C, decay, dv):
     L = (T - 1).bit_length() + 1
-    cfg = W.FwdConfig("tc", 2, 3, T, 128, 128, C, L, "bf16", decay, "softplus", seed=T + C)
+    cfg = W.FwdConfig("tc", 2, 3, T, 128, dv, C, L, "bf16", decay, "softplus", seed=T + C + dv)
     x = W.make_fwd_inputs(cfg)
-    assert LL.resolve_path(128, 128, C, 1) == "tc"
+    assert LL.resolve_path(128, dv, C, 1) == "tc"
     want = oracle_fwd(x)
     got = run(LL, x, C, path="tc")
     got32 = run(LL, x, C, path="tc", out_dtype=torch.float32)
     assert LL.device_error() == 0
     e16, e32 = rel_l2(got, want), rel_l2(got32, want)
-    print(f"tc T={T} C={C}: rel_l2 bf16-out={e16:.3e} f32-out={e32:.3e} "
+    print(f"tc T={T} C={C} dv={dv}: rel_l2 bf16-out={e16:.3e} f32-out={e32:.3e} "
           f"max_abs={max_abs(got32, want):.3e}")
     assert e16 <= TOL_BF16 and e32 <= TOL_BF16
 
@@ -175,25 +178,25 @@ def test_tc_level_map_bit_exact(LL):
         assert np.array_equal(got, oracle.level_matrix(T)), T
 
 
-@pytest.mark.parametrize("T", [256, 1151])
-def test_tc_onehot_lambda_bit_exact(LL, T):
+@pytest.mark.parametrize("T,dv", [(256, 128), (1151, 128), (1151, 64)])
+def test_tc_onehot_lambda_bit_exact(LL, T, dv):
     """Integer inputs that stay exact through bf16 states: the tensor-core result must
     equal the oracle bit for bit at every level, intra-tile and inter-tile."""
     L = (T - 1).bit_length() + 1
     for lvl in range(L):
-        x = W.make_sparse_int_inputs(1, T, 2, 128, L, lvl, seed=lvl)
+        x = W.make_sparse_int_inputs(1, T, 2, 128, L, lvl, seed=lvl, dv=dv)
         got = run(LL, x, 64, path="tc", out_dtype=torch.float32)
         want = oracle_fwd(x)
         assert np.array_equal(got.double().numpy(), want), lvl
     assert LL.device_error() == 0
 
 
-@pytest.mark.parametrize("T", [40000])
-def test_tc_many_tiles_sampled(LL, T):
+@pytest.mark.parametrize("T,dv", [(40000, 128), (40000, 64)])
+def test_tc_many_tiles_sampled(LL, T, dv):
     """A deep block tree (313 tiles, not a power of two): the block states of every level
     are merged across many CTAs; sampled rows of every head against the oracle."""
     L = (T - 1).bit_length() + 1
-    cfg = W.FwdConfig("tc_deep", 1, 2, T, 128, 128, 64, L, "bf16", True, "softplus", seed=11)
+    cfg = W.FwdConfig("tc_deep", 1, 2, T, 128, dv, 64, L, "bf16", True, "softplus", seed=11)
     x = W.make_fwd_inputs(cfg)
     got = run(LL, x, 64, path="tc", out_dtype=torch.float32)
     assert LL.device_error() == 0

@@ -57,13 +57,14 @@ def test_prefill_state_simt(LL, T, C):
     print(f"simt T={T}: state rel_l2={err:.2e}")
 
 
-@pytest.mark.parametrize("T", [1, 128, 300, 1000, 2049])
-def test_prefill_state_tc(LL, T):
+@pytest.mark.parametrize("T,dv", [(1, 128), (128, 128), (300, 128), (1000, 128), (2049, 128),
+                                  (1, 64), (300, 64), (2049, 64)])
+def test_prefill_state_tc(LL, T, dv):
     L = max((T - 1).bit_length() + 1, 1)
-    cfg = W.FwdConfig("p", 2, 3, T, 128, 128, 64, L, "bf16", True, "softplus", seed=T + 5)
+    cfg = W.FwdConfig("p", 2, 3, T, 128, dv, 64, L, "bf16", True, "softplus", seed=T + 5)
     x = W.make_fwd_inputs(cfg)
     d = cuda(x)
-    assert LL.resolve_path(128, 128, 64, 1) == "tc"
+    assert LL.resolve_path(128, dv, 64, 1) == "tc"
     out, state = LL.loglinear_prefill(d["q"], d["k"], d["v"], d["log_a"], d["lam"], 64, path="tc")
     torch.cuda.synchronize()
     assert LL.device_error() == 0
@@ -71,13 +72,15 @@ def test_prefill_state_tc(LL, T):
     print(f"tc T={T}: state rel_l2={err:.2e}")
 
 
-@pytest.mark.parametrize("path,T,dk,dtype", [("simt", 300, 16, "f32"), ("tc", 1151, 128, "bf16")])
-def test_decode_continues_from_prefill(LL, path, T, dk, dtype):
+@pytest.mark.parametrize("path,T,dk,dv,dtype", [("simt", 300, 16, 16, "f32"),
+                                                ("tc", 1151, 128, 128, "bf16"),
+                                                ("tc", 1151, 128, 64, "bf16")])
+def test_decode_continues_from_prefill(LL, path, T, dk, dv, dtype):
     """Prefill T positions, then decode positions T..T+n-1 from the handed-over state; the
     outputs must match the direct form over the whole T+n sequence."""
     n = 6
     L = (T + n - 1).bit_length() + 1
-    cfg = W.FwdConfig("pd", 2, 2, T + n, dk, dk, 64, L, dtype, True, "softplus", seed=11)
+    cfg = W.FwdConfig("pd", 2, 2, T + n, dk, dv, 64, L, dtype, True, "softplus", seed=11)
     x = W.make_fwd_inputs(cfg)
     d = cuda(x)
     pre = {k: (None if v is None else v[:, :T].contiguous()) for k, v in d.items()}

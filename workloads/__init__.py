@@ -117,14 +117,14 @@ def make_int_inputs(B, T, H, dk, dv, L, onehot_level: int, seed: int = 0, dtype=
     return dict(q=q.to(dt), k=k.to(dt), v=v.to(dt), log_a=None, lam=lam)
 
 
-def make_sparse_int_inputs(B, T, H, d, L, onehot_level: int, seed: int = 0):
+def make_sparse_int_inputs(B, T, H, d, L, onehot_level: int, seed: int = 0, dv=None):
     """bf16 inputs whose every intermediate stays an exactly representable integer even
     through bf16 storage of the chunk states: q, v in {-1, 0, 1}, each k a signed one-hot
     vector (so q.k is in {-1, 0, 1} and a state entry counts the tokens of a block whose k
-    hits that feature), no decay, one-hot lambda."""
+    hits that feature), no decay, one-hot lambda.  d is d_k; d_v defaults to d."""
     g = _gen(seed)
     q = torch.randint(-1, 2, (B, T, H, d), generator=g).float()
-    v = torch.randint(-1, 2, (B, T, H, d), generator=g).float()
+    v = torch.randint(-1, 2, (B, T, H, d if dv is None else dv), generator=g).float()
     hot = torch.randint(0, d, (B, T, H), generator=g)
     sign = torch.randint(0, 2, (B, T, H), generator=g).float() * 2 - 1
     k = torch.zeros(B, T, H, d)
