@@ -88,7 +88,11 @@ LL_API int loglinear_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t
  * chunk states, a level scan over Fenwick block pairs of chunks, and a lambda-weighted
  * readout of the block states fused into the output epilogue.
  *
- *   q, k    [B, T, H, dk]   in_dtype (LL_F32 or LL_BF16)
+ *   q, k    [B, T, Hqk, dk] in_dtype (LL_F32 or LL_BF16).  Hqk q/k heads shared by the
+ *                           H value heads in contiguous groups of H / Hqk: head h reads
+ *                           q/k head h / (H / Hqk).  Hqk = H is one q/k per head; Hqk = 1
+ *                           shares one q/k across all heads (Mamba-2's multi-value form).
+ *                           1 <= Hqk <= H and H % Hqk == 0, else LL_ERR_SHAPE.
  *   v       [B, T, H, dv]   in_dtype
  *   log_a   [B, T, H]       fp32, log of the decay a_t (<= 0 expected); NULL = no decay
  *   lambda  [B, T, H, L]    fp32 level weights lambda[t, l]; L >= bit_length(T-1) + 1;
@@ -108,8 +112,9 @@ LL_API int loglinear_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t
  */
 LL_API int loglinear_fwd(const void* q, const void* k, const void* v, const float* log_a,
                   const float* lambda, void* out, int64_t B, int64_t T, int64_t H,
-                  int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype,
-                  int path, void* workspace, size_t workspace_bytes, ll_stream_t stream);
+                  int64_t Hqk, int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
+                  int out_dtype, int path, void* workspace, size_t workspace_bytes,
+                  ll_stream_t stream);
 
 /*
  * loglinear_fwd with per-kernel timing: identical work and results, plus cudaEventRecord
@@ -120,7 +125,8 @@ LL_API int loglinear_fwd(const void* q, const void* k, const void* v, const floa
  */
 LL_API int loglinear_fwd_with_events(const void* q, const void* k, const void* v,
                                      const float* log_a, const float* lambda, void* out,
-                                     int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
+                                     int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk,
+                                     int64_t dv,
                                      int64_t L, int chunk, int in_dtype, int out_dtype, int path,
                                      void* workspace, size_t workspace_bytes, ll_stream_t stream,
                                      void* const* stage_events, int n_events, int* n_kernels);
@@ -141,7 +147,8 @@ LL_API int loglinear_fwd_with_events(const void* q, const void* k, const void* v
  */
 LL_API int loglinear_prefill(const void* q, const void* k, const void* v, const float* log_a,
                              const float* lambda, void* out, float* state_out, int64_t B,
-                             int64_t T, int64_t H, int64_t dk, int64_t dv, int64_t L, int chunk,
+                             int64_t T, int64_t H, int64_t Hqk, int64_t dk, int64_t dv,
+                             int64_t L, int chunk,
                              int in_dtype, int out_dtype, int path, void* workspace,
                              size_t workspace_bytes, ll_stream_t stream);
 
@@ -156,7 +163,8 @@ LL_API int loglinear_prefill(const void* q, const void* k, const void* v, const 
  * are empty after t-1 (bit j-1 of t-1 clear, j >= 1) are neither read nor written.
  *
  *   state   [B, H, L, dk, dv] fp32, updated in place, 16-byte aligned
- *   q, k    [B, H, dk]   in_dtype;   v [B, H, dv] in_dtype
+ *   q, k    [B, Hqk, dk] in_dtype (q/k heads shared as in loglinear_fwd);
+ *   v       [B, H, dv]   in_dtype
  *   log_a   [B, H] fp32 or NULL (no decay);   lambda [B, H, L] fp32
  *   out     [B, H, dv]   out_dtype, overwritten
  *   t       >= 0, same for every (b, h); L >= bit_length(t) + 1
@@ -166,8 +174,8 @@ LL_API int loglinear_prefill(const void* q, const void* k, const void* v, const 
  */
 LL_API int loglinear_decode_step(float* state, const void* q, const void* k, const void* v,
                           const float* log_a, const float* lambda, int64_t t, void* out,
-                          int64_t B, int64_t H, int64_t dk, int64_t dv, int64_t L,
-                          int in_dtype, int out_dtype, ll_stream_t stream);
+                          int64_t B, int64_t H, int64_t Hqk, int64_t dk, int64_t dv,
+                          int64_t L, int in_dtype, int out_dtype, ll_stream_t stream);
 
 /*
  * Reads and clears the device error word of the tensor-core path (synchronises `stream`).
@@ -201,9 +209,9 @@ LL_API int loglinear_device_error(ll_stream_t stream, unsigned* flags);
 #define LL_FWD_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 LL_API int loglinear_fwd_noalloc(const void* q, const void* k, const void* v,
                                  const float* log_a, const float* lambda, void* out,
-                                 int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv,
-                                 int64_t L, int chunk, int in_dtype, int out_dtype, int path,
-                                 ll_stream_t stream);
+                                 int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk,
+                                 int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype,
+                                 int path, ll_stream_t stream);
 
 /*
  * Debug view of the forward's level indexing (first page, sections 层级判定算法 and 矩阵

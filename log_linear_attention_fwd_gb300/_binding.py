@@ -33,18 +33,18 @@ SIGNATURES = {
     "loglinear_fwd_workspace_size": (_int, [_i64, _i64, _i64, _i64, _i64, _int, _int, _int,
                                             ctypes.POINTER(_sz)]),
     "loglinear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
-                             _int, _int, _int, _int, _vp, _sz, _vp]),
+                             _i64, _int, _int, _int, _int, _vp, _sz, _vp]),
     "loglinear_fwd_with_events": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
-                                         _i64, _i64, _int, _int, _int, _int, _vp, _sz, _vp,
+                                         _i64, _i64, _i64, _int, _int, _int, _int, _vp, _sz, _vp,
                                          ctypes.POINTER(_vp), _int, ctypes.POINTER(_int)]),
     "loglinear_decode_step": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _i64,
-                                     _i64, _i64, _int, _int, _vp]),
+                                     _i64, _i64, _i64, _int, _int, _vp]),
     "loglinear_debug_level_map": (_int, [_i64, _int, _int, _vp, _vp]),
     "loglinear_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "loglinear_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
-                                     _i64, _int, _int, _int, _int, _vp]),
+                                     _i64, _i64, _int, _int, _int, _int, _vp]),
     "loglinear_prefill": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
-                                 _i64, _int, _int, _int, _int, _vp, _sz, _vp]),
+                                 _i64, _i64, _int, _int, _int, _int, _vp, _sz, _vp]),
 }
 
 
@@ -129,12 +129,13 @@ def fwd_workspace_size(B, T, H, dk, dv, chunk, in_dtype, path="auto") -> int:
 
 def loglinear_fwd(q, k, v, log_a, lam, chunk, out=None, out_dtype=None, workspace=None,
                   path="auto", stream=None):
-    """O = (Q K^T ⊙ M^S ⊙ M^H) V through the C ABI (q, k [B,T,H,dk]; v [B,T,H,dv];
-    log_a [B,T,H] fp32 or None; lam [B,T,H,L] fp32).  Returns out [B,T,H,dv]."""
-    B, T, H, dk = q.shape
-    dv, L = v.shape[-1], lam.shape[-1]
-    _check_dev("q", q, shape=(B, T, H, dk))
-    _check_dev("k", k, q.dtype, (B, T, H, dk))
+    """O = (Q K^T ⊙ M^S ⊙ M^H) V through the C ABI (q, k [B,T,Hqk,dk]; v [B,T,H,dv];
+    log_a [B,T,H] fp32 or None; lam [B,T,H,L] fp32; head h reads q/k head h // (H/Hqk)).
+    Returns out [B,T,H,dv]."""
+    B, T, Hqk, dk = q.shape
+    H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
+    _check_dev("q", q, shape=(B, T, Hqk, dk))
+    _check_dev("k", k, q.dtype, (B, T, Hqk, dk))
     _check_dev("v", v, q.dtype, (B, T, H, dv))
     _check_dev("log_a", log_a, torch.float32, (B, T, H))
     _check_dev("lam", lam, torch.float32, (B, T, H, L))
@@ -147,7 +148,7 @@ def loglinear_fwd(q, k, v, log_a, lam, chunk, out=None, out_dtype=None, workspac
         workspace = torch.empty(max(ws_bytes, 1), device=q.device, dtype=torch.uint8)
     _check_dev("workspace", workspace, torch.uint8)
     st = _lib.loglinear_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
-                            B, T, H, dk, dv, L, chunk, in_dt, _dtype_code(out), PATHS[path],
+                            B, T, H, Hqk, dk, dv, L, chunk, in_dt, _dtype_code(out), PATHS[path],
                             _ptr(workspace), workspace.numel(), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_fwd")
@@ -158,8 +159,8 @@ def loglinear_fwd_with_events(q, k, v, log_a, lam, chunk, events, out, workspace
                               stream=None):
     """loglinear_fwd plus torch.cuda.Event records between its kernels (events are
     created with enable_timing=True by the caller).  Returns the number of kernels."""
-    B, T, H, dk = q.shape
-    dv, L = v.shape[-1], lam.shape[-1]
+    B, T, Hqk, dk = q.shape
+    H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
     st_ = stream if stream is not None else torch.cuda.current_stream()
     for e in events:          # torch creates the CUDA event lazily, on its first record
         if not e.cuda_event:
@@ -167,7 +168,7 @@ def loglinear_fwd_with_events(q, k, v, log_a, lam, chunk, events, out, workspace
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     nk = ctypes.c_int(0)
     st = _lib.loglinear_fwd_with_events(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam),
-                                        _ptr(out), B, T, H, dk, dv, L, chunk, _dtype_code(q),
+                                        _ptr(out), B, T, H, Hqk, dk, dv, L, chunk, _dtype_code(q),
                                         _dtype_code(out), PATHS[path], _ptr(workspace),
                                         workspace.numel(), _stream(stream), arr, len(events),
                                         ctypes.byref(nk))
@@ -178,11 +179,12 @@ def loglinear_fwd_with_events(q, k, v, log_a, lam, chunk, events, out, workspace
 
 def loglinear_decode_step(state, q, k, v, log_a, lam, t, out=None, out_dtype=None, stream=None):
     """One lssb decode step at position t; updates state [B,H,L,dk,dv] (fp32) in place
-    and returns out [B,H,dv]."""
+    and returns out [B,H,dv].  q, k [B,Hqk,dk] (head h reads q/k head h // (H/Hqk))."""
     B, H, L, dk, dv = state.shape
+    Hqk = q.shape[1]
     _check_dev("state", state, torch.float32)
-    _check_dev("q", q, shape=(B, H, dk))
-    _check_dev("k", k, q.dtype, (B, H, dk))
+    _check_dev("q", q, shape=(B, Hqk, dk))
+    _check_dev("k", k, q.dtype, (B, Hqk, dk))
     _check_dev("v", v, q.dtype, (B, H, dv))
     _check_dev("log_a", log_a, torch.float32, (B, H))
     _check_dev("lam", lam, torch.float32, (B, H, L))
@@ -190,7 +192,7 @@ def loglinear_decode_step(state, q, k, v, log_a, lam, t, out=None, out_dtype=Non
         out = torch.empty(B, H, dv, device=q.device, dtype=out_dtype or q.dtype)
     _check_dev("out", out, shape=(B, H, dv))
     st = _lib.loglinear_decode_step(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_a),
-                                    _ptr(lam), int(t), _ptr(out), B, H, dk, dv, L, _dtype_code(q),
+                                    _ptr(lam), int(t), _ptr(out), B, H, Hqk, dk, dv, L, _dtype_code(q),
                                     _dtype_code(out), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_decode_step")
@@ -201,11 +203,11 @@ def loglinear_prefill(q, k, v, log_a, lam, chunk, out=None, state=None, out_dtyp
                       workspace=None, path="auto", stream=None):
     """loglinear_fwd over the prompt plus the per-level decode state at its last position
     (fp32 [B, H, L, dk, dv]), ready for loglinear_decode_step at t = T.
-    Returns (out, state)."""
-    B, T, H, dk = q.shape
-    dv, L = v.shape[-1], lam.shape[-1]
-    _check_dev("q", q, shape=(B, T, H, dk))
-    _check_dev("k", k, q.dtype, (B, T, H, dk))
+    Returns (out, state).  q/k heads as in loglinear_fwd."""
+    B, T, Hqk, dk = q.shape
+    H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
+    _check_dev("q", q, shape=(B, T, Hqk, dk))
+    _check_dev("k", k, q.dtype, (B, T, Hqk, dk))
     _check_dev("v", v, q.dtype, (B, T, H, dv))
     _check_dev("log_a", log_a, torch.float32, (B, T, H))
     _check_dev("lam", lam, torch.float32, (B, T, H, L))
@@ -221,7 +223,7 @@ def loglinear_prefill(q, k, v, log_a, lam, chunk, out=None, state=None, out_dtyp
         workspace = torch.empty(max(ws_bytes, 1), device=q.device, dtype=torch.uint8)
     _check_dev("workspace", workspace, torch.uint8)
     st = _lib.loglinear_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
-                                _ptr(state), B, T, H, dk, dv, L, chunk, in_dt, _dtype_code(out),
+                                _ptr(state), B, T, H, Hqk, dk, dv, L, chunk, in_dt, _dtype_code(out),
                                 PATHS[path], _ptr(workspace), workspace.numel(), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_prefill")
@@ -232,12 +234,12 @@ def loglinear_fwd_noalloc(q, k, v, log_a, lam, chunk, out, path="auto", stream=N
     """loglinear_fwd without a workspace, for callers that cannot allocate device memory:
     the scratch is the library's fixed device array (see include/loglinear.h).  `out` is
     caller-provided; nothing is allocated here either."""
-    B, T, H, dk = q.shape
-    dv, L = v.shape[-1], lam.shape[-1]
+    B, T, Hqk, dk = q.shape
+    H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
     for name, t in (("q", q), ("k", k), ("v", v), ("log_a", log_a), ("lam", lam), ("out", out)):
         _check_dev(name, t)
     st = _lib.loglinear_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
-                                    B, T, H, dk, dv, L, chunk, _dtype_code(q), _dtype_code(out),
+                                    B, T, H, Hqk, dk, dv, L, chunk, _dtype_code(q), _dtype_code(out),
                                     PATHS[path], _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_fwd_noalloc")

@@ -36,16 +36,17 @@ template <typename InT, typename OutT, int kFew>
 __global__ void __launch_bounds__(kThreads, kFew == 16 ? 1 : 2) decode_step_kernel(
     float* __restrict__ state, const void* __restrict__ q, const void* __restrict__ k,
     const void* __restrict__ v, const float* __restrict__ log_a, const float* __restrict__ lam,
-    void* __restrict__ out, int H, int dk, int dv, int L, DecodePlan plan) {
+    void* __restrict__ out, int H, int hg, int dk, int dv, int L, DecodePlan plan) {
   __shared__ float qs[128];
   __shared__ float ks[128];
   __shared__ float lam_s[kMaxLv];
   __shared__ float4 red[kThreads];
   const int64_t bh = blockIdx.x;
+  const int64_t bq = bh / hg;  // (b, q/k head): H = Hqk * hg, head h reads q/k head h / hg
   const int tid = threadIdx.x;
   for (int i = tid; i < dk; i += kThreads) {
-    qs[i] = ldx<InT>(q, bh * dk + i);
-    ks[i] = ldx<InT>(k, bh * dk + i);
+    qs[i] = ldx<InT>(q, bq * dk + i);
+    ks[i] = ldx<InT>(k, bq * dk + i);
   }
   for (int i = tid; i < L && i < kMaxLv; i += kThreads) lam_s[i] = lam[bh * L + i];
   __syncthreads();
@@ -165,37 +166,38 @@ __global__ void __launch_bounds__(kThreads, kFew == 16 ? 1 : 2) decode_step_kern
 
 template <typename InT, typename OutT>
 cudaError_t launch_typed(float* state, const void* q, const void* k, const void* v,
-                         const float* log_a, const float* lam, void* out, int B, int H, int dk,
-                         int dv, int L, const DecodePlan& plan, cudaStream_t s) {
+                         const float* log_a, const float* lam, void* out, int B, int H, int hg,
+                         int dk, int dv, int L, const DecodePlan& plan, cudaStream_t s) {
   const unsigned grid = (unsigned)((int64_t)B * H);
   const int touched = plan.t_zero ? 0 : plan.l + 1 + plan.n_hi;
   if (touched <= 8)
     decode_step_kernel<InT, OutT, 8><<<grid, kThreads, 0, s>>>(state, q, k, v, log_a, lam, out, H,
-                                                                dk, dv, L, plan);
+                                                                hg, dk, dv, L, plan);
   else if (touched <= 16)
     decode_step_kernel<InT, OutT, 16><<<grid, kThreads, 0, s>>>(state, q, k, v, log_a, lam, out, H,
-                                                                 dk, dv, L, plan);
+                                                                 hg, dk, dv, L, plan);
   else
     decode_step_kernel<InT, OutT, 0><<<grid, kThreads, 0, s>>>(state, q, k, v, log_a, lam, out, H,
-                                                                dk, dv, L, plan);
+                                                                hg, dk, dv, L, plan);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode(float* state, const void* q, const void* k, const void* v,
-                          const float* log_a, const float* lam, void* out, int B, int H, int dk,
-                          int dv, int L, const DecodePlan& plan, int in_dtype, int out_dtype,
-                          cudaStream_t s) {
+                          const float* log_a, const float* lam, void* out, int B, int H, int Hqk,
+                          int dk, int dv, int L, const DecodePlan& plan, int in_dtype,
+                          int out_dtype, cudaStream_t s) {
+  const int hg = H / Hqk;
   if (in_dtype == LL_F32 && out_dtype == LL_F32)
-    return launch_typed<float, float>(state, q, k, v, log_a, lam, out, B, H, dk, dv, L, plan, s);
+    return launch_typed<float, float>(state, q, k, v, log_a, lam, out, B, H, hg, dk, dv, L, plan, s);
   if (in_dtype == LL_F32)
-    return launch_typed<float, __nv_bfloat16>(state, q, k, v, log_a, lam, out, B, H, dk, dv, L,
+    return launch_typed<float, __nv_bfloat16>(state, q, k, v, log_a, lam, out, B, H, hg, dk, dv, L,
                                               plan, s);
   if (out_dtype == LL_F32)
-    return launch_typed<__nv_bfloat16, float>(state, q, k, v, log_a, lam, out, B, H, dk, dv, L,
+    return launch_typed<__nv_bfloat16, float>(state, q, k, v, log_a, lam, out, B, H, hg, dk, dv, L,
                                               plan, s);
-  return launch_typed<__nv_bfloat16, __nv_bfloat16>(state, q, k, v, log_a, lam, out, B, H, dk,
+  return launch_typed<__nv_bfloat16, __nv_bfloat16>(state, q, k, v, log_a, lam, out, B, H, hg, dk,
                                                     dv, L, plan, s);
 }
 

@@ -59,7 +59,7 @@ extern "C" {
 
 int loglinear_fwd_noalloc(const void* q, const void* k, const void* v, const float* log_a,
                           const float* lambda, void* out, int64_t B, int64_t T, int64_t H,
-                          int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
+                          int64_t Hqk, int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
                           int out_dtype, int path, ll_stream_t stream) {
   size_t need = 0;
   const int st = loglinear_fwd_workspace_size(B, T, H, dk, dv, chunk, in_dtype, path, &need);
@@ -68,7 +68,7 @@ int loglinear_fwd_noalloc(const void* q, const void* k, const void* v, const flo
   void* scratch = nullptr;
   const cudaError_t e = ll::scratch_on_current_device(&scratch);
   if (e != cudaSuccess) return ll::report_cuda_error(e);
-  return loglinear_fwd(q, k, v, log_a, lambda, out, B, T, H, dk, dv, L, chunk, in_dtype,
+  return loglinear_fwd(q, k, v, log_a, lambda, out, B, T, H, Hqk, dk, dv, L, chunk, in_dtype,
                        out_dtype, path, scratch, ll::kNoallocScratchBytes, stream);
 }
 

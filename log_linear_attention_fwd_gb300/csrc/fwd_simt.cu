@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_state(FwdArgs a) {
   chunk_cumsum(a, b, h, t0, n, cs);
   for (int idx = threadIdx.x; idx < n * dk; idx += kThreads) {
     const int r = idx / dk, c = idx - r * dk;
-    Ks[idx] = ld<InT>(a.k, (((int64_t)b * a.T + t0 + r) * a.H + h) * dk + c);
+    Ks[idx] = ld<InT>(a.k, (((int64_t)b * a.T + t0 + r) * a.Hqk + h / a.hg) * dk + c);
   }
   for (int idx = threadIdx.x; idx < n * dv; idx += kThreads) {
     const int r = idx / dv, c = idx - r * dv;
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads) simt_intra_readout(FwdArgs a) {
   chunk_cumsum(a, b, h, t0, n, cs);
   for (int idx = threadIdx.x; idx < C * dk; idx += kThreads) {
     const int r = idx / dk, c = idx - r * dk;
-    const int64_t g = (((int64_t)b * a.T + t0 + r) * a.H + h) * dk + c;
+    const int64_t g = (((int64_t)b * a.T + t0 + r) * a.Hqk + h / a.hg) * dk + c;
     Qs[idx] = r < n ? ld<InT>(a.q, g) : 0.f;
     Ks[idx] = r < n ? ld<InT>(a.k, g) : 0.f;
   }

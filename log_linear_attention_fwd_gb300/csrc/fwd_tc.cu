@@ -48,6 +48,7 @@ constexpr int kMaxChunkLevels = 32;         // chunk levels m = 1..31 (positions
 
 struct TcParams {
   int B, T, H, L, N;
+  int hg;            // value heads per q/k head: head h reads q/k head h / hg
   const float* log_a;
   const float* lam;
   void* out;
@@ -266,6 +267,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   const int tk = (int)ints[0];
   const int j = tk / BH, bhi = tk - j * BH;
   const int b = bhi / p.H, h = bhi - b * p.H;
+  const int hq = h / p.hg;  // q/k head
   const int64_t N = p.N;
   const int64_t bh = bhi;
   const int t0 = j * kTile;
@@ -276,10 +278,10 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   bool landed = true;  // thread 0: Q, K and V arrived
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_load, 2 * kOperand + G::kVBytes);
-    tma_load_4d(&tmQ, bar_load, Qb, 0, h, t0, b);
-    tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, h, t0, b);
-    tma_load_4d(&tmK, bar_load, Kb, 0, h, t0, b);
-    tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, h, t0, b);
+    tma_load_4d(&tmQ, bar_load, Qb, 0, hq, t0, b);
+    tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, hq, t0, b);
+    tma_load_4d(&tmK, bar_load, Kb, 0, hq, t0, b);
+    tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, hq, t0, b);
 #pragma unroll
     for (int pv = 0; pv < G::kPanels; ++pv)
       tma_load_4d(&tmV, bar_load, Vb + pv * kPanel, 64 * pv, h, t0, b);
@@ -445,8 +447,8 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   if (tid == 0 && nlev > 0) {
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar_q, kOperand);
-    tma_load_4d(&tmQ, bar_q, Qb, 0, h, t0, b);
-    tma_load_4d(&tmQ, bar_q, Qb + kPanel, 64, h, t0, b);
+    tma_load_4d(&tmQ, bar_q, Qb, 0, hq, t0, b);
+    tma_load_4d(&tmQ, bar_q, Qb + kPanel, 64, hq, t0, b);
   }
   __syncwarp();
 
@@ -724,14 +726,14 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   if (a.dk != kD || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
   const int dv = (int)a.dv;
   CUtensorMap tmQ, tmK, tmV, tmOut, tmU, tmNode;
-  if (!make_tokens_map(&tmQ, a.q, a.B, a.T, a.H, kD) ||
-      !make_tokens_map(&tmK, a.k, a.B, a.T, a.H, kD) ||
+  if (!make_tokens_map(&tmQ, a.q, a.B, a.T, a.Hqk, kD) ||
+      !make_tokens_map(&tmK, a.k, a.B, a.T, a.Hqk, kD) ||
       !make_tokens_map(&tmV, a.v, a.B, a.T, a.H, dv) ||
       !make_tokens_map(&tmOut, a.out, a.B, a.T, a.H, dv) || !make_rows_map(&tmU, a.U, rows, dv) ||
       !make_rows_map(&tmNode, a.nodes, rows, dv))
     return cudaErrorInvalidValue;
   TcParams p;
-  p.B = a.B; p.T = a.T; p.H = a.H; p.L = a.L; p.N = a.N;
+  p.B = a.B; p.T = a.T; p.H = a.H; p.L = a.L; p.N = a.N; p.hg = a.hg;
   p.log_a = a.log_a; p.lam = a.lam; p.out = a.out;
   p.U = static_cast<uint8_t*>(a.U);
   p.nodes = static_cast<uint8_t*>(a.nodes);

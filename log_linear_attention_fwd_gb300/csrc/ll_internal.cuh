@@ -57,6 +57,8 @@ struct FwdArgs {
   const float* lam;
   void* out;
   int B, T, H, dk, dv, L;
+  int Hqk, hg;  // q/k heads and value heads per q/k head (H = Hqk * hg): head h reads
+                // q/k head h / hg
   int C, lc;  // tile length and log2(tile)
   int N;      // tiles per (b, h)
   // workspace
@@ -118,7 +120,7 @@ struct DecodePlan {
 };
 cudaError_t launch_decode(float* state, const void* q, const void* k, const void* v,
                           const float* log_a, const float* lam, void* out, int B, int H,
-                          int dk, int dv, int L, const DecodePlan& plan, int in_dtype,
+                          int Hqk, int dk, int dv, int L, const DecodePlan& plan, int in_dtype,
                           int out_dtype, cudaStream_t s);
 
 cudaError_t launch_level_map(int T, int tile, int lc, int8_t* levels, cudaStream_t s);

@@ -110,6 +110,13 @@ int check_fwd_sizes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv, int
 
 size_t node_bytes(int path) { return path == LL_PATH_TC ? 2 : 4; }
 
+// q/k heads: H = Hqk * (value heads per q/k head); with H = 0 any Hqk >= 0 passes (no-op).
+int check_qk_heads(int64_t H, int64_t Hqk) {
+  if (Hqk < 0) return LL_ERR_INVALID;
+  if (H > 0 && (Hqk < 1 || Hqk > H || H % Hqk != 0)) return LL_ERR_SHAPE;
+  return LL_OK;
+}
+
 }  // namespace
 
 int ll::report_cuda_error(cudaError_t e) { return cuda_fail(e); }
@@ -153,14 +160,15 @@ int loglinear_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t dk, in
 }
 
 static int fwd_impl(const void* q, const void* k, const void* v, const float* log_a,
-                    const float* lambda, void* out, int64_t B, int64_t T, int64_t H, int64_t dk,
-                    int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype, int path,
-                    void* workspace, size_t workspace_bytes, ll_stream_t stream,
-                    StageEvents* ev, float* state_out = nullptr) {
+                    const float* lambda, void* out, int64_t B, int64_t T, int64_t H,
+                    int64_t Hqk, int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
+                    int out_dtype, int path, void* workspace, size_t workspace_bytes,
+                    ll_stream_t stream, StageEvents* ev, float* state_out = nullptr) {
   int p, tile;
   int64_t N;
   int st = check_fwd_sizes(B, T, H, dk, dv, chunk, in_dtype, path, &p, &tile, &N);
   if (st != LL_OK) return st;
+  if ((st = check_qk_heads(H, Hqk)) != LL_OK) return st;
   if (!dtype_ok(out_dtype)) return LL_ERR_DTYPE;
   if (L < 1) return LL_ERR_INVALID;
   if (B == 0 || T == 0 || H == 0) return LL_OK;
@@ -175,6 +183,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* lo
   FwdArgs a;
   a.q = q; a.k = k; a.v = v; a.log_a = log_a; a.lam = lambda; a.out = out;
   a.B = (int)B; a.T = (int)T; a.H = (int)H; a.dk = (int)dk; a.dv = (int)dv; a.L = (int)L;
+  a.Hqk = (int)Hqk; a.hg = (int)(H / Hqk);
   a.C = tile; a.lc = log2_exact(tile); a.N = (int)N;
   char* ws = static_cast<char*>(workspace);
   a.U = ws + w.off_U;
@@ -193,32 +202,35 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* lo
 }
 
 int loglinear_fwd(const void* q, const void* k, const void* v, const float* log_a,
-                  const float* lambda, void* out, int64_t B, int64_t T, int64_t H, int64_t dk,
-                  int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype, int path,
-                  void* workspace, size_t workspace_bytes, ll_stream_t stream) {
-  return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, dk, dv, L, chunk, in_dtype, out_dtype,
-                  path, workspace, workspace_bytes, stream, nullptr);
+                  const float* lambda, void* out, int64_t B, int64_t T, int64_t H, int64_t Hqk,
+                  int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype,
+                  int path, void* workspace, size_t workspace_bytes, ll_stream_t stream) {
+  return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, Hqk, dk, dv, L, chunk, in_dtype,
+                  out_dtype, path, workspace, workspace_bytes, stream, nullptr);
 }
 
 int loglinear_prefill(const void* q, const void* k, const void* v, const float* log_a,
                       const float* lambda, void* out, float* state_out, int64_t B, int64_t T,
-                      int64_t H, int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
-                      int out_dtype, int path, void* workspace, size_t workspace_bytes,
-                      ll_stream_t stream) {
+                      int64_t H, int64_t Hqk, int64_t dk, int64_t dv, int64_t L, int chunk,
+                      int in_dtype, int out_dtype, int path, void* workspace,
+                      size_t workspace_bytes, ll_stream_t stream) {
   if (!state_out) return LL_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(state_out) & 3u) != 0) return LL_ERR_ALIGN;
+  const int sh = check_qk_heads(H, Hqk);
+  if (sh != LL_OK) return sh;
   if (B > 0 && H > 0 && T == 0 && L >= 1 && dk >= 1 && dv >= 1) {  // no prefix: empty state
     const cudaError_t e = cudaMemsetAsync(state_out, 0, sizeof(float) * (size_t)(B * H * L * dk * dv),
                                           reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LL_OK : cuda_fail(e);
   }
-  return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, dk, dv, L, chunk, in_dtype, out_dtype,
-                  path, workspace, workspace_bytes, stream, nullptr, state_out);
+  return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, Hqk, dk, dv, L, chunk, in_dtype,
+                  out_dtype, path, workspace, workspace_bytes, stream, nullptr, state_out);
 }
 
 int loglinear_fwd_with_events(const void* q, const void* k, const void* v, const float* log_a,
                               const float* lambda, void* out, int64_t B, int64_t T, int64_t H,
-                              int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
+                              int64_t Hqk, int64_t dk, int64_t dv, int64_t L, int chunk,
+                              int in_dtype,
                               int out_dtype, int path, void* workspace, size_t workspace_bytes,
                               ll_stream_t stream, void* const* stage_events, int n_events,
                               int* n_kernels) {
@@ -227,17 +239,19 @@ int loglinear_fwd_with_events(const void* q, const void* k, const void* v, const
   ev.ev = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events));
   ev.n = n_events;
   if (n_kernels) *n_kernels = 0;
-  const int st = fwd_impl(q, k, v, log_a, lambda, out, B, T, H, dk, dv, L, chunk, in_dtype,
-                          out_dtype, path, workspace, workspace_bytes, stream, &ev);
+  const int st = fwd_impl(q, k, v, log_a, lambda, out, B, T, H, Hqk, dk, dv, L, chunk,
+                          in_dtype, out_dtype, path, workspace, workspace_bytes, stream, &ev);
   if (n_kernels) *n_kernels = ev.launched;
   return st;
 }
 
 int loglinear_decode_step(float* state, const void* q, const void* k, const void* v,
                           const float* log_a, const float* lambda, int64_t t, void* out,
-                          int64_t B, int64_t H, int64_t dk, int64_t dv, int64_t L,
+                          int64_t B, int64_t H, int64_t Hqk, int64_t dk, int64_t dv, int64_t L,
                           int in_dtype, int out_dtype, ll_stream_t stream) {
   if (B < 0 || H < 0 || dk < 1 || dv < 1 || t < 0 || L < 1) return LL_ERR_INVALID;
+  const int sh = check_qk_heads(H, Hqk);
+  if (sh != LL_OK) return sh;
   if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return LL_ERR_DTYPE;
   if (t > INT32_MAX) return LL_ERR_UNSUPPORTED;
   if (L < bit_length(t) + 1) return LL_ERR_SHAPE;
@@ -261,8 +275,8 @@ int loglinear_decode_step(float* state, const void* q, const void* k, const void
       if (((t - 1) >> (lv - 1)) & 1) plan.lv[n++] = lv;
     plan.n_hi = n - (l + 1);
   }
-  const cudaError_t e = launch_decode(state, q, k, v, log_a, lambda, out, (int)B, (int)H, (int)dk,
-                                      (int)dv, (int)L, plan, in_dtype, out_dtype,
+  const cudaError_t e = launch_decode(state, q, k, v, log_a, lambda, out, (int)B, (int)H,
+                                      (int)Hqk, (int)dk, (int)dv, (int)L, plan, in_dtype, out_dtype,
                                       reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }

@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
     for (int i = threadIdx.x; i < nb * kMaxDim; i += kThreads) {
       const int r = i / kMaxDim, d = i - r * kMaxDim;
       const int64_t tok = ((int64_t)b * a.T + lo + r) * a.H + h;
-      ks[i] = d < dk ? w[r] * ld<InT>(a.k, tok * dk + d) : 0.f;
+      const int64_t tok_k = ((int64_t)b * a.T + lo + r) * a.Hqk + h / a.hg;
+      ks[i] = d < dk ? w[r] * ld<InT>(a.k, tok_k * dk + d) : 0.f;
       vs[i] = d < dv ? ld<InT>(a.v, tok * dv + d) : 0.f;
     }
     __syncthreads();

@@ -29,3 +29,16 @@ def cuda(d):
 
 def tol_for(dtype):
     return TOL_F32 if dtype in ("f32", torch.float32) else TOL_BF16
+
+
+def per_head_qk(x):
+    """The same inputs with q and k given per value head: q/k head g serves the value heads
+    g * (H / Hqk) .. (g + 1) * (H / Hqk) - 1, so each is repeated H / Hqk times in place.
+    Input marshalling for the oracle, whose definition is per head."""
+    H, G = x["v"].shape[2], x["q"].shape[2]
+    if G == H:
+        return x
+    y = dict(x)
+    for n in ("q", "k"):
+        y[n] = x[n].repeat_interleave(H // G, dim=2).contiguous()
+    return y

@@ -48,13 +48,14 @@ FAKE = ctypes.c_void_p(0x1000)   # never dereferenced: every call here fails val
 
 
 def fwd(L, **kw):
-    a = dict(q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, out=FAKE, B=1, T=64, H=2, dk=16, dv=16,
-             Lv=7, chunk=16, ind=L.LL_F32, outd=L.LL_F32, path=L.LL_PATH_SIMT, ws=None, wsb=0,
-             stream=None)
+    a = dict(q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, out=FAKE, B=1, T=64, H=2, Hqk=None,
+             dk=16, dv=16, Lv=7, chunk=16, ind=L.LL_F32, outd=L.LL_F32, path=L.LL_PATH_SIMT,
+             ws=None, wsb=0, stream=None)
     a.update(kw)
+    hqk = a["H"] if a["Hqk"] is None else a["Hqk"]
     return L.lib().loglinear_fwd(a["q"], a["k"], a["v"], a["log_a"], a["lam"], a["out"], a["B"],
-                                 a["T"], a["H"], a["dk"], a["dv"], a["Lv"], a["chunk"], a["ind"],
-                                 a["outd"], a["path"], a["ws"], a["wsb"], a["stream"])
+                                 a["T"], a["H"], hqk, a["dk"], a["dv"], a["Lv"], a["chunk"],
+                                 a["ind"], a["outd"], a["path"], a["ws"], a["wsb"], a["stream"])
 
 
 def test_fwd_validation_codes(L):
@@ -77,21 +78,28 @@ def test_fwd_validation_codes(L):
                q=ctypes.c_void_p(0x1002), ws=FAKE, wsb=1 << 40) == L.LL_ERR_ALIGN
     assert fwd(L, dk=64, dv=64, ind=L.LL_BF16, path=L.LL_PATH_TC) == L.LL_ERR_UNSUPPORTED
     assert fwd(L, dk=128, dv=128, ind=L.LL_F32, path=L.LL_PATH_TC) == L.LL_ERR_UNSUPPORTED
+    # q/k heads: 1 <= Hqk <= H, H a multiple of Hqk
+    assert fwd(L, H=6, Hqk=4) == L.LL_ERR_SHAPE
+    assert fwd(L, H=2, Hqk=4) == L.LL_ERR_SHAPE
+    assert fwd(L, H=2, Hqk=0) == L.LL_ERR_SHAPE
+    assert fwd(L, H=2, Hqk=-1) == L.LL_ERR_INVALID
+    assert fwd(L, H=6, Hqk=3, ws=None, wsb=0) == L.LL_ERR_WORKSPACE   # valid grouping
+    assert fwd(L, H=6, Hqk=1, ws=None, wsb=0) == L.LL_ERR_WORKSPACE
     # empty problems are no-ops, even with null pointers
-    for kw in (dict(B=0), dict(T=0), dict(H=0)):
+    for kw in (dict(B=0), dict(T=0), dict(H=0), dict(H=0, Hqk=0)):
         assert fwd(L, q=None, k=None, v=None, lam=None, out=None, **kw) == L.LL_OK
 
 
 def test_prefill_validation_codes(L):
     def pre(state, **kw):
-        a = dict(q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, out=FAKE, B=1, T=64, H=2, dk=16,
-                 dv=16, Lv=7, chunk=16, ind=L.LL_F32, outd=L.LL_F32, path=L.LL_PATH_SIMT,
+        a = dict(q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, out=FAKE, B=1, T=64, H=2, Hqk=2,
+                 dk=16, dv=16, Lv=7, chunk=16, ind=L.LL_F32, outd=L.LL_F32, path=L.LL_PATH_SIMT,
                  ws=None, wsb=0, stream=None)
         a.update(kw)
         return L.lib().loglinear_prefill(a["q"], a["k"], a["v"], a["log_a"], a["lam"], a["out"],
-                                         state, a["B"], a["T"], a["H"], a["dk"], a["dv"], a["Lv"],
-                                         a["chunk"], a["ind"], a["outd"], a["path"], a["ws"],
-                                         a["wsb"], a["stream"])
+                                         state, a["B"], a["T"], a["H"], a["Hqk"], a["dk"], a["dv"],
+                                         a["Lv"], a["chunk"], a["ind"], a["outd"], a["path"],
+                                         a["ws"], a["wsb"], a["stream"])
     assert pre(None) == L.LL_ERR_INVALID
     assert pre(ctypes.c_void_p(0x1002)) == L.LL_ERR_ALIGN
     # the forward's own validation applies unchanged
@@ -99,6 +107,8 @@ def test_prefill_validation_codes(L):
     assert pre(FAKE, Lv=6) == L.LL_ERR_SHAPE
     assert pre(FAKE, ws=None, wsb=0) == L.LL_ERR_WORKSPACE
     assert pre(FAKE, B=0, q=None, k=None, v=None, lam=None, out=None) == L.LL_OK
+    assert pre(FAKE, Hqk=3) == L.LL_ERR_SHAPE
+    assert pre(FAKE, T=0, Hqk=3) == L.LL_ERR_SHAPE      # checked before the empty-prompt path
 
 
 def test_workspace_size_and_paths(L):
@@ -129,11 +139,11 @@ def test_workspace_size_and_paths(L):
 
 def dec(L, **kw):
     a = dict(state=FAKE, q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, t=5, out=FAKE, B=2, H=2,
-             dk=16, dv=16, Lv=4, ind=L.LL_F32, outd=L.LL_F32, stream=None)
+             Hqk=2, dk=16, dv=16, Lv=4, ind=L.LL_F32, outd=L.LL_F32, stream=None)
     a.update(kw)
     return L.lib().loglinear_decode_step(a["state"], a["q"], a["k"], a["v"], a["log_a"], a["lam"],
-                                         a["t"], a["out"], a["B"], a["H"], a["dk"], a["dv"],
-                                         a["Lv"], a["ind"], a["outd"], a["stream"])
+                                         a["t"], a["out"], a["B"], a["H"], a["Hqk"], a["dk"],
+                                         a["dv"], a["Lv"], a["ind"], a["outd"], a["stream"])
 
 
 def test_decode_validation_codes(L):
@@ -147,6 +157,8 @@ def test_decode_validation_codes(L):
     assert dec(L, out=None) == L.LL_ERR_INVALID
     assert dec(L, state=ctypes.c_void_p(0x1004)) == L.LL_ERR_ALIGN
     assert dec(L, B=0, state=None) == L.LL_OK
+    assert dec(L, H=4, Hqk=3) == L.LL_ERR_SHAPE
+    assert dec(L, Hqk=0) == L.LL_ERR_SHAPE
 
 
 def test_level_map_validation(L):

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.helpers import TOL_BF16, TOL_F32, cuda, max_abs, rel_l2, tol_for
+from tests.helpers import TOL_BF16, TOL_F32, cuda, max_abs, per_head_qk, rel_l2, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -222,3 +222,27 @@ def test_tc_repeated_calls_same_workspace(LL):
         outs.append(o.clone())
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
     assert LL.device_error() == 0
+
+
+# ------------------------------------------------------------------ shared q/k heads
+
+
+@pytest.mark.parametrize("path,H,Hqk,dk,dv,T,dtype", [
+    ("simt", 6, 1, 32, 16, 300, "f32"), ("simt", 6, 2, 32, 16, 300, "f32"),
+    ("simt", 6, 3, 16, 32, 129, "f32"),
+    ("tc", 4, 1, 128, 64, 1000, "bf16"), ("tc", 6, 2, 128, 64, 2125, "bf16"),
+    ("tc", 4, 2, 128, 128, 1000, "bf16"), ("tc", 48, 1, 128, 64, 300, "bf16")])
+def test_shared_qk_heads_match_oracle(LL, path, H, Hqk, dk, dv, T, dtype):
+    """q/k shared by groups of H / Hqk value heads (Hqk = 1: one q/k for every head) equal
+    the per-head definition with q/k repeated over each group."""
+    L = (T - 1).bit_length() + 1
+    cfg = W.FwdConfig("mva", 2, H, T, dk, dv, 64, L, dtype, True, "softplus", seed=H + Hqk + T,
+                      Hqk=Hqk)
+    x = W.make_fwd_inputs(cfg)
+    assert x["q"].shape[2] == Hqk and x["v"].shape[2] == H
+    got = run(LL, x, 64, path=path, out_dtype=torch.float32)
+    assert LL.device_error() == 0
+    want = oracle_fwd(per_head_qk(x))
+    err = rel_l2(got, want)
+    print(f"shared q/k {path} H={H} Hqk={Hqk}: rel_l2={err:.3e}")
+    assert err <= tol_for(dtype)

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.helpers import TOL_BF16, TOL_F32, cuda, rel_l2
+from tests.helpers import TOL_BF16, TOL_F32, cuda, per_head_qk, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -20,6 +20,7 @@ def LL():
 
 def oracle_state(x, T):
     """[B, H, L, dk, dv] per-level states at position T-1 (bucket definition)."""
+    x = per_head_qk(x)
     B, _, H, dk = x["q"].shape
     dv, L = x["v"].shape[-1], x["lam"].shape[-1]
     S = np.zeros((B, H, L, dk, dv))
@@ -57,11 +58,12 @@ def test_prefill_state_simt(LL, T, C):
     print(f"simt T={T}: state rel_l2={err:.2e}")
 
 
-@pytest.mark.parametrize("T,dv", [(1, 128), (128, 128), (300, 128), (1000, 128), (2049, 128),
-                                  (1, 64), (300, 64), (2049, 64)])
-def test_prefill_state_tc(LL, T, dv):
+@pytest.mark.parametrize("T,dv,Hqk", [(1, 128, 0), (128, 128, 0), (300, 128, 0), (1000, 128, 0),
+                                      (2049, 128, 0), (1, 64, 0), (300, 64, 0), (2049, 64, 0),
+                                      (2049, 64, 1)])
+def test_prefill_state_tc(LL, T, dv, Hqk):
     L = max((T - 1).bit_length() + 1, 1)
-    cfg = W.FwdConfig("p", 2, 3, T, 128, dv, 64, L, "bf16", True, "softplus", seed=T + 5)
+    cfg = W.FwdConfig("p", 2, 3, T, 128, dv, 64, L, "bf16", True, "softplus", seed=T + 5, Hqk=Hqk)
     x = W.make_fwd_inputs(cfg)
     d = cuda(x)
     assert LL.resolve_path(128, dv, 64, 1) == "tc"
@@ -72,15 +74,18 @@ def test_prefill_state_tc(LL, T, dv):
     print(f"tc T={T}: state rel_l2={err:.2e}")
 
 
-@pytest.mark.parametrize("path,T,dk,dv,dtype", [("simt", 300, 16, 16, "f32"),
-                                                ("tc", 1151, 128, 128, "bf16"),
-                                                ("tc", 1151, 128, 64, "bf16")])
-def test_decode_continues_from_prefill(LL, path, T, dk, dv, dtype):
+@pytest.mark.parametrize("path,T,dk,dv,dtype,H,Hqk", [("simt", 300, 16, 16, "f32", 2, 2),
+                                                      ("tc", 1151, 128, 128, "bf16", 2, 2),
+                                                      ("tc", 1151, 128, 64, "bf16", 2, 2),
+                                                      ("simt", 300, 16, 16, "f32", 4, 2),
+                                                      ("tc", 1151, 128, 64, "bf16", 4, 1)])
+def test_decode_continues_from_prefill(LL, path, T, dk, dv, dtype, H, Hqk):
     """Prefill T positions, then decode positions T..T+n-1 from the handed-over state; the
-    outputs must match the direct form over the whole T+n sequence."""
+    outputs must match the direct form over the whole T+n sequence (q/k shared by groups of
+    H / Hqk heads where Hqk < H)."""
     n = 6
     L = (T + n - 1).bit_length() + 1
-    cfg = W.FwdConfig("pd", 2, 2, T + n, dk, dv, 64, L, dtype, True, "softplus", seed=11)
+    cfg = W.FwdConfig("pd", 2, H, T + n, dk, dv, 64, L, dtype, True, "softplus", seed=11, Hqk=Hqk)
     x = W.make_fwd_inputs(cfg)
     d = cuda(x)
     pre = {k: (None if v is None else v[:, :T].contiguous()) for k, v in d.items()}
@@ -95,7 +100,8 @@ def test_decode_continues_from_prefill(LL, path, T, dk, dv, dtype):
     torch.cuda.synchronize()
     got = torch.stack(outs, dim=1).cpu()  # [B, n, H, dv]
     rows = np.arange(T, T + n)
-    want = oracle.forward_direct(x["q"], x["k"], x["v"], x["log_a"], x["lam"], rows=rows)[:, rows]
+    xp = per_head_qk(x)
+    want = oracle.forward_direct(xp["q"], xp["k"], xp["v"], xp["log_a"], xp["lam"], rows=rows)[:, rows]
     tol = TOL_F32 if dtype == "f32" else TOL_BF16
     err = rel_l2(got, want)
     print(f"{path}: continuation rel_l2={err:.2e}")

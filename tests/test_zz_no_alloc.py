@@ -39,7 +39,7 @@ def test_noalloc_matches_workspace_entry_point(path, cfg):
             ctypes.c_void_p(d["v"].data_ptr()),
             None if d["log_a"] is None else ctypes.c_void_p(d["log_a"].data_ptr()),
             ctypes.c_void_p(d["lam"].data_ptr()), ctypes.c_void_p(got.data_ptr()),
-            cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv, cfg.L, cfg.C, LL._binding._dtype_code(d["q"]),
+            cfg.B, cfg.T, cfg.H, cfg.H, cfg.dk, cfg.dv, cfg.L, cfg.C, LL._binding._dtype_code(d["q"]),
             LL._binding._dtype_code(got), LL._binding.PATHS[path],
             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert st == 0, LL.status_string(st)
@@ -56,5 +56,5 @@ def test_noalloc_rejects_oversized_problem():
     st = LL.lib().loglinear_fwd_noalloc(
         ctypes.c_void_p(big.data_ptr()), ctypes.c_void_p(big.data_ptr()),
         ctypes.c_void_p(big.data_ptr()), None, ctypes.c_void_p(big.data_ptr()),
-        ctypes.c_void_p(big.data_ptr()), 1, 16384, 16, 128, 128, 15, 64, 1, 1, 0, None)
+        ctypes.c_void_p(big.data_ptr()), 1, 16384, 16, 16, 128, 128, 15, 64, 1, 1, 0, None)
     assert st == LL._binding.LL_ERR_WORKSPACE

@@ -43,6 +43,11 @@ class FwdConfig:
     decay: bool         # Mamba-2 decay (True) or M^S all ones (False)
     lam: str            # "uniform" (U(0,1)) or "softplus" (softplus(N(0,1)))
     seed: int = 0
+    Hqk: int = 0        # q/k heads shared by the H value heads (0: one q/k per head)
+
+    @property
+    def qk_heads(self) -> int:
+        return self.Hqk or self.H
 
     def with_(self, **kw) -> "FwdConfig":
         return replace(self, **kw)
@@ -84,11 +89,11 @@ def _gen(seed: int) -> torch.Generator:
 
 def make_fwd_inputs(cfg: FwdConfig):
     """Returns dict(q, k, v, log_a, lam) of CPU tensors in the product's layout:
-    q, k [B,T,H,dk]; v [B,T,H,dv]; log_a [B,T,H] fp32 or None; lam [B,T,H,L] fp32."""
+    q, k [B,T,Hqk,dk]; v [B,T,H,dv]; log_a [B,T,H] fp32 or None; lam [B,T,H,L] fp32."""
     g = _gen(cfg.seed)
-    B, T, H = cfg.B, cfg.T, cfg.H
-    q = torch.randn(B, T, H, cfg.dk, generator=g) / math.sqrt(cfg.dk)
-    k = torch.randn(B, T, H, cfg.dk, generator=g) / math.sqrt(cfg.dk)
+    B, T, H, G = cfg.B, cfg.T, cfg.H, cfg.qk_heads
+    q = torch.randn(B, T, G, cfg.dk, generator=g) / math.sqrt(cfg.dk)
+    k = torch.randn(B, T, G, cfg.dk, generator=g) / math.sqrt(cfg.dk)
     v = torch.randn(B, T, H, cfg.dv, generator=g)
     a_noise = torch.randn(B, T, H, generator=g)
     l_noise = torch.randn(B, T, H, cfg.L, generator=g)
