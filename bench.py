@@ -92,7 +92,8 @@ def fwd_algorithmic(cfg):
     e = 2 if cfg.dtype == "bf16" else 4
     BH = cfg.B * cfg.H
     tok = cfg.B * cfg.T * cfg.H
-    bytes_ = tok * (2 * cfg.dk + cfg.dv) * e + tok * 4 + tok * cfg.L * 4 + tok * cfg.dv * e
+    tok_qk = cfg.B * cfg.T * cfg.qk_heads     # q/k are shared by groups of heads
+    bytes_ = tok_qk * 2 * cfg.dk * e + tok * cfg.dv * e + tok * 4 + tok * cfg.L * 4 + tok * cfg.dv * e
     C = cfg.C
     N = cfg.T // C
     intra = C * (C + 1) / 2 * 2 * (cfg.dk + cfg.dv) * N
@@ -322,6 +323,8 @@ def run_ours(args, rank, world, local_rank):
                          "dv": dcfg.dv, "L": dcfg.L, "t": dcfg.t, "state": "fp32"}}
     e2e = measure_e2e(LL, cfg, x, dev, ws, args)
     prefill = measure_prefill(LL, cfg, d, out, ws, flush, peaks)
+    del ws
+    bench_shape = measure_benchmark_shape(LL, W.FWD_CONFIGS["mva_B2H48_T16384"], dev, flush, peaks)
     res = {"metric": METRIC, "value": fwd_tok_s, "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": (fwd_mean + dec_mean) * 1e3, "higher_is_better": True,
@@ -335,7 +338,7 @@ def run_ours(args, rank, world, local_rank):
                       "parallelism": f"replicas x{world} (independent (b,h) work, no collective)"},
            "fwd_ms": fwd_mean * 1e3, "fwd_stage_us": dict(zip(stage_names, [s * 1e6 for s in stage_mean])),
            "roofline": roofline, "roofline_fwd": roofline_fwd, "decode": decode, "e2e": e2e,
-           "prefill": prefill,
+           "prefill": prefill, "benchmark_shape": bench_shape,
            "gpu_launches": args.steps * (n_kernels + 1), "clocks": clk,
            "wall_s_timed_region": wall}
     return res
@@ -349,11 +352,11 @@ def stage_bytes(cfg, path, name):
     N = -(-cfg.T // tile)
     st = cfg.B * cfg.H * N * cfg.dk * cfg.dv
     node_e = 2 if path == "tc" else 4
-    qkv = tok * (2 * cfg.dk + cfg.dv) * e
+    qkv = cfg.B * cfg.T * cfg.qk_heads * 2 * cfg.dk * e + tok * cfg.dv * e
     if name == "tc_forward":  # one kernel: q, k, v, log a, lambda in, out out
         return qkv + tok * 4 + tok * cfg.L * 4 + tok * cfg.dv * e
     if name.endswith("chunk_state"):
-        return tok * (cfg.dk + cfg.dv) * e + tok * 4 + st * 4
+        return cfg.B * cfg.T * cfg.qk_heads * cfg.dk * e + tok * cfg.dv * e + tok * 4 + st * 4
     if name.endswith("level_scan"):
         return st * 4 + st * node_e
     return qkv + tok * 4 + tok * cfg.L * 4 + st * node_e + tok * cfg.dv * e
@@ -394,6 +397,41 @@ def measure_prefill(LL, cfg, d, out, ws, flush, peaks, reps=10):
             "state_kernel_gbs": (state_bytes + read_bytes) / t_state / 1e9,
             "note": "state kernel = prefill - forward (medians); bytes = fp32 state written "
                     "+ bf16 block states read"}
+
+
+def measure_benchmark_shape(LL, cfg, dev, flush, peaks, reps=10):
+    """The forward on the pages' kernel-benchmark shape (B2, 48 heads, d_v 64, d_k 128,
+    one q/k shared by all heads): median of `reps` calls, L2 flushed before each call
+    outside the events; tokens/s counts B*T tokens (all heads)."""
+    x = W.make_fwd_inputs(cfg)
+    d = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
+    out = torch.empty(cfg.B, cfg.T, cfg.H, cfg.dv, device=dev, dtype=d["q"].dtype)
+    ws = torch.empty(LL.fwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv, cfg.C, 1),
+                     device=dev, dtype=torch.uint8)
+    ts = []
+    for i in range(reps + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C, out=out,
+                         workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+    if LL.device_error() != 0:
+        raise RuntimeError("tensor-core forward reported a device error")
+    t = statistics.median(ts)
+    fbytes, fflops = fwd_algorithmic(cfg)
+    return {"workload": f"{cfg.name}: loglinear_fwd B{cfg.B} H{cfg.H} (q/k heads "
+                        f"{cfg.qk_heads}) T{cfg.T} dk={cfg.dk} dv={cfg.dv} C{cfg.C} L{cfg.L} bf16",
+            "path": LL.resolve_path(cfg.dk, cfg.dv, cfg.C, 1), "fwd_us": t * 1e6,
+            "tokens_per_s": cfg.B * cfg.T / t,
+            "roofline": {"bound": "hbm", "achieved": fbytes / t / 1e9, "peak": peaks["hbm"],
+                         "unit": "GB/s", "frac": fbytes / t / 1e9 / peaks["hbm"],
+                         "algorithmic_bytes": fbytes, "peak_source": peaks["src"],
+                         "tensor_frac": fflops / t / 1e12 / peaks["bf16"],
+                         "algorithmic_flops": fflops}}
 
 
 def measure_e2e(LL, cfg, x, dev, ws, args):

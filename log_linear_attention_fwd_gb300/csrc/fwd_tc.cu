@@ -104,13 +104,12 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
 //      128..128+d_v (the tile's chunk state, d_k x d_v).
 //   4. (after 5) P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t,s)] on the causal half, bf16
 //      into the K buffer; O = P V into columns 0..d_v.
-//   5. Right after the state MMA (before P): U_j is published (staged bf16 in the Q
+//   5. Right after the state MMA (before P): U_j is published (staged bf16 in the K
 //      buffer, stored coalesced); for odd j the CTA then forms the block state of slot
-//      j+1 (below) and publishes it; Q is loaded again by TMA for the levels.
+//      j+1 (below) and publishes it.  Q stays in shared memory for step 6.
 //   6. For every set bit m-1 of j, in increasing m: the block state of slot c_m by TMA
 //      into shared memory (two buffers), MMA Q Tot into one of two TMEM buffers (columns
-//      0.. and 128..), and the
-//      previous level's product added to O with the row weights
+//      0.. and 128..), and the previous level's product added to O with the row weights
 //      lambda[t, 7+m] exp(cs_t + D_m).  D_m, the log decay from the block's end to the
 //      tile's start, is the sum of the log decays of the lower levels' blocks, which
 //      their producers store next to them.
@@ -211,8 +210,8 @@ __global__ void __launch_bounds__(kThreadsF, 2)
                       const __grid_constant__ CUtensorMap tmNode, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* Qb = smem + FSmem::kQ;    // Q, then U in bf16, then Q again, then the output
-  uint8_t* Kb = smem + FSmem::kK;    // K, then w ⊙ K, then P, then block states
+  uint8_t* Qb = smem + FSmem::kQ;    // Q (kept for the level MMAs), then the output
+  uint8_t* Kb = smem + FSmem::kK;    // K, then w ⊙ K, then U in bf16, then P, then block states
   uint8_t* Vb = smem + FSmem::kV;    // V, then block states
   using G = Dv<DV>;
   constexpr int kStatePieces = G::kStatePieces;
@@ -223,8 +222,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint64_t* bar_o = &bars[3];
   uint64_t* bar_lvl = &bars[4];      // [2]: level MMAs
   uint64_t* bar_node = &bars[6];     // [2]: block-state loads
-  uint64_t* bar_q = &bars[8];        // Q loaded again for the levels
-  uint64_t* bar_free = &bars[9];     // [2]: every warp has read a level's TMEM buffer
+  uint64_t* bar_free = &bars[8];     // [2]: every warp has read a level's TMEM buffer
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + FSmem::kTslot);
   uint32_t* ints = reinterpret_cast<uint32_t*>(smem + FSmem::kInt);  // [0] ticket
   float* red = reinterpret_cast<float*>(smem + FSmem::kRed);
@@ -253,7 +251,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     prefetch_tensormap(&tmOut);
     prefetch_tensormap(&tmU);
     prefetch_tensormap(&tmNode);
-    for (int q = 0; q < 9; ++q) mbar_init(&bars[q], 1);
+    for (int q = 0; q < 8; ++q) mbar_init(&bars[q], 1);
     mbar_init(&bar_free[0], kThreadsF / 32);
     mbar_init(&bar_free[1], kThreadsF / 32);
     fence_mbar_init();
@@ -365,9 +363,9 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
 
-  // ---- publish U_j (staged bf16 in Qb, which S no longer reads, then stored coalesced)
-  // and, for odd j, form the block state of slot j+1 and publish it; then Q comes back
-  // by TMA for the levels.  Published states are row-major [d_k][d_v] bf16; thread tid
+  // ---- publish U_j (staged bf16 in Kb, which the state MMA no longer reads, then stored
+  // coalesced) and, for odd j, form the block state of slot j+1 and publish it.  Q stays
+  // in Qb for the level MMAs.  Published states are row-major [d_k][d_v] bf16; thread tid
   // moves the 16-byte pieces q = it * 256 + tid.  This runs even after an error, so that
   // no reader waits for a flag that is never raised.
   const uint8_t* Ug = p.U + bh * N * G::kStateBytes;
@@ -377,10 +375,10 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint32_t* rdy_u = p.rdy_u + bh * N;
   uint32_t* rdy_n = p.rdy_n + bh * N;
 #pragma unroll
-  for (int c = 0; c < G::kPanels; ++c) {  // U row r (d_k), this thread's half of d_v -> Qb
+  for (int c = 0; c < G::kPanels; ++c) {  // U row r (d_k), this thread's half of d_v -> Kb
     float v[32];
     tmem_ld32(tmem + lane_base + 128 + G::kHalf * hh + 32 * c, v);
-    put_row32_bf16(Qb, r, G::kPanels * hh + c, v);
+    put_row32_bf16(Kb, r, G::kPanels * hh + c, v);
   }
   __syncthreads();
   const bool forms = (j & 1) && j + 1 < N;  // odd j forms the block state of slot j+1
@@ -388,7 +386,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
 #pragma unroll
   for (int it = 0; it < kStatePieces; ++it) {
     const int q = it * kThreadsF + tid;
-    const uint4 w = *reinterpret_cast<const uint4*>(Qb + piece_offset<DV>(q));
+    const uint4 w = *reinterpret_cast<const uint4*>(Kb + piece_offset<DV>(q));
     reinterpret_cast<uint4*>(const_cast<uint8_t*>(Ug) + (int64_t)j * G::kStateBytes)[q] = w;
     const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -443,14 +441,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     if (tid == 0) st_release_gpu(&rdy_n[c], 1u);
   }
 
-  __syncthreads();  // Qb is no longer read
-  if (tid == 0 && nlev > 0) {
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar_q, kOperand);
-    tma_load_4d(&tmQ, bar_q, Qb, 0, hq, t0, b);
-    tma_load_4d(&tmQ, bar_q, Qb + kPanel, 64, hq, t0, b);
-  }
-  __syncwarp();
+  __syncthreads();  // the staged U in Kb is no longer read
 
   // ---- P, bf16 into Kb (the state MMA is done with it).  The two warps of
   // quarter qt take the 32-column chunks of their parity: chunks c > qt lie above the
@@ -585,7 +576,6 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint32_t lvl_ph[2] = {0, 0}, node_ph[2] = {0, 0}, free_ph[2] = {0, 0};
   float D = 0.f;  // log decay from block k's end to the tile's start
   bool lv_ok = all_ok;
-  if (tid == 0 && nlev > 0 && lv_ok) lv_ok = mbar_wait(bar_q, 0);  // Q is back
   for (int k = 0; k <= nlev && all_ok; ++k) {
     if (tid == 0 && k < nlev) {  // issue level k
       bool go = lv_ok && mbar_wait(&bar_node[k & 1], node_ph[k & 1]);

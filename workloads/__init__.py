@@ -16,6 +16,9 @@ Recipes (shapes, distributions) are the five workloads the method is measured on
                       (the pages' pretraining length; the headline forward workload).
 * ``decode_B128``     decode step at t=12345, B128 H16 dk=dv=128 L15, fp32 states, bf16
                       tokens, Mamba-2 distributions.
+* ``mva_B2H48_T16384`` the pages' kernel-benchmark shape: bf16, B2, 48 heads, head dim
+                      (d_v) 64, state dim (d_k) 128, C64, one q/k shared by all heads
+                      (Mamba-2's multi-value form), T16384 L15, Mamba-2 distributions.
 
 Draw order for a forward input: q, k, v, log-a noise, lambda noise, all fp32 from one
 CPU ``torch.Generator`` seeded with ``seed``; bf16 workloads cast after drawing.
@@ -72,6 +75,8 @@ FWD_CONFIGS = {
     "mamba2_T1024": FwdConfig("mamba2_T1024", 2, 4, 1024, 64, 64, 64, 11, "f32", True, "softplus"),
     "mamba2_T4096": FwdConfig("mamba2_T4096", 4, 16, 4096, 128, 128, 64, 13, "bf16", True, "softplus"),
     "mamba2_T16384": FwdConfig("mamba2_T16384", 1, 16, 16384, 128, 128, 64, 15, "bf16", True, "softplus"),
+    "mva_B2H48_T16384": FwdConfig("mva_B2H48_T16384", 2, 48, 16384, 128, 64, 64, 15, "bf16", True,
+                                  "softplus", Hqk=1),
 }
 DECODE_CONFIG = DecodeConfig("decode_B128", 128, 16, 128, 128, 15, 12345)
 HEADLINE_FWD = "mamba2_T16384"
