@@ -1,5 +1,6 @@
 """CPU oracle (test infrastructure only; see loglinear_oracle's header)."""
 from .loglinear_oracle import (  # noqa: F401
+    backward_direct,
     decay_rows,
     decode_step,
     fenwick_partition,

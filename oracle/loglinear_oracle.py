@@ -164,6 +164,58 @@ def forward_direct(q, k, v, log_a, lam, rows=None, heads=None):
     return out
 
 
+def backward_direct(q, k, v, log_a, lam, dout):
+    """Gradients of sum(dout ⊙ O) for O = (Q K^T ⊙ M^S ⊙ M^H) V, by the chain rule on the
+    dense definition, fp64.
+
+    News article, section 讨论与局限性: training needs, besides the gradients of the
+    attention terms, those of the level weights lambda; its Figure 4 times the forward and
+    backward kernels.  With A = Q K^T, M = M^S ⊙ M^H and dA = dO V^T:
+        dV = (A ⊙ M)^T dO,   dQ = (dA ⊙ M) K,   dK = (dA ⊙ M)^T Q,
+        dlam[t, l] = sum over s with level(t, s) = l of dA[t, s] A[t, s] M^S[t, s],
+    and, since M^S[t, s] = exp(cum_t - cum_s) with cum the prefix sums of log a,
+        dcum_t = sum_s G[t, s] - sum_t' G[t', t]   (G = dA ⊙ A ⊙ M),
+        dlog_a[i] = sum over t >= i of dcum_t.
+    Rows are taken in blocks of 512 (evaluation order only).
+
+    Returns dict(q, k, v, log_a, lam) of fp64 arrays in the input layouts (log_a is None
+    when log_a is None).
+    """
+    q, k, v, lam, do = _f64(q), _f64(k), _f64(v), _f64(lam), _f64(dout)
+    log_a = _f64(log_a)
+    B, T, H, dk = q.shape
+    dv, L = v.shape[-1], lam.shape[-1]
+    g = {"q": np.zeros_like(q), "k": np.zeros_like(k), "v": np.zeros_like(v),
+         "lam": np.zeros_like(lam), "log_a": None if log_a is None else np.zeros_like(log_a)}
+    for b in range(B):
+        for h in range(H):
+            Q, K, V, dO = q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h]
+            la = None if log_a is None else log_a[b, :, h]
+            row_sum = np.zeros(T)
+            col_sum = np.zeros(T)
+            for r0 in range(0, T, 512):
+                rr = np.arange(r0, min(T, r0 + 512))
+                MS = decay_rows(la, rr, T)
+                M = MS * hier_rows(lam[b, :, h, :], rr, T)
+                A = Q[rr] @ K.T
+                dA = dO[rr] @ V.T
+                dAM = dA * M
+                g["q"][b, rr, h] = dAM @ K
+                g["k"][b, :, h] += dAM.T @ Q[rr]
+                g["v"][b, :, h] += (A * M).T @ dO[rr]
+                W = dA * A * MS
+                for i, t in enumerate(rr):
+                    lv = level_row(int(t))
+                    np.add.at(g["lam"][b, t, h], lv, W[i, : t + 1])
+                G = dAM * A
+                row_sum[rr] = G.sum(axis=1)
+                col_sum += G.sum(axis=0)
+            if la is not None:
+                dcum = row_sum - col_sum
+                g["log_a"][b, :, h] = np.cumsum(dcum[::-1])[::-1]
+    return g
+
+
 # --------------------------------------------------------------------------------------
 # L2a: per-level states and the lssb decode recurrence
 # --------------------------------------------------------------------------------------
