@@ -178,6 +178,35 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
                           int64_t L, int in_dtype, int out_dtype, ll_stream_t stream);
 
 /*
+ * Backward of loglinear_fwd (page "算力终结者来了！…", sections 结构矩阵 and 讨论与局限性:
+ * training takes the gradients of the attention terms and of the level weights lambda):
+ * given dout = dL/dO, the gradients of L with respect to every input, for
+ * O = (Q K^T ⊙ M^S ⊙ M^H) V exactly as loglinear_fwd defines it:
+ *   dq, dk  [B, T, Hqk, dk]  grad_dtype (summed over the heads that share a q/k head)
+ *   dv      [B, T, H, dv]    grad_dtype
+ *   dlog_a  [B, T, H] fp32   (required when log_a is given; ignored when log_a is NULL)
+ *   dlambda [B, T, H, L] fp32 (levels above bit_length(T-1) receive 0)
+ *   dout    [B, T, H, dv]    grad_dtype
+ * q, k, v, log_a, lambda, B, T, H, Hqk, dk, dv and L as in loglinear_fwd; no chunk
+ * argument: the gradients do not depend on it (the kernels work on 32-token tiles, fp32
+ * on CUDA cores).  1 <= dk, dv <= 128, L <= 64.  All outputs are fully overwritten.
+ * workspace: device scratch of at least loglinear_bwd_workspace_size() bytes, 256-byte
+ * aligned (recomputed forward states, per-head q and k gradients).
+ * Errors: LL_ERR_INVALID (null pointer, negative size, dlog_a NULL with log_a given),
+ * LL_ERR_SHAPE (L too small, Hqk not dividing H), LL_ERR_DTYPE, LL_ERR_UNSUPPORTED,
+ * LL_ERR_WORKSPACE, LL_ERR_ALIGN (workspace), LL_ERR_CUDA.
+ */
+LL_API int loglinear_bwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Hqk,
+                                        int64_t dk, int64_t dv, int64_t L, int in_dtype,
+                                        int grad_dtype, size_t* bytes);
+LL_API int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_a,
+                         const float* lambda, const void* dout, void* dq, void* dk, void* dv,
+                         float* dlog_a, float* dlambda, int64_t B, int64_t T, int64_t H,
+                         int64_t Hqk, int64_t dk_dim, int64_t dv_dim, int64_t L, int in_dtype,
+                         int grad_dtype, void* workspace, size_t workspace_bytes,
+                         ll_stream_t stream);
+
+/*
  * Reads and clears the device error word of the tensor-core path (synchronises `stream`).
  * *flags = 0 when every wait of the kernels run so far completed.  Bit 0: an mbarrier
  * wait ran out of time (the CTA then skipped its remaining work and its output tile is

@@ -1,14 +1,16 @@
-"""Log-linear attention forward and lssb decode on GB300 (sm_103a).
+"""Log-linear attention forward, backward and lssb decode on GB300 (sm_103a).
 
 Python face of the C ABI in include/loglinear.h; see ``_binding`` for the calls.
 """
 from ._binding import (  # noqa: F401
     LIB_PATH,
     LoglinearError,
+    bwd_workspace_size,
     debug_level_map,
     device_error,
     fwd_workspace_size,
     lib,
+    loglinear_bwd,
     loglinear_decode_step,
     loglinear_fwd,
     loglinear_fwd_noalloc,

@@ -1,0 +1,569 @@
+// Backward on CUDA cores in fp32 (any d_k, d_v <= 128; fp32 or bf16 inputs and gradients).
+//
+// The gradients of sum(dO ⊙ O) for O = (Q K^T ⊙ M) V, M[t, s] = exp(cum_t - cum_s)
+// lambda[t, l(t, s)] (page "算力终结者来了！…", sections 结构矩阵 and 讨论与局限性: training
+// needs the lambda gradients besides the attention ones), taken through the same chunked
+// decomposition as the forward (page "论文阅读：Log-Linear Attention", sections 矩阵分解 and
+// 两阶段计算) on tiles of 32 tokens:
+//
+//   dQ_t  = sum_s M[t, s] (dO_t . v_s) k_s
+//         = intra-tile pairs + sum over the set bits m-1 of the tile index of
+//           lambda[t, 5+m] exp(cs_t + D_m) Tot_m dO_t, Tot_m the forward's block state
+//           (d_k x d_v, decayed to its end);
+//   dlambda[t, l] = sum over the level-l bucket of exp(...) (dO_t . v_s)(q_t . k_s); on an
+//           inter-tile level exp(cs_t + D_m) q_t^T Tot_m dO_t;
+//   dK_s  = sum_t M[t, s] (dO_t . v_s) q_t,   dV_s = sum_t M[t, s] (q_t . k_s) dO_t:
+//           the same pairs seen from the source.  Source s in tile i meets, at tile level
+//           m (bit m-1 of i clear), the queries of the aligned block of 2^(m-1) tiles
+//           starting at c' = ((i >> (m-1)) | 1) << (m-1); lambda[t, 5+m] depends on t, so
+//           it is folded into that block's mirrored state
+//           R_c' = sum_t exp(cum_t - cum_start(c')) lambda[t, 5+m] q_t dO_t^T, and
+//           dK_s += exp(cum_start(c') - cum_s) R_c' v_s,  dV_s += (same) R_c'^T k_s;
+//   dcum_t = q_t . dQ_t - k_t . dK_t  (the row and column sums of dA ⊙ A ⊙ M), and
+//   dlog_a_i = sum over t >= i of dcum_t.
+//
+// Kernels: the forward's K1/K2 recompute U, the block states and the tile log decays;
+// bwd_dq (dQ, dlambda, q.dQ); bwd_rstate (R, accumulated over the block's tiles with
+// float4 atomics into the U buffer, which the level scan no longer needs); bwd_dkv (dK,
+// dV, k.dK); bwd_reduce_qk (per-head dQ, dK summed over the heads sharing a q/k head,
+// cast to the gradient type); bwd_dlog_a (reverse prefix sums over t).
+#include <algorithm>
+
+#include "ll_internal.cuh"
+
+namespace ll {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kC = kBwdTile;          // tokens per tile
+constexpr int kLc = 5;                // log2(kC)
+constexpr int kSub = kThreads / kC;   // threads per tile row (8, lanes of one warp)
+constexpr int kPer = 128 / kSub;      // features per thread and operand (d <= 128)
+constexpr int kStage = 32;            // rows of a d_k x d_v state staged at a time
+static_assert(kC == 1 << kLc, "tile");
+
+template <typename T>
+__device__ __forceinline__ float ld(const void* p, int64_t i) {
+  return to_f32(reinterpret_cast<const T*>(p)[i]);
+}
+
+// Sum over the kSub lanes of one tile row (all 32 lanes of the warp must call it).
+__device__ __forceinline__ float row_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  return x;
+}
+
+// Shared-memory views of one tile's rows (row strides padded by one float) and its
+// tile-local inclusive prefix sums of log a.
+struct TileRows {
+  float *q, *k, *v, *g, *cs, *lam;
+  int lq, lv;
+};
+
+template <typename InT, typename GT>
+__device__ void load_tile(const BwdArgs& A, int b, int h, int t0, int n, const TileRows& s) {
+  const FwdArgs& a = A.f;
+  const int dk = a.dk, dv = a.dv, L = a.L, hq = h / a.hg;
+  if (threadIdx.x == 0) {
+    float run = 0.f;
+    for (int r = 0; r < kC; ++r) {
+      if (r < n && a.log_a) run += a.log_a[((int64_t)b * a.T + t0 + r) * a.H + h];
+      s.cs[r] = run;
+    }
+  }
+  for (int idx = threadIdx.x; idx < kC * dk; idx += kThreads) {
+    const int r = idx / dk, c = idx - r * dk;
+    const int64_t row = ((int64_t)b * a.T + t0 + r) * a.Hqk + hq;
+    s.q[r * s.lq + c] = r < n ? ld<InT>(a.q, row * dk + c) : 0.f;
+    s.k[r * s.lq + c] = r < n ? ld<InT>(a.k, row * dk + c) : 0.f;
+  }
+  for (int idx = threadIdx.x; idx < kC * dv; idx += kThreads) {
+    const int r = idx / dv, c = idx - r * dv;
+    const int64_t row = ((int64_t)b * a.T + t0 + r) * a.H + h;
+    s.v[r * s.lv + c] = r < n ? ld<InT>(a.v, row * dv + c) : 0.f;
+    s.g[r * s.lv + c] = r < n ? ld<GT>(A.dout, row * dv + c) : 0.f;
+  }
+  for (int idx = threadIdx.x; idx < kC * L; idx += kThreads) {
+    const int r = idx / L;
+    s.lam[idx] =
+        r < n ? a.lam[(((int64_t)b * a.T + t0 + r) * a.H + h) * L + (idx - r * L)] : 0.f;
+  }
+}
+
+__host__ __device__ inline size_t tile_rows_floats(int dk, int dv, int L) {
+  return (size_t)2 * kC * (dk + 1) + (size_t)2 * kC * (dv + 1) + kC + (size_t)kC * L;
+}
+
+__device__ TileRows carve_rows(float* sm, int dk, int dv) {
+  TileRows s;
+  s.lq = dk + 1;
+  s.lv = dv + 1;
+  s.q = sm;
+  s.k = s.q + kC * s.lq;
+  s.v = s.k + kC * s.lq;
+  s.g = s.v + kC * s.lv;
+  s.cs = s.g + kC * s.lv;
+  s.lam = s.cs + kC;
+  return s;
+}
+
+// ---------------------------------------------------------------- dQ, dlambda, q . dQ
+
+template <typename InT, typename GT>
+__global__ void __launch_bounds__(kThreads) bwd_dq_kernel(BwdArgs A) {
+  extern __shared__ float sm[];
+  const FwdArgs& a = A.f;
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int dk = a.dk, dv = a.dv, L = a.L;
+  const int t0 = j * kC, n = min(kC, a.T - t0);
+  const int64_t bh = (int64_t)b * a.H + h;
+  const TileRows s = carve_rows(sm, dk, dv);
+  float* Ap = s.lam + kC * L;       // [kC][kC+1] exp(cs_t - cs_s) lambda (dO_t . v_s)
+  float* Wm = Ap + kC * (kC + 1);   // [kC][kC+1] exp(cs_t - cs_s) (dO_t . v_s)(q_t . k_s)
+  float* Sb = Wm + kC * (kC + 1);   // [kStage][dv+1] staged block-state rows
+  float* dl = Sb + kStage * s.lv;   // [kC][L] dlambda of the tile's rows
+  load_tile<InT, GT>(A, b, h, t0, n, s);
+  for (int idx = threadIdx.x; idx < kC * L; idx += kThreads) dl[idx] = 0.f;
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kC * kC; idx += kThreads) {
+    const int t = idx >> kLc, u = idx & (kC - 1);
+    float ap = 0.f, w = 0.f;
+    if (u <= t && t < n) {
+      float dov = 0.f, qk = 0.f;
+      for (int e = 0; e < dv; ++e) dov = fmaf(s.g[t * s.lv + e], s.v[u * s.lv + e], dov);
+      for (int d = 0; d < dk; ++d) qk = fmaf(s.q[t * s.lq + d], s.k[u * s.lq + d], qk);
+      const float ex = expf(s.cs[t] - s.cs[u]);
+      // t0 is a multiple of the tile, so the level depends on the tile-local indices only
+      ap = ex * s.lam[t * L + fenwick_level((uint32_t)t, (uint32_t)u)] * dov;
+      w = ex * dov * qk;
+    }
+    Ap[t * (kC + 1) + u] = ap;
+    Wm[t * (kC + 1) + u] = w;
+  }
+  __syncthreads();
+  // intra-tile dlambda: level 0 is the pair (t, t); level l >= 1 (bit l-1 of t set) the
+  // sources [hi - 2^(l-1), hi), hi = t with its low l-1 bits cleared
+  if (threadIdx.x < kC * (kLc + 1)) {
+    const int t = threadIdx.x / (kLc + 1), l = threadIdx.x - t * (kLc + 1);
+    if (t < n && l < L) {
+      float x = 0.f;
+      if (l == 0) {
+        x = Wm[t * (kC + 1) + t];
+      } else if ((t >> (l - 1)) & 1) {
+        const int hi = (t >> (l - 1)) << (l - 1);
+        for (int u = hi - (1 << (l - 1)); u < hi; ++u) x += Wm[t * (kC + 1) + u];
+      }
+      dl[t * L + l] = x;
+    }
+  }
+  // dQ: this thread's row t, features d = sub + kSub i
+  const int t = threadIdx.x / kSub, sub = threadIdx.x % kSub;
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  for (int u = 0; u <= t; ++u) {
+    const float p = Ap[t * (kC + 1) + u];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int d = sub + kSub * i;
+      if (d < dk) acc[i] = fmaf(p, s.k[u * s.lq + d], acc[i]);
+    }
+  }
+  // inter-tile levels: Tot_m dO_t for the block state of slot c
+  const int64_t elems = (int64_t)dk * dv;
+  const float* nodes = reinterpret_cast<const float*>(a.nodes) + bh * a.N * elems;
+  const float* lg = a.lg + bh * a.N;
+  for (int m = 1; (int64_t(1) << (m - 1)) <= j; ++m) {
+    int64_t c;
+    if (!inter_block(j, m, &c)) continue;
+    float D = 0.f;  // log decay from the block's end to the start of tile j
+    for (int64_t i = c; i < j; ++i) D += lg[i];
+    const float* S = nodes + c * elems;
+    float part[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) part[i] = 0.f;
+    for (int d0 = 0; d0 < dk; d0 += kStage) {
+      const int rows = min(kStage, dk - d0);
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < rows * dv; idx += kThreads) {
+        const int r = idx / dv;
+        Sb[r * s.lv + (idx - r * dv)] = S[(int64_t)d0 * dv + idx];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int d = sub + kSub * i;
+        if (d >= d0 && d < d0 + rows) {
+          const float* sr = Sb + (d - d0) * s.lv;
+          const float* gr = s.g + t * s.lv;
+          float x = 0.f;
+          for (int e = 0; e < dv; ++e) x = fmaf(sr[e], gr[e], x);
+          part[i] = x;
+        }
+      }
+    }
+    const int lvl = kLc + m;
+    const float wq = t < n ? expf(s.cs[t] + D) : 0.f;
+    const float wl = wq * s.lam[t * L + lvl];
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int d = sub + kSub * i;
+      if (d < dk) {
+        acc[i] = fmaf(wl, part[i], acc[i]);
+        dot = fmaf(s.q[t * s.lq + d], part[i], dot);
+      }
+    }
+    dot = row_sum(dot);
+    if (sub == 0 && t < n) dl[t * L + lvl] = wq * dot;
+  }
+  // outputs: per-head dQ, q . dQ, the tile rows' dlambda
+  float qd = 0.f;
+  const int64_t row = ((int64_t)b * a.T + t0 + t) * a.H + h;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int d = sub + kSub * i;
+    if (d < dk) {
+      if (t < n) A.dqh[row * dk + d] = acc[i];
+      qd = fmaf(s.q[t * s.lq + d], acc[i], qd);
+    }
+  }
+  qd = row_sum(qd);
+  if (sub == 0 && t < n && A.dcq) A.dcq[row] = qd;
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < n * L; idx += kThreads) {
+    const int r = idx / L;
+    A.dlam[(((int64_t)b * a.T + t0 + r) * a.H + h) * L + (idx - r * L)] = dl[idx];
+  }
+}
+
+// ---------------------------------------------------------------- mirrored block states
+
+// Tile j adds, for every set bit m-1 of j, its part of the mirrored state of the block
+// starting at c' = j with its low m-1 bits cleared:
+//   sum_{t in j} exp(cs_t + D) lambda[t, 5+m] q_t dO_t^T,  D = log decay over [c', j).
+// Thread (td, te) owns rows [8 td, +8) and columns [8 te, +8) of the d_k x d_v state.
+template <typename InT, typename GT>
+__global__ void __launch_bounds__(kThreads) bwd_rstate_kernel(BwdArgs A) {
+  extern __shared__ float sm[];
+  const FwdArgs& a = A.f;
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (j == 0) return;
+  const int dk = a.dk, dv = a.dv, L = a.L, hq = h / a.hg;
+  const int t0 = j * kC, n = min(kC, a.T - t0);
+  const int64_t bh = (int64_t)b * a.H + h;
+  float* Qr = sm;              // [kC][128] q, zero-padded
+  float* Qw = Qr + kC * 128;   // [kC][128] weighted q
+  float* Gd = Qw + kC * 128;   // [kC][128] dO, zero-padded
+  float* cs = Gd + kC * 128;   // [kC]
+  float* wt = cs + kC;         // [kC]
+  if (threadIdx.x == 0) {
+    float run = 0.f;
+    for (int r = 0; r < n; ++r) {
+      if (a.log_a) run += a.log_a[((int64_t)b * a.T + t0 + r) * a.H + h];
+      cs[r] = run;
+    }
+  }
+  for (int idx = threadIdx.x; idx < kC * 128; idx += kThreads) {
+    const int r = idx >> 7, c = idx & 127;
+    const int64_t rq = ((int64_t)b * a.T + t0 + r) * a.Hqk + hq;
+    const int64_t rv = ((int64_t)b * a.T + t0 + r) * a.H + h;
+    Qr[idx] = (r < n && c < dk) ? ld<InT>(a.q, rq * dk + c) : 0.f;
+    Gd[idx] = (r < n && c < dv) ? ld<GT>(A.dout, rv * dv + c) : 0.f;
+  }
+  const int64_t elems = (int64_t)dk * dv;
+  float* R = reinterpret_cast<float*>(a.U) + bh * a.N * elems;
+  const float* lg = a.lg + bh * a.N;
+  const int td = threadIdx.x >> 4, te = threadIdx.x & 15;
+  for (int m = 1; (int64_t(1) << (m - 1)) <= j; ++m) {
+    if (!((j >> (m - 1)) & 1)) continue;
+    const int64_t c0 = ((int64_t)j >> (m - 1)) << (m - 1);
+    float D = 0.f;
+    for (int64_t i = c0; i < j; ++i) D += lg[i];
+    __syncthreads();  // cs ready (first level); Qw no longer read (later levels)
+    if (threadIdx.x < kC) {
+      const int r = threadIdx.x;
+      wt[r] = r < n ? expf(cs[r] + D) *
+                          a.lam[(((int64_t)b * a.T + t0 + r) * a.H + h) * L + kLc + m]
+                    : 0.f;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < kC * 128; idx += kThreads) Qw[idx] = wt[idx >> 7] * Qr[idx];
+    __syncthreads();
+    float acc[8][8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+#pragma unroll
+      for (int y = 0; y < 8; ++y) acc[x][y] = 0.f;
+    for (int r = 0; r < n; ++r) {
+      const float4* qr = reinterpret_cast<const float4*>(Qw + r * 128 + 8 * td);
+      const float4* gr = reinterpret_cast<const float4*>(Gd + r * 128 + 8 * te);
+      const float4 q0 = qr[0], q1 = qr[1], g0 = gr[0], g1 = gr[1];
+      const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+      for (int x = 0; x < 8; ++x)
+#pragma unroll
+        for (int y = 0; y < 8; ++y) acc[x][y] = fmaf(qq[x], gg[y], acc[x][y]);
+    }
+    float* Rc = R + c0 * elems;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const int d = 8 * td + x;
+      if (d >= dk) break;
+      float* rr = Rc + (int64_t)d * dv;
+      if ((dv & 3) == 0 && 8 * te + 8 <= dv) {  // 16-byte aligned: two vector atomics
+        atomicAdd(reinterpret_cast<float4*>(rr + 8 * te),
+                  make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]));
+        atomicAdd(reinterpret_cast<float4*>(rr + 8 * te + 4),
+                  make_float4(acc[x][4], acc[x][5], acc[x][6], acc[x][7]));
+      } else {
+#pragma unroll
+        for (int y = 0; y < 8; ++y)
+          if (8 * te + y < dv) atomicAdd(rr + 8 * te + y, acc[x][y]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- dK, dV, k . dK
+
+template <typename InT, typename GT>
+__global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
+  extern __shared__ float sm[];
+  const FwdArgs& a = A.f;
+  const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int dk = a.dk, dv = a.dv, L = a.L;
+  const int t0 = i * kC, n = min(kC, a.T - t0);
+  const int64_t bh = (int64_t)b * a.H + h;
+  const TileRows s = carve_rows(sm, dk, dv);
+  float* X1 = s.lam + kC * L;       // [kC][kC+1] M[t, s] (dO_t . v_s)
+  float* X2 = X1 + kC * (kC + 1);   // [kC][kC+1] M[t, s] (q_t . k_s)
+  float* Sb = X2 + kC * (kC + 1);   // [kStage][dv+1]
+  load_tile<InT, GT>(A, b, h, t0, n, s);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kC * kC; idx += kThreads) {
+    const int t = idx >> kLc, u = idx & (kC - 1);
+    float x1 = 0.f, x2 = 0.f;
+    if (u <= t && t < n) {
+      float dov = 0.f, qk = 0.f;
+      for (int e = 0; e < dv; ++e) dov = fmaf(s.g[t * s.lv + e], s.v[u * s.lv + e], dov);
+      for (int d = 0; d < dk; ++d) qk = fmaf(s.q[t * s.lq + d], s.k[u * s.lq + d], qk);
+      const float mts =
+          expf(s.cs[t] - s.cs[u]) * s.lam[t * L + fenwick_level((uint32_t)t, (uint32_t)u)];
+      x1 = mts * dov;
+      x2 = mts * qk;
+    }
+    X1[t * (kC + 1) + u] = x1;
+    X2[t * (kC + 1) + u] = x2;
+  }
+  __syncthreads();
+  // this thread: source row u, features sub + kSub i of dK (d) and of dV (e)
+  const int u = threadIdx.x / kSub, sub = threadIdx.x % kSub;
+  float ak[kPer], av[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) ak[q] = av[q] = 0.f;
+  for (int t = u; t < kC; ++t) {
+    const float x1 = X1[t * (kC + 1) + u], x2 = X2[t * (kC + 1) + u];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int f = sub + kSub * q;
+      if (f < dk) ak[q] = fmaf(x1, s.q[t * s.lq + f], ak[q]);
+      if (f < dv) av[q] = fmaf(x2, s.g[t * s.lv + f], av[q]);
+    }
+  }
+  // inter-tile levels: the mirrored states of the blocks of later tiles
+  const int64_t elems = (int64_t)dk * dv;
+  const float* R = reinterpret_cast<const float*>(a.U) + bh * a.N * elems;
+  const float* lg = a.lg + bh * a.N;
+  const float lg_i = s.cs[kC - 1];  // this tile's log decay (tiles before the last are full)
+  for (int m = 1; (int64_t(1) << (m - 1)) < a.N; ++m) {
+    if ((i >> (m - 1)) & 1) continue;
+    const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
+    if (c1 >= a.N) continue;
+    float E = 0.f;  // log decay over the tiles strictly between i and c1
+    for (int64_t x = i + 1; x < c1; ++x) E += lg[x];
+    const float gs = u < n ? expf(lg_i - s.cs[u] + E) : 0.f;
+    const float* Rc = R + c1 * elems;
+    float pk[kPer], pv[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) pk[q] = pv[q] = 0.f;
+    for (int d0 = 0; d0 < dk; d0 += kStage) {
+      const int rows = min(kStage, dk - d0);
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < rows * dv; idx += kThreads) {
+        const int r = idx / dv;
+        Sb[r * s.lv + (idx - r * dv)] = Rc[(int64_t)d0 * dv + idx];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int f = sub + kSub * q;
+        if (f >= d0 && f < d0 + rows) {  // (R v_u)[f]
+          const float* sr = Sb + (f - d0) * s.lv;
+          const float* vr = s.v + u * s.lv;
+          float x = 0.f;
+          for (int e = 0; e < dv; ++e) x = fmaf(sr[e], vr[e], x);
+          pk[q] = x;
+        }
+        if (f < dv) {  // (R^T k_u)[f], rows d0 .. d0 + rows
+          float y = pv[q];
+          for (int r = 0; r < rows; ++r) y = fmaf(Sb[r * s.lv + f], s.k[u * s.lq + d0 + r], y);
+          pv[q] = y;
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      ak[q] = fmaf(gs, pk[q], ak[q]);
+      av[q] = fmaf(gs, pv[q], av[q]);
+    }
+  }
+  float kd = 0.f;
+  const int64_t row = ((int64_t)b * a.T + t0 + u) * a.H + h;
+  GT* dvo = reinterpret_cast<GT*>(A.dv);
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int f = sub + kSub * q;
+    if (f < dk) {
+      if (u < n) A.dkh[row * dk + f] = ak[q];
+      kd = fmaf(s.k[u * s.lq + f], ak[q], kd);
+    }
+    if (f < dv && u < n) dvo[row * dv + f] = from_f32<GT>(av[q]);
+  }
+  kd = row_sum(kd);
+  if (sub == 0 && u < n && A.dck) A.dck[row] = kd;
+}
+
+// ---------------------------------------------------------------- group sums, d log a
+
+template <typename GT>
+__global__ void __launch_bounds__(kThreads) bwd_reduce_qk_kernel(BwdArgs A, int64_t total) {
+  const FwdArgs& a = A.f;
+  const int dk = a.dk, hg = a.hg;
+  GT* dq = reinterpret_cast<GT*>(A.dq);
+  GT* dk_out = reinterpret_cast<GT*>(A.dk);
+  for (int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * kThreads) {
+    const int64_t d = idx % dk, bt_g = idx / dk;  // (b, t, q/k head g)
+    const int64_t g = bt_g % a.Hqk, bt = bt_g / a.Hqk;
+    const int64_t src = (bt * a.H + g * hg) * dk + d;
+    float x = 0.f, y = 0.f;
+    for (int r = 0; r < hg; ++r) {
+      x += A.dqh[src + (int64_t)r * dk];
+      y += A.dkh[src + (int64_t)r * dk];
+    }
+    dq[idx] = from_f32<GT>(x);
+    dk_out[idx] = from_f32<GT>(y);
+  }
+}
+
+// dlog_a_i = sum over t >= i of (q_t . dQ_t - k_t . dK_t), one CTA per (b, h), walking
+// tiles of kThreads positions from the end.
+__global__ void __launch_bounds__(kThreads) bwd_dlog_a_kernel(BwdArgs A) {
+  __shared__ float red[kThreads / 32];
+  __shared__ float carry_s;
+  const FwdArgs& a = A.f;
+  const int64_t bh = blockIdx.x;
+  const int64_t b = bh / a.H, h = bh - b * a.H;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float carry = 0.f;
+  for (int base = a.T - 1; base >= 0; base -= kThreads) {
+    const int i = base - (int)threadIdx.x;
+    const int64_t at = (b * a.T + i) * a.H + h;
+    float x = i >= 0 ? A.dcq[at] - A.dck[at] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) red[warp] = x;
+    __syncthreads();
+    float pre = 0.f;
+    for (int w = 0; w < warp; ++w) pre += red[w];
+    x += pre + carry;
+    if (i >= 0) A.dlog_a[at] = x;
+    if (threadIdx.x == kThreads - 1) carry_s = x;
+    __syncthreads();
+    carry = carry_s;
+    __syncthreads();
+  }
+}
+
+template <typename InT, typename GT>
+cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
+  const FwdArgs& a = A.f;
+  const dim3 grid(a.N, a.H, a.B);
+  const size_t rows = tile_rows_floats(a.dk, a.dv, a.L);
+  const size_t sm_dq = sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * (a.dv + 1) +
+                                        (size_t)kC * a.L);
+  const size_t sm_dkv =
+      sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * (a.dv + 1));
+  const size_t sm_r = sizeof(float) * (3 * kC * 128 + 2 * kC);
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(bwd_dq_kernel<InT, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sm_dq)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_dkv_kernel<InT, GT>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_dkv)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_rstate_kernel<InT, GT>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_r)) !=
+          cudaSuccess)
+    return e;
+  bwd_dq_kernel<InT, GT><<<grid, kThreads, sm_dq, s>>>(A);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.N > 1) {
+    const size_t rbytes = sizeof(float) * (size_t)a.B * a.H * a.N * a.dk * a.dv;
+    if ((e = cudaMemsetAsync(a.U, 0, rbytes, s)) != cudaSuccess) return e;
+    bwd_rstate_kernel<InT, GT><<<grid, kThreads, sm_r, s>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  bwd_dkv_kernel<InT, GT><<<grid, kThreads, sm_dkv, s>>>(A);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t total = (int64_t)a.B * a.T * a.Hqk * a.dk;
+  const unsigned blocks = (unsigned)std::min<int64_t>((total + kThreads - 1) / kThreads, 152 * 16);
+  bwd_reduce_qk_kernel<GT><<<blocks, kThreads, 0, s>>>(A, total);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.log_a && A.dlog_a) {
+    bwd_dlog_a_kernel<<<(unsigned)((int64_t)a.B * a.H), kThreads, 0, s>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, int64_t dk,
+                                  int64_t dv) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  BwdWorkspace w;
+  const size_t states = (size_t)(B * H * N) * (size_t)(dk * dv) * sizeof(float);
+  const size_t rows = (size_t)(B * T * H);
+  w.off_U = 0;
+  w.off_nodes = up(w.off_U + states);
+  w.off_lg = up(w.off_nodes + states);
+  w.off_dqh = up(w.off_lg + (size_t)(B * H * N) * sizeof(float));
+  w.off_dkh = up(w.off_dqh + rows * dk * sizeof(float));
+  w.off_dcq = up(w.off_dkh + rows * dk * sizeof(float));
+  w.off_dck = up(w.off_dcq + rows * sizeof(float));
+  w.total = up(w.off_dck + rows * sizeof(float));
+  return w;
+}
+
+size_t bwd_smem_max(int dk, int dv, int L) {
+  return sizeof(float) * (tile_rows_floats(dk, dv, L) + 2 * kC * (kC + 1) +
+                          (size_t)kStage * (dv + 1) + (size_t)kC * L);
+}
+
+cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype, cudaStream_t s) {
+  cudaError_t e = launch_simt_states(A.f, in_dtype, s);
+  if (e != cudaSuccess) return e;
+  if (in_dtype == LL_F32 && grad_dtype == LL_F32) return launch_typed<float, float>(A, s);
+  if (in_dtype == LL_F32) return launch_typed<float, __nv_bfloat16>(A, s);
+  if (grad_dtype == LL_F32) return launch_typed<__nv_bfloat16, float>(A, s);
+  return launch_typed<__nv_bfloat16, __nv_bfloat16>(A, s);
+}
+
+}  // namespace ll

@@ -213,7 +213,23 @@ cudaError_t launch_typed(const FwdArgs& a, cudaStream_t s, StageEvents* ev) {
   return ev ? ev->finish(s) : cudaSuccess;
 }
 
+template <typename InT>
+cudaError_t launch_states_typed(const FwdArgs& a, cudaStream_t s) {
+  const size_t sm1 = sizeof(float) * ((size_t)a.C * (a.dk + a.dv) + 2 * a.C);
+  cudaError_t e = cudaFuncSetAttribute(simt_chunk_state<InT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
+  if (e != cudaSuccess) return e;
+  simt_chunk_state<InT><<<dim3(a.N, a.H, a.B), kThreads, sm1, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return a.N > 1 ? launch_level_scan(a, s) : cudaSuccess;
+}
+
 }  // namespace
+
+cudaError_t launch_simt_states(const FwdArgs& a, int in_dtype, cudaStream_t s) {
+  return in_dtype == LL_F32 ? launch_states_typed<float>(a, s)
+                            : launch_states_typed<__nv_bfloat16>(a, s);
+}
 
 cudaError_t launch_simt_forward(const FwdArgs& a, int in_dtype, int out_dtype, cudaStream_t s,
                                 StageEvents* ev) {

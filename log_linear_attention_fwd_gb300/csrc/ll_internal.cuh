@@ -103,6 +103,33 @@ cudaError_t launch_simt_forward(const FwdArgs& a, int in_dtype, int out_dtype, c
                                 StageEvents* ev);
 cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev);
 cudaError_t launch_level_scan(const FwdArgs& a, cudaStream_t s);
+// The CUDA-core path's chunk states U and fp32 block states of every slot (K1 and K2 of
+// the forward, without the readout).
+cudaError_t launch_simt_states(const FwdArgs& a, int in_dtype, cudaStream_t s);
+
+// Backward (fp32 on CUDA cores): the forward's states are recomputed on tiles of
+// kBwdTile tokens; U is then reused for the mirrored block states.
+constexpr int kBwdTile = 32;
+struct BwdArgs {
+  FwdArgs f;            // inputs, tile geometry, recomputed states (U, nodes, lg)
+  const void* dout;     // [B, T, H, dv] grad dtype
+  void* dq;             // [B, T, Hqk, dk] grad dtype
+  void* dk;             // [B, T, Hqk, dk] grad dtype
+  void* dv;             // [B, T, H, dv] grad dtype
+  float* dlog_a;        // [B, T, H] or null (no decay)
+  float* dlam;          // [B, T, H, L]
+  float* dqh;           // [B, T, H, dk] per-head dq (workspace)
+  float* dkh;           // [B, T, H, dk] per-head dk (workspace)
+  float* dcq;           // [B, T, H] q_t . dq_t per head (workspace)
+  float* dck;           // [B, T, H] k_t . dk_t per head (workspace)
+};
+struct BwdWorkspace {
+  size_t off_U, off_nodes, off_lg, off_dqh, off_dkh, off_dcq, off_dck, total;
+};
+BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, int64_t dk,
+                                  int64_t dv);
+cudaError_t launch_simt_backward(const BwdArgs& a, int in_dtype, int grad_dtype, cudaStream_t s);
+size_t bwd_smem_max(int dk, int dv, int L);  // largest dynamic shared memory of a kernel
 // The decode state at position T-1 from a completed forward's workspace (tc_layout: the
 // tensor-core path's bf16 block states; both paths store them [d_k][d_v]).
 cudaError_t launch_prefill_state(const FwdArgs& a, bool tc_layout, int in_dtype, float* state,

@@ -281,6 +281,70 @@ int loglinear_decode_step(float* state, const void* q, const void* k, const void
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 
+// ---------------------------------------------------------------- backward
+
+static int check_bwd(int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk, int64_t dv,
+                     int64_t L, int in_dtype, int grad_dtype, int64_t* N) {
+  if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1 || L < 1) return LL_ERR_INVALID;
+  if (!dtype_ok(in_dtype) || !dtype_ok(grad_dtype)) return LL_ERR_DTYPE;
+  const int sh = check_qk_heads(H, Hqk);
+  if (sh != LL_OK) return sh;
+  if (T > INT32_MAX || B * H > INT32_MAX / 2) return LL_ERR_UNSUPPORTED;
+  if (dk > kMaxHeadDim || dv > kMaxHeadDim || L > 64) return LL_ERR_UNSUPPORTED;
+  if (T > 0 && L < bit_length(T - 1) + 1) return LL_ERR_SHAPE;
+  *N = (T + kBwdTile - 1) / kBwdTile;
+  return LL_OK;
+}
+
+int loglinear_bwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk,
+                                 int64_t dv, int64_t L, int in_dtype, int grad_dtype,
+                                 size_t* bytes) {
+  if (!bytes) return LL_ERR_INVALID;
+  int64_t N;
+  const int st = check_bwd(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, &N);
+  if (st != LL_OK) return st;
+  *bytes = bwd_workspace_layout(B, T, H, N, dk, dv).total;
+  return LL_OK;
+}
+
+int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_a,
+                  const float* lambda, const void* dout, void* dq, void* dk_out, void* dv_out,
+                  float* dlog_a, float* dlambda, int64_t B, int64_t T, int64_t H, int64_t Hqk,
+                  int64_t dk, int64_t dv, int64_t L, int in_dtype, int grad_dtype,
+                  void* workspace, size_t workspace_bytes, ll_stream_t stream) {
+  int64_t N;
+  const int st = check_bwd(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, &N);
+  if (st != LL_OK) return st;
+  if (B == 0 || T == 0 || H == 0) return LL_OK;
+  if (!q || !k || !v || !lambda || !dout || !dq || !dk_out || !dv_out || !dlambda)
+    return LL_ERR_INVALID;
+  if (log_a && !dlog_a) return LL_ERR_INVALID;
+  const BwdWorkspace w = bwd_workspace_layout(B, T, H, N, dk, dv);
+  if (!workspace || workspace_bytes < w.total) return LL_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_ALIGN;
+  BwdArgs A;
+  FwdArgs& a = A.f;
+  a.q = q; a.k = k; a.v = v; a.log_a = log_a; a.lam = lambda; a.out = nullptr;
+  a.B = (int)B; a.T = (int)T; a.H = (int)H; a.dk = (int)dk; a.dv = (int)dv; a.L = (int)L;
+  a.Hqk = (int)Hqk; a.hg = (int)(H / Hqk);
+  a.C = kBwdTile; a.lc = log2_exact(kBwdTile); a.N = (int)N;
+  char* ws = static_cast<char*>(workspace);
+  a.U = ws + w.off_U;
+  a.nodes = ws + w.off_nodes;
+  a.lg = reinterpret_cast<float*>(ws + w.off_lg);
+  a.nlg = nullptr; a.rdy_u = nullptr; a.rdy_n = nullptr; a.tick = nullptr;
+  A.dout = dout; A.dq = dq; A.dk = dk_out; A.dv = dv_out;
+  A.dlog_a = log_a ? dlog_a : nullptr;
+  A.dlam = dlambda;
+  A.dqh = reinterpret_cast<float*>(ws + w.off_dqh);
+  A.dkh = reinterpret_cast<float*>(ws + w.off_dkh);
+  A.dcq = log_a ? reinterpret_cast<float*>(ws + w.off_dcq) : nullptr;
+  A.dck = log_a ? reinterpret_cast<float*>(ws + w.off_dck) : nullptr;
+  const cudaError_t e =
+      launch_simt_backward(A, in_dtype, grad_dtype, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LL_OK : cuda_fail(e);
+}
+
 int loglinear_device_error(ll_stream_t stream, unsigned* flags) {
   if (!flags) return LL_ERR_INVALID;
   const cudaError_t e = tc_take_error(reinterpret_cast<cudaStream_t>(stream), flags);

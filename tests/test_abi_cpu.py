@@ -175,3 +175,30 @@ def test_binding_rejects_host_tensors(L):
     q = torch.zeros(1, 8, 1, 4)
     with pytest.raises(ValueError):
         L.loglinear_fwd(q, q, q, None, torch.zeros(1, 8, 1, 4), 4)
+
+
+def test_bwd_validation_codes(L):
+    def bwd(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, dout=FAKE, dq=FAKE, dk=FAKE,
+                 dv=FAKE, dla=None, dlam=FAKE, B=1, T=64, H=2, Hqk=2, dkd=16, dvd=16, Lv=7,
+                 ind=L.LL_F32, gd=L.LL_F32, ws=None, wsb=0, stream=None)
+        a.update(kw)
+        return L.lib().loglinear_bwd(a["q"], a["k"], a["v"], a["log_a"], a["lam"], a["dout"],
+                                     a["dq"], a["dk"], a["dv"], a["dla"], a["dlam"], a["B"],
+                                     a["T"], a["H"], a["Hqk"], a["dkd"], a["dvd"], a["Lv"],
+                                     a["ind"], a["gd"], a["ws"], a["wsb"], a["stream"])
+    assert bwd(Lv=6) == L.LL_ERR_SHAPE                  # T=64 needs L >= 7
+    assert bwd(H=4, Hqk=3) == L.LL_ERR_SHAPE
+    assert bwd(ind=3) == L.LL_ERR_DTYPE
+    assert bwd(gd=-1) == L.LL_ERR_DTYPE
+    assert bwd(dkd=129) == L.LL_ERR_UNSUPPORTED
+    assert bwd(dvd=0) == L.LL_ERR_INVALID
+    assert bwd(dq=None) == L.LL_ERR_INVALID
+    assert bwd(dlam=None) == L.LL_ERR_INVALID
+    assert bwd(log_a=FAKE, dla=None) == L.LL_ERR_INVALID   # d log a wanted with a decay
+    assert bwd() == L.LL_ERR_WORKSPACE
+    assert bwd(ws=ctypes.c_void_p(0x1010), wsb=1 << 40) == L.LL_ERR_ALIGN
+    assert bwd(T=0, q=None, k=None, v=None, lam=None, dout=None, dq=None, dk=None, dv=None,
+               dlam=None) == L.LL_OK
+    sz = L.bwd_workspace_size(1, 64, 2, 2, 16, 16, 7, L.LL_F32, L.LL_F32)
+    assert sz >= 2 * (1 * 2 * 2 * 16 * 16 * 4) + 2 * 64 * 2 * 16 * 4   # states + per-head dq, dk

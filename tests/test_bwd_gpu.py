@@ -1,0 +1,130 @@
+"""Parity of the CUDA backward with the CPU oracle's backward, through the C ABI (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.helpers import TOL_BF16, cuda, per_head_qk, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+# fp32 gradients: every term is accumulated in fp32 (relative rounding ~1e-7 per add over
+# at most a few thousand terms); 1e-5 rel-L2 leaves two orders of margin.  d log a is a
+# suffix sum of q.dQ - k.dK whose terms cancel (its total is exactly 0), so its error is
+# measured against the scale of those terms: 1e-4.
+TOL_G32 = 1e-5
+TOL_DLA32 = 1e-4
+
+
+@pytest.fixture(scope="module")
+def LL():
+    import log_linear_attention_fwd_gb300 as m
+    return m
+
+
+def _dout(cfg, seed):
+    g = torch.Generator().manual_seed(seed)
+    d = torch.randn(cfg.B, cfg.T, cfg.H, cfg.dv, generator=g)
+    return d.to(W.torch_dtype(cfg.dtype))
+
+
+def _oracle_grads(x, dout):
+    """Oracle gradients, with q/k gradients summed over each group of heads sharing a q/k
+    head (the oracle's definition is per head), and the scale of the terms q_t . dQ_t
+    that cancel in d log a (the norm of that [B, T, H] array)."""
+    xp = per_head_qk(x)
+    g = oracle.backward_direct(xp["q"], xp["k"], xp["v"], xp["log_a"], xp["lam"], dout)
+    qf = xp["q"].double().numpy()
+    dla_scale = float(np.linalg.norm(np.sum(qf * g["q"], axis=-1)))
+    H, G = x["v"].shape[2], x["q"].shape[2]
+    for n in ("q", "k"):
+        B, T, _, dk = g[n].shape
+        g[n] = g[n].reshape(B, T, G, H // G, dk).sum(axis=3)
+    return g, dla_scale
+
+
+def _check(LL, cfg, tol, tol_dla, seed=0):
+    x = W.make_fwd_inputs(cfg)
+    dout = _dout(cfg, seed + 100)
+    d = cuda(x)
+    got = LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout.cuda())
+    torch.cuda.synchronize()
+    want, dla_scale = _oracle_grads(x, dout)
+    errs = {}
+    for name, gt in zip(("q", "k", "v", "log_a", "lam"), got):
+        if want[name] is None:
+            assert gt is None
+            continue
+        if name == "log_a":  # relative to the terms that cancel in it (its value may be 0)
+            diff = gt.cpu().double().numpy() - want[name]
+            errs[name] = float(np.linalg.norm(diff)) / max(np.linalg.norm(want[name]), dla_scale,
+                                                           1e-300)
+        else:
+            errs[name] = rel_l2(gt.cpu(), want[name])
+    print(f"bwd {cfg.name} T={cfg.T} H={cfg.H}/{cfg.qk_heads} dk={cfg.dk} dv={cfg.dv} "
+          + " ".join(f"{k}={v:.2e}" for k, v in errs.items()))
+    for name, e in errs.items():
+        assert e <= (tol_dla if name == "log_a" else tol), (name, e)
+
+
+@pytest.mark.parametrize("T,decay", [(1, True), (31, True), (32, True), (33, True), (100, False),
+                                     (300, True), (1000, True), (2049, True)])
+def test_bwd_f32_matches_oracle(LL, T, decay):
+    L = max((T - 1).bit_length() + 1, 1)
+    cfg = W.FwdConfig("bwd_f32", 2, 3, T, 16, 8, 64, L, "f32", decay, "softplus", seed=T)
+    _check(LL, cfg, TOL_G32, TOL_DLA32, seed=T)
+
+
+@pytest.mark.parametrize("dk,dv", [(7, 5), (32, 64), (128, 128)])
+def test_bwd_f32_head_dims(LL, dk, dv):
+    cfg = W.FwdConfig("bwd_dims", 1, 2, 450, dk, dv, 64, 10, "f32", True, "softplus", seed=dk)
+    _check(LL, cfg, TOL_G32, TOL_DLA32, seed=dk)
+
+
+@pytest.mark.parametrize("T,dv", [(300, 64), (2049, 64), (1000, 128)])
+def test_bwd_bf16_matches_oracle(LL, T, dv):
+    L = (T - 1).bit_length() + 1
+    cfg = W.FwdConfig("bwd_bf16", 1, 2, T, 128, dv, 64, L, "bf16", True, "softplus", seed=T + dv)
+    _check(LL, cfg, TOL_BF16, TOL_BF16, seed=T)
+
+
+@pytest.mark.parametrize("H,Hqk,dtype", [(4, 1, "f32"), (6, 2, "f32"), (4, 1, "bf16")])
+def test_bwd_shared_qk_heads(LL, H, Hqk, dtype):
+    cfg = W.FwdConfig("bwd_mva", 2, H, 700, 32 if dtype == "f32" else 128, 16 if dtype == "f32" else 64,
+                      64, 11, dtype, True, "softplus", seed=H + Hqk, Hqk=Hqk)
+    tol = TOL_G32 if dtype == "f32" else TOL_BF16
+    _check(LL, cfg, tol, TOL_DLA32 if dtype == "f32" else TOL_BF16, seed=H)
+
+
+def test_bwd_one_hot_lambda_exact(LL):
+    """Small integers, no decay, lambda one-hot at each level in turn: every product and
+    sum is an integer far below 2^24, so the fp32 gradients equal the oracle's exactly."""
+    T, L = 200, 9
+    for lvl in range(L):
+        x = W.make_int_inputs(1, T, 2, 6, 4, L, lvl, seed=lvl)
+        g = torch.Generator().manual_seed(lvl)
+        dout = torch.randint(-2, 3, (1, T, 2, 4), generator=g).float()
+        d = cuda(x)
+        got = LL.loglinear_bwd(d["q"], d["k"], d["v"], None, d["lam"], dout.cuda())
+        want = oracle.backward_direct(x["q"], x["k"], x["v"], None, x["lam"], dout)
+        for name, gt in zip(("q", "k", "v"), got[:3]):
+            assert np.array_equal(gt.cpu().double().numpy(), want[name]), (lvl, name)
+        assert np.array_equal(got[4].cpu().double().numpy(), want["lam"]), lvl
+
+
+def test_bwd_workspace_reuse_and_empty(LL):
+    cfg = W.FwdConfig("bwd_rep", 1, 2, 500, 16, 16, 64, 10, "f32", True, "softplus", seed=3)
+    x = cuda(W.make_fwd_inputs(cfg))
+    dout = _dout(cfg, 1).cuda()
+    ws = torch.empty(LL.bwd_workspace_size(1, 500, 2, 2, 16, 16, 10, 0, 0), device="cuda",
+                     dtype=torch.uint8)
+    a = LL.loglinear_bwd(x["q"], x["k"], x["v"], x["log_a"], x["lam"], dout, workspace=ws)
+    a = [t.clone() for t in a]
+    b = LL.loglinear_bwd(x["q"], x["k"], x["v"], x["log_a"], x["lam"], dout, workspace=ws)
+    for u, w in zip(a, b):
+        assert torch.allclose(u, w, rtol=1e-6, atol=1e-6)
+    q = torch.zeros(1, 0, 2, 8, device="cuda")
+    lam = torch.zeros(1, 0, 2, 3, device="cuda")
+    out = LL.loglinear_bwd(q, q, q, None, lam, q)
+    assert out[0].shape == (1, 0, 2, 8)
