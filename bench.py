@@ -103,6 +103,30 @@ def fwd_algorithmic(cfg):
     return bytes_, flops
 
 
+def bwd_algorithmic(cfg):
+    """Bytes and FLOPs of the backward in the chunked form at C = 64: per causal pair
+    inside a chunk q.k, dO.v and the dQ, dK, dV updates; per chunk the recomputed chunk
+    state; per (chunk, inter level) the dQ readout (dO Tot^T) with its dlambda dot, the
+    chunk's part of the mirrored state (q dO^T), and the dK, dV readouts (R v, R^T k).
+    Bytes: q, k, v, dO, log a, lambda read once; dq, dk, dv, dlog a, dlambda written once."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    BH, dk, dv = cfg.B * cfg.H, cfg.dk, cfg.dv
+    tok, tok_qk = cfg.B * cfg.T * cfg.H, cfg.B * cfg.T * cfg.qk_heads
+    bytes_ = 2 * (tok_qk * 2 * dk * e + tok * 2 * dv * e + tok * 4 + tok * cfg.L * 4)
+    C = 64
+    N = -(-cfg.T // C)
+    pairs = C * (C + 1) / 2 * N
+    inter = sum(bin(j).count("1") for j in range(N))
+    flops = BH * (pairs * 2 * (3 * dk + 2 * dv) + N * 2 * C * dk * dv
+                  + inter * (4 * 2 * C * dk * dv + 2 * C * dk))
+    return bytes_, flops
+
+
+def fp32_alu_peak():
+    """FP32 FMA peak: 152 SMs x 128 lanes x 2 FLOPs x 2.07 GHz (maximum SM clock)."""
+    return 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 def decode_algorithmic(cfg):
     """Bytes of the levels the step must read (non-empty after t-1) and write (every
     level that changes), fp32."""
@@ -324,6 +348,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = measure_e2e(LL, cfg, x, dev, ws, args)
     prefill = measure_prefill(LL, cfg, d, out, ws, flush, peaks)
     del ws
+    backward = measure_backward(LL, cfg, d, dev, flush, peaks)
     bench_shape = measure_benchmark_shape(LL, W.FWD_CONFIGS["mva_B2H48_T16384"], dev, flush, peaks)
     res = {"metric": METRIC, "value": fwd_tok_s, "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
@@ -338,7 +363,7 @@ def run_ours(args, rank, world, local_rank):
                       "parallelism": f"replicas x{world} (independent (b,h) work, no collective)"},
            "fwd_ms": fwd_mean * 1e3, "fwd_stage_us": dict(zip(stage_names, [s * 1e6 for s in stage_mean])),
            "roofline": roofline, "roofline_fwd": roofline_fwd, "decode": decode, "e2e": e2e,
-           "prefill": prefill, "benchmark_shape": bench_shape,
+           "prefill": prefill, "backward": backward, "benchmark_shape": bench_shape,
            "gpu_launches": args.steps * (n_kernels + 1), "clocks": clk,
            "wall_s_timed_region": wall}
     return res
@@ -399,6 +424,46 @@ def measure_prefill(LL, cfg, d, out, ws, flush, peaks, reps=10):
                     "+ bf16 block states read"}
 
 
+def _median_us(fn, flush, reps):
+    ts = []
+    for i in range(reps + 2):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 2:
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+    return statistics.median(ts)
+
+
+def _bwd_report(cfg, t, peaks):
+    bbytes, bflops = bwd_algorithmic(cfg)
+    return {"bwd_us": t * 1e6, "tokens_per_s": cfg.B * cfg.T / t,
+            "roofline": {"bound": "alu", "achieved": bflops / t / 1e12,
+                         "peak": fp32_alu_peak(), "unit": "TFLOP/s",
+                         "frac": bflops / t / 1e12 / fp32_alu_peak(),
+                         "algorithmic_flops": bflops,
+                         "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
+                         "hbm_frac": bbytes / t / 1e9 / peaks["hbm"],
+                         "algorithmic_bytes": bbytes}}
+
+
+def measure_backward(LL, cfg, d, dev, flush, peaks, reps=5):
+    """The backward (CUDA cores, fp32) on the headline shape: median of `reps` calls,
+    L2 flushed before each, outside the events; dO drawn on the device (timing only)."""
+    g = torch.Generator(device=dev).manual_seed(7)
+    dout = torch.randn(cfg.B, cfg.T, cfg.H, cfg.dv, device=dev, generator=g).to(d["q"].dtype)
+    ws = torch.empty(LL.bwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.qk_heads, cfg.dk, cfg.dv,
+                                           cfg.L, 1, 1), device=dev, dtype=torch.uint8)
+    t = _median_us(lambda: LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout,
+                                            workspace=ws), flush, reps)
+    rep = _bwd_report(cfg, t, peaks)
+    rep["workload"] = f"{cfg.name}: loglinear_bwd, bf16 inputs and gradients, fp32 compute"
+    return rep
+
+
 def measure_benchmark_shape(LL, cfg, dev, flush, peaks, reps=10):
     """The forward on the pages' kernel-benchmark shape (B2, 48 heads, d_v 64, d_k 128,
     one q/k shared by all heads): median of `reps` calls, L2 flushed before each call
@@ -423,9 +488,18 @@ def measure_benchmark_shape(LL, cfg, dev, flush, peaks, reps=10):
         raise RuntimeError("tensor-core forward reported a device error")
     t = statistics.median(ts)
     fbytes, fflops = fwd_algorithmic(cfg)
+    del ws
+    g = torch.Generator(device=dev).manual_seed(7)
+    dout = torch.randn(cfg.B, cfg.T, cfg.H, cfg.dv, device=dev, generator=g).to(d["q"].dtype)
+    bws = torch.empty(LL.bwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.qk_heads, cfg.dk, cfg.dv,
+                                            cfg.L, 1, 1), device=dev, dtype=torch.uint8)
+    tb = _median_us(lambda: LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout,
+                                             workspace=bws), flush, 3)
+    bwd = _bwd_report(cfg, tb, peaks)
     return {"workload": f"{cfg.name}: loglinear_fwd B{cfg.B} H{cfg.H} (q/k heads "
                         f"{cfg.qk_heads}) T{cfg.T} dk={cfg.dk} dv={cfg.dv} C{cfg.C} L{cfg.L} bf16",
             "path": LL.resolve_path(cfg.dk, cfg.dv, cfg.C, 1), "fwd_us": t * 1e6,
+            "fwd_bwd_us": (t + tb) * 1e6, "backward": bwd,
             "tokens_per_s": cfg.B * cfg.T / t,
             "roofline": {"bound": "hbm", "achieved": fbytes / t / 1e9, "peak": peaks["hbm"],
                          "unit": "GB/s", "frac": fbytes / t / 1e9 / peaks["hbm"],

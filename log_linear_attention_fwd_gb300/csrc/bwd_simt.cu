@@ -18,7 +18,8 @@
 //           starting at c' = ((i >> (m-1)) | 1) << (m-1); lambda[t, 5+m] depends on t, so
 //           it is folded into that block's mirrored state
 //           R_c' = sum_t exp(cum_t - cum_start(c')) lambda[t, 5+m] q_t dO_t^T, and
-//           dK_s += exp(cum_start(c') - cum_s) R_c' v_s,  dV_s += (same) R_c'^T k_s;
+//           dK_s += exp(cum_start(c') - cum_s) R_c' v_s,  dV_s += (same) R_c'^T k_s (the
+//           levels of a tile share the row factor and are summed into one state first);
 //   dcum_t = q_t . dQ_t - k_t . dK_t  (the row and column sums of dA ⊙ A ⊙ M), and
 //   dlog_a_i = sum over t >= i of dcum_t.
 //
@@ -122,8 +123,10 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_kernel(BwdArgs A) {
   const TileRows s = carve_rows(sm, dk, dv);
   float* Ap = s.lam + kC * L;       // [kC][kC+1] exp(cs_t - cs_s) lambda (dO_t . v_s)
   float* Wm = Ap + kC * (kC + 1);   // [kC][kC+1] exp(cs_t - cs_s) (dO_t . v_s)(q_t . k_s)
-  float* Sb = Wm + kC * (kC + 1);   // [kStage][dv+1] staged block-state rows
-  float* dl = Sb + kStage * s.lv;   // [kC][L] dlambda of the tile's rows
+  float* St = Wm + kC * (kC + 1);   // [kStage][128] staged block-state columns (swizzled)
+  float* dl = St + kStage * 128;    // [kC][L] dlambda of the tile's rows
+  float* Gt = s.v;                  // [dv][kC] dO transposed, in V's place (after the pairs)
+  float* Xs = s.k;                  // [kC][dk+1] Tot dO_t, in K's place (after intra dQ)
   load_tile<InT, GT>(A, b, h, t0, n, s);
   for (int idx = threadIdx.x; idx < kC * L; idx += kThreads) dl[idx] = 0.f;
   __syncthreads();
@@ -143,6 +146,10 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_kernel(BwdArgs A) {
     Wm[t * (kC + 1) + u] = w;
   }
   __syncthreads();
+  for (int idx = threadIdx.x; idx < kC * dv; idx += kThreads) {  // V is no longer read
+    const int r = idx / dv, e = idx - r * dv;
+    Gt[e * kC + r] = s.g[r * s.lv + e];
+  }
   // intra-tile dlambda: level 0 is the pair (t, t); level l >= 1 (bit l-1 of t set) the
   // sources [hi - 2^(l-1), hi), hi = t with its low l-1 bits cleared
   if (threadIdx.x < kC * (kLc + 1)) {
@@ -171,39 +178,53 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_kernel(BwdArgs A) {
       if (d < dk) acc[i] = fmaf(p, s.k[u * s.lq + d], acc[i]);
     }
   }
-  // inter-tile levels: Tot_m dO_t for the block state of slot c
+  // inter-tile levels: X = dO Tot_m^T ([kC] x [d_k]) for the block state of slot c, as a
+  // register-blocked product: warp w owns rows 4w..4w+3, lane g columns 4g..4g+3; per
+  // step one float4 of dO^T (broadcast) and one of the staged Tot^T columns (stored with
+  // the 16-byte groups XOR-swizzled by the row, so the transposing stores and the float4
+  // reads do not collide).  X then goes through shared memory to the row layout above.
   const int64_t elems = (int64_t)dk * dv;
   const float* nodes = reinterpret_cast<const float*>(a.nodes) + bh * a.N * elems;
   const float* lg = a.lg + bh * a.N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // dO^T is in place; K is no longer read
   for (int m = 1; (int64_t(1) << (m - 1)) <= j; ++m) {
     int64_t c;
     if (!inter_block(j, m, &c)) continue;
     float D = 0.f;  // log decay from the block's end to the start of tile j
     for (int64_t i = c; i < j; ++i) D += lg[i];
     const float* S = nodes + c * elems;
-    float part[kPer];
+    float x[4][4];
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) part[i] = 0.f;
-    for (int d0 = 0; d0 < dk; d0 += kStage) {
-      const int rows = min(kStage, dk - d0);
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x[r][q] = 0.f;
+    for (int e0 = 0; e0 < dv; e0 += kStage) {
       __syncthreads();
-      for (int idx = threadIdx.x; idx < rows * dv; idx += kThreads) {
-        const int r = idx / dv;
-        Sb[r * s.lv + (idx - r * dv)] = S[(int64_t)d0 * dv + idx];
+      for (int idx = threadIdx.x; idx < kStage * 128; idx += kThreads) {
+        const int e = idx & (kStage - 1), f = idx >> 5;
+        const float val = (f < dk && e0 + e < dv) ? S[(int64_t)f * dv + e0 + e] : 0.f;
+        St[e * 128 + ((((f >> 2) ^ e) << 2) | (f & 3))] = val;
       }
       __syncthreads();
+      const int ne = min(kStage, dv - e0);
+      for (int e = 0; e < ne; ++e) {
+        const float4 av = *reinterpret_cast<const float4*>(Gt + (e0 + e) * kC + 4 * warp);
+        const float4 bv = *reinterpret_cast<const float4*>(St + e * 128 + ((lane ^ e) << 2));
+        const float aa[4] = {av.x, av.y, av.z, av.w};
+        const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int d = sub + kSub * i;
-        if (d >= d0 && d < d0 + rows) {
-          const float* sr = Sb + (d - d0) * s.lv;
-          const float* gr = s.g + t * s.lv;
-          float x = 0.f;
-          for (int e = 0; e < dv; ++e) x = fmaf(sr[e], gr[e], x);
-          part[i] = x;
-        }
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) x[r][q] = fmaf(aa[r], bb[q], x[r][q]);
       }
     }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (4 * lane + q < dk) Xs[(4 * warp + r) * s.lq + 4 * lane + q] = x[r][q];
+    __syncthreads();
     const int lvl = kLc + m;
     const float wq = t < n ? expf(s.cs[t] + D) : 0.f;
     const float wl = wq * s.lam[t * L + lvl];
@@ -212,8 +233,9 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_kernel(BwdArgs A) {
     for (int i = 0; i < kPer; ++i) {
       const int d = sub + kSub * i;
       if (d < dk) {
-        acc[i] = fmaf(wl, part[i], acc[i]);
-        dot = fmaf(s.q[t * s.lq + d], part[i], dot);
+        const float part = Xs[t * s.lq + d];
+        acc[i] = fmaf(wl, part, acc[i]);
+        dot = fmaf(s.q[t * s.lq + d], part, dot);
       }
     }
     dot = row_sum(dot);
@@ -374,19 +396,36 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
       if (f < dv) av[q] = fmaf(x2, s.g[t * s.lv + f], av[q]);
     }
   }
-  // inter-tile levels: the mirrored states of the blocks of later tiles
+  // inter-tile levels: the mirrored states of the blocks of later tiles.  The weight
+  // exp(cum_start(c1) - cum_u) of level m is exp(lg_i - cs_u) (a row factor, the same at
+  // every level) times exp(E_m) (E_m: log decay of the tiles strictly between i and c1),
+  // so the levels merge into R_tot = sum_m exp(E_m) R_{c1(m)} and one pair of products:
+  //   dK_u += exp(lg_i - cs_u) R_tot v_u,   dV_u += exp(lg_i - cs_u) R_tot^T k_u.
+  __shared__ long long lv_c[64];
+  __shared__ float lv_w[64];
+  __shared__ int lv_n;
   const int64_t elems = (int64_t)dk * dv;
   const float* R = reinterpret_cast<const float*>(a.U) + bh * a.N * elems;
   const float* lg = a.lg + bh * a.N;
-  const float lg_i = s.cs[kC - 1];  // this tile's log decay (tiles before the last are full)
-  for (int m = 1; (int64_t(1) << (m - 1)) < a.N; ++m) {
-    if ((i >> (m - 1)) & 1) continue;
-    const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
-    if (c1 >= a.N) continue;
-    float E = 0.f;  // log decay over the tiles strictly between i and c1
-    for (int64_t x = i + 1; x < c1; ++x) E += lg[x];
-    const float gs = u < n ? expf(lg_i - s.cs[u] + E) : 0.f;
-    const float* Rc = R + c1 * elems;
+  if (threadIdx.x == 0) {
+    int nl = 0;
+    for (int m = 1; (int64_t(1) << (m - 1)) < a.N; ++m) {
+      if ((i >> (m - 1)) & 1) continue;
+      const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
+      if (c1 >= a.N) continue;
+      float E = 0.f;
+      for (int64_t x = i + 1; x < c1; ++x) E += lg[x];
+      lv_c[nl] = c1;
+      lv_w[nl] = expf(E);
+      ++nl;
+    }
+    lv_n = nl;
+  }
+  __syncthreads();
+  const int nl = lv_n;
+  if (nl > 0) {
+    const float lg_i = s.cs[kC - 1];  // this tile's log decay (tiles before the last are full)
+    const float gs = u < n ? expf(lg_i - s.cs[u]) : 0.f;
     float pk[kPer], pv[kPer];
 #pragma unroll
     for (int q = 0; q < kPer; ++q) pk[q] = pv[q] = 0.f;
@@ -395,20 +434,22 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
       __syncthreads();
       for (int idx = threadIdx.x; idx < rows * dv; idx += kThreads) {
         const int r = idx / dv;
-        Sb[r * s.lv + (idx - r * dv)] = Rc[(int64_t)d0 * dv + idx];
+        float x = 0.f;
+        for (int l = 0; l < nl; ++l) x = fmaf(lv_w[l], R[lv_c[l] * elems + (int64_t)d0 * dv + idx], x);
+        Sb[r * s.lv + (idx - r * dv)] = x;
       }
       __syncthreads();
 #pragma unroll
       for (int q = 0; q < kPer; ++q) {
         const int f = sub + kSub * q;
-        if (f >= d0 && f < d0 + rows) {  // (R v_u)[f]
+        if (f >= d0 && f < d0 + rows) {  // (R_tot v_u)[f]
           const float* sr = Sb + (f - d0) * s.lv;
           const float* vr = s.v + u * s.lv;
           float x = 0.f;
           for (int e = 0; e < dv; ++e) x = fmaf(sr[e], vr[e], x);
           pk[q] = x;
         }
-        if (f < dv) {  // (R^T k_u)[f], rows d0 .. d0 + rows
+        if (f < dv) {  // (R_tot^T k_u)[f], rows d0 .. d0 + rows
           float y = pv[q];
           for (int r = 0; r < rows; ++r) y = fmaf(Sb[r * s.lv + f], s.k[u * s.lq + d0 + r], y);
           pv[q] = y;
@@ -497,8 +538,8 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
   const FwdArgs& a = A.f;
   const dim3 grid(a.N, a.H, a.B);
   const size_t rows = tile_rows_floats(a.dk, a.dv, a.L);
-  const size_t sm_dq = sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * (a.dv + 1) +
-                                        (size_t)kC * a.L);
+  const size_t sm_dq =
+      sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * 128 + (size_t)kC * a.L);
   const size_t sm_dkv =
       sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * (a.dv + 1));
   const size_t sm_r = sizeof(float) * (3 * kC * 128 + 2 * kC);
@@ -553,8 +594,8 @@ BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, in
 }
 
 size_t bwd_smem_max(int dk, int dv, int L) {
-  return sizeof(float) * (tile_rows_floats(dk, dv, L) + 2 * kC * (kC + 1) +
-                          (size_t)kStage * (dv + 1) + (size_t)kC * L);
+  return sizeof(float) * (tile_rows_floats(dk, dv, L) + 2 * kC * (kC + 1) + (size_t)kStage * 128 +
+                          (size_t)kC * L);
 }
 
 cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype, cudaStream_t s) {
