@@ -47,6 +47,10 @@ def parse():
     p.add_argument("--fwd-only", action="store_true",
                    help="profiling aid: time only the forward (no decode state, no e2e, no "
                         "CPU baseline) and print its own short JSON line")
+    p.add_argument("--bwd-only", action="store_true",
+                   help="profiling aid: time only the backward, like --fwd-only")
+    p.add_argument("--workload", default=None,
+                   help="forward workload of --fwd-only / --bwd-only (default: the headline)")
     return p.parse_args()
 
 
@@ -542,40 +546,53 @@ def measure_e2e(LL, cfg, x, dev, ws, args):
             "d2h_bytes_per_step": d2h, "ms_per_step": t * 1e3}
 
 
-def run_fwd_only(args):
-    """The headline forward alone, K timed calls after W warm-ups (L2 flushed between
-    calls); for profilers, which should not see the 2 GiB decode state."""
+def run_one_pass(args, backward):
+    """The forward (or the backward) alone on one workload (the headline by default), K
+    timed calls after W warm-ups, L2 flushed between calls; for profilers, which should not
+    see the 2 GiB decode state."""
     import log_linear_attention_fwd_gb300 as LL
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    cfg = W.FWD_CONFIGS[W.HEADLINE_FWD]
+    cfg = W.FWD_CONFIGS[args.workload or W.HEADLINE_FWD]
     x = W.make_fwd_inputs(cfg)
     d = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
-    out = torch.empty(cfg.B, cfg.T, cfg.H, cfg.dv, device=dev, dtype=d["q"].dtype)
     in_code = 1 if cfg.dtype == "bf16" else 0
-    ws = torch.empty(LL.fwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv, cfg.C, in_code),
-                     device=dev, dtype=torch.uint8)
+    if backward:
+        g = torch.Generator(device=dev).manual_seed(7)
+        dout = torch.randn(cfg.B, cfg.T, cfg.H, cfg.dv, device=dev, generator=g).to(d["q"].dtype)
+        ws = torch.empty(LL.bwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.qk_heads, cfg.dk, cfg.dv,
+                                               cfg.L, in_code, in_code), device=dev,
+                         dtype=torch.uint8)
+        call = lambda: LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout,
+                                        workspace=ws)
+    else:
+        out = torch.empty(cfg.B, cfg.T, cfg.H, cfg.dv, device=dev, dtype=d["q"].dtype)
+        ws = torch.empty(LL.fwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv, cfg.C,
+                                               in_code), device=dev, dtype=torch.uint8)
+        call = lambda: LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C,
+                                        out=out, workspace=ws)
     flush = torch.empty(512 << 20, device=dev, dtype=torch.uint8)
     times = []
     for i in range(args.warmup + args.steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C, out=out, workspace=ws)
+        call()
         e1.record()
         torch.cuda.synchronize()
         if i >= args.warmup:
             times.append(e0.elapsed_time(e1) * 1e3)
     assert LL.device_error() == 0
-    print(json.dumps({"mode": "fwd-only", "workload": cfg.name, "steps": args.steps,
-                      "warmup": args.warmup, "fwd_us_mean": sum(times) / len(times),
-                      "fwd_us_min": min(times)}), flush=True)
+    name = "bwd" if backward else "fwd"
+    print(json.dumps({"mode": f"{name}-only", "workload": cfg.name, "steps": args.steps,
+                      "warmup": args.warmup, f"{name}_us_mean": sum(times) / len(times),
+                      f"{name}_us_min": min(times)}), flush=True)
 
 
 def main():
     args = parse()
-    if args.fwd_only:
-        run_fwd_only(args)
+    if args.fwd_only or args.bwd_only:
+        run_one_pass(args, backward=args.bwd_only)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -363,7 +363,13 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
   const TileRows s = carve_rows(sm, dk, dv);
   float* X1 = s.lam + kC * L;       // [kC][kC+1] M[t, s] (dO_t . v_s)
   float* X2 = X1 + kC * (kC + 1);   // [kC][kC+1] M[t, s] (q_t . k_s)
-  float* Sb = X2 + kC * (kC + 1);   // [kStage][dv+1]
+  float* St = X2 + kC * (kC + 1);   // [kStage][128] staged rows or columns of R_tot
+  // after the intra-tile part: k and v transposed in the places of q and dO, and the
+  // level products in the places of k and v
+  float* Kt = s.q;                  // [dk][kC]
+  float* Vt = s.g;                  // [dv][kC]
+  float* Xd = s.k;                  // [kC][dk+1]  R_tot v_u
+  float* Yd = s.v;                  // [kC][dv+1]  R_tot^T k_u
   load_tile<InT, GT>(A, b, h, t0, n, s);
   __syncthreads();
   for (int idx = threadIdx.x; idx < kC * kC; idx += kThreads) {
@@ -422,45 +428,91 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
     lv_n = nl;
   }
   __syncthreads();
-  const int nl = lv_n;
+  const int nl = lv_n;  // (the barrier above also ends the intra-tile reads of q and dO)
+  for (int idx = threadIdx.x; idx < kC * dk; idx += kThreads) {
+    const int r = idx / dk, c = idx - r * dk;
+    Kt[c * kC + r] = s.k[r * s.lq + c];
+  }
+  for (int idx = threadIdx.x; idx < kC * dv; idx += kThreads) {
+    const int r = idx / dv, c = idx - r * dv;
+    Vt[c * kC + r] = s.v[r * s.lv + c];
+  }
   if (nl > 0) {
+    // register-blocked products: warp w owns source rows 4w..4w+3, lane g the features
+    // 4g..4g+3; R_tot is formed while it is staged (levels summed with their weights)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float x[4][4], y[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x[r][q] = y[r][q] = 0.f;
+    // X = V R_tot^T: columns e0..e0+31 of R_tot, transposed, 16-byte groups swizzled
+    for (int e0 = 0; e0 < dv; e0 += kStage) {
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < kStage * 128; idx += kThreads) {
+        const int e = idx & (kStage - 1), f = idx >> 5;
+        float val = 0.f;
+        if (f < dk && e0 + e < dv)
+          for (int l = 0; l < nl; ++l)
+            val = fmaf(lv_w[l], R[lv_c[l] * elems + (int64_t)f * dv + e0 + e], val);
+        St[e * 128 + ((((f >> 2) ^ e) << 2) | (f & 3))] = val;
+      }
+      __syncthreads();
+      const int ne = min(kStage, dv - e0);
+      for (int e = 0; e < ne; ++e) {
+        const float4 av4 = *reinterpret_cast<const float4*>(Vt + (e0 + e) * kC + 4 * warp);
+        const float4 bv4 = *reinterpret_cast<const float4*>(St + e * 128 + ((lane ^ e) << 2));
+        const float aa[4] = {av4.x, av4.y, av4.z, av4.w};
+        const float bb[4] = {bv4.x, bv4.y, bv4.z, bv4.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) x[r][q] = fmaf(aa[r], bb[q], x[r][q]);
+      }
+    }
+    // Y = K R_tot: rows d0..d0+31 of R_tot, row-major
+    for (int d0 = 0; d0 < dk; d0 += kStage) {
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < kStage * 128; idx += kThreads) {
+        const int f = idx >> 7, e = idx & 127;
+        float val = 0.f;
+        if (d0 + f < dk && e < dv)
+          for (int l = 0; l < nl; ++l)
+            val = fmaf(lv_w[l], R[lv_c[l] * elems + (int64_t)(d0 + f) * dv + e], val);
+        St[idx] = val;
+      }
+      __syncthreads();
+      const int nf = min(kStage, dk - d0);
+      for (int f = 0; f < nf; ++f) {
+        const float4 av4 = *reinterpret_cast<const float4*>(Kt + (d0 + f) * kC + 4 * warp);
+        const float4 bv4 = *reinterpret_cast<const float4*>(St + f * 128 + 4 * lane);
+        const float aa[4] = {av4.x, av4.y, av4.z, av4.w};
+        const float bb[4] = {bv4.x, bv4.y, bv4.z, bv4.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) y[r][q] = fmaf(aa[r], bb[q], y[r][q]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int f = 4 * lane + q;
+        if (f < dk) Xd[(4 * warp + r) * s.lq + f] = x[r][q];
+        if (f < dv) Yd[(4 * warp + r) * s.lv + f] = y[r][q];
+      }
+    __syncthreads();
     const float lg_i = s.cs[kC - 1];  // this tile's log decay (tiles before the last are full)
     const float gs = u < n ? expf(lg_i - s.cs[u]) : 0.f;
-    float pk[kPer], pv[kPer];
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) pk[q] = pv[q] = 0.f;
-    for (int d0 = 0; d0 < dk; d0 += kStage) {
-      const int rows = min(kStage, dk - d0);
-      __syncthreads();
-      for (int idx = threadIdx.x; idx < rows * dv; idx += kThreads) {
-        const int r = idx / dv;
-        float x = 0.f;
-        for (int l = 0; l < nl; ++l) x = fmaf(lv_w[l], R[lv_c[l] * elems + (int64_t)d0 * dv + idx], x);
-        Sb[r * s.lv + (idx - r * dv)] = x;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        const int f = sub + kSub * q;
-        if (f >= d0 && f < d0 + rows) {  // (R_tot v_u)[f]
-          const float* sr = Sb + (f - d0) * s.lv;
-          const float* vr = s.v + u * s.lv;
-          float x = 0.f;
-          for (int e = 0; e < dv; ++e) x = fmaf(sr[e], vr[e], x);
-          pk[q] = x;
-        }
-        if (f < dv) {  // (R_tot^T k_u)[f], rows d0 .. d0 + rows
-          float y = pv[q];
-          for (int r = 0; r < rows; ++r) y = fmaf(Sb[r * s.lv + f], s.k[u * s.lq + d0 + r], y);
-          pv[q] = y;
-        }
-      }
-    }
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
-      ak[q] = fmaf(gs, pk[q], ak[q]);
-      av[q] = fmaf(gs, pv[q], av[q]);
+      const int f = sub + kSub * q;
+      if (f < dk) ak[q] = fmaf(gs, Xd[u * s.lq + f], ak[q]);
+      if (f < dv) av[q] = fmaf(gs, Yd[u * s.lv + f], av[q]);
     }
+  } else {
+    __syncthreads();  // the transposed k is complete
   }
   float kd = 0.f;
   const int64_t row = ((int64_t)b * a.T + t0 + u) * a.H + h;
@@ -470,7 +522,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
     const int f = sub + kSub * q;
     if (f < dk) {
       if (u < n) A.dkh[row * dk + f] = ak[q];
-      kd = fmaf(s.k[u * s.lq + f], ak[q], kd);
+      kd = fmaf(Kt[f * kC + u], ak[q], kd);
     }
     if (f < dv && u < n) dvo[row * dv + f] = from_f32<GT>(av[q]);
   }
@@ -540,8 +592,7 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
   const size_t rows = tile_rows_floats(a.dk, a.dv, a.L);
   const size_t sm_dq =
       sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * 128 + (size_t)kC * a.L);
-  const size_t sm_dkv =
-      sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * (a.dv + 1));
+  const size_t sm_dkv = sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * 128);
   const size_t sm_r = sizeof(float) * (3 * kC * 128 + 2 * kC);
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(bwd_dq_kernel<InT, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize,

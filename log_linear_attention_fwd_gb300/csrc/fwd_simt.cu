@@ -41,6 +41,10 @@ __device__ __forceinline__ void chunk_cumsum(const FwdArgs& a, int b, int h, int
   }
 }
 
+constexpr int kPad = 128;  // staged rows of K1 are zero-padded to the largest head dim
+
+// K1: thread (td, te) owns U rows [8 td, +8) and columns [8 te, +8) (register-blocked
+// outer products over the chunk's rows, k scaled by its decay when staged).
 template <typename InT>
 __global__ void __launch_bounds__(kThreads) simt_chunk_state(FwdArgs a) {
   extern __shared__ float sm[];
@@ -48,30 +52,49 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_state(FwdArgs a) {
   const int C = a.C, dk = a.dk, dv = a.dv;
   const int t0 = i * C;
   const int n = min(C, a.T - t0);
-  float* Ks = sm;             // [C][dk]
-  float* Vs = Ks + C * dk;    // [C][dv]
-  float* cs = Vs + C * dv;    // [C]
-  float* w = cs + C;          // [C]
+  float* Ks = sm;               // [C][kPad] w_r k_r
+  float* Vs = Ks + C * kPad;    // [C][kPad] v_r
+  float* cs = Vs + C * kPad;    // [C]
+  float* w = cs + C;            // [C]
   chunk_cumsum(a, b, h, t0, n, cs);
-  for (int idx = threadIdx.x; idx < n * dk; idx += kThreads) {
-    const int r = idx / dk, c = idx - r * dk;
-    Ks[idx] = ld<InT>(a.k, (((int64_t)b * a.T + t0 + r) * a.Hqk + h / a.hg) * dk + c);
-  }
-  for (int idx = threadIdx.x; idx < n * dv; idx += kThreads) {
-    const int r = idx / dv, c = idx - r * dv;
-    Vs[idx] = ld<InT>(a.v, (((int64_t)b * a.T + t0 + r) * a.H + h) * dv + c);
-  }
   __syncthreads();
   const float lgi = cs[n - 1];
   for (int r = threadIdx.x; r < n; r += kThreads) w[r] = expf(lgi - cs[r]);
   __syncthreads();
+  for (int idx = threadIdx.x; idx < n * kPad; idx += kThreads) {
+    const int r = idx / kPad, c = idx - r * kPad;
+    const int64_t rk = ((int64_t)b * a.T + t0 + r) * a.Hqk + h / a.hg;
+    const int64_t rv = ((int64_t)b * a.T + t0 + r) * a.H + h;
+    Ks[idx] = c < dk ? w[r] * ld<InT>(a.k, rk * dk + c) : 0.f;
+    Vs[idx] = c < dv ? ld<InT>(a.v, rv * dv + c) : 0.f;
+  }
+  __syncthreads();
+  const int td = threadIdx.x >> 4, te = threadIdx.x & 15;
+  float acc[8][8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x)
+#pragma unroll
+    for (int y = 0; y < 8; ++y) acc[x][y] = 0.f;
+  for (int r = 0; r < n; ++r) {
+    const float4* kr = reinterpret_cast<const float4*>(Ks + r * kPad + 8 * td);
+    const float4* vr = reinterpret_cast<const float4*>(Vs + r * kPad + 8 * te);
+    const float4 k0 = kr[0], k1 = kr[1], v0 = vr[0], v1 = vr[1];
+    const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+    const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+#pragma unroll
+      for (int y = 0; y < 8; ++y) acc[x][y] = fmaf(kk[x], vv[y], acc[x][y]);
+  }
   const int64_t bh = (int64_t)b * a.H + h;
   float* U = reinterpret_cast<float*>(a.U) + (bh * a.N + i) * (int64_t)dk * dv;
-  for (int idx = threadIdx.x; idx < dk * dv; idx += kThreads) {
-    const int d = idx / dv, e = idx - d * dv;
-    float acc = 0.f;
-    for (int r = 0; r < n; ++r) acc = fmaf(w[r] * Ks[r * dk + d], Vs[r * dv + e], acc);
-    U[idx] = acc;
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    const int d = 8 * td + x;
+    if (d >= dk) break;
+#pragma unroll
+    for (int y = 0; y < 8; ++y)
+      if (8 * te + y < dv) U[(int64_t)d * dv + 8 * te + y] = acc[x][y];
   }
   if (threadIdx.x == 0) a.lg[bh * a.N + i] = lgi;
 }
@@ -188,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) simt_intra_readout(FwdArgs a) {
 template <typename InT, typename OutT>
 cudaError_t launch_typed(const FwdArgs& a, cudaStream_t s, StageEvents* ev) {
   const dim3 grid_c(a.N, a.H, a.B);
-  const size_t sm1 = sizeof(float) * ((size_t)a.C * (a.dk + a.dv) + 2 * a.C);
+  const size_t sm1 = sizeof(float) * ((size_t)a.C * 2 * kPad + 2 * a.C);
   const size_t sm3 = sizeof(float) * ((size_t)a.C * (2 * a.dk + a.dv) + (size_t)a.C * a.C +
                                       (size_t)kRowsPerStage * a.dv + a.C + (size_t)a.C * a.L);
   cudaError_t e;
@@ -215,7 +238,7 @@ cudaError_t launch_typed(const FwdArgs& a, cudaStream_t s, StageEvents* ev) {
 
 template <typename InT>
 cudaError_t launch_states_typed(const FwdArgs& a, cudaStream_t s) {
-  const size_t sm1 = sizeof(float) * ((size_t)a.C * (a.dk + a.dv) + 2 * a.C);
+  const size_t sm1 = sizeof(float) * ((size_t)a.C * 2 * kPad + 2 * a.C);
   cudaError_t e = cudaFuncSetAttribute(simt_chunk_state<InT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
   if (e != cudaSuccess) return e;
