@@ -56,6 +56,21 @@ __device__ __forceinline__ float row_sum(float x) {
   return x;
 }
 
+// Sum of lg[lo, hi) by the 32 lanes of warp 0, written to *dst by lane 0 (the caller
+// reads it after a block barrier).
+__device__ __forceinline__ void range_sum_warp0(const float* lg, int64_t lo, int64_t hi,
+                                                float* dst) {
+  if (threadIdx.x < 32) {
+    float x = 0.f;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += 32) x += lg[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (threadIdx.x == 0) *dst = x;
+  }
+}
+
+constexpr int kStageEl = kStage * 128 / kThreads;  // staged elements per thread (16)
+
 // Shared-memory views of one tile's rows (row strides padded by one float) and its
 // tile-local inclusive prefix sums of log a.
 struct TileRows {
@@ -113,7 +128,7 @@ __device__ TileRows carve_rows(float* sm, int dk, int dv) {
 // ---------------------------------------------------------------- dQ, dlambda, q . dQ
 
 template <typename InT, typename GT>
-__global__ void __launch_bounds__(kThreads) bwd_dq_kernel(BwdArgs A) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(BwdArgs A) {
   extern __shared__ float sm[];
   const FwdArgs& a = A.f;
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -187,12 +202,12 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_kernel(BwdArgs A) {
   const float* nodes = reinterpret_cast<const float*>(a.nodes) + bh * a.N * elems;
   const float* lg = a.lg + bh * a.N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float D_s[2];  // log decay from the block's end to the start of tile j
   __syncthreads();  // dO^T is in place; K is no longer read
   for (int m = 1; (int64_t(1) << (m - 1)) <= j; ++m) {
     int64_t c;
     if (!inter_block(j, m, &c)) continue;
-    float D = 0.f;  // log decay from the block's end to the start of tile j
-    for (int64_t i = c; i < j; ++i) D += lg[i];
+    range_sum_warp0(lg, c, j, &D_s[m & 1]);
     const float* S = nodes + c * elems;
     float x[4][4];
 #pragma unroll
@@ -226,6 +241,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_kernel(BwdArgs A) {
         if (4 * lane + q < dk) Xs[(4 * warp + r) * s.lq + 4 * lane + q] = x[r][q];
     __syncthreads();
     const int lvl = kLc + m;
+    const float D = D_s[m & 1];
     const float wq = t < n ? expf(s.cs[t] + D) : 0.f;
     const float wl = wq * s.lam[t * L + lvl];
     float dot = 0.f;
@@ -268,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_kernel(BwdArgs A) {
 //   sum_{t in j} exp(cs_t + D) lambda[t, 5+m] q_t dO_t^T,  D = log decay over [c', j).
 // Thread (td, te) owns rows [8 td, +8) and columns [8 te, +8) of the d_k x d_v state.
 template <typename InT, typename GT>
-__global__ void __launch_bounds__(kThreads) bwd_rstate_kernel(BwdArgs A) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_rstate_kernel(BwdArgs A) {
   extern __shared__ float sm[];
   const FwdArgs& a = A.f;
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -280,7 +296,7 @@ __global__ void __launch_bounds__(kThreads) bwd_rstate_kernel(BwdArgs A) {
   float* Qw = Qr + kC * 128;   // [kC][128] weighted q
   float* Gd = Qw + kC * 128;   // [kC][128] dO, zero-padded
   float* cs = Gd + kC * 128;   // [kC]
-  float* wt = cs + kC;         // [kC]
+  float* wt = cs + kC;         // [kC] row weights, then D of two levels
   if (threadIdx.x == 0) {
     float run = 0.f;
     for (int r = 0; r < n; ++r) {
@@ -302,11 +318,11 @@ __global__ void __launch_bounds__(kThreads) bwd_rstate_kernel(BwdArgs A) {
   for (int m = 1; (int64_t(1) << (m - 1)) <= j; ++m) {
     if (!((j >> (m - 1)) & 1)) continue;
     const int64_t c0 = ((int64_t)j >> (m - 1)) << (m - 1);
-    float D = 0.f;
-    for (int64_t i = c0; i < j; ++i) D += lg[i];
-    __syncthreads();  // cs ready (first level); Qw no longer read (later levels)
+    range_sum_warp0(lg, c0, j, &wt[kC + (m & 1)]);  // D: log decay over [c0, j)
+    __syncthreads();  // cs and D ready; Qw no longer read (later levels)
     if (threadIdx.x < kC) {
       const int r = threadIdx.x;
+      const float D = wt[kC + (m & 1)];
       wt[r] = r < n ? expf(cs[r] + D) *
                           a.lam[(((int64_t)b * a.T + t0 + r) * a.H + h) * L + kLc + m]
                     : 0.f;
@@ -413,19 +429,24 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
   const int64_t elems = (int64_t)dk * dv;
   const float* R = reinterpret_cast<const float*>(a.U) + bh * a.N * elems;
   const float* lg = a.lg + bh * a.N;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {  // warp 0: the level list, E_m summed across the lanes
+    const int lane0 = threadIdx.x;
     int nl = 0;
     for (int m = 1; (int64_t(1) << (m - 1)) < a.N; ++m) {
       if ((i >> (m - 1)) & 1) continue;
       const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
       if (c1 >= a.N) continue;
       float E = 0.f;
-      for (int64_t x = i + 1; x < c1; ++x) E += lg[x];
-      lv_c[nl] = c1;
-      lv_w[nl] = expf(E);
+      for (int64_t x = i + 1 + lane0; x < c1; x += 32) E += lg[x];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) E += __shfl_xor_sync(0xffffffffu, E, o);
+      if (lane0 == 0) {
+        lv_c[nl] = c1;
+        lv_w[nl] = expf(E);
+      }
       ++nl;
     }
-    lv_n = nl;
+    if (lane0 == 0) lv_n = nl;
   }
   __syncthreads();
   const int nl = lv_n;  // (the barrier above also ends the intra-tile reads of q and dO)
@@ -441,21 +462,32 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
     // register-blocked products: warp w owns source rows 4w..4w+3, lane g the features
     // 4g..4g+3; R_tot is formed while it is staged (levels summed with their weights)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float x[4][4], y[4][4];
+    float x[4][4];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) x[r][q] = y[r][q] = 0.f;
+      for (int q = 0; q < 4; ++q) x[r][q] = 0.f;
     // X = V R_tot^T: columns e0..e0+31 of R_tot, transposed, 16-byte groups swizzled
     for (int e0 = 0; e0 < dv; e0 += kStage) {
+      float val[kStageEl];  // summed over the levels before the barrier that frees the stage
+#pragma unroll
+      for (int it = 0; it < kStageEl; ++it) val[it] = 0.f;
+      for (int l = 0; l < nl; ++l) {
+        const float wl = lv_w[l];
+        const float* Rl = R + lv_c[l] * elems;
+#pragma unroll
+        for (int it = 0; it < kStageEl; ++it) {
+          const int idx = threadIdx.x + it * kThreads;
+          const int e = idx & (kStage - 1), f = idx >> 5;
+          if (f < dk && e0 + e < dv) val[it] = fmaf(wl, Rl[(int64_t)f * dv + e0 + e], val[it]);
+        }
+      }
       __syncthreads();
-      for (int idx = threadIdx.x; idx < kStage * 128; idx += kThreads) {
+#pragma unroll
+      for (int it = 0; it < kStageEl; ++it) {
+        const int idx = threadIdx.x + it * kThreads;
         const int e = idx & (kStage - 1), f = idx >> 5;
-        float val = 0.f;
-        if (f < dk && e0 + e < dv)
-          for (int l = 0; l < nl; ++l)
-            val = fmaf(lv_w[l], R[lv_c[l] * elems + (int64_t)f * dv + e0 + e], val);
-        St[e * 128 + ((((f >> 2) ^ e) << 2) | (f & 3))] = val;
+        St[e * 128 + ((((f >> 2) ^ e) << 2) | (f & 3))] = val[it];
       }
       __syncthreads();
       const int ne = min(kStage, dv - e0);
@@ -470,17 +502,34 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
           for (int q = 0; q < 4; ++q) x[r][q] = fmaf(aa[r], bb[q], x[r][q]);
       }
     }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)  // (k and v were transposed before the first barrier above)
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (4 * lane + q < dk) Xd[(4 * warp + r) * s.lq + 4 * lane + q] = x[r][q];
+    float y[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) y[r][q] = 0.f;
     // Y = K R_tot: rows d0..d0+31 of R_tot, row-major
     for (int d0 = 0; d0 < dk; d0 += kStage) {
-      __syncthreads();
-      for (int idx = threadIdx.x; idx < kStage * 128; idx += kThreads) {
-        const int f = idx >> 7, e = idx & 127;
-        float val = 0.f;
-        if (d0 + f < dk && e < dv)
-          for (int l = 0; l < nl; ++l)
-            val = fmaf(lv_w[l], R[lv_c[l] * elems + (int64_t)(d0 + f) * dv + e], val);
-        St[idx] = val;
+      float val[kStageEl];
+#pragma unroll
+      for (int it = 0; it < kStageEl; ++it) val[it] = 0.f;
+      for (int l = 0; l < nl; ++l) {
+        const float wl = lv_w[l];
+        const float* Rl = R + lv_c[l] * elems;
+#pragma unroll
+        for (int it = 0; it < kStageEl; ++it) {
+          const int idx = threadIdx.x + it * kThreads;
+          const int f = idx >> 7, e = idx & 127;
+          if (d0 + f < dk && e < dv) val[it] = fmaf(wl, Rl[(int64_t)(d0 + f) * dv + e], val[it]);
+        }
       }
+      __syncthreads();
+#pragma unroll
+      for (int it = 0; it < kStageEl; ++it) St[threadIdx.x + it * kThreads] = val[it];
       __syncthreads();
       const int nf = min(kStage, dk - d0);
       for (int f = 0; f < nf; ++f) {
@@ -497,11 +546,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int f = 4 * lane + q;
-        if (f < dk) Xd[(4 * warp + r) * s.lq + f] = x[r][q];
-        if (f < dv) Yd[(4 * warp + r) * s.lv + f] = y[r][q];
-      }
+      for (int q = 0; q < 4; ++q)
+        if (4 * lane + q < dv) Yd[(4 * warp + r) * s.lv + 4 * lane + q] = y[r][q];
     __syncthreads();
     const float lg_i = s.cs[kC - 1];  // this tile's log decay (tiles before the last are full)
     const float gs = u < n ? expf(lg_i - s.cs[u]) : 0.f;
@@ -593,7 +639,7 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
   const size_t sm_dq =
       sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * 128 + (size_t)kC * a.L);
   const size_t sm_dkv = sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * 128);
-  const size_t sm_r = sizeof(float) * (3 * kC * 128 + 2 * kC);
+  const size_t sm_r = sizeof(float) * (3 * kC * 128 + 2 * kC + 2);
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(bwd_dq_kernel<InT, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)sm_dq)) != cudaSuccess ||
