@@ -24,8 +24,9 @@
 //   dlog_a_i = sum over t >= i of dcum_t.
 //
 // Kernels: the forward's K1/K2 recompute U, the block states and the tile log decays;
-// bwd_dq (dQ, dlambda, q.dQ); bwd_rstate (R, accumulated over the block's tiles with
-// float4 atomics into the U buffer, which the level scan no longer needs); bwd_dkv (dK,
+// bwd_dq (dQ, dlambda, q.dQ); bwd_rstate (R, accumulated over the block's tiles, two
+// tiles per CTA, with float4 atomics into the U buffer, which the level scan no longer
+// needs); bwd_dkv (dK,
 // dV, k.dK); bwd_reduce_qk (per-head dQ, dK summed over the heads sharing a q/k head,
 // cast to the gradient type); bwd_dlog_a (reverse prefix sums over t).
 #include <algorithm>
@@ -279,63 +280,82 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(BwdArgs A) {
 
 // ---------------------------------------------------------------- mirrored block states
 
-// Tile j adds, for every set bit m-1 of j, its part of the mirrored state of the block
-// starting at c' = j with its low m-1 bits cleared:
-//   sum_{t in j} exp(cs_t + D) lambda[t, 5+m] q_t dO_t^T,  D = log decay over [c', j).
-// Thread (td, te) owns rows [8 td, +8) and columns [8 te, +8) of the d_k x d_v state.
+// Tiles j0 = 2p and j1 = 2p + 1 (one CTA) add, for every set bit m-1 of their indices,
+// their parts of the mirrored state of the block starting at c' = j with its low m-1
+// bits cleared:
+//   sum_{t in j} exp(cs_t + D_j) lambda[t, 5+m] q_t dO_t^T,  D_j = log decay over [c', j).
+// At every level above the first both tiles lie in the same block, so their parts are
+// summed before the atomics; level 1 is tile j1's alone.  Thread (td, te) owns rows
+// [8 td, +8) and columns [8 te, +8) of the d_k x d_v state.
 template <typename InT, typename GT>
 __global__ void __launch_bounds__(kThreads, 2) bwd_rstate_kernel(BwdArgs A) {
   extern __shared__ float sm[];
   const FwdArgs& a = A.f;
-  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  if (j == 0) return;
+  const int j0 = 2 * blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int j1 = j0 + 1;
+  if (j1 >= a.N && j0 == 0) return;  // a single tile has no mirrored state
   const int dk = a.dk, dv = a.dv, L = a.L, hq = h / a.hg;
-  const int t0 = j * kC, n = min(kC, a.T - t0);
+  const int n0 = min(kC, a.T - j0 * kC);
+  const int n1 = j1 < a.N ? min(kC, a.T - j1 * kC) : 0;
   const int64_t bh = (int64_t)b * a.H + h;
-  float* Qr = sm;              // [kC][128] q, zero-padded
-  float* Qw = Qr + kC * 128;   // [kC][128] weighted q
-  float* Gd = Qw + kC * 128;   // [kC][128] dO, zero-padded
-  float* cs = Gd + kC * 128;   // [kC]
-  float* wt = cs + kC;         // [kC] row weights, then D of two levels
-  if (threadIdx.x == 0) {
+  constexpr int kR = 2 * kC;   // rows of the pair
+  float* Qr = sm;              // [kR][128] q, zero-padded
+  float* Qw = Qr + kR * 128;   // [kR][128] weighted q
+  float* Gd = Qw + kR * 128;   // [kR][128] dO, zero-padded
+  float* cs = Gd + kR * 128;   // [kR] tile-local prefix sums of log a
+  float* wt = cs + kR;         // [kR] row weights
+  float* Ds = wt + kR;         // [2] D of the two tiles
+  if (threadIdx.x == 0 || threadIdx.x == 32) {
+    const int tile = threadIdx.x >> 5, n = tile ? n1 : n0;
+    const int64_t tok0 = (int64_t)b * a.T + (int64_t)(j0 + tile) * kC;
     float run = 0.f;
     for (int r = 0; r < n; ++r) {
-      if (a.log_a) run += a.log_a[((int64_t)b * a.T + t0 + r) * a.H + h];
-      cs[r] = run;
+      if (a.log_a) run += a.log_a[(tok0 + r) * a.H + h];
+      cs[tile * kC + r] = run;
     }
   }
-  for (int idx = threadIdx.x; idx < kC * 128; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < kR * 128; idx += kThreads) {
     const int r = idx >> 7, c = idx & 127;
-    const int64_t rq = ((int64_t)b * a.T + t0 + r) * a.Hqk + hq;
-    const int64_t rv = ((int64_t)b * a.T + t0 + r) * a.H + h;
-    Qr[idx] = (r < n && c < dk) ? ld<InT>(a.q, rq * dk + c) : 0.f;
-    Gd[idx] = (r < n && c < dv) ? ld<GT>(A.dout, rv * dv + c) : 0.f;
+    const bool live = r < kC ? r < n0 : r - kC < n1;
+    const int64_t tok = (int64_t)b * a.T + (int64_t)j0 * kC + r;
+    Qr[idx] = (live && c < dk) ? ld<InT>(a.q, (tok * a.Hqk + hq) * dk + c) : 0.f;
+    Gd[idx] = (live && c < dv) ? ld<GT>(A.dout, (tok * a.H + h) * dv + c) : 0.f;
   }
   const int64_t elems = (int64_t)dk * dv;
   float* R = reinterpret_cast<float*>(a.U) + bh * a.N * elems;
   const float* lg = a.lg + bh * a.N;
   const int td = threadIdx.x >> 4, te = threadIdx.x & 15;
-  for (int m = 1; (int64_t(1) << (m - 1)) <= j; ++m) {
-    if (!((j >> (m - 1)) & 1)) continue;
-    const int64_t c0 = ((int64_t)j >> (m - 1)) << (m - 1);
-    range_sum_warp0(lg, c0, j, &wt[kC + (m & 1)]);  // D: log decay over [c0, j)
-    __syncthreads();  // cs and D ready; Qw no longer read (later levels)
-    if (threadIdx.x < kC) {
-      const int r = threadIdx.x;
-      const float D = wt[kC + (m & 1)];
-      wt[r] = r < n ? expf(cs[r] + D) *
-                          a.lam[(((int64_t)b * a.T + t0 + r) * a.H + h) * L + kLc + m]
-                    : 0.f;
+  const int jtop = n1 > 0 ? j1 : j0;  // its set bits are the levels of the pair
+  for (int m = 1; (int64_t(1) << (m - 1)) <= jtop; ++m) {
+    if (!((jtop >> (m - 1)) & 1)) continue;
+    const int64_t c0 = ((int64_t)jtop >> (m - 1)) << (m - 1);
+    const bool in0 = (j0 >> (m - 1)) & 1, in1 = n1 > 0 && ((j1 >> (m - 1)) & 1);
+    __syncthreads();  // cs ready (first level); Qw and Ds no longer read (later levels)
+    if (threadIdx.x < 64) {  // warp w: D of tile j0 + w
+      const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      float x = 0.f;
+      for (int64_t i = c0 + lane; i < j0 + w; i += 32) x += lg[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (lane == 0) Ds[w] = x;
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < kC * 128; idx += kThreads) Qw[idx] = wt[idx >> 7] * Qr[idx];
+    if (threadIdx.x < kR) {
+      const int r = threadIdx.x, tile = r >= kC, rr = r - tile * kC;
+      const bool live = tile ? (in1 && rr < n1) : (in0 && rr < n0);
+      const int64_t tok = (int64_t)b * a.T + (int64_t)j0 * kC + r;
+      wt[r] = live ? expf(cs[r] + Ds[tile]) * a.lam[(tok * a.H + h) * L + kLc + m] : 0.f;
+    }
     __syncthreads();
+    for (int idx = threadIdx.x; idx < kR * 128; idx += kThreads) Qw[idx] = wt[idx >> 7] * Qr[idx];
+    __syncthreads();
+    const int r0 = in0 ? 0 : kC, r1 = in1 ? kC + n1 : n0;  // rows that contribute
     float acc[8][8];
 #pragma unroll
     for (int x = 0; x < 8; ++x)
 #pragma unroll
       for (int y = 0; y < 8; ++y) acc[x][y] = 0.f;
-    for (int r = 0; r < n; ++r) {
+    for (int r = r0; r < r1; ++r) {
       const float4* qr = reinterpret_cast<const float4*>(Qw + r * 128 + 8 * td);
       const float4* gr = reinterpret_cast<const float4*>(Gd + r * 128 + 8 * te);
       const float4 q0 = qr[0], q1 = qr[1], g0 = gr[0], g1 = gr[1];
@@ -639,7 +659,7 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
   const size_t sm_dq =
       sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * 128 + (size_t)kC * a.L);
   const size_t sm_dkv = sizeof(float) * (rows + 2 * kC * (kC + 1) + (size_t)kStage * 128);
-  const size_t sm_r = sizeof(float) * (3 * kC * 128 + 2 * kC + 2);
+  const size_t sm_r = sizeof(float) * (3 * 2 * kC * 128 + 2 * 2 * kC + 2);
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(bwd_dq_kernel<InT, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)sm_dq)) != cudaSuccess ||
@@ -655,7 +675,7 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
   if (a.N > 1) {
     const size_t rbytes = sizeof(float) * (size_t)a.B * a.H * a.N * a.dk * a.dv;
     if ((e = cudaMemsetAsync(a.U, 0, rbytes, s)) != cudaSuccess) return e;
-    bwd_rstate_kernel<InT, GT><<<grid, kThreads, sm_r, s>>>(A);
+    bwd_rstate_kernel<InT, GT><<<dim3((a.N + 1) / 2, a.H, a.B), kThreads, sm_r, s>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   bwd_dkv_kernel<InT, GT><<<grid, kThreads, sm_dkv, s>>>(A);
