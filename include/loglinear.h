@@ -188,8 +188,16 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
  *   dlambda [B, T, H, L] fp32 (levels above bit_length(T-1) receive 0)
  *   dout    [B, T, H, dv]    grad_dtype
  * q, k, v, log_a, lambda, B, T, H, Hqk, dk, dv and L as in loglinear_fwd; no chunk
- * argument: the gradients do not depend on it (the kernels work on 32-token tiles, fp32
- * on CUDA cores).  1 <= dk, dv <= 128, L <= 64.  All outputs are fully overwritten.
+ * argument: the gradients do not depend on it.  1 <= dk, dv <= 128, L <= 64.  All
+ * outputs are fully overwritten.
+ * path: LL_PATH_TC computes dq and dlambda on the tensor cores (bf16 inputs and
+ *   gradients, dk = 128, dv in {64, 128}; q, k, v, dout 16-byte aligned): a tensor-core
+ *   forward over the same inputs publishes its block states into the workspace, then
+ *   128-token tiles take dQ and dlambda from them with tcgen05; its dlambda and dq carry
+ *   bf16 roundings of P' and of the block states.  dk, dv and d log a use fp32 CUDA-core
+ *   kernels on 32-token tiles on every path.  LL_PATH_SIMT computes everything on CUDA
+ *   cores in fp32.  LL_PATH_AUTO takes the tensor cores when they apply.  The workspace
+ *   size depends on the path.
  * workspace: device scratch of at least loglinear_bwd_workspace_size() bytes, 256-byte
  * aligned (recomputed forward states, per-head q and k gradients).
  * Errors: LL_ERR_INVALID (null pointer, negative size, dlog_a NULL with log_a given),
@@ -198,12 +206,12 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
  */
 LL_API int loglinear_bwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Hqk,
                                         int64_t dk, int64_t dv, int64_t L, int in_dtype,
-                                        int grad_dtype, size_t* bytes);
+                                        int grad_dtype, int path, size_t* bytes);
 LL_API int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_a,
                          const float* lambda, const void* dout, void* dq, void* dk, void* dv,
                          float* dlog_a, float* dlambda, int64_t B, int64_t T, int64_t H,
                          int64_t Hqk, int64_t dk_dim, int64_t dv_dim, int64_t L, int in_dtype,
-                         int grad_dtype, void* workspace, size_t workspace_bytes,
+                         int grad_dtype, int path, void* workspace, size_t workspace_bytes,
                          ll_stream_t stream);
 
 /*

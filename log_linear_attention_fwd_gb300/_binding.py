@@ -46,9 +46,9 @@ SIGNATURES = {
     "loglinear_prefill": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                  _i64, _i64, _int, _int, _int, _int, _vp, _sz, _vp]),
     "loglinear_bwd_workspace_size": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _int, _int,
-                                            ctypes.POINTER(_sz)]),
+                                            _int, ctypes.POINTER(_sz)]),
     "loglinear_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
-                             _i64, _i64, _i64, _i64, _i64, _int, _int, _vp, _sz, _vp]),
+                             _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _sz, _vp]),
 }
 
 
@@ -250,19 +250,21 @@ def loglinear_fwd_noalloc(q, k, v, log_a, lam, chunk, out, path="auto", stream=N
     return out
 
 
-def bwd_workspace_size(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype) -> int:
+def bwd_workspace_size(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, path="auto") -> int:
     out = ctypes.c_size_t(0)
     st = _lib.loglinear_bwd_workspace_size(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype,
-                                           ctypes.byref(out))
+                                           PATHS[path], ctypes.byref(out))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_bwd_workspace_size")
     return int(out.value)
 
 
-def loglinear_bwd(q, k, v, log_a, lam, dout, workspace=None, stream=None):
+def loglinear_bwd(q, k, v, log_a, lam, dout, workspace=None, path="auto", stream=None):
     """Gradients of sum(dout ⊙ O) for O = loglinear_fwd(q, k, v, log_a, lam): returns
     (dq, dk, dv, dlog_a, dlam); dq, dk, dv in dout's dtype, dlog_a (None without decay)
-    and dlam fp32."""
+    and dlam fp32.  path: "tc" computes dq and dlam on the tensor cores (bf16, d_k = 128,
+    d_v in {64, 128}), "simt" everything on CUDA cores, "auto" the tensor cores if they
+    apply."""
     B, T, Hqk, dk = q.shape
     H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
     _check_dev("q", q, shape=(B, T, Hqk, dk))
@@ -277,14 +279,14 @@ def loglinear_bwd(q, k, v, log_a, lam, dout, workspace=None, stream=None):
     dv_ = torch.empty_like(v, dtype=dout.dtype)
     dla = None if log_a is None else torch.empty_like(log_a)
     dlam = torch.empty_like(lam)
-    ws_bytes = bwd_workspace_size(B, T, H, Hqk, dk, dv, L, in_dt, g_dt)
+    ws_bytes = bwd_workspace_size(B, T, H, Hqk, dk, dv, L, in_dt, g_dt, path)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), device=q.device, dtype=torch.uint8)
     _check_dev("workspace", workspace, torch.uint8)
     st = _lib.loglinear_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(dout),
                             _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dla), _ptr(dlam), B, T, H, Hqk,
-                            dk, dv, L, in_dt, g_dt, _ptr(workspace), workspace.numel(),
-                            _stream(stream))
+                            dk, dv, L, in_dt, g_dt, PATHS[path], _ptr(workspace),
+                            workspace.numel(), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_bwd")
     return dq, dk_, dv_, dla, dlam

@@ -651,8 +651,22 @@ __global__ void __launch_bounds__(kThreads) bwd_dlog_a_kernel(BwdArgs A) {
   }
 }
 
+// The tiles' log decays alone (when dQ runs on the tensor cores): one thread per tile.
+__global__ void __launch_bounds__(kThreads) bwd_tile_decay_kernel(FwdArgs a) {
+  const int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t tiles = (int64_t)a.B * a.H * a.N;
+  if (idx >= tiles) return;
+  const int64_t bh = idx / a.N, i = idx - bh * a.N;
+  const int64_t b = bh / a.H, h = bh - b * a.H;
+  const int t0 = (int)i * kC, n = min(kC, a.T - t0);
+  float run = 0.f;
+  if (a.log_a)
+    for (int r = 0; r < n; ++r) run += a.log_a[(b * a.T + t0 + r) * a.H + h];
+  a.lg[idx] = run;
+}
+
 template <typename InT, typename GT>
-cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
+cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s, bool dq_on_tc) {
   const FwdArgs& a = A.f;
   const dim3 grid(a.N, a.H, a.B);
   const size_t rows = tile_rows_floats(a.dk, a.dv, a.L);
@@ -670,8 +684,10 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_r)) !=
           cudaSuccess)
     return e;
-  bwd_dq_kernel<InT, GT><<<grid, kThreads, sm_dq, s>>>(A);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!dq_on_tc) {
+    bwd_dq_kernel<InT, GT><<<grid, kThreads, sm_dq, s>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (a.N > 1) {
     const size_t rbytes = sizeof(float) * (size_t)a.B * a.H * a.N * a.dk * a.dv;
     if ((e = cudaMemsetAsync(a.U, 0, rbytes, s)) != cudaSuccess) return e;
@@ -694,7 +710,7 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
 }  // namespace
 
 BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, int64_t dk,
-                                  int64_t dv) {
+                                  int64_t dv, int64_t n_tc) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   BwdWorkspace w;
   const size_t states = (size_t)(B * H * N) * (size_t)(dk * dv) * sizeof(float);
@@ -706,7 +722,15 @@ BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, in
   w.off_dkh = up(w.off_dqh + rows * dk * sizeof(float));
   w.off_dcq = up(w.off_dkh + rows * dk * sizeof(float));
   w.off_dck = up(w.off_dcq + rows * sizeof(float));
+  w.off_fwd = w.off_out = 0;
+  w.fwd = FwdWorkspace{};
   w.total = up(w.off_dck + rows * sizeof(float));
+  if (n_tc > 0) {
+    w.fwd = fwd_workspace_layout(B, H, n_tc, dk, dv, 2);
+    w.off_fwd = w.total;
+    w.off_out = up(w.off_fwd + w.fwd.total);
+    w.total = up(w.off_out + rows * dv * 2);
+  }
   return w;
 }
 
@@ -715,13 +739,21 @@ size_t bwd_smem_max(int dk, int dv, int L) {
                           (size_t)kC * L);
 }
 
-cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype, cudaStream_t s) {
-  cudaError_t e = launch_simt_states(A.f, in_dtype, s);
+cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype, cudaStream_t s,
+                                 bool dq_on_tc) {
+  cudaError_t e;
+  if (dq_on_tc) {
+    const int64_t tiles = (int64_t)A.f.B * A.f.H * A.f.N;
+    bwd_tile_decay_kernel<<<(unsigned)((tiles + kThreads - 1) / kThreads), kThreads, 0, s>>>(A.f);
+    e = cudaGetLastError();
+  } else {
+    e = launch_simt_states(A.f, in_dtype, s);
+  }
   if (e != cudaSuccess) return e;
-  if (in_dtype == LL_F32 && grad_dtype == LL_F32) return launch_typed<float, float>(A, s);
-  if (in_dtype == LL_F32) return launch_typed<float, __nv_bfloat16>(A, s);
-  if (grad_dtype == LL_F32) return launch_typed<__nv_bfloat16, float>(A, s);
-  return launch_typed<__nv_bfloat16, __nv_bfloat16>(A, s);
+  if (in_dtype == LL_F32 && grad_dtype == LL_F32) return launch_typed<float, float>(A, s, dq_on_tc);
+  if (in_dtype == LL_F32) return launch_typed<float, __nv_bfloat16>(A, s, dq_on_tc);
+  if (grad_dtype == LL_F32) return launch_typed<__nv_bfloat16, float>(A, s, dq_on_tc);
+  return launch_typed<__nv_bfloat16, __nv_bfloat16>(A, s, dq_on_tc);
 }
 
 }  // namespace ll

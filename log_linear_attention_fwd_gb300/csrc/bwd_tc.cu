@@ -1,0 +1,552 @@
+// Backward, dQ and dlambda, on the 5th-generation tensor cores (tcgen05 + TMEM + TMA):
+// bf16 q, k, v and dO with fp32 accumulation, d_k = 128, d_v = 64 or 128, 128-token tiles.
+//
+// With A = Q K^T, M[t, s] = exp(cum_t - cum_s) lambda[t, l(t, s)] (s <= t) and dA = dO V^T
+// (page "算力终结者来了！…", sections 结构矩阵 and 讨论与局限性: the backward needs the
+// lambda gradients besides the attention ones):
+//   dQ = (dA ⊙ M) K,
+//   dlambda[t, l] = sum over the level-l bucket of t of exp(cum_t - cum_s) dA[t, s] A[t, s].
+// Through the chunked decomposition with the 128-token tile as the chunk (page "论文阅读：
+// Log-Linear Attention", sections 矩阵分解 and 两阶段计算):
+//   * inside the tile both products are dense: S = Q K^T and S' = dO V^T go to TMEM;
+//     P' = S' ⊙ M is written to shared memory in bf16 while the dlambda bucket sums of
+//     exp(...) S' S are formed; dQ = P' K;
+//   * for every set bit m-1 of the tile index j, the block state Tot of slot
+//     c_m = (j >> (m-1)) << (m-1) (d_k x d_v) gives X = dO Tot^T, and
+//       dQ_t += lambda[t, 7+m] exp(cs_t + D_m) X_t,
+//       dlambda[t, 7+m] = exp(cs_t + D_m) q_t . X_t,
+//     D_m being the log decay from the block's end to the tile's start.
+// The block states are the ones a completed tensor-core forward over the same inputs left
+// in its workspace (tile states, the even slots' block states, their log decays), so no
+// CTA waits on another.  One CTA per tile, 8 warps (warps w and w+4 share TMEM lane
+// quarter w mod 4 and split the columns), 512 TMEM columns, one CTA per SM.  Every
+// mbarrier wait is bounded; a CTA whose wait times out sets g_tcb_error, skips what
+// depends on it, frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ll_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace ll {
+
+__device__ unsigned int g_tcb_error = 0;
+
+namespace {
+
+using namespace tc;
+
+constexpr int kTile = 128;                  // tokens per tile (= MMA M)
+constexpr int kD = 128;                     // d_k
+constexpr int kPanel = kTile * 64 * 2;      // one [128][64] bf16 panel: 16 KiB
+constexpr int kOperand = 2 * kPanel;        // a 128 x 128 bf16 tile: 32 KiB
+constexpr int kThreadsB = 256;
+constexpr int kIntra = 8;                   // levels inside a 128-token tile: 0..7
+constexpr int kLamStride = 9;
+constexpr int kTileLc = 7;
+constexpr int kMaxChunkLevels = 32;
+
+struct BqParams {
+  int B, T, H, hg, L, N;
+  const float* log_a;
+  const float* lam;
+  const float* lgu;    // [B*H][N] the tiles' log decays (forward workspace)
+  const float* nlg;    // [B*H][N] the even slots' block log decays (forward workspace)
+  float* dqh;          // [B, T, H, 128] per-head dQ
+  float* dcq;          // [B, T, H] q . dQ, or null
+  float* dlam;         // [B, T, H, L]
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 32 fp32 values as bf16 into columns [32c, 32c+32) of row r of a swizzled tile.
+__device__ __forceinline__ void put_row32_bf16(uint8_t* buf, int r, int c, const float* v) {
+  uint8_t* panel = buf + (c >> 1) * kPanel;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(panel + sw128_offset(r, (c & 1) * 4 + q)) =
+        make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                   pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+__device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
+  uint8_t* panel = buf + (c >> 1) * kPanel;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(panel + sw128_offset(r, (c & 1) * 4 + q)) = make_uint4(0, 0, 0, 0);
+}
+
+// Columns [32c, 32c+32) of row r of a swizzled bf16 tile, as fp32.
+__device__ __forceinline__ void get_row32(const uint8_t* buf, int r, int c, float* v) {
+  const uint8_t* panel = buf + (c >> 1) * kPanel;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = *reinterpret_cast<const uint4*>(panel + sw128_offset(r, (c & 1) * 4 + q));
+    const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+      v[8 * q + 2 * e] = f.x;
+      v[8 * q + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ float block_scan256(float x, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  float pre = 0.f;
+  for (int w = 0; w < warp; ++w) pre += red[w];
+  return x + pre;
+}
+
+struct BSmem {
+  // byte offsets from the 1024-aligned base
+  static constexpr int kQ = 0, kK = kOperand, kV = 2 * kOperand, kG = 3 * kOperand;
+  static constexpr int kBars = 4 * kOperand;                   // 9 mbarriers
+  static constexpr int kTslot = kBars + 12 * 8;
+  static constexpr int kRed = kTslot + 16;                     // 8 floats
+  static constexpr int kLg = kRed + 32;                        // 4 floats
+  static constexpr int kNl = kLg + 16;                         // kMaxChunkLevels floats
+  static constexpr int kCs = kNl + 4 * kMaxChunkLevels;        // 128 floats
+  static constexpr int kFcol = kCs + 4 * kTile;                // 128 floats
+  static constexpr int kLam = kFcol + 4 * kTile;               // [128][kLamStride] floats
+  static constexpr int kDlb = kLam + 4 * kTile * kLamStride;   // [2][128][8] floats
+  static constexpr int kLamX = kDlb + 4 * 2 * kTile * kIntra;  // [levels][128] floats
+};
+
+// ... then [levels][128] floats of inter-level dlambda sums after LamX
+size_t smem_bwd_dq(int levels) {
+  return (size_t)BSmem::kLamX + 2 * 4 * (size_t)kTile * levels + 1024;
+}
+
+template <int DV>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                     const __grid_constant__ CUtensorMap tmU,
+                     const __grid_constant__ CUtensorMap tmNode, BqParams p, int levels) {
+  constexpr int kPanels = DV / 64;
+  constexpr int kVBytes = kTile * DV * 2;
+  constexpr int kStateBytes = kD * DV * 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* Qb = smem + BSmem::kQ;    // Q (S, then the q . X dots)
+  uint8_t* Kb = smem + BSmem::kK;    // K (S, then dQ = P' K), then block states
+  uint8_t* Vb = smem + BSmem::kV;    // V (S'), then P', then block states
+  uint8_t* Gb = smem + BSmem::kG;    // dO (S' and the level MMAs)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BSmem::kBars);
+  uint64_t* bar_load = &bars[0];
+  uint64_t* bar_s = &bars[1];
+  uint64_t* bar_dq = &bars[2];
+  uint64_t* bar_lvl = &bars[3];      // [2]
+  uint64_t* bar_node = &bars[5];     // [2]
+  uint64_t* bar_free = &bars[7];     // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + BSmem::kTslot);
+  float* red = reinterpret_cast<float*>(smem + BSmem::kRed);
+  float* lg_s = reinterpret_cast<float*>(smem + BSmem::kLg);
+  float* nl_s = reinterpret_cast<float*>(smem + BSmem::kNl);
+  float* cs_s = reinterpret_cast<float*>(smem + BSmem::kCs);
+  float* fcol = reinterpret_cast<float*>(smem + BSmem::kFcol);
+  float* lam_s = reinterpret_cast<float*>(smem + BSmem::kLam);
+  float* dlb = reinterpret_cast<float*>(smem + BSmem::kDlb);
+  float* lamx = reinterpret_cast<float*>(smem + BSmem::kLamX);
+  float* dli = lamx + levels * kTile;  // [levels][128] q . X sums of the inter levels
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int qt = warp & 3, hh = warp >> 2;
+  const int r = tid & (kTile - 1);
+  const int BH = p.B * p.H;
+  const int j = blockIdx.x / BH, bhi = blockIdx.x - j * BH;  // tile j of every (b, h) in turn
+  const int b = bhi / p.H, h = bhi - b * p.H, hq = h / p.hg;
+  const int64_t N = p.N, bh = bhi;
+  const int t0 = j * kTile;
+  const int n = min(kTile, p.T - t0);
+  const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;
+  const int nlev = __popc((unsigned)j);
+  const bool row_live = r < n;
+
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  if (tid == 64) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    prefetch_tensormap(&tmG);
+    prefetch_tensormap(&tmU);
+    prefetch_tensormap(&tmNode);
+    for (int q = 0; q < 7; ++q) mbar_init(&bars[q], 1);
+    mbar_init(&bar_free[0], kThreadsB / 32);
+    mbar_init(&bar_free[1], kThreadsB / 32);
+    fence_mbar_init();
+  }
+  for (int i = tid; i < 2 * kTile * kIntra; i += kThreadsB) dlb[i] = 0.f;
+  for (int i = tid; i < levels * kTile; i += kThreadsB) dli[i] = 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
+  bool landed = true;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_load, 2 * kOperand + 2 * kVBytes);
+    tma_load_4d(&tmQ, bar_load, Qb, 0, hq, t0, b);
+    tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, hq, t0, b);
+    tma_load_4d(&tmK, bar_load, Kb, 0, hq, t0, b);
+    tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, hq, t0, b);
+#pragma unroll
+    for (int pv = 0; pv < kPanels; ++pv) {
+      tma_load_4d(&tmV, bar_load, Vb + pv * kPanel, 64 * pv, h, t0, b);
+      tma_load_4d(&tmG, bar_load, Gb + pv * kPanel, 64 * pv, h, t0, b);
+    }
+  }
+  __syncwarp();
+
+  // per-row data: log a, the intra-tile lambdas (levels 0..7, split between the row's two
+  // threads), the inter-level lambdas
+  const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
+  float lam_in[kIntra / 2];
+#pragma unroll
+  for (int i = 0; i < kIntra / 2; ++i) {
+    const int l = hh * (kIntra / 2) + i;
+    lam_in[i] = (row_live && l < p.L) ? p.lam[row * p.L + l] : 0.f;
+  }
+  {
+    int k = 0;
+    for (int m = 1; m < kMaxChunkLevels; ++m) {
+      if (!((j >> (m - 1)) & 1)) continue;
+      if ((k & 1) == hh) lamx[k * kTile + r] = row_live ? p.lam[row * p.L + kTileLc + m] : 0.f;
+      ++k;
+    }
+  }
+  if (tid == 0) {  // S = Q K^T and S' = dO V^T as soon as the tiles land
+    landed = mbar_wait(bar_load, 0);
+    if (landed) {
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+      const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb), ga = smem_u32(Gb), va = smem_u32(Vb);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+        mma_bf16(tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                 idesc, kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < DV / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+        mma_bf16(tmem + 128, smem_desc_sw128(ga + off, 16, 1024),
+                 smem_desc_sw128(va + off, 16, 1024), idesc, kk > 0);
+      }
+      mma_commit(bar_s);
+    }
+  }
+  const float cs_scan = block_scan256(la, red);
+  if (hh == 0) cs_s[r] = cs_scan;
+  if (tid == kTile - 1) lg_s[0] = cs_scan;
+#pragma unroll
+  for (int i = 0; i < kIntra / 2; ++i)
+    lam_s[r * kLamStride + hh * (kIntra / 2) + i] = lam_in[i];
+  __syncthreads();
+  const float cs = cs_s[r];
+  if (hh == 1) fcol[r] = __expf(cs_s[r | 31] - cs);
+
+  bool all_ok = __syncthreads_and(landed);
+  bool ok = all_ok && mbar_wait(bar_s, 0);
+  tc_fence_after();
+  all_ok = __syncthreads_and(ok);
+
+  // ---- P' = S' ⊙ M (bf16, into Vb: S' no longer reads V) and the intra-tile dlambda bins
+  // sum_s exp(cs_t - cs_s) S'[t, s] S[t, s] per level; chunk c of row r as in the forward
+  float* bins = dlb + (hh * kTile + r) * kIntra;  // this thread's bins (private)
+  if (all_ok) {
+    const float* lam_r = lam_s + r * kLamStride;
+    for (int c = hh; c < kTile / 32; c += 2) {
+      if (c > qt) {
+        put_row32_zero(Vb, r, c);
+        continue;
+      }
+      float sp[32], sa[32];
+      tmem_ld32(tmem + lane_base + 128 + c * 32, sp);
+      tmem_ld32(tmem + lane_base + c * 32, sa);
+      if (c < qt) {  // one level for the whole chunk: 5 + bit_length(qt XOR c)
+        const int lvl = 5 + (32 - __clz((unsigned)(qt ^ c)));
+        const float ge = __expf(cs - cs_s[c * 32 + 31]);
+        const float wl = lam_r[lvl] * ge;
+        float wsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float x = sp[k] * fcol[c * 32 + k];
+          wsum = fmaf(x, sa[k], wsum);
+          sp[k] = x * wl;
+        }
+        bins[lvl] += ge * wsum;
+      } else {  // the diagonal chunk
+        const bool fact = cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f;
+        const float gt = __expf(cs - cs_s[c * 32 + 31]);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int s = c * 32 + k;
+          float pv = 0.f;
+          if (s <= r && row_live) {
+            const int lvl = fenwick_level((uint32_t)r, (uint32_t)s);
+            const float e = fact ? gt * fcol[s] : __expf(cs - cs_s[s]);
+            const float x = sp[k] * e;
+            bins[lvl] += x * sa[k];
+            pv = x * lam_r[lvl];
+          }
+          sp[k] = pv;
+        }
+      }
+      put_row32_bf16(Vb, r, c, sp);
+    }
+  }
+  tc_fence_after();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  all_ok = __syncthreads_and(all_ok);
+  // ---- dQ = P' K into TMEM columns 256..383 (K MN-major as B)
+  if (all_ok && tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+    const uint32_t pa = smem_u32(Vb), ka = smem_u32(Kb);
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk) {
+      const uint32_t aoff = (kk >> 2) * kPanel + (kk & 3) * 32;
+      mma_bf16(tmem + 256, smem_desc_sw128(pa + aoff, 16, 1024),
+               smem_desc_sw128(ka + kk * 2048, kPanel, 1024), idesc, kk > 0);
+    }
+    mma_commit(bar_dq);
+  }
+  __syncwarp();
+  // the row's intra-tile dlambda (levels 0..7) and zeros for the levels above, which the
+  // inter levels overwrite below (the same thread writes both)
+  if (all_ok && hh == 0 && row_live) {
+    for (int l = 0; l < p.L; ++l)
+      p.dlam[row * p.L + l] = l < kIntra ? bins[l] + dlb[(kTile + r) * kIntra + l] : 0.f;
+  }
+  // the levels' block states: slot c_m holds U_{c-1} for odd c, the even block state else
+  int my_c = 0;
+  {
+    const int k = tid - 32;
+    if (k >= 0 && k < nlev) {
+      int m = 0;
+      for (int seen = -1; seen < k;) {
+        ++m;
+        if ((j >> (m - 1)) & 1) ++seen;
+      }
+      my_c = (j >> (m - 1)) << (m - 1);
+      nl_s[k] = (my_c & 1) ? p.lgu[bh * N + my_c - 1] : p.nlg[bh * N + my_c];
+    }
+  }
+  ok = all_ok && mbar_wait(bar_dq, 0);
+  tc_fence_after();
+  all_ok = __syncthreads_and(ok);
+  auto fetch = [&](int k) {  // thread 32+k: TMA of level k's block state into (k odd ? Kb : Vb)
+    if (tid == 32 + k) {
+      uint8_t* dst = (k & 1) ? Kb : Vb;
+      const bool is_u = (my_c & 1) != 0;
+      const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
+      mbar_arrive_expect_tx(&bar_node[k & 1], kStateBytes);
+#pragma unroll
+      for (int pv = 0; pv < kPanels; ++pv)
+        tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[k & 1], dst + pv * kPanel, 64 * pv, row0);
+    }
+  };
+  if (all_ok) {  // Kb (dQ's B) and Vb (P') are free
+    if (nlev > 0) fetch(0);
+    if (nlev > 1) fetch(1);
+  }
+  __syncwarp();
+
+  // ---- dQ into registers: this thread's half row, d in [64 hh, 64 hh + 64)
+  float dq[64];
+#pragma unroll
+  for (int q = 0; q < 64; ++q) dq[q] = 0.f;
+  if (all_ok) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float v[32];
+      tmem_ld32(tmem + lane_base + 256 + 64 * hh + c * 32, v);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) dq[c * 32 + q] = v[q];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- inter-tile levels (the forward's barrier-free loop): MMA k = dO Tot_k^T into TMEM
+  // columns [128 (k & 1), +128); each warp adds level k-1 to dQ and its q . X to the
+  // level's dlambda sum, then releases that TMEM buffer
+  const int lane = tid & 31;
+  uint32_t lvl_ph[2] = {0, 0}, node_ph[2] = {0, 0}, free_ph[2] = {0, 0};
+  float D = 0.f;
+  bool lv_ok = all_ok;
+  for (int k = 0; k <= nlev && all_ok; ++k) {
+    if (tid == 0 && k < nlev) {
+      bool go = lv_ok && mbar_wait(&bar_node[k & 1], node_ph[k & 1]);
+      node_ph[k & 1] ^= 1;
+      if (k >= 2) {
+        go = go && mbar_wait(&bar_free[k & 1], free_ph[k & 1]);
+        free_ph[k & 1] ^= 1;
+      }
+      if (go) {
+        tc_fence_after();
+        // A = dO (K-major over d_v), B = the block state [d_k][d_v] (K-major: N = d_k)
+        constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+        const uint32_t ga = smem_u32(Gb), sa = smem_u32((k & 1) ? Kb : Vb);
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+          mma_bf16(tmem + (k & 1) * 128, smem_desc_sw128(ga + off, 16, 1024),
+                   smem_desc_sw128(sa + off, 16, 1024), idesc, kk > 0);
+        }
+        mma_commit(&bar_lvl[k & 1]);
+      }
+      lv_ok = go;
+    }
+    __syncwarp();
+    if (k >= 1) {
+      const int bf = (k - 1) & 1;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_lvl[bf], lvl_ph[bf]));
+      lvl_ph[bf] ^= 1;
+      if (!got) {
+        lv_ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (k + 1 < nlev) fetch(k + 1);  // into the buffer MMA k-1 has finished reading
+      const float e = __expf(cs + D);
+      const float wl = lamx[(k - 1) * kTile + r] * e;
+      D += nl_s[k - 1];
+      float dot = 0.f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float v[32], qv[32];
+        tmem_ld32(tmem + lane_base + bf * 128 + 64 * hh + c * 32, v);
+        get_row32(Qb, r, 2 * hh + c, qv);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          dq[c * 32 + q] = fmaf(wl, v[q], dq[c * 32 + q]);
+          dot = fmaf(qv[q], v[q], dot);
+        }
+      }
+      atomicAdd(&dli[(k - 1) * kTile + r], e * dot);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_free[bf]);
+    }
+  }
+  all_ok = __syncthreads_and(all_ok && lv_ok);
+
+  // ---- epilogue: the inter-level dlambda, dQ (fp32), and q . dQ = sum_l lambda[t, l]
+  // dlambda[t, l] (O is linear in each row's lambdas), which takes q . dQ from the fp32
+  // products S and S' rather than from dQ, whose P' was rounded to bf16
+  if (all_ok) {
+    if (hh == 0 && row_live) {
+      const float* lam_r = lam_s + r * kLamStride;
+      float qd = 0.f;
+#pragma unroll
+      for (int l = 0; l < kIntra; ++l)
+        qd = fmaf(lam_r[l], dlb[r * kIntra + l] + dlb[(kTile + r) * kIntra + l], qd);
+      int k = 0;
+      for (int m = 1; m < kMaxChunkLevels && k < nlev; ++m) {
+        if (!((j >> (m - 1)) & 1)) continue;
+        const float v = dli[k * kTile + r];
+        p.dlam[row * p.L + kTileLc + m] = v;
+        qd = fmaf(lamx[k * kTile + r], v, qd);
+        ++k;
+      }
+      if (p.dcq) p.dcq[row] = qd;
+    }
+    if (row_live) {
+      float4* dst = reinterpret_cast<float4*>(p.dqh + row * kD + 64 * hh);
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        dst[q] = make_float4(dq[4 * q], dq[4 * q + 1], dq[4 * q + 2], dq[4 * q + 3]);
+    }
+  } else if (tid == 0) {
+    atomicOr(&g_tcb_error, 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+bool tc_bwd_dq_supported(int64_t dk, int64_t dv, int in_dtype, int grad_dtype) {
+  return in_dtype == LL_BF16 && grad_dtype == LL_BF16 && dk == kD && (dv == 64 || dv == 128);
+}
+
+cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, float* dcq,
+                             float* dlam, cudaStream_t s) {
+  if (f.dk != kD || (f.dv != 64 && f.dv != 128) || f.C != kTile) return cudaErrorInvalidValue;
+  const int64_t rows = (int64_t)f.B * f.H * f.N * kD;  // TMA row coordinates are int32
+  if (rows > INT32_MAX) return cudaErrorInvalidValue;
+  const int dv = f.dv;
+  CUtensorMap tmQ, tmK, tmV, tmG, tmU, tmNode;
+  if (!make_tokens_map(&tmQ, f.q, f.B, f.T, f.Hqk, kD) ||
+      !make_tokens_map(&tmK, f.k, f.B, f.T, f.Hqk, kD) ||
+      !make_tokens_map(&tmV, f.v, f.B, f.T, f.H, dv) ||
+      !make_tokens_map(&tmG, dout, f.B, f.T, f.H, dv) || !make_rows_map(&tmU, f.U, rows, dv) ||
+      !make_rows_map(&tmNode, f.nodes, rows, dv))
+    return cudaErrorInvalidValue;
+  BqParams p;
+  p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
+  p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.nlg = f.nlg;
+  p.dqh = dqh; p.dcq = dcq; p.dlam = dlam;
+  int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
+  while ((int64_t(1) << levels) < f.N) ++levels;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(tc_bwd_dq_kernel<128>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem_bwd_dq(kMaxChunkLevels - 1));
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(tc_bwd_dq_kernel<64>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem_bwd_dq(kMaxChunkLevels - 1));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
+  if (dv == 128)
+    tc_bwd_dq_kernel<128><<<tiles, kThreadsB, smem_bwd_dq(levels), s>>>(tmQ, tmK, tmV, tmG, tmU,
+                                                                         tmNode, p, levels);
+  else
+    tc_bwd_dq_kernel<64><<<tiles, kThreadsB, smem_bwd_dq(levels), s>>>(tmQ, tmK, tmV, tmG, tmU,
+                                                                        tmNode, p, levels);
+  return cudaGetLastError();
+}
+
+cudaError_t tcb_take_error(cudaStream_t s, unsigned* flags) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_tcb_error, sizeof(v), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && v) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_tcb_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  *flags = v;
+  return e;
+}
+
+}  // namespace ll

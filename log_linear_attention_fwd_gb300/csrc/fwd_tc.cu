@@ -659,9 +659,11 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
+}  // namespace
+
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -703,8 +705,6 @@ bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows, int width) {
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int /*chunk*/) {
   return in_dtype == LL_BF16 && dk == kD && (dv == 64 || dv == 128);

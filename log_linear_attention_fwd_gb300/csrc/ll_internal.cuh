@@ -124,11 +124,24 @@ struct BwdArgs {
   float* dck;           // [B, T, H] k_t . dk_t per head (workspace)
 };
 struct BwdWorkspace {
-  size_t off_U, off_nodes, off_lg, off_dqh, off_dkh, off_dcq, off_dck, total;
+  size_t off_U, off_nodes, off_lg, off_dqh, off_dkh, off_dcq, off_dck;
+  size_t off_fwd, off_out;  // tensor-core dQ only: a forward's workspace and its output
+  FwdWorkspace fwd;         // that forward workspace's own layout (offsets from off_fwd)
+  size_t total;
 };
+// N: 32-token tiles; n_tc: 128-token tiles of the tensor-core dQ, or 0 without it.
 BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, int64_t dk,
-                                  int64_t dv);
-cudaError_t launch_simt_backward(const BwdArgs& a, int in_dtype, int grad_dtype, cudaStream_t s);
+                                  int64_t dv, int64_t n_tc);
+// dq_on_tc: dQ, dlambda and q . dQ come from the tensor cores; the CUDA-core part then
+// computes only the tile log decays, the mirrored states and dK, dV.
+cudaError_t launch_simt_backward(const BwdArgs& a, int in_dtype, int grad_dtype, cudaStream_t s,
+                                 bool dq_on_tc);
+// Tensor-core dQ and dlambda from a completed tensor-core forward's workspace (f: that
+// forward's arguments, 128-token tiles): per-head dQ, q . dQ (dcq may be null), dlambda.
+bool tc_bwd_dq_supported(int64_t dk, int64_t dv, int in_dtype, int grad_dtype);
+cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, float* dcq,
+                             float* dlam, cudaStream_t s);
+cudaError_t tcb_take_error(cudaStream_t s, unsigned* flags);
 size_t bwd_smem_max(int dk, int dv, int L);  // largest dynamic shared memory of a kernel
 // The decode state at position T-1 from a completed forward's workspace (tc_layout: the
 // tensor-core path's bf16 block states; both paths store them [d_k][d_v]).

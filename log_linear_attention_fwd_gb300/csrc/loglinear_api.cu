@@ -283,10 +283,18 @@ int loglinear_decode_step(float* state, const void* q, const void* k, const void
 
 // ---------------------------------------------------------------- backward
 
+// N: 32-token tiles of the CUDA-core part; *n_tc: 128-token tiles of the tensor-core dQ
+// when that path is taken, else 0.
 static int check_bwd(int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk, int64_t dv,
-                     int64_t L, int in_dtype, int grad_dtype, int64_t* N) {
+                     int64_t L, int in_dtype, int grad_dtype, int path, int64_t* N,
+                     int64_t* n_tc) {
   if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1 || L < 1) return LL_ERR_INVALID;
   if (!dtype_ok(in_dtype) || !dtype_ok(grad_dtype)) return LL_ERR_DTYPE;
+  if (path != LL_PATH_AUTO && path != LL_PATH_SIMT && path != LL_PATH_TC) return LL_ERR_INVALID;
+  const bool tc_ok = tc_bwd_dq_supported(dk, dv, in_dtype, grad_dtype);
+  if (path == LL_PATH_TC && !tc_ok) return LL_ERR_UNSUPPORTED;
+  const bool tc = path == LL_PATH_TC || (path == LL_PATH_AUTO && tc_ok);
+  *n_tc = tc ? (T + kTcTile - 1) / kTcTile : 0;
   const int sh = check_qk_heads(H, Hqk);
   if (sh != LL_OK) return sh;
   if (T > INT32_MAX || B * H > INT32_MAX / 2) return LL_ERR_UNSUPPORTED;
@@ -297,31 +305,33 @@ static int check_bwd(int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk, i
 }
 
 int loglinear_bwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk,
-                                 int64_t dv, int64_t L, int in_dtype, int grad_dtype,
+                                 int64_t dv, int64_t L, int in_dtype, int grad_dtype, int path,
                                  size_t* bytes) {
   if (!bytes) return LL_ERR_INVALID;
-  int64_t N;
-  const int st = check_bwd(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, &N);
+  int64_t N, n_tc;
+  const int st = check_bwd(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, path, &N, &n_tc);
   if (st != LL_OK) return st;
-  *bytes = bwd_workspace_layout(B, T, H, N, dk, dv).total;
+  *bytes = bwd_workspace_layout(B, T, H, N, dk, dv, n_tc).total;
   return LL_OK;
 }
 
 int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_a,
                   const float* lambda, const void* dout, void* dq, void* dk_out, void* dv_out,
                   float* dlog_a, float* dlambda, int64_t B, int64_t T, int64_t H, int64_t Hqk,
-                  int64_t dk, int64_t dv, int64_t L, int in_dtype, int grad_dtype,
+                  int64_t dk, int64_t dv, int64_t L, int in_dtype, int grad_dtype, int path,
                   void* workspace, size_t workspace_bytes, ll_stream_t stream) {
-  int64_t N;
-  const int st = check_bwd(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, &N);
+  int64_t N, n_tc;
+  const int st = check_bwd(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, path, &N, &n_tc);
   if (st != LL_OK) return st;
   if (B == 0 || T == 0 || H == 0) return LL_OK;
   if (!q || !k || !v || !lambda || !dout || !dq || !dk_out || !dv_out || !dlambda)
     return LL_ERR_INVALID;
   if (log_a && !dlog_a) return LL_ERR_INVALID;
-  const BwdWorkspace w = bwd_workspace_layout(B, T, H, N, dk, dv);
+  const BwdWorkspace w = bwd_workspace_layout(B, T, H, N, dk, dv, n_tc);
   if (!workspace || workspace_bytes < w.total) return LL_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_ALIGN;
+  if (n_tc > 0 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(dout)))
+    return LL_ERR_ALIGN;
   BwdArgs A;
   FwdArgs& a = A.f;
   a.q = q; a.k = k; a.v = v; a.log_a = log_a; a.lam = lambda; a.out = nullptr;
@@ -340,14 +350,37 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
   A.dkh = reinterpret_cast<float*>(ws + w.off_dkh);
   A.dcq = log_a ? reinterpret_cast<float*>(ws + w.off_dcq) : nullptr;
   A.dck = log_a ? reinterpret_cast<float*>(ws + w.off_dck) : nullptr;
-  const cudaError_t e =
-      launch_simt_backward(A, in_dtype, grad_dtype, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (n_tc > 0) {
+    // dQ and dlambda on the tensor cores: a tensor-core forward publishes the block states
+    // (its output goes to scratch), then the dQ kernel reads them
+    FwdArgs f = a;
+    f.C = kTcTile;
+    f.lc = log2_exact(kTcTile);
+    f.N = (int)n_tc;
+    char* fw = ws + w.off_fwd;
+    f.out = ws + w.off_out;
+    f.U = fw + w.fwd.off_U;
+    f.nodes = fw + w.fwd.off_nodes;
+    f.lg = reinterpret_cast<float*>(fw + w.fwd.off_lg);
+    f.nlg = reinterpret_cast<float*>(fw + w.fwd.off_nlg);
+    f.rdy_u = reinterpret_cast<uint32_t*>(fw + w.fwd.off_rdy_u);
+    f.rdy_n = reinterpret_cast<uint32_t*>(fw + w.fwd.off_rdy_n);
+    f.tick = reinterpret_cast<uint32_t*>(fw + w.fwd.off_tick);
+    e = launch_tc_forward(f, LL_BF16, s, nullptr);
+    if (e == cudaSuccess) e = launch_tc_bwd_dq(f, dout, A.dqh, A.dcq, dlambda, s);
+  }
+  if (e == cudaSuccess) e = launch_simt_backward(A, in_dtype, grad_dtype, s, n_tc > 0);
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 
 int loglinear_device_error(ll_stream_t stream, unsigned* flags) {
   if (!flags) return LL_ERR_INVALID;
-  const cudaError_t e = tc_take_error(reinterpret_cast<cudaStream_t>(stream), flags);
+  unsigned f1 = 0, f2 = 0;
+  cudaError_t e = tc_take_error(reinterpret_cast<cudaStream_t>(stream), &f1);
+  if (e == cudaSuccess) e = tcb_take_error(reinterpret_cast<cudaStream_t>(stream), &f2);
+  *flags = f1 | f2;
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 

@@ -181,12 +181,13 @@ def test_bwd_validation_codes(L):
     def bwd(**kw):
         a = dict(q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, dout=FAKE, dq=FAKE, dk=FAKE,
                  dv=FAKE, dla=None, dlam=FAKE, B=1, T=64, H=2, Hqk=2, dkd=16, dvd=16, Lv=7,
-                 ind=L.LL_F32, gd=L.LL_F32, ws=None, wsb=0, stream=None)
+                 ind=L.LL_F32, gd=L.LL_F32, path=L.LL_PATH_AUTO, ws=None, wsb=0, stream=None)
         a.update(kw)
         return L.lib().loglinear_bwd(a["q"], a["k"], a["v"], a["log_a"], a["lam"], a["dout"],
                                      a["dq"], a["dk"], a["dv"], a["dla"], a["dlam"], a["B"],
                                      a["T"], a["H"], a["Hqk"], a["dkd"], a["dvd"], a["Lv"],
-                                     a["ind"], a["gd"], a["ws"], a["wsb"], a["stream"])
+                                     a["ind"], a["gd"], a["path"], a["ws"], a["wsb"],
+                                     a["stream"])
     assert bwd(Lv=6) == L.LL_ERR_SHAPE                  # T=64 needs L >= 7
     assert bwd(H=4, Hqk=3) == L.LL_ERR_SHAPE
     assert bwd(ind=3) == L.LL_ERR_DTYPE
@@ -196,9 +197,20 @@ def test_bwd_validation_codes(L):
     assert bwd(dq=None) == L.LL_ERR_INVALID
     assert bwd(dlam=None) == L.LL_ERR_INVALID
     assert bwd(log_a=FAKE, dla=None) == L.LL_ERR_INVALID   # d log a wanted with a decay
+    assert bwd(path=7) == L.LL_ERR_INVALID
+    assert bwd(path=L.LL_PATH_TC) == L.LL_ERR_UNSUPPORTED   # fp32, d 16: no tensor-core dQ
+    assert bwd(path=L.LL_PATH_TC, dkd=128, dvd=64, ind=L.LL_BF16, gd=L.LL_F32) == \
+        L.LL_ERR_UNSUPPORTED                                 # dO must be bf16 as well
+    tc_kw = dict(dkd=128, dvd=64, ind=L.LL_BF16, gd=L.LL_BF16, ws=FAKE, wsb=1 << 40)
+    assert bwd(path=L.LL_PATH_TC, q=ctypes.c_void_p(0x1002), **tc_kw) == L.LL_ERR_ALIGN
     assert bwd() == L.LL_ERR_WORKSPACE
     assert bwd(ws=ctypes.c_void_p(0x1010), wsb=1 << 40) == L.LL_ERR_ALIGN
     assert bwd(T=0, q=None, k=None, v=None, lam=None, dout=None, dq=None, dk=None, dv=None,
                dlam=None) == L.LL_OK
     sz = L.bwd_workspace_size(1, 64, 2, 2, 16, 16, 7, L.LL_F32, L.LL_F32)
     assert sz >= 2 * (1 * 2 * 2 * 16 * 16 * 4) + 2 * 64 * 2 * 16 * 4   # states + per-head dq, dk
+    # the tensor-core dQ adds a forward's workspace and an output scratch
+    tc = L.bwd_workspace_size(1, 1000, 2, 2, 128, 64, 11, L.LL_BF16, L.LL_BF16, "tc")
+    simt = L.bwd_workspace_size(1, 1000, 2, 2, 128, 64, 11, L.LL_BF16, L.LL_BF16, "simt")
+    assert tc >= simt + 1000 * 2 * 64 * 2
+    assert L.bwd_workspace_size(1, 1000, 2, 2, 128, 64, 11, L.LL_BF16, L.LL_BF16) == tc

@@ -44,12 +44,13 @@ def _oracle_grads(x, dout):
     return g, dla_scale
 
 
-def _check(LL, cfg, tol, tol_dla, seed=0):
+def _check(LL, cfg, tol, tol_dla, seed=0, path="auto"):
     x = W.make_fwd_inputs(cfg)
     dout = _dout(cfg, seed + 100)
     d = cuda(x)
-    got = LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout.cuda())
+    got = LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout.cuda(), path=path)
     torch.cuda.synchronize()
+    assert LL.device_error() == 0
     want, dla_scale = _oracle_grads(x, dout)
     errs = {}
     for name, gt in zip(("q", "k", "v", "log_a", "lam"), got):
@@ -62,7 +63,7 @@ def _check(LL, cfg, tol, tol_dla, seed=0):
                                                            1e-300)
         else:
             errs[name] = rel_l2(gt.cpu(), want[name])
-    print(f"bwd {cfg.name} T={cfg.T} H={cfg.H}/{cfg.qk_heads} dk={cfg.dk} dv={cfg.dv} "
+    print(f"bwd {path} {cfg.name} T={cfg.T} H={cfg.H}/{cfg.qk_heads} dk={cfg.dk} dv={cfg.dv} "
           + " ".join(f"{k}={v:.2e}" for k, v in errs.items()))
     for name, e in errs.items():
         assert e <= (tol_dla if name == "log_a" else tol), (name, e)
@@ -82,11 +83,32 @@ def test_bwd_f32_head_dims(LL, dk, dv):
     _check(LL, cfg, TOL_G32, TOL_DLA32, seed=dk)
 
 
-@pytest.mark.parametrize("T,dv", [(300, 64), (2049, 64), (1000, 128)])
-def test_bwd_bf16_matches_oracle(LL, T, dv):
+@pytest.mark.parametrize("path", ["tc", "simt"])
+@pytest.mark.parametrize("T,dv", [(300, 64), (2049, 64), (1000, 128), (77, 128), (4096, 128)])
+def test_bwd_bf16_matches_oracle(LL, T, dv, path):
     L = (T - 1).bit_length() + 1
     cfg = W.FwdConfig("bwd_bf16", 1, 2, T, 128, dv, 64, L, "bf16", True, "softplus", seed=T + dv)
-    _check(LL, cfg, TOL_BF16, TOL_BF16, seed=T)
+    _check(LL, cfg, TOL_BF16, TOL_BF16, seed=T, path=path)
+
+
+def test_bwd_tc_one_hot_lambda_exact(LL):
+    """Integers that stay exact through bf16 states and P': dlambda of the tensor-core
+    path equals the oracle's bit for bit at every level, and dq equals it up to the final
+    bf16 rounding."""
+    T = 1151
+    L = (T - 1).bit_length() + 1
+    for lvl in range(L):
+        x = W.make_sparse_int_inputs(1, T, 2, 128, L, lvl, seed=lvl, dv=64)
+        g = torch.Generator().manual_seed(lvl)
+        dout = torch.randint(-1, 2, (1, T, 2, 64), generator=g).to(torch.bfloat16)
+        d = cuda(x)
+        got = LL.loglinear_bwd(d["q"], d["k"], d["v"], None, d["lam"], dout.cuda(), path="tc")
+        want = oracle.backward_direct(x["q"], x["k"], x["v"], None, x["lam"], dout)
+        assert LL.device_error() == 0
+        # dq is exact in fp32 and then cast to dO's bf16: compare with the exact value
+        # rounded the same way
+        assert torch.equal(got[0].cpu(), torch.tensor(want["q"]).to(torch.bfloat16)), lvl
+        assert np.array_equal(got[4].cpu().double().numpy(), want["lam"]), lvl
 
 
 @pytest.mark.parametrize("H,Hqk,dtype", [(4, 1, "f32"), (6, 2, "f32"), (4, 1, "bf16")])
