@@ -190,14 +190,15 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
  * q, k, v, log_a, lambda, B, T, H, Hqk, dk, dv and L as in loglinear_fwd; no chunk
  * argument: the gradients do not depend on it.  1 <= dk, dv <= 128, L <= 64.  All
  * outputs are fully overwritten.
- * path: LL_PATH_TC computes dq and dlambda on the tensor cores (bf16 inputs and
+ * path: LL_PATH_TC computes dq, dk, dv and dlambda on the tensor cores (bf16 inputs and
  *   gradients, dk = 128, dv in {64, 128}; q, k, v, dout 16-byte aligned): a tensor-core
  *   forward over the same inputs publishes its block states into the workspace, then
- *   128-token tiles take dQ and dlambda from them with tcgen05; its dlambda and dq carry
- *   bf16 roundings of P' and of the block states.  dk, dv and d log a use fp32 CUDA-core
- *   kernels on 32-token tiles on every path.  LL_PATH_SIMT computes everything on CUDA
- *   cores in fp32.  LL_PATH_AUTO takes the tensor cores when they apply.  The workspace
- *   size depends on the path.
+ *   128-token tiles take dQ and dlambda from them with tcgen05; the mirrored states of
+ *   later tiles that dk and dv read are accumulated in fp32 on CUDA cores, then dK and dV
+ *   are formed per 128-token tile with tcgen05.  These carry the bf16 roundings of P, P'
+ *   and of the states.  LL_PATH_SIMT computes everything on CUDA cores in fp32.
+ *   LL_PATH_AUTO takes the tensor cores when they apply.  The workspace size depends on
+ *   the path.
  * workspace: device scratch of at least loglinear_bwd_workspace_size() bytes, 256-byte
  * aligned (recomputed forward states, per-head q and k gradients).
  * Errors: LL_ERR_INVALID (null pointer, negative size, dlog_a NULL with log_a given),

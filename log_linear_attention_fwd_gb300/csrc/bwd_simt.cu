@@ -30,6 +30,7 @@
 // dV, k.dK); bwd_reduce_qk (per-head dQ, dK summed over the heads sharing a q/k head,
 // cast to the gradient type); bwd_dlog_a (reverse prefix sums over t).
 #include <algorithm>
+#include <functional>
 
 #include "ll_internal.cuh"
 
@@ -666,7 +667,8 @@ __global__ void __launch_bounds__(kThreads) bwd_tile_decay_kernel(FwdArgs a) {
 }
 
 template <typename InT, typename GT>
-cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s, bool dq_on_tc) {
+cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s, bool dq_on_tc,
+                         const std::function<cudaError_t()>& dkv_tc) {
   const FwdArgs& a = A.f;
   const dim3 grid(a.N, a.H, a.B);
   const size_t rows = tile_rows_floats(a.dk, a.dv, a.L);
@@ -694,8 +696,12 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s, bool dq_on_tc) {
     bwd_rstate_kernel<InT, GT><<<dim3((a.N + 1) / 2, a.H, a.B), kThreads, sm_r, s>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  bwd_dkv_kernel<InT, GT><<<grid, kThreads, sm_dkv, s>>>(A);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (dkv_tc) {
+    if ((e = dkv_tc()) != cudaSuccess) return e;
+  } else {
+    bwd_dkv_kernel<InT, GT><<<grid, kThreads, sm_dkv, s>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   const int64_t total = (int64_t)a.B * a.T * a.Hqk * a.dk;
   const unsigned blocks = (unsigned)std::min<int64_t>((total + kThreads - 1) / kThreads, 152 * 16);
   bwd_reduce_qk_kernel<GT><<<blocks, kThreads, 0, s>>>(A, total);
@@ -740,7 +746,7 @@ size_t bwd_smem_max(int dk, int dv, int L) {
 }
 
 cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype, cudaStream_t s,
-                                 bool dq_on_tc) {
+                                 bool dq_on_tc, const std::function<cudaError_t()>& dkv_tc) {
   cudaError_t e;
   if (dq_on_tc) {
     const int64_t tiles = (int64_t)A.f.B * A.f.H * A.f.N;
@@ -750,10 +756,11 @@ cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype,
     e = launch_simt_states(A.f, in_dtype, s);
   }
   if (e != cudaSuccess) return e;
-  if (in_dtype == LL_F32 && grad_dtype == LL_F32) return launch_typed<float, float>(A, s, dq_on_tc);
-  if (in_dtype == LL_F32) return launch_typed<float, __nv_bfloat16>(A, s, dq_on_tc);
-  if (grad_dtype == LL_F32) return launch_typed<__nv_bfloat16, float>(A, s, dq_on_tc);
-  return launch_typed<__nv_bfloat16, __nv_bfloat16>(A, s, dq_on_tc);
+  if (in_dtype == LL_F32 && grad_dtype == LL_F32)
+    return launch_typed<float, float>(A, s, dq_on_tc, dkv_tc);
+  if (in_dtype == LL_F32) return launch_typed<float, __nv_bfloat16>(A, s, dq_on_tc, dkv_tc);
+  if (grad_dtype == LL_F32) return launch_typed<__nv_bfloat16, float>(A, s, dq_on_tc, dkv_tc);
+  return launch_typed<__nv_bfloat16, __nv_bfloat16>(A, s, dq_on_tc, dkv_tc);
 }
 
 }  // namespace ll

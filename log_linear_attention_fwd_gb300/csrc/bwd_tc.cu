@@ -489,6 +489,399 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ------------------------------------------------------------------ dK and dV
+//
+// Source s of tile i receives, from the queries t of its own tile,
+//   dK_s = sum_t P'[t, s] q_t,  dV_s = sum_t P[t, s] dO_t   (P = M ⊙ S, P' = M ⊙ S'),
+// i.e. dK = P'^T Q and dV = P^T dO with P and P' read MN-major as the A operand; and from
+// the later tiles, through the mirrored states (fp32, accumulated by the state kernel on
+// 32-token tiles; the 128-token block at c is its 32-token slot 4c), summed over the
+// tile's levels into R_tot = sum_m exp(E_m) R_{c_m} (E_m: log decay of the tiles strictly
+// between i and c_m):
+//   dK_s += g_s R_tot v_s,  dV_s += g_s R_tot^T k_s,  g_s = exp(lg_i - cs_s),
+// taken as MMAs with the rows of V and K scaled by g in place.  k_s . dK_s, which d log a
+// needs, is the column sum of G = M ⊙ S ⊙ S' (from the fp32 S and S') plus v_s . dV_inter.
+
+struct BkvParams {
+  int B, T, H, hg, L, N, N32;
+  const float* log_a;
+  const float* lam;
+  const float* lgu;          // [B*H][N] the tiles' log decays (forward workspace)
+  const float* R32;          // [B*H][N32][d_k][d_v] mirrored states, fp32
+  const __nv_bfloat16* v;    // [B, T, H, d_v] (for v . dV)
+  float* dkh;                // [B, T, H, 128] per-head dK
+  float* dck;                // [B, T, H] k . dK, or null
+  __nv_bfloat16* dv;         // [B, T, H, d_v]
+};
+
+struct KvSmem {
+  static constexpr int kQ = 0, kK = kOperand, kV = 2 * kOperand, kG = 3 * kOperand;
+  static constexpr int kP1 = 4 * kOperand;   // P' (dK), then R_tot
+  static constexpr int kP0 = 5 * kOperand;   // P (dV)
+  static constexpr int kBars = 6 * kOperand; // load, s, kv, inter
+  static constexpr int kTslot = kBars + 8 * 8;
+  static constexpr int kRed = kTslot + 16;
+  static constexpr int kLg = kRed + 32;
+  static constexpr int kCs = kLg + 16;                         // 128 floats
+  static constexpr int kFcol = kCs + 4 * kTile;                // 128 floats
+  static constexpr int kCol = kFcol + 4 * kTile;               // 128 floats: column sums of G
+  static constexpr int kVd = kCol + 4 * kTile;                 // [2][128] floats
+  static constexpr int kLvC = kVd + 4 * 2 * kTile;             // 32 ints: block starts
+  static constexpr int kLvW = kLvC + 4 * kMaxChunkLevels;      // 32 floats: exp(E_m)
+  static constexpr int kLvN = kLvW + 4 * kMaxChunkLevels;      // 1 int
+  static constexpr int kLam = kLvN + 16;                       // [128][kLamStride] floats
+  static constexpr int kEnd = kLam + 4 * kTile * kLamStride;
+};
+
+size_t smem_bwd_dkv() { return (size_t)KvSmem::kEnd + 1024; }
+
+// Multiplies the 16-byte chunks [g0, g0 + cnt) of row r of a swizzled tile by s (chunk g
+// is columns 8g..8g+7: panel g / 8).
+__device__ __forceinline__ void scale_row_chunks(uint8_t* buf, int r, int g0, int cnt, float sc) {
+  for (int g = g0; g < g0 + cnt; ++g) {
+    uint4* ptr = reinterpret_cast<uint4*>(buf + (g >> 3) * kPanel + sw128_offset(r, g & 7));
+    uint4 u = *ptr;
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[k]));
+      w[k] = pack_bf16(f.x * sc, f.y * sc);
+    }
+    *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <int DV>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                      BkvParams p) {
+  constexpr int kPanels = DV / 64;
+  constexpr int kVBytes = kTile * DV * 2;
+  constexpr int kHalf = DV / 2;      // d_v columns per thread
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* Qb = smem + KvSmem::kQ;
+  uint8_t* Kb = smem + KvSmem::kK;
+  uint8_t* Vb = smem + KvSmem::kV;
+  uint8_t* Gb = smem + KvSmem::kG;
+  uint8_t* P1 = smem + KvSmem::kP1;
+  uint8_t* P0 = smem + KvSmem::kP0;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + KvSmem::kBars);
+  uint64_t* bar_load = &bars[0];
+  uint64_t* bar_s = &bars[1];
+  uint64_t* bar_kv = &bars[2];
+  uint64_t* bar_inter = &bars[3];
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + KvSmem::kTslot);
+  float* red = reinterpret_cast<float*>(smem + KvSmem::kRed);
+  float* lg_s = reinterpret_cast<float*>(smem + KvSmem::kLg);
+  float* cs_s = reinterpret_cast<float*>(smem + KvSmem::kCs);
+  float* fcol = reinterpret_cast<float*>(smem + KvSmem::kFcol);
+  float* colsum = reinterpret_cast<float*>(smem + KvSmem::kCol);
+  float* vd_s = reinterpret_cast<float*>(smem + KvSmem::kVd);
+  int* lv_c = reinterpret_cast<int*>(smem + KvSmem::kLvC);
+  float* lv_w = reinterpret_cast<float*>(smem + KvSmem::kLvW);
+  int* lv_n = reinterpret_cast<int*>(smem + KvSmem::kLvN);
+  float* lam_s = reinterpret_cast<float*>(smem + KvSmem::kLam);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = warp & 3, hh = warp >> 2;
+  const int r = tid & (kTile - 1);
+  const int BH = p.B * p.H;
+  const int i = blockIdx.x / BH, bhi = blockIdx.x - i * BH;
+  const int b = bhi / p.H, h = bhi - b * p.H, hq = h / p.hg;
+  const int64_t bh = bhi;
+  const int t0 = i * kTile;
+  const int n = min(kTile, p.T - t0);
+  const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;
+  const bool row_live = r < n;
+
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  if (tid == 64) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    prefetch_tensormap(&tmG);
+    for (int q = 0; q < 4; ++q) mbar_init(&bars[q], 1);
+    fence_mbar_init();
+  }
+  if (tid < kTile) colsum[tid] = 0.f;
+  if (warp == 2) {  // the tile's levels: blocks of later tiles, with exp(E_m)
+    int nl = 0;
+    for (int m = 1; (int64_t(1) << (m - 1)) < p.N; ++m) {
+      if ((i >> (m - 1)) & 1) continue;
+      const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
+      if (c1 >= p.N) continue;
+      float E = 0.f;
+      for (int64_t x = i + 1 + lane; x < c1; x += 32) E += p.lgu[bh * p.N + x];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) E += __shfl_xor_sync(0xffffffffu, E, o);
+      if (lane == 0) {
+        lv_c[nl] = (int)c1;
+        lv_w[nl] = __expf(E);
+      }
+      ++nl;
+    }
+    if (lane == 0) *lv_n = nl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
+  const int nl = *lv_n;
+  bool landed = true;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_load, 2 * kOperand + 2 * kVBytes);
+    tma_load_4d(&tmQ, bar_load, Qb, 0, hq, t0, b);
+    tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, hq, t0, b);
+    tma_load_4d(&tmK, bar_load, Kb, 0, hq, t0, b);
+    tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, hq, t0, b);
+#pragma unroll
+    for (int pv = 0; pv < kPanels; ++pv) {
+      tma_load_4d(&tmV, bar_load, Vb + pv * kPanel, 64 * pv, h, t0, b);
+      tma_load_4d(&tmG, bar_load, Gb + pv * kPanel, 64 * pv, h, t0, b);
+    }
+  }
+  __syncwarp();
+  const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
+  float lam_in[kIntra / 2];
+#pragma unroll
+  for (int q = 0; q < kIntra / 2; ++q) {
+    const int l = hh * (kIntra / 2) + q;
+    lam_in[q] = (row_live && l < p.L) ? p.lam[row * p.L + l] : 0.f;
+  }
+  if (tid == 0) {  // S = Q K^T, S' = dO V^T
+    landed = mbar_wait(bar_load, 0);
+    if (landed) {
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+      const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb), ga = smem_u32(Gb), va = smem_u32(Vb);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+        mma_bf16(tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                 idesc, kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < DV / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+        mma_bf16(tmem + 128, smem_desc_sw128(ga + off, 16, 1024),
+                 smem_desc_sw128(va + off, 16, 1024), idesc, kk > 0);
+      }
+      mma_commit(bar_s);
+    }
+  }
+  const float cs_scan = block_scan256(la, red);
+  if (hh == 0) cs_s[r] = cs_scan;
+  if (tid == kTile - 1) lg_s[0] = cs_scan;
+#pragma unroll
+  for (int q = 0; q < kIntra / 2; ++q) lam_s[r * kLamStride + hh * (kIntra / 2) + q] = lam_in[q];
+  __syncthreads();
+  const float cs = cs_s[r];
+  const float lg = lg_s[0];
+  if (hh == 1) fcol[r] = __expf(cs_s[r | 31] - cs);
+
+  bool all_ok = __syncthreads_and(landed);
+  bool ok = all_ok && mbar_wait(bar_s, 0);
+  tc_fence_after();
+  all_ok = __syncthreads_and(ok);
+
+  // ---- P (into P0) and P' (into P1) for row r's chunks, the column sums of G; and the
+  // rows of K and V scaled by g_r = exp(lg - cs_r) for the inter-tile MMAs (S and S' are
+  // done with K and V)
+  if (all_ok) {
+    const float* lam_r = lam_s + r * kLamStride;
+    for (int c = hh; c < kTile / 32; c += 2) {
+      if (c > qt) {
+        put_row32_zero(P0, r, c);
+        put_row32_zero(P1, r, c);
+        continue;
+      }
+      float sa[32], sp[32];
+      tmem_ld32(tmem + lane_base + c * 32, sa);
+      tmem_ld32(tmem + lane_base + 128 + c * 32, sp);
+      if (c < qt) {
+        const int lvl = 5 + (32 - __clz((unsigned)(qt ^ c)));
+        const float wl = lam_r[lvl] * __expf(cs - cs_s[c * 32 + 31]);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float m = wl * fcol[c * 32 + k];
+          const float g = m * sa[k] * sp[k];
+          sa[k] *= m;
+          sp[k] *= m;
+          float x = g;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+          if (lane == 0) atomicAdd(&colsum[c * 32 + k], x);
+        }
+      } else {
+        const bool fact = cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f;
+        const float gt = __expf(cs - cs_s[c * 32 + 31]);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int s = c * 32 + k;
+          float m = 0.f;
+          if (s <= r && row_live)
+            m = lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] *
+                (fact ? gt * fcol[s] : __expf(cs - cs_s[s]));
+          float x = m * sa[k] * sp[k];
+          sa[k] *= m;
+          sp[k] *= m;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+          if (lane == 0) atomicAdd(&colsum[s], x);
+        }
+      }
+      put_row32_bf16(P0, r, c, sa);
+      put_row32_bf16(P1, r, c, sp);
+    }
+    if (nl > 0) {  // g_r = exp(lg - cs_r): decay from row r to the tile's end
+      const float g = row_live ? __expf(lg - cs) : 0.f;
+      scale_row_chunks(Kb, r, 8 * hh, 8, g);
+      scale_row_chunks(Vb, r, (DV / 16) * hh, DV / 16, g);
+    }
+  }
+  tc_fence_after();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  all_ok = __syncthreads_and(all_ok);
+  // ---- dK = P'^T Q into TMEM 256..383, dV = P^T dO into 384..384+DV (A MN-major)
+  if (all_ok && tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t idk = idesc_bf16(128, 128, 1, 1);
+    constexpr uint32_t idv = idesc_bf16(128, DV, 1, 1);
+    const uint32_t p1 = smem_u32(P1), p0 = smem_u32(P0), qa = smem_u32(Qb), ga = smem_u32(Gb);
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk) {
+      mma_bf16(tmem + 256, smem_desc_sw128(p1 + kk * 2048, kPanel, 1024),
+               smem_desc_sw128(qa + kk * 2048, kPanel, 1024), idk, kk > 0);
+      mma_bf16(tmem + 384, smem_desc_sw128(p0 + kk * 2048, kPanel, 1024),
+               smem_desc_sw128(ga + kk * 2048, kPanel, 1024), idv, kk > 0);
+    }
+    mma_commit(bar_kv);
+  }
+  __syncwarp();
+  // ---- R_tot row r (d_k), this thread's half of d_v, summed over the levels while the
+  // MMAs run (fp32 loads), then written in bf16 over P' once dK's MMA is done with it
+  float rt[kHalf];
+#pragma unroll
+  for (int q = 0; q < kHalf; ++q) rt[q] = 0.f;
+  if (all_ok) {
+    const int64_t elems = (int64_t)kD * DV;
+    for (int l = 0; l < nl; ++l) {
+      const float w = lv_w[l];
+      const float4* src = reinterpret_cast<const float4*>(
+          p.R32 + (bh * p.N32 + 4 * (int64_t)lv_c[l]) * elems + (int64_t)r * DV + kHalf * hh);
+#pragma unroll
+      for (int q = 0; q < kHalf / 4; ++q) {
+        const float4 x = __ldcg(src + q);
+        rt[4 * q] = fmaf(w, x.x, rt[4 * q]);
+        rt[4 * q + 1] = fmaf(w, x.y, rt[4 * q + 1]);
+        rt[4 * q + 2] = fmaf(w, x.z, rt[4 * q + 2]);
+        rt[4 * q + 3] = fmaf(w, x.w, rt[4 * q + 3]);
+      }
+    }
+  }
+  ok = all_ok && mbar_wait(bar_kv, 0);
+  tc_fence_after();
+  all_ok = __syncthreads_and(ok);
+  if (all_ok && nl > 0) {
+#pragma unroll
+    for (int c = 0; c < kPanels; ++c) put_row32_bf16(P1, r, kPanels * hh + c, rt + 32 * c);
+  }
+  tc_fence_after();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  // ---- dK += (g V) R_tot^T (B K-major: N = d_k), dV_inter = (g K) R_tot (B MN-major: N = d_v)
+  if (all_ok && nl > 0 && tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t idk = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idv = idesc_bf16(128, DV, 0, 1);
+    const uint32_t ra = smem_u32(P1), va = smem_u32(Vb), ka = smem_u32(Kb);
+#pragma unroll
+    for (int kk = 0; kk < DV / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+      mma_bf16(tmem + 256, smem_desc_sw128(va + off, 16, 1024), smem_desc_sw128(ra + off, 16, 1024),
+               idk, 1);
+    }
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+      mma_bf16(tmem, smem_desc_sw128(ka + off, 16, 1024),
+               smem_desc_sw128(ra + kk * 2048, kPanel, 1024), idv, kk > 0);
+    }
+    mma_commit(bar_inter);
+  }
+  __syncwarp();
+  if (nl > 0) {
+    ok = all_ok && mbar_wait(bar_inter, 0);
+    tc_fence_after();
+    all_ok = __syncthreads_and(ok);
+  }
+  // ---- epilogue: dK (fp32, per head), dV = intra + inter (bf16), k . dK
+  if (all_ok) {
+    float vd = 0.f;
+    {
+      float v0[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld32(tmem + lane_base + 256 + 64 * hh + 32 * c, v0);
+        if (row_live) {
+          float4* dst = reinterpret_cast<float4*>(p.dkh + row * kD + 64 * hh + 32 * c);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kPanels; ++c) {
+      float a[32], x[32];
+      tmem_ld32(tmem + lane_base + 384 + kHalf * hh + 32 * c, a);
+      if (nl > 0) {
+        tmem_ld32(tmem + lane_base + kHalf * hh + 32 * c, x);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) x[q] = 0.f;
+      }
+      if (row_live) {
+        const int col = kHalf * hh + 32 * c;
+        const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + row * DV + col);
+        uint4* dst = reinterpret_cast<uint4*>(p.dv + row * DV + col);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = vsrc[q];
+          const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+            vd = fmaf(f.x, x[8 * q + 2 * e], vd);
+            vd = fmaf(f.y, x[8 * q + 2 * e + 1], vd);
+          }
+          dst[q] = make_uint4(pack_bf16(a[8 * q] + x[8 * q], a[8 * q + 1] + x[8 * q + 1]),
+                              pack_bf16(a[8 * q + 2] + x[8 * q + 2], a[8 * q + 3] + x[8 * q + 3]),
+                              pack_bf16(a[8 * q + 4] + x[8 * q + 4], a[8 * q + 5] + x[8 * q + 5]),
+                              pack_bf16(a[8 * q + 6] + x[8 * q + 6], a[8 * q + 7] + x[8 * q + 7]));
+        }
+      }
+    }
+    vd_s[hh * kTile + r] = vd;
+    __syncthreads();
+    if (hh == 0 && row_live && p.dck)
+      p.dck[row] = colsum[r] + vd_s[r] + vd_s[kTile + r];
+  } else if (tid == 0) {
+    atomicOr(&g_tcb_error, 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
 }  // namespace
 
 bool tc_bwd_dq_supported(int64_t dk, int64_t dv, int in_dtype, int grad_dtype) {
@@ -533,6 +926,41 @@ cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, flo
   else
     tc_bwd_dq_kernel<64><<<tiles, kThreadsB, smem_bwd_dq(levels), s>>>(tmQ, tmK, tmV, tmG, tmU,
                                                                         tmNode, p, levels);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R32, int N32,
+                              float* dkh, float* dck, void* dv, cudaStream_t s) {
+  if (f.dk != kD || (f.dv != 64 && f.dv != 128) || f.C != kTile) return cudaErrorInvalidValue;
+  const int dvw = f.dv;
+  CUtensorMap tmQ, tmK, tmV, tmG;
+  if (!make_tokens_map(&tmQ, f.q, f.B, f.T, f.Hqk, kD) ||
+      !make_tokens_map(&tmK, f.k, f.B, f.T, f.Hqk, kD) ||
+      !make_tokens_map(&tmV, f.v, f.B, f.T, f.H, dvw) ||
+      !make_tokens_map(&tmG, dout, f.B, f.T, f.H, dvw))
+    return cudaErrorInvalidValue;
+  BkvParams p;
+  p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N; p.N32 = N32;
+  p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.R32 = R32;
+  p.v = static_cast<const __nv_bfloat16*>(f.v);
+  p.dkh = dkh; p.dck = dck; p.dv = static_cast<__nv_bfloat16*>(dv);
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(tc_bwd_dkv_kernel<128>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem_bwd_dkv());
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(tc_bwd_dkv_kernel<64>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem_bwd_dkv());
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
+  if (dvw == 128)
+    tc_bwd_dkv_kernel<128><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, p);
+  else
+    tc_bwd_dkv_kernel<64><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, p);
   return cudaGetLastError();
 }
 

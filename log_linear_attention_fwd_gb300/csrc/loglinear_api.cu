@@ -370,8 +370,14 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
     f.tick = reinterpret_cast<uint32_t*>(fw + w.fwd.off_tick);
     e = launch_tc_forward(f, LL_BF16, s, nullptr);
     if (e == cudaSuccess) e = launch_tc_bwd_dq(f, dout, A.dqh, A.dcq, dlambda, s);
+    if (e == cudaSuccess)
+      e = launch_simt_backward(A, in_dtype, grad_dtype, s, true, [&]() {
+        return launch_tc_bwd_dkv(f, dout, reinterpret_cast<const float*>(a.U), a.N, A.dkh,
+                                 A.dck, dv_out, s);
+      });
+    return e == cudaSuccess ? LL_OK : cuda_fail(e);
   }
-  if (e == cudaSuccess) e = launch_simt_backward(A, in_dtype, grad_dtype, s, n_tc > 0);
+  e = launch_simt_backward(A, in_dtype, grad_dtype, s, false, nullptr);
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 
