@@ -30,7 +30,6 @@
 // dV, k.dK); bwd_reduce_qk (per-head dQ, dK summed over the heads sharing a q/k head,
 // cast to the gradient type); bwd_dlog_a (reverse prefix sums over t).
 #include <algorithm>
-#include <functional>
 
 #include "ll_internal.cuh"
 
@@ -652,23 +651,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dlog_a_kernel(BwdArgs A) {
   }
 }
 
-// The tiles' log decays alone (when dQ runs on the tensor cores): one thread per tile.
-__global__ void __launch_bounds__(kThreads) bwd_tile_decay_kernel(FwdArgs a) {
-  const int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-  const int64_t tiles = (int64_t)a.B * a.H * a.N;
-  if (idx >= tiles) return;
-  const int64_t bh = idx / a.N, i = idx - bh * a.N;
-  const int64_t b = bh / a.H, h = bh - b * a.H;
-  const int t0 = (int)i * kC, n = min(kC, a.T - t0);
-  float run = 0.f;
-  if (a.log_a)
-    for (int r = 0; r < n; ++r) run += a.log_a[(b * a.T + t0 + r) * a.H + h];
-  a.lg[idx] = run;
-}
-
 template <typename InT, typename GT>
-cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s, bool dq_on_tc,
-                         const std::function<cudaError_t()>& dkv_tc) {
+cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
   const FwdArgs& a = A.f;
   const dim3 grid(a.N, a.H, a.B);
   const size_t rows = tile_rows_floats(a.dk, a.dv, a.L);
@@ -686,31 +670,16 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s, bool dq_on_tc,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_r)) !=
           cudaSuccess)
     return e;
-  if (!dq_on_tc) {
-    bwd_dq_kernel<InT, GT><<<grid, kThreads, sm_dq, s>>>(A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+  bwd_dq_kernel<InT, GT><<<grid, kThreads, sm_dq, s>>>(A);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.N > 1) {
     const size_t rbytes = sizeof(float) * (size_t)a.B * a.H * a.N * a.dk * a.dv;
     if ((e = cudaMemsetAsync(a.U, 0, rbytes, s)) != cudaSuccess) return e;
     bwd_rstate_kernel<InT, GT><<<dim3((a.N + 1) / 2, a.H, a.B), kThreads, sm_r, s>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (dkv_tc) {
-    if ((e = dkv_tc()) != cudaSuccess) return e;
-  } else {
-    bwd_dkv_kernel<InT, GT><<<grid, kThreads, sm_dkv, s>>>(A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  const int64_t total = (int64_t)a.B * a.T * a.Hqk * a.dk;
-  const unsigned blocks = (unsigned)std::min<int64_t>((total + kThreads - 1) / kThreads, 152 * 16);
-  bwd_reduce_qk_kernel<GT><<<blocks, kThreads, 0, s>>>(A, total);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (a.log_a && A.dlog_a) {
-    bwd_dlog_a_kernel<<<(unsigned)((int64_t)a.B * a.H), kThreads, 0, s>>>(A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  bwd_dkv_kernel<InT, GT><<<grid, kThreads, sm_dkv, s>>>(A);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -745,22 +714,31 @@ size_t bwd_smem_max(int dk, int dv, int L) {
                           (size_t)kC * L);
 }
 
-cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype, cudaStream_t s,
-                                 bool dq_on_tc, const std::function<cudaError_t()>& dkv_tc) {
-  cudaError_t e;
-  if (dq_on_tc) {
-    const int64_t tiles = (int64_t)A.f.B * A.f.H * A.f.N;
-    bwd_tile_decay_kernel<<<(unsigned)((tiles + kThreads - 1) / kThreads), kThreads, 0, s>>>(A.f);
-    e = cudaGetLastError();
-  } else {
-    e = launch_simt_states(A.f, in_dtype, s);
-  }
+cudaError_t launch_bwd_finish(const BwdArgs& A, int grad_dtype, cudaStream_t s) {
+  const FwdArgs& a = A.f;
+  const int64_t total = (int64_t)a.B * a.T * a.Hqk * a.dk;
+  const unsigned blocks = (unsigned)std::min<int64_t>((total + kThreads - 1) / kThreads, 152 * 16);
+  if (grad_dtype == LL_F32)
+    bwd_reduce_qk_kernel<float><<<blocks, kThreads, 0, s>>>(A, total);
+  else
+    bwd_reduce_qk_kernel<__nv_bfloat16><<<blocks, kThreads, 0, s>>>(A, total);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (in_dtype == LL_F32 && grad_dtype == LL_F32)
-    return launch_typed<float, float>(A, s, dq_on_tc, dkv_tc);
-  if (in_dtype == LL_F32) return launch_typed<float, __nv_bfloat16>(A, s, dq_on_tc, dkv_tc);
-  if (grad_dtype == LL_F32) return launch_typed<__nv_bfloat16, float>(A, s, dq_on_tc, dkv_tc);
-  return launch_typed<__nv_bfloat16, __nv_bfloat16>(A, s, dq_on_tc, dkv_tc);
+  if (a.log_a && A.dlog_a) {
+    bwd_dlog_a_kernel<<<(unsigned)((int64_t)a.B * a.H), kThreads, 0, s>>>(A);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype, cudaStream_t s) {
+  cudaError_t e = launch_simt_states(A.f, in_dtype, s);
+  if (e != cudaSuccess) return e;
+  if (in_dtype == LL_F32 && grad_dtype == LL_F32) e = launch_typed<float, float>(A, s);
+  else if (in_dtype == LL_F32) e = launch_typed<float, __nv_bfloat16>(A, s);
+  else if (grad_dtype == LL_F32) e = launch_typed<__nv_bfloat16, float>(A, s);
+  else e = launch_typed<__nv_bfloat16, __nv_bfloat16>(A, s);
+  return e == cudaSuccess ? launch_bwd_finish(A, grad_dtype, s) : e;
 }
 
 }  // namespace ll

@@ -494,20 +494,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // Source s of tile i receives, from the queries t of its own tile,
 //   dK_s = sum_t P'[t, s] q_t,  dV_s = sum_t P[t, s] dO_t   (P = M ⊙ S, P' = M ⊙ S'),
 // i.e. dK = P'^T Q and dV = P^T dO with P and P' read MN-major as the A operand; and from
-// the later tiles, through the mirrored states (fp32, accumulated by the state kernel on
-// 32-token tiles; the 128-token block at c is its 32-token slot 4c), summed over the
-// tile's levels into R_tot = sum_m exp(E_m) R_{c_m} (E_m: log decay of the tiles strictly
+// the later tiles, through the mirrored states (fp32, accumulated by the kernel above),
+// summed over the tile's levels into R_tot = sum_m exp(E_m) R_{c_m} (E_m: log decay of the tiles strictly
 // between i and c_m):
 //   dK_s += g_s R_tot v_s,  dV_s += g_s R_tot^T k_s,  g_s = exp(lg_i - cs_s),
 // taken as MMAs with the rows of V and K scaled by g in place.  k_s . dK_s, which d log a
 // needs, is the column sum of G = M ⊙ S ⊙ S' (from the fp32 S and S') plus v_s . dV_inter.
 
 struct BkvParams {
-  int B, T, H, hg, L, N, N32;
+  int B, T, H, hg, L, N;
   const float* log_a;
   const float* lam;
   const float* lgu;          // [B*H][N] the tiles' log decays (forward workspace)
-  const float* R32;          // [B*H][N32][d_k][d_v] mirrored states, fp32
+  const float* R;            // [B*H][N][d_k][d_v] mirrored states, fp32
   const __nv_bfloat16* v;    // [B, T, H, d_v] (for v . dV)
   float* dkh;                // [B, T, H, 128] per-head dK
   float* dck;                // [B, T, H] k . dK, or null
@@ -775,7 +774,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     for (int l = 0; l < nl; ++l) {
       const float w = lv_w[l];
       const float4* src = reinterpret_cast<const float4*>(
-          p.R32 + (bh * p.N32 + 4 * (int64_t)lv_c[l]) * elems + (int64_t)r * DV + kHalf * hh);
+          p.R + (bh * p.N + (int64_t)lv_c[l]) * elems + (int64_t)r * DV + kHalf * hh);
 #pragma unroll
       for (int q = 0; q < kHalf / 4; ++q) {
         const float4 x = __ldcg(src + q);
@@ -882,6 +881,208 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ------------------------------------------------------------------ mirrored states
+//
+// Tile j adds, for every set bit m-1 of j, its part of the mirrored state of the block
+// starting at c = j with its low m-1 bits cleared (the block that the sources of tiles
+// [c - 2^(m-1), c) meet at level 7+m):
+//   R_c += sum_{t in j} w_t q_t dO_t^T,  w_t = exp(cs_t + D) lambda[t, 7+m],
+// D = log decay of the tiles [c, j).  Per level the rows of Q are scaled by w and split
+// into a bf16 high part and a bf16 residual (w q to about 16 bits; dO is exact in bf16),
+// and (w Q)^T dO = hi^T dO + lo^T dO (A and B MN-major) goes into one of two TMEM buffers;
+// the previous level's product is added to R_c (fp32, float4 atomics) meanwhile.  The
+// states feed k . dK, and with it d log a, a sum whose terms cancel, which is why w q is
+// not rounded to bf16 alone.
+
+struct BrParams {
+  int B, T, H, hg, L, N;
+  const float* log_a;
+  const float* lam;
+  const float* lgu;   // [B*H][N] the tiles' log decays (forward workspace)
+  float* R;           // [B*H][N][d_k][d_v] mirrored states (zeroed before)
+};
+
+struct RsSmem {
+  static constexpr int kQ = 0, kG = kOperand, kW = 2 * kOperand;  // W: [2 levels][hi, lo]
+  static constexpr int kBars = 6 * kOperand;  // load, r[2]
+  static constexpr int kTslot = kBars + 4 * 8;
+  static constexpr int kRed = kTslot + 16;
+  static constexpr int kCs = kRed + 32;                        // 128 floats
+  static constexpr int kD = kCs + 4 * kTile;                   // kMaxChunkLevels floats
+  static constexpr int kLamX = kD + 4 * kMaxChunkLevels;       // [levels][128] floats
+};
+
+size_t smem_bwd_rstate(int levels) { return (size_t)RsSmem::kLamX + 4 * (size_t)kTile * levels + 1024; }
+
+template <int DV>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    tc_bwd_rstate_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmG, BrParams p) {
+  constexpr int kPanels = DV / 64;
+  constexpr int kVBytes = kTile * DV * 2;
+  constexpr int kHalf = DV / 2;
+  const int BH = p.B * p.H;
+  const int j = blockIdx.x / BH, bhi = blockIdx.x - j * BH;
+  const int nlev = __popc((unsigned)j);
+  if (nlev == 0) return;  // tile 0 of each (b, h) belongs to no mirrored block
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* Qb = smem + RsSmem::kQ;
+  uint8_t* Gb = smem + RsSmem::kG;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RsSmem::kBars);
+  uint64_t* bar_load = &bars[0];
+  uint64_t* bar_r = &bars[1];  // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + RsSmem::kTslot);
+  float* red = reinterpret_cast<float*>(smem + RsSmem::kRed);
+  float* cs_s = reinterpret_cast<float*>(smem + RsSmem::kCs);
+  float* D_s = reinterpret_cast<float*>(smem + RsSmem::kD);
+  float* lamx = reinterpret_cast<float*>(smem + RsSmem::kLamX);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = warp & 3, hh = warp >> 2;
+  const int r = tid & (kTile - 1);
+  const int b = bhi / p.H, h = bhi - b * p.H, hq = h / p.hg;
+  const int64_t bh = bhi;
+  const int t0 = j * kTile;
+  const int n = min(kTile, p.T - t0);
+  const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;
+  const bool row_live = r < n;
+
+  if (warp == 1) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+  if (tid == 64) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmG);
+    for (int q = 0; q < 3; ++q) mbar_init(&bars[q], 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {  // D of every level: log decay of the tiles [c, j)
+    int k = 0;
+    for (int m = 1; m < kMaxChunkLevels && k < nlev; ++m) {
+      if (!((j >> (m - 1)) & 1)) continue;
+      const int64_t c = ((int64_t)j >> (m - 1)) << (m - 1);
+      float x = 0.f;
+      for (int64_t i = c + lane; i < j; i += 32) x += p.lgu[bh * p.N + i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (lane == 0) D_s[k] = x;
+      ++k;
+    }
+  }
+  {
+    int k = 0;
+    for (int m = 1; m < kMaxChunkLevels && k < nlev; ++m) {
+      if (!((j >> (m - 1)) & 1)) continue;
+      if ((k & 1) == hh) lamx[k * kTile + r] = row_live ? p.lam[row * p.L + kTileLc + m] : 0.f;
+      ++k;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
+  bool landed = true;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_load, kOperand + kVBytes);
+    tma_load_4d(&tmQ, bar_load, Qb, 0, hq, t0, b);
+    tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, hq, t0, b);
+#pragma unroll
+    for (int pv = 0; pv < kPanels; ++pv)
+      tma_load_4d(&tmG, bar_load, Gb + pv * kPanel, 64 * pv, h, t0, b);
+  }
+  __syncwarp();
+  const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
+  const float cs_scan = block_scan256(la, red);
+  if (hh == 0) cs_s[r] = cs_scan;
+  if (tid == 0) landed = mbar_wait(bar_load, 0);
+  bool all_ok = __syncthreads_and(landed);
+  tc_fence_after();
+  const float cs = cs_s[r];
+
+  uint32_t ph[2] = {0, 0};
+  int c_prev = 0;  // block start of the level being drained
+  for (int k = 0; k <= nlev && all_ok; ++k) {
+    int c_k = 0;
+    if (k < nlev) {
+      int m = 0;
+      for (int seen = -1; seen < k;) {
+        ++m;
+        if ((j >> (m - 1)) & 1) ++seen;
+      }
+      c_k = (j >> (m - 1)) << (m - 1);
+      // rows of Q scaled by w_t, high part and residual, into buffer pair k & 1 (its
+      // previous MMA was drained before)
+      uint8_t* Wh = smem + RsSmem::kW + (k & 1) * 2 * kOperand;
+      uint8_t* Wl = Wh + kOperand;
+      const float w = row_live ? __expf(cs + D_s[k]) * lamx[k * kTile + r] : 0.f;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const int off = hh * kPanel + sw128_offset(r, g);
+        const uint4 u = *reinterpret_cast<const uint4*>(Qb + off);
+        uint32_t x4[4] = {u.x, u.y, u.z, u.w}, y4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x4[e]));
+          const float a0 = f.x * w, a1 = f.y * w;
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(a0, a1);
+          const float2 hf = __bfloat1622float2(hi);
+          x4[e] = *reinterpret_cast<const uint32_t*>(&hi);
+          y4[e] = pack_bf16(a0 - hf.x, a1 - hf.y);
+        }
+        *reinterpret_cast<uint4*>(Wh + off) = make_uint4(x4[0], x4[1], x4[2], x4[3]);
+        *reinterpret_cast<uint4*>(Wl + off) = make_uint4(y4[0], y4[1], y4[2], y4[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t idesc = idesc_bf16(128, DV, 1, 1);
+        const uint32_t wh = smem_u32(Wh), wl = smem_u32(Wl), ga = smem_u32(Gb);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16(tmem + (k & 1) * 128, smem_desc_sw128(wh + kk * 2048, kPanel, 1024),
+                   smem_desc_sw128(ga + kk * 2048, kPanel, 1024), idesc, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16(tmem + (k & 1) * 128, smem_desc_sw128(wl + kk * 2048, kPanel, 1024),
+                   smem_desc_sw128(ga + kk * 2048, kPanel, 1024), idesc, 1);
+        mma_commit(&bar_r[k & 1]);
+      }
+      __syncwarp();
+    }
+    if (k >= 1) {  // level k-1: row d = r of its d_k x d_v part, this thread's half of d_v
+      const int bf = (k - 1) & 1;
+      const bool got = __syncthreads_and(mbar_wait(&bar_r[bf], ph[bf]));
+      ph[bf] ^= 1;
+      if (!got) {
+        all_ok = false;
+        break;
+      }
+      tc_fence_after();
+      float* dst = p.R + ((bh * p.N + c_prev) * kD + r) * DV + kHalf * hh;
+#pragma unroll
+      for (int c = 0; c < kPanels; ++c) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + bf * 128 + kHalf * hh + 32 * c, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * q),
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+      }
+      tc_fence_before();
+    }
+    c_prev = c_k;
+  }
+  if (!all_ok && tid == 0) atomicOr(&g_tcb_error, 1u);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
 }  // namespace
 
 bool tc_bwd_dq_supported(int64_t dk, int64_t dv, int in_dtype, int grad_dtype) {
@@ -929,8 +1130,8 @@ cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, flo
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R32, int N32,
-                              float* dkh, float* dck, void* dv, cudaStream_t s) {
+cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R, float* dkh,
+                              float* dck, void* dv, cudaStream_t s) {
   if (f.dk != kD || (f.dv != 64 && f.dv != 128) || f.C != kTile) return cudaErrorInvalidValue;
   const int dvw = f.dv;
   CUtensorMap tmQ, tmK, tmV, tmG;
@@ -940,8 +1141,8 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
       !make_tokens_map(&tmG, dout, f.B, f.T, f.H, dvw))
     return cudaErrorInvalidValue;
   BkvParams p;
-  p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N; p.N32 = N32;
-  p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.R32 = R32;
+  p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
+  p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.R = R;
   p.v = static_cast<const __nv_bfloat16*>(f.v);
   p.dkh = dkh; p.dck = dck; p.dv = static_cast<__nv_bfloat16*>(dv);
   static std::once_flag attr_once;
@@ -961,6 +1162,39 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
     tc_bwd_dkv_kernel<128><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, p);
   else
     tc_bwd_dkv_kernel<64><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_bwd_rstate(const FwdArgs& f, const void* dout, float* R, cudaStream_t s) {
+  if (f.dk != kD || (f.dv != 64 && f.dv != 128) || f.C != kTile) return cudaErrorInvalidValue;
+  CUtensorMap tmQ, tmG;
+  if (!make_tokens_map(&tmQ, f.q, f.B, f.T, f.Hqk, kD) ||
+      !make_tokens_map(&tmG, dout, f.B, f.T, f.H, f.dv))
+    return cudaErrorInvalidValue;
+  BrParams p;
+  p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
+  p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.R = R;
+  int levels = 0;
+  while ((int64_t(1) << levels) < f.N) ++levels;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(tc_bwd_rstate_kernel<128>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem_bwd_rstate(kMaxChunkLevels - 1));
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(tc_bwd_rstate_kernel<64>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem_bwd_rstate(kMaxChunkLevels - 1));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  cudaError_t e = cudaMemsetAsync(R, 0, sizeof(float) * (size_t)f.B * f.H * f.N * kD * f.dv, s);
+  if (e != cudaSuccess) return e;
+  const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
+  if (f.dv == 128)
+    tc_bwd_rstate_kernel<128><<<tiles, kThreadsB, smem_bwd_rstate(levels), s>>>(tmQ, tmG, p);
+  else
+    tc_bwd_rstate_kernel<64><<<tiles, kThreadsB, smem_bwd_rstate(levels), s>>>(tmQ, tmG, p);
   return cudaGetLastError();
 }
 

@@ -5,8 +5,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <functional>
-
 #include "loglinear.h"
 
 namespace ll {
@@ -134,21 +132,23 @@ struct BwdWorkspace {
 // N: 32-token tiles; n_tc: 128-token tiles of the tensor-core dQ, or 0 without it.
 BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, int64_t dk,
                                   int64_t dv, int64_t n_tc);
-// dq_on_tc: dQ, dlambda and q . dQ come from the tensor cores; the CUDA-core part then
-// computes only the tile log decays and the mirrored states before dK, dV.  dkv_tc, if
-// set, launches dK, dV and k . dK (after the mirrored states, before the reductions) in
-// place of the CUDA-core kernel.
-cudaError_t launch_simt_backward(const BwdArgs& a, int in_dtype, int grad_dtype, cudaStream_t s,
-                                 bool dq_on_tc, const std::function<cudaError_t()>& dkv_tc);
-// Tensor-core dQ and dlambda from a completed tensor-core forward's workspace (f: that
-// forward's arguments, 128-token tiles): per-head dQ, q . dQ (dcq may be null), dlambda.
+// The whole backward on CUDA cores (fp32, 32-token tiles).
+cudaError_t launch_simt_backward(const BwdArgs& a, int in_dtype, int grad_dtype, cudaStream_t s);
+// Tensor-core backward (bf16, d_k = 128, d_v in {64, 128}) on the 128-token tiles of a
+// completed tensor-core forward over the same inputs (f: that forward's arguments and
+// workspace).  dQ and dlambda from its block states: per-head dQ, q . dQ (dcq may be
+// null), dlambda.
 bool tc_bwd_dq_supported(int64_t dk, int64_t dv, int in_dtype, int grad_dtype);
 cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, float* dcq,
                              float* dlam, cudaStream_t s);
-// Tensor-core dK, dV and k . dK (f as above; R32: the mirrored states on N32 32-token
-// tiles).  dv in bf16.
-cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R32, int N32,
-                              float* dkh, float* dck, void* dv, cudaStream_t s);
+// Tensor-core mirrored states on the forward's 128-token tiles into R ([B*H][N][d_k][d_v]
+// fp32, zeroed here), then dK, dV and k . dK from them (f as above).  dv in bf16.
+cudaError_t launch_tc_bwd_rstate(const FwdArgs& f, const void* dout, float* R, cudaStream_t s);
+cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R, float* dkh,
+                              float* dck, void* dv, cudaStream_t s);
+// The group sums of dq and dk with their cast, and d log a (the last two kernels of every
+// backward path).
+cudaError_t launch_bwd_finish(const BwdArgs& a, int grad_dtype, cudaStream_t s);
 cudaError_t tcb_take_error(cudaStream_t s, unsigned* flags);
 size_t bwd_smem_max(int dk, int dv, int L);  // largest dynamic shared memory of a kernel
 // The decode state at position T-1 from a completed forward's workspace (tc_layout: the

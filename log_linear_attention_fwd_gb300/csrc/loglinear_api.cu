@@ -368,16 +368,16 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
     f.rdy_u = reinterpret_cast<uint32_t*>(fw + w.fwd.off_rdy_u);
     f.rdy_n = reinterpret_cast<uint32_t*>(fw + w.fwd.off_rdy_n);
     f.tick = reinterpret_cast<uint32_t*>(fw + w.fwd.off_tick);
+    // the mirrored states on the same 128-token tiles go into U's buffer (fp32)
+    float* R = reinterpret_cast<float*>(a.U);
     e = launch_tc_forward(f, LL_BF16, s, nullptr);
     if (e == cudaSuccess) e = launch_tc_bwd_dq(f, dout, A.dqh, A.dcq, dlambda, s);
-    if (e == cudaSuccess)
-      e = launch_simt_backward(A, in_dtype, grad_dtype, s, true, [&]() {
-        return launch_tc_bwd_dkv(f, dout, reinterpret_cast<const float*>(a.U), a.N, A.dkh,
-                                 A.dck, dv_out, s);
-      });
+    if (e == cudaSuccess && f.N > 1) e = launch_tc_bwd_rstate(f, dout, R, s);
+    if (e == cudaSuccess) e = launch_tc_bwd_dkv(f, dout, R, A.dkh, A.dck, dv_out, s);
+    if (e == cudaSuccess) e = launch_bwd_finish(A, grad_dtype, s);
     return e == cudaSuccess ? LL_OK : cuda_fail(e);
   }
-  e = launch_simt_backward(A, in_dtype, grad_dtype, s, false, nullptr);
+  e = launch_simt_backward(A, in_dtype, grad_dtype, s);
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 
