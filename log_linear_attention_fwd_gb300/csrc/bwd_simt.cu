@@ -598,56 +598,132 @@ __global__ void __launch_bounds__(kThreads) bwd_dkv_kernel(BwdArgs A) {
 
 // ---------------------------------------------------------------- group sums, d log a
 
-template <typename GT>
-__global__ void __launch_bounds__(kThreads) bwd_reduce_qk_kernel(BwdArgs A, int64_t total) {
+// dq[b, t, g, :] = sum over the heads of group g of dq_h (same for dk), cast to the gradient
+// type.  Block (x: position b*T+t, y: a slice of kThreads*4 of the row's Hqk*d_k values);
+// 4 consecutive values per thread when d_k is a multiple of 4.
+template <typename GT, bool kVec4>
+__global__ void __launch_bounds__(kThreads) bwd_reduce_qk_kernel(BwdArgs A) {
   const FwdArgs& a = A.f;
-  const int dk = a.dk, hg = a.hg;
-  GT* dq = reinterpret_cast<GT*>(A.dq);
-  GT* dk_out = reinterpret_cast<GT*>(A.dk);
-  for (int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * kThreads) {
-    const int64_t d = idx % dk, bt_g = idx / dk;  // (b, t, q/k head g)
-    const int64_t g = bt_g % a.Hqk, bt = bt_g / a.Hqk;
-    const int64_t src = (bt * a.H + g * hg) * dk + d;
-    float x = 0.f, y = 0.f;
+  const int dk = a.dk, hg = a.hg, rowlen = a.Hqk * dk;
+  const int64_t bt = blockIdx.x;
+  const int i0 = (blockIdx.y * kThreads + threadIdx.x) * 4;
+  if (i0 >= rowlen) return;
+  GT* dq = reinterpret_cast<GT*>(A.dq) + bt * rowlen;
+  GT* dko = reinterpret_cast<GT*>(A.dk) + bt * rowlen;
+  const float* sq = A.dqh + bt * a.H * dk;
+  const float* sk = A.dkh + bt * a.H * dk;
+  if (kVec4) {  // the 4 values share their head group (d_k % 4 == 0)
+    const int g = i0 / dk, d = i0 - g * dk;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
     for (int r = 0; r < hg; ++r) {
-      x += A.dqh[src + (int64_t)r * dk];
-      y += A.dkh[src + (int64_t)r * dk];
+      const int off = (g * hg + r) * dk + d;
+      const float4 u = *reinterpret_cast<const float4*>(sq + off);
+      const float4 v = *reinterpret_cast<const float4*>(sk + off);
+      x.x += u.x; x.y += u.y; x.z += u.z; x.w += u.w;
+      y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
     }
-    dq[idx] = from_f32<GT>(x);
-    dk_out[idx] = from_f32<GT>(y);
+    dq[i0] = from_f32<GT>(x.x); dq[i0 + 1] = from_f32<GT>(x.y);
+    dq[i0 + 2] = from_f32<GT>(x.z); dq[i0 + 3] = from_f32<GT>(x.w);
+    dko[i0] = from_f32<GT>(y.x); dko[i0 + 1] = from_f32<GT>(y.y);
+    dko[i0 + 2] = from_f32<GT>(y.z); dko[i0 + 3] = from_f32<GT>(y.w);
+  } else {
+    for (int i = i0; i < i0 + 4 && i < rowlen; ++i) {
+      const int g = i / dk, d = i - g * dk;
+      float x = 0.f, y = 0.f;
+      for (int r = 0; r < hg; ++r) {
+        x += sq[(g * hg + r) * dk + d];
+        y += sk[(g * hg + r) * dk + d];
+      }
+      dq[i] = from_f32<GT>(x);
+      dko[i] = from_f32<GT>(y);
+    }
   }
 }
 
-// dlog_a_i = sum over t >= i of (q_t . dQ_t - k_t . dK_t), one CTA per (b, h), walking
-// tiles of kThreads positions from the end.
-__global__ void __launch_bounds__(kThreads) bwd_dlog_a_kernel(BwdArgs A) {
-  __shared__ float red[kThreads / 32];
-  __shared__ float carry_s;
-  const FwdArgs& a = A.f;
-  const int64_t bh = blockIdx.x;
-  const int64_t b = bh / a.H, h = bh - b * a.H;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float carry = 0.f;
-  for (int base = a.T - 1; base >= 0; base -= kThreads) {
-    const int i = base - (int)threadIdx.x;
-    const int64_t at = (b * a.T + i) * a.H + h;
-    float x = i >= 0 ? A.dcq[at] - A.dck[at] : 0.f;
+// dlog_a_i = sum over t >= i of (q_t . dQ_t - k_t . dK_t), in two passes over chunks of
+// kScanChunk positions of each (b, h): the chunks' sums, then each chunk's suffix scan
+// plus the sum of the chunks after it.
+constexpr int kScanChunk = 1024;
+constexpr int kScanPer = kScanChunk / kThreads;  // positions per thread (4)
+
+__device__ __forceinline__ float block_sum_all(float x, float* red) {
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < kThreads / 32; ++w) t += red[w];
+  return t;
+}
+
+__global__ void __launch_bounds__(kThreads) bwd_dlog_a_sums_kernel(BwdArgs A, float* sums, int nch) {
+  __shared__ float red[kThreads / 32];
+  const FwdArgs& a = A.f;
+  const int64_t bh = blockIdx.y;
+  const int64_t b = bh / a.H, h = bh - b * a.H;
+  const int c = blockIdx.x;
+  float x = 0.f;
+#pragma unroll
+  for (int k = 0; k < kScanPer; ++k) {
+    const int i = c * kScanChunk + k * kThreads + threadIdx.x;
+    if (i < a.T) {
+      const int64_t at = (b * a.T + i) * a.H + h;
+      x += A.dcq[at] - A.dck[at];
     }
-    if (lane == 31) red[warp] = x;
-    __syncthreads();
-    float pre = 0.f;
-    for (int w = 0; w < warp; ++w) pre += red[w];
-    x += pre + carry;
-    if (i >= 0) A.dlog_a[at] = x;
-    if (threadIdx.x == kThreads - 1) carry_s = x;
-    __syncthreads();
-    carry = carry_s;
-    __syncthreads();
+  }
+  x = block_sum_all(x, red);
+  if (threadIdx.x == 0) sums[bh * nch + c] = x;
+}
+
+__global__ void __launch_bounds__(kThreads) bwd_dlog_a_scan_kernel(BwdArgs A, const float* sums,
+                                                                   int nch) {
+  __shared__ float red[kThreads / 32];
+  __shared__ float after_s;
+  const FwdArgs& a = A.f;
+  const int64_t bh = blockIdx.y;
+  const int64_t b = bh / a.H, h = bh - b * a.H;
+  const int c = blockIdx.x;
+  if (threadIdx.x < 32) {  // the sum of the chunks after c
+    float x = 0.f;
+    for (int k = c + 1 + (int)threadIdx.x; k < nch; k += 32) x += sums[bh * nch + k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (threadIdx.x == 0) after_s = x;
+  }
+  // thread tid owns positions i = base + tid*kScanPer + k, base the chunk's first position;
+  // the suffix sum inside the chunk = (own suffix) + (sum of the later threads' values)
+  const int base = c * kScanChunk + threadIdx.x * kScanPer;
+  float v[kScanPer];
+  float own = 0.f;
+#pragma unroll
+  for (int k = 0; k < kScanPer; ++k) {
+    const int i = base + k;
+    float x = 0.f;
+    if (i < a.T) {
+      const int64_t at = (b * a.T + i) * a.H + h;
+      x = A.dcq[at] - A.dck[at];
+    }
+    v[k] = x;
+    own += x;
+  }
+  // exclusive suffix over threads: inclusive prefix over the reversed thread order
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  if (lane == 0) red[warp] = incl;  // the warp's total
+  __syncthreads();
+  float later_warps = 0.f;
+  for (int w = warp + 1; w < kThreads / 32; ++w) later_warps += red[w];
+  float run = (incl - own) + later_warps + after_s;  // everything after this thread's values
+#pragma unroll
+  for (int k = kScanPer - 1; k >= 0; --k) {
+    run += v[k];
+    const int i = base + k;
+    if (i < a.T) A.dlog_a[(b * a.T + i) * a.H + h] = run;
   }
 }
 
@@ -697,9 +773,10 @@ BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, in
   w.off_dkh = up(w.off_dqh + rows * dk * sizeof(float));
   w.off_dcq = up(w.off_dkh + rows * dk * sizeof(float));
   w.off_dck = up(w.off_dcq + rows * sizeof(float));
+  w.off_scan = up(w.off_dck + rows * sizeof(float));
   w.off_fwd = w.off_out = 0;
   w.fwd = FwdWorkspace{};
-  w.total = up(w.off_dck + rows * sizeof(float));
+  w.total = up(w.off_scan + (size_t)(B * H) * (size_t)((T + 1023) / 1024 + 1) * sizeof(float));
   if (n_tc > 0) {
     w.fwd = fwd_workspace_layout(B, H, n_tc, dk, dv, 2);
     w.off_fwd = w.total;
@@ -716,16 +793,24 @@ size_t bwd_smem_max(int dk, int dv, int L) {
 
 cudaError_t launch_bwd_finish(const BwdArgs& A, int grad_dtype, cudaStream_t s) {
   const FwdArgs& a = A.f;
-  const int64_t total = (int64_t)a.B * a.T * a.Hqk * a.dk;
-  const unsigned blocks = (unsigned)std::min<int64_t>((total + kThreads - 1) / kThreads, 152 * 16);
-  if (grad_dtype == LL_F32)
-    bwd_reduce_qk_kernel<float><<<blocks, kThreads, 0, s>>>(A, total);
-  else
-    bwd_reduce_qk_kernel<__nv_bfloat16><<<blocks, kThreads, 0, s>>>(A, total);
+  const int rowlen = a.Hqk * a.dk;
+  const dim3 grid_r((unsigned)((int64_t)a.B * a.T), (unsigned)((rowlen + 4 * kThreads - 1) / (4 * kThreads)));
+  const bool vec = a.dk % 4 == 0;
+  if (grad_dtype == LL_F32) {
+    if (vec) bwd_reduce_qk_kernel<float, true><<<grid_r, kThreads, 0, s>>>(A);
+    else bwd_reduce_qk_kernel<float, false><<<grid_r, kThreads, 0, s>>>(A);
+  } else {
+    if (vec) bwd_reduce_qk_kernel<__nv_bfloat16, true><<<grid_r, kThreads, 0, s>>>(A);
+    else bwd_reduce_qk_kernel<__nv_bfloat16, false><<<grid_r, kThreads, 0, s>>>(A);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.log_a && A.dlog_a) {
-    bwd_dlog_a_kernel<<<(unsigned)((int64_t)a.B * a.H), kThreads, 0, s>>>(A);
+    const int nch = (a.T + kScanChunk - 1) / kScanChunk;
+    const dim3 grid_s((unsigned)nch, (unsigned)((int64_t)a.B * a.H));
+    bwd_dlog_a_sums_kernel<<<grid_s, kThreads, 0, s>>>(A, A.scan, nch);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_dlog_a_scan_kernel<<<grid_s, kThreads, 0, s>>>(A, A.scan, nch);
     e = cudaGetLastError();
   }
   return e;

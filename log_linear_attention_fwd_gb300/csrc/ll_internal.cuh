@@ -122,9 +122,10 @@ struct BwdArgs {
   float* dkh;           // [B, T, H, dk] per-head dk (workspace)
   float* dcq;           // [B, T, H] q_t . dq_t per head (workspace)
   float* dck;           // [B, T, H] k_t . dk_t per head (workspace)
+  float* scan;          // [B*H][ceil(T/1024)] chunk sums of the d log a scan (workspace)
 };
 struct BwdWorkspace {
-  size_t off_U, off_nodes, off_lg, off_dqh, off_dkh, off_dcq, off_dck;
+  size_t off_U, off_nodes, off_lg, off_dqh, off_dkh, off_dcq, off_dck, off_scan;
   size_t off_fwd, off_out;  // tensor-core dQ only: a forward's workspace and its output
   FwdWorkspace fwd;         // that forward workspace's own layout (offsets from off_fwd)
   size_t total;

@@ -350,6 +350,7 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
   A.dkh = reinterpret_cast<float*>(ws + w.off_dkh);
   A.dcq = log_a ? reinterpret_cast<float*>(ws + w.off_dcq) : nullptr;
   A.dck = log_a ? reinterpret_cast<float*>(ws + w.off_dck) : nullptr;
+  A.scan = reinterpret_cast<float*>(ws + w.off_scan);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (n_tc > 0) {
