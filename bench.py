@@ -442,16 +442,33 @@ def _median_us(fn, flush, reps):
     return statistics.median(ts)
 
 
-def _bwd_report(cfg, t, peaks):
+def _bwd_report(cfg, t, peaks, path):
+    """The backward's time and roofline.  The tensor-core path is bound by HBM or the bf16
+    tensor peak, whichever takes longer for its algorithmic bytes and FLOPs; the CUDA-core
+    path by the FP32 FMA peak."""
     bbytes, bflops = bwd_algorithmic(cfg)
-    return {"bwd_us": t * 1e6, "tokens_per_s": cfg.B * cfg.T / t,
-            "roofline": {"bound": "alu", "achieved": bflops / t / 1e12,
-                         "peak": fp32_alu_peak(), "unit": "TFLOP/s",
-                         "frac": bflops / t / 1e12 / fp32_alu_peak(),
-                         "algorithmic_flops": bflops,
-                         "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
-                         "hbm_frac": bbytes / t / 1e9 / peaks["hbm"],
-                         "algorithmic_bytes": bbytes}}
+    if path == "tc":
+        t_hbm = bbytes / (peaks["hbm"] * 1e9)
+        t_tc = bflops / (peaks["bf16"] * 1e12)
+        if t_hbm >= t_tc:
+            roof = {"bound": "hbm", "achieved": bbytes / t / 1e9, "peak": peaks["hbm"],
+                    "unit": "GB/s", "frac": bbytes / t / 1e9 / peaks["hbm"]}
+        else:
+            roof = {"bound": "tensor", "achieved": bflops / t / 1e12, "peak": peaks["bf16"],
+                    "unit": "TFLOP/s", "frac": bflops / t / 1e12 / peaks["bf16"]}
+        roof.update({"tensor_frac": bflops / t / 1e12 / peaks["bf16"],
+                     "peak_source": peaks["src"]})
+    else:
+        roof = {"bound": "alu", "achieved": bflops / t / 1e12, "peak": fp32_alu_peak(),
+                "unit": "TFLOP/s", "frac": bflops / t / 1e12 / fp32_alu_peak(),
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
+                "hbm_frac": bbytes / t / 1e9 / peaks["hbm"]}
+    roof.update({"algorithmic_flops": bflops, "algorithmic_bytes": bbytes})
+    return {"bwd_us": t * 1e6, "tokens_per_s": cfg.B * cfg.T / t, "path": path, "roofline": roof}
+
+
+def _bwd_path(LL, cfg):
+    return "tc" if (cfg.dtype == "bf16" and cfg.dk == 128 and cfg.dv in (64, 128)) else "simt"
 
 
 def measure_backward(LL, cfg, d, dev, flush, peaks, reps=5):
@@ -463,8 +480,8 @@ def measure_backward(LL, cfg, d, dev, flush, peaks, reps=5):
                                            cfg.L, 1, 1), device=dev, dtype=torch.uint8)
     t = _median_us(lambda: LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout,
                                             workspace=ws), flush, reps)
-    rep = _bwd_report(cfg, t, peaks)
-    rep["workload"] = f"{cfg.name}: loglinear_bwd, bf16 inputs and gradients, fp32 compute"
+    rep = _bwd_report(cfg, t, peaks, _bwd_path(LL, cfg))
+    rep["workload"] = f"{cfg.name}: loglinear_bwd, bf16 inputs and gradients"
     return rep
 
 
@@ -499,7 +516,7 @@ def measure_benchmark_shape(LL, cfg, dev, flush, peaks, reps=10):
                                             cfg.L, 1, 1), device=dev, dtype=torch.uint8)
     tb = _median_us(lambda: LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout,
                                              workspace=bws), flush, 3)
-    bwd = _bwd_report(cfg, tb, peaks)
+    bwd = _bwd_report(cfg, tb, peaks, _bwd_path(LL, cfg))
     return {"workload": f"{cfg.name}: loglinear_fwd B{cfg.B} H{cfg.H} (q/k heads "
                         f"{cfg.qk_heads}) T{cfg.T} dk={cfg.dk} dv={cfg.dv} C{cfg.C} L{cfg.L} bf16",
             "path": LL.resolve_path(cfg.dk, cfg.dv, cfg.C, 1), "fwd_us": t * 1e6,
