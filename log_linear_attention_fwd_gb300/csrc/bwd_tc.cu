@@ -550,6 +550,22 @@ __device__ __forceinline__ void scale_row_chunks(uint8_t* buf, int r, int g0, in
   }
 }
 
+// Column sums of a 32 x 32 block held one row per lane: a transpose-reduce butterfly
+// (31 shuffles); on return a[0] of lane k is the sum of column k over the warp's rows.
+__device__ __forceinline__ void warp_column_sums(float (&a)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? a[i] : a[i + o];
+      const float keep = up ? a[i + o] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+}
+
 template <int DV>
 __global__ void __launch_bounds__(kThreadsB, 1)
     tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -632,6 +648,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const uint32_t tmem = *tslot;
   const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
   const int nl = *lv_n;
+  const int64_t elems = (int64_t)kD * DV;
+  if (tid >= 32 && tid < 32 + nl)  // warm L2 with the mirrored states summed below
+    prefetch_l2_bulk(p.R + (bh * p.N + lv_c[tid - 32]) * elems, (uint32_t)(elems * 4));
   bool landed = true;
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_load, 2 * kOperand + 2 * kVBytes);
@@ -706,20 +725,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       if (c < qt) {
         const int lvl = 5 + (32 - __clz((unsigned)(qt ^ c)));
         const float wl = lam_r[lvl] * __expf(cs - cs_s[c * 32 + 31]);
+        float g[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const float m = wl * fcol[c * 32 + k];
-          const float g = m * sa[k] * sp[k];
+          g[k] = m * sa[k] * sp[k];
           sa[k] *= m;
           sp[k] *= m;
-          float x = g;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-          if (lane == 0) atomicAdd(&colsum[c * 32 + k], x);
         }
+        warp_column_sums(g);
+        atomicAdd(&colsum[c * 32 + lane], g[0]);
       } else {
         const bool fact = cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f;
         const float gt = __expf(cs - cs_s[c * 32 + 31]);
+        float g[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int s = c * 32 + k;
@@ -727,13 +746,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           if (s <= r && row_live)
             m = lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] *
                 (fact ? gt * fcol[s] : __expf(cs - cs_s[s]));
-          float x = m * sa[k] * sp[k];
+          g[k] = m * sa[k] * sp[k];
           sa[k] *= m;
           sp[k] *= m;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-          if (lane == 0) atomicAdd(&colsum[s], x);
         }
+        warp_column_sums(g);
+        atomicAdd(&colsum[c * 32 + lane], g[0]);
       }
       put_row32_bf16(P0, r, c, sa);
       put_row32_bf16(P1, r, c, sp);
@@ -764,24 +782,28 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     mma_commit(bar_kv);
   }
   __syncwarp();
-  // ---- R_tot row r (d_k), this thread's half of d_v, summed over the levels while the
-  // MMAs run (fp32 loads), then written in bf16 over P' once dK's MMA is done with it
-  float rt[kHalf];
+  // ---- R_tot summed over the levels while the MMAs run (fp32 loads, a warp reads whole
+  // rows: lane owns 4 consecutive columns, warp w rows w, w+8, ...), then written in bf16
+  // over P' once dK's MMA is done with it
+  constexpr int kLanesPerRow = DV / 4;             // 32 or 16
+  constexpr int kRowsPerIter = 32 / kLanesPerRow;  // 1 or 2
+  constexpr int kIters = kTile / 8 / kRowsPerIter; // 16 or 8
+  const int lrow = lane / kLanesPerRow, col = 4 * (lane % kLanesPerRow);
+  float4 rt[kIters];
 #pragma unroll
-  for (int q = 0; q < kHalf; ++q) rt[q] = 0.f;
+  for (int it = 0; it < kIters; ++it) rt[it] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (all_ok) {
-    const int64_t elems = (int64_t)kD * DV;
     for (int l = 0; l < nl; ++l) {
       const float w = lv_w[l];
-      const float4* src = reinterpret_cast<const float4*>(
-          p.R + (bh * p.N + (int64_t)lv_c[l]) * elems + (int64_t)r * DV + kHalf * hh);
+      const float* src = p.R + (bh * p.N + (int64_t)lv_c[l]) * elems + col;
 #pragma unroll
-      for (int q = 0; q < kHalf / 4; ++q) {
-        const float4 x = __ldcg(src + q);
-        rt[4 * q] = fmaf(w, x.x, rt[4 * q]);
-        rt[4 * q + 1] = fmaf(w, x.y, rt[4 * q + 1]);
-        rt[4 * q + 2] = fmaf(w, x.z, rt[4 * q + 2]);
-        rt[4 * q + 3] = fmaf(w, x.w, rt[4 * q + 3]);
+      for (int it = 0; it < kIters; ++it) {
+        const int d = (it * kRowsPerIter + lrow) * 8 + warp;
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)d * DV));
+        rt[it].x = fmaf(w, x.x, rt[it].x);
+        rt[it].y = fmaf(w, x.y, rt[it].y);
+        rt[it].z = fmaf(w, x.z, rt[it].z);
+        rt[it].w = fmaf(w, x.w, rt[it].w);
       }
     }
   }
@@ -790,7 +812,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   all_ok = __syncthreads_and(ok);
   if (all_ok && nl > 0) {
 #pragma unroll
-    for (int c = 0; c < kPanels; ++c) put_row32_bf16(P1, r, kPanels * hh + c, rt + 32 * c);
+    for (int it = 0; it < kIters; ++it) {
+      const int d = (it * kRowsPerIter + lrow) * 8 + warp;
+      uint8_t* dst = P1 + (col >> 6) * kPanel + sw128_offset(d, (col & 63) >> 3) + (col & 7) * 2;
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16(rt[it].x, rt[it].y), pack_bf16(rt[it].z, rt[it].w));
+    }
   }
   tc_fence_after();
   fence_proxy_async_smem();
