@@ -191,7 +191,7 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
  * argument: the gradients do not depend on it.  1 <= dk, dv <= 128, L <= 64.  All
  * outputs are fully overwritten.
  * path: LL_PATH_TC computes dq, dk, dv and dlambda on the tensor cores (bf16 inputs and
- *   gradients, dk = 128, dv in {64, 128}; q, k, v, dout 16-byte aligned): a tensor-core
+ *   gradients, dk = 128, dv in {64, 128}; q, k, v, dout, dq, dk, dv 16-byte aligned): a tensor-core
  *   forward over the same inputs publishes its block states into the workspace, then
  *   128-token tiles take dQ and dlambda from them with tcgen05; the mirrored states of
  *   later tiles that dk and dv read are accumulated in fp32 on CUDA cores, then dK and dV

@@ -791,20 +791,23 @@ size_t bwd_smem_max(int dk, int dv, int L) {
                           (size_t)kC * L);
 }
 
-cudaError_t launch_bwd_finish(const BwdArgs& A, int grad_dtype, cudaStream_t s) {
+cudaError_t launch_bwd_finish(const BwdArgs& A, int grad_dtype, cudaStream_t s, bool with_qk) {
   const FwdArgs& a = A.f;
-  const int rowlen = a.Hqk * a.dk;
-  const dim3 grid_r((unsigned)((int64_t)a.B * a.T), (unsigned)((rowlen + 4 * kThreads - 1) / (4 * kThreads)));
-  const bool vec = a.dk % 4 == 0;
-  if (grad_dtype == LL_F32) {
-    if (vec) bwd_reduce_qk_kernel<float, true><<<grid_r, kThreads, 0, s>>>(A);
-    else bwd_reduce_qk_kernel<float, false><<<grid_r, kThreads, 0, s>>>(A);
-  } else {
-    if (vec) bwd_reduce_qk_kernel<__nv_bfloat16, true><<<grid_r, kThreads, 0, s>>>(A);
-    else bwd_reduce_qk_kernel<__nv_bfloat16, false><<<grid_r, kThreads, 0, s>>>(A);
+  cudaError_t e = cudaSuccess;
+  if (with_qk) {
+    const int rowlen = a.Hqk * a.dk;
+    const dim3 grid_r((unsigned)((int64_t)a.B * a.T),
+                      (unsigned)((rowlen + 4 * kThreads - 1) / (4 * kThreads)));
+    const bool vec = a.dk % 4 == 0;
+    if (grad_dtype == LL_F32) {
+      if (vec) bwd_reduce_qk_kernel<float, true><<<grid_r, kThreads, 0, s>>>(A);
+      else bwd_reduce_qk_kernel<float, false><<<grid_r, kThreads, 0, s>>>(A);
+    } else {
+      if (vec) bwd_reduce_qk_kernel<__nv_bfloat16, true><<<grid_r, kThreads, 0, s>>>(A);
+      else bwd_reduce_qk_kernel<__nv_bfloat16, false><<<grid_r, kThreads, 0, s>>>(A);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   if (a.log_a && A.dlog_a) {
     const int nch = (a.T + kScanChunk - 1) / kScanChunk;
     const dim3 grid_s((unsigned)nch, (unsigned)((int64_t)a.B * a.H));
@@ -823,7 +826,7 @@ cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype,
   else if (in_dtype == LL_F32) e = launch_typed<float, __nv_bfloat16>(A, s);
   else if (grad_dtype == LL_F32) e = launch_typed<__nv_bfloat16, float>(A, s);
   else e = launch_typed<__nv_bfloat16, __nv_bfloat16>(A, s);
-  return e == cudaSuccess ? launch_bwd_finish(A, grad_dtype, s) : e;
+  return e == cudaSuccess ? launch_bwd_finish(A, grad_dtype, s, true) : e;
 }
 
 }  // namespace ll

@@ -53,7 +53,8 @@ struct BqParams {
   const float* lam;
   const float* lgu;    // [B*H][N] the tiles' log decays (forward workspace)
   const float* nlg;    // [B*H][N] the even slots' block log decays (forward workspace)
-  float* dqh;          // [B, T, H, 128] per-head dQ
+  float* dqh;          // [B, T, H, 128] per-head dQ (fp32), or null
+  __nv_bfloat16* dq;   // [B, T, H, 128] dQ in bf16 when every head has its own q/k, or null
   float* dcq;          // [B, T, H] q . dQ, or null
   float* dlam;         // [B, T, H, L]
 };
@@ -475,7 +476,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       if (p.dcq) p.dcq[row] = qd;
     }
-    if (row_live) {
+    if (row_live && p.dq) {
+      uint4* dst = reinterpret_cast<uint4*>(p.dq + row * kD + 64 * hh);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_uint4(pack_bf16(dq[8 * q], dq[8 * q + 1]), pack_bf16(dq[8 * q + 2], dq[8 * q + 3]),
+                            pack_bf16(dq[8 * q + 4], dq[8 * q + 5]),
+                            pack_bf16(dq[8 * q + 6], dq[8 * q + 7]));
+    } else if (row_live) {
       float4* dst = reinterpret_cast<float4*>(p.dqh + row * kD + 64 * hh);
 #pragma unroll
       for (int q = 0; q < 16; ++q)
@@ -508,7 +516,8 @@ struct BkvParams {
   const float* lgu;          // [B*H][N] the tiles' log decays (forward workspace)
   const float* R;            // [B*H][N][d_k][d_v] mirrored states, fp32
   const __nv_bfloat16* v;    // [B, T, H, d_v] (for v . dV)
-  float* dkh;                // [B, T, H, 128] per-head dK
+  float* dkh;                // [B, T, H, 128] per-head dK (fp32), or null
+  __nv_bfloat16* dk;         // [B, T, H, 128] dK in bf16 when every head has its own q/k, or null
   float* dck;                // [B, T, H] k . dK, or null
   __nv_bfloat16* dv;         // [B, T, H, d_v]
 };
@@ -849,7 +858,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tc_fence_after();
     all_ok = __syncthreads_and(ok);
   }
-  // ---- epilogue: dK (fp32, per head), dV = intra + inter (bf16), k . dK
+  // ---- epilogue: dK (bf16, or fp32 per head), dV = intra + inter (bf16), k . dK
   if (all_ok) {
     float vd = 0.f;
     {
@@ -857,7 +866,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         tmem_ld32(tmem + lane_base + 256 + 64 * hh + 32 * c, v0);
-        if (row_live) {
+        if (row_live && p.dk) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dk + row * kD + 64 * hh + 32 * c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pack_bf16(v0[8 * q], v0[8 * q + 1]), pack_bf16(v0[8 * q + 2], v0[8 * q + 3]),
+                                pack_bf16(v0[8 * q + 4], v0[8 * q + 5]),
+                                pack_bf16(v0[8 * q + 6], v0[8 * q + 7]));
+        } else if (row_live) {
           float4* dst = reinterpret_cast<float4*>(p.dkh + row * kD + 64 * hh + 32 * c);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -1116,8 +1132,8 @@ bool tc_bwd_dq_supported(int64_t dk, int64_t dv, int in_dtype, int grad_dtype) {
   return in_dtype == LL_BF16 && grad_dtype == LL_BF16 && dk == kD && (dv == 64 || dv == 128);
 }
 
-cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, float* dcq,
-                             float* dlam, cudaStream_t s) {
+cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, void* dq_bf16,
+                             float* dcq, float* dlam, cudaStream_t s) {
   if (f.dk != kD || (f.dv != 64 && f.dv != 128) || f.C != kTile) return cudaErrorInvalidValue;
   const int64_t rows = (int64_t)f.B * f.H * f.N * kD;  // TMA row coordinates are int32
   if (rows > INT32_MAX) return cudaErrorInvalidValue;
@@ -1132,7 +1148,7 @@ cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, flo
   BqParams p;
   p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
   p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.nlg = f.nlg;
-  p.dqh = dqh; p.dcq = dcq; p.dlam = dlam;
+  p.dqh = dqh; p.dq = static_cast<__nv_bfloat16*>(dq_bf16); p.dcq = dcq; p.dlam = dlam;
   int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
   while ((int64_t(1) << levels) < f.N) ++levels;
   static std::once_flag attr_once;
@@ -1158,7 +1174,7 @@ cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, flo
 }
 
 cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R, float* dkh,
-                              float* dck, void* dv, cudaStream_t s) {
+                              void* dk_bf16, float* dck, void* dv, cudaStream_t s) {
   if (f.dk != kD || (f.dv != 64 && f.dv != 128) || f.C != kTile) return cudaErrorInvalidValue;
   const int dvw = f.dv;
   CUtensorMap tmQ, tmK, tmV, tmG;
@@ -1171,7 +1187,8 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
   p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
   p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.R = R;
   p.v = static_cast<const __nv_bfloat16*>(f.v);
-  p.dkh = dkh; p.dck = dck; p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dkh = dkh; p.dk = static_cast<__nv_bfloat16*>(dk_bf16); p.dck = dck;
+  p.dv = static_cast<__nv_bfloat16*>(dv);
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {

@@ -137,19 +137,19 @@ BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, in
 cudaError_t launch_simt_backward(const BwdArgs& a, int in_dtype, int grad_dtype, cudaStream_t s);
 // Tensor-core backward (bf16, d_k = 128, d_v in {64, 128}) on the 128-token tiles of a
 // completed tensor-core forward over the same inputs (f: that forward's arguments and
-// workspace).  dQ and dlambda from its block states: per-head dQ, q . dQ (dcq may be
-// null), dlambda.
+// workspace).  dQ and dlambda from its block states: dQ (bf16 into dq_bf16 when every
+// head has its own q/k, else fp32 per head into dqh), q . dQ (dcq may be null), dlambda.
 bool tc_bwd_dq_supported(int64_t dk, int64_t dv, int in_dtype, int grad_dtype);
-cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, float* dcq,
-                             float* dlam, cudaStream_t s);
+cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, void* dq_bf16,
+                             float* dcq, float* dlam, cudaStream_t s);
 // Tensor-core mirrored states on the forward's 128-token tiles into R ([B*H][N][d_k][d_v]
 // fp32, zeroed here), then dK, dV and k . dK from them (f as above).  dv in bf16.
 cudaError_t launch_tc_bwd_rstate(const FwdArgs& f, const void* dout, float* R, cudaStream_t s);
 cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R, float* dkh,
-                              float* dck, void* dv, cudaStream_t s);
-// The group sums of dq and dk with their cast, and d log a (the last two kernels of every
-// backward path).
-cudaError_t launch_bwd_finish(const BwdArgs& a, int grad_dtype, cudaStream_t s);
+                              void* dk_bf16, float* dck, void* dv, cudaStream_t s);
+// The group sums of dq and dk with their cast (skipped when with_qk is false: the
+// kernels wrote them), and d log a (the last kernels of every backward path).
+cudaError_t launch_bwd_finish(const BwdArgs& a, int grad_dtype, cudaStream_t s, bool with_qk);
 cudaError_t tcb_take_error(cudaStream_t s, unsigned* flags);
 size_t bwd_smem_max(int dk, int dv, int L);  // largest dynamic shared memory of a kernel
 // The decode state at position T-1 from a completed forward's workspace (tc_layout: the

@@ -330,7 +330,8 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
   const BwdWorkspace w = bwd_workspace_layout(B, T, H, N, dk, dv, n_tc);
   if (!workspace || workspace_bytes < w.total) return LL_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_ALIGN;
-  if (n_tc > 0 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(dout)))
+  if (n_tc > 0 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(dout) &&
+                    aligned16(dq) && aligned16(dk_out) && aligned16(dv_out)))
     return LL_ERR_ALIGN;
   BwdArgs A;
   FwdArgs& a = A.f;
@@ -371,11 +372,16 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
     f.tick = reinterpret_cast<uint32_t*>(fw + w.fwd.off_tick);
     // the mirrored states on the same 128-token tiles go into U's buffer (fp32)
     float* R = reinterpret_cast<float*>(a.U);
+    // with one q/k per head the kernels write dq and dk in bf16 themselves; shared q/k
+    // heads need the per-head fp32 values summed over each group
+    const bool own_qk = a.hg == 1;
     e = launch_tc_forward(f, LL_BF16, s, nullptr);
-    if (e == cudaSuccess) e = launch_tc_bwd_dq(f, dout, A.dqh, A.dcq, dlambda, s);
+    if (e == cudaSuccess)
+      e = launch_tc_bwd_dq(f, dout, A.dqh, own_qk ? dq : nullptr, A.dcq, dlambda, s);
     if (e == cudaSuccess && f.N > 1) e = launch_tc_bwd_rstate(f, dout, R, s);
-    if (e == cudaSuccess) e = launch_tc_bwd_dkv(f, dout, R, A.dkh, A.dck, dv_out, s);
-    if (e == cudaSuccess) e = launch_bwd_finish(A, grad_dtype, s);
+    if (e == cudaSuccess)
+      e = launch_tc_bwd_dkv(f, dout, R, A.dkh, own_qk ? dk_out : nullptr, A.dck, dv_out, s);
+    if (e == cudaSuccess) e = launch_bwd_finish(A, grad_dtype, s, !own_qk);
     return e == cudaSuccess ? LL_OK : cuda_fail(e);
   }
   e = launch_simt_backward(A, in_dtype, grad_dtype, s);

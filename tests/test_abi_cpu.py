@@ -203,6 +203,7 @@ def test_bwd_validation_codes(L):
         L.LL_ERR_UNSUPPORTED                                 # dO must be bf16 as well
     tc_kw = dict(dkd=128, dvd=64, ind=L.LL_BF16, gd=L.LL_BF16, ws=FAKE, wsb=1 << 40)
     assert bwd(path=L.LL_PATH_TC, q=ctypes.c_void_p(0x1002), **tc_kw) == L.LL_ERR_ALIGN
+    assert bwd(path=L.LL_PATH_TC, dv=ctypes.c_void_p(0x1008), **tc_kw) == L.LL_ERR_ALIGN
     assert bwd() == L.LL_ERR_WORKSPACE
     assert bwd(ws=ctypes.c_void_p(0x1010), wsb=1 << 40) == L.LL_ERR_ALIGN
     assert bwd(T=0, q=None, k=None, v=None, lam=None, dout=None, dq=None, dk=None, dv=None,
