@@ -1,6 +1,7 @@
 """CPU oracle (test infrastructure only; see loglinear_oracle's header)."""
 from .loglinear_oracle import (  # noqa: F401
     backward_direct,
+    backward_sampled,
     decay_rows,
     decode_step,
     fenwick_partition,

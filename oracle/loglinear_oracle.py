@@ -216,6 +216,57 @@ def backward_direct(q, k, v, log_a, lam, dout):
     return g
 
 
+def backward_sampled(q, k, v, log_a, lam, dout, rows, cols, heads):
+    """The gradients of backward_direct for chosen positions only, fp64: dq and dlam of the
+    query rows `rows`, dk and dv of the source positions `cols`, for the (b, h) pairs in
+    `heads`.  Same definition, evaluated one row (for dq, dlam) or one column (for dk, dv)
+    at a time, so that long sequences stay cheap:
+        dq_t = sum_{s<=t} M[t, s] (dO_t . v_s) k_s,
+        dlam[t, l] = sum over the level-l bucket of t of M^S[t, s] (dO_t . v_s)(q_t . k_s),
+        dk_s = sum_{t>=s} M[t, s] (dO_t . v_s) q_t,   dv_s = sum_{t>=s} M[t, s] (q_t . k_s) dO_t.
+    Returns dict(q [n_heads, len(rows), dk], lam [.., len(rows), L], k [.., len(cols), dk],
+    v [.., len(cols), dv]) in the order of `heads`."""
+    q, k, v, lam, do = _f64(q), _f64(k), _f64(v), _f64(lam), _f64(dout)
+    log_a = _f64(log_a)
+    T = q.shape[1]
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    out = {"q": [], "lam": [], "k": [], "v": []}
+    for b, h in heads:
+        Q, K, V, dO, lm = q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h], lam[b, :, h]
+        cum = np.zeros(T) if log_a is None else np.cumsum(log_a[b, :, h])
+        gq = np.zeros((len(rows), Q.shape[1]))
+        gl = np.zeros((len(rows), lm.shape[1]))
+        for i, t in enumerate(rows):
+            lv = level_row(int(t))
+            ms = np.exp(cum[t] - cum[: t + 1])
+            dov = V[: t + 1] @ dO[t]
+            qk = K[: t + 1] @ Q[t]
+            gq[i] = (ms * lm[t, lv] * dov) @ K[: t + 1]
+            np.add.at(gl[i], lv, ms * dov * qk)
+        gk = np.zeros((len(cols), K.shape[1]))
+        gv = np.zeros((len(cols), V.shape[1]))
+        for i, s0 in enumerate(cols):
+            ts = np.arange(s0, T)
+            # level(t, s0) for every t >= s0 by its closed form bit_length(t XOR s0), which the
+            # pins check against the Fenwick walk; exact integer shifts
+            x = ts ^ s0
+            lv = np.zeros(len(ts), dtype=np.int64)
+            while x.any():
+                lv += x > 0
+                x = x >> 1
+            m = np.exp(cum[ts] - cum[s0]) * lm[ts, lv]
+            dov = dO[ts] @ V[s0]
+            qk = Q[ts] @ K[s0]
+            gk[i] = (m * dov) @ Q[ts]
+            gv[i] = (m * qk) @ dO[ts]
+        out["q"].append(gq)
+        out["lam"].append(gl)
+        out["k"].append(gk)
+        out["v"].append(gv)
+    return {n: np.stack(a) for n, a in out.items()}
+
+
 # --------------------------------------------------------------------------------------
 # L2a: per-level states and the lssb decode recurrence
 # --------------------------------------------------------------------------------------

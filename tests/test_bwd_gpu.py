@@ -152,3 +152,33 @@ def test_bwd_workspace_reuse_and_empty(LL):
     lam = torch.zeros(1, 0, 2, 3, device="cuda")
     out = LL.loglinear_bwd(q, q, q, None, lam, q)
     assert out[0].shape == (1, 0, 2, 8)
+
+
+def _positions(T, n, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, T // 2, T - 129, T - 2, T - 1]
+    return np.unique(np.concatenate([fixed, rng.integers(0, T, n)]))
+
+
+def test_bwd_tc_full_size_sampled(LL):
+    """The headline workload (B1 H16 T16384 dk=dv=128 bf16) on the tensor-core path, as
+    the bench times it: dq and dlambda of sampled query rows, dk and dv of sampled source
+    positions, on two heads, against the oracle's row and column evaluation."""
+    cfg = W.FWD_CONFIGS["mamba2_T16384"]
+    x = W.make_fwd_inputs(cfg)
+    dout = _dout(cfg, 99)
+    d = cuda(x)
+    got = LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout.cuda(), path="tc")
+    torch.cuda.synchronize()
+    assert LL.device_error() == 0
+    rows, cols = _positions(cfg.T, 24, 1), _positions(cfg.T, 24, 2)
+    heads = [(0, 3), (0, 11)]
+    want = oracle.backward_sampled(x["q"], x["k"], x["v"], x["log_a"], x["lam"], dout, rows,
+                                   cols, heads)
+    for i, (b, h) in enumerate(heads):
+        errs = {"q": rel_l2(got[0][b, rows, h].cpu(), want["q"][i]),
+                "lam": rel_l2(got[4][b, rows, h].cpu(), want["lam"][i]),
+                "k": rel_l2(got[1][b, cols, h].cpu(), want["k"][i]),
+                "v": rel_l2(got[2][b, cols, h].cpu(), want["v"][i])}
+        print(f"bwd tc full size head {h}: " + " ".join(f"{k}={e:.2e}" for k, e in errs.items()))
+        assert all(e <= TOL_BF16 for e in errs.values()), errs

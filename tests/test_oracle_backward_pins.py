@@ -86,3 +86,19 @@ def test_backward_linear_attention_special_case():
     o.backward(torch.tensor(dout))
     for name, t in (("q", q), ("k", k), ("v", v)):
         np.testing.assert_allclose(g[name], t.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_backward_sampled_equals_direct():
+    """The row / column evaluation of the sampled backward equals the dense one."""
+    x, dout = _inputs(2, 150, 3, 8, 4, 9, seed=13)
+    g = oracle.backward_direct(x["q"], x["k"], x["v"], x["log_a"], x["lam"], dout)
+    rows = [0, 1, 7, 64, 127, 149]
+    cols = [0, 5, 63, 64, 100, 149]
+    heads = [(0, 1), (1, 2)]
+    gs = oracle.backward_sampled(x["q"], x["k"], x["v"], x["log_a"], x["lam"], dout, rows, cols,
+                                 heads)
+    for i, (b, h) in enumerate(heads):
+        np.testing.assert_allclose(gs["q"][i], g["q"][b, rows, h], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(gs["lam"][i], g["lam"][b, rows, h], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(gs["k"][i], g["k"][b, cols, h], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(gs["v"][i], g["v"][b, cols, h], rtol=1e-12, atol=1e-13)
