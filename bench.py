@@ -480,8 +480,19 @@ def measure_backward(LL, cfg, d, dev, flush, peaks, reps=5):
                                            cfg.L, 1, 1), device=dev, dtype=torch.uint8)
     t = _median_us(lambda: LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout,
                                             workspace=ws), flush, reps)
-    rep = _bwd_report(cfg, t, peaks, _bwd_path(LL, cfg))
+    path = _bwd_path(LL, cfg)
+    rep = _bwd_report(cfg, t, peaks, path)
     rep["workload"] = f"{cfg.name}: loglinear_bwd, bf16 inputs and gradients"
+    if path == "tc":  # the training step: the forward's workspace kept for the backward
+        fws = torch.empty(LL.fwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv, cfg.C, 1),
+                          device=dev, dtype=torch.uint8)
+        LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C, workspace=fws)
+        tg = _median_us(lambda: LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"],
+                                                 dout, workspace=ws, fwd_workspace=fws),
+                        flush, reps)
+        rep["bwd_given_fwd_us"] = tg * 1e6
+        rep["note"] = ("bwd_us recomputes the forward's block states; bwd_given_fwd_us reads "
+                       "them from the forward's workspace")
     return rep
 
 
@@ -509,7 +520,6 @@ def measure_benchmark_shape(LL, cfg, dev, flush, peaks, reps=10):
         raise RuntimeError("tensor-core forward reported a device error")
     t = statistics.median(ts)
     fbytes, fflops = fwd_algorithmic(cfg)
-    del ws
     g = torch.Generator(device=dev).manual_seed(7)
     dout = torch.randn(cfg.B, cfg.T, cfg.H, cfg.dv, device=dev, generator=g).to(d["q"].dtype)
     bws = torch.empty(LL.bwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.qk_heads, cfg.dk, cfg.dv,
@@ -517,10 +527,22 @@ def measure_benchmark_shape(LL, cfg, dev, flush, peaks, reps=10):
     tb = _median_us(lambda: LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout,
                                              workspace=bws), flush, 3)
     bwd = _bwd_report(cfg, tb, peaks, _bwd_path(LL, cfg))
+    # the training step: a forward that keeps its workspace, then the backward reading it
+    fws = ws
+
+    def step():
+        LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C, out=out,
+                         workspace=fws)
+        LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout, workspace=bws,
+                         fwd_workspace=fws)
+
+    t_step = _median_us(step, flush, 3)
     return {"workload": f"{cfg.name}: loglinear_fwd B{cfg.B} H{cfg.H} (q/k heads "
                         f"{cfg.qk_heads}) T{cfg.T} dk={cfg.dk} dv={cfg.dv} C{cfg.C} L{cfg.L} bf16",
             "path": LL.resolve_path(cfg.dk, cfg.dv, cfg.C, 1), "fwd_us": t * 1e6,
-            "fwd_bwd_us": (t + tb) * 1e6, "backward": bwd,
+            "fwd_bwd_us": t_step * 1e6, "backward": bwd,
+            "fwd_bwd_note": "one forward keeping its workspace, then the backward reading it "
+                            "(the training step); backward.bwd_us alone recomputes the states",
             "tokens_per_s": cfg.B * cfg.T / t,
             "roofline": {"bound": "hbm", "achieved": fbytes / t / 1e9, "peak": peaks["hbm"],
                          "unit": "GB/s", "frac": fbytes / t / 1e9 / peaks["hbm"],

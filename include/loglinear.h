@@ -199,6 +199,15 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
  *   and of the states.  LL_PATH_SIMT computes everything on CUDA cores in fp32.
  *   LL_PATH_AUTO takes the tensor cores when they apply.  The workspace size depends on
  *   the path.
+ * fwd_workspace: NULL, or, on the tensor-core path, the workspace of a loglinear_fwd call
+ *   that ran on the tensor-core path (LL_PATH_TC or AUTO with bf16, dk = 128) over these
+ *   same q, k, v, log_a, lambda and sizes, with nothing written to it since.  Its block
+ *   states are then read instead of being recomputed by a forward inside this call (the
+ *   usual training step: forward, then backward).  The library cannot check that the
+ *   contents match the inputs; that is the caller's contract.  fwd_workspace_bytes must
+ *   be at least loglinear_fwd_workspace_size() for the forward's arguments
+ *   (LL_ERR_WORKSPACE); a non-NULL fwd_workspace on the CUDA-core path is
+ *   LL_ERR_UNSUPPORTED.
  * workspace: device scratch of at least loglinear_bwd_workspace_size() bytes, 256-byte
  * aligned (recomputed forward states, per-head q and k gradients).
  * Errors: LL_ERR_INVALID (null pointer, negative size, dlog_a NULL with log_a given),
@@ -212,7 +221,8 @@ LL_API int loglinear_bwd(const void* q, const void* k, const void* v, const floa
                          const float* lambda, const void* dout, void* dq, void* dk, void* dv,
                          float* dlog_a, float* dlambda, int64_t B, int64_t T, int64_t H,
                          int64_t Hqk, int64_t dk_dim, int64_t dv_dim, int64_t L, int in_dtype,
-                         int grad_dtype, int path, void* workspace, size_t workspace_bytes,
+                         int grad_dtype, int path, const void* fwd_workspace,
+                         size_t fwd_workspace_bytes, void* workspace, size_t workspace_bytes,
                          ll_stream_t stream);
 
 /*

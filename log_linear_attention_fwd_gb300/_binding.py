@@ -48,7 +48,8 @@ SIGNATURES = {
     "loglinear_bwd_workspace_size": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _int, _int,
                                             _int, ctypes.POINTER(_sz)]),
     "loglinear_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
-                             _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _sz, _vp]),
+                             _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _sz, _vp, _sz,
+                             _vp]),
 }
 
 
@@ -259,12 +260,14 @@ def bwd_workspace_size(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, path="auto
     return int(out.value)
 
 
-def loglinear_bwd(q, k, v, log_a, lam, dout, workspace=None, path="auto", stream=None):
+def loglinear_bwd(q, k, v, log_a, lam, dout, workspace=None, path="auto", fwd_workspace=None,
+                  stream=None):
     """Gradients of sum(dout ⊙ O) for O = loglinear_fwd(q, k, v, log_a, lam): returns
     (dq, dk, dv, dlog_a, dlam); dq, dk, dv in dout's dtype, dlog_a (None without decay)
     and dlam fp32.  path: "tc" computes dq and dlam on the tensor cores (bf16, d_k = 128,
     d_v in {64, 128}), "simt" everything on CUDA cores, "auto" the tensor cores if they
-    apply."""
+    apply.  fwd_workspace: the workspace of a tensor-core loglinear_fwd over the same
+    inputs, whose block states are then read instead of recomputed."""
     B, T, Hqk, dk = q.shape
     H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
     _check_dev("q", q, shape=(B, T, Hqk, dk))
@@ -283,10 +286,13 @@ def loglinear_bwd(q, k, v, log_a, lam, dout, workspace=None, path="auto", stream
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), device=q.device, dtype=torch.uint8)
     _check_dev("workspace", workspace, torch.uint8)
+    if fwd_workspace is not None:
+        _check_dev("fwd_workspace", fwd_workspace, torch.uint8)
     st = _lib.loglinear_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(dout),
                             _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dla), _ptr(dlam), B, T, H, Hqk,
-                            dk, dv, L, in_dt, g_dt, PATHS[path], _ptr(workspace),
-                            workspace.numel(), _stream(stream))
+                            dk, dv, L, in_dt, g_dt, PATHS[path], _ptr(fwd_workspace),
+                            0 if fwd_workspace is None else fwd_workspace.numel(),
+                            _ptr(workspace), workspace.numel(), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_bwd")
     return dq, dk_, dv_, dla, dlam

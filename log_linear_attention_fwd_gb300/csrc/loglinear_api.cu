@@ -319,10 +319,13 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
                   const float* lambda, const void* dout, void* dq, void* dk_out, void* dv_out,
                   float* dlog_a, float* dlambda, int64_t B, int64_t T, int64_t H, int64_t Hqk,
                   int64_t dk, int64_t dv, int64_t L, int in_dtype, int grad_dtype, int path,
-                  void* workspace, size_t workspace_bytes, ll_stream_t stream) {
+                  const void* fwd_workspace, size_t fwd_workspace_bytes, void* workspace,
+                  size_t workspace_bytes, ll_stream_t stream) {
   int64_t N, n_tc;
   const int st = check_bwd(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, path, &N, &n_tc);
   if (st != LL_OK) return st;
+  if (fwd_workspace && n_tc == 0) return LL_ERR_UNSUPPORTED;  // only the tensor-core path
+                                                              // reads a forward's states
   if (B == 0 || T == 0 || H == 0) return LL_OK;
   if (!q || !k || !v || !lambda || !dout || !dq || !dk_out || !dv_out || !dlambda)
     return LL_ERR_INVALID;
@@ -333,6 +336,10 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
   if (n_tc > 0 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(dout) &&
                     aligned16(dq) && aligned16(dk_out) && aligned16(dv_out)))
     return LL_ERR_ALIGN;
+  if (fwd_workspace) {
+    if (fwd_workspace_bytes < w.fwd.total) return LL_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(fwd_workspace) & 255u) != 0) return LL_ERR_ALIGN;
+  }
   BwdArgs A;
   FwdArgs& a = A.f;
   a.q = q; a.k = k; a.v = v; a.log_a = log_a; a.lam = lambda; a.out = nullptr;
@@ -361,7 +368,9 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
     f.C = kTcTile;
     f.lc = log2_exact(kTcTile);
     f.N = (int)n_tc;
-    char* fw = ws + w.off_fwd;
+    // the states: those a forward call left in its own workspace, else a forward here
+    char* fw = fwd_workspace ? static_cast<char*>(const_cast<void*>(fwd_workspace))
+                             : ws + w.off_fwd;
     f.out = ws + w.off_out;
     f.U = fw + w.fwd.off_U;
     f.nodes = fw + w.fwd.off_nodes;
@@ -375,7 +384,7 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
     // with one q/k per head the kernels write dq and dk in bf16 themselves; shared q/k
     // heads need the per-head fp32 values summed over each group
     const bool own_qk = a.hg == 1;
-    e = launch_tc_forward(f, LL_BF16, s, nullptr);
+    if (!fwd_workspace) e = launch_tc_forward(f, LL_BF16, s, nullptr);
     if (e == cudaSuccess)
       e = launch_tc_bwd_dq(f, dout, A.dqh, own_qk ? dq : nullptr, A.dcq, dlambda, s);
     if (e == cudaSuccess && f.N > 1) e = launch_tc_bwd_rstate(f, dout, R, s);

@@ -181,13 +181,14 @@ def test_bwd_validation_codes(L):
     def bwd(**kw):
         a = dict(q=FAKE, k=FAKE, v=FAKE, log_a=None, lam=FAKE, dout=FAKE, dq=FAKE, dk=FAKE,
                  dv=FAKE, dla=None, dlam=FAKE, B=1, T=64, H=2, Hqk=2, dkd=16, dvd=16, Lv=7,
-                 ind=L.LL_F32, gd=L.LL_F32, path=L.LL_PATH_AUTO, ws=None, wsb=0, stream=None)
+                 ind=L.LL_F32, gd=L.LL_F32, path=L.LL_PATH_AUTO, fws=None, fwsb=0, ws=None,
+                 wsb=0, stream=None)
         a.update(kw)
         return L.lib().loglinear_bwd(a["q"], a["k"], a["v"], a["log_a"], a["lam"], a["dout"],
                                      a["dq"], a["dk"], a["dv"], a["dla"], a["dlam"], a["B"],
                                      a["T"], a["H"], a["Hqk"], a["dkd"], a["dvd"], a["Lv"],
-                                     a["ind"], a["gd"], a["path"], a["ws"], a["wsb"],
-                                     a["stream"])
+                                     a["ind"], a["gd"], a["path"], a["fws"], a["fwsb"],
+                                     a["ws"], a["wsb"], a["stream"])
     assert bwd(Lv=6) == L.LL_ERR_SHAPE                  # T=64 needs L >= 7
     assert bwd(H=4, Hqk=3) == L.LL_ERR_SHAPE
     assert bwd(ind=3) == L.LL_ERR_DTYPE
@@ -204,6 +205,11 @@ def test_bwd_validation_codes(L):
     tc_kw = dict(dkd=128, dvd=64, ind=L.LL_BF16, gd=L.LL_BF16, ws=FAKE, wsb=1 << 40)
     assert bwd(path=L.LL_PATH_TC, q=ctypes.c_void_p(0x1002), **tc_kw) == L.LL_ERR_ALIGN
     assert bwd(path=L.LL_PATH_TC, dv=ctypes.c_void_p(0x1008), **tc_kw) == L.LL_ERR_ALIGN
+    # a forward's workspace: tensor-core path only, large enough, 256-byte aligned
+    assert bwd(fws=FAKE, fwsb=1 << 40) == L.LL_ERR_UNSUPPORTED
+    assert bwd(path=L.LL_PATH_TC, fws=FAKE, fwsb=16, **tc_kw) == L.LL_ERR_WORKSPACE
+    assert bwd(path=L.LL_PATH_TC, fws=ctypes.c_void_p(0x1010), fwsb=1 << 40, **tc_kw) == \
+        L.LL_ERR_ALIGN
     assert bwd() == L.LL_ERR_WORKSPACE
     assert bwd(ws=ctypes.c_void_p(0x1010), wsb=1 << 40) == L.LL_ERR_ALIGN
     assert bwd(T=0, q=None, k=None, v=None, lam=None, dout=None, dq=None, dk=None, dv=None,

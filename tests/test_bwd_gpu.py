@@ -182,3 +182,26 @@ def test_bwd_tc_full_size_sampled(LL):
                 "v": rel_l2(got[2][b, cols, h].cpu(), want["v"][i])}
         print(f"bwd tc full size head {h}: " + " ".join(f"{k}={e:.2e}" for k, e in errs.items()))
         assert all(e <= TOL_BF16 for e in errs.values()), errs
+
+
+@pytest.mark.parametrize("dv,Hqk", [(128, 0), (64, 1)])
+def test_bwd_reads_forward_workspace(LL, dv, Hqk):
+    """The backward given a tensor-core forward's workspace (its block states kept) equals
+    the backward that recomputes them: dq and dlambda bit for bit (their arithmetic has a
+    fixed order), dk, dv and d log a up to the order of the float atomics that sum the
+    mirrored states (which also moves a few bf16 roundings by one step)."""
+    cfg = W.FwdConfig("bwd_fws", 1, 4, 1500, 128, dv, 64, 12, "bf16", True, "softplus", seed=dv,
+                      Hqk=Hqk)
+    x = cuda(W.make_fwd_inputs(cfg))
+    dout = _dout(cfg, 5).cuda()
+    fws = torch.empty(LL.fwd_workspace_size(cfg.B, cfg.T, cfg.H, 128, dv, 64, 1, "tc"),
+                      device="cuda", dtype=torch.uint8)
+    LL.loglinear_fwd(x["q"], x["k"], x["v"], x["log_a"], x["lam"], 64, workspace=fws, path="tc")
+    a = LL.loglinear_bwd(x["q"], x["k"], x["v"], x["log_a"], x["lam"], dout, path="tc",
+                         fwd_workspace=fws)
+    b = LL.loglinear_bwd(x["q"], x["k"], x["v"], x["log_a"], x["lam"], dout, path="tc")
+    torch.cuda.synchronize()
+    assert LL.device_error() == 0
+    assert torch.equal(a[0], b[0]) and torch.equal(a[4], b[4])
+    for u, w in zip(a[1:4], b[1:4]):
+        assert rel_l2(u.cpu(), w.cpu().double().numpy()) <= 1e-3
