@@ -47,6 +47,25 @@ constexpr int kLamStride = 9;
 constexpr int kTileLc = 7;
 constexpr int kMaxChunkLevels = 32;
 
+// The tile a CTA on this SM most likely takes next: one CTA per SM and tiles started in
+// index order make it this tile + the number of SMs (`ahead`).  Its coordinates, or false
+// when there is none.
+struct TileAt {
+  int b, h, hq, t0;
+};
+
+__device__ __forceinline__ bool next_tile(int ahead, int B, int T, int H, int hg, TileAt* t) {
+  const int64_t nt = (int64_t)blockIdx.x + ahead;
+  if (ahead <= 0 || nt >= (int64_t)gridDim.x) return false;
+  const int BH = B * H;
+  const int j = (int)(nt / BH), bhi = (int)(nt - (int64_t)j * BH);
+  t->b = bhi / H;
+  t->h = bhi - t->b * H;
+  t->hq = t->h / hg;
+  t->t0 = j * 128;
+  return t->t0 < T;
+}
+
 struct BqParams {
   int B, T, H, hg, L, N;
   const float* log_a;
@@ -57,6 +76,7 @@ struct BqParams {
   __nv_bfloat16* dq;   // [B, T, H, 128] dQ in bf16 when every head has its own q/k, or null
   float* dcq;          // [B, T, H] q . dQ, or null
   float* dlam;         // [B, T, H, L]
+  int ahead;  // tiles between this one and the next on the same SM
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -216,6 +236,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     for (int pv = 0; pv < kPanels; ++pv) {
       tma_load_4d(&tmV, bar_load, Vb + pv * kPanel, 64 * pv, h, t0, b);
       tma_load_4d(&tmG, bar_load, Gb + pv * kPanel, 64 * pv, h, t0, b);
+    }
+    TileAt nx;  // warm L2 with the next tile's operands
+    if (next_tile(p.ahead, p.B, p.T, p.H, p.hg, &nx)) {
+      tma_prefetch_4d(&tmQ, 0, nx.hq, nx.t0, nx.b);
+      tma_prefetch_4d(&tmQ, 64, nx.hq, nx.t0, nx.b);
+      tma_prefetch_4d(&tmK, 0, nx.hq, nx.t0, nx.b);
+      tma_prefetch_4d(&tmK, 64, nx.hq, nx.t0, nx.b);
+#pragma unroll
+      for (int pv = 0; pv < kPanels; ++pv) {
+        tma_prefetch_4d(&tmV, 64 * pv, nx.h, nx.t0, nx.b);
+        tma_prefetch_4d(&tmG, 64 * pv, nx.h, nx.t0, nx.b);
+      }
     }
   }
   __syncwarp();
@@ -520,6 +552,7 @@ struct BkvParams {
   __nv_bfloat16* dk;         // [B, T, H, 128] dK in bf16 when every head has its own q/k, or null
   float* dck;                // [B, T, H] k . dK, or null
   __nv_bfloat16* dv;         // [B, T, H, d_v]
+  int ahead;  // tiles between this one and the next on the same SM
 };
 
 struct KvSmem {
@@ -671,6 +704,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     for (int pv = 0; pv < kPanels; ++pv) {
       tma_load_4d(&tmV, bar_load, Vb + pv * kPanel, 64 * pv, h, t0, b);
       tma_load_4d(&tmG, bar_load, Gb + pv * kPanel, 64 * pv, h, t0, b);
+    }
+    TileAt nx;  // warm L2 with the next tile's operands
+    if (next_tile(p.ahead, p.B, p.T, p.H, p.hg, &nx)) {
+      tma_prefetch_4d(&tmQ, 0, nx.hq, nx.t0, nx.b);
+      tma_prefetch_4d(&tmQ, 64, nx.hq, nx.t0, nx.b);
+      tma_prefetch_4d(&tmK, 0, nx.hq, nx.t0, nx.b);
+      tma_prefetch_4d(&tmK, 64, nx.hq, nx.t0, nx.b);
+#pragma unroll
+      for (int pv = 0; pv < kPanels; ++pv) {
+        tma_prefetch_4d(&tmV, 64 * pv, nx.h, nx.t0, nx.b);
+        tma_prefetch_4d(&tmG, 64 * pv, nx.h, nx.t0, nx.b);
+      }
     }
   }
   __syncwarp();
@@ -943,6 +988,7 @@ struct BrParams {
   const float* lam;
   const float* lgu;   // [B*H][N] the tiles' log decays (forward workspace)
   float* R;           // [B*H][N][d_k][d_v] mirrored states (zeroed before)
+  int ahead;  // tiles between this one and the next on the same SM
 };
 
 struct RsSmem {
@@ -1035,6 +1081,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
     for (int pv = 0; pv < kPanels; ++pv)
       tma_load_4d(&tmG, bar_load, Gb + pv * kPanel, 64 * pv, h, t0, b);
+    TileAt nx;
+    if (next_tile(p.ahead, p.B, p.T, p.H, p.hg, &nx)) {
+      tma_prefetch_4d(&tmQ, 0, nx.hq, nx.t0, nx.b);
+      tma_prefetch_4d(&tmQ, 64, nx.hq, nx.t0, nx.b);
+#pragma unroll
+      for (int pv = 0; pv < kPanels; ++pv) tma_prefetch_4d(&tmG, 64 * pv, nx.h, nx.t0, nx.b);
+    }
   }
   __syncwarp();
   const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
@@ -1128,6 +1181,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 }  // namespace
 
+static int sm_count() {
+  static const int sms = [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 0;
+    return n;
+  }();
+  return sms;
+}
+
 bool tc_bwd_dq_supported(int64_t dk, int64_t dv, int in_dtype, int grad_dtype) {
   return in_dtype == LL_BF16 && grad_dtype == LL_BF16 && dk == kD && (dv == 64 || dv == 128);
 }
@@ -1149,6 +1213,7 @@ cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, voi
   p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
   p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.nlg = f.nlg;
   p.dqh = dqh; p.dq = static_cast<__nv_bfloat16*>(dq_bf16); p.dcq = dcq; p.dlam = dlam;
+  p.ahead = sm_count();
   int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
   while ((int64_t(1) << levels) < f.N) ++levels;
   static std::once_flag attr_once;
@@ -1189,6 +1254,7 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
   p.v = static_cast<const __nv_bfloat16*>(f.v);
   p.dkh = dkh; p.dk = static_cast<__nv_bfloat16*>(dk_bf16); p.dck = dck;
   p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.ahead = sm_count();
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -1218,6 +1284,7 @@ cudaError_t launch_tc_bwd_rstate(const FwdArgs& f, const void* dout, float* R, c
   BrParams p;
   p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
   p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.R = R;
+  p.ahead = sm_count();
   int levels = 0;
   while ((int64_t(1) << levels) < f.N) ++levels;
   static std::once_flag attr_once;
