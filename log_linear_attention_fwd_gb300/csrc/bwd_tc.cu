@@ -1150,7 +1150,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       __syncwarp();
     }
-    if (k >= 1) {  // level k-1: row d = r of its d_k x d_v part, this thread's half of d_v
+    if (k >= 1) {  // level k-1 into its block's d_k x d_v part
       const int bf = (k - 1) & 1;
       const bool got = __syncthreads_and(mbar_wait(&bar_r[bf], ph[bf]));
       ph[bf] ^= 1;
@@ -1159,17 +1159,32 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         break;
       }
       tc_fence_after();
-      float* dst = p.R + ((bh * p.N + c_prev) * kD + r) * DV + kHalf * hh;
+      // Row d = r, this thread's half of d_v, staged in the W pair level k-1 read (its MMAs
+      // are done) as 16-byte chunks, chunk x of row d at x ^ (d & 7): the stores of 8
+      // consecutive rows and the reads of one row are free of bank conflicts.
+      float4* stage = reinterpret_cast<float4*>(smem + RsSmem::kW + bf * 2 * kOperand);
+      constexpr int kRowChunks = DV / 4;
 #pragma unroll
       for (int c = 0; c < kPanels; ++c) {
         float v[32];
         tmem_ld32(tmem + lane_base + bf * 128 + kHalf * hh + 32 * c, v);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * q),
-                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        for (int q = 0; q < 8; ++q) {
+          const int x = (kHalf * hh + 32 * c) / 4 + q;
+          stage[r * kRowChunks + (x ^ (r & 7))] =
+              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
       }
       tc_fence_before();
+      __syncthreads();
+      // the block's part is contiguous in R: one warp's atomics cover 512 bytes
+      float4* dst = reinterpret_cast<float4*>(p.R + (bh * p.N + c_prev) * kD * DV);
+#pragma unroll 4
+      for (int i = tid; i < kD * kRowChunks; i += kThreadsB) {
+        const int d = i / kRowChunks, x = i - d * kRowChunks;
+        atomicAdd(dst + i, stage[d * kRowChunks + (x ^ (d & 7))]);
+      }
+      __syncthreads();  // the stage is the W pair the next level writes
     }
     c_prev = c_k;
   }
