@@ -73,7 +73,7 @@ struct BqParams {
   const float* lgu;    // [B*H][N] the tiles' log decays (forward workspace)
   const float* nlg;    // [B*H][N] the even slots' block log decays (forward workspace)
   float* dqh;          // [B, T, H, 128] per-head dQ (fp32), or null
-  __nv_bfloat16* dq;   // [B, T, H, 128] dQ in bf16 when every head has its own q/k, or null
+  const void* dq;      // non-null: dQ in bf16 through the dQ map (one q/k per head)
   float* dcq;          // [B, T, H] q . dQ, or null
   float* dlam;         // [B, T, H, L]
   int ahead;  // tiles between this one and the next on the same SM
@@ -87,6 +87,27 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Writes 32 fp32 values as bf16 into columns [32c, 32c+32) of row r of a tile of 128-byte
+// swizzled [128][64] panels (the layout a tokens map's TMA load or store uses).
+__device__ __forceinline__ void stage_row32_bf16(uint8_t* buf, int r, int c, const float* v) {
+  uint8_t* panel = buf + (c >> 1) * kPanel;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(panel + sw128_offset(r, (c & 1) * 4 + q)) =
+        make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                   pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+// Warms L2 with the box of a 4-d tensor map at (c0, c1, c2, c3), as tma_load_4d would read
+// it; no shared memory, no completion signal.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
 }
 
 // 32 fp32 values as bf16 into columns [32c, 32c+32) of row r of a swizzled tile.
@@ -161,7 +182,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                      const __grid_constant__ CUtensorMap tmU,
-                     const __grid_constant__ CUtensorMap tmNode, BqParams p, int levels) {
+                     const __grid_constant__ CUtensorMap tmNode,
+                     const __grid_constant__ CUtensorMap tmDQ, BqParams p, int levels) {
   constexpr int kPanels = DV / 64;
   constexpr int kVBytes = kTile * DV * 2;
   constexpr int kStateBytes = kD * DV * 2;
@@ -508,13 +530,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       if (p.dcq) p.dcq[row] = qd;
     }
-    if (row_live && p.dq) {
-      uint4* dst = reinterpret_cast<uint4*>(p.dq + row * kD + 64 * hh);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        dst[q] = make_uint4(pack_bf16(dq[8 * q], dq[8 * q + 1]), pack_bf16(dq[8 * q + 2], dq[8 * q + 3]),
-                            pack_bf16(dq[8 * q + 4], dq[8 * q + 5]),
-                            pack_bf16(dq[8 * q + 6], dq[8 * q + 7]));
+    if (p.dq) {  // no MMA reads Q any more: stage dQ there and store it with TMA
+      stage_row32_bf16(Qb, r, 2 * hh, dq);
+      stage_row32_bf16(Qb, r, 2 * hh + 1, dq + 32);
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {  // rows past T are clipped by the map
+        tma_store_4d(&tmDQ, Qb, 0, h, t0, b);
+        tma_store_4d(&tmDQ, Qb + kPanel, 64, h, t0, b);
+        tma_store_commit();
+        tma_store_wait_read();
+      }
     } else if (row_live) {
       float4* dst = reinterpret_cast<float4*>(p.dqh + row * kD + 64 * hh);
 #pragma unroll
@@ -549,9 +575,8 @@ struct BkvParams {
   const float* R;            // [B*H][N][d_k][d_v] mirrored states, fp32
   const __nv_bfloat16* v;    // [B, T, H, d_v] (for v . dV)
   float* dkh;                // [B, T, H, 128] per-head dK (fp32), or null
-  __nv_bfloat16* dk;         // [B, T, H, 128] dK in bf16 when every head has its own q/k, or null
+  const void* dk;            // non-null: dK in bf16 through the dK map (one q/k per head)
   float* dck;                // [B, T, H] k . dK, or null
-  __nv_bfloat16* dv;         // [B, T, H, d_v]
   int ahead;  // tiles between this one and the next on the same SM
 };
 
@@ -612,7 +637,8 @@ template <int DV>
 __global__ void __launch_bounds__(kThreadsB, 1)
     tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                      BkvParams p) {
+                      const __grid_constant__ CUtensorMap tmDK,
+                      const __grid_constant__ CUtensorMap tmDV, BkvParams p) {
   constexpr int kPanels = DV / 64;
   constexpr int kVBytes = kTile * DV * 2;
   constexpr int kHalf = DV / 2;      // d_v columns per thread
@@ -903,21 +929,23 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tc_fence_after();
     all_ok = __syncthreads_and(ok);
   }
-  // ---- epilogue: dK (bf16, or fp32 per head), dV = intra + inter (bf16), k . dK
+  // ---- epilogue: dK (bf16, or fp32 per head), dV = intra + inter (bf16), k . dK.  No MMA
+  // reads Q or dO any more: the bf16 dK and dV tiles are staged there and stored by TMA.
   if (all_ok) {
+    uint4 vrow[kHalf / 8];  // this row's half of v, loaded first so its latency overlaps
+    if (row_live) {
+      const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + row * DV + kHalf * hh);
+#pragma unroll
+      for (int q = 0; q < kHalf / 8; ++q) vrow[q] = vsrc[q];
+    }
     float vd = 0.f;
     {
       float v0[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         tmem_ld32(tmem + lane_base + 256 + 64 * hh + 32 * c, v0);
-        if (row_live && p.dk) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dk + row * kD + 64 * hh + 32 * c);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(pack_bf16(v0[8 * q], v0[8 * q + 1]), pack_bf16(v0[8 * q + 2], v0[8 * q + 3]),
-                                pack_bf16(v0[8 * q + 4], v0[8 * q + 5]),
-                                pack_bf16(v0[8 * q + 6], v0[8 * q + 7]));
+        if (p.dk) {
+          stage_row32_bf16(Qb, r, 2 * hh + c, v0);
         } else if (row_live) {
           float4* dst = reinterpret_cast<float4*>(p.dkh + row * kD + 64 * hh + 32 * c);
 #pragma unroll
@@ -937,12 +965,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         for (int q = 0; q < 32; ++q) x[q] = 0.f;
       }
       if (row_live) {
-        const int col = kHalf * hh + 32 * c;
-        const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + row * DV + col);
-        uint4* dst = reinterpret_cast<uint4*>(p.dv + row * DV + col);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint4 w = vsrc[q];
+          const uint4 w = vrow[4 * c + q];
           const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -950,17 +975,27 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             vd = fmaf(f.x, x[8 * q + 2 * e], vd);
             vd = fmaf(f.y, x[8 * q + 2 * e + 1], vd);
           }
-          dst[q] = make_uint4(pack_bf16(a[8 * q] + x[8 * q], a[8 * q + 1] + x[8 * q + 1]),
-                              pack_bf16(a[8 * q + 2] + x[8 * q + 2], a[8 * q + 3] + x[8 * q + 3]),
-                              pack_bf16(a[8 * q + 4] + x[8 * q + 4], a[8 * q + 5] + x[8 * q + 5]),
-                              pack_bf16(a[8 * q + 6] + x[8 * q + 6], a[8 * q + 7] + x[8 * q + 7]));
         }
       }
+#pragma unroll
+      for (int q = 0; q < 32; ++q) a[q] += x[q];
+      stage_row32_bf16(Gb, r, kPanels * hh + c, a);
     }
     vd_s[hh * kTile + r] = vd;
+    fence_proxy_async_smem();
     __syncthreads();
+    if (tid == 0) {  // rows past T are clipped by the maps
+      if (p.dk) {
+        tma_store_4d(&tmDK, Qb, 0, h, t0, b);
+        tma_store_4d(&tmDK, Qb + kPanel, 64, h, t0, b);
+      }
+#pragma unroll
+      for (int pv = 0; pv < kPanels; ++pv) tma_store_4d(&tmDV, Gb + pv * kPanel, 64 * pv, h, t0, b);
+      tma_store_commit();
+    }
     if (hh == 0 && row_live && p.dck)
       p.dck[row] = colsum[r] + vd_s[r] + vd_s[kTile + r];
+    if (tid == 0) tma_store_wait_read();  // the stage must outlive the stores' reads
   } else if (tid == 0) {
     atomicOr(&g_tcb_error, 1u);
   }
@@ -1217,17 +1252,23 @@ cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, voi
   const int64_t rows = (int64_t)f.B * f.H * f.N * kD;  // TMA row coordinates are int32
   if (rows > INT32_MAX) return cudaErrorInvalidValue;
   const int dv = f.dv;
-  CUtensorMap tmQ, tmK, tmV, tmG, tmU, tmNode;
+  CUtensorMap tmQ, tmK, tmV, tmG, tmU, tmNode, tmDQ;
   if (!make_tokens_map(&tmQ, f.q, f.B, f.T, f.Hqk, kD) ||
       !make_tokens_map(&tmK, f.k, f.B, f.T, f.Hqk, kD) ||
       !make_tokens_map(&tmV, f.v, f.B, f.T, f.H, dv) ||
       !make_tokens_map(&tmG, dout, f.B, f.T, f.H, dv) || !make_rows_map(&tmU, f.U, rows, dv) ||
       !make_rows_map(&tmNode, f.nodes, rows, dv))
     return cudaErrorInvalidValue;
+  if (dq_bf16) {  // one q/k per head: dQ is [B, T, H, 128]
+    if (f.Hqk != f.H || !make_tokens_map(&tmDQ, dq_bf16, f.B, f.T, f.H, kD))
+      return cudaErrorInvalidValue;
+  } else {
+    tmDQ = tmQ;  // not used
+  }
   BqParams p;
   p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
   p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.nlg = f.nlg;
-  p.dqh = dqh; p.dq = static_cast<__nv_bfloat16*>(dq_bf16); p.dcq = dcq; p.dlam = dlam;
+  p.dqh = dqh; p.dq = dq_bf16; p.dcq = dcq; p.dlam = dlam;
   p.ahead = sm_count();
   int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
   while ((int64_t(1) << levels) < f.N) ++levels;
@@ -1246,10 +1287,10 @@ cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, voi
   const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
   if (dv == 128)
     tc_bwd_dq_kernel<128><<<tiles, kThreadsB, smem_bwd_dq(levels), s>>>(tmQ, tmK, tmV, tmG, tmU,
-                                                                         tmNode, p, levels);
+                                                                         tmNode, tmDQ, p, levels);
   else
     tc_bwd_dq_kernel<64><<<tiles, kThreadsB, smem_bwd_dq(levels), s>>>(tmQ, tmK, tmV, tmG, tmU,
-                                                                        tmNode, p, levels);
+                                                                        tmNode, tmDQ, p, levels);
   return cudaGetLastError();
 }
 
@@ -1257,18 +1298,24 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
                               void* dk_bf16, float* dck, void* dv, cudaStream_t s) {
   if (f.dk != kD || (f.dv != 64 && f.dv != 128) || f.C != kTile) return cudaErrorInvalidValue;
   const int dvw = f.dv;
-  CUtensorMap tmQ, tmK, tmV, tmG;
+  CUtensorMap tmQ, tmK, tmV, tmG, tmDK, tmDV;
   if (!make_tokens_map(&tmQ, f.q, f.B, f.T, f.Hqk, kD) ||
       !make_tokens_map(&tmK, f.k, f.B, f.T, f.Hqk, kD) ||
       !make_tokens_map(&tmV, f.v, f.B, f.T, f.H, dvw) ||
-      !make_tokens_map(&tmG, dout, f.B, f.T, f.H, dvw))
+      !make_tokens_map(&tmG, dout, f.B, f.T, f.H, dvw) ||
+      !make_tokens_map(&tmDV, dv, f.B, f.T, f.H, dvw))
     return cudaErrorInvalidValue;
+  if (dk_bf16) {  // one q/k per head: dK is [B, T, H, 128]
+    if (f.Hqk != f.H || !make_tokens_map(&tmDK, dk_bf16, f.B, f.T, f.H, kD))
+      return cudaErrorInvalidValue;
+  } else {
+    tmDK = tmK;  // not used
+  }
   BkvParams p;
   p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
   p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.R = R;
   p.v = static_cast<const __nv_bfloat16*>(f.v);
-  p.dkh = dkh; p.dk = static_cast<__nv_bfloat16*>(dk_bf16); p.dck = dck;
-  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dkh = dkh; p.dk = dk_bf16; p.dck = dck;
   p.ahead = sm_count();
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1284,9 +1331,11 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
   if (attr_err != cudaSuccess) return attr_err;
   const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
   if (dvw == 128)
-    tc_bwd_dkv_kernel<128><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, p);
+    tc_bwd_dkv_kernel<128><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, tmDK,
+                                                                    tmDV, p);
   else
-    tc_bwd_dkv_kernel<64><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, p);
+    tc_bwd_dkv_kernel<64><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, tmDK,
+                                                                   tmDV, p);
   return cudaGetLastError();
 }
 

@@ -149,16 +149,6 @@ __device__ __forceinline__ void prefetch_l2_range(const void* p, int64_t bytes) 
   }
 }
 
-// Warms L2 with the box of a 4-d tensor map at (c0, c1, c2, c3), as tma_load_4d would read
-// it; no shared memory, no completion signal.
-__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2,
-                                                int c3) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
