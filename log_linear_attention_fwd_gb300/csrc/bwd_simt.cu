@@ -640,6 +640,47 @@ __global__ void __launch_bounds__(kThreads) bwd_reduce_qk_kernel(BwdArgs A) {
   }
 }
 
+// The same sum when a position's Hqk * d_k values are few (Hqk * d_k / 4 columns of 4
+// dividing the block): the block's threads split the hg heads of each group into slices,
+// each slice summing its heads for 4 values (several loads in flight per thread), and the
+// slices are added in shared memory.  Block x: position b*T+t.
+template <typename GT>
+__global__ void __launch_bounds__(kThreads) bwd_reduce_qk_sliced_kernel(BwdArgs A, int ncol4) {
+  const FwdArgs& a = A.f;
+  const int dk = a.dk, hg = a.hg, rowlen = a.Hqk * dk;
+  const int nsl = kThreads / ncol4;
+  const int col = threadIdx.x % ncol4, sl = threadIdx.x / ncol4;
+  const int64_t bt = blockIdx.x;
+  const int i0 = col * 4;
+  const int g = i0 / dk, d = i0 - g * dk;
+  const float* sq = A.dqh + (bt * a.H + (int64_t)g * hg) * dk + d;
+  const float* sk = A.dkh + (bt * a.H + (int64_t)g * hg) * dk + d;
+  float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+#pragma unroll 4
+  for (int r = sl; r < hg; r += nsl) {
+    const float4 u = *reinterpret_cast<const float4*>(sq + (int64_t)r * dk);
+    const float4 v = *reinterpret_cast<const float4*>(sk + (int64_t)r * dk);
+    x.x += u.x; x.y += u.y; x.z += u.z; x.w += u.w;
+    y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+  }
+  __shared__ float4 red[2][kThreads];
+  red[0][threadIdx.x] = x;
+  red[1][threadIdx.x] = y;
+  __syncthreads();
+  if (sl != 0) return;
+  for (int o = 1; o < nsl; ++o) {
+    const float4 u = red[0][o * ncol4 + col], v = red[1][o * ncol4 + col];
+    x.x += u.x; x.y += u.y; x.z += u.z; x.w += u.w;
+    y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+  }
+  GT* dq = reinterpret_cast<GT*>(A.dq) + bt * rowlen + i0;
+  GT* dko = reinterpret_cast<GT*>(A.dk) + bt * rowlen + i0;
+  dq[0] = from_f32<GT>(x.x); dq[1] = from_f32<GT>(x.y);
+  dq[2] = from_f32<GT>(x.z); dq[3] = from_f32<GT>(x.w);
+  dko[0] = from_f32<GT>(y.x); dko[1] = from_f32<GT>(y.y);
+  dko[2] = from_f32<GT>(y.z); dko[3] = from_f32<GT>(y.w);
+}
+
 // dlog_a_i = sum over t >= i of (q_t . dQ_t - k_t . dK_t), in two passes over chunks of
 // kScanChunk positions of each (b, h): the chunks' sums, then each chunk's suffix scan
 // plus the sum of the chunks after it.
@@ -799,7 +840,14 @@ cudaError_t launch_bwd_finish(const BwdArgs& A, int grad_dtype, cudaStream_t s, 
     const dim3 grid_r((unsigned)((int64_t)a.B * a.T),
                       (unsigned)((rowlen + 4 * kThreads - 1) / (4 * kThreads)));
     const bool vec = a.dk % 4 == 0;
-    if (grad_dtype == LL_F32) {
+    const int ncol4 = rowlen / 4;
+    if (vec && a.hg > 1 && ncol4 <= kThreads / 2 && kThreads % ncol4 == 0) {
+      const unsigned grid_p = (unsigned)((int64_t)a.B * a.T);
+      if (grad_dtype == LL_F32)
+        bwd_reduce_qk_sliced_kernel<float><<<grid_p, kThreads, 0, s>>>(A, ncol4);
+      else
+        bwd_reduce_qk_sliced_kernel<__nv_bfloat16><<<grid_p, kThreads, 0, s>>>(A, ncol4);
+    } else if (grad_dtype == LL_F32) {
       if (vec) bwd_reduce_qk_kernel<float, true><<<grid_r, kThreads, 0, s>>>(A);
       else bwd_reduce_qk_kernel<float, false><<<grid_r, kThreads, 0, s>>>(A);
     } else {

@@ -1013,7 +1013,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // D = log decay of the tiles [c, j).  Per level the rows of Q are scaled by w and split
 // into a bf16 high part and a bf16 residual (w q to about 16 bits; dO is exact in bf16),
 // and (w Q)^T dO = hi^T dO + lo^T dO (A and B MN-major) goes into one of two TMEM buffers;
-// the previous level's product is added to R_c (fp32, float4 atomics) meanwhile.  The
+// the previous level's product is added to R_c (fp32, float4 atomics; a level-1 block is
+// the tile itself, so it is stored) meanwhile.  The
 // states feed k . dK, and with it d log a, a sum whose terms cancel, which is why w q is
 // not rounded to bf16 alone.
 
@@ -1022,7 +1023,7 @@ struct BrParams {
   const float* log_a;
   const float* lam;
   const float* lgu;   // [B*H][N] the tiles' log decays (forward workspace)
-  float* R;           // [B*H][N][d_k][d_v] mirrored states (zeroed before)
+  float* R;           // [B*H][N][d_k][d_v] mirrored states (even slots zeroed before)
   int ahead;  // tiles between this one and the next on the same SM
 };
 
@@ -1212,12 +1213,21 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       tc_fence_before();
       __syncthreads();
-      // the block's part is contiguous in R: one warp's atomics cover 512 bytes
+      // the block's part is contiguous in R: one warp's accesses cover 512 bytes.  A
+      // level-1 block (odd start) is this tile alone: stored, the others added.
       float4* dst = reinterpret_cast<float4*>(p.R + (bh * p.N + c_prev) * kD * DV);
+      if (c_prev & 1) {
 #pragma unroll 4
-      for (int i = tid; i < kD * kRowChunks; i += kThreadsB) {
-        const int d = i / kRowChunks, x = i - d * kRowChunks;
-        atomicAdd(dst + i, stage[d * kRowChunks + (x ^ (d & 7))]);
+        for (int i = tid; i < kD * kRowChunks; i += kThreadsB) {
+          const int d = i / kRowChunks, x = i - d * kRowChunks;
+          dst[i] = stage[d * kRowChunks + (x ^ (d & 7))];
+        }
+      } else {
+#pragma unroll 4
+        for (int i = tid; i < kD * kRowChunks; i += kThreadsB) {
+          const int d = i / kRowChunks, x = i - d * kRowChunks;
+          atomicAdd(dst + i, stage[d * kRowChunks + (x ^ (d & 7))]);
+        }
       }
       __syncthreads();  // the stage is the W pair the next level writes
     }
@@ -1363,7 +1373,13 @@ cudaError_t launch_tc_bwd_rstate(const FwdArgs& f, const void* dout, float* R, c
                                       (int)smem_bwd_rstate(kMaxChunkLevels - 1));
   });
   if (attr_err != cudaSuccess) return attr_err;
-  cudaError_t e = cudaMemsetAsync(R, 0, sizeof(float) * (size_t)f.B * f.H * f.N * kD * f.dv, s);
+  // Only blocks with an even start are sums over several tiles; the odd ones (level 1) are
+  // stored whole by their one tile.  With N even the even slots are every other one.
+  const size_t slot = sizeof(float) * (size_t)kD * f.dv;
+  const size_t slots = (size_t)f.B * f.H * f.N;
+  cudaError_t e = (f.N % 2 == 0)
+                      ? cudaMemset2DAsync(R, 2 * slot, 0, slot, slots / 2, s)
+                      : cudaMemsetAsync(R, 0, slot * slots, s);
   if (e != cudaSuccess) return e;
   const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
   if (f.dv == 128)
