@@ -89,17 +89,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Writes 32 fp32 values as bf16 into columns [32c, 32c+32) of row r of a tile of 128-byte
-// swizzled [128][64] panels (the layout a tokens map's TMA load or store uses).
-__device__ __forceinline__ void stage_row32_bf16(uint8_t* buf, int r, int c, const float* v) {
-  uint8_t* panel = buf + (c >> 1) * kPanel;
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    *reinterpret_cast<uint4*>(panel + sw128_offset(r, (c & 1) * 4 + q)) =
-        make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
-                   pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
-}
-
 // Warms L2 with the box of a 4-d tensor map at (c0, c1, c2, c3), as tma_load_4d would read
 // it; no shared memory, no completion signal.
 __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2,
@@ -110,7 +99,8 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, 
                : "memory");
 }
 
-// 32 fp32 values as bf16 into columns [32c, 32c+32) of row r of a swizzled tile.
+// 32 fp32 values as bf16 into columns [32c, 32c+32) of row r of a tile of 128-byte
+// swizzled [128][64] panels (the layout of a tokens map's TMA loads and stores).
 __device__ __forceinline__ void put_row32_bf16(uint8_t* buf, int r, int c, const float* v) {
   uint8_t* panel = buf + (c >> 1) * kPanel;
 #pragma unroll
@@ -531,8 +521,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       if (p.dcq) p.dcq[row] = qd;
     }
     if (p.dq) {  // no MMA reads Q any more: stage dQ there and store it with TMA
-      stage_row32_bf16(Qb, r, 2 * hh, dq);
-      stage_row32_bf16(Qb, r, 2 * hh + 1, dq + 32);
+      put_row32_bf16(Qb, r, 2 * hh, dq);
+      put_row32_bf16(Qb, r, 2 * hh + 1, dq + 32);
       fence_proxy_async_smem();
       __syncthreads();
       if (tid == 0) {  // rows past T are clipped by the map
@@ -945,7 +935,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       for (int c = 0; c < 2; ++c) {
         tmem_ld32(tmem + lane_base + 256 + 64 * hh + 32 * c, v0);
         if (p.dk) {
-          stage_row32_bf16(Qb, r, 2 * hh + c, v0);
+          put_row32_bf16(Qb, r, 2 * hh + c, v0);
         } else if (row_live) {
           float4* dst = reinterpret_cast<float4*>(p.dkh + row * kD + 64 * hh + 32 * c);
 #pragma unroll
@@ -979,7 +969,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
 #pragma unroll
       for (int q = 0; q < 32; ++q) a[q] += x[q];
-      stage_row32_bf16(Gb, r, kPanels * hh + c, a);
+      put_row32_bf16(Gb, r, kPanels * hh + c, a);
     }
     vd_s[hh * kTile + r] = vd;
     fence_proxy_async_smem();
