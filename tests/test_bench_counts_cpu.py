@@ -92,3 +92,23 @@ def test_traffic_record_dropped_when_source_changes(tmp_path, monkeypatch):
         f.write("\n// edited\n")
     assert bench.load_traffic("tc_forward_kernel") is None
     assert bench.load_traffic("no_such_kernel") is None
+
+
+@pytest.mark.parametrize("T,dk,dv", [(512, 8, 4), (1024, 16, 8)])
+def test_backward_counts_match_brute_force(T, dk, dv):
+    """The backward at C = 64: per causal pair in a chunk q.k, dO.v and the dQ, dK, dV
+    updates; per chunk the recomputed state; per (chunk, inter level) the dQ readout with
+    its dlambda dot, the mirrored part and the dK, dV readouts.  Bytes: the forward's
+    inputs and dO read once, their gradients written once."""
+    C = 64
+    cfg = W.FwdConfig("count", 1, 2, T, dk, dv, C, (T - 1).bit_length() + 1, "bf16", True,
+                      "softplus")
+    nbytes, flops = bench.bwd_algorithmic(cfg)
+    N = T // C
+    pairs = sum(1 for j in range(N) for t in range(C) for s in range(t + 1))
+    inter = sum(_inter_levels_of_chunk(j, C) for j in range(N))
+    per_pair = 2 * dk + 2 * dv + 2 * dk + 2 * dk + 2 * dv
+    per_level = 4 * 2 * C * dk * dv + 2 * C * dk
+    assert flops == cfg.B * cfg.H * (pairs * per_pair + N * 2 * C * dk * dv + inter * per_level)
+    tok = cfg.B * T * cfg.H
+    assert nbytes == 2 * (tok * (2 * dk + 2 * dv) * 2 + tok * 4 + tok * cfg.L * 4)
