@@ -207,7 +207,8 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
  *   contents match the inputs; that is the caller's contract.  fwd_workspace_bytes must
  *   be at least loglinear_fwd_workspace_size() for the forward's arguments
  *   (LL_ERR_WORKSPACE); a non-NULL fwd_workspace on the CUDA-core path is
- *   LL_ERR_UNSUPPORTED.
+ *   LL_ERR_UNSUPPORTED.  An empty call (B, T or H zero) returns LL_OK before any of
+ *   these checks of pointers and workspaces.
  * workspace: device scratch of at least loglinear_bwd_workspace_size() bytes, 256-byte
  * aligned (recomputed forward states, per-head q and k gradients).
  * Errors: LL_ERR_INVALID (null pointer, negative size, dlog_a NULL with log_a given),

@@ -324,9 +324,9 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
   int64_t N, n_tc;
   const int st = check_bwd(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, path, &N, &n_tc);
   if (st != LL_OK) return st;
+  if (B == 0 || T == 0 || H == 0) return LL_OK;
   if (fwd_workspace && n_tc == 0) return LL_ERR_UNSUPPORTED;  // only the tensor-core path
                                                               // reads a forward's states
-  if (B == 0 || T == 0 || H == 0) return LL_OK;
   if (!q || !k || !v || !lambda || !dout || !dq || !dk_out || !dv_out || !dlambda)
     return LL_ERR_INVALID;
   if (log_a && !dlog_a) return LL_ERR_INVALID;

@@ -214,6 +214,8 @@ def test_bwd_validation_codes(L):
     assert bwd(ws=ctypes.c_void_p(0x1010), wsb=1 << 40) == L.LL_ERR_ALIGN
     assert bwd(T=0, q=None, k=None, v=None, lam=None, dout=None, dq=None, dk=None, dv=None,
                dlam=None) == L.LL_OK
+    # nothing to compute: a forward's workspace given to an empty call is not an error
+    assert bwd(T=0, path=L.LL_PATH_TC, fws=FAKE, fwsb=1 << 40, **tc_kw) == L.LL_OK
     sz = L.bwd_workspace_size(1, 64, 2, 2, 16, 16, 7, L.LL_F32, L.LL_F32)
     assert sz >= 2 * (1 * 2 * 2 * 16 * 16 * 4) + 2 * 64 * 2 * 16 * 4   # states + per-head dq, dk
     # the tensor-core dQ adds a forward's workspace and an output scratch
