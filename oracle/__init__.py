@@ -16,3 +16,10 @@ from .loglinear_oracle import (  # noqa: F401
     recurrence,
     states_from_buckets,
 )
+from .gdn_oracle import (  # noqa: F401
+    gated_deltanet_recurrent,
+    gdn_decode_step,
+    gdn_direct,
+    gdn_recurrence,
+    gdn_states_from_buckets,
+)

@@ -101,10 +101,16 @@ def lssb(t: int) -> int:
 
 
 def _f64(x):
+    """Input upcast to fp64 NumPy.  Torch tensors of 16-bit types (which NumPy lacks) go
+    through fp32 exactly; fp32 and fp64 tensors convert directly, so fp64 inputs keep
+    their precision."""
     if x is None:
         return None
     if hasattr(x, "detach"):            # torch tensor (any dtype, incl. bfloat16)
-        x = x.detach().cpu().float().numpy()
+        x = x.detach().cpu()
+        if x.element_size() < 4:
+            x = x.float()
+        x = x.numpy()
     return np.asarray(x, dtype=np.float64)
 
 

@@ -145,6 +145,32 @@ def make_sparse_int_inputs(B, T, H, d, L, onehot_level: int, seed: int = 0, dv=N
     return dict(q=q.to(bf), k=k.to(bf), v=v.to(bf), log_a=None, lam=lam)
 
 
+def make_gdn_inputs(cfg: FwdConfig):
+    """Log-Linear Gated DeltaNet inputs: the forward recipe of ``cfg`` (q, v, log a, lambda),
+    with each k scaled to unit length (the gated delta rule's keys are L2-normalised, which
+    keeps I - beta k k^T a contraction) and a write strength beta = sigmoid(N(0,1)) per
+    (b, t, h), drawn after the others.  Returns dict(q, k, v, log_a, beta, lam)."""
+    x = make_fwd_inputs(cfg)
+    g = _gen(cfg.seed + 7001)
+    k = x["k"].float()
+    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-6)
+    beta = torch.sigmoid(torch.randn(cfg.B, cfg.T, cfg.H, generator=g))
+    return dict(q=x["q"], k=k.to(x["k"].dtype).contiguous(), v=x["v"], log_a=x["log_a"],
+                beta=beta.contiguous(), lam=x["lam"])
+
+
+def make_gdn_decode_step_inputs(cfg: DecodeConfig):
+    """The new token of a Gated DeltaNet decode step at position cfg.t: the decode recipe
+    with unit-length k and beta = sigmoid(N(0,1)) [B, H]."""
+    x = make_decode_step_inputs(cfg)
+    g = _gen(cfg.seed + 7002)
+    k = x["k"].float()
+    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-6)
+    beta = torch.sigmoid(torch.randn(cfg.B, cfg.H, generator=g))
+    return dict(q=x["q"], k=k.to(x["k"].dtype).contiguous(), v=x["v"], log_a=x["log_a"],
+                beta=beta.contiguous(), lam=x["lam"])
+
+
 def make_decode_tokens(cfg: DecodeConfig, b: int, h: int, T: int):
     """Prefill stream of one (b, h): k [T,dk], v [T,dv] (cfg dtype), log_a [T] fp32.
 
