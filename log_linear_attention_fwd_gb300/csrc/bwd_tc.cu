@@ -1231,15 +1231,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 }  // namespace
 
+// SMs of the current device (queried per call: the library may run on several devices).
 static int sm_count() {
-  static const int sms = [] {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      n = 0;
-    return n;
-  }();
-  return sms;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    n = 0;
+  return n;
 }
 
 bool tc_bwd_dq_supported(int64_t dk, int64_t dv, int in_dtype, int grad_dtype) {
@@ -1272,17 +1270,13 @@ cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, voi
   p.ahead = sm_count();
   int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
   while ((int64_t(1) << levels) < f.N) ++levels;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(tc_bwd_dq_kernel<128>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem_bwd_dq(kMaxChunkLevels - 1));
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(tc_bwd_dq_kernel<64>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem_bwd_dq(kMaxChunkLevels - 1));
-  });
+  // The shared-memory limit is an attribute of the function on each device: set it
+  // on every launch (a host-side call), so that every device the library runs on has it.
+  const cudaError_t attr_err =
+      dv == 128 ? cudaFuncSetAttribute(tc_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bwd_dq(kMaxChunkLevels - 1))
+                : cudaFuncSetAttribute(tc_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bwd_dq(kMaxChunkLevels - 1));
   if (attr_err != cudaSuccess) return attr_err;
   const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
   if (dv == 128)
@@ -1317,17 +1311,13 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
   p.v = static_cast<const __nv_bfloat16*>(f.v);
   p.dkh = dkh; p.dk = dk_bf16; p.dck = dck;
   p.ahead = sm_count();
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(tc_bwd_dkv_kernel<128>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem_bwd_dkv());
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(tc_bwd_dkv_kernel<64>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem_bwd_dkv());
-  });
+  // The shared-memory limit is an attribute of the function on each device: set it
+  // on every launch (a host-side call), so that every device the library runs on has it.
+  const cudaError_t attr_err =
+      dvw == 128 ? cudaFuncSetAttribute(tc_bwd_dkv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bwd_dkv())
+                : cudaFuncSetAttribute(tc_bwd_dkv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bwd_dkv());
   if (attr_err != cudaSuccess) return attr_err;
   const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
   if (dvw == 128)
@@ -1351,17 +1341,13 @@ cudaError_t launch_tc_bwd_rstate(const FwdArgs& f, const void* dout, float* R, c
   p.ahead = sm_count();
   int levels = 0;
   while ((int64_t(1) << levels) < f.N) ++levels;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(tc_bwd_rstate_kernel<128>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem_bwd_rstate(kMaxChunkLevels - 1));
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(tc_bwd_rstate_kernel<64>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem_bwd_rstate(kMaxChunkLevels - 1));
-  });
+  // The shared-memory limit is an attribute of the function on each device: set it
+  // on every launch (a host-side call), so that every device the library runs on has it.
+  const cudaError_t attr_err =
+      f.dv == 128 ? cudaFuncSetAttribute(tc_bwd_rstate_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bwd_rstate(kMaxChunkLevels - 1))
+                : cudaFuncSetAttribute(tc_bwd_rstate_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bwd_rstate(kMaxChunkLevels - 1));
   if (attr_err != cudaSuccess) return attr_err;
   // Only blocks with an even start are sums over several tiles; the odd ones (level 1) are
   // stored whole by their one tile.  With N even the even slots are every other one.

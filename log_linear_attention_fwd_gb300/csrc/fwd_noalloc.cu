@@ -11,14 +11,19 @@
 //   * Every GPU on which the library's device code is loaded holds this array until the
 //     process exits.
 //   * The first call on a device, with that device current, looks the array's device
-//     address up (cudaGetSymbolAddress) and caches it; that first call should come before
-//     any stream capture.
+//     address up (cudaGetSymbolAddress, which also loads the module on that device) and
+//     caches it together with the unique ID of the current CUDA context; that first call
+//     should come before any stream capture.  A later call under another context (after
+//     cudaDeviceReset, or once the application replaced the primary context) looks the
+//     address up again, since the module, and the array with it, moved.
 //   * All calls share the one array, and it keeps the last call's contents.  The forward
 //     writes every scratch entry before it reads it, so nothing needs clearing between
 //     calls; but two calls whose work overlaps on the GPU (different streams, or different
 //     host threads) race on the array and give wrong results.  Serialise them.
 //   * Problems whose scratch would exceed kNoallocScratchBytes are rejected with
 //     LL_ERR_WORKSPACE before anything is launched.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "ll_internal.cuh"
@@ -30,11 +35,42 @@ constexpr size_t kNoallocScratchBytes = LL_FWD_NOALLOC_SCRATCH_BYTES;  // 32 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device.  In host code the
-// array's name only stands in for the symbol; it is not a device address.
+// Device address of g_noalloc_scratch, looked up once per device and context.  In host
+// code the array's name only stands in for the symbol; it is not a device address.
 constexpr int kMaxDevices = 128;
+struct ScratchAddr {
+  unsigned long long ctx_id;  // unique ID of the context the address belongs to (0: none)
+  void* addr;
+};
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
+
+// Unique ID of the calling thread's current CUDA context, or 0 when there is none or the
+// driver does not offer the query.  Context IDs are never reused within a process, unlike
+// context handles.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 cudaError_t scratch_on_current_device(void** addr) {
   int dev = -1;
@@ -42,13 +78,17 @@ cudaError_t scratch_on_current_device(void** addr) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  const unsigned long long id = current_context_id();
+  ScratchAddr& c = g_scratch_addr[dev];
+  if (!c.addr || id == 0 || c.ctx_id != id) {
+    // first call on this device, or another context than the cached address belongs to
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    c.addr = p;
+    c.ctx_id = current_context_id();  // the lookup made a context current if none was
   }
-  *addr = g_scratch_addr[dev];
+  *addr = c.addr;
   return cudaSuccess;
 }
 

@@ -10,6 +10,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from tests.helpers import TOL_BF16, TOL_F32, rel_l2
 
@@ -26,27 +27,54 @@ def _dev(x):
     return {k: (None if v is None else v.cuda()) for k, v in x.items()}
 
 
+def _call_noalloc(LL, d, cfg, path, out):
+    return LL.lib().loglinear_fwd_noalloc(
+        ctypes.c_void_p(d["q"].data_ptr()), ctypes.c_void_p(d["k"].data_ptr()),
+        ctypes.c_void_p(d["v"].data_ptr()),
+        None if d["log_a"] is None else ctypes.c_void_p(d["log_a"].data_ptr()),
+        ctypes.c_void_p(d["lam"].data_ptr()), ctypes.c_void_p(out.data_ptr()),
+        cfg.B, cfg.T, cfg.H, cfg.H, cfg.dk, cfg.dv, cfg.L, cfg.C, LL._binding._dtype_code(d["q"]),
+        LL._binding._dtype_code(out), LL._binding.PATHS[path],
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
 @pytest.mark.parametrize("path,cfg", CASES, ids=[c[0] for c in CASES])
-def test_noalloc_matches_workspace_entry_point(path, cfg):
+def test_noalloc_matches_oracle_and_workspace_entry_point(path, cfg):
+    """Two calls in a row on different inputs: each result against the CPU oracle (the
+    definition) and against loglinear_fwd with a caller workspace (same kernels)."""
     import log_linear_attention_fwd_gb300 as LL
     tol = TOL_F32 if cfg.dtype == "f32" else TOL_BF16
-    for call, seed in enumerate((11, 12)):          # two calls in a row, different inputs
-        d = _dev(W.make_fwd_inputs(cfg.with_(seed=seed)))
-        want = LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C, path=path)
-        got = torch.empty_like(want)
-        st = LL.lib().loglinear_fwd_noalloc(
-            ctypes.c_void_p(d["q"].data_ptr()), ctypes.c_void_p(d["k"].data_ptr()),
-            ctypes.c_void_p(d["v"].data_ptr()),
-            None if d["log_a"] is None else ctypes.c_void_p(d["log_a"].data_ptr()),
-            ctypes.c_void_p(d["lam"].data_ptr()), ctypes.c_void_p(got.data_ptr()),
-            cfg.B, cfg.T, cfg.H, cfg.H, cfg.dk, cfg.dv, cfg.L, cfg.C, LL._binding._dtype_code(d["q"]),
-            LL._binding._dtype_code(got), LL._binding.PATHS[path],
-            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    for call, seed in enumerate((11, 12)):
+        x = W.make_fwd_inputs(cfg.with_(seed=seed))
+        d = _dev(x)
+        want_ws = LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C, path=path)
+        got = torch.empty_like(want_ws)
+        st = _call_noalloc(LL, d, cfg, path, got)
         assert st == 0, LL.status_string(st)
         torch.cuda.synchronize()
-        err = rel_l2(got, want)
-        print(f"noalloc {path} call {call}: rel_l2 vs loglinear_fwd = {err:.3e}")
-        assert err <= tol
+        assert LL.device_error() == 0
+        want = oracle.forward_direct(x["q"], x["k"], x["v"], x["log_a"], x["lam"])
+        err_oracle, err_ws = rel_l2(got.cpu(), want), rel_l2(got, want_ws)
+        print(f"noalloc {path} call {call}: rel_l2 vs oracle = {err_oracle:.3e}, "
+              f"vs loglinear_fwd = {err_ws:.3e}")
+        assert err_oracle <= tol and err_ws <= tol
+
+
+@pytest.mark.parametrize("path,cfg", CASES, ids=[c[0] for c in CASES])
+def test_noalloc_allocates_no_device_memory(path, cfg):
+    """After a first call (which loads the module and with it the fixed array), further
+    calls leave the device's free memory exactly where it was."""
+    import log_linear_attention_fwd_gb300 as LL
+    d = _dev(W.make_fwd_inputs(cfg))
+    out = torch.empty(cfg.B, cfg.T, cfg.H, cfg.dv, device="cuda", dtype=d["q"].dtype)
+    assert _call_noalloc(LL, d, cfg, path, out) == 0
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(5):
+        assert _call_noalloc(LL, d, cfg, path, out) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert LL.device_error() == 0
 
 
 def test_noalloc_rejects_oversized_problem():
