@@ -17,6 +17,7 @@ bounded sample of the same forward workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -132,15 +133,21 @@ def fp32_alu_peak():
     return 152 * 128 * 2 * 2.07e9 / 1e12
 
 
+def decode_levels_written(cfg):
+    """Levels the step changes: every level that held data (decayed, merged or cleared)
+    and the level lssb(t)+1 that receives the merge."""
+    t = cfg.t
+    pre = W.nonempty_levels_before(t, cfg.L)
+    l = (t & -t).bit_length() - 1
+    return len(set(pre) | {l + 1})
+
+
 def decode_algorithmic(cfg):
     """Bytes of the levels the step must read (non-empty after t-1) and write (every
     level that changes), fp32."""
     lvl_bytes = cfg.dk * cfg.dv * 4
-    t = cfg.t
-    pre = W.nonempty_levels_before(t, cfg.L)
-    l = (t & -t).bit_length() - 1
-    written = set(pre) | {l + 1}            # decayed, merged, cleared or new
-    return cfg.B * cfg.H * lvl_bytes * (len(pre) + len(written))
+    pre = W.nonempty_levels_before(cfg.t, cfg.L)
+    return cfg.B * cfg.H * lvl_bytes * (len(pre) + decode_levels_written(cfg))
 
 
 # ---------------------------------------------------------------- ranks
@@ -242,17 +249,64 @@ def oracle_sample(cfg, seconds, seed=0):
     pairs_total = cfg.B * cfg.H * T * (T + 1) / 2
     t_total = el * pairs_total / pairs_done
     tok_s = cfg.B * T / t_total
-    threads = torch.get_num_threads()
-    try:
-        import threadpoolctl
-        info = threadpoolctl.threadpool_info()
-        threads = max([i.get("num_threads", 1) for i in info] + [1])
-    except Exception:
-        threads = os.cpu_count()
+    threads = _blas_threads()
     desc = (f"oracle forward_direct (fp64 NumPy) on {rows_done} random query rows of one head "
             f"of {cfg.name} in {el:.1f} s, extrapolated by (query, source) pair count to "
             f"B{cfg.B} H{cfg.H} T{T}")
     return tok_s, desc, threads
+
+
+def oracle_decode_sample(dcfg, seconds):
+    """Times the oracle's lssb decode step (fp64 NumPy) on a few (b, h) of the decode
+    workload until about `seconds` of CPU time; returns (tokens/s extrapolated to all
+    B x H, sample description, threads used)."""
+    import oracle
+    inp = W.make_decode_step_inputs(dcfg)
+    nb = 2                                    # batch rows per call: 2 x H (b, h) pairs
+    sub = dataclasses.replace(dcfg, B=nb)
+    S = W.make_random_state(sub, dcfg.t, seed=3, scale=0.05).double().numpy()
+    x = {k: (None if v is None else v[:nb]) for k, v in inp.items()}
+    calls, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds or calls == 0:
+        oracle.decode_step(S, x["q"], x["k"], x["v"], x["log_a"], x["lam"], dcfg.t)
+        calls += 1
+    el = time.perf_counter() - t0
+    per_pair = el / (calls * nb * dcfg.H)
+    t_step = per_pair * dcfg.B * dcfg.H
+    desc = (f"oracle decode_step (fp64 NumPy) on {nb} x {dcfg.H} (b, h) pairs at t={dcfg.t}, "
+            f"{calls} calls in {el:.1f} s, extrapolated by pair count to B{dcfg.B} H{dcfg.H}")
+    return dcfg.B / t_step, desc, _blas_threads()
+
+
+def oracle_gdn_decode_sample(dcfg, seconds):
+    """Times the oracle's Log-Linear Gated DeltaNet decode step (fp64 NumPy) on a few (b, h)
+    of the decode workload; returns (tokens/s extrapolated to all B x H, description,
+    threads used)."""
+    import oracle
+    inp = W.make_gdn_decode_step_inputs(dcfg)
+    nb = 2
+    sub = dataclasses.replace(dcfg, B=nb)
+    S = W.make_random_state(sub, dcfg.t, seed=3, scale=0.05).double().numpy()
+    x = {k: (None if v is None else v[:nb]) for k, v in inp.items()}
+    calls, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds or calls == 0:
+        oracle.gdn_decode_step(S, x["q"], x["k"], x["v"], x["log_a"], x["beta"], x["lam"], dcfg.t)
+        calls += 1
+    el = time.perf_counter() - t0
+    t_step = el / (calls * nb * dcfg.H) * dcfg.B * dcfg.H
+    desc = (f"oracle gdn_decode_step (fp64 NumPy) on {nb} x {dcfg.H} (b, h) pairs at "
+            f"t={dcfg.t}, {calls} calls in {el:.1f} s, extrapolated by pair count to "
+            f"B{dcfg.B} H{dcfg.H}")
+    return dcfg.B / t_step, desc, _blas_threads()
+
+
+def _blas_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] + [1])
+    except Exception:
+        return os.cpu_count()
 
 
 # ---------------------------------------------------------------- our implementation
@@ -272,11 +326,14 @@ def run_ours(args, rank, world, local_rank):
     path = LL.resolve_path(cfg.dk, cfg.dv, cfg.C, in_code)
     ws = torch.empty(LL.fwd_workspace_size(cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv, cfg.C, in_code),
                      device=dev, dtype=torch.uint8)
-    # decode inputs: state generated on the device from a seeded generator (timing only)
+    # decode inputs: state generated on the device from a seeded generator (timing only);
+    # every timed step starts from this same state (restored outside the events), so each
+    # step is the t = 12345 step on the state after position 12344
     gen = torch.Generator(device=dev).manual_seed(1234)
-    state = torch.zeros(dcfg.B, dcfg.H, dcfg.L, dcfg.dk, dcfg.dv, device=dev)
+    state0 = torch.zeros(dcfg.B, dcfg.H, dcfg.L, dcfg.dk, dcfg.dv, device=dev)
     for lv in W.nonempty_levels_before(dcfg.t, dcfg.L):
-        state[:, :, lv].normal_(0.0, 0.05, generator=gen)
+        state0[:, :, lv].normal_(0.0, 0.05, generator=gen)
+    state = torch.empty_like(state0)
     dinp = {k: (None if v is None else v.to(dev)) for k, v in W.make_decode_step_inputs(dcfg).items()}
     dout = torch.empty(dcfg.B, dcfg.H, dcfg.dv, device=dev, dtype=torch.float32)
     flush = torch.empty(512 << 20, device=dev, dtype=torch.uint8)
@@ -284,6 +341,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def one_step(ev_f, ev_d):
+        state.copy_(state0)  # restore the decode state (before the L2 flush and the events)
+        flush.zero_()
         n_k = LL.loglinear_fwd_with_events(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C,
                                            ev_f, out, ws)
         ev_d[0].record(stream)
@@ -298,7 +357,6 @@ def run_ours(args, rank, world, local_rank):
     clocks = ClockSampler(local_rank)
     clocks.start()
     for _ in range(args.warmup):
-        flush.zero_()
         one_step(mk(n_ev), mk(2))
     torch.cuda.synchronize()
     if world > 1:
@@ -307,7 +365,6 @@ def run_ours(args, rank, world, local_rank):
     wall0 = time.perf_counter()
     n_kernels = 0
     for ef, ed in evs:
-        flush.zero_()
         n_kernels = one_step(ef, ed)
     torch.cuda.synchronize()
     if world > 1:
@@ -351,7 +408,12 @@ def run_ours(args, rank, world, local_rank):
                            "algorithmic_bytes": dbytes, "peak_source": peaks["src"],
                            "traffic": None},
               "config": {"workload": dcfg.name, "B": dcfg.B, "H": dcfg.H, "dk": dcfg.dk,
-                         "dv": dcfg.dv, "L": dcfg.L, "t": dcfg.t, "state": "fp32"}}
+                         "dv": dcfg.dv, "L": dcfg.L, "t": dcfg.t, "state": "fp32",
+                         "levels_read": len(W.nonempty_levels_before(dcfg.t, dcfg.L)),
+                         "levels_written": decode_levels_written(dcfg),
+                         "state_restored": "every timed step starts from the same state "
+                                           "after t-1 (device copy outside the events)"}}
+    gdn = measure_gdn_decode(LL, dcfg, state0, state, flush, peaks)
     e2e = measure_e2e(LL, cfg, x, dev, ws, args)
     prefill = measure_prefill(LL, cfg, d, out, ws, flush, peaks)
     del ws
@@ -371,6 +433,7 @@ def run_ours(args, rank, world, local_rank):
            "fwd_ms": fwd_mean * 1e3, "fwd_stage_us": dict(zip(stage_names, [s * 1e6 for s in stage_mean])),
            "roofline": roofline, "roofline_fwd": roofline_fwd, "decode": decode, "e2e": e2e,
            "prefill": prefill, "backward": backward, "benchmark_shape": bench_shape,
+           "gdn_decode": gdn,
            "gpu_launches": args.steps * (n_kernels + 1), "clocks": clk,
            "wall_s_timed_region": wall}
     return res
@@ -392,6 +455,38 @@ def stage_bytes(cfg, path, name):
     if name.endswith("level_scan"):
         return st * 4 + st * node_e
     return qkv + tok * 4 + tok * cfg.L * 4 + st * node_e + tok * cfg.dv * e
+
+
+def measure_gdn_decode(LL, dcfg, state0, state, flush, peaks, reps=20):
+    """The Log-Linear Gated DeltaNet decode step on the decode workload's shape (B128 H16
+    d128 L15 fp32 states, bf16 tokens, t = 12345): median of `reps` steps, each from the
+    same state after t-1 (restored by a device copy, then L2 flushed, both outside the
+    events).  With the delta rule every level that holds data changes, so the bytes are the
+    decode step's: the non-empty levels read and the changed levels written."""
+    dev = state.device
+    inp = {k: (None if v is None else v.to(dev)) for k, v in W.make_gdn_decode_step_inputs(dcfg).items()}
+    out = torch.empty(dcfg.B, dcfg.H, dcfg.dv, device=dev, dtype=torch.float32)
+    ts = []
+    for i in range(reps + 3):
+        state.copy_(state0)
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        LL.loglinear_gdn_decode_step(state, inp["q"], inp["k"], inp["v"], inp["log_a"],
+                                     inp["beta"], inp["lam"], dcfg.t, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(ts)
+    dbytes = decode_algorithmic(dcfg)
+    return {"workload": f"{dcfg.name}: loglinear_gdn_decode_step B{dcfg.B} H{dcfg.H} "
+                        f"dk=dv={dcfg.dk} L{dcfg.L} t={dcfg.t}, fp32 states, bf16 tokens",
+            "tokens_per_s": dcfg.B / t, "us_per_step": t * 1e6,
+            "roofline": {"kernel": "gdn_decode_kernel", "bound": "hbm",
+                         "achieved": dbytes / t / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": dbytes / t / 1e9 / peaks["hbm"], "algorithmic_bytes": dbytes,
+                         "peak_source": peaks["src"], "traffic": None}}
 
 
 def measure_prefill(LL, cfg, d, out, ws, flush, peaks, reps=10):
@@ -713,6 +808,12 @@ def main():
         tok_s, desc, thr = oracle_sample(cfg, args.cpu_seconds)
         res["cpu_baseline"] = {"value": tok_s, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                "sample": desc}
+        dtok_s, ddesc, dthr = oracle_decode_sample(W.DECODE_CONFIG, max(2.0, args.cpu_seconds / 3))
+        res["decode"]["cpu_baseline"] = {"value": dtok_s, "unit": "tokens/s", "cores": dthr,
+                                         "kind": "oracle", "sample": ddesc}
+        gtok_s, gdesc, gthr = oracle_gdn_decode_sample(W.DECODE_CONFIG, max(2.0, args.cpu_seconds / 3))
+        res["gdn_decode"]["cpu_baseline"] = {"value": gtok_s, "unit": "tokens/s", "cores": gthr,
+                                             "kind": "oracle", "sample": gdesc}
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
