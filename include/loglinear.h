@@ -14,8 +14,8 @@
  * (first page, section 层级判定算法), equal to the bit length of (t XOR s).
  *
  * Conventions shared by every entry point:
- *   - All tensor arguments are DEVICE pointers to dense row-major arrays (no strides),
- *     owned by the caller.  The library never allocates, frees or synchronises; all work
+ *   - All tensor arguments are DEVICE pointers to dense row-major arrays, owned by the
+ *     caller (loglinear_fwd_strided takes strided q, k, v and out).  The library never allocates, frees or synchronises; all work
  *     is enqueued on `stream` (NULL = the legacy default stream) and is asynchronous.
  *   - Sizes are element counts.  Positions t are 0-based and must fit in int32.
  *   - Every call validates its arguments on the host before launching anything and
@@ -117,6 +117,36 @@ LL_API int loglinear_fwd(const void* q, const void* k, const void* v, const floa
                   ll_stream_t stream);
 
 /*
+ * Element strides of a [B, T, Hx, width] tensor whose feature dimension (width) is
+ * contiguous: the distance between consecutive batch entries, positions and heads.  A
+ * dense tensor has {T*Hx*width, Hx*width, width}.  A q, k or v slice of a fused
+ * [B, T, H, 3*d] projection has {T*H*3d, H*3d, 3d}.
+ */
+typedef struct {
+  int64_t b, t, h;
+} ll_strides;
+
+/*
+ * loglinear_fwd on strided q, k, v and out (each pointer addresses element [0, 0, 0, 0];
+ * a NULL stride descriptor means dense).  log_a and lambda stay dense.  Same operation,
+ * workspace and errors as loglinear_fwd, and in addition:
+ *   LL_ERR_INVALID      a negative stride, or out strides under which two output
+ *                       elements would share an address;
+ *   LL_ERR_ALIGN        tensor-core path: a stride of a dimension longer than 1 that is not
+ *                       a multiple of 16 bytes (8 bf16 or 4 fp32 elements), as TMA requires;
+ *   LL_ERR_UNSUPPORTED  tensor-core path: a zero stride on a dimension longer than 1.
+ * Strides of dimensions of size 1 are ignored.
+ */
+LL_API int loglinear_fwd_strided(const void* q, const ll_strides* q_strides, const void* k,
+                                 const ll_strides* k_strides, const void* v,
+                                 const ll_strides* v_strides, const float* log_a,
+                                 const float* lambda, void* out, const ll_strides* out_strides,
+                                 int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk,
+                                 int64_t dv, int64_t L, int chunk, int in_dtype, int out_dtype,
+                                 int path, void* workspace, size_t workspace_bytes,
+                                 ll_stream_t stream);
+
+/*
  * loglinear_fwd with per-kernel timing: identical work and results, plus cudaEventRecord
  * of stage_events[0] before the first kernel and of stage_events[i+1] after kernel i, on
  * `stream`.  stage_events is a host array of n_events cudaEvent_t handles created by the
@@ -176,6 +206,37 @@ LL_API int loglinear_decode_step(float* state, const void* q, const void* k, con
                           const float* log_a, const float* lambda, int64_t t, void* out,
                           int64_t B, int64_t H, int64_t Hqk, int64_t dk, int64_t dv,
                           int64_t L, int in_dtype, int out_dtype, ll_stream_t stream);
+
+/*
+ * One decode step of Log-Linear Gated DeltaNet at position t for every (b, h).  The pages
+ * build the log-linear form of a model by keeping its transition and composing its mask
+ * with the Fenwick mask (page "算力终结者来了！…", section 对Mamba-2和门控DeltaNet的对数线性
+ * 推广; first page, section 与已有模型的组合); the transition is the published gated delta
+ * rule (Yang, Kautz and Hatamizadeh, "Gated Delta Networks", 2024).  With the state
+ * stored [d_k][d_v] and A_t = alpha_t (I - beta_t k_t k_t^T), alpha_t = exp(log_a_t):
+ *   every level that holds data after t-1:  S^(j) <- A_t S^(j);  then, with l = lssb(t),
+ *   S^(l+1) <- sum_{j<=l} S^(j);  S^(1..l) <- 0;  S^(0) <- beta_t k_t v_t^T;
+ *   out = sum_j lambda[j] * S^(j)^T q_t   (non-empty levels only).
+ * At t = 0 the state is (re)initialised: S^(0) <- beta_0 k_0 v_0^T, every other level <- 0.
+ * Lambda constant across levels gives plain Gated DeltaNet; without the k k^T term it is
+ * loglinear_decode_step with v scaled by beta.
+ *   state   [B, H, L, dk, dv] fp32, updated in place, 16-byte aligned (levels that are
+ *           empty after t-1, other than lssb(t)+1, are neither read nor written)
+ *   q, k    [B, Hqk, dk] in_dtype (q/k heads shared as in loglinear_fwd); k is expected
+ *           to have unit length, as the gated delta rule assumes (not checked)
+ *   v       [B, H, dv]   in_dtype
+ *   log_a   [B, H] fp32 or NULL (alpha = 1);   beta [B, H] fp32;   lambda [B, H, L] fp32
+ *   out     [B, H, dv]   out_dtype, overwritten
+ *   t       >= 0, same for every (b, h); L >= bit_length(t) + 1
+ * Supported: 1 <= dk <= 128; dv a power of two in [4, 128].
+ * Errors: LL_ERR_INVALID (a NULL required pointer, beta included), LL_ERR_SHAPE,
+ * LL_ERR_DTYPE, LL_ERR_UNSUPPORTED, LL_ERR_ALIGN, LL_ERR_CUDA.
+ */
+LL_API int loglinear_gdn_decode_step(float* state, const void* q, const void* k, const void* v,
+                                     const float* log_a, const float* beta, const float* lambda,
+                                     int64_t t, void* out, int64_t B, int64_t H, int64_t Hqk,
+                                     int64_t dk, int64_t dv, int64_t L, int in_dtype,
+                                     int out_dtype, ll_stream_t stream);
 
 /*
  * Backward of loglinear_fwd (page "算力终结者来了！…", sections 结构矩阵 and 讨论与局限性:
@@ -246,7 +307,13 @@ LL_API int loglinear_device_error(ll_stream_t stream, unsigned* flags);
  * GPU that loads the library's device code holds it until the process exits.  This call
  * allocates nothing (no cudaMalloc, no allocating library routine).
  *   - The first call on a device (with that device current) looks up the array's device
- *     address and caches it; make that first call before any stream capture.
+ *     address and caches it with the ID of the current CUDA context; make that first call
+ *     before any stream capture.  A call under a different context (after
+ *     cudaDeviceReset, or when the application replaced the primary context) looks the
+ *     address up again; make it, too, outside any stream capture.
+ *   - The ready flags and the tile counter in the array are zeroed by every call, on
+ *     `stream`, before the kernel that reads them; everything else in it is written
+ *     before it is read.
  *   - All calls share the array and it keeps the last call's contents.  Nothing in it
  *     needs clearing between calls, but calls whose work overlaps on the GPU (another
  *     stream, another host thread) race on it: serialise them.

@@ -1,4 +1,5 @@
-"""Log-linear attention forward, backward and lssb decode on GB300 (sm_103a).
+"""Log-linear attention forward, backward and lssb decode (Mamba-2 and Gated DeltaNet
+transitions) on GB300 (sm_103a).
 
 Python face of the C ABI in include/loglinear.h; see ``_binding`` for the calls.
 """
@@ -15,6 +16,7 @@ from ._binding import (  # noqa: F401
     loglinear_fwd,
     loglinear_fwd_noalloc,
     loglinear_fwd_with_events,
+    loglinear_gdn_decode_step,
     loglinear_prefill,
     resolve_path,
     status_string,

@@ -23,8 +23,14 @@ LL_F32, LL_BF16 = 0, 1
 LL_PATH_AUTO, LL_PATH_SIMT, LL_PATH_TC = 0, 1, 2
 PATHS = {"auto": LL_PATH_AUTO, "simt": LL_PATH_SIMT, "tc": LL_PATH_TC}
 
+class LLStrides(ctypes.Structure):
+    """ll_strides: element strides of the batch, position and head dimensions."""
+    _fields_ = [("b", ctypes.c_int64), ("t", ctypes.c_int64), ("h", ctypes.c_int64)]
+
+
 # Every symbol include/loglinear.h declares, with its ctypes signature.
 _i64, _int, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+_sp = ctypes.POINTER(LLStrides)
 SIGNATURES = {
     "loglinear_version": (_int, []),
     "loglinear_status_string": (ctypes.c_char_p, [_int]),
@@ -34,11 +40,16 @@ SIGNATURES = {
                                             ctypes.POINTER(_sz)]),
     "loglinear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
                              _i64, _int, _int, _int, _int, _vp, _sz, _vp]),
+    "loglinear_fwd_strided": (_int, [_vp, _sp, _vp, _sp, _vp, _sp, _vp, _vp, _vp, _sp, _i64, _i64,
+                                     _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _int, _vp,
+                                     _sz, _vp]),
     "loglinear_fwd_with_events": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                          _i64, _i64, _i64, _int, _int, _int, _int, _vp, _sz, _vp,
                                          ctypes.POINTER(_vp), _int, ctypes.POINTER(_int)]),
     "loglinear_decode_step": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _i64,
                                      _i64, _i64, _i64, _int, _int, _vp]),
+    "loglinear_gdn_decode_step": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i64, _i64,
+                                         _i64, _i64, _i64, _i64, _int, _int, _vp]),
     "loglinear_debug_level_map": (_int, [_i64, _int, _int, _vp, _vp]),
     "loglinear_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "loglinear_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
@@ -103,12 +114,17 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check_dev(name, t, dtype=None, shape=None):
+def _check_dev(name, t, dtype=None, shape=None, strided=False):
+    """Device, dtype and shape checks; contiguity, or with strided=True only a contiguous
+    last dimension (the others are passed as strides)."""
     if t is None:
         return
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
+    if strided:
+        if t.dim() != 4 or (t.shape[-1] > 1 and t.stride(-1) != 1):
+            raise ValueError(f"{name} must have a contiguous last dimension")
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -136,25 +152,34 @@ def loglinear_fwd(q, k, v, log_a, lam, chunk, out=None, out_dtype=None, workspac
                   path="auto", stream=None):
     """O = (Q K^T ⊙ M^S ⊙ M^H) V through the C ABI (q, k [B,T,Hqk,dk]; v [B,T,H,dv];
     log_a [B,T,H] fp32 or None; lam [B,T,H,L] fp32; head h reads q/k head h // (H/Hqk)).
+    q, k, v and out may be strided views with a contiguous last dimension (e.g. slices of
+    a fused q/k/v projection); they then go through loglinear_fwd_strided.
     Returns out [B,T,H,dv]."""
     B, T, Hqk, dk = q.shape
     H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
-    _check_dev("q", q, shape=(B, T, Hqk, dk))
-    _check_dev("k", k, q.dtype, (B, T, Hqk, dk))
-    _check_dev("v", v, q.dtype, (B, T, H, dv))
+    _check_dev("q", q, shape=(B, T, Hqk, dk), strided=True)
+    _check_dev("k", k, q.dtype, (B, T, Hqk, dk), strided=True)
+    _check_dev("v", v, q.dtype, (B, T, H, dv), strided=True)
     _check_dev("log_a", log_a, torch.float32, (B, T, H))
     _check_dev("lam", lam, torch.float32, (B, T, H, L))
     in_dt = _dtype_code(q)
     if out is None:
         out = torch.empty(B, T, H, dv, device=q.device, dtype=out_dtype or q.dtype)
-    _check_dev("out", out, shape=(B, T, H, dv))
+    _check_dev("out", out, shape=(B, T, H, dv), strided=True)
     ws_bytes = fwd_workspace_size(B, T, H, dk, dv, chunk, in_dt, path)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), device=q.device, dtype=torch.uint8)
     _check_dev("workspace", workspace, torch.uint8)
-    st = _lib.loglinear_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
-                            B, T, H, Hqk, dk, dv, L, chunk, in_dt, _dtype_code(out), PATHS[path],
-                            _ptr(workspace), workspace.numel(), _stream(stream))
+    if all(x.is_contiguous() for x in (q, k, v, out)):
+        st = _lib.loglinear_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
+                                B, T, H, Hqk, dk, dv, L, chunk, in_dt, _dtype_code(out),
+                                PATHS[path], _ptr(workspace), workspace.numel(), _stream(stream))
+    else:
+        sd = [ctypes.byref(LLStrides(*x.stride()[:3])) for x in (q, k, v, out)]
+        st = _lib.loglinear_fwd_strided(_ptr(q), sd[0], _ptr(k), sd[1], _ptr(v), sd[2],
+                                        _ptr(log_a), _ptr(lam), _ptr(out), sd[3], B, T, H, Hqk, dk,
+                                        dv, L, chunk, in_dt, _dtype_code(out), PATHS[path],
+                                        _ptr(workspace), workspace.numel(), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_fwd")
     return out
@@ -201,6 +226,30 @@ def loglinear_decode_step(state, q, k, v, log_a, lam, t, out=None, out_dtype=Non
                                     _dtype_code(out), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_decode_step")
+    return out
+
+
+def loglinear_gdn_decode_step(state, q, k, v, log_a, beta, lam, t, out=None, out_dtype=None,
+                              stream=None):
+    """One Log-Linear Gated DeltaNet decode step at position t; updates state [B,H,L,dk,dv]
+    (fp32) in place and returns out [B,H,dv].  q, k [B,Hqk,dk]; beta [B,H] fp32."""
+    B, H, L, dk, dv = state.shape
+    Hqk = q.shape[1]
+    _check_dev("state", state, torch.float32)
+    _check_dev("q", q, shape=(B, Hqk, dk))
+    _check_dev("k", k, q.dtype, (B, Hqk, dk))
+    _check_dev("v", v, q.dtype, (B, H, dv))
+    _check_dev("log_a", log_a, torch.float32, (B, H))
+    _check_dev("beta", beta, torch.float32, (B, H))
+    _check_dev("lam", lam, torch.float32, (B, H, L))
+    if out is None:
+        out = torch.empty(B, H, dv, device=q.device, dtype=out_dtype or q.dtype)
+    _check_dev("out", out, shape=(B, H, dv))
+    st = _lib.loglinear_gdn_decode_step(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_a),
+                                        _ptr(beta), _ptr(lam), int(t), _ptr(out), B, H, Hqk, dk,
+                                        dv, L, _dtype_code(q), _dtype_code(out), _stream(stream))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_gdn_decode_step")
     return out
 
 

@@ -63,10 +63,11 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_state(FwdArgs a) {
   __syncthreads();
   for (int idx = threadIdx.x; idx < n * kPad; idx += kThreads) {
     const int r = idx / kPad, c = idx - r * kPad;
-    const int64_t rk = ((int64_t)b * a.T + t0 + r) * a.Hqk + h / a.hg;
-    const int64_t rv = ((int64_t)b * a.T + t0 + r) * a.H + h;
-    Ks[idx] = c < dk ? w[r] * ld<InT>(a.k, rk * dk + c) : 0.f;
-    Vs[idx] = c < dv ? ld<InT>(a.v, rv * dv + c) : 0.f;
+    const int64_t t = t0 + r;
+    const int64_t rk = (int64_t)b * a.sk[0] + t * a.sk[1] + (int64_t)(h / a.hg) * a.sk[2];
+    const int64_t rv = (int64_t)b * a.sv[0] + t * a.sv[1] + (int64_t)h * a.sv[2];
+    Ks[idx] = c < dk ? w[r] * ld<InT>(a.k, rk + c) : 0.f;
+    Vs[idx] = c < dv ? ld<InT>(a.v, rv + c) : 0.f;
   }
   __syncthreads();
   const int td = threadIdx.x >> 4, te = threadIdx.x & 15;
@@ -117,13 +118,15 @@ __global__ void __launch_bounds__(kThreads) simt_intra_readout(FwdArgs a) {
   chunk_cumsum(a, b, h, t0, n, cs);
   for (int idx = threadIdx.x; idx < C * dk; idx += kThreads) {
     const int r = idx / dk, c = idx - r * dk;
-    const int64_t g = (((int64_t)b * a.T + t0 + r) * a.Hqk + h / a.hg) * dk + c;
-    Qs[idx] = r < n ? ld<InT>(a.q, g) : 0.f;
-    Ks[idx] = r < n ? ld<InT>(a.k, g) : 0.f;
+    const int64_t t = t0 + r, hq = h / a.hg;
+    Qs[idx] = r < n ? ld<InT>(a.q, (int64_t)b * a.sq[0] + t * a.sq[1] + hq * a.sq[2] + c) : 0.f;
+    Ks[idx] = r < n ? ld<InT>(a.k, (int64_t)b * a.sk[0] + t * a.sk[1] + hq * a.sk[2] + c) : 0.f;
   }
   for (int idx = threadIdx.x; idx < C * dv; idx += kThreads) {
     const int r = idx / dv, c = idx - r * dv;
-    Vs[idx] = r < n ? ld<InT>(a.v, (((int64_t)b * a.T + t0 + r) * a.H + h) * dv + c) : 0.f;
+    Vs[idx] = r < n ? ld<InT>(a.v, (int64_t)b * a.sv[0] + (int64_t)(t0 + r) * a.sv[1] +
+                                       (int64_t)h * a.sv[2] + c)
+                    : 0.f;
   }
   for (int idx = threadIdx.x; idx < C * L; idx += kThreads) {
     const int r = idx / L;
@@ -203,7 +206,9 @@ __global__ void __launch_bounds__(kThreads) simt_intra_readout(FwdArgs a) {
     const int idx = threadIdx.x + o * kThreads;
     if (o < n_out && idx < C * dv) {
       const int t = idx / dv, e = idx - t * dv;
-      if (t < n) out[(((int64_t)b * a.T + t0 + t) * a.H + h) * dv + e] = from_f32<OutT>(acc[o]);
+      if (t < n)
+        out[(int64_t)b * a.so[0] + (int64_t)(t0 + t) * a.so[1] + (int64_t)h * a.so[2] + e] =
+            from_f32<OutT>(acc[o]);
     }
   }
 }

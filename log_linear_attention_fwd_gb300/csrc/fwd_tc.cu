@@ -52,6 +52,7 @@ struct TcParams {
   const float* log_a;
   const float* lam;
   void* out;
+  int64_t so_b, so_t, so_h;  // element strides of out's b, t and h dimensions
   uint8_t* U;        // [B*H][N] tile states U_i, bf16 [d_k][d_v]
   uint8_t* nodes;    // [B*H][N] block states of the even slots, bf16 [d_k][d_v]
   float* lgu;        // [B*H][N] log decay of each tile
@@ -460,14 +461,19 @@ __global__ void __launch_bounds__(kThreadsF, 2)
           for (int k = 0; k < 32; ++k) sv[k] *= wl * fcol[c * 32 + k];
         } else if (cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f) {
           // the diagonal chunk with a decay range that keeps exp(cs_t - cs_e) <= e^80:
-          // exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s)
-          const float gt = __expf(cs - cs_s[c * 32 + 31]);
+          // exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s).  The pair (r, s) has level
+          // bit_length(lane XOR k) <= 5 for column k <= lane: the six lambdas of the levels
+          // inside a 32-token chunk are held in registers and picked by select.
+          const float gt = row_live ? __expf(cs - cs_s[c * 32 + 31]) : 0.f;
+          const int lane = tid & 31;
+          const float l0 = lam_r[0], l1 = lam_r[1], l2 = lam_r[2], l3 = lam_r[3],
+                      l4 = lam_r[4], l5 = lam_r[5];
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            const int s = c * 32 + k;
-            sv[k] = (s <= r && row_live)
-                        ? sv[k] * lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * (gt * fcol[s])
-                        : 0.f;
+            const int x = lane ^ k;
+            const float lv = x >= 16 ? l5 : x >= 8 ? l4 : x >= 4 ? l3 : x >= 2 ? l2 : x >= 1 ? l1 : l0;
+            const float v = sv[k] * lv * (gt * fcol[c * 32 + k]);
+            sv[k] = k <= lane ? v : 0.f;
           }
         } else {
 #pragma unroll
@@ -630,8 +636,9 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   if (all_ok) {
     if (p.out_f32) {
       if (row_live) {
-        float4* dst =
-            reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * DV + col0);
+        float4* dst = reinterpret_cast<float4*>(
+            reinterpret_cast<float*>(p.out) + (int64_t)b * p.so_b + (int64_t)(t0 + r) * p.so_t +
+            (int64_t)h * p.so_h + col0);
 #pragma unroll
         for (int q = 0; q < G::kHalf / 4; ++q)
           dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
@@ -680,11 +687,17 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // [B, T, H, width] bf16 (width 64 or 128), boxes of 128 tokens x 64 features of one
 // (b, h); rows past T read as 0 and are not written.
 bool make_tokens_map(CUtensorMap* m, const void* base, int B, int T, int H, int width) {
+  int64_t s[3];
+  dense_strides(s, T, H, width);
+  return make_tokens_map_strided(m, base, B, T, H, width, s);
+}
+
+bool make_tokens_map_strided(CUtensorMap* m, const void* base, int B, int T, int H, int width,
+                             const int64_t* es) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {(cuuint64_t)width, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)width * 2, (cuuint64_t)H * width * 2,
-                           (cuuint64_t)T * H * width * 2};
+  cuuint64_t strides[3] = {(cuuint64_t)es[2] * 2, (cuuint64_t)es[1] * 2, (cuuint64_t)es[0] * 2};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
@@ -716,15 +729,17 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   if (a.dk != kD || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
   const int dv = (int)a.dv;
   CUtensorMap tmQ, tmK, tmV, tmOut, tmU, tmNode;
-  if (!make_tokens_map(&tmQ, a.q, a.B, a.T, a.Hqk, kD) ||
-      !make_tokens_map(&tmK, a.k, a.B, a.T, a.Hqk, kD) ||
-      !make_tokens_map(&tmV, a.v, a.B, a.T, a.H, dv) ||
-      !make_tokens_map(&tmOut, a.out, a.B, a.T, a.H, dv) || !make_rows_map(&tmU, a.U, rows, dv) ||
+  if (!make_tokens_map_strided(&tmQ, a.q, a.B, a.T, a.Hqk, kD, a.sq) ||
+      !make_tokens_map_strided(&tmK, a.k, a.B, a.T, a.Hqk, kD, a.sk) ||
+      !make_tokens_map_strided(&tmV, a.v, a.B, a.T, a.H, dv, a.sv) ||
+      !make_tokens_map_strided(&tmOut, a.out, a.B, a.T, a.H, dv, a.so) ||
+      !make_rows_map(&tmU, a.U, rows, dv) ||
       !make_rows_map(&tmNode, a.nodes, rows, dv))
     return cudaErrorInvalidValue;
   TcParams p;
   p.B = a.B; p.T = a.T; p.H = a.H; p.L = a.L; p.N = a.N; p.hg = a.hg;
   p.log_a = a.log_a; p.lam = a.lam; p.out = a.out;
+  p.so_b = a.so[0]; p.so_t = a.so[1]; p.so_h = a.so[2];
   p.U = static_cast<uint8_t*>(a.U);
   p.nodes = static_cast<uint8_t*>(a.nodes);
   p.lgu = a.lg;
@@ -735,17 +750,13 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   p.out_f32 = out_dtype == LL_F32;
   int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
   while ((int64_t(1) << levels) < a.N) ++levels;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(tc_forward_kernel<128>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem_fused(kMaxChunkLevels - 1));
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(tc_forward_kernel<64>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem_fused(kMaxChunkLevels - 1));
-  });
+  // The shared-memory limit is an attribute of the function on each device: set it
+  // on every launch (a host-side call), so that every device the library runs on has it.
+  const cudaError_t attr_err =
+      dv == 128 ? cudaFuncSetAttribute(tc_forward_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_fused(kMaxChunkLevels - 1))
+                : cudaFuncSetAttribute(tc_forward_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_fused(kMaxChunkLevels - 1));
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles = (int64_t)a.B * a.H * a.N;
   cudaError_t e;

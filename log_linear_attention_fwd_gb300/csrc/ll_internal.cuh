@@ -61,6 +61,9 @@ struct FwdArgs {
                 // q/k head h / hg
   int C, lc;  // tile length and log2(tile)
   int N;      // tiles per (b, h)
+  // element strides of the batch, position and head dimensions of q, k, v and out (the
+  // feature dimension is contiguous); dense: {T*Hx*w, Hx*w, w}
+  int64_t sq[3], sk[3], sv[3], so[3];
   // workspace
   void* U;        // [B*H][N][dk][dv] chunk states (fp32 on CUDA cores, bf16 on tensor cores)
   void* nodes;    // [B*H][N][dk*dv] Fenwick block states, slot c = first reader chunk
@@ -71,6 +74,19 @@ struct FwdArgs {
   uint32_t* rdy_n;  // [B*H][N] ready flags of the block states, and by
   uint32_t* tick;   // one tile ticket counter (the three are zeroed together)
 };
+
+// Dense strides of [B, T, Hx, width]: {T*Hx*width, Hx*width, width}.
+inline void dense_strides(int64_t* s, int64_t T, int64_t Hx, int64_t width) {
+  s[2] = width;
+  s[1] = Hx * width;
+  s[0] = T * Hx * width;
+}
+inline void set_dense_strides(FwdArgs& a) {
+  dense_strides(a.sq, a.T, a.Hqk, a.dk);
+  dense_strides(a.sk, a.T, a.Hqk, a.dk);
+  dense_strides(a.sv, a.T, a.H, a.dv);
+  dense_strides(a.so, a.T, a.H, a.dv);
+}
 
 // Workspace carving (identical on host for size queries and for launches).
 struct FwdWorkspace {
@@ -171,6 +187,12 @@ cudaError_t launch_decode(float* state, const void* q, const void* k, const void
                           const float* log_a, const float* lam, void* out, int B, int H,
                           int Hqk, int dk, int dv, int L, const DecodePlan& plan, int in_dtype,
                           int out_dtype, cudaStream_t s);
+
+// Log-Linear Gated DeltaNet decode step (gated delta rule transition on every level).
+cudaError_t launch_gdn_decode(float* state, const void* q, const void* k, const void* v,
+                              const float* log_a, const float* beta, const float* lam, void* out,
+                              int B, int H, int Hqk, int dk, int dv, int L, const DecodePlan& plan,
+                              int in_dtype, int out_dtype, cudaStream_t s);
 
 cudaError_t launch_level_map(int T, int tile, int lc, int8_t* levels, cudaStream_t s);
 

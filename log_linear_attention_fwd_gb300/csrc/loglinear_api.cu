@@ -117,6 +117,62 @@ int check_qk_heads(int64_t H, int64_t Hqk) {
   return LL_OK;
 }
 
+// Strides of a [B, T, Hx, width] tensor with a contiguous feature dimension: the given
+// ones (NULL: dense).  A dimension of size 1 takes its dense stride (it is never stepped).
+void resolve_strides(const ll_strides* st, int64_t B, int64_t T, int64_t Hx, int64_t width,
+                     int64_t* s) {
+  dense_strides(s, T, Hx, width);
+  if (!st) return;
+  if (B > 1) s[0] = st->b;
+  if (T > 1) s[1] = st->t;
+  if (Hx > 1) s[2] = st->h;
+}
+
+// out: no two elements may share an address.  Sorting the dimensions by stride, each must
+// step past the whole extent of the ones inside it.
+bool non_overlapping(const int64_t* s, int64_t B, int64_t T, int64_t H, int64_t width) {
+  int64_t d[4][2] = {{1, width}, {s[2], H}, {s[1], T}, {s[0], B}};  // {stride, size}
+  for (int i = 1; i < 4; ++i)
+    for (int j = i; j > 0 && d[j][0] < d[j - 1][0]; --j)
+      for (int c = 0; c < 2; ++c) {
+        const int64_t x = d[j][c];
+        d[j][c] = d[j - 1][c];
+        d[j - 1][c] = x;
+      }
+  int64_t reach = 1;  // largest offset covered by the dimensions so far, plus one
+  for (int i = 0; i < 4; ++i) {
+    if (d[i][1] <= 1) continue;
+    if (d[i][0] < reach) return false;
+    reach += d[i][0] * (d[i][1] - 1);
+  }
+  return true;
+}
+
+// The strides a path can take: none negative; out non-overlapping; on the tensor-core
+// path every stride of a dimension longer than 1 a positive multiple of 16 bytes (TMA).
+int check_strides(const int64_t* sq, const int64_t* sk, const int64_t* sv, const int64_t* so,
+                  int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk, int64_t dv, int path,
+                  int in_dtype, int out_dtype) {
+  const int64_t* all[4] = {sq, sk, sv, so};
+  for (const int64_t* x : all)
+    for (int i = 0; i < 3; ++i)
+      if (x[i] < 0) return LL_ERR_INVALID;
+  if (!non_overlapping(so, B, T, H, dv)) return LL_ERR_INVALID;
+  if (path == LL_PATH_TC) {
+    const int64_t sizes[4][3] = {{B, T, Hqk}, {B, T, Hqk}, {B, T, H}, {B, T, H}};
+    for (int x = 0; x < 4; ++x) {
+      const int64_t unit = x == 3 && out_dtype == LL_F32 ? 4 : 8;  // elements per 16 bytes
+      const int64_t u = x < 3 && in_dtype == LL_F32 ? 4 : unit;
+      for (int i = 0; i < 3; ++i) {
+        if (sizes[x][i] <= 1) continue;
+        if (all[x][i] == 0) return LL_ERR_UNSUPPORTED;
+        if (all[x][i] % u != 0) return LL_ERR_ALIGN;
+      }
+    }
+  }
+  return LL_OK;
+}
+
 }  // namespace
 
 int ll::report_cuda_error(cudaError_t e) { return cuda_fail(e); }
@@ -163,7 +219,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* lo
                     const float* lambda, void* out, int64_t B, int64_t T, int64_t H,
                     int64_t Hqk, int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
                     int out_dtype, int path, void* workspace, size_t workspace_bytes,
-                    ll_stream_t stream, StageEvents* ev, float* state_out = nullptr) {
+                    ll_stream_t stream, StageEvents* ev, float* state_out = nullptr,
+                    const ll_strides* const* strides = nullptr) {
   int p, tile;
   int64_t N;
   int st = check_fwd_sizes(B, T, H, dk, dv, chunk, in_dtype, path, &p, &tile, &N);
@@ -185,6 +242,13 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* lo
   a.B = (int)B; a.T = (int)T; a.H = (int)H; a.dk = (int)dk; a.dv = (int)dv; a.L = (int)L;
   a.Hqk = (int)Hqk; a.hg = (int)(H / Hqk);
   a.C = tile; a.lc = log2_exact(tile); a.N = (int)N;
+  resolve_strides(strides ? strides[0] : nullptr, B, T, Hqk, dk, a.sq);
+  resolve_strides(strides ? strides[1] : nullptr, B, T, Hqk, dk, a.sk);
+  resolve_strides(strides ? strides[2] : nullptr, B, T, H, dv, a.sv);
+  resolve_strides(strides ? strides[3] : nullptr, B, T, H, dv, a.so);
+  if ((st = check_strides(a.sq, a.sk, a.sv, a.so, B, T, H, Hqk, dk, dv, p, in_dtype,
+                          out_dtype)) != LL_OK)
+    return st;
   char* ws = static_cast<char*>(workspace);
   a.U = ws + w.off_U;
   a.nodes = ws + w.off_nodes;
@@ -207,6 +271,18 @@ int loglinear_fwd(const void* q, const void* k, const void* v, const float* log_
                   int path, void* workspace, size_t workspace_bytes, ll_stream_t stream) {
   return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, Hqk, dk, dv, L, chunk, in_dtype,
                   out_dtype, path, workspace, workspace_bytes, stream, nullptr);
+}
+
+int loglinear_fwd_strided(const void* q, const ll_strides* q_strides, const void* k,
+                          const ll_strides* k_strides, const void* v, const ll_strides* v_strides,
+                          const float* log_a, const float* lambda, void* out,
+                          const ll_strides* out_strides, int64_t B, int64_t T, int64_t H,
+                          int64_t Hqk, int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
+                          int out_dtype, int path, void* workspace, size_t workspace_bytes,
+                          ll_stream_t stream) {
+  const ll_strides* strides[4] = {q_strides, k_strides, v_strides, out_strides};
+  return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, Hqk, dk, dv, L, chunk, in_dtype,
+                  out_dtype, path, workspace, workspace_bytes, stream, nullptr, nullptr, strides);
 }
 
 int loglinear_prefill(const void* q, const void* k, const void* v, const float* log_a,
@@ -245,10 +321,14 @@ int loglinear_fwd_with_events(const void* q, const void* k, const void* v, const
   return st;
 }
 
-int loglinear_decode_step(float* state, const void* q, const void* k, const void* v,
-                          const float* log_a, const float* lambda, int64_t t, void* out,
-                          int64_t B, int64_t H, int64_t Hqk, int64_t dk, int64_t dv, int64_t L,
-                          int in_dtype, int out_dtype, ll_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the decode steps and the levels a step at position t touches: 0..l
+// (merged into l+1) and the levels above l+1 that hold data after t-1.
+int check_decode(int64_t B, int64_t H, int64_t Hqk, int64_t dk, int64_t dv, int64_t L, int64_t t,
+                 int in_dtype, int out_dtype) {
   if (B < 0 || H < 0 || dk < 1 || dv < 1 || t < 0 || L < 1) return LL_ERR_INVALID;
   const int sh = check_qk_heads(H, Hqk);
   if (sh != LL_OK) return sh;
@@ -257,10 +337,11 @@ int loglinear_decode_step(float* state, const void* q, const void* k, const void
   if (L < bit_length(t) + 1) return LL_ERR_SHAPE;
   if (dk > kMaxHeadDim || !is_pow2(dv) || dv < 4 || dv > kMaxHeadDim || L > 64)
     return LL_ERR_UNSUPPORTED;
-  if (B * H > INT32_MAX) return LL_ERR_UNSUPPORTED;
-  if (B == 0 || H == 0) return LL_OK;
-  if (!state || !q || !k || !v || !lambda || !out) return LL_ERR_INVALID;
-  if (!aligned16(state)) return LL_ERR_ALIGN;
+  if (B * H > INT32_MAX / 32) return LL_ERR_UNSUPPORTED;
+  return LL_OK;
+}
+
+DecodePlan decode_plan(int64_t t, int64_t L) {
   DecodePlan plan;
   memset(&plan, 0, sizeof(plan));
   if (t == 0) {
@@ -275,9 +356,44 @@ int loglinear_decode_step(float* state, const void* q, const void* k, const void
       if (((t - 1) >> (lv - 1)) & 1) plan.lv[n++] = lv;
     plan.n_hi = n - (l + 1);
   }
+  return plan;
+}
+
+}  // namespace
+
+extern "C" {
+
+int loglinear_decode_step(float* state, const void* q, const void* k, const void* v,
+                          const float* log_a, const float* lambda, int64_t t, void* out,
+                          int64_t B, int64_t H, int64_t Hqk, int64_t dk, int64_t dv, int64_t L,
+                          int in_dtype, int out_dtype, ll_stream_t stream) {
+  const int st = check_decode(B, H, Hqk, dk, dv, L, t, in_dtype, out_dtype);
+  if (st != LL_OK) return st;
+  if (B == 0 || H == 0) return LL_OK;
+  if (!state || !q || !k || !v || !lambda || !out) return LL_ERR_INVALID;
+  if (!aligned16(state)) return LL_ERR_ALIGN;
+  const DecodePlan plan = decode_plan(t, L);
   const cudaError_t e = launch_decode(state, q, k, v, log_a, lambda, out, (int)B, (int)H,
                                       (int)Hqk, (int)dk, (int)dv, (int)L, plan, in_dtype, out_dtype,
                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LL_OK : cuda_fail(e);
+}
+
+int loglinear_gdn_decode_step(float* state, const void* q, const void* k, const void* v,
+                              const float* log_a, const float* beta, const float* lambda,
+                              int64_t t, void* out, int64_t B, int64_t H, int64_t Hqk, int64_t dk,
+                              int64_t dv, int64_t L, int in_dtype, int out_dtype,
+                              ll_stream_t stream) {
+  const int st = check_decode(B, H, Hqk, dk, dv, L, t, in_dtype, out_dtype);
+  if (st != LL_OK) return st;
+  if (B == 0 || H == 0) return LL_OK;
+  if (!state || !q || !k || !v || !beta || !lambda || !out) return LL_ERR_INVALID;
+  if (!aligned16(state)) return LL_ERR_ALIGN;
+  const DecodePlan plan = decode_plan(t, L);
+  const cudaError_t e = launch_gdn_decode(state, q, k, v, log_a, beta, lambda, out, (int)B,
+                                          (int)H, (int)Hqk, (int)dk, (int)dv, (int)L, plan,
+                                          in_dtype, out_dtype,
+                                          reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 
@@ -346,6 +462,7 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
   a.B = (int)B; a.T = (int)T; a.H = (int)H; a.dk = (int)dk; a.dv = (int)dv; a.L = (int)L;
   a.Hqk = (int)Hqk; a.hg = (int)(H / Hqk);
   a.C = kBwdTile; a.lc = log2_exact(kBwdTile); a.N = (int)N;
+  set_dense_strides(a);
   char* ws = static_cast<char*>(workspace);
   a.U = ws + w.off_U;
   a.nodes = ws + w.off_nodes;

@@ -271,8 +271,12 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
 
 // Host: TMA tensor maps of the tensor-core kernels (defined with the forward).
 // [B, T, H, width] bf16 (width 64 or 128), boxes of 128 tokens x 64 features of one
-// (b, h), 128-byte swizzle; rows past T read as 0 and are not written.
+// (b, h), 128-byte swizzle; rows past T read as 0 and are not written.  The strided form
+// takes the element strides of the b, t and h dimensions (multiples of 8: TMA strides
+// are multiples of 16 bytes); the features are contiguous.
 bool make_tokens_map(CUtensorMap* m, const void* base, int B, int T, int H, int width);
+bool make_tokens_map_strided(CUtensorMap* m, const void* base, int B, int T, int H, int width,
+                             const int64_t* strides);
 // [rows][width] bf16 matrices, boxes of 128 rows x 64 columns, 128-byte swizzle.
 bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows, int width);
 

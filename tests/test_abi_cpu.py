@@ -161,6 +161,51 @@ def test_decode_validation_codes(L):
     assert dec(L, Hqk=0) == L.LL_ERR_SHAPE
 
 
+def test_gdn_decode_validation_codes(L):
+    """The Gated DeltaNet decode step checks its arguments before touching the GPU."""
+    f = L.lib().loglinear_gdn_decode_step
+    p = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation first
+    ok = dict(state=p, q=p, k=p, v=p, log_a=None, beta=p, lam=p, t=5, out=p, B=1, H=2, Hqk=2,
+              dk=8, dv=8, L=4, i=0, o=0, s=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["state"], a["q"], a["k"], a["v"], a["log_a"], a["beta"], a["lam"], a["t"],
+                 a["out"], a["B"], a["H"], a["Hqk"], a["dk"], a["dv"], a["L"], a["i"], a["o"], a["s"])
+
+    assert call(beta=None) == L.LL_ERR_INVALID
+    assert call(t=-1) == L.LL_ERR_INVALID
+    assert call(L=2, t=5) == L.LL_ERR_SHAPE          # t = 5 needs L >= 4
+    assert call(Hqk=3) == L.LL_ERR_SHAPE
+    assert call(dv=12) == L.LL_ERR_UNSUPPORTED        # d_v not a power of two
+    assert call(dk=129) == L.LL_ERR_UNSUPPORTED
+    assert call(i=7) == L.LL_ERR_DTYPE
+    assert call(state=ctypes.c_void_p(24)) == L.LL_ERR_ALIGN
+    assert call(B=0) == L.LL_OK                       # empty: nothing to do
+
+
+def test_fwd_strided_validation_codes(L):
+    """Bad strides are refused on the host before any launch."""
+    f = L.lib().loglinear_fwd_strided
+    p = ctypes.c_void_p(256)  # never dereferenced: every call below fails validation first
+    ws = ctypes.c_void_p(1 << 20)
+
+    def S(b, t, h):
+        return ctypes.byref(L.LLStrides(b, t, h))
+
+    B, T, H, d = 2, 64, 4, 128
+    def call(qs=None, os_=None, path=0, out_dtype=1):
+        ss = L.fwd_workspace_size(B, T, H, d, d, 64, 1, {0: "auto", 1: "simt", 2: "tc"}[path])
+        return f(p, qs, p, None, p, None, None, p, p, os_, B, T, H, H, d, d, 7, 64, 1, out_dtype,
+                 path, ws, ss, None)
+
+    assert call(qs=S(-1, d * H, d)) == L.LL_ERR_INVALID                 # negative stride
+    assert call(os_=S(T * H * d, H * d, d - 1)) == L.LL_ERR_INVALID     # heads overlap
+    assert call(os_=S(T * H * d, d, d)) == L.LL_ERR_INVALID             # positions hit heads
+    assert call(qs=S(T * H * 3 * d + 4, H * 3 * d, 3 * d), path=2) == L.LL_ERR_ALIGN
+    assert call(qs=S(T * H * 3 * d, H * 3 * d, 0), path=2) == L.LL_ERR_UNSUPPORTED
+
+
 def test_level_map_validation(L):
     lib = L.lib()
     assert lib.loglinear_debug_level_map(-1, 16, 0, FAKE, None) == L.LL_ERR_INVALID

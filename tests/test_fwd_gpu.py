@@ -191,6 +191,71 @@ def test_tc_onehot_lambda_bit_exact(LL, T, dv):
     assert LL.device_error() == 0
 
 
+def _top_level_rows(T, seed):
+    """Query rows in the tiles that read the highest block states of a long sequence:
+    every 128-token tile from tile 64 on (its first and last row and one random row),
+    the tiles 64, 127, 128 and the last one in full, and a few rows of the early tiles."""
+    rng = np.random.default_rng(seed)
+    n = -(-T // 128)
+    rows = set(range(0, 300, 37))
+    for j in range(64, n):
+        lo, hi = j * 128, min(T, (j + 1) * 128)
+        rows.update({lo, hi - 1, int(rng.integers(lo, hi))})
+    for j in (64, 127, 128, n - 1):
+        if j < n:
+            rows.update(range(j * 128, min(T, (j + 1) * 128), 3))
+    return np.array(sorted(r for r in rows if r < T))
+
+
+@pytest.mark.parametrize("T,dv", [(16384, 128), (20000, 128), (20000, 64)])
+def test_tc_onehot_lambda_top_levels(LL, T, dv):
+    """Levels up to the top of a 16K (L = 15) and a ragged 20000-token (L = 16) sequence on
+    the tensor-core path: with one-hot lambda, no decay and integer inputs that stay exact
+    through bf16 states, every level l = 0..L-1 (the block states of tiles >= 64 included:
+    chunk levels 7 and 8 of the tile pairing) must equal the oracle bit for bit on rows
+    sampled across those tiles."""
+    L = (T - 1).bit_length() + 1
+    rows = _top_level_rows(T, T + dv)
+    for lvl in range(L):
+        x = W.make_sparse_int_inputs(1, T, 2, 128, L, lvl, seed=1000 + lvl, dv=dv)
+        got = run(LL, x, 64, path="tc", out_dtype=torch.float32)
+        want = oracle_fwd(x, rows=rows)
+        g = got[:, rows].double().numpy()
+        assert np.array_equal(g, want[:, rows]), (lvl, float(np.abs(g - want[:, rows]).max()))
+        if lvl >= 13:  # the top levels carry weight in these rows (not a vacuous zero)
+            assert np.abs(want[:, rows]).sum() > 0, lvl
+    assert LL.device_error() == 0
+
+
+def test_tc_no_decay_headline_shape(LL):
+    """The headline shape (B1 H16 T16384 d128 bf16) without decay, so that every level up to
+    l = 14 carries weight: one whole head and sampled rows of every head against the oracle."""
+    cfg = W.FWD_CONFIGS["mamba2_T16384"].with_(name="linear_T16384", decay=False, seed=21)
+    x = W.make_fwd_inputs(cfg)
+    got = run(LL, x, cfg.C, path="tc", out_dtype=torch.float32)
+    assert LL.device_error() == 0
+    h = 5
+    want = oracle_fwd(x, heads=[(0, h)])
+    err_full = rel_l2(got[0, :, h], want[0, :, h])
+    rows = _sample_rows(cfg.T, 64, 3)
+    want_s = oracle_fwd(x, rows=rows, heads=[(0, hh) for hh in range(cfg.H)])
+    err_s = rel_l2(got[:, rows], want_s[:, rows])
+    print(f"no-decay T16384: rel_l2(full head)={err_full:.3e} rel_l2(sampled rows)={err_s:.3e} "
+          f"max_abs={max_abs(got[:, rows], want_s[:, rows]):.3e}")
+    assert err_full <= TOL_BF16 and err_s <= TOL_BF16
+
+
+def test_tc_level_map_headline_length(LL):
+    """The tensor-core path's level indexing at T = 16384 (L = 15), row by row against the
+    oracle's Fenwick walk."""
+    T = 16384
+    got = LL.debug_level_map(T, 64, path="tc").cpu().numpy()
+    for t in range(T):
+        want = oracle.level_row(t)
+        assert np.array_equal(got[t, : t + 1].astype(np.int64), want), t
+        assert (got[t, t + 1:] == -1).all(), t
+
+
 @pytest.mark.parametrize("T,dv", [(40000, 128), (40000, 64)])
 def test_tc_many_tiles_sampled(LL, T, dv):
     """A deep block tree (313 tiles, not a power of two): the block states of every level
@@ -246,3 +311,57 @@ def test_shared_qk_heads_match_oracle(LL, path, H, Hqk, dk, dv, T, dtype):
     err = rel_l2(got, want)
     print(f"shared q/k {path} H={H} Hqk={Hqk}: rel_l2={err:.3e}")
     assert err <= tol_for(dtype)
+
+
+# ------------------------------------------------------------------ strided views
+
+
+def _fused_views(x, H):
+    """q, k, v as slices of one fused [B, T, H, 3d] projection buffer (each a strided view
+    with a contiguous last dimension), plus a fresh output laid out [B, H, T, dv] and seen
+    as [B, T, H, dv]."""
+    B, T, _, d = x["q"].shape
+    fused = torch.empty(B, T, H, 3 * d, dtype=x["q"].dtype, device="cuda")
+    fused[..., :d] = x["q"].cuda()
+    fused[..., d:2 * d] = x["k"].cuda()
+    fused[..., 2 * d:] = x["v"].cuda()
+    return fused[..., :d], fused[..., d:2 * d], fused[..., 2 * d:]
+
+
+@pytest.mark.parametrize("path,dtype,d,T", [("tc", "bf16", 128, 700), ("simt", "f32", 32, 333),
+                                            ("simt", "bf16", 16, 130)])
+def test_strided_fused_qkv_and_permuted_out(LL, path, dtype, d, T):
+    """The forward on q/k/v slices of a fused projection and into a [B, H, T, dv] output
+    buffer (through loglinear_fwd_strided) equals the oracle on the dense tensors."""
+    L = (T - 1).bit_length() + 1
+    cfg = W.FwdConfig("strided", 2, 3, T, d, d, 64, L, dtype, True, "softplus", seed=d + T)
+    x = W.make_fwd_inputs(cfg)
+    q, k, v = _fused_views(x, cfg.H)
+    assert not q.is_contiguous() and q.stride(-1) == 1
+    out_dt = torch.float32
+    out_bhtd = torch.empty(cfg.B, cfg.H, T, d, device="cuda", dtype=out_dt)
+    out = out_bhtd.permute(0, 2, 1, 3)
+    got = LL.loglinear_fwd(q, k, v, x["log_a"].cuda(), x["lam"].cuda(), 64, out=out, path=path)
+    torch.cuda.synchronize()
+    assert got.data_ptr() == out_bhtd.data_ptr()
+    want = oracle_fwd(x)
+    err = rel_l2(out_bhtd.permute(0, 2, 1, 3).cpu(), want)
+    print(f"strided {path} {dtype} d={d} T={T}: rel_l2={err:.3e}")
+    assert err <= tol_for(dtype)
+    dense = run(LL, x, 64, path=path, out_dtype=out_dt)
+    assert rel_l2(out_bhtd.permute(0, 2, 1, 3).cpu(), dense) <= 1e-6
+    assert LL.device_error() == 0
+
+
+def test_strided_bf16_output_tc(LL):
+    """bf16 output through a strided TMA store: out is a [B, T, H, 2*dv] buffer's first half."""
+    T = 300
+    cfg = W.FwdConfig("strided_o", 1, 2, T, 128, 64, 64, 10, "bf16", True, "softplus", seed=8)
+    x = W.make_fwd_inputs(cfg)
+    d = cuda(x)
+    big = torch.zeros(1, T, 2, 128, device="cuda", dtype=torch.bfloat16)
+    out = big[..., :64]
+    LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], 64, out=out, path="tc")
+    torch.cuda.synchronize()
+    assert (big[..., 64:] == 0).all()  # nothing written outside the view
+    assert rel_l2(out.cpu(), oracle_fwd(x)) <= TOL_BF16
