@@ -57,8 +57,9 @@ struct TcParams {
   uint8_t* nodes;    // [B*H][N] block states of the even slots, bf16 [d_k][d_v]
   float* lgu;        // [B*H][N] log decay of each tile
   float* nlg;        // [B*H][N] log decay of the block in each even slot
-  uint32_t* rdy_u;   // [B*H][N] ready flags of U
-  uint32_t* rdy_n;   // [B*H][N] ready flags of the even slots' block states
+  uint32_t* rdy_u;   // [B*H][N] ready flags of U, carrying the tile's log decay
+  uint32_t* rdy_n;   // [B*H][N] ready flags of the even slots' block states, carrying the
+                     // block's log decay (decay_flag: bit-inverted, never 0)
   uint32_t* tick;    // tile ticket counter
   int out_f32;
 };
@@ -126,7 +127,9 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
 // what it forms before it waits for the block states it reads.
 //
 // Publication: every thread's generic stores, a block barrier, then thread 0 raises the
-// ready flag with a release store.  Readers: one thread acquires the flag; generic loads
+// ready flag with a release store; the flag's value is the published state's log decay
+// (bit-inverted so that it is never 0), which readers need next and so get in the same
+// load as the flag.  Readers: one thread acquires the flag; generic loads
 // by the others follow a block barrier; a TMA load is issued by the acquiring thread
 // itself after a global proxy fence.
 
@@ -399,22 +402,26 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   }
   if (tid == 0) p.lgu[bh * N + j] = lg;
   __syncthreads();
-  if (tid == 0) st_release_gpu(&rdy_u[j], 1u);
+  if (tid == 0) st_release_gpu(&rdy_u[j], decay_flag(lg));
   if (forms) {
     // Slot c = j+1 holds [c - 2^z, c), z = ctz(c): the block states of slots c - 2^(k-1)
     // (k = z..2), then U_{j-1}, then U_j; summed right to left, each weighted by the
     // decay across what lies to its right, in fp32, rounded once to bf16.
     const int c = j + 1, zc = __ffs(c) - 1;
     bool fl = true;
-    if (tid < zc)  // thread 0: U_{j-1}; thread t >= 1: slot c - 2^t
-      fl = wait_flag_acquire(tid == 0 ? &rdy_u[j - 1] : &rdy_n[c - (1 << tid)]);
+    if (tid < zc) {  // thread 0: U_{j-1}; thread t >= 1: slot c - 2^t; each flag carries
+                     // its part's log decay
+      uint32_t fv;
+      fl = wait_flag_acquire_value(tid == 0 ? &rdy_u[j - 1] : &rdy_n[c - (1 << tid)], &fv);
+      nl_s[tid] = fl ? flag_decay(fv) : 0.f;
+    }
     if (!__syncthreads_and(fl) && tid == 0) atomicOr(&g_tc_error, 2u);
     float G = lg;  // log decay of what has been summed so far
     for (int k = 1; k <= zc; ++k) {  // k = 1: U_{j-1}; k >= 2: slot c - 2^(k-1)
       const int cs_k = c - (1 << (k - 1));
       const uint4* src = reinterpret_cast<const uint4*>(
           k == 1 ? Ug + (int64_t)(j - 1) * G::kStateBytes : nodes + (int64_t)cs_k * G::kStateBytes);
-      const float L = __ldcg(k == 1 ? &lgu[j - 1] : &nlg[cs_k]);
+      const float L = nl_s[k - 1];
       const float g = __expf(G);
       uint4 y[kStatePieces];
 #pragma unroll
@@ -439,7 +446,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
                      pack_bf16(acc[8 * it + 6], acc[8 * it + 7]));
     if (tid == 0) nlg[c] = G;
     __syncthreads();
-    if (tid == 0) st_release_gpu(&rdy_n[c], 1u);
+    if (tid == 0) st_release_gpu(&rdy_n[c], decay_flag(G));
   }
 
   __syncthreads();  // the staged U in Kb is no longer read
@@ -527,8 +534,9 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       }
       my_c = (j >> (m - 1)) << (m - 1);
       const bool is_u = (my_c & 1) != 0;
-      fl = wait_flag_acquire(is_u ? &rdy_u[my_c - 1] : &rdy_n[my_c]);
-      nl_s[k] = fl ? __ldcg(is_u ? &lgu[my_c - 1] : &nlg[my_c]) : 0.f;
+      uint32_t fv;
+      fl = wait_flag_acquire_value(is_u ? &rdy_u[my_c - 1] : &rdy_n[my_c], &fv);
+      nl_s[k] = fl ? flag_decay(fv) : 0.f;
       fence_proxy_async_global();
     }
     if (!__syncthreads_and(fl) && tid == 0) atomicOr(&g_tc_error, 2u);

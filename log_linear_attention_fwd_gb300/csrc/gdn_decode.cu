@@ -10,22 +10,30 @@
 // 更新, and level 0 <- beta_t k_t v_t^T; out = sum_l lambda_l S_l^T q.
 //
 // Column e of A_t S needs only column e of S and u_e = (S^T k)_e, so the d_v columns split
-// across CTAs: one CTA per (b, h, 16-column slice).  With u = S^T k and w = S^T q of an old
-// level, its carried state is alpha (S - beta k u^T) and that state's readout is
-// alpha (w - beta (k.q) u); a merged level reads out with lambda of the level it lands in.
-// Each thread holds up to two rows of a 4-column group; the levels a step touches are
-// loaded in batches of kBatch, all loads of a batch in flight before any is used, with
-// one block reduction of u and w per batch.  The state is streamed with 16-byte
-// evict-first accesses (it has no reuse inside a step).
+// across CTAs: one CTA per (b, h, 32-column slice), which covers one 128-byte line of every
+// state row.  With u = S^T k and w = S^T q of an old level, its carried state is
+// alpha (S - beta k u^T) and that state's readout is alpha (w - beta (k.q) u); a merged
+// level reads out with lambda of the level it lands in.
+//
+// Two passes per CTA keep the registers few, so that four CTAs share an SM and keep many
+// loads in flight: pass 1 streams the touched levels from HBM and forms u and w (each
+// thread its rows, then the lanes and warps that share a column group), its first loads
+// issued before the CTA reads q, k and lambda; pass 2 reads the same rows again, from L2
+// where pass 1 just left them, and writes the carried states.  The second reads and
+// every write are marked evict-first.  Measured at B128 H16 d128 L15 t = 12345 (six levels
+// read, seven written): one pass holding every level in registers (two CTAs per SM) took
+// 569 us; two passes at two, three and four CTAs per SM 422, 352 and 330 us; with the
+// early first loads 320 us.
 #include "ll_internal.cuh"
 
 namespace ll {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kCols = 16;      // d_v columns per CTA
-constexpr int kRows = 2;       // rows per thread: d_k <= 128 rows over >= 64 row slots
-constexpr int kBatch = 6;      // levels loaded together
+constexpr int kCols = 32;      // d_v columns per CTA (one 128-byte line of an fp32 row)
+constexpr int kRows = 4;       // rows per thread: d_k <= 128 rows over >= 32 row slots
+constexpr int kBatch1 = 2;     // levels whose loads are issued together: pass 1 (HBM)
+constexpr int kBatch2 = 1;     // and pass 2 (L2), which also holds the merged rows
 constexpr int kMaxLv = 64;
 
 template <typename T>
@@ -49,7 +57,7 @@ __device__ __forceinline__ float4 f4_shfl_xor(float4 x, int o) {
 }
 
 template <typename InT, typename OutT>
-__global__ void __launch_bounds__(kThreads, 2) gdn_decode_kernel(
+__global__ void __launch_bounds__(kThreads, 4) gdn_decode_kernel(
     float* __restrict__ state, const void* __restrict__ q, const void* __restrict__ k,
     const void* __restrict__ v, const float* __restrict__ log_a, const float* __restrict__ beta,
     const float* __restrict__ lam, void* __restrict__ out, int hg, int dk, int dv, int L,
@@ -57,13 +65,35 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_kernel(
   __shared__ float qs[128];
   __shared__ float ks[128];
   __shared__ float lam_s[kMaxLv];
-  __shared__ float4 part[kBatch][2][kThreads / 32][kCols / 4];  // per-warp partial u, w
-  const int cpc = dv < kCols ? dv : kCols;    // columns of this CTA
+  __shared__ float4 part[kMaxLv][2][kCols / 4];  // u and w of every touched level
+  const int cpc = dv < kCols ? dv : kCols;       // columns of this CTA
   const int slices = dv / cpc;
   const int64_t bh = blockIdx.x / slices;
   const int slice = blockIdx.x - (int)(bh * slices);
   const int64_t bq = bh / hg;  // (b, q/k head): head h reads q/k head h / hg
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int groups = cpc >> 2;                 // float4 column groups of the slice: 1, 2, 4 or 8
+  const int cg = tid % groups;
+  const int row0 = tid / groups;
+  const int row_step = kThreads / groups;      // 256, 128, 64 or 32
+  const int col = slice * cpc + 4 * cg;        // first column of this thread's group
+  const int64_t l4 = ((int64_t)dk * dv) >> 2;  // float4 per level
+  float4* S = reinterpret_cast<float4*>(state + bh * L * (int64_t)dk * dv);
+  const int g_all = dv >> 2;                   // float4 per row
+  const float4 zero = f4(0.f);
+  const int cnt = plan.t_zero ? 0 : plan.l + 1 + plan.n_hi;
+  // the first batch of pass 1 goes out before anything else: it needs no q, k or lambda
+  float4 x1[kBatch1][kRows];
+#pragma unroll
+  for (int i = 0; i < kBatch1; ++i)
+#pragma unroll
+    for (int rr = 0; rr < kRows; ++rr) {
+      const int r = row0 + rr * row_step;
+      x1[i][rr] = (i < cnt && r < dk) ? S[plan.lv[i] * l4 + (int64_t)r * g_all + (col >> 2)]
+                                      : zero;
+    }
+  for (int i = tid; i < cnt * 2 * (kCols / 4); i += kThreads)
+    (&part[0][0][0])[i] = zero;
   for (int i = tid; i < dk; i += kThreads) {
     qs[i] = ldx<InT>(q, bq * dk + i);
     ks[i] = ldx<InT>(k, bq * dk + i);
@@ -72,54 +102,33 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_kernel(
   __syncthreads();
   const float a = log_a ? expf(log_a[bh]) : 1.f;
   const float bt = beta[bh];
-  float kq = 0.f;  // k . q (every thread the same sum)
-  for (int i = 0; i < dk; ++i) kq = fmaf(ks[i], qs[i], kq);
-  const int groups = cpc >> 2;                 // float4 column groups of the slice: 1, 2 or 4
-  const int cg = tid % groups;
-  const int row0 = tid / groups;
-  const int row_step = kThreads / groups;      // 256, 128 or 64
-  const int col = slice * cpc + 4 * cg;        // first column of this thread's group
+  float kq = 0.f;  // k . q: every warp forms the same sum, lanes over features
+  for (int i = lane; i < dk; i += 32) kq = fmaf(ks[i], qs[i], kq);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
   const float4 vv = make_float4(ldx<InT>(v, bh * dv + col), ldx<InT>(v, bh * dv + col + 1),
                                 ldx<InT>(v, bh * dv + col + 2), ldx<InT>(v, bh * dv + col + 3));
-  const int64_t l4 = ((int64_t)dk * dv) >> 2;  // float4 per level
-  float4* S = reinterpret_cast<float4*>(state + bh * L * (int64_t)dk * dv);
-  const int g_all = dv >> 2;                   // float4 per row
-  const float4 zero = f4(0.f);
-  float4 o = f4(0.f);                          // the readout of this column group
+  float4 o = f4_scale(lam_s[0] * bt * kq, vv);  // level 0 (beta k v^T) reads out
+                                                // lambda_0 beta (k.q) v
 
   if (plan.t_zero) {
 #pragma unroll
     for (int rr = 0; rr < kRows; ++rr) {
       const int r = row0 + rr * row_step;
-      if (r >= dk) break;
-      const int64_t off = (int64_t)r * g_all + (col >> 2);
-      __stcs(S + off, f4_scale(bt * ks[r], vv));
-      for (int lv = 1; lv < L; ++lv) __stcs(S + lv * l4 + off, zero);
+      if (r < dk) {
+        const int64_t off = (int64_t)r * g_all + (col >> 2);
+        __stcs(S + off, f4_scale(bt * ks[r], vv));
+        for (int lv = 1; lv < L; ++lv) __stcs(S + lv * l4 + off, zero);
+      }
     }
   } else {
     const int l = plan.l;
     const int n_low = l + 1;                   // levels 0..l merge into level l+1
-    const int cnt = n_low + plan.n_hi;
-    float4 merged[kRows];
+    // ---- pass 1: u = S^T k and w = S^T q of every touched level
+    auto reduce_batch = [&](const float4 (&x)[kBatch1][kRows], int i0) {
 #pragma unroll
-    for (int rr = 0; rr < kRows; ++rr) merged[rr] = zero;
-    for (int i0 = 0; i0 < cnt; i0 += kBatch) {
-      // ---- every row of the batch's levels in flight together
-      float4 x[kBatch][kRows];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-#pragma unroll
-        for (int rr = 0; rr < kRows; ++rr) {
-          const int r = row0 + rr * row_step;
-          x[i][rr] = (i0 + i < cnt && r < dk)
-                         ? __ldcs(S + plan.lv[i0 + i] * l4 + (int64_t)r * g_all + (col >> 2))
-                         : zero;
-        }
-      }
-      // ---- u = S^T k and w = S^T q of each level: this thread's rows, then the lanes of
-      // the warp that share the column group, then the warps
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
+      for (int i = 0; i < kBatch1; ++i) {
+        if (i0 + i >= cnt) break;
         float4 pu = zero, pw = zero;
 #pragma unroll
         for (int rr = 0; rr < kRows; ++rr) {
@@ -129,26 +138,52 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_kernel(
             pw = f4_fma(qs[r], x[i][rr], pw);
           }
         }
-        for (int off = groups; off < 32; off <<= 1) {
+        for (int off = groups; off < 32; off <<= 1) {  // lanes of the same column group
           pu = f4_add(pu, f4_shfl_xor(pu, off));
           pw = f4_add(pw, f4_shfl_xor(pw, off));
         }
-        if (lane < groups) {
-          part[i][0][warp][lane] = pu;
-          part[i][1][warp][lane] = pw;
+        if (lane < groups) {  // then the warps, by shared-memory atomics
+          float* du = reinterpret_cast<float*>(&part[i0 + i][0][lane]);
+          float* dw = reinterpret_cast<float*>(&part[i0 + i][1][lane]);
+          atomicAdd(du, pu.x); atomicAdd(du + 1, pu.y); atomicAdd(du + 2, pu.z); atomicAdd(du + 3, pu.w);
+          atomicAdd(dw, pw.x); atomicAdd(dw + 1, pw.y); atomicAdd(dw + 2, pw.z); atomicAdd(dw + 3, pw.w);
         }
       }
-      __syncthreads();
-      // ---- carry, merge / store, read out
+    };
+    reduce_batch(x1, 0);
+    for (int i0 = kBatch1; i0 < cnt; i0 += kBatch1) {
+      float4 x[kBatch1][kRows];
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        if (i0 + i >= cnt) break;
-        float4 u = zero, w = zero;
+      for (int i = 0; i < kBatch1; ++i)
 #pragma unroll
-        for (int wp = 0; wp < kThreads / 32; ++wp) {
-          u = f4_add(u, part[i][0][wp][cg]);
-          w = f4_add(w, part[i][1][wp][cg]);
+        for (int rr = 0; rr < kRows; ++rr) {
+          const int r = row0 + rr * row_step;
+          x[i][rr] = (i0 + i < cnt && r < dk)
+                         ? S[plan.lv[i0 + i] * l4 + (int64_t)r * g_all + (col >> 2)]
+                         : zero;
         }
+      reduce_batch(x, i0);
+    }
+    __syncthreads();
+    // ---- pass 2: the carried states (from L2), merged into level l+1 or stored in place
+    float4 merged[kRows];
+#pragma unroll
+    for (int rr = 0; rr < kRows; ++rr) merged[rr] = zero;
+    for (int i0 = 0; i0 < cnt; i0 += kBatch2) {
+      float4 x[kBatch2][kRows];
+#pragma unroll
+      for (int i = 0; i < kBatch2; ++i)
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) {
+          const int r = row0 + rr * row_step;
+          x[i][rr] = (i0 + i < cnt && r < dk)
+                         ? __ldcs(S + plan.lv[i0 + i] * l4 + (int64_t)r * g_all + (col >> 2))
+                         : zero;
+        }
+#pragma unroll
+      for (int i = 0; i < kBatch2; ++i) {
+        if (i0 + i >= cnt) break;
+        const float4 u = part[i0 + i][0][cg], w = part[i0 + i][1][cg];
         const int lv = plan.lv[i0 + i];
         const bool low = i0 + i < n_low;
 #pragma unroll
@@ -163,7 +198,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_kernel(
         }
         o = f4_fma(lam_s[low ? l + 1 : lv] * a, f4_fma(-bt * kq, u, w), o);
       }
-      __syncthreads();  // part is rewritten by the next batch
     }
 #pragma unroll
     for (int rr = 0; rr < kRows; ++rr) {
@@ -175,8 +209,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_kernel(
       __stcs(S + off, f4_scale(bt * ks[r], vv));
     }
   }
-  // level 0 (beta k v^T) reads out lambda_0 beta (k.q) v
-  o = f4_fma(lam_s[0] * bt * kq, vv, o);
   if (row0 == 0) {
     OutT* dst = reinterpret_cast<OutT*>(out) + bh * dv + col;
     dst[0] = from_f32<OutT>(o.x);

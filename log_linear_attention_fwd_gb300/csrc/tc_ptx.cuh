@@ -217,6 +217,29 @@ __device__ __forceinline__ bool wait_flag_acquire(const uint32_t* flag) {
   }
 }
 
+// As wait_flag_acquire, also returning the flag's value.
+__device__ __forceinline__ bool wait_flag_acquire_value(const uint32_t* flag, uint32_t* value) {
+  uint32_t v = ld_acquire_gpu(flag);
+  if (v == 0) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      __nanosleep(100);
+      if ((v = ld_acquire_gpu(flag)) != 0) break;
+      if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  *value = v;
+  return v != 0;
+}
+
+// A log decay as a ready-flag value: bit-inverted, so that no finite value is 0 (the
+// one NaN pattern that would be is stored as another NaN).
+__device__ __forceinline__ uint32_t decay_flag(float x) {
+  const uint32_t w = ~__float_as_uint(x);
+  return w ? w : 1u;
+}
+__device__ __forceinline__ float flag_decay(uint32_t w) { return __uint_as_float(~w); }
+
 // ---------------------------------------------------------------- MMA
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D, dense.
