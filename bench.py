@@ -53,6 +53,11 @@ def parse():
                    help="profiling aid: time only the backward, like --fwd-only")
     p.add_argument("--workload", default=None,
                    help="forward workload of --fwd-only / --bwd-only (default: the headline)")
+    p.add_argument("--decode-only", choices=["mamba2", "gdn"], default=None,
+                   help="profiling aid: time only the decode step (Mamba-2 or Gated DeltaNet) "
+                        "on the decode workload, or on --decode-batch rows of it")
+    p.add_argument("--decode-batch", type=int, default=None,
+                   help="batch of --decode-only (default: the decode workload's 128)")
     return p.parse_args()
 
 
@@ -770,10 +775,53 @@ def run_one_pass(args, backward):
                       f"{name}_us_min": min(times)}), flush=True)
 
 
+def run_decode_only(args):
+    """The decode step alone (K timed steps after W warm-ups, each from the same state after
+    t-1, L2 flushed between steps), for profilers."""
+    import log_linear_attention_fwd_gb300 as LL
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dcfg = W.DECODE_CONFIG
+    if args.decode_batch:
+        dcfg = dataclasses.replace(dcfg, B=args.decode_batch)
+    gen = torch.Generator(device=dev).manual_seed(1234)
+    state0 = torch.zeros(dcfg.B, dcfg.H, dcfg.L, dcfg.dk, dcfg.dv, device=dev)
+    for lv in W.nonempty_levels_before(dcfg.t, dcfg.L):
+        state0[:, :, lv].normal_(0.0, 0.05, generator=gen)
+    state = torch.empty_like(state0)
+    gdn = args.decode_only == "gdn"
+    make = W.make_gdn_decode_step_inputs if gdn else W.make_decode_step_inputs
+    inp = {k: (None if v is None else v.to(dev)) for k, v in make(dcfg).items()}
+    out = torch.empty(dcfg.B, dcfg.H, dcfg.dv, device=dev)
+    flush = torch.empty(512 << 20, device=dev, dtype=torch.uint8)
+    times = []
+    for i in range(args.warmup + args.steps):
+        state.copy_(state0)
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        if gdn:
+            LL.loglinear_gdn_decode_step(state, inp["q"], inp["k"], inp["v"], inp["log_a"],
+                                         inp["beta"], inp["lam"], dcfg.t, out=out)
+        else:
+            LL.loglinear_decode_step(state, inp["q"], inp["k"], inp["v"], inp["log_a"], inp["lam"],
+                                     dcfg.t, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1) * 1e3)
+    print(json.dumps({"mode": f"{args.decode_only}-decode-only", "B": dcfg.B, "t": dcfg.t,
+                      "steps": args.steps, "warmup": args.warmup,
+                      "us_mean": sum(times) / len(times), "us_min": min(times)}), flush=True)
+
+
 def main():
     args = parse()
     if args.fwd_only or args.bwd_only:
         run_one_pass(args, backward=args.bwd_only)
+        return
+    if args.decode_only:
+        run_decode_only(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -374,7 +374,6 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   // no reader waits for a flag that is never raised.
   const uint8_t* Ug = p.U + bh * N * G::kStateBytes;
   uint8_t* nodes = p.nodes + bh * N * G::kStateBytes;
-  const float* lgu = p.lgu + bh * N;
   float* nlg = p.nlg + bh * N;
   uint32_t* rdy_u = p.rdy_u + bh * N;
   uint32_t* rdy_n = p.rdy_n + bh * N;

@@ -205,19 +205,9 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Waits until *flag is non-zero, with acquire semantics.  Returns false if that takes
-// longer than kWaitLimitNs (the caller records the error and carries on).
-__device__ __forceinline__ bool wait_flag_acquire(const uint32_t* flag) {
-  if (ld_acquire_gpu(flag) != 0) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    __nanosleep(100);
-    if (ld_acquire_gpu(flag) != 0) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
-// As wait_flag_acquire, also returning the flag's value.
+// Waits until *flag is non-zero, with acquire semantics, and returns its value in *value.
+// Returns false if that takes longer than kWaitLimitNs (the caller records the error and
+// carries on).
 __device__ __forceinline__ bool wait_flag_acquire_value(const uint32_t* flag, uint32_t* value) {
   uint32_t v = ld_acquire_gpu(flag);
   if (v == 0) {
