@@ -177,7 +177,48 @@ def whole_job_rate(world, units_per_rank, seconds):
 # ---------------------------------------------------------------- clocks
 
 
+class NvmlClocks:
+    """SM clock, maximum SM clock, power and clock-event reasons of one GPU through NVML
+    (ctypes on libnvidia-ml, which the driver installs); the device is found by the UUID
+    torch reports for it, so CUDA_VISIBLE_DEVICES does not matter.  Raises if NVML cannot
+    be loaded."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index):
+        import ctypes
+        self.c = ctypes
+        self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+        self.h = ctypes.c_void_p()
+        if self.nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML device with UUID " + uuid)
+        self.reasons_fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        m = ctypes.c_uint()
+        self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(m))   # 1: the SM clock
+        self.max_mhz = float(m.value)
+
+    def read(self):
+        c = self.c
+        clk, pw, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, c.byref(clk))
+        self.nv.nvmlDeviceGetPowerUsage(self.h, c.byref(pw))
+        self.reasons_fn(self.h, c.byref(rs))
+        return float(clk.value), pw.value / 1000.0, int(rs.value)
+
+
 class ClockSampler:
+    """SM clocks and throttle reasons sampled during the run, with a marked window.
+
+    With NVML a background thread reads the clock every millisecond, so that a timed region
+    of 10-30 ms holds a few dozen samples; without it, nvidia-smi samples every 20 ms.
+    mark_start()/mark_end() bracket the timed region; stop() reports the median SM clock
+    and the reasons seen over the samples inside it (and the sample counts)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -185,11 +226,34 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
-        # the raw samples; LL_CLOCKS_DIR keeps them where the caller wants them
+        self.thread = None
+        self.samples = []          # (host time, sm MHz, power W, reason names)
+        self.t0 = self.t1 = None
+        self.source = None
         out_dir = os.environ.get("LL_CLOCKS_DIR") or tempfile.gettempdir()
         self.path = os.path.join(out_dir, f"clocks_bench_{os.getpid()}.csv")
 
     def start(self):
+        try:
+            self.nvml = NvmlClocks(self.idx)
+            self.source = "nvml, every 1 ms"
+            import threading
+            self.stop_flag = threading.Event()
+
+            def loop():
+                while not self.stop_flag.is_set():
+                    mhz, w, rs = self.nvml.read()
+                    names = [n for bit, n in NvmlClocks.REASONS.items() if rs & bit]
+                    self.samples.append((time.perf_counter(), mhz, w, names))
+                    time.sleep(0.001)
+
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            while not self.samples:
+                time.sleep(0.001)
+            return
+        except Exception:
+            self.thread = None
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
@@ -197,13 +261,32 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi, every 20 ms"
             t0 = time.time()  # wait for the first sample so the window really starts here
             while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0:
                 time.sleep(0.02)
         except Exception:
             self.proc = None
 
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+            inside = [x for x in self.samples
+                      if self.t0 is not None and self.t0 <= x[0] <= (self.t1 or x[0])]
+            sm = [x[1] for x in inside]
+            reasons = sorted({n for x in inside for n in x[3]})
+            return {"sm_mhz": statistics.median(sm) if sm else None,
+                    "sm_max_mhz": self.nvml.max_mhz, "reasons": reasons,
+                    "samples": len(inside), "samples_whole_run": len(self.samples),
+                    "power_w_max": max((x[2] for x in inside), default=None),
+                    "window": "the timed region (marked on the host)", "source": self.source}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -228,7 +311,8 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm), "window": "warm-up + timed region, every 20 ms"}
+                "samples": len(sm), "window": "warm-up + timed region, every 20 ms",
+                "source": self.source}
 
 
 # ---------------------------------------------------------------- CPU oracle sample
@@ -368,10 +452,12 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    clocks.mark_start()
     n_kernels = 0
     for ef, ed in evs:
         n_kernels = one_step(ef, ed)
     torch.cuda.synchronize()
+    clocks.mark_end()
     if world > 1:
         torch.distributed.barrier()
     wall = time.perf_counter() - wall0
@@ -496,39 +582,34 @@ def measure_gdn_decode(LL, dcfg, state0, state, flush, peaks, reps=20):
 
 def measure_prefill(LL, cfg, d, out, ws, flush, peaks, reps=10):
     """The prefill -> decode handoff on the headline prompt: loglinear_prefill (forward
-    plus the per-level decode state at T-1) against loglinear_fwd alone, medians of
-    `reps` calls each (L2 flushed before every call, outside the events).  The
-    difference is the state kernel; its bytes are the fp32 state it writes plus the
+    plus the per-level decode state at T-1), medians of `reps` calls (L2 flushed before
+    every call, outside the events), with events between its kernels so that the state
+    kernel is timed by its own events.  Its bytes are the fp32 state it writes plus the
     block states it reads."""
     state = torch.empty(cfg.B, cfg.H, cfg.L, cfg.dk, cfg.dv, device=out.device,
                         dtype=torch.float32)
 
-    def timed(fn):
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) * 1e-3)
-        return statistics.median(ts)
-
-    t_pre = timed(lambda: LL.loglinear_prefill(d["q"], d["k"], d["v"], d["log_a"], d["lam"],
-                                               cfg.C, out=out, state=state, workspace=ws))
-    t_fwd = timed(lambda: LL.loglinear_fwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C,
-                                           out=out, workspace=ws))
+    t_pre, t_k = [], []
+    for i in range(reps + 2):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        nk = LL.loglinear_prefill_with_events(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C,
+                                              ev, out, state, ws)
+        torch.cuda.synchronize()
+        if i >= 2:
+            t_pre.append(ev[0].elapsed_time(ev[nk]) * 1e-3)
+            t_k.append(ev[nk - 1].elapsed_time(ev[nk]) * 1e-3)   # the state kernel, last
     t = cfg.T - 1
     j = t >> 7
     state_bytes = cfg.B * cfg.H * cfg.L * cfg.dk * cfg.dv * 4
     read_bytes = cfg.B * cfg.H * bin(j).count("1") * cfg.dk * cfg.dv * 2
-    t_state = max(t_pre - t_fwd, 1e-9)
-    return {"prefill_us": t_pre * 1e6, "fwd_us": t_fwd * 1e6, "state_kernel_us": t_state * 1e6,
-            "state_bytes": state_bytes + read_bytes,
+    t_state = statistics.median(t_k)
+    return {"prefill_us": statistics.median(t_pre) * 1e6, "kernels": nk,
+            "state_kernel_us": t_state * 1e6, "state_bytes": state_bytes + read_bytes,
             "state_kernel_gbs": (state_bytes + read_bytes) / t_state / 1e9,
-            "note": "state kernel = prefill - forward (medians); bytes = fp32 state written "
-                    "+ bf16 block states read"}
+            "state_kernel_frac_of_hbm": (state_bytes + read_bytes) / t_state / 1e9 / peaks["hbm"],
+            "note": "state kernel timed by its own events inside loglinear_prefill_with_events; "
+                    "bytes = fp32 state written + bf16 block states read"}
 
 
 def _median_us(fn, flush, reps):

@@ -183,6 +183,21 @@ LL_API int loglinear_prefill(const void* q, const void* k, const void* v, const 
                              size_t workspace_bytes, ll_stream_t stream);
 
 /*
+ * loglinear_prefill with per-kernel timing, as loglinear_fwd_with_events: stage_events[0]
+ * is recorded before the first kernel and stage_events[i+1] after kernel i, the last of
+ * which is the kernel that forms the decode state.  T = 0 launches no kernel and records
+ * no event (*n_kernels = 0).
+ */
+LL_API int loglinear_prefill_with_events(const void* q, const void* k, const void* v,
+                                         const float* log_a, const float* lambda, void* out,
+                                         float* state_out, int64_t B, int64_t T, int64_t H,
+                                         int64_t Hqk, int64_t dk, int64_t dv, int64_t L,
+                                         int chunk, int in_dtype, int out_dtype, int path,
+                                         void* workspace, size_t workspace_bytes,
+                                         ll_stream_t stream, void* const* stage_events,
+                                         int n_events, int* n_kernels);
+
+/*
  * One decode step at position t for every (b, h) (first page, section 解码：基于 lssb 的
  * 状态更新; slide deck "論文紹介：Log Linear Attention", slide 21).  With l = lssb(t) (index of
  * the lowest set bit of t > 0):
@@ -265,7 +280,9 @@ LL_API int loglinear_gdn_decode_step(float* state, const void* q, const void* k,
  *   same q, k, v, log_a, lambda and sizes, with nothing written to it since.  Its block
  *   states are then read instead of being recomputed by a forward inside this call (the
  *   usual training step: forward, then backward).  The library cannot check that the
- *   contents match the inputs; that is the caller's contract.  fwd_workspace_bytes must
+ *   contents match the inputs; that is the caller's contract.  It does check, on the GPU,
+ *   the layout tag the tensor-core forward leaves in its workspace (sizes and path): a
+ *   mismatch raises bit 2 of loglinear_device_error.  fwd_workspace_bytes must
  *   be at least loglinear_fwd_workspace_size() for the forward's arguments
  *   (LL_ERR_WORKSPACE); a non-NULL fwd_workspace on the CUDA-core path is
  *   LL_ERR_UNSUPPORTED.  An empty call (B, T or H zero) returns LL_OK before any of
@@ -292,7 +309,10 @@ LL_API int loglinear_bwd(const void* q, const void* k, const void* v, const floa
  * *flags = 0 when every wait of the kernels run so far completed.  Bit 0: an mbarrier
  * wait ran out of time (the CTA then skipped its remaining work and its output tile is
  * not valid).  Bit 1: a wait for another tile's published state ran out of time (the
- * output of that tile is not valid).  The launch itself still reported success.
+ * output of that tile is not valid).  Bit 2: loglinear_bwd was given a fwd_workspace
+ * that a tensor-core loglinear_fwd with the same B, T, H, Hqk and dv did not write (its
+ * layout tag does not match; the gradients are not valid).  The launch itself still
+ * reported success.
  */
 LL_API int loglinear_device_error(ll_stream_t stream, unsigned* flags);
 

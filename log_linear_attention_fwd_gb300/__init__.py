@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     loglinear_fwd_with_events,
     loglinear_gdn_decode_step,
     loglinear_prefill,
+    loglinear_prefill_with_events,
     resolve_path,
     status_string,
 )

@@ -43,6 +43,10 @@ SIGNATURES = {
     "loglinear_fwd_strided": (_int, [_vp, _sp, _vp, _sp, _vp, _sp, _vp, _vp, _vp, _sp, _i64, _i64,
                                      _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _int, _vp,
                                      _sz, _vp]),
+    "loglinear_prefill_with_events": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                             _i64, _i64, _i64, _i64, _int, _int, _int, _int, _vp,
+                                             _sz, _vp, ctypes.POINTER(_vp), _int,
+                                             ctypes.POINTER(_int)]),
     "loglinear_fwd_with_events": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                          _i64, _i64, _i64, _int, _int, _int, _int, _vp, _sz, _vp,
                                          ctypes.POINTER(_vp), _int, ctypes.POINTER(_int)]),
@@ -251,6 +255,28 @@ def loglinear_gdn_decode_step(state, q, k, v, log_a, beta, lam, t, out=None, out
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_gdn_decode_step")
     return out
+
+
+def loglinear_prefill_with_events(q, k, v, log_a, lam, chunk, events, out, state, workspace,
+                                  path="auto", stream=None):
+    """loglinear_prefill plus torch.cuda.Event records between its kernels (the last
+    kernel forms the decode state).  Returns the number of kernels."""
+    B, T, Hqk, dk = q.shape
+    H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
+    st_ = stream if stream is not None else torch.cuda.current_stream()
+    for e in events:          # torch creates the CUDA event lazily, on its first record
+        if not e.cuda_event:
+            e.record(st_)
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    nk = ctypes.c_int(0)
+    st = _lib.loglinear_prefill_with_events(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam),
+                                            _ptr(out), _ptr(state), B, T, H, Hqk, dk, dv, L,
+                                            chunk, _dtype_code(q), _dtype_code(out), PATHS[path],
+                                            _ptr(workspace), workspace.numel(), _stream(stream),
+                                            arr, len(events), ctypes.byref(nk))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_prefill_with_events")
+    return nk.value
 
 
 def loglinear_prefill(q, k, v, log_a, lam, chunk, out=None, state=None, out_dtype=None,

@@ -77,6 +77,8 @@ struct BqParams {
   float* dcq;          // [B, T, H] q . dQ, or null
   float* dlam;         // [B, T, H, L]
   int ahead;  // tiles between this one and the next on the same SM
+  const uint32_t* tag;  // the forward workspace's layout tag, and the value it must have
+  uint32_t tag_value;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -198,6 +200,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   float* fcol = reinterpret_cast<float*>(smem + BSmem::kFcol);
   float* lam_s = reinterpret_cast<float*>(smem + BSmem::kLam);
   float* dlb = reinterpret_cast<float*>(smem + BSmem::kDlb);
+  // the block states come from a tensor-core forward of exactly these sizes, or the
+  // results are not valid: bit 2 of the error word says so
+  if (blockIdx.x == 0 && threadIdx.x == 0 && (!p.tag || *p.tag != p.tag_value))
+    atomicOr(&g_tcb_error, 4u);
   float* lamx = reinterpret_cast<float*>(smem + BSmem::kLamX);
   float* dli = lamx + levels * kTile;  // [levels][128] q . X sums of the inter levels
 
@@ -1268,6 +1274,8 @@ cudaError_t launch_tc_bwd_dq(const FwdArgs& f, const void* dout, float* dqh, voi
   p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.nlg = f.nlg;
   p.dqh = dqh; p.dq = dq_bf16; p.dcq = dcq; p.dlam = dlam;
   p.ahead = sm_count();
+  p.tag = f.tag;
+  p.tag_value = fwd_layout_tag(f.B, f.T, f.H, f.Hqk, f.dv);
   int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
   while ((int64_t(1) << levels) < f.N) ++levels;
   // The shared-memory limit is an attribute of the function on each device: set it

@@ -61,6 +61,8 @@ struct TcParams {
   uint32_t* rdy_n;   // [B*H][N] ready flags of the even slots' block states, carrying the
                      // block's log decay (decay_flag: bit-inverted, never 0)
   uint32_t* tick;    // tile ticket counter
+  uint32_t* tag;     // the workspace's layout tag, written by the CTA of ticket 0
+  uint32_t tag_value;
   int out_f32;
 };
 
@@ -267,6 +269,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
   const int BH = p.B * p.H;
   const int tk = (int)ints[0];
+  if (tk == 0 && tid == 0) *p.tag = p.tag_value;  // the layout a backward may read
   const int j = tk / BH, bhi = tk - j * BH;
   const int b = bhi / p.H, h = bhi - b * p.H;
   const int hq = h / p.hg;  // q/k head
@@ -754,6 +757,8 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   p.rdy_u = a.rdy_u;
   p.rdy_n = a.rdy_n;
   p.tick = a.tick;
+  p.tag = a.tag;
+  p.tag_value = fwd_layout_tag(a.B, a.T, a.H, a.Hqk, a.dv);
   p.out_f32 = out_dtype == LL_F32;
   int levels = 0;  // inter-chunk levels a tile can have: bit length of N-1
   while ((int64_t(1) << levels) < a.N) ++levels;

@@ -73,6 +73,8 @@ struct FwdArgs {
   uint32_t* rdy_u;  // [B*H][N] ready flags of U; followed in memory by
   uint32_t* rdy_n;  // [B*H][N] ready flags of the block states, and by
   uint32_t* tick;   // one tile ticket counter (the three are zeroed together)
+  uint32_t* tag;    // tensor-core path: the workspace's layout tag (fwd_layout_tag), which
+                    // the forward writes and a backward given this workspace checks
 };
 
 // Dense strides of [B, T, Hx, width]: {T*Hx*width, Hx*width, width}.
@@ -90,10 +92,19 @@ inline void set_dense_strides(FwdArgs& a) {
 
 // Workspace carving (identical on host for size queries and for launches).
 struct FwdWorkspace {
-  size_t off_U, off_nodes, off_lg, off_nlg, off_rdy_u, off_rdy_n, off_tick, total;
+  size_t off_U, off_nodes, off_lg, off_nlg, off_rdy_u, off_rdy_n, off_tick, off_tag, total;
 };
 FwdWorkspace fwd_workspace_layout(int64_t B, int64_t H, int64_t N, int64_t dk, int64_t dv,
                                   size_t state_elem_bytes);
+// The tag a tensor-core forward leaves in its workspace: a non-zero mix of the sizes that
+// fix its layout, so that a backward reading that workspace can tell whether it matches.
+inline uint32_t fwd_layout_tag(int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dv) {
+  uint64_t x = 0x4C4C5443ull;  // any fixed start
+  const int64_t f[5] = {B, T, H, Hqk, dv};
+  for (int64_t v : f) x = (x ^ (uint64_t)v) * 0x100000001B3ull;
+  const uint32_t t = (uint32_t)(x ^ (x >> 32));
+  return t ? t : 1u;
+}
 
 // Optional per-kernel event recording by the launchers (instrumentation only).
 struct StageEvents {
@@ -104,10 +115,12 @@ struct StageEvents {
     if (recorded < n) return cudaEventRecord(ev[recorded++], s);
     return cudaSuccess;
   }
+  bool hold = false;  // a later kernel of the same call still follows: finish() counts only
   cudaError_t finish(cudaStream_t s) {
     cudaError_t e = cudaSuccess;
     const int kernels = recorded > 0 ? recorded - 1 : 0;
     launched = kernels;
+    if (hold) return e;
     while (recorded < n && e == cudaSuccess) e = cudaEventRecord(ev[recorded++], s);
     return e;
   }

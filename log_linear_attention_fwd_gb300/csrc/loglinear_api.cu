@@ -22,7 +22,8 @@ FwdWorkspace fwd_workspace_layout(int64_t B, int64_t H, int64_t N, int64_t dk, i
   w.off_rdy_u = align_up(w.off_nlg + tiles * sizeof(float), 256);
   w.off_rdy_n = w.off_rdy_u + tiles * sizeof(uint32_t);  // contiguous: zeroed by one memset
   w.off_tick = w.off_rdy_n + tiles * sizeof(uint32_t);
-  w.total = align_up(w.off_tick + sizeof(uint32_t), 256);
+  w.off_tag = w.off_tick + sizeof(uint32_t);  // not zeroed: the forward writes it
+  w.total = align_up(w.off_tag + sizeof(uint32_t), 256);
   return w;
 }
 
@@ -257,11 +258,18 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* lo
   a.rdy_u = reinterpret_cast<uint32_t*>(ws + w.off_rdy_u);
   a.rdy_n = reinterpret_cast<uint32_t*>(ws + w.off_rdy_n);
   a.tick = reinterpret_cast<uint32_t*>(ws + w.off_tick);
+  a.tag = reinterpret_cast<uint32_t*>(ws + w.off_tag);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (ev && state_out) ev->hold = true;  // the state kernel follows the forward's kernels
   cudaError_t e = p == LL_PATH_TC ? launch_tc_forward(a, out_dtype, s, ev)
                                   : launch_simt_forward(a, in_dtype, out_dtype, s, ev);
-  if (e == cudaSuccess && state_out)
+  if (e == cudaSuccess && state_out) {
     e = launch_prefill_state(a, p == LL_PATH_TC, in_dtype, state_out, s);
+    if (e == cudaSuccess && ev) {
+      ev->hold = false;
+      if ((e = ev->record(s)) == cudaSuccess) e = ev->finish(s);
+    }
+  }
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 
@@ -301,6 +309,29 @@ int loglinear_prefill(const void* q, const void* k, const void* v, const float* 
   }
   return fwd_impl(q, k, v, log_a, lambda, out, B, T, H, Hqk, dk, dv, L, chunk, in_dtype,
                   out_dtype, path, workspace, workspace_bytes, stream, nullptr, state_out);
+}
+
+int loglinear_prefill_with_events(const void* q, const void* k, const void* v,
+                                  const float* log_a, const float* lambda, void* out,
+                                  float* state_out, int64_t B, int64_t T, int64_t H, int64_t Hqk,
+                                  int64_t dk, int64_t dv, int64_t L, int chunk, int in_dtype,
+                                  int out_dtype, int path, void* workspace,
+                                  size_t workspace_bytes, ll_stream_t stream,
+                                  void* const* stage_events, int n_events, int* n_kernels) {
+  if (n_events < 0 || (n_events > 0 && !stage_events)) return LL_ERR_INVALID;
+  if (n_kernels) *n_kernels = 0;
+  if (!state_out) return LL_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(state_out) & 3u) != 0) return LL_ERR_ALIGN;
+  if (T == 0)  // no kernels to time: the plain call zeroes the state
+    return loglinear_prefill(q, k, v, log_a, lambda, out, state_out, B, T, H, Hqk, dk, dv, L,
+                             chunk, in_dtype, out_dtype, path, workspace, workspace_bytes, stream);
+  StageEvents ev;
+  ev.ev = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events));
+  ev.n = n_events;
+  const int st = fwd_impl(q, k, v, log_a, lambda, out, B, T, H, Hqk, dk, dv, L, chunk, in_dtype,
+                          out_dtype, path, workspace, workspace_bytes, stream, &ev, state_out);
+  if (n_kernels) *n_kernels = ev.launched;
+  return st;
 }
 
 int loglinear_fwd_with_events(const void* q, const void* k, const void* v, const float* log_a,
@@ -467,7 +498,7 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
   a.U = ws + w.off_U;
   a.nodes = ws + w.off_nodes;
   a.lg = reinterpret_cast<float*>(ws + w.off_lg);
-  a.nlg = nullptr; a.rdy_u = nullptr; a.rdy_n = nullptr; a.tick = nullptr;
+  a.nlg = nullptr; a.rdy_u = nullptr; a.rdy_n = nullptr; a.tick = nullptr; a.tag = nullptr;
   A.dout = dout; A.dq = dq; A.dk = dk_out; A.dv = dv_out;
   A.dlog_a = log_a ? dlog_a : nullptr;
   A.dlam = dlambda;
@@ -496,6 +527,7 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
     f.rdy_u = reinterpret_cast<uint32_t*>(fw + w.fwd.off_rdy_u);
     f.rdy_n = reinterpret_cast<uint32_t*>(fw + w.fwd.off_rdy_n);
     f.tick = reinterpret_cast<uint32_t*>(fw + w.fwd.off_tick);
+    f.tag = reinterpret_cast<uint32_t*>(fw + w.fwd.off_tag);
     // the mirrored states on the same 128-token tiles go into U's buffer (fp32)
     float* R = reinterpret_cast<float*>(a.U);
     // with one q/k per head the kernels write dq and dk in bf16 themselves; shared q/k

@@ -205,3 +205,38 @@ def test_bwd_reads_forward_workspace(LL, dv, Hqk):
     assert torch.equal(a[0], b[0]) and torch.equal(a[4], b[4])
     for u, w in zip(a[1:4], b[1:4]):
         assert rel_l2(u.cpu(), w.cpu().double().numpy()) <= 1e-3
+
+
+def test_bwd_flags_a_foreign_forward_workspace(LL):
+    """A fwd_workspace that a tensor-core forward of these sizes did not write (here one a
+    CUDA-core forward filled, whose layout differs, or one of another length) raises bit 2
+    of the device error word; the matching workspace raises nothing."""
+    T = 300
+    cfg = W.FwdConfig("bwd_tag", 1, 2, T, 128, 64, 64, 10, "bf16", True, "softplus", seed=3)
+    x = W.make_fwd_inputs(cfg)
+    d = cuda(x)
+    dout = _dout(cfg, 5).cuda()
+    args = (d["q"], d["k"], d["v"], d["log_a"], d["lam"])
+    ws_simt = torch.zeros(LL.fwd_workspace_size(1, T, 2, 128, 64, 64, 1, "simt"), device="cuda",
+                          dtype=torch.uint8)
+    LL.loglinear_fwd(*args, 64, path="simt", workspace=ws_simt)
+    assert LL.device_error() == 0
+    LL.loglinear_bwd(*args, dout, path="tc", fwd_workspace=ws_simt)
+    torch.cuda.synchronize()
+    assert LL.device_error() & 4
+    ws_tc = torch.zeros(LL.fwd_workspace_size(1, T, 2, 128, 64, 64, 1, "tc"), device="cuda",
+                        dtype=torch.uint8)
+    LL.loglinear_fwd(*args, 64, path="tc", workspace=ws_tc)
+    want = LL.loglinear_bwd(*args, dout, path="tc")
+    got = LL.loglinear_bwd(*args, dout, path="tc", fwd_workspace=ws_tc)
+    torch.cuda.synchronize()
+    assert LL.device_error() == 0
+    for g, w in zip(got, want):  # same values up to the order of the float atomics
+        if w is not None:
+            assert rel_l2(g.cpu(), w.cpu()) <= 1e-3
+    # a tensor-core forward of another length over a large enough workspace
+    short = {k: (None if v is None else v[:, :250].contiguous()) for k, v in d.items()}
+    LL.loglinear_bwd(short["q"], short["k"], short["v"], short["log_a"], short["lam"],
+                     dout[:, :250].contiguous(), path="tc", fwd_workspace=ws_tc)
+    torch.cuda.synchronize()
+    assert LL.device_error() & 4

@@ -117,3 +117,25 @@ def test_prefill_empty_prompt(LL):
     _, state = LL.loglinear_prefill(q, q, q, la, lam, 16, state=state, path="simt")
     torch.cuda.synchronize()
     assert float(state.abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("path,dtype,dk,dv", [("tc", "bf16", 128, 128), ("simt", "f32", 16, 8)])
+def test_prefill_with_events_matches_prefill(LL, path, dtype, dk, dv):
+    """The timed prefill launches the forward's kernels and then the state kernel, records
+    an event around each, and gives the same output and state as loglinear_prefill."""
+    T = 700
+    cfg = W.FwdConfig("pre_ev", 1, 2, T, dk, dv, 64, (T - 1).bit_length() + 1, dtype, True,
+                      "softplus", seed=17)
+    d = cuda(W.make_fwd_inputs(cfg))
+    out0, S0 = LL.loglinear_prefill(d["q"], d["k"], d["v"], d["log_a"], d["lam"], 64, path=path)
+    ws = torch.empty(LL.fwd_workspace_size(1, T, 2, dk, dv, 64, 1 if dtype == "bf16" else 0, path),
+                     device="cuda", dtype=torch.uint8)
+    out1, S1 = torch.empty_like(out0), torch.empty_like(S0)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    nk = LL.loglinear_prefill_with_events(d["q"], d["k"], d["v"], d["log_a"], d["lam"], 64, ev,
+                                          out1, S1, ws, path=path)
+    torch.cuda.synchronize()
+    assert nk == (2 if path == "tc" else 4)       # forward kernel(s), then the state kernel
+    assert torch.equal(out0, out1) and torch.equal(S0, S1)
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(nk)]
+    assert all(t >= 0 for t in times)
