@@ -13,9 +13,9 @@
 // tile and is taken in the dense masked product; the sum is the same.
 //
 // Shared-memory tiles are 128 rows x 64 or 128 bf16 stored as 64-column panels with the
-// 128-byte swizzle TMA produces; K-major operands (Q, K, P, block states) and MN-major
-// ones (V as the B of P V; V and K in the state GEMM) are described to tcgen05 with the
-// matching descriptors.  Every wait (mbarriers, block-state flags) is bounded (see
+// 128-byte swizzle TMA produces; K-major operands (Q, K, block states) and MN-major ones
+// (V as the B of P V; V and K in the state GEMM) are described to tcgen05 with the
+// matching descriptors.  P, the A of P V, is written to TMEM (two bf16 per column).  Every wait (mbarriers, block-state flags) is bounded (see
 // tc_ptx.cuh); a CTA whose wait times out raises g_tc_error, skips the MMAs and stores
 // that depend on it, frees its TMEM and exits.
 //
@@ -86,13 +86,6 @@ __device__ __forceinline__ void put_row32_bf16(uint8_t* buf, int r, int c, const
                    pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
 }
 
-__device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
-  uint8_t* panel = buf + (c >> 1) * kPanel;
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    *reinterpret_cast<uint4*>(panel + sw128_offset(r, (c & 1) * 4 + q)) = make_uint4(0, 0, 0, 0);
-}
-
 // ------------------------------------------------------------------ the forward kernel
 //
 // One CTA per 128-token tile; 8 warps: warps w and w+4 share TMEM lane quarter w mod 4
@@ -107,13 +100,16 @@ __device__ __forceinline__ void put_row32_zero(uint8_t* buf, int r, int c) {
 //   3. K rows scaled in place by w_s = exp(lg - cs_s); U = (w ⊙ K)^T V into columns
 //      128..128+d_v (the tile's chunk state, d_k x d_v).
 //   4. (after 5) P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t,s)] on the causal half, bf16
-//      into the K buffer; O = P V into columns 0..d_v.
+//      into TMEM columns 128..191 (the state's, read out by then); O = P V into columns
+//      0..d_v.
 //   5. Right after the state MMA (before P): U_j is published (staged bf16 in the K
 //      buffer, stored coalesced); for odd j the CTA then forms the block state of slot
 //      j+1 (below) and publishes it.  Q stays in shared memory for step 6.
 //   6. For every set bit m-1 of j, in increasing m: the block state of slot c_m by TMA
-//      into shared memory (two buffers), MMA Q Tot into one of two TMEM buffers (columns
-//      0.. and 128..), and the previous level's product added to O with the row weights
+//      into shared memory (K's tile holds one state of d_v = 128 or two of d_v = 64 and
+//      is free before P is built: the lowest levels load then if their flags are up;
+//      V's tile after P V), MMA Q Tot into one of two TMEM buffers (columns 0.. and
+//      128..), and the previous level's product added to O with the row weights
 //      lambda[t, 7+m] exp(cs_t + D_m).  D_m, the log decay from the block's end to the
 //      tile's start, is the sum of the log decays of the lower levels' blocks, which
 //      their producers store next to them.
@@ -156,9 +152,9 @@ __device__ __forceinline__ float block_scan256(float x, float* red) {
 struct FSmem {
   // byte offsets from the 1024-aligned base
   static constexpr int kQ = 0, kK = kOperand, kV = 2 * kOperand;
-  static constexpr int kBars = 3 * kOperand;                   // 11 mbarriers
+  static constexpr int kBars = 3 * kOperand;                   // 11 mbarriers (12 slots)
   static constexpr int kTslot = kBars + 12 * 8;
-  static constexpr int kInt = kTslot + 16;                     // ticket: 4 u32
+  static constexpr int kInt = kTslot + 16;                     // ticket, loads per buffer
   static constexpr int kRed = kInt + 16;                       // 8 floats
   static constexpr int kLg = kRed + 32;                        // 4 floats
   static constexpr int kNl = kLg + 16;                         // kMaxChunkLevels floats
@@ -198,6 +194,9 @@ struct Dv {
   static constexpr int kPanels = DV / 64;                     // 64-column panels of d_v
   static constexpr int kStatePieces = kStateBytes / 16 / 256; // per thread: 8 or 4
   static constexpr int kHalf = DV / 2;                        // d_v columns per thread
+  // shared buffers for the levels' block states: K's tile (one state of d_v = 128, two of
+  // d_v = 64) and V's
+  static constexpr int kNodeBufs = DV == 64 ? 3 : 2;
 };
 
 template <int DV>
@@ -227,10 +226,10 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint64_t* bar_u = &bars[2];
   uint64_t* bar_o = &bars[3];
   uint64_t* bar_lvl = &bars[4];      // [2]: level MMAs
-  uint64_t* bar_node = &bars[6];     // [2]: block-state loads
-  uint64_t* bar_free = &bars[8];     // [2]: every warp has read a level's TMEM buffer
+  uint64_t* bar_node = &bars[6];     // [3]: block-state loads, one per shared buffer
+  uint64_t* bar_free = &bars[9];     // [2]: every warp has read a level's TMEM buffer
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + FSmem::kTslot);
-  uint32_t* ints = reinterpret_cast<uint32_t*>(smem + FSmem::kInt);  // [0] ticket
+  uint32_t* ints = reinterpret_cast<uint32_t*>(smem + FSmem::kInt);  // ticket, loads[3]
   float* red = reinterpret_cast<float*>(smem + FSmem::kRed);
   float* lg_s = reinterpret_cast<float*>(smem + FSmem::kLg);
   float* nl_s = reinterpret_cast<float*>(smem + FSmem::kNl);
@@ -257,7 +256,8 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     prefetch_tensormap(&tmOut);
     prefetch_tensormap(&tmU);
     prefetch_tensormap(&tmNode);
-    for (int q = 0; q < 8; ++q) mbar_init(&bars[q], 1);
+    for (int q = 0; q < 9; ++q) mbar_init(&bars[q], 1);
+    for (int q = 1; q < 4; ++q) ints[q] = 0;
     mbar_init(&bar_free[0], kThreadsF / 32);
     mbar_init(&bar_free[1], kThreadsF / 32);
     fence_mbar_init();
@@ -453,8 +453,57 @@ __global__ void __launch_bounds__(kThreadsF, 2)
 
   __syncthreads();  // the staged U in Kb is no longer read
 
-  // ---- P, bf16 into Kb (the state MMA is done with it).  The two warps of
-  // quarter qt take the 32-column chunks of their parity: chunks c > qt lie above the
+  // ---- the levels' block states.  Level k (the k-th set bit of j, from the lowest) is
+  // owned by thread 32+k: it finds its slot c, acquires the slot's ready flag (which
+  // carries the block's log decay) and issues the TMA load itself, after a proxy fence,
+  // so the acquire and the async-proxy read are ordered in one thread.  Level k goes to
+  // shared buffer k mod kNodeBufs: K's tile (free now; one buffer for d_v = 128, two for
+  // d_v = 64), then V's (free once P V is done).  The block state of slot c is U_{c-1}
+  // for odd c.
+  int my_c = 0;         // thread 32+k, k < nlev: the slot of level k
+  bool acquired = false;
+  {
+    const int k = tid - 32;
+    if (k >= 0 && k < nlev) {
+      int m = 0;
+      for (int seen = -1; seen < k;) {
+        ++m;
+        if ((j >> (m - 1)) & 1) ++seen;
+      }
+      my_c = (j >> (m - 1)) << (m - 1);
+    }
+  }
+  auto node_buf = [&](int b) -> uint8_t* {
+    return b == G::kNodeBufs - 1 ? Vb : Kb + b * G::kStateBytes;
+  };
+  auto fetch = [&](int k) {  // thread 32+k: TMA of level k's block state
+    if (tid == 32 + k) {
+      const int b = k % G::kNodeBufs;
+      uint8_t* dst = node_buf(b);
+      const bool is_u = (my_c & 1) != 0;
+      const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
+      atomicAdd(&ints[1 + b], 1u);
+      mbar_arrive_expect_tx(&bar_node[b], G::kStateBytes);
+#pragma unroll
+      for (int pv = 0; pv < G::kPanels; ++pv)
+        tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[b], dst + pv * kPanel, 64 * pv, row0);
+    }
+  };
+  // levels whose buffer lies in K's tile: load now if the flag is already up (one poll)
+  if (all_ok && tid >= 32 && tid - 32 < nlev && tid - 32 < G::kNodeBufs - 1) {
+    const uint32_t fv = ld_acquire_gpu(my_c & 1 ? &rdy_u[my_c - 1] : &rdy_n[my_c]);
+    if (fv != 0) {
+      acquired = true;
+      nl_s[tid - 32] = flag_decay(fv);
+      fence_proxy_async_global();
+      fetch(tid - 32);
+    }
+  }
+  __syncwarp();
+
+  // ---- P, bf16 (two per column) into TMEM columns 128..191: the state's columns, read
+  // out above.  The two warps of quarter qt take the 32-column chunks of their parity;
+  // chunk c of row r goes to columns [128 + 16c, +16).  Chunks c > qt lie above the
   // diagonal (zero), chunks c < qt below it (level 5 + bit_length(qt XOR c) for every
   // pair), chunk qt holds the diagonal.
   if (all_ok) {
@@ -494,74 +543,50 @@ __global__ void __launch_bounds__(kThreadsF, 2)
             sv[k] = v;
           }
         }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) sv[k] = 0.f;
       }
-      if (c > qt)
-        put_row32_zero(Kb, r, c);
-      else
-        put_row32_bf16(Kb, r, c, sv);
+      uint32_t pw[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pw[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
+      tmem_st16(tmem + lane_base + 128 + 16 * c, pw);
     }
+    tmem_wait_st();
   }
-  tc_fence_after();
-  fence_proxy_async_smem();
   tc_fence_before();
   all_ok = __syncthreads_and(ok);
-  // ---- O = P V into columns 0..DV (V MN-major as B)
+  // ---- O = P V into columns 0..DV (P from TMEM, V MN-major as B)
   if (all_ok && tid == 0) {
     tc_fence_after();
     constexpr uint32_t idesc = idesc_bf16(128, DV, 0, 1);
-    const uint32_t pa = smem_u32(Kb), va = smem_u32(Vb);
+    const uint32_t va = smem_u32(Vb);
 #pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk) {
-      const uint32_t aoff = (kk >> 2) * kPanel + (kk & 3) * 32;
-      mma_bf16(tmem, smem_desc_sw128(pa + aoff, 16, 1024),
-               smem_desc_sw128(va + kk * 2048, kPanel, 1024), idesc, kk > 0);
-    }
+    for (int kk = 0; kk < kTile / 16; ++kk)
+      mma_bf16_ts(tmem, tmem + 128 + 8 * kk, smem_desc_sw128(va + kk * 2048, kPanel, 1024), idesc,
+                  kk > 0);
     mma_commit(bar_o);
   }
   __syncwarp();
 
-  // ---- while P V runs, the levels' block states: thread 32+k (warp 1) acquires level
-  // k's ready flag now and later issues its TMA load itself (after a proxy fence), so the
-  // acquire and the async-proxy read are ordered in one thread.  The block state of slot
-  // c is U_{c-1} for odd c.
-  int my_c = 0;  // thread 32+k, k < nlev: the slot of level k
+  // ---- while P V runs, the remaining levels' flags (waited for, bounded)
   {
     bool fl = true;
     const int k = tid - 32;
-    if (k >= 0 && k < nlev) {
-      int m = 0;
-      for (int seen = -1; seen < k;) {
-        ++m;
-        if ((j >> (m - 1)) & 1) ++seen;
-      }
-      my_c = (j >> (m - 1)) << (m - 1);
-      const bool is_u = (my_c & 1) != 0;
+    if (k >= 0 && k < nlev && !acquired) {
       uint32_t fv;
-      fl = wait_flag_acquire_value(is_u ? &rdy_u[my_c - 1] : &rdy_n[my_c], &fv);
+      fl = wait_flag_acquire_value(my_c & 1 ? &rdy_u[my_c - 1] : &rdy_n[my_c], &fv);
       nl_s[k] = fl ? flag_decay(fv) : 0.f;
       fence_proxy_async_global();
     }
     if (!__syncthreads_and(fl) && tid == 0) atomicOr(&g_tc_error, 2u);
   }
-  // ---- O = P V is done: Kb and Vb are free
+  // ---- O = P V is done: V's tile is free
   ok = all_ok && mbar_wait(bar_o, 0);
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
-  auto fetch = [&](int k) {  // thread 32+k: TMA of level k's block state into (k odd ? Kb : Vb)
-    if (tid == 32 + k) {
-      uint8_t* dst = (k & 1) ? Kb : Vb;
-      const bool is_u = (my_c & 1) != 0;
-      const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
-      mbar_arrive_expect_tx(&bar_node[k & 1], G::kStateBytes);
-#pragma unroll
-      for (int pv = 0; pv < G::kPanels; ++pv)
-        tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[k & 1], dst + pv * kPanel, 64 * pv, row0);
-    }
-  };
-  if (all_ok) {  // Kb (U staging) and Vb are free
-    if (nlev > 0) fetch(0);
-    if (nlev > 1) fetch(1);
-  }
+  if (all_ok && tid >= 32 && tid - 32 < nlev && tid - 32 < G::kNodeBufs && !acquired)
+    fetch(tid - 32);
   __syncwarp();
 
   // ---- O from TMEM into registers: this thread's half row, columns [DV/2 hh, +DV/2)
@@ -581,30 +606,32 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   tc_fence_before();
   __syncthreads();  // TMEM is free
 
-  // ---- inter-chunk levels, without block barriers.  Level k (the k-th set bit of j,
-  // from the lowest) uses shared buffer (k odd ? Kb : Vb) and TMEM columns
-  // [128 (k&1), +DV).  Thread 0 issues MMA k once its block state has landed
-  // (bar_node[k&1]) and every warp has added level k-2 to O (bar_free[k&1]); each warp
-  // adds level k-1 to O once MMA k-1 is done (bar_lvl), then releases that TMEM buffer.
-  // The load of level k+1 starts as soon as MMA k-1 is done with its shared buffer
-  // (levels 0 and 1 were started above).
+  // ---- inter-chunk levels, without block barriers.  Level k uses shared buffer
+  // k mod kNodeBufs and TMEM columns [128 (k&1), +DV).  Thread 0 issues MMA k once its
+  // block state has landed and every warp has added level k-2 to O (bar_free[k&1]); each
+  // warp adds level k-1 to O once MMA k-1 is done (bar_lvl), then releases that TMEM
+  // buffer.  The load of level k-1+kNodeBufs starts as soon as MMA k-1 is done with its
+  // shared buffer.
   const int lane = tid & 31;
-  uint32_t lvl_ph[2] = {0, 0}, node_ph[2] = {0, 0}, free_ph[2] = {0, 0};
+  uint32_t lvl_ph = 0, node_ph = 0, free_ph = 0;  // phase bits per buffer
+  uint32_t consumed = 0;  // thread 0: block-state loads waited for, 8 bits per buffer
   float D = 0.f;  // log decay from block k's end to the tile's start
   bool lv_ok = all_ok;
+  int nb = 0;  // k mod kNodeBufs
   for (int k = 0; k <= nlev && all_ok; ++k) {
     if (tid == 0 && k < nlev) {  // issue level k
-      bool go = lv_ok && mbar_wait(&bar_node[k & 1], node_ph[k & 1]);
-      node_ph[k & 1] ^= 1;
+      bool go = lv_ok && mbar_wait(&bar_node[nb], (node_ph >> nb) & 1);
+      node_ph ^= 1u << nb;
+      if (go) consumed += 1u << (8 * nb);
       if (k >= 2) {
-        go = go && mbar_wait(&bar_free[k & 1], free_ph[k & 1]);
-        free_ph[k & 1] ^= 1;
+        go = go && mbar_wait(&bar_free[k & 1], (free_ph >> (k & 1)) & 1);
+        free_ph ^= 1u << (k & 1);
       }
       if (go) {
         tc_fence_after();
         // A = Q (K-major), B = the block state [d_k][d_v] (MN-major, like V in P V)
         constexpr uint32_t idesc = idesc_bf16(128, DV, 0, 1);
-        const uint32_t qa = smem_u32(Qb), sa = smem_u32((k & 1) ? Kb : Vb);
+        const uint32_t qa = smem_u32(Qb), sa = smem_u32(node_buf(nb));
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
@@ -615,17 +642,18 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       }
       lv_ok = go;
     }
+    nb = nb + 1 == G::kNodeBufs ? 0 : nb + 1;
     __syncwarp();
     if (k >= 1) {  // level k-1 into O
       const int bf = (k - 1) & 1;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_lvl[bf], lvl_ph[bf]));
-      lvl_ph[bf] ^= 1;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_lvl[bf], (lvl_ph >> bf) & 1));
+      lvl_ph ^= 1u << bf;
       if (!got) {
         lv_ok = false;
         break;
       }
       tc_fence_after();
-      if (k + 1 < nlev) fetch(k + 1);  // thread 33+k, into the buffer MMA k-1 read
+      if (k - 1 + G::kNodeBufs < nlev) fetch(k - 1 + G::kNodeBufs);  // into MMA k-1's buffer
       const float wr = lamx[(k - 1) * kTile + r] * __expf(cs + D);
       D += nl_s[k - 1];
 #pragma unroll
@@ -673,6 +701,14 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && !all_ok) {
+    // after an error: wait (bounded) for the loads still in flight into this CTA's
+    // shared memory before it is handed to another CTA
+    if (!landed) mbar_wait(bar_load, 0);
+    for (int b = 0; b < G::kNodeBufs; ++b)
+      for (uint32_t c = (consumed >> (8 * b)) & 255u; c < ints[1 + b]; ++c)
+        mbar_wait(&bar_node[b], c & 1);
+  }
   if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
