@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   __syncwarp();
 
   // ---- per-row data: log a, the intra-tile lambdas, the raw inter-level lambdas (the
-  // two threads of a row split the loads)
+  // two threads of a row split the loads; the last ones go straight to shared memory)
   const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
   float lam_in[kIntraLevels / 2];
 #pragma unroll
@@ -313,7 +313,9 @@ __global__ void __launch_bounds__(kThreadsF, 2)
 #pragma unroll 4
     for (int m = 1; m < kMaxChunkLevels; ++m) {
       if (!((j >> (m - 1)) & 1)) continue;
-      if ((k & 1) == hh) lamx[k * kTile + r] = row_live ? p.lam[row * p.L + kTileLc + m] : 0.f;
+      if ((k & 1) == hh)  // copied in the background: read only by the level loop
+        cp_async4(&lamx[k * kTile + r], row_live ? p.lam + row * p.L + kTileLc + m : p.lam,
+                  row_live ? 4u : 0u);
       ++k;
     }
   }
@@ -603,6 +605,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       for (int q = 0; q < 32; ++q) o[c * 32 + q] = v[q];
     }
   }
+  cp_async_wait_all();  // the inter-level lambdas
   tc_fence_before();
   __syncthreads();  // TMEM is free
 
