@@ -13,7 +13,8 @@
 //     decayed from the block's end to t by exp(D_m + cs_t) (D_m = sum of the tile log
 //     decays over [c, j), cs_t = log decay from tile j's start to t);
 //   * every other level is zero.
-// One CTA per (level, b, h); a level is written whole.
+// One CTA per (level, b, h, slice of 32 state rows), so that a few CTAs per SM keep
+// enough loads and stores in flight.
 #include "ll_internal.cuh"
 
 namespace ll {
@@ -21,7 +22,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxTile = 128;   // largest tile of either forward path
-constexpr int kMaxDim = 128;    // d_k, d_v <= 128 (16 x 16 threads of 8 x 8 outputs)
+constexpr int kMaxDim = 128;    // d_k, d_v <= 128
+constexpr int kSliceRows = 32;  // state rows per CTA (4 x 64 threads of 8 rows x 2 columns)
 
 template <typename InT>
 __device__ __forceinline__ float ld(const void* p, int64_t i) {
@@ -58,16 +60,21 @@ __device__ float block_sum(float x, float* sh) {
 
 // tc_layout: block states are bf16 (tensor-core path; odd slots are U_{c-1}); otherwise
 // fp32 for every slot.  Both are row-major [d_k][d_v], the layout of the state.
+// One CTA per (level, b*h, slice of kSliceRows state rows).
 template <typename InT, bool kTcLayout>
 __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, float* state) {
   extern __shared__ float sm[];
   const int lvl = blockIdx.x;
   const int64_t bh = blockIdx.y;
+  const int r0 = blockIdx.z * kSliceRows;  // this CTA's state rows [r0, r0 + rows)
   const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
-  const int dk = a.dk, dv = a.dv, tile = a.C, lc = a.lc;
-  const int64_t elems = (int64_t)dk * dv;
-  float* S = state + (bh * a.L + lvl) * elems;
+  const int dk = a.dk, dv = a.dv, lc = a.lc;
+  if (r0 >= dk) return;
+  const int rows = min(kSliceRows, dk - r0);
+  const int64_t elems = (int64_t)rows * dv;  // of this slice, contiguous in the state
+  float* S = state + (bh * a.L + lvl) * (int64_t)dk * dv + (int64_t)r0 * dv;
   const int t = a.T - 1, j = t >> lc, t0 = j << lc;
+  const bool vec = (dv & 7) == 0;  // 8 columns per step: 16-byte loads and stores
 
   // this level's bucket [lo, hi) of positions
   int lo, hi;
@@ -82,7 +89,12 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
     lo = hi - (has ? 1 << (lvl - 1) : 0);
   }
   if (!has) {
-    for (int64_t i = threadIdx.x; i < elems; i += kThreads) S[i] = 0.f;
+    if (vec) {
+      for (int64_t i = threadIdx.x; i < elems / 4; i += kThreads)
+        reinterpret_cast<float4*>(S)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      for (int64_t i = threadIdx.x; i < elems; i += kThreads) S[i] = 0.f;
+    }
     return;
   }
 
@@ -90,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
   float* red = sm;                  // [32]
   float* cs = sm + 32;              // [kMaxTile]
   float* w = cs + kMaxTile;         // [kMaxTile] weights of the bucket's positions
-  float* ks = w + kMaxTile;         // [bucket][128], then v
+  float* ks = w + kMaxTile;         // [bucket][kSliceRows], then v [bucket][128]
   const int n = t - t0 + 1;         // positions of tile j up to t
   {
     const float la = (a.log_a && (int)threadIdx.x < n)
@@ -103,53 +115,53 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
   const float cs_t = cs[n - 1];
 
   if (lvl <= lc) {
-    // a range of positions inside tile j: sum_s exp(cs_t - cs_s) k_s v_s^T, as outer
-    // products accumulated in registers: thread (td, te) owns the 8 x 8 block of rows
-    // [8 td, 8 td + 8) and columns [8 te, 8 te + 8); rows of k (scaled by the decay) and
-    // of v are staged zero-padded to 128 columns.
+    // a range of positions inside tile j: sum_s exp(cs_t - cs_s) k_s v_s^T over the
+    // slice's rows, as outer products accumulated in registers: thread (td, te) owns rows
+    // [8 td, 8 td + 8) of the slice and columns 2 te, 2 te + 1; the slice's columns of k
+    // (scaled by the decay) and the rows of v are staged zero-padded.
     const int nb = hi - lo;
-    float* vs = ks + nb * kMaxDim;
+    float* vs = ks + nb * kSliceRows;
     for (int i = threadIdx.x; i < nb; i += kThreads) w[i] = __expf(cs_t - cs[lo - t0 + i]);
     __syncthreads();
+    // (unrolled, so that each thread has several loads in flight)
+#pragma unroll 8
+    for (int i = threadIdx.x; i < nb * kSliceRows; i += kThreads) {
+      const int r = i / kSliceRows, d = i - r * kSliceRows;
+      const int64_t tok_k = ((int64_t)b * a.T + lo + r) * a.Hqk + h / a.hg;
+      ks[i] = d < rows ? w[r] * ld<InT>(a.k, tok_k * dk + r0 + d) : 0.f;
+    }
+#pragma unroll 8
     for (int i = threadIdx.x; i < nb * kMaxDim; i += kThreads) {
       const int r = i / kMaxDim, d = i - r * kMaxDim;
       const int64_t tok = ((int64_t)b * a.T + lo + r) * a.H + h;
-      const int64_t tok_k = ((int64_t)b * a.T + lo + r) * a.Hqk + h / a.hg;
-      ks[i] = d < dk ? w[r] * ld<InT>(a.k, tok_k * dk + d) : 0.f;
       vs[i] = d < dv ? ld<InT>(a.v, tok * dv + d) : 0.f;
     }
     __syncthreads();
-    const int td = threadIdx.x >> 4, te = threadIdx.x & 15;
-    float acc[8][8];
+    const int td = threadIdx.x >> 6, te = threadIdx.x & 63;
+    float acc[8][2];
 #pragma unroll
-    for (int x = 0; x < 8; ++x)
-#pragma unroll
-      for (int y = 0; y < 8; ++y) acc[x][y] = 0.f;
+    for (int x = 0; x < 8; ++x) acc[x][0] = acc[x][1] = 0.f;
     for (int r = 0; r < nb; ++r) {
-      const float4* kr = reinterpret_cast<const float4*>(ks + r * kMaxDim + 8 * td);
-      const float4* vr = reinterpret_cast<const float4*>(vs + r * kMaxDim + 8 * te);
-      const float4 k0 = kr[0], k1 = kr[1], v0 = vr[0], v1 = vr[1];
+      const float4* kr = reinterpret_cast<const float4*>(ks + r * kSliceRows + 8 * td);
+      const float2 vv = reinterpret_cast<const float2*>(vs + r * kMaxDim)[te];
+      const float4 k0 = kr[0], k1 = kr[1];
       const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-      const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-      for (int x = 0; x < 8; ++x)
-#pragma unroll
-        for (int y = 0; y < 8; ++y) acc[x][y] = fmaf(kk[x], vv[y], acc[x][y]);
+      for (int x = 0; x < 8; ++x) {
+        acc[x][0] = fmaf(kk[x], vv.x, acc[x][0]);
+        acc[x][1] = fmaf(kk[x], vv.y, acc[x][1]);
+      }
     }
 #pragma unroll
     for (int x = 0; x < 8; ++x) {
       const int d = 8 * td + x;
-      if (d >= dk) break;
+      if (d >= rows) break;
       float* row = S + (int64_t)d * dv;
-      if ((dv & 7) == 0 && 8 * te < dv) {  // two aligned 16-byte stores
-        reinterpret_cast<float4*>(row + 8 * te)[0] =
-            make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
-        reinterpret_cast<float4*>(row + 8 * te)[1] =
-            make_float4(acc[x][4], acc[x][5], acc[x][6], acc[x][7]);
+      if ((dv & 1) == 0 && 2 * te < dv) {
+        reinterpret_cast<float2*>(row)[te] = make_float2(acc[x][0], acc[x][1]);
       } else {
-#pragma unroll
-        for (int y = 0; y < 8; ++y)
-          if (8 * te + y < dv) row[8 * te + y] = acc[x][y];
+        if (2 * te < dv) row[2 * te] = acc[x][0];
+        if (2 * te + 1 < dv) row[2 * te + 1] = acc[x][1];
       }
     }
     return;
@@ -162,13 +174,38 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
   for (int i = c + (int)threadIdx.x; i < j; i += kThreads) D += a.lg[bh * a.N + i];
   D = block_sum(D, red);
   const float g = __expf(D + cs_t);
+  const int64_t src0 = (bh * a.N + ((kTcLayout && (c & 1)) ? c - 1 : c)) * (int64_t)dk * dv +
+                       (int64_t)r0 * dv;
   if (kTcLayout) {
-    const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(
-        (c & 1) ? a.U : a.nodes) + (bh * a.N + ((c & 1) ? c - 1 : c)) * elems;
-    for (int64_t i = threadIdx.x; i < elems; i += kThreads) S[i] = g * __bfloat162float(src[i]);
+    const __nv_bfloat16* src =
+        reinterpret_cast<const __nv_bfloat16*>((c & 1) ? a.U : a.nodes) + src0;
+    if (vec) {  // 8 bf16 in, 8 fp32 out
+      for (int64_t i = threadIdx.x; i < elems / 8; i += kThreads) {
+        const uint4 u = __ldcs(reinterpret_cast<const uint4*>(src) + i);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+          f[2 * e] = g * x.x;
+          f[2 * e + 1] = g * x.y;
+        }
+        reinterpret_cast<float4*>(S)[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(S)[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < elems; i += kThreads) S[i] = g * __bfloat162float(src[i]);
+    }
   } else {
-    const float* src = reinterpret_cast<const float*>(a.nodes) + (bh * a.N + c) * elems;
-    for (int64_t i = threadIdx.x; i < elems; i += kThreads) S[i] = g * src[i];
+    const float* src = reinterpret_cast<const float*>(a.nodes) + src0;
+    if (vec) {
+      for (int64_t i = threadIdx.x; i < elems / 4; i += kThreads) {
+        const float4 x = __ldcs(reinterpret_cast<const float4*>(src) + i);
+        reinterpret_cast<float4*>(S)[i] = make_float4(g * x.x, g * x.y, g * x.z, g * x.w);
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < elems; i += kThreads) S[i] = g * src[i];
+    }
   }
 }
 
@@ -180,8 +217,9 @@ cudaError_t launch_prefill_state(const FwdArgs& a, bool tc_layout, int in_dtype,
   if (a.dk > kMaxDim || a.dv > kMaxDim) return cudaErrorInvalidValue;
   const int nb_max = a.C / 2 > 1 ? a.C / 2 : 1;  // largest bucket inside a tile
   const size_t smem =
-      sizeof(float) * (32 + 2 * kMaxTile + (size_t)nb_max * 2 * kMaxDim);
-  const dim3 grid((unsigned)a.L, (unsigned)(a.B * a.H));
+      sizeof(float) * (32 + 2 * kMaxTile + (size_t)nb_max * (kSliceRows + kMaxDim));
+  const dim3 grid((unsigned)a.L, (unsigned)(a.B * a.H),
+                  (unsigned)((a.dk + kSliceRows - 1) / kSliceRows));
   cudaError_t e = cudaSuccess;
   if (in_dtype == LL_BF16) {
     if (tc_layout) {
