@@ -505,6 +505,7 @@ def run_ours(args, rank, world, local_rank):
                          "state_restored": "every timed step starts from the same state "
                                            "after t-1 (device copy outside the events)"}}
     gdn = measure_gdn_decode(LL, dcfg, state0, state, flush, peaks)
+    gdn_fwd = measure_gdn_fwd(LL, cfg, dev, flush, peaks)
     e2e = measure_e2e(LL, cfg, x, dev, ws, args)
     prefill = measure_prefill(LL, cfg, d, out, ws, flush, peaks)
     del ws
@@ -524,7 +525,7 @@ def run_ours(args, rank, world, local_rank):
            "fwd_ms": fwd_mean * 1e3, "fwd_stage_us": dict(zip(stage_names, [s * 1e6 for s in stage_mean])),
            "roofline": roofline, "roofline_fwd": roofline_fwd, "decode": decode, "e2e": e2e,
            "prefill": prefill, "backward": backward, "benchmark_shape": bench_shape,
-           "gdn_decode": gdn,
+           "gdn_decode": gdn, "gdn_fwd": gdn_fwd,
            "gpu_launches": args.steps * (n_kernels + 1), "clocks": clk,
            "wall_s_timed_region": wall}
     return res
@@ -578,6 +579,52 @@ def measure_gdn_decode(LL, dcfg, state0, state, flush, peaks, reps=20):
                          "achieved": dbytes / t / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": dbytes / t / 1e9 / peaks["hbm"], "algorithmic_bytes": dbytes,
                          "peak_source": peaks["src"], "traffic": None}}
+
+
+def gdn_fwd_algorithmic(cfg):
+    """Bytes the Gated DeltaNet forward must move: q, k, v, log a, beta and lambda in, out
+    out (the states stay on chip)."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    tok = cfg.B * cfg.T * cfg.H
+    return (cfg.B * cfg.T * cfg.qk_heads * 2 * cfg.dk * e + tok * cfg.dv * e + tok * 4 * 2 +
+            tok * cfg.L * 4 + tok * cfg.dv * e)
+
+
+def measure_gdn_fwd(LL, cfg, dev, flush, peaks, reps=3):
+    """The Log-Linear Gated DeltaNet forward (recurrent form) on the headline shape: median
+    of `reps` calls after one warm-up, L2 flushed before each (outside the events)."""
+    x = {k: (None if v is None else v.to(dev)) for k, v in W.make_gdn_inputs(cfg).items()}
+    out = torch.empty(cfg.B, cfg.T, cfg.H, cfg.dv, device=dev, dtype=torch.bfloat16)
+    run = lambda: LL.loglinear_gdn_fwd(x["q"], x["k"], x["v"], x["log_a"], x["beta"], x["lam"],
+                                       out=out)
+    run()
+    t = _median_us(run, flush, reps)
+    gbytes = gdn_fwd_algorithmic(cfg)
+    return {"workload": f"{cfg.name}: loglinear_gdn_fwd B{cfg.B} H{cfg.H} T{cfg.T} "
+                        f"dk=dv={cfg.dk} L{cfg.L} bf16 (recurrent form)",
+            "tokens_per_s": cfg.B * cfg.T * cfg.H / t, "ms": t * 1e3,
+            "roofline": {"kernel": "gdn_fwd_kernel", "bound": "hbm",
+                         "achieved": gbytes / t / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbytes / t / 1e9 / peaks["hbm"], "algorithmic_bytes": gbytes,
+                         "peak_source": peaks["src"], "traffic": None},
+            "note": "sequential in t: one lssb step per token per (b, h, 8 columns); far "
+                    "below the HBM roofline by construction (the chunked form is not built)"}
+
+
+def oracle_gdn_fwd_sample(cfg, seconds):
+    """Times the oracle's Gated DeltaNet recurrence (fp64 NumPy) on one (b, h) of the
+    headline shape for a prefix of the sequence; returns (tokens/s, description, threads)."""
+    import oracle
+    sub = dataclasses.replace(cfg, B=1, H=1, T=256, L=9)
+    x = W.make_gdn_inputs(sub)
+    calls, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds or calls == 0:
+        oracle.gdn_recurrence(x["q"], x["k"], x["v"], x["log_a"], x["beta"], x["lam"])
+        calls += 1
+    el = time.perf_counter() - t0
+    desc = (f"oracle gdn_recurrence (fp64 NumPy) on one (b, h), T={sub.T}, dk=dv={sub.dk}: "
+            f"{calls} calls in {el:.1f} s; tokens of that sample per second")
+    return calls * sub.T / el, desc, _blas_threads()
 
 
 def measure_prefill(LL, cfg, d, out, ws, flush, peaks, reps=10):
@@ -943,6 +990,9 @@ def main():
         gtok_s, gdesc, gthr = oracle_gdn_decode_sample(W.DECODE_CONFIG, max(2.0, args.cpu_seconds / 3))
         res["gdn_decode"]["cpu_baseline"] = {"value": gtok_s, "unit": "tokens/s", "cores": gthr,
                                              "kind": "oracle", "sample": gdesc}
+        ftok_s, fdesc, fthr = oracle_gdn_fwd_sample(cfg, max(2.0, args.cpu_seconds / 5))
+        res["gdn_fwd"]["cpu_baseline"] = {"value": ftok_s, "unit": "tokens/s", "cores": fthr,
+                                          "kind": "oracle", "sample": fdesc}
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

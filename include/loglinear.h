@@ -254,6 +254,31 @@ LL_API int loglinear_gdn_decode_step(float* state, const void* q, const void* k,
                                      int out_dtype, ll_stream_t stream);
 
 /*
+ * Forward of Log-Linear Gated DeltaNet over a whole sequence, in the recurrent form: the
+ * lssb step of loglinear_gdn_decode_step applied at t = 0..T-1 for every (b, h), with every
+ * level's state kept on chip (same sources as loglinear_gdn_decode_step).  Equivalently
+ *   o_t = sum_{s<=t} lambda[t, level(t, s)] beta_s (q_t^T A_t ... A_{s+1} k_s) v_s,
+ * the model's own attention matrix composed with the Fenwick mask.
+ *   q, k       [B, T, Hqk, dk] in_dtype, 4-byte aligned (heads shared as in loglinear_fwd);
+ *              k is expected to have unit length (not checked)
+ *   v          [B, T, H, dv] in_dtype
+ *   log_a      [B, T, H] fp32 or NULL (alpha = 1);  beta [B, T, H] fp32
+ *   lambda     [B, T, H, L] fp32, L >= bit_length(T-1) + 1
+ *   out        [B, T, H, dv] out_dtype, overwritten
+ *   state_out  NULL, or [B, H, L, dk, dv] fp32, overwritten with the per-level state after
+ *              position T-1 (all zero for T = 0): the state loglinear_gdn_decode_step
+ *              continues from at t = T
+ * Supported: 1 <= dk, dv <= 128 (dk even for bf16), L <= 64.  The recurrence is sequential
+ * in t (one CTA per (b, h, 8 columns of d_v)); the chunked form is not provided.
+ * Errors: LL_ERR_INVALID, LL_ERR_SHAPE, LL_ERR_DTYPE, LL_ERR_UNSUPPORTED, LL_ERR_ALIGN,
+ * LL_ERR_CUDA.
+ */
+LL_API int loglinear_gdn_fwd(const void* q, const void* k, const void* v, const float* log_a,
+                             const float* beta, const float* lambda, void* out, float* state_out,
+                             int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk, int64_t dv,
+                             int64_t L, int in_dtype, int out_dtype, ll_stream_t stream);
+
+/*
  * Backward of loglinear_fwd (page "算力终结者来了！…", sections 结构矩阵 and 讨论与局限性:
  * training takes the gradients of the attention terms and of the level weights lambda):
  * given dout = dL/dO, the gradients of L with respect to every input, for

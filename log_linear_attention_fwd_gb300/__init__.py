@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     loglinear_fwd_noalloc,
     loglinear_fwd_with_events,
     loglinear_gdn_decode_step,
+    loglinear_gdn_fwd,
     loglinear_prefill,
     loglinear_prefill_with_events,
     resolve_path,

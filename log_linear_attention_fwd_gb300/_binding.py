@@ -54,6 +54,8 @@ SIGNATURES = {
                                      _i64, _i64, _i64, _int, _int, _vp]),
     "loglinear_gdn_decode_step": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i64, _i64,
                                          _i64, _i64, _i64, _i64, _int, _int, _vp]),
+    "loglinear_gdn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                 _i64, _i64, _i64, _int, _int, _vp]),
     "loglinear_debug_level_map": (_int, [_i64, _int, _int, _vp, _vp]),
     "loglinear_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "loglinear_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
@@ -254,6 +256,33 @@ def loglinear_gdn_decode_step(state, q, k, v, log_a, beta, lam, t, out=None, out
                                         dv, L, _dtype_code(q), _dtype_code(out), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_gdn_decode_step")
+    return out
+
+
+def loglinear_gdn_fwd(q, k, v, log_a, beta, lam, out=None, out_dtype=None, state=None,
+                      stream=None):
+    """Log-Linear Gated DeltaNet over a whole sequence (recurrent form).  q, k [B,T,Hqk,dk];
+    v [B,T,H,dv]; log_a [B,T,H] fp32 or None; beta [B,T,H] fp32; lam [B,T,H,L] fp32.
+    Returns out [B,T,H,dv]; when `state` ([B,H,L,dk,dv] fp32) is given it receives the
+    per-level state after position T-1."""
+    B, T, Hqk, dk = q.shape
+    H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
+    _check_dev("q", q)
+    _check_dev("k", k, q.dtype, (B, T, Hqk, dk))
+    _check_dev("v", v, q.dtype, (B, T, H, dv))
+    _check_dev("log_a", log_a, torch.float32, (B, T, H))
+    _check_dev("beta", beta, torch.float32, (B, T, H))
+    _check_dev("lam", lam, torch.float32, (B, T, H, L))
+    if state is not None:
+        _check_dev("state", state, torch.float32, (B, H, L, dk, dv))
+    if out is None:
+        out = torch.empty(B, T, H, dv, device=q.device, dtype=out_dtype or q.dtype)
+    _check_dev("out", out, shape=(B, T, H, dv))
+    st = _lib.loglinear_gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(beta), _ptr(lam),
+                                _ptr(out), _ptr(state), B, T, H, Hqk, dk, dv, L, _dtype_code(q),
+                                _dtype_code(out), _stream(stream))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_gdn_fwd")
     return out
 
 

@@ -206,6 +206,12 @@ cudaError_t launch_gdn_decode(float* state, const void* q, const void* k, const 
                               const float* log_a, const float* beta, const float* lam, void* out,
                               int B, int H, int Hqk, int dk, int dv, int L, const DecodePlan& plan,
                               int in_dtype, int out_dtype, cudaStream_t s);
+// Log-Linear Gated DeltaNet forward in the recurrent form (levels = bit_length(T-1) + 1
+// Fenwick levels in use); state, when non-null, receives the per-level state after T-1.
+cudaError_t launch_gdn_fwd(const void* q, const void* k, const void* v, const float* log_a,
+                           const float* beta, const float* lam, void* out, float* state, int B,
+                           int T, int H, int Hqk, int dk, int dv, int L, int levels, int in_dtype,
+                           int out_dtype, cudaStream_t s);
 
 cudaError_t launch_level_map(int T, int tile, int lc, int8_t* levels, cudaStream_t s);
 

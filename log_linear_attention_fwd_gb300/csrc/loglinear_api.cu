@@ -428,6 +428,30 @@ int loglinear_gdn_decode_step(float* state, const void* q, const void* k, const 
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 
+int loglinear_gdn_fwd(const void* q, const void* k, const void* v, const float* log_a,
+                      const float* beta, const float* lambda, void* out, float* state_out,
+                      int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t dk, int64_t dv,
+                      int64_t L, int in_dtype, int out_dtype, ll_stream_t stream) {
+  if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1 || L < 1) return LL_ERR_INVALID;
+  const int sh = check_qk_heads(H, Hqk);
+  if (sh != LL_OK) return sh;
+  if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return LL_ERR_DTYPE;
+  if (T > INT32_MAX || dk > kMaxHeadDim || dv > kMaxHeadDim || L > 64) return LL_ERR_UNSUPPORTED;
+  if (in_dtype == LL_BF16 && (dk & 1)) return LL_ERR_UNSUPPORTED;
+  if (B * H > INT32_MAX / 16) return LL_ERR_UNSUPPORTED;
+  const int levels = T > 0 ? bit_length(T - 1) + 1 : 1;
+  if (L < levels) return LL_ERR_SHAPE;
+  if (B == 0 || H == 0) return LL_OK;
+  if (T > 0 && (!q || !k || !v || !beta || !lambda || !out)) return LL_ERR_INVALID;
+  if (T > 0 && (reinterpret_cast<uintptr_t>(q) % 4 || reinterpret_cast<uintptr_t>(k) % 4))
+    return LL_ERR_ALIGN;
+  if (state_out && reinterpret_cast<uintptr_t>(state_out) % 4) return LL_ERR_ALIGN;
+  const cudaError_t e = launch_gdn_fwd(q, k, v, log_a, beta, lambda, out, state_out, (int)B,
+                                       (int)T, (int)H, (int)Hqk, (int)dk, (int)dv, (int)L, levels,
+                                       in_dtype, out_dtype, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LL_OK : cuda_fail(e);
+}
+
 // ---------------------------------------------------------------- backward
 
 // N: 32-token tiles of the CUDA-core part; *n_tc: 128-token tiles of the tensor-core dQ

@@ -268,3 +268,30 @@ def test_bwd_validation_codes(L):
     simt = L.bwd_workspace_size(1, 1000, 2, 2, 128, 64, 11, L.LL_BF16, L.LL_BF16, "simt")
     assert tc >= simt + 1000 * 2 * 64 * 2
     assert L.bwd_workspace_size(1, 1000, 2, 2, 128, 64, 11, L.LL_BF16, L.LL_BF16) == tc
+
+
+def test_gdn_fwd_validation_codes(L):
+    """The Gated DeltaNet forward checks its arguments before touching the GPU."""
+    f = L.lib().loglinear_gdn_fwd
+    p = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation first
+    ok = dict(q=p, k=p, v=p, log_a=None, beta=p, lam=p, out=p, state=None, B=1, T=100, H=2,
+              Hqk=2, dk=8, dv=8, L=8, i=0, o=0, s=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["k"], a["v"], a["log_a"], a["beta"], a["lam"], a["out"], a["state"],
+                 a["B"], a["T"], a["H"], a["Hqk"], a["dk"], a["dv"], a["L"], a["i"], a["o"], a["s"])
+
+    assert call(beta=None) == L.LL_ERR_INVALID
+    assert call(T=-1) == L.LL_ERR_INVALID
+    assert call(L=7) == L.LL_ERR_SHAPE                # T = 100 needs L >= 8
+    assert call(Hqk=3) == L.LL_ERR_SHAPE
+    assert call(dk=129) == L.LL_ERR_UNSUPPORTED
+    assert call(dv=129) == L.LL_ERR_UNSUPPORTED
+    assert call(L=65) == L.LL_ERR_UNSUPPORTED
+    assert call(dk=7, i=1) == L.LL_ERR_UNSUPPORTED    # bf16 rows of odd length
+    assert call(o=5) == L.LL_ERR_DTYPE
+    assert call(q=ctypes.c_void_p(18)) == L.LL_ERR_ALIGN
+    assert call(state=ctypes.c_void_p(19)) == L.LL_ERR_ALIGN
+    assert call(B=0) == L.LL_OK                       # empty: nothing to do
+    assert call(H=0, Hqk=0) in (L.LL_OK, L.LL_ERR_SHAPE)
