@@ -801,18 +801,25 @@ cudaError_t launch_typed(const BwdArgs& A, cudaStream_t s) {
 
 }  // namespace
 
-BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, int64_t dk,
-                                  int64_t dv, int64_t n_tc) {
+BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t N,
+                                  int64_t dk, int64_t dv, int64_t n_tc) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   BwdWorkspace w;
-  const size_t states = (size_t)(B * H * N) * (size_t)(dk * dv) * sizeof(float);
   const size_t rows = (size_t)(B * T * H);
+  // CUDA cores: chunk states, fp32 block states of every slot, tile log decays, and
+  // per-head fp32 dq and dk.  Tensor cores: the mirrored states on the 128-token tiles in
+  // U's place (the block states come from the forward's workspace below), and fp32 dq and
+  // dk per q/k head only when heads share them.
+  const size_t states = (size_t)(B * H * (n_tc > 0 ? n_tc : N)) * (size_t)(dk * dv) * sizeof(float);
+  const size_t nodes = n_tc > 0 ? 0 : states;
+  const size_t lg = n_tc > 0 ? 0 : (size_t)(B * H * N) * sizeof(float);
+  const size_t qk_rows = n_tc > 0 ? (Hqk < H ? (size_t)(B * T * Hqk) : 0) : rows;
   w.off_U = 0;
   w.off_nodes = up(w.off_U + states);
-  w.off_lg = up(w.off_nodes + states);
-  w.off_dqh = up(w.off_lg + (size_t)(B * H * N) * sizeof(float));
-  w.off_dkh = up(w.off_dqh + rows * dk * sizeof(float));
-  w.off_dcq = up(w.off_dkh + rows * dk * sizeof(float));
+  w.off_lg = up(w.off_nodes + nodes);
+  w.off_dqh = up(w.off_lg + lg);
+  w.off_dkh = up(w.off_dqh + qk_rows * dk * sizeof(float));
+  w.off_dcq = up(w.off_dkh + qk_rows * dk * sizeof(float));
   w.off_dck = up(w.off_dcq + rows * sizeof(float));
   w.off_scan = up(w.off_dck + rows * sizeof(float));
   w.off_fwd = w.off_out = 0;
@@ -832,7 +839,16 @@ size_t bwd_smem_max(int dk, int dv, int L) {
                           (size_t)kC * L);
 }
 
-cudaError_t launch_bwd_finish(const BwdArgs& A, int grad_dtype, cudaStream_t s, bool with_qk) {
+cudaError_t launch_bwd_finish(const BwdArgs& A0, int grad_dtype, cudaStream_t s, bool with_qk,
+                              bool qk_summed) {
+  // qk_summed: dqh and dkh already hold each q/k head's sum ([B, T, Hqk, d_k]); the pass
+  // below is then a cast (one head per group)
+  BwdArgs As = A0;
+  if (qk_summed) {
+    As.f.H = A0.f.Hqk;
+    As.f.hg = 1;
+  }
+  const BwdArgs& A = with_qk ? As : A0;
   const FwdArgs& a = A.f;
   cudaError_t e = cudaSuccess;
   if (with_qk) {
@@ -856,12 +872,13 @@ cudaError_t launch_bwd_finish(const BwdArgs& A, int grad_dtype, cudaStream_t s, 
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (a.log_a && A.dlog_a) {
-    const int nch = (a.T + kScanChunk - 1) / kScanChunk;
-    const dim3 grid_s((unsigned)nch, (unsigned)((int64_t)a.B * a.H));
-    bwd_dlog_a_sums_kernel<<<grid_s, kThreads, 0, s>>>(A, A.scan, nch);
+  if (A0.f.log_a && A0.dlog_a) {  // per value head: the original sizes
+    const FwdArgs& f = A0.f;
+    const int nch = (f.T + kScanChunk - 1) / kScanChunk;
+    const dim3 grid_s((unsigned)nch, (unsigned)((int64_t)f.B * f.H));
+    bwd_dlog_a_sums_kernel<<<grid_s, kThreads, 0, s>>>(A0, A0.scan, nch);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_dlog_a_scan_kernel<<<grid_s, kThreads, 0, s>>>(A, A.scan, nch);
+    bwd_dlog_a_scan_kernel<<<grid_s, kThreads, 0, s>>>(A0, A0.scan, nch);
     e = cudaGetLastError();
   }
   return e;
@@ -874,7 +891,7 @@ cudaError_t launch_simt_backward(const BwdArgs& A, int in_dtype, int grad_dtype,
   else if (in_dtype == LL_F32) e = launch_typed<float, __nv_bfloat16>(A, s);
   else if (grad_dtype == LL_F32) e = launch_typed<__nv_bfloat16, float>(A, s);
   else e = launch_typed<__nv_bfloat16, __nv_bfloat16>(A, s);
-  return e == cudaSuccess ? launch_bwd_finish(A, grad_dtype, s, true) : e;
+  return e == cudaSuccess ? launch_bwd_finish(A, grad_dtype, s, true, false) : e;
 }
 
 }  // namespace ll

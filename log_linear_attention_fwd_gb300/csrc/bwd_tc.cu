@@ -72,7 +72,8 @@ struct BqParams {
   const float* lam;
   const float* lgu;    // [B*H][N] the tiles' log decays (forward workspace)
   const float* nlg;    // [B*H][N] the even slots' block log decays (forward workspace)
-  float* dqh;          // [B, T, H, 128] per-head dQ (fp32), or null
+  float* dqh;          // [B, T, Hqk, 128] fp32 dQ of each q/k head, added to with atomics
+                       // by the hg heads that share it (zeroed before), or null
   const void* dq;      // non-null: dQ in bf16 through the dQ map (one q/k per head)
   float* dcq;          // [B, T, H] q . dQ, or null
   float* dlam;         // [B, T, H, L]
@@ -537,11 +538,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tma_store_commit();
         tma_store_wait_read();
       }
-    } else if (row_live) {
-      float4* dst = reinterpret_cast<float4*>(p.dqh + row * kD + 64 * hh);
+    } else if (row_live) {  // shared q/k: this head's part of its group's dQ
+      float4* dst = reinterpret_cast<float4*>(
+          p.dqh + (((int64_t)b * p.T + t0 + r) * (p.H / p.hg) + hq) * kD + 64 * hh);
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        dst[q] = make_float4(dq[4 * q], dq[4 * q + 1], dq[4 * q + 2], dq[4 * q + 3]);
+        atomicAdd(dst + q, make_float4(dq[4 * q], dq[4 * q + 1], dq[4 * q + 2], dq[4 * q + 3]));
     }
   } else if (tid == 0) {
     atomicOr(&g_tcb_error, 1u);
@@ -570,7 +572,8 @@ struct BkvParams {
   const float* lgu;          // [B*H][N] the tiles' log decays (forward workspace)
   const float* R;            // [B*H][N][d_k][d_v] mirrored states, fp32
   const __nv_bfloat16* v;    // [B, T, H, d_v] (for v . dV)
-  float* dkh;                // [B, T, H, 128] per-head dK (fp32), or null
+  float* dkh;                // [B, T, Hqk, 128] fp32 dK of each q/k head, added to with
+                             // atomics by the hg heads that share it (zeroed before), or null
   const void* dk;            // non-null: dK in bf16 through the dK map (one q/k per head)
   float* dck;                // [B, T, H] k . dK, or null
   int ahead;  // tiles between this one and the next on the same SM
@@ -942,11 +945,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tmem_ld32(tmem + lane_base + 256 + 64 * hh + 32 * c, v0);
         if (p.dk) {
           put_row32_bf16(Qb, r, 2 * hh + c, v0);
-        } else if (row_live) {
-          float4* dst = reinterpret_cast<float4*>(p.dkh + row * kD + 64 * hh + 32 * c);
+        } else if (row_live) {  // shared q/k: this head's part of its group's dK
+          float4* dst = reinterpret_cast<float4*>(
+              p.dkh + (((int64_t)b * p.T + t0 + r) * (p.H / p.hg) + hq) * kD + 64 * hh + 32 * c);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]);
+            atomicAdd(dst + q, make_float4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]));
         }
       }
     }

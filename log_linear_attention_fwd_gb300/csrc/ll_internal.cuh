@@ -160,8 +160,8 @@ struct BwdWorkspace {
   size_t total;
 };
 // N: 32-token tiles; n_tc: 128-token tiles of the tensor-core dQ, or 0 without it.
-BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t N, int64_t dk,
-                                  int64_t dv, int64_t n_tc);
+BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t Hqk, int64_t N,
+                                  int64_t dk, int64_t dv, int64_t n_tc);
 // The whole backward on CUDA cores (fp32, 32-token tiles).
 cudaError_t launch_simt_backward(const BwdArgs& a, int in_dtype, int grad_dtype, cudaStream_t s);
 // Tensor-core backward (bf16, d_k = 128, d_v in {64, 128}) on the 128-token tiles of a
@@ -178,7 +178,10 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
                               void* dk_bf16, float* dck, void* dv, cudaStream_t s);
 // The group sums of dq and dk with their cast (skipped when with_qk is false: the
 // kernels wrote them), and d log a (the last kernels of every backward path).
-cudaError_t launch_bwd_finish(const BwdArgs& a, int grad_dtype, cudaStream_t s, bool with_qk);
+// qk_summed: dqh and dkh hold the q/k heads' sums [B, T, Hqk, d_k] (tensor-core path with
+// shared q/k) rather than per value head [B, T, H, d_k].
+cudaError_t launch_bwd_finish(const BwdArgs& a, int grad_dtype, cudaStream_t s, bool with_qk,
+                              bool qk_summed);
 cudaError_t tcb_take_error(cudaStream_t s, unsigned* flags);
 size_t bwd_smem_max(int dk, int dv, int L);  // largest dynamic shared memory of a kernel
 // The decode state at position T-1 from a completed forward's workspace (tc_layout: the

@@ -482,7 +482,7 @@ int loglinear_bwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Hqk, i
   int64_t N, n_tc;
   const int st = check_bwd(B, T, H, Hqk, dk, dv, L, in_dtype, grad_dtype, path, &N, &n_tc);
   if (st != LL_OK) return st;
-  *bytes = bwd_workspace_layout(B, T, H, N, dk, dv, n_tc).total;
+  *bytes = bwd_workspace_layout(B, T, H, Hqk, N, dk, dv, n_tc).total;
   return LL_OK;
 }
 
@@ -501,7 +501,7 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
   if (!q || !k || !v || !lambda || !dout || !dq || !dk_out || !dv_out || !dlambda)
     return LL_ERR_INVALID;
   if (log_a && !dlog_a) return LL_ERR_INVALID;
-  const BwdWorkspace w = bwd_workspace_layout(B, T, H, N, dk, dv, n_tc);
+  const BwdWorkspace w = bwd_workspace_layout(B, T, H, Hqk, N, dk, dv, n_tc);
   if (!workspace || workspace_bytes < w.total) return LL_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_ALIGN;
   if (n_tc > 0 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(dout) &&
@@ -554,16 +554,23 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
     f.tag = reinterpret_cast<uint32_t*>(fw + w.fwd.off_tag);
     // the mirrored states on the same 128-token tiles go into U's buffer (fp32)
     float* R = reinterpret_cast<float*>(a.U);
-    // with one q/k per head the kernels write dq and dk in bf16 themselves; shared q/k
-    // heads need the per-head fp32 values summed over each group
+    // with one q/k per head the kernels write dq and dk in bf16 themselves; with shared
+    // q/k heads each head adds its fp32 dq and dk into its group's sum (atomics into
+    // zeroed [B, T, Hqk, d_k] buffers), which the last pass casts
     const bool own_qk = a.hg == 1;
+    if (!own_qk) {
+      const size_t qk_bytes = sizeof(float) * (size_t)B * T * Hqk * dk;
+      if ((e = cudaMemsetAsync(A.dqh, 0, qk_bytes, s)) == cudaSuccess)
+        e = cudaMemsetAsync(A.dkh, 0, qk_bytes, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
     if (!fwd_workspace) e = launch_tc_forward(f, LL_BF16, s, nullptr);
     if (e == cudaSuccess)
       e = launch_tc_bwd_dq(f, dout, A.dqh, own_qk ? dq : nullptr, A.dcq, dlambda, s);
     if (e == cudaSuccess && f.N > 1) e = launch_tc_bwd_rstate(f, dout, R, s);
     if (e == cudaSuccess)
       e = launch_tc_bwd_dkv(f, dout, R, A.dkh, own_qk ? dk_out : nullptr, A.dck, dv_out, s);
-    if (e == cudaSuccess) e = launch_bwd_finish(A, grad_dtype, s, !own_qk);
+    if (e == cudaSuccess) e = launch_bwd_finish(A, grad_dtype, s, !own_qk, true);
     return e == cudaSuccess ? LL_OK : cuda_fail(e);
   }
   e = launch_simt_backward(A, in_dtype, grad_dtype, s);
