@@ -279,6 +279,31 @@ LL_API int loglinear_gdn_fwd(const void* q, const void* k, const void* v, const 
                              int64_t L, int in_dtype, int out_dtype, ll_stream_t stream);
 
 /*
+ * The same forward of Log-Linear Gated DeltaNet in chunks of 64 tokens, fp32 on CUDA cores:
+ * per chunk the UT-transform form of the delta rule (Yang et al., "Parallelizing Linear
+ * Transformers with the Delta Rule over Sequence Length", 2024) gives the chunk's own
+ * attention matrix (masked by the Fenwick levels inside the chunk), its queries carried
+ * back to the chunk start, its d_k x d_k transition and its own state; a sequential scan over
+ * the chunks then carries every chunk-level block state by the chunk transitions, merges
+ * them by the lssb rule on chunk indices and adds their lambda-weighted readout (first
+ * page, sections 矩阵分解 and 两阶段计算, with the transition in place of the scalar decay).
+ * Arguments as loglinear_gdn_fwd, without the final state, plus a workspace of
+ * loglinear_gdn_fwd_chunked_workspace_size() bytes (256-byte aligned; the chunks' partial
+ * outputs, carried queries, transitions and states in fp32).  No alignment is needed of
+ * q, k, v.  Supported: 1 <= dk, dv <= 128, L <= 64.
+ * Errors: LL_ERR_INVALID, LL_ERR_SHAPE, LL_ERR_DTYPE, LL_ERR_UNSUPPORTED, LL_ERR_WORKSPACE,
+ * LL_ERR_ALIGN, LL_ERR_CUDA.
+ */
+LL_API int loglinear_gdn_fwd_chunked_workspace_size(int64_t B, int64_t T, int64_t H, int64_t dk,
+                                                    int64_t dv, size_t* bytes);
+LL_API int loglinear_gdn_fwd_chunked(const void* q, const void* k, const void* v,
+                                     const float* log_a, const float* beta, const float* lambda,
+                                     void* out, int64_t B, int64_t T, int64_t H, int64_t Hqk,
+                                     int64_t dk, int64_t dv, int64_t L, int in_dtype,
+                                     int out_dtype, void* workspace, size_t workspace_bytes,
+                                     ll_stream_t stream);
+
+/*
  * Backward of loglinear_fwd (page "算力终结者来了！…", sections 结构矩阵 and 讨论与局限性:
  * training takes the gradients of the attention terms and of the level weights lambda):
  * given dout = dL/dO, the gradients of L with respect to every input, for

@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     debug_level_map,
     device_error,
     fwd_workspace_size,
+    gdn_fwd_chunked_workspace_size,
     lib,
     loglinear_bwd,
     loglinear_decode_step,
@@ -18,6 +19,7 @@ from ._binding import (  # noqa: F401
     loglinear_fwd_with_events,
     loglinear_gdn_decode_step,
     loglinear_gdn_fwd,
+    loglinear_gdn_fwd_chunked,
     loglinear_prefill,
     loglinear_prefill_with_events,
     resolve_path,

@@ -56,6 +56,10 @@ SIGNATURES = {
                                          _i64, _i64, _i64, _i64, _int, _int, _vp]),
     "loglinear_gdn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                  _i64, _i64, _i64, _int, _int, _vp]),
+    "loglinear_gdn_fwd_chunked_workspace_size": (_int, [_i64, _i64, _i64, _i64, _i64,
+                                                        ctypes.POINTER(ctypes.c_size_t)]),
+    "loglinear_gdn_fwd_chunked": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                         _i64, _i64, _i64, _i64, _int, _int, _vp, _sz, _vp]),
     "loglinear_debug_level_map": (_int, [_i64, _int, _int, _vp, _vp]),
     "loglinear_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "loglinear_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
@@ -283,6 +287,45 @@ def loglinear_gdn_fwd(q, k, v, log_a, beta, lam, out=None, out_dtype=None, state
                                 _dtype_code(out), _stream(stream))
     if st != LL_OK:
         raise LoglinearError(st, "loglinear_gdn_fwd")
+    return out
+
+
+def gdn_fwd_chunked_workspace_size(B, T, H, dk, dv) -> int:
+    out = ctypes.c_size_t(0)
+    st = _lib.loglinear_gdn_fwd_chunked_workspace_size(B, T, H, dk, dv, ctypes.byref(out))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_gdn_fwd_chunked_workspace_size")
+    return int(out.value)
+
+
+def loglinear_gdn_fwd_chunked(q, k, v, log_a, beta, lam, out=None, out_dtype=None,
+                              workspace=None, stream=None):
+    """Log-Linear Gated DeltaNet over a whole sequence in chunks of 64 tokens (same inputs and
+    output as loglinear_gdn_fwd, no final state).  The workspace is allocated with torch
+    when not given."""
+    B, T, Hqk, dk = q.shape
+    H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
+    _check_dev("q", q)
+    _check_dev("k", k, q.dtype, (B, T, Hqk, dk))
+    _check_dev("v", v, q.dtype, (B, T, H, dv))
+    _check_dev("log_a", log_a, torch.float32, (B, T, H))
+    _check_dev("beta", beta, torch.float32, (B, T, H))
+    _check_dev("lam", lam, torch.float32, (B, T, H, L))
+    if out is None:
+        out = torch.empty(B, T, H, dv, device=q.device, dtype=out_dtype or q.dtype)
+    _check_dev("out", out, shape=(B, T, H, dv))
+    sz = ctypes.c_size_t(0)
+    st = _lib.loglinear_gdn_fwd_chunked_workspace_size(B, T, H, dk, dv, ctypes.byref(sz))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_gdn_fwd_chunked_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(max(sz.value, 1), device=q.device, dtype=torch.uint8)
+    st = _lib.loglinear_gdn_fwd_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(beta),
+                                        _ptr(lam), _ptr(out), B, T, H, Hqk, dk, dv, L,
+                                        _dtype_code(q), _dtype_code(out), _ptr(workspace),
+                                        workspace.numel(), _stream(stream))
+    if st != LL_OK:
+        raise LoglinearError(st, "loglinear_gdn_fwd_chunked")
     return out
 
 

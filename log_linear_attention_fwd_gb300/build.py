@@ -21,7 +21,7 @@ LIB_NAME = "libloglinear.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
 SOURCES = ["loglinear_api.cu", "fwd_simt.cu", "fwd_tc.cu", "level_scan.cu", "decode.cu",
-           "gdn_decode.cu", "gdn_fwd.cu", "fwd_noalloc.cu", "prefill_state.cu", "bwd_simt.cu",
+           "gdn_decode.cu", "gdn_fwd.cu", "gdn_chunk.cu", "fwd_noalloc.cu", "prefill_state.cu", "bwd_simt.cu",
            "bwd_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

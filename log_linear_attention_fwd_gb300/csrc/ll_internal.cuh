@@ -209,6 +209,13 @@ cudaError_t launch_gdn_decode(float* state, const void* q, const void* k, const 
                               const float* log_a, const float* beta, const float* lam, void* out,
                               int B, int H, int Hqk, int dk, int dv, int L, const DecodePlan& plan,
                               int in_dtype, int out_dtype, cudaStream_t s);
+// Log-Linear Gated DeltaNet forward in chunks of 64 tokens (UT transform per chunk, then a
+// sequential scan of the chunk-level states); workspace of gdn_chunk_workspace_bytes().
+size_t gdn_chunk_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv);
+cudaError_t launch_gdn_chunked(const void* q, const void* k, const void* v, const float* log_a,
+                               const float* beta, const float* lam, void* out, int B, int T, int H,
+                               int Hqk, int dk, int dv, int L, int in_dtype, int out_dtype,
+                               void* workspace, cudaStream_t s);
 // Log-Linear Gated DeltaNet forward in the recurrent form (levels = bit_length(T-1) + 1
 // Fenwick levels in use); state, when non-null, receives the per-level state after T-1.
 cudaError_t launch_gdn_fwd(const void* q, const void* k, const void* v, const float* log_a,

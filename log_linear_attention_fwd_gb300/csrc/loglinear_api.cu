@@ -452,6 +452,40 @@ int loglinear_gdn_fwd(const void* q, const void* k, const void* v, const float* 
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }
 
+int loglinear_gdn_fwd_chunked_workspace_size(int64_t B, int64_t T, int64_t H, int64_t dk,
+                                              int64_t dv, size_t* bytes) {
+  if (!bytes || B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1) return LL_ERR_INVALID;
+  if (dk > kMaxHeadDim || dv > kMaxHeadDim || T > INT32_MAX) return LL_ERR_UNSUPPORTED;
+  *bytes = gdn_chunk_workspace_bytes(B, T, H, dk, dv);
+  return LL_OK;
+}
+
+int loglinear_gdn_fwd_chunked(const void* q, const void* k, const void* v, const float* log_a,
+                              const float* beta, const float* lambda, void* out, int64_t B,
+                              int64_t T, int64_t H, int64_t Hqk, int64_t dk, int64_t dv,
+                              int64_t L, int in_dtype, int out_dtype, void* workspace,
+                              size_t workspace_bytes, ll_stream_t stream) {
+  if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1 || L < 1) return LL_ERR_INVALID;
+  const int sh = check_qk_heads(H, Hqk);
+  if (sh != LL_OK) return sh;
+  if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return LL_ERR_DTYPE;
+  if (T > INT32_MAX || dk > kMaxHeadDim || dv > kMaxHeadDim || L > 64) return LL_ERR_UNSUPPORTED;
+  if (B * H * ((T + 63) / 64) > INT32_MAX) return LL_ERR_UNSUPPORTED;
+  // the scan keeps every chunk level of its columns in shared memory: up to 2^19 chunks
+  if (T > ((int64_t)64 << 19)) return LL_ERR_UNSUPPORTED;
+  if (T > 0 && L < bit_length(T - 1) + 1) return LL_ERR_SHAPE;
+  if (B == 0 || H == 0 || T == 0) return LL_OK;
+  if (!q || !k || !v || !beta || !lambda || !out) return LL_ERR_INVALID;
+  if (!workspace || workspace_bytes < gdn_chunk_workspace_bytes(B, T, H, dk, dv))
+    return LL_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_ALIGN;
+  const cudaError_t e = launch_gdn_chunked(q, k, v, log_a, beta, lambda, out, (int)B, (int)T,
+                                           (int)H, (int)Hqk, (int)dk, (int)dv, (int)L, in_dtype,
+                                           out_dtype, workspace,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LL_OK : cuda_fail(e);
+}
+
 // ---------------------------------------------------------------- backward
 
 // N: 32-token tiles of the CUDA-core part; *n_tc: 128-token tiles of the tensor-core dQ

@@ -133,3 +133,83 @@ def test_gdn_fwd_empty(LL):
     LL.loglinear_gdn_fwd(q, q, v, None, beta, lam, state=state)
     torch.cuda.synchronize()
     assert (state == 0).all()
+
+
+# ---------------------------------------------------------------- the chunked form
+
+
+def _run_chunked(LL, x, out_dtype=torch.float32):
+    d = _dev(x)
+    out = LL.loglinear_gdn_fwd_chunked(d["q"], d["k"], d["v"], d["log_a"], d["beta"], d["lam"],
+                                       out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+@pytest.mark.parametrize("B,H,Hqk,T,dk,dv,dtype,decay", [
+    (1, 1, 1, 1, 16, 8, "f32", True),         # one token
+    (2, 3, 0, 37, 32, 16, "f32", True),       # one ragged chunk
+    (1, 4, 1, 130, 64, 24, "f32", False),     # three chunks, the last ragged; shared q/k
+    (1, 2, 2, 300, 128, 64, "bf16", True),
+    (1, 1, 1, 1000, 128, 128, "f32", True),   # 16 chunks: chunk levels 1..4
+    (2, 2, 0, 77, 7, 3, "f32", True),         # odd d_k, d_v
+    (1, 2, 0, 2100, 32, 32, "f32", False),    # 33 chunks without decay: every level weighs
+])
+def test_gdn_fwd_chunked_matches_recurrence(LL, B, H, Hqk, T, dk, dv, dtype, decay):
+    """The chunked form (UT transform per 64-token chunk, chunk-level states carried by the
+    chunk transitions) against the oracle's lssb recurrence, every output row."""
+    L = max(1, (T - 1).bit_length() + 1) + 1
+    cfg = W.FwdConfig("gdn_chunk", B, H, T, dk, dv, 64, L, dtype, decay, "softplus",
+                      seed=T + dk + 1, Hqk=Hqk)
+    x = W.make_gdn_inputs(cfg)
+    want, _ = oracle.gdn_recurrence(*_bcast_qk(x, H))
+    got = _run_chunked(LL, x)
+    err = rel_l2(got, want)
+    print(f"gdn chunked B{B} H{H} Hqk{Hqk} T{T} dk{dk} dv{dv} {dtype}: rel_l2={err:.2e}")
+    assert err <= TOL_F32
+
+
+def test_gdn_fwd_chunked_bf16_out_and_constant_lambda(LL):
+    """bf16 output; and lambda equal at every level gives plain Gated DeltaNet."""
+    cfg = W.FwdConfig("gdn_chunk_b", 1, 2, 500, 128, 64, 64, 10, "bf16", True, "softplus", seed=4)
+    x = W.make_gdn_inputs(cfg)
+    want, _ = oracle.gdn_recurrence(*_bcast_qk(x, cfg.H))
+    got = _run_chunked(LL, x, out_dtype=torch.bfloat16)
+    assert rel_l2(got.float(), want) <= TOL_BF16
+    cfg2 = W.FwdConfig("gdn_chunk_c", 1, 2, 400, 32, 16, 64, 10, "f32", True, "softplus", seed=6)
+    x2 = W.make_gdn_inputs(cfg2)
+    c = x2["lam"][..., :1]
+    x2["lam"] = c.expand_as(x2["lam"]).contiguous()
+    want2 = oracle.gated_deltanet_recurrent(x2["q"], x2["k"], x2["v"], x2["log_a"], x2["beta"],
+                                            c[..., 0])
+    assert rel_l2(_run_chunked(LL, x2), want2) <= TOL_F32
+
+
+def test_gdn_fwd_chunked_long_sampled_rows(LL):
+    """T = 70000 (1094 chunks, chunk levels up to 11), small heads, slow decay: rows sampled
+    across the sequence against the direct form."""
+    T = 70000
+    cfg = W.FwdConfig("gdn_chunk_long", 1, 1, T, 8, 8, 64, 18, "f32", False, "softplus", seed=3)
+    x = W.make_gdn_inputs(cfg)
+    x["log_a"] = torch.full((1, T, 1), -2e-4)
+    rows = [0, 63, 64, 1023, 1024, 4095, 32767, 32768, 65535, 65536, T - 2, T - 1]
+    want = oracle.gdn_direct(x["q"], x["k"], x["v"], x["log_a"], x["beta"], x["lam"], rows=rows)
+    got = _run_chunked(LL, x)
+    for r in rows:
+        assert rel_l2(got[:, r], want[:, r]) <= 1e-4, r
+
+
+def test_gdn_fwd_chunked_matches_recurrent_full_size(LL):
+    """Two heads of the headline shape (T = 16384, d_k = d_v = 128, bf16 inputs): the chunked
+    and the recurrent GPU forms agree (the recurrent one is pinned to the oracle above)."""
+    cfg = W.FwdConfig("gdn_chunk_full", 1, 2, 16384, 128, 128, 64, 15, "bf16", True, "softplus",
+                      seed=11)
+    x = _dev(W.make_gdn_inputs(cfg))
+    a = LL.loglinear_gdn_fwd(x["q"], x["k"], x["v"], x["log_a"], x["beta"], x["lam"],
+                             out_dtype=torch.float32)
+    b = LL.loglinear_gdn_fwd_chunked(x["q"], x["k"], x["v"], x["log_a"], x["beta"], x["lam"],
+                                     out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    err = rel_l2(b.cpu(), a.cpu().double().numpy())
+    print(f"gdn chunked vs recurrent, T=16384: rel_l2={err:.2e}")
+    assert err <= 1e-4
