@@ -35,8 +35,8 @@ constexpr int kC = 64;          // tokens per chunk
 constexpr int kLc = 6;          // log2(kC)
 constexpr int kD = 128;         // d_k, d_v <= 128 (zero-padded in shared memory)
 constexpr int kThreads = 256;
-constexpr int kLd = kD + 4;     // row stride of [64][128] fp32 tiles (16-byte rows, fewer conflicts)
-constexpr int kLdc = kC + 4;    // row stride of [64][64] fp32 tiles
+constexpr int kLd = kD + 1;     // row stride of [64][128] fp32 tiles (odd: rows on all banks)
+constexpr int kLdc = kC + 1;    // row stride of [64][64] fp32 tiles
 constexpr int kCols = 16;       // d_v columns per scan CTA
 
 struct ChunkSmem {
@@ -54,9 +54,11 @@ struct ChunkSmem {
   static constexpr int kEnd = kLam + kC * 8;            // floats
 };
 
-// acc[i][j] += sum_k A(m0 + i, k) B(k, n0 + j) over k in [k0, k1), A(m, k) = A[m lda + k]
-// (or A[k lda + m] when AT), B(k, n) = B[k ldb + n] (or B[n ldb + k] when BT).
-template <int TM, int TN, bool AT, bool BT>
+// acc[i][j] += sum_k A(m0 + i, k) B(k, n0 + CS j) over k in [k0, k1), A(m, k) = A[m lda + k]
+// (or A[k lda + m] when AT), B(k, n) = B[k ldb + n] (or B[n ldb + k] when BT).  CS = 16
+// interleaves the 16 threads of a row of the thread grid over consecutive columns (no bank
+// conflicts in B).
+template <int TM, int TN, bool AT, bool BT, int CS = 1>
 __device__ __forceinline__ void mma_tile(float (&acc)[TM][TN], const float* A, int lda,
                                          const float* B, int ldb, int k0, int k1, int m0,
                                          int n0) {
@@ -65,7 +67,7 @@ __device__ __forceinline__ void mma_tile(float (&acc)[TM][TN], const float* A, i
 #pragma unroll
     for (int i = 0; i < TM; ++i) a[i] = AT ? A[k * lda + m0 + i] : A[(m0 + i) * lda + k];
 #pragma unroll
-    for (int j = 0; j < TN; ++j) bv[j] = BT ? B[(n0 + j) * ldb + k] : B[k * ldb + n0 + j];
+    for (int j = 0; j < TN; ++j) bv[j] = BT ? B[(n0 + CS * j) * ldb + k] : B[k * ldb + n0 + CS * j];
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -120,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
   const int dk = a.dk, dv = a.dv;
 
   // ---- the chunk's q, k, v (fp32, zero past n rows and past dk / dv columns), gates
+#pragma unroll 8
   for (int i = tid; i < kC * kD; i += kThreads) {
     const int t = i / kD, d = i - t * kD;
     const bool live = t < n;
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
   {
     float o[4][8];
     zero(o);
-    mma_tile<4, 8, false, false>(o, Ws, kLdc, Vs, kLd, 0, kC, 4 * tm, 8 * tn);
+    mma_tile<4, 8, false, false, 16>(o, Ws, kLdc, Vs, kLd, 0, kC, 4 * tm, tn);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = 4 * tm + i;
@@ -212,10 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
       float* dst = a.o_intra + (((int64_t)b * a.T + t0 + t) * a.H + h) * dv;
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj)
-        if (8 * tn + jj < dv) dst[8 * tn + jj] = o[i][jj];
+        if (tn + 16 * jj < dv) dst[tn + 16 * jj] = o[i][jj];
     }
   }
-  // ---- X = T diag(beta gamma) K: rows 4 tm.., columns 8 tn..
+  // ---- X = T diag(beta gamma) K: rows 4 tm.., columns tn + 16 jj
   {
     float x[4][8];
     zero(x);
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
 #pragma unroll
       for (int i = 0; i < 4; ++i) tv[i] = Ts[(4 * tm + i) * kLdc + k];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) kv[jj] = sc * Ks[k * kLd + 8 * tn + jj];
+      for (int jj = 0; jj < 8; ++jj) kv[jj] = sc * Ks[k * kLd + tn + 16 * jj];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) Xs[(4 * tm + i) * kLd + 8 * tn + jj] = x[i][jj];
+      for (int jj = 0; jj < 8; ++jj) Xs[(4 * tm + i) * kLd + tn + 16 * jj] = x[i][jj];
   }
   __syncthreads();
   const int64_t chunk = bh * a.N + j;
@@ -242,19 +245,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
   {
     float qv[4][8];
     zero(qv);
-    mma_tile<4, 8, false, false>(qv, Aqk, kLdc, Xs, kLd, 0, kC, 4 * tm, 8 * tn);
+    mma_tile<4, 8, false, false, 16>(qv, Aqk, kLdc, Xs, kLd, 0, kC, 4 * tm, tn);
     float* dst = a.qt + chunk * kC * dk;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = 4 * tm + i;
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
-        const int d = 8 * tn + jj;
+        const int d = tn + 16 * jj;
         if (d < dk) dst[t * dk + d] = gam[t] * Qs[t * kLd + d] - qv[i][jj];
       }
     }
   }
-  // ---- P = gamma_end I - K^T diag(Gam[end, :]) X  (dk x dk): thread rows 8 tm.., cols 8 tn..
+  // ---- P = gamma_end I - K^T diag(Gam[end, :]) X  (dk x dk): thread rows 8 tm.., columns
+  // tn + 16 jj
   {
     const float g_end = gs[n - 1];
     float pv[8][8];
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
 #pragma unroll
       for (int i = 0; i < 8; ++i) kv[i] = ge * Ks[s * kLd + 8 * tm + i];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) xv[jj] = Xs[s * kLd + 8 * tn + jj];
+      for (int jj = 0; jj < 8; ++jj) xv[jj] = Xs[s * kLd + tn + 16 * jj];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -279,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
       if (r >= dk) continue;
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
-        const int c = 8 * tn + jj;
+        const int c = tn + 16 * jj;
         if (c < dk) dst[r * dk + c] = (r == c ? gend : 0.f) - pv[i][jj];
       }
     }
@@ -294,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
 #pragma unroll
       for (int i = 0; i < 4; ++i) tv[i] = Ts[(4 * tm + i) * kLdc + k];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) vv[jj] = bet[k] * Vs[k * kLd + 8 * tn + jj];
+      for (int jj = 0; jj < 8; ++jj) vv[jj] = bet[k] * Vs[k * kLd + tn + 16 * jj];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) Qs[(4 * tm + i) * kLd + 8 * tn + jj] = y[i][jj];
+      for (int jj = 0; jj < 8; ++jj) Qs[(4 * tm + i) * kLd + tn + 16 * jj] = y[i][jj];
   }
   __syncthreads();
   // ---- U = K^T diag(Gam[end, :]) Y  (dk x dv)
@@ -317,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
 #pragma unroll
       for (int i = 0; i < 8; ++i) kv[i] = ge * Ks[s * kLd + 8 * tm + i];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) yv[jj] = Qs[s * kLd + 8 * tn + jj];
+      for (int jj = 0; jj < 8; ++jj) yv[jj] = Qs[s * kLd + tn + 16 * jj];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
       if (r >= dk) continue;
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
-        const int c = 8 * tn + jj;
+        const int c = tn + 16 * jj;
         if (c < dv) dst[r * dv + c] = u[i][jj];
       }
     }
@@ -339,12 +343,37 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
 
 // ---------------------------------------------------------------- the scan over chunks
 //
-// Thread layout: 256 threads = 16 columns x 16 row groups of 8 rows (d_k <= 128).  Z^m of
-// the CTA's columns, [level][128][16] fp32, in shared memory.
-template <typename OutT>
+// Thread layout: 256 threads = 16 columns x 16 row groups; thread (rg, col) holds rows
+// [8 rg, 8 rg + 8) of column col of every chunk level in registers (Z^m, m < kLv: 12 slots
+// up to 2^11 chunks, 20 up to 2^19).  Per
+// chunk and live level the level's column block is staged in shared memory, then each
+// thread adds its four tokens' readout (Qt Z^m) and carries its rows (P Z^m).  The chunk's
+// P and Qt are in shared memory, the next chunk's loading meanwhile (cp.async, two buffers).
+constexpr int kMaxLv = 20;     // chunk levels 1..19: up to 2^19 chunks
+constexpr int kLdp = kD + 4;   // row stride of P and Qt in shared memory (16-byte rows)
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4g(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <typename OutT, int kLv>
 __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(GdnChunkArgs a, int levels) {
-  extern __shared__ __align__(16) float zs[];   // [levels][kD][kCols], then P [kD][kD + 1]
-  float* Ps = zs + (size_t)levels * kD * kCols;  // the chunk's transition (rows < dk)
+  extern __shared__ __align__(16) float sm2[];
+  float* Pb = sm2;                          // [2][kD][kLdp]
+  float* Qb = Pb + 2 * kD * kLdp;           // [2][kC][kLdp]
+  float* Zs = Qb + 2 * kC * kLdp;           // [kD][kCols]: one level's column block
+  float* Lb = Zs + kD * kCols;              // [2][kC][kMaxLv]: lambda of the chunk levels
   const int tid = threadIdx.x;
   const int slices = (a.dv + kCols - 1) / kCols;
   const int64_t bh = blockIdx.x / slices;
@@ -352,71 +381,166 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(GdnChunkArg
   const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
   const int dk = a.dk, dv = a.dv;
   const int col = tid & (kCols - 1), rg = tid >> 4;  // column, row group (rows 8 rg..)
-  for (int i = tid; i < levels * kD * kCols; i += kThreads) zs[i] = 0.f;
-  __syncthreads();
+  const bool col_ok = c0 + col < dv;
+  const bool vec = (dk & 3) == 0;  // 16-byte copies of P and Qt rows
+
+  // the chunk's transition P [dk][dk], carried queries Qt [64][dk] and the lambdas of its
+  // tokens at the chunk levels into buffer j & 1
+  auto issue = [&](int j) {
+    const int64_t chunk = bh * a.N + j;
+    const float* Pg = a.P + chunk * (int64_t)dk * dk;
+    const float* Qg = a.qt + chunk * kC * dk;
+    float* Pd = Pb + (j & 1) * kD * kLdp;
+    float* Qd = Qb + (j & 1) * kC * kLdp;
+    float* Ld = Lb + (j & 1) * kC * kMaxLv;
+    const int nt = min(kC, a.T - j * kC);
+    for (int i = tid; i < nt * (levels - 1); i += kThreads) {
+      const int t = i / (levels - 1), m = 1 + i - t * (levels - 1);
+      const int64_t tv = ((int64_t)b * a.T + j * kC + t) * a.H + h;
+      cp_async4g(Ld + t * kMaxLv + m, a.lam + tv * a.L + kLc + m);
+    }
+    if (vec) {
+      const int q4 = dk / 4;
+      for (int i = tid; i < dk * q4; i += kThreads) {
+        const int r = i / q4, c = i - r * q4;
+        cp_async16(Pd + r * kLdp + 4 * c, Pg + r * dk + 4 * c);
+      }
+      for (int i = tid; i < kC * q4; i += kThreads) {
+        const int r = i / q4, c = i - r * q4;
+        cp_async16(Qd + r * kLdp + 4 * c, Qg + r * dk + 4 * c);
+      }
+    } else {
+      for (int i = tid; i < dk * dk; i += kThreads) {
+        const int r = i / dk, c = i - r * dk;
+        cp_async4g(Pd + r * kLdp + c, Pg + i);
+      }
+      for (int i = tid; i < kC * dk; i += kThreads) {
+        const int r = i / dk, c = i - r * dk;
+        cp_async4g(Qd + r * kLdp + c, Qg + i);
+      }
+    }
+  };
+
+  float z[kLv][8];  // Z^m rows 8 rg.., column col (index m; slot 0 unused)
+#pragma unroll
+  for (int m = 0; m < kLv; ++m)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) z[m][i] = 0.f;
   uint32_t live = 0;  // bit m: Z^m holds data
+  float u_next[8];    // U_{j} rows 8 rg.., column col: merged at the start of chunk j+1
+  // the copies fill columns [0, dk) of each row; the padding up to a multiple of 4, read
+  // by the float4 loop (times zero rows of Z), stays zero
+  for (int i = tid; i < 2 * kD * kLdp + 2 * kC * kLdp + kD * kCols + 2 * kC * kMaxLv; i += kThreads)
+    Pb[i] = 0.f;
+  __syncthreads();
+  issue(0);
+  cp_commit();
   for (int j = 0; j < a.N; ++j) {
     const int64_t chunk = bh * a.N + j;
     const int t0 = j * kC, n = min(kC, a.T - t0);
+    if (j + 1 < a.N) issue(j + 1);
+    cp_commit();
     // ---- merge at the chunk start: Z^{l+1} <- U_{j-1} + sum_{m <= l} Z^m, l = lssb(j)
     if (j > 0) {
       const int l = __ffs(j) - 1;
-      const float* Up = a.U + (chunk - 1) * (int64_t)dk * dv;
+      float x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = u_next[i];
+#pragma unroll
+      for (int m = 1; m < kLv; ++m) {
+        if (m > l) break;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          x[i] += z[m][i];
+          z[m][i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int m = 1; m < kLv; ++m)
+        if (m == l + 1) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) z[m][i] = x[i];
+        }
+      live = (live & ~((2u << l) - 2u)) | (1u << (l + 1));
+    }
+    // this chunk's own state (merged at the next chunk) and partial outputs: loads issued
+    // now, used after the level work
+    {
+      const float* Uc = a.U + chunk * (int64_t)dk * dv;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = 8 * rg + i;
-        float x = (r < dk && c0 + col < dv) ? Up[r * dv + c0 + col] : 0.f;
-        for (int m = 1; m <= l; ++m) {
-          float* z = zs + ((size_t)m * kD + r) * kCols + col;
-          x += *z;
-          *z = 0.f;
-        }
-        zs[((size_t)(l + 1) * kD + r) * kCols + col] = x;
+        u_next[i] = (r < dk && col_ok) ? Uc[r * dv + c0 + col] : 0.f;
       }
-      live = (live & ~((2u << l) - 2u)) | (1u << (l + 1));
     }
-    // the chunk's transition into shared memory
-    const float* Pg = a.P + chunk * (int64_t)dk * dk;
-    for (int i = tid; i < dk * dk; i += kThreads) {
-      const int r = i / dk, c = i - r * dk;
-      Ps[r * (kD + 1) + c] = Pg[i];
-    }
-    __syncthreads();
-    // ---- readout: O[t][col] = O_intra + sum_m lambda[t, 6+m] sum_d Qt[t][d] Z^m[d][col];
-    // thread (rg, col) takes tokens rg, rg + 16, ... (4 of them)
-    const float* qt = a.qt + chunk * kC * dk;
-    for (int t = rg; t < n; t += 16) {
+    float oi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = rg + 16 * i;
       const int64_t tv = ((int64_t)b * a.T + t0 + t) * a.H + h;
-      float o = (c0 + col < dv) ? a.o_intra[tv * dv + c0 + col] : 0.f;
-      for (int m = 1; m < levels; ++m) {
-        if (!((live >> m) & 1)) continue;
-        const float* z = zs + (size_t)m * kD * kCols + col;
-        float x = 0.f;
-        for (int d = 0; d < dk; ++d) x = fmaf(qt[t * dk + d], z[d * kCols], x);
-        o = fmaf(a.lam[tv * a.L + kLc + m], x, o);
-      }
-      if (c0 + col < dv) static_cast<OutT*>(a.out)[tv * dv + c0 + col] = from_f32<OutT>(o);
+      oi[i] = (t < n && col_ok) ? a.o_intra[tv * dv + c0 + col] : 0.f;
     }
+    cp_wait1();  // this chunk's P, Qt and lambdas have landed (the next chunk's may not)
     __syncthreads();
-    // ---- carry every live level through the chunk: Z^m <- P Z^m
-    for (int m = 1; m < levels; ++m) {
+    const float* Ps = Pb + (j & 1) * kD * kLdp;
+    const float* Qs = Qb + (j & 1) * kC * kLdp;
+    const float* Ls = Lb + (j & 1) * kC * kMaxLv;
+    // ---- per live level: readout of four tokens (t = rg + 16 i) and the carry of 8 rows
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 1; m < kLv; ++m) {
+      if (m >= levels) break;
       if (!((live >> m) & 1)) continue;
-      float* z = zs + (size_t)m * kD * kCols;
-      float acc[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int d = 0; d < dk; ++d) {
-        const float zv = z[d * kCols + col];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(Ps[(8 * rg + i) * (kD + 1) + d], zv, acc[i]);
-      }
-      __syncthreads();  // every thread has read the old Z^m
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (8 * rg + i < dk) z[(8 * rg + i) * kCols + col] = acc[i];
+      for (int i = 0; i < 8; ++i) Zs[(8 * rg + i) * kCols + col] = z[m][i];
       __syncthreads();
+      float rd[4] = {0.f, 0.f, 0.f, 0.f};
+      float cr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // four d at a time: rows of P and Qt as float4 (padded to a multiple of 4 with the
+      // zero rows of Z beyond d_k)
+      for (int d = 0; d < dk; d += 4) {
+        float zd[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) zd[e] = Zs[(d + e) * kCols + col];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 q4 = *reinterpret_cast<const float4*>(Qs + (rg + 16 * i) * kLdp + d);
+          rd[i] = fmaf(q4.x, zd[0], fmaf(q4.y, zd[1], fmaf(q4.z, zd[2], fmaf(q4.w, zd[3], rd[i]))));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 p4 = *reinterpret_cast<const float4*>(Ps + (8 * rg + i) * kLdp + d);
+          cr[i] = fmaf(p4.x, zd[0], fmaf(p4.y, zd[1], fmaf(p4.z, zd[2], fmaf(p4.w, zd[3], cr[i]))));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = fmaf(Ls[(rg + 16 * i) * kMaxLv + m], rd[i], o[i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) z[m][i] = 8 * rg + i < dk ? cr[i] : 0.f;
+      __syncthreads();  // Zs is rewritten by the next level
     }
+    // ---- the chunk's output rows: O_intra + readout
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = rg + 16 * i;
+      if (t < n && col_ok) {
+        const int64_t tv = ((int64_t)b * a.T + t0 + t) * a.H + h;
+        static_cast<OutT*>(a.out)[tv * dv + c0 + col] = from_f32<OutT>(oi[i] + o[i]);
+      }
+    }
+    __syncthreads();  // buffer j & 1 is refilled by the issue of chunk j + 2
   }
+}
+
+template <typename OutT, int kLv>
+cudaError_t launch_scan(const GdnChunkArgs& a, int levels, unsigned grid, size_t smem,
+                        cudaStream_t s) {
+  const cudaError_t e = cudaFuncSetAttribute(gdn_chunk_scan_kernel<OutT, kLv>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+  if (e != cudaSuccess) return e;
+  gdn_chunk_scan_kernel<OutT, kLv><<<grid, kThreads, smem, s>>>(a, levels);
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -467,21 +591,17 @@ cudaError_t launch_gdn_chunked(const void* q, const void* k, const void* v, cons
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   int levels = 1;  // chunk levels 1..bit_length(N-1), plus the unused slot 0
   while ((1 << (levels - 1)) < a.N) ++levels;
-  const size_t smem2 = sizeof(float) * ((size_t)levels * kD * kCols + kD * (kD + 1));
+  if (levels > kMaxLv) return cudaErrorInvalidValue;
+  const size_t smem2 =
+      sizeof(float) * ((size_t)2 * kD * kLdp + 2 * kC * kLdp + kD * kCols + 2 * kC * kMaxLv);
   const unsigned grid2 = (unsigned)((int64_t)B * H * ((dv + kCols - 1) / kCols));
-  if (out_dtype == LL_BF16) {
-    if ((e = cudaFuncSetAttribute(gdn_chunk_scan_kernel<__nv_bfloat16>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2)) !=
-        cudaSuccess)
-      return e;
-    gdn_chunk_scan_kernel<__nv_bfloat16><<<grid2, kThreads, smem2, s>>>(a, levels);
-  } else {
-    if ((e = cudaFuncSetAttribute(gdn_chunk_scan_kernel<float>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2)) !=
-        cudaSuccess)
-      return e;
-    gdn_chunk_scan_kernel<float><<<grid2, kThreads, smem2, s>>>(a, levels);
-  }
+  if (out_dtype == LL_BF16)
+    e = levels <= 12 ? launch_scan<__nv_bfloat16, 12>(a, levels, grid2, smem2, s)
+                     : launch_scan<__nv_bfloat16, kMaxLv>(a, levels, grid2, smem2, s);
+  else
+    e = levels <= 12 ? launch_scan<float, 12>(a, levels, grid2, smem2, s)
+                     : launch_scan<float, kMaxLv>(a, levels, grid2, smem2, s);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

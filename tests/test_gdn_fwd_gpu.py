@@ -213,3 +213,17 @@ def test_gdn_fwd_chunked_matches_recurrent_full_size(LL):
     err = rel_l2(b.cpu(), a.cpu().double().numpy())
     print(f"gdn chunked vs recurrent, T=16384: rel_l2={err:.2e}")
     assert err <= 1e-4
+
+
+def test_gdn_fwd_chunked_many_chunk_levels(LL):
+    """T = 140000: 2188 chunks, 13 chunk-level slots (the wider register layout of the scan);
+    sampled rows against the direct form."""
+    T = 140000
+    cfg = W.FwdConfig("gdn_chunk_longer", 1, 1, T, 4, 8, 64, 19, "f32", False, "softplus", seed=5)
+    x = W.make_gdn_inputs(cfg)
+    x["log_a"] = torch.full((1, T, 1), -1e-4)
+    rows = [131071, 131072, 139999]
+    want = oracle.gdn_direct(x["q"], x["k"], x["v"], x["log_a"], x["beta"], x["lam"], rows=rows)
+    got = _run_chunked(LL, x)
+    for r in rows:
+        assert rel_l2(got[:, r], want[:, r]) <= 1e-4, r
