@@ -284,7 +284,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     int k = 0;
     for (int m = 1; m < kMaxChunkLevels; ++m) {
       if (!((j >> (m - 1)) & 1)) continue;
-      if ((k & 1) == hh) lamx[k * kTile + r] = row_live ? p.lam[row * p.L + kTileLc + m] : 0.f;
+      if ((k & 1) == hh)  // copied in the background: read only after the dQ MMA
+        cp_async4(&lamx[k * kTile + r], row_live ? p.lam + row * p.L + kTileLc + m : p.lam,
+                  row_live ? 4u : 0u);
       ++k;
     }
   }
@@ -407,6 +409,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       nl_s[k] = (my_c & 1) ? p.lgu[bh * N + my_c - 1] : p.nlg[bh * N + my_c];
     }
   }
+  cp_async_wait_all();  // the inter-level lambdas (read after the barrier below)
   ok = all_ok && mbar_wait(bar_dq, 0);
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
@@ -1083,27 +1086,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     for (int q = 0; q < 3; ++q) mbar_init(&bars[q], 1);
     fence_mbar_init();
   }
-  if (warp == 2) {  // D of every level: log decay of the tiles [c, j)
-    int k = 0;
-    for (int m = 1; m < kMaxChunkLevels && k < nlev; ++m) {
-      if (!((j >> (m - 1)) & 1)) continue;
-      const int64_t c = ((int64_t)j >> (m - 1)) << (m - 1);
-      float x = 0.f;
-      for (int64_t i = c + lane; i < j; i += 32) x += p.lgu[bh * p.N + i];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      if (lane == 0) D_s[k] = x;
-      ++k;
-    }
-  }
-  {
-    int k = 0;
-    for (int m = 1; m < kMaxChunkLevels && k < nlev; ++m) {
-      if (!((j >> (m - 1)) & 1)) continue;
-      if ((k & 1) == hh) lamx[k * kTile + r] = row_live ? p.lam[row * p.L + kTileLc + m] : 0.f;
-      ++k;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1126,9 +1108,34 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
   }
   __syncwarp();
+  // while the tiles load: every level's D and the inter-level lambdas
+  if (warp == 2) {  // D of every level: log decay of the tiles [c, j)
+    int k = 0;
+    for (int m = 1; m < kMaxChunkLevels && k < nlev; ++m) {
+      if (!((j >> (m - 1)) & 1)) continue;
+      const int64_t c = ((int64_t)j >> (m - 1)) << (m - 1);
+      float x = 0.f;
+      for (int64_t i = c + lane; i < j; i += 32) x += p.lgu[bh * p.N + i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (lane == 0) D_s[k] = x;
+      ++k;
+    }
+  }
+  {
+    int k = 0;
+    for (int m = 1; m < kMaxChunkLevels && k < nlev; ++m) {
+      if (!((j >> (m - 1)) & 1)) continue;
+      if ((k & 1) == hh)  // copied in the background: read after the barrier below
+        cp_async4(&lamx[k * kTile + r], row_live ? p.lam + row * p.L + kTileLc + m : p.lam,
+                  row_live ? 4u : 0u);
+      ++k;
+    }
+  }
   const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
   const float cs_scan = block_scan256(la, red);
   if (hh == 0) cs_s[r] = cs_scan;
+  cp_async_wait_all();
   if (tid == 0) landed = mbar_wait(bar_load, 0);
   bool all_ok = __syncthreads_and(landed);
   tc_fence_after();
