@@ -693,34 +693,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     for (int q = 0; q < 4; ++q) mbar_init(&bars[q], 1);
     fence_mbar_init();
   }
-  if (tid < kTile) colsum[tid] = 0.f;
-  if (warp == 2) {  // the tile's levels: blocks of later tiles, with exp(E_m)
-    int nl = 0;
-    for (int m = 1; (int64_t(1) << (m - 1)) < p.N; ++m) {
-      if ((i >> (m - 1)) & 1) continue;
-      const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
-      if (c1 >= p.N) continue;
-      float E = 0.f;
-      for (int64_t x = i + 1 + lane; x < c1; x += 32) E += p.lgu[bh * p.N + x];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) E += __shfl_xor_sync(0xffffffffu, E, o);
-      if (lane == 0) {
-        lv_c[nl] = (int)c1;
-        lv_w[nl] = __expf(E);
-      }
-      ++nl;
-    }
-    if (lane == 0) *lv_n = nl;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
-  const int nl = *lv_n;
-  const int64_t elems = (int64_t)kD * DV;
-  if (tid >= 32 && tid < 32 + nl)  // warm L2 with the mirrored states summed below
-    prefetch_l2_bulk(p.R + (bh * p.N + lv_c[tid - 32]) * elems, (uint32_t)(elems * 4));
   bool landed = true;
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_load, 2 * kOperand + 2 * kVBytes);
@@ -747,6 +724,31 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
   }
   __syncwarp();
+  // while the tiles load: the tile's levels and their weights
+  if (tid < kTile) colsum[tid] = 0.f;
+  if (warp == 2) {  // the tile's levels: blocks of later tiles, with exp(E_m)
+    int nl = 0;
+    for (int m = 1; (int64_t(1) << (m - 1)) < p.N; ++m) {
+      if ((i >> (m - 1)) & 1) continue;
+      const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
+      if (c1 >= p.N) continue;
+      float E = 0.f;
+      for (int64_t x = i + 1 + lane; x < c1; x += 32) E += p.lgu[bh * p.N + x];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) E += __shfl_xor_sync(0xffffffffu, E, o);
+      if (lane == 0) {
+        lv_c[nl] = (int)c1;
+        lv_w[nl] = __expf(E);
+      }
+      ++nl;
+    }
+    if (lane == 0) *lv_n = nl;
+  }
+  __syncthreads();
+  const int nl = *lv_n;
+  const int64_t elems = (int64_t)kD * DV;
+  if (tid >= 32 && tid < 32 + nl)  // warm L2 with the mirrored states summed below
+    prefetch_l2_bulk(p.R + (bh * p.N + lv_c[tid - 32]) * elems, (uint32_t)(elems * 4));
   const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
   float lam_in[kIntra / 2];
 #pragma unroll
