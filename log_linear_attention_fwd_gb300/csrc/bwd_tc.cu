@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     for (int q = 0; q < 7; ++q) mbar_init(&bars[q], 1);
     mbar_init(&bar_free[0], kThreadsB / 32);
     mbar_init(&bar_free[1], kThreadsB / 32);
+    tslot[1] = tslot[2] = 0;  // block-state loads issued into Vb and Kb
     fence_mbar_init();
   }
   for (int i = tid; i < 2 * kTile * kIntra; i += kThreadsB) dlb[i] = 0.f;
@@ -326,14 +327,48 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
 
-  // ---- P' = S' ⊙ M (bf16, into Vb: S' no longer reads V) and the intra-tile dlambda bins
-  // sum_s exp(cs_t - cs_s) S'[t, s] S[t, s] per level; chunk c of row r as in the forward
+  // the levels' block states: slot c_m holds U_{c-1} for odd c, the even block state else
+  int my_c = 0;
+  {
+    const int k = tid - 32;
+    if (k >= 0 && k < nlev) {
+      int m = 0;
+      for (int seen = -1; seen < k;) {
+        ++m;
+        if ((j >> (m - 1)) & 1) ++seen;
+      }
+      my_c = (j >> (m - 1)) << (m - 1);
+      nl_s[k] = (my_c & 1) ? p.lgu[bh * N + my_c - 1] : p.nlg[bh * N + my_c];
+    }
+  }
+  auto fetch = [&](int k) {  // thread 32+k: TMA of level k's block state into (k odd ? Kb : Vb)
+    if (tid == 32 + k) {
+      uint8_t* dst = (k & 1) ? Kb : Vb;
+      const bool is_u = (my_c & 1) != 0;
+      const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
+      atomicAdd(&tslot[1 + (k & 1)], 1u);
+      mbar_arrive_expect_tx(&bar_node[k & 1], kStateBytes);
+#pragma unroll
+      for (int pv = 0; pv < kPanels; ++pv)
+        tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[k & 1], dst + pv * kPanel, 64 * pv, row0);
+    }
+  };
+  // V's tile is free (S' is done): the lowest level's block state loads now
+  if (all_ok && nlev > 0) fetch(0);
+  __syncwarp();
+
+  // ---- P' = S' ⊙ M (bf16, two per column, into TMEM columns 384..447: chunk c of row r at
+  // [384 + 16c, +16)) and the intra-tile dlambda bins sum_s exp(cs_t - cs_s) S'[t, s]
+  // S[t, s] per level; chunk c of row r as in the forward
   float* bins = dlb + (hh * kTile + r) * kIntra;  // this thread's bins (private)
   if (all_ok) {
     const float* lam_r = lam_s + r * kLamStride;
     for (int c = hh; c < kTile / 32; c += 2) {
       if (c > qt) {
-        put_row32_zero(Vb, r, c);
+        uint32_t pz[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pz[e] = 0u;
+        tmem_st16(tmem + lane_base + 384 + 16 * c, pz);
         continue;
       }
       float sp[32], sa[32];
@@ -368,24 +403,24 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           sp[k] = pv;
         }
       }
-      put_row32_bf16(Vb, r, c, sp);
+      uint32_t pw[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pw[e] = pack_bf16(sp[2 * e], sp[2 * e + 1]);
+      tmem_st16(tmem + lane_base + 384 + 16 * c, pw);
     }
+    tmem_wait_st();
   }
-  tc_fence_after();
-  fence_proxy_async_smem();
   tc_fence_before();
   all_ok = __syncthreads_and(all_ok);
-  // ---- dQ = P' K into TMEM columns 256..383 (K MN-major as B)
+  // ---- dQ = P' K into TMEM columns 256..383 (P' from TMEM, K MN-major as B)
   if (all_ok && tid == 0) {
     tc_fence_after();
     constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
-    const uint32_t pa = smem_u32(Vb), ka = smem_u32(Kb);
+    const uint32_t ka = smem_u32(Kb);
 #pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk) {
-      const uint32_t aoff = (kk >> 2) * kPanel + (kk & 3) * 32;
-      mma_bf16(tmem + 256, smem_desc_sw128(pa + aoff, 16, 1024),
-               smem_desc_sw128(ka + kk * 2048, kPanel, 1024), idesc, kk > 0);
-    }
+    for (int kk = 0; kk < kTile / 16; ++kk)
+      mma_bf16_ts(tmem + 256, tmem + 384 + 8 * kk, smem_desc_sw128(ka + kk * 2048, kPanel, 1024),
+                  idesc, kk > 0);
     mma_commit(bar_dq);
   }
   __syncwarp();
@@ -395,39 +430,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     for (int l = 0; l < p.L; ++l)
       p.dlam[row * p.L + l] = l < kIntra ? bins[l] + dlb[(kTile + r) * kIntra + l] : 0.f;
   }
-  // the levels' block states: slot c_m holds U_{c-1} for odd c, the even block state else
-  int my_c = 0;
-  {
-    const int k = tid - 32;
-    if (k >= 0 && k < nlev) {
-      int m = 0;
-      for (int seen = -1; seen < k;) {
-        ++m;
-        if ((j >> (m - 1)) & 1) ++seen;
-      }
-      my_c = (j >> (m - 1)) << (m - 1);
-      nl_s[k] = (my_c & 1) ? p.lgu[bh * N + my_c - 1] : p.nlg[bh * N + my_c];
-    }
-  }
   cp_async_wait_all();  // the inter-level lambdas (read after the barrier below)
   ok = all_ok && mbar_wait(bar_dq, 0);
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
-  auto fetch = [&](int k) {  // thread 32+k: TMA of level k's block state into (k odd ? Kb : Vb)
-    if (tid == 32 + k) {
-      uint8_t* dst = (k & 1) ? Kb : Vb;
-      const bool is_u = (my_c & 1) != 0;
-      const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
-      mbar_arrive_expect_tx(&bar_node[k & 1], kStateBytes);
-#pragma unroll
-      for (int pv = 0; pv < kPanels; ++pv)
-        tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[k & 1], dst + pv * kPanel, 64 * pv, row0);
-    }
-  };
-  if (all_ok) {  // Kb (dQ's B) and Vb (P') are free
-    if (nlev > 0) fetch(0);
-    if (nlev > 1) fetch(1);
-  }
+  if (all_ok && nlev > 1) fetch(1);  // K's tile is free (dQ's MMA is done)
   __syncwarp();
 
   // ---- dQ into registers: this thread's half row, d in [64 hh, 64 hh + 64)
@@ -451,11 +458,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   // level's dlambda sum, then releases that TMEM buffer
   const int lane = tid & 31;
   uint32_t lvl_ph[2] = {0, 0}, node_ph[2] = {0, 0}, free_ph[2] = {0, 0};
+  uint32_t used[2] = {0, 0};  // thread 0: block-state loads waited for, per buffer
   float D = 0.f;
   bool lv_ok = all_ok;
   for (int k = 0; k <= nlev && all_ok; ++k) {
     if (tid == 0 && k < nlev) {
       bool go = lv_ok && mbar_wait(&bar_node[k & 1], node_ph[k & 1]);
+      if (go) ++used[k & 1];
       node_ph[k & 1] ^= 1;
       if (k >= 2) {
         go = go && mbar_wait(&bar_free[k & 1], free_ph[k & 1]);
@@ -553,6 +562,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && !all_ok) {
+    // after an error: wait (bounded) for the block-state loads still in flight into this
+    // CTA's shared memory before it is handed to another CTA
+    for (int bf = 0; bf < 2; ++bf)
+      for (uint32_t c = used[bf]; c < tslot[1 + bf]; ++c) mbar_wait(&bar_node[bf], c & 1);
+  }
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
