@@ -62,7 +62,8 @@ __device__ float block_sum(float x, float* sh) {
 // fp32 for every slot.  Both are row-major [d_k][d_v], the layout of the state.
 // One CTA per (level, b*h, slice of kSliceRows state rows).
 template <typename InT, bool kTcLayout>
-__global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, float* state) {
+__global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, float* state,
+                                                                 bool vec_in) {
   extern __shared__ float sm[];
   const int lvl = blockIdx.x;
   const int64_t bh = blockIdx.y;
@@ -123,18 +124,53 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(FwdArgs a, floa
     float* vs = ks + nb * kSliceRows;
     for (int i = threadIdx.x; i < nb; i += kThreads) w[i] = __expf(cs_t - cs[lo - t0 + i]);
     __syncthreads();
-    // (unrolled, so that each thread has several loads in flight)
+    if (sizeof(InT) == 2 && vec_in && rows == kSliceRows) {
+      // bf16 rows with 16-byte alignment: 8 values per load, all of them in flight at once
+      for (int i = threadIdx.x; i < nb * (kSliceRows / 8); i += kThreads) {
+        const int r = i / (kSliceRows / 8), q = i - r * (kSliceRows / 8);
+        const int64_t tok_k = ((int64_t)b * a.T + lo + r) * a.Hqk + h / a.hg;
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const InT*>(a.k) +
+                                                        tok_k * dk + r0 + 8 * q);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+          ks[r * kSliceRows + 8 * q + 2 * e] = w[r] * f.x;
+          ks[r * kSliceRows + 8 * q + 2 * e + 1] = w[r] * f.y;
+        }
+      }
+      const int vq = dv / 8;
+      for (int i = threadIdx.x; i < nb * vq; i += kThreads) {
+        const int r = i / vq, q = i - r * vq;
+        const int64_t tok = ((int64_t)b * a.T + lo + r) * a.H + h;
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const InT*>(a.v) + tok * dv +
+                                                        8 * q);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+          vs[r * kMaxDim + 8 * q + 2 * e] = f.x;
+          vs[r * kMaxDim + 8 * q + 2 * e + 1] = f.y;
+        }
+      }
+      for (int i = threadIdx.x; i < nb * (kMaxDim - dv); i += kThreads) {
+        const int r = i / (kMaxDim - dv), d = dv + i - r * (kMaxDim - dv);
+        vs[r * kMaxDim + d] = 0.f;
+      }
+    } else {
+      // (unrolled, so that each thread has several loads in flight)
 #pragma unroll 8
-    for (int i = threadIdx.x; i < nb * kSliceRows; i += kThreads) {
-      const int r = i / kSliceRows, d = i - r * kSliceRows;
-      const int64_t tok_k = ((int64_t)b * a.T + lo + r) * a.Hqk + h / a.hg;
-      ks[i] = d < rows ? w[r] * ld<InT>(a.k, tok_k * dk + r0 + d) : 0.f;
-    }
+      for (int i = threadIdx.x; i < nb * kSliceRows; i += kThreads) {
+        const int r = i / kSliceRows, d = i - r * kSliceRows;
+        const int64_t tok_k = ((int64_t)b * a.T + lo + r) * a.Hqk + h / a.hg;
+        ks[i] = d < rows ? w[r] * ld<InT>(a.k, tok_k * dk + r0 + d) : 0.f;
+      }
 #pragma unroll 8
-    for (int i = threadIdx.x; i < nb * kMaxDim; i += kThreads) {
-      const int r = i / kMaxDim, d = i - r * kMaxDim;
-      const int64_t tok = ((int64_t)b * a.T + lo + r) * a.H + h;
-      vs[i] = d < dv ? ld<InT>(a.v, tok * dv + d) : 0.f;
+      for (int i = threadIdx.x; i < nb * kMaxDim; i += kThreads) {
+        const int r = i / kMaxDim, d = i - r * kMaxDim;
+        const int64_t tok = ((int64_t)b * a.T + lo + r) * a.H + h;
+        vs[i] = d < dv ? ld<InT>(a.v, tok * dv + d) : 0.f;
+      }
     }
     __syncthreads();
     const int td = threadIdx.x >> 6, te = threadIdx.x & 63;
@@ -220,22 +256,27 @@ cudaError_t launch_prefill_state(const FwdArgs& a, bool tc_layout, int in_dtype,
       sizeof(float) * (32 + 2 * kMaxTile + (size_t)nb_max * (kSliceRows + kMaxDim));
   const dim3 grid((unsigned)a.L, (unsigned)(a.B * a.H),
                   (unsigned)((a.dk + kSliceRows - 1) / kSliceRows));
+  // 16-byte loads of bf16 k and v rows: dense rows of a multiple of 8 values, aligned bases
+  const bool vec_in = in_dtype == LL_BF16 && a.dk % 8 == 0 && a.dv % 8 == 0 &&
+                      (reinterpret_cast<uintptr_t>(a.k) & 15u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(a.v) & 15u) == 0 && a.sk[2] == a.dk &&
+                      a.sv[2] == a.dv;
   cudaError_t e = cudaSuccess;
   if (in_dtype == LL_BF16) {
     if (tc_layout) {
       if ((e = cudaFuncSetAttribute(prefill_state_kernel<__nv_bfloat16, true>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) ==
           cudaSuccess)
-        prefill_state_kernel<__nv_bfloat16, true><<<grid, kThreads, smem, s>>>(a, state);
+        prefill_state_kernel<__nv_bfloat16, true><<<grid, kThreads, smem, s>>>(a, state, vec_in);
     } else if ((e = cudaFuncSetAttribute(prefill_state_kernel<__nv_bfloat16, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem)) == cudaSuccess) {
-      prefill_state_kernel<__nv_bfloat16, false><<<grid, kThreads, smem, s>>>(a, state);
+      prefill_state_kernel<__nv_bfloat16, false><<<grid, kThreads, smem, s>>>(a, state, vec_in);
     }
   } else if ((e = cudaFuncSetAttribute(prefill_state_kernel<float, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) ==
              cudaSuccess) {
-    prefill_state_kernel<float, false><<<grid, kThreads, smem, s>>>(a, state);
+    prefill_state_kernel<float, false><<<grid, kThreads, smem, s>>>(a, state, vec_in);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
