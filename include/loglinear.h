@@ -287,10 +287,13 @@ LL_API int loglinear_gdn_fwd(const void* q, const void* k, const void* v, const 
  * the chunks then carries every chunk-level block state by the chunk transitions, merges
  * them by the lssb rule on chunk indices and adds their lambda-weighted readout (first
  * page, sections 矩阵分解 and 两阶段计算, with the transition in place of the scalar decay).
- * Arguments as loglinear_gdn_fwd, without the final state, plus a workspace of
+ * Arguments as loglinear_gdn_fwd, plus a workspace of
  * loglinear_gdn_fwd_chunked_workspace_size() bytes (256-byte aligned; the chunks' partial
- * outputs, carried queries, transitions and states in fp32).  No alignment is needed of
- * q, k, v.  Supported: 1 <= dk, dv <= 128, L <= 64.
+ * outputs, carried queries, transitions and states in fp32).  state_out (optional) receives
+ * the decode state after T-1: the chunk-level states from the scan, the levels inside the
+ * last chunk from the lssb steps over its tokens alone (then q and k must be 4-byte aligned
+ * and, for bf16, dk even).  Otherwise no alignment is needed of q, k, v.  Supported:
+ * 1 <= dk, dv <= 128, L <= 64, T <= 2^25.
  * Errors: LL_ERR_INVALID, LL_ERR_SHAPE, LL_ERR_DTYPE, LL_ERR_UNSUPPORTED, LL_ERR_WORKSPACE,
  * LL_ERR_ALIGN, LL_ERR_CUDA.
  */
@@ -298,7 +301,8 @@ LL_API int loglinear_gdn_fwd_chunked_workspace_size(int64_t B, int64_t T, int64_
                                                     int64_t dv, size_t* bytes);
 LL_API int loglinear_gdn_fwd_chunked(const void* q, const void* k, const void* v,
                                      const float* log_a, const float* beta, const float* lambda,
-                                     void* out, int64_t B, int64_t T, int64_t H, int64_t Hqk,
+                                     void* out, float* state_out, int64_t B, int64_t T,
+                                     int64_t H, int64_t Hqk,
                                      int64_t dk, int64_t dv, int64_t L, int in_dtype,
                                      int out_dtype, void* workspace, size_t workspace_bytes,
                                      ll_stream_t stream);

@@ -58,8 +58,9 @@ SIGNATURES = {
                                  _i64, _i64, _i64, _int, _int, _vp]),
     "loglinear_gdn_fwd_chunked_workspace_size": (_int, [_i64, _i64, _i64, _i64, _i64,
                                                         ctypes.POINTER(ctypes.c_size_t)]),
-    "loglinear_gdn_fwd_chunked": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
-                                         _i64, _i64, _i64, _i64, _int, _int, _vp, _sz, _vp]),
+    "loglinear_gdn_fwd_chunked": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                         _i64, _i64, _i64, _i64, _i64, _int, _int, _vp, _sz,
+                                         _vp]),
     "loglinear_debug_level_map": (_int, [_i64, _int, _int, _vp, _vp]),
     "loglinear_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "loglinear_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
@@ -299,10 +300,10 @@ def gdn_fwd_chunked_workspace_size(B, T, H, dk, dv) -> int:
 
 
 def loglinear_gdn_fwd_chunked(q, k, v, log_a, beta, lam, out=None, out_dtype=None,
-                              workspace=None, stream=None):
+                              workspace=None, state=None, stream=None):
     """Log-Linear Gated DeltaNet over a whole sequence in chunks of 64 tokens (same inputs and
-    output as loglinear_gdn_fwd, no final state).  The workspace is allocated with torch
-    when not given."""
+    output as loglinear_gdn_fwd; `state`, [B,H,L,dk,dv] fp32, receives the decode state after
+    T-1 when given).  The workspace is allocated with torch when not given."""
     B, T, Hqk, dk = q.shape
     H, dv, L = v.shape[2], v.shape[-1], lam.shape[-1]
     _check_dev("q", q)
@@ -311,6 +312,8 @@ def loglinear_gdn_fwd_chunked(q, k, v, log_a, beta, lam, out=None, out_dtype=Non
     _check_dev("log_a", log_a, torch.float32, (B, T, H))
     _check_dev("beta", beta, torch.float32, (B, T, H))
     _check_dev("lam", lam, torch.float32, (B, T, H, L))
+    if state is not None:
+        _check_dev("state", state, torch.float32, (B, H, L, dk, dv))
     if out is None:
         out = torch.empty(B, T, H, dv, device=q.device, dtype=out_dtype or q.dtype)
     _check_dev("out", out, shape=(B, T, H, dv))
@@ -321,7 +324,8 @@ def loglinear_gdn_fwd_chunked(q, k, v, log_a, beta, lam, out=None, out_dtype=Non
     if workspace is None:
         workspace = torch.empty(max(sz.value, 1), device=q.device, dtype=torch.uint8)
     st = _lib.loglinear_gdn_fwd_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(beta),
-                                        _ptr(lam), _ptr(out), B, T, H, Hqk, dk, dv, L,
+                                        _ptr(lam), _ptr(out), _ptr(state), B, T, H, Hqk, dk, dv,
+                                        L,
                                         _dtype_code(q), _dtype_code(out), _ptr(workspace),
                                         workspace.numel(), _stream(stream))
     if st != LL_OK:

@@ -95,6 +95,7 @@ struct GdnChunkArgs {
   float* qt;          // [B*H][N][64][dk]   workspace
   float* P;           // [B*H][N][dk][dk]   workspace
   float* U;           // [B*H][N][dk][dv]   workspace
+  float* state;       // [B, H, L, dk, dv] or null: the chunk levels of the state after T-1
   int B, T, H, hg, dk, dv, L, N;
 };
 
@@ -530,6 +531,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(GdnChunkArg
     }
     __syncthreads();  // buffer j & 1 is refilled by the issue of chunk j + 2
   }
+  // ---- the chunk-level states after the last chunk: levels 6 + m of the decode state
+  if (a.state && col_ok) {
+#pragma unroll
+    for (int m = 1; m < kLv; ++m) {
+      if (m >= levels || !((live >> m) & 1)) continue;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 8 * rg + i;
+        if (r < dk) a.state[((bh * a.L + kLc + m) * dk + r) * (int64_t)dv + c0 + col] = z[m][i];
+      }
+    }
+  }
 }
 
 template <typename OutT, int kLv>
@@ -555,12 +568,18 @@ size_t gdn_chunk_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, in
 }
 
 cudaError_t launch_gdn_chunked(const void* q, const void* k, const void* v, const float* log_a,
-                               const float* beta, const float* lam, void* out, int B, int T, int H,
-                               int Hqk, int dk, int dv, int L, int in_dtype, int out_dtype,
-                               void* workspace, cudaStream_t s) {
+                               const float* beta, const float* lam, void* out, float* state,
+                               int B, int T, int H, int Hqk, int dk, int dv, int L, int in_dtype,
+                               int out_dtype, void* workspace, cudaStream_t s) {
+  if (state) {  // levels the state does not reach stay zero
+    const cudaError_t e =
+        cudaMemsetAsync(state, 0, sizeof(float) * (size_t)B * H * L * dk * dv, s);
+    if (e != cudaSuccess) return e;
+  }
   if (T == 0) return cudaSuccess;
   GdnChunkArgs a;
   a.q = q; a.k = k; a.v = v; a.log_a = log_a; a.beta = beta; a.lam = lam; a.out = out;
+  a.state = state;
   a.B = B; a.T = T; a.H = H; a.hg = H / Hqk; a.dk = dk; a.dv = dv; a.L = L;
   a.N = (T + kC - 1) / kC;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -602,7 +621,15 @@ cudaError_t launch_gdn_chunked(const void* q, const void* k, const void* v, cons
     e = levels <= 12 ? launch_scan<float, 12>(a, levels, grid2, smem2, s)
                      : launch_scan<float, kMaxLv>(a, levels, grid2, smem2, s);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!state) return cudaSuccess;
+  // the levels inside the last chunk (0..6): its own tokens run through the lssb steps from
+  // an empty state (the chunk starts at a multiple of 64, so the low bits of the positions
+  // are the same); the outputs of that run land in the partial-output scratch, which the
+  // scan has consumed
+  const int t_last = (a.N - 1) * kC;
+  return launch_gdn_fwd_tail(q, k, v, log_a, beta, lam, a.o_intra, state, B, T, t_last, H, Hqk,
+                             dk, dv, L, L < kLc + 1 ? L : kLc + 1, in_dtype, s);
 }
 
 }  // namespace ll

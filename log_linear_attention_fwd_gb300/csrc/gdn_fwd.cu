@@ -50,6 +50,8 @@ struct GdnFwdArgs {
   void* out;            // [B, T, H, dv]
   float* state;         // [B, H, L, dk, dv] or null (zeroed by the host when given)
   int B, T, H, hg, dk, dv, L;
+  int Tfull, t0;        // the run covers tokens [t0, t0 + T) of sequences of Tfull tokens
+  int state_levels;     // levels of the final state written (the rest left as they are)
 };
 
 template <typename InT, typename OutT, int kLv>
@@ -90,7 +92,7 @@ __global__ void __launch_bounds__(kLv * kCols, 1) gdn_fwd_kernel(GdnFwdArgs a) {
       const int which = i / (n * row_words);  // 0: q, 1: k
       const int rem = i - which * n * row_words;
       const int tt = rem / row_words, wd = rem - tt * row_words;
-      const int64_t tok = ((int64_t)b * T + s * kStage + tt) * Hqk + hq;
+      const int64_t tok = ((int64_t)b * a.Tfull + a.t0 + s * kStage + tt) * Hqk + hq;
       const uint32_t* src =
           reinterpret_cast<const uint32_t*>(static_cast<const InT*>(which ? a.k : a.q) + tok * dk);
       cp_async_4(dst + (which * kStage + tt) * row_words + wd, src + wd);
@@ -121,17 +123,17 @@ __global__ void __launch_bounds__(kLv * kCols, 1) gdn_fwd_kernel(GdnFwdArgs a) {
       }
       for (int i = tid; i < kStage * kCols; i += kThreads) {
         const int tt = i / kCols, c = i - tt * kCols;
-        const int64_t tok = ((int64_t)b * T + s * kStage + tt) * a.H + h;
+        const int64_t tok = ((int64_t)b * a.Tfull + a.t0 + s * kStage + tt) * a.H + h;
         vs[i] = (tt < n && c0 + c < dv) ? to_f32(static_cast<const InT*>(a.v)[tok * dv + c0 + c])
                                         : 0.f;
       }
       for (int i = tid; i < kStage * kLv; i += kThreads) {
         const int tt = i / kLv, l = i - tt * kLv;
-        const int64_t tok = ((int64_t)b * T + s * kStage + tt) * a.H + h;
+        const int64_t tok = ((int64_t)b * a.Tfull + a.t0 + s * kStage + tt) * a.H + h;
         ls[i] = (tt < n && l < a.L) ? a.lam[tok * a.L + l] : 0.f;
       }
       if (tid < kStage) {
-        const int64_t tok = ((int64_t)b * T + s * kStage + tid) * a.H + h;
+        const int64_t tok = ((int64_t)b * a.Tfull + a.t0 + s * kStage + tid) * a.H + h;
         al[tid] = (tid < n && a.log_a) ? __expf(a.log_a[tok]) : 1.f;
         bt[tid] = tid < n ? a.beta[tok] : 0.f;
       }
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kLv * kCols, 1) gdn_fwd_kernel(GdnFwdArgs a) {
     for (int i = tid; i < n * kCols; i += kThreads) {
       const int tt = i / kCols, c = i - tt * kCols;
       if (c0 + c < dv) {
-        const int64_t tok = ((int64_t)b * T + s * kStage + tt) * a.H + h;
+        const int64_t tok = ((int64_t)b * a.Tfull + a.t0 + s * kStage + tt) * a.H + h;
         static_cast<OutT*>(a.out)[tok * dv + c0 + c] = from_f32<OutT>(os[i]);
       }
     }
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(kLv * kCols, 1) gdn_fwd_kernel(GdnFwdArgs a) {
     // barrier at its top; os is rewritten only after the next conversion's barriers)
   }
   // ---- the final per-level state (the decode state after position T-1)
-  if (a.state && col_ok && lv < a.L) {
+  if (a.state && col_ok && lv < a.state_levels) {
     float* dst = a.state + ((bh * a.L + lv) * (int64_t)dk) * dv + col;
 #pragma unroll
     for (int d = 0; d < kDk; ++d)
@@ -269,6 +271,7 @@ cudaError_t launch_gdn_fwd(const void* q, const void* k, const void* v, const fl
   a.q = q; a.k = k; a.v = v; a.log_a = log_a; a.beta = beta; a.lam = lam; a.out = out;
   a.state = state;
   a.B = B; a.T = T; a.H = H; a.hg = H / Hqk; a.dk = dk; a.dv = dv; a.L = L;
+  a.Tfull = T; a.t0 = 0; a.state_levels = L;
   if (state) {
     const cudaError_t e =
         cudaMemsetAsync(state, 0, sizeof(float) * (size_t)B * H * L * dk * dv, s);
@@ -280,6 +283,21 @@ cudaError_t launch_gdn_fwd(const void* q, const void* k, const void* v, const fl
                                 : launch_io<__nv_bfloat16, float>(a, levels, s);
   return out_dtype == LL_BF16 ? launch_io<float, __nv_bfloat16>(a, levels, s)
                               : launch_io<float, float>(a, levels, s);
+}
+
+cudaError_t launch_gdn_fwd_tail(const void* q, const void* k, const void* v, const float* log_a,
+                                const float* beta, const float* lam, float* out_f32,
+                                float* state, int B, int Tfull, int t0, int H, int Hqk, int dk,
+                                int dv, int L, int state_levels, int in_dtype, cudaStream_t s) {
+  GdnFwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_a = log_a; a.beta = beta; a.lam = lam; a.out = out_f32;
+  a.state = state;
+  a.B = B; a.T = Tfull - t0; a.H = H; a.hg = H / Hqk; a.dk = dk; a.dv = dv; a.L = L;
+  a.Tfull = Tfull; a.t0 = t0; a.state_levels = state_levels;
+  if (a.T <= 0) return cudaSuccess;
+  const int levels = a.T > 1 ? 32 - __builtin_clz((unsigned)(a.T - 1)) + 1 : 1;
+  return in_dtype == LL_BF16 ? launch_io<__nv_bfloat16, float>(a, levels, s)
+                             : launch_io<float, float>(a, levels, s);
 }
 
 }  // namespace ll

@@ -213,9 +213,15 @@ cudaError_t launch_gdn_decode(float* state, const void* q, const void* k, const 
 // sequential scan of the chunk-level states); workspace of gdn_chunk_workspace_bytes().
 size_t gdn_chunk_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t dk, int64_t dv);
 cudaError_t launch_gdn_chunked(const void* q, const void* k, const void* v, const float* log_a,
-                               const float* beta, const float* lam, void* out, int B, int T, int H,
-                               int Hqk, int dk, int dv, int L, int in_dtype, int out_dtype,
-                               void* workspace, cudaStream_t s);
+                               const float* beta, const float* lam, void* out, float* state,
+                               int B, int T, int H, int Hqk, int dk, int dv, int L, int in_dtype,
+                               int out_dtype, void* workspace, cudaStream_t s);
+// The recurrent form over tokens [t0, Tfull) only, from an empty state: fp32 outputs into
+// out_f32 ([B, Tfull, H, dv] indexing) and the first state_levels levels of the state.
+cudaError_t launch_gdn_fwd_tail(const void* q, const void* k, const void* v, const float* log_a,
+                                const float* beta, const float* lam, float* out_f32,
+                                float* state, int B, int Tfull, int t0, int H, int Hqk, int dk,
+                                int dv, int L, int state_levels, int in_dtype, cudaStream_t s);
 // Log-Linear Gated DeltaNet forward in the recurrent form (levels = bit_length(T-1) + 1
 // Fenwick levels in use); state, when non-null, receives the per-level state after T-1.
 cudaError_t launch_gdn_fwd(const void* q, const void* k, const void* v, const float* log_a,

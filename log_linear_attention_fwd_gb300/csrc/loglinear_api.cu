@@ -461,7 +461,8 @@ int loglinear_gdn_fwd_chunked_workspace_size(int64_t B, int64_t T, int64_t H, in
 }
 
 int loglinear_gdn_fwd_chunked(const void* q, const void* k, const void* v, const float* log_a,
-                              const float* beta, const float* lambda, void* out, int64_t B,
+                              const float* beta, const float* lambda, void* out,
+                              float* state_out, int64_t B,
                               int64_t T, int64_t H, int64_t Hqk, int64_t dk, int64_t dv,
                               int64_t L, int in_dtype, int out_dtype, void* workspace,
                               size_t workspace_bytes, ll_stream_t stream) {
@@ -474,14 +475,25 @@ int loglinear_gdn_fwd_chunked(const void* q, const void* k, const void* v, const
   // the scan keeps every chunk level of its columns in shared memory: up to 2^19 chunks
   if (T > ((int64_t)64 << 19)) return LL_ERR_UNSUPPORTED;
   if (T > 0 && L < bit_length(T - 1) + 1) return LL_ERR_SHAPE;
-  if (B == 0 || H == 0 || T == 0) return LL_OK;
+  if (in_dtype == LL_BF16 && (dk & 1) && state_out) return LL_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0) return LL_OK;
+  if (state_out && reinterpret_cast<uintptr_t>(state_out) % 4) return LL_ERR_ALIGN;
+  if (T == 0) {  // an empty prompt: an empty state
+    const cudaError_t e = launch_gdn_chunked(q, k, v, log_a, beta, lambda, out, state_out,
+                                             (int)B, 0, (int)H, (int)Hqk, (int)dk, (int)dv,
+                                             (int)L, in_dtype, out_dtype, workspace,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LL_OK : cuda_fail(e);
+  }
   if (!q || !k || !v || !beta || !lambda || !out) return LL_ERR_INVALID;
   if (!workspace || workspace_bytes < gdn_chunk_workspace_bytes(B, T, H, dk, dv))
     return LL_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_ALIGN;
-  const cudaError_t e = launch_gdn_chunked(q, k, v, log_a, beta, lambda, out, (int)B, (int)T,
-                                           (int)H, (int)Hqk, (int)dk, (int)dv, (int)L, in_dtype,
-                                           out_dtype, workspace,
+  if (state_out && (reinterpret_cast<uintptr_t>(q) % 4 || reinterpret_cast<uintptr_t>(k) % 4))
+    return LL_ERR_ALIGN;  // the last chunk's run stages q and k with 4-byte copies
+  const cudaError_t e = launch_gdn_chunked(q, k, v, log_a, beta, lambda, out, state_out, (int)B,
+                                           (int)T, (int)H, (int)Hqk, (int)dk, (int)dv, (int)L,
+                                           in_dtype, out_dtype, workspace,
                                            reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? LL_OK : cuda_fail(e);
 }

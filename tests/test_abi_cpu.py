@@ -305,14 +305,14 @@ def test_gdn_fwd_chunked_validation_codes(L):
     f = L.lib().loglinear_gdn_fwd_chunked
     p = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation first
     need = L.gdn_fwd_chunked_workspace_size(1, 100, 2, 8, 8)
-    ok = dict(q=p, k=p, v=p, log_a=None, beta=p, lam=p, out=p, B=1, T=100, H=2, Hqk=2, dk=8,
-              dv=8, L=8, i=0, o=0, ws=ctypes.c_void_p(256), wsb=need - 1, s=None)
+    ok = dict(q=p, k=p, v=p, log_a=None, beta=p, lam=p, out=p, state=None, B=1, T=100, H=2,
+              Hqk=2, dk=8, dv=8, L=8, i=0, o=0, ws=ctypes.c_void_p(256), wsb=need - 1, s=None)
 
     def call(**kw):
         a = dict(ok, **kw)
-        return f(a["q"], a["k"], a["v"], a["log_a"], a["beta"], a["lam"], a["out"], a["B"], a["T"],
-                 a["H"], a["Hqk"], a["dk"], a["dv"], a["L"], a["i"], a["o"], a["ws"], a["wsb"],
-                 a["s"])
+        return f(a["q"], a["k"], a["v"], a["log_a"], a["beta"], a["lam"], a["out"], a["state"],
+                 a["B"], a["T"], a["H"], a["Hqk"], a["dk"], a["dv"], a["L"], a["i"], a["o"],
+                 a["ws"], a["wsb"], a["s"])
 
     assert need >= 4 * (100 * 2 * 8 + 2 * 2 * 64 * 8 + 2 * 2 * 8 * 8 + 2 * 2 * 8 * 8)
     assert call(beta=None, wsb=need) == L.LL_ERR_INVALID
@@ -323,4 +323,7 @@ def test_gdn_fwd_chunked_validation_codes(L):
     assert call(o=5) == L.LL_ERR_DTYPE
     assert call() == L.LL_ERR_WORKSPACE               # one byte short
     assert call(wsb=need, ws=ctypes.c_void_p(272)) == L.LL_ERR_ALIGN
+    assert call(wsb=need, state=ctypes.c_void_p(258)) == L.LL_ERR_ALIGN
+    assert call(wsb=need, state=p, q=ctypes.c_void_p(18)) == L.LL_ERR_ALIGN
+    assert call(wsb=need, state=p, dk=7, i=1) == L.LL_ERR_UNSUPPORTED  # bf16 rows, odd d_k
     assert call(T=0) == L.LL_OK                       # empty: nothing to do

@@ -227,3 +227,34 @@ def test_gdn_fwd_chunked_many_chunk_levels(LL):
     got = _run_chunked(LL, x)
     for r in rows:
         assert rel_l2(got[:, r], want[:, r]) <= 1e-4, r
+
+
+@pytest.mark.parametrize("T,dk,dv,dtype,decay", [(37, 32, 16, "f32", True),
+                                                  (130, 64, 32, "f32", False),
+                                                  (1000, 128, 128, "f32", True),
+                                                  (2100, 32, 32, "bf16", True)])
+def test_gdn_fwd_chunked_final_state(LL, T, dk, dv, dtype, decay):
+    """The chunked form's final state (chunk levels from the scan, the last chunk's levels from
+    the lssb steps over its tokens) against the oracle's recurrence, every level; and the
+    decode step continuing from it."""
+    L = (T - 1).bit_length() + 2
+    cfg = W.FwdConfig("gdn_chunk_state", 1, 2, T + 3, dk, dv, 64, L, dtype, decay, "softplus",
+                      seed=T + 17)
+    x = W.make_gdn_inputs(cfg)
+    want, _ = oracle.gdn_recurrence(x["q"], x["k"], x["v"], x["log_a"], x["beta"], x["lam"])
+    head = {k: (None if v is None else v[:, :T].contiguous()) for k, v in x.items()}
+    _, S_want = oracle.gdn_recurrence(head["q"], head["k"], head["v"], head["log_a"],
+                                      head["beta"], head["lam"])
+    d = _dev(head)
+    S = torch.full((1, 2, L, dk, dv), float("nan"), device="cuda")
+    LL.loglinear_gdn_fwd_chunked(d["q"], d["k"], d["v"], d["log_a"], d["beta"], d["lam"],
+                                 out_dtype=torch.float32, state=S)
+    torch.cuda.synchronize()
+    assert rel_l2(S.cpu(), S_want) <= TOL_F32
+    outs = []
+    for t in range(T, T + 3):
+        sl = lambda n: None if x[n] is None else x[n][:, t].contiguous().cuda()
+        o = LL.loglinear_gdn_decode_step(S, sl("q"), sl("k"), sl("v"), sl("log_a"), sl("beta"),
+                                         sl("lam"), t, out_dtype=torch.float32)
+        outs.append(o.cpu())
+    assert rel_l2(torch.stack(outs, 1), want[:, T:]) <= TOL_F32
