@@ -53,7 +53,7 @@ struct TcParams {
   const float* lam;
   void* out;
   int64_t so_b, so_t, so_h;  // element strides of out's b, t and h dimensions
-  uint8_t* U;        // [B*H][N] tile states U_i, bf16 [d_k][d_v]
+  uint8_t* U;        // [B*H][N] tile states U_i, bf16 [d_k][d_v] (written for even i only)
   uint8_t* nodes;    // [B*H][N] block states of the even slots, bf16 [d_k][d_v]
   float* lgu;        // [B*H][N] log decay of each tile
   float* nlg;        // [B*H][N] log decay of the block in each even slot
@@ -102,9 +102,9 @@ __device__ __forceinline__ void put_row32_bf16(uint8_t* buf, int r, int c, const
 //   4. (after 5) P = S ⊙ exp(cs_t - cs_s) ⊙ lambda[t, l(t,s)] on the causal half, bf16
 //      into TMEM columns 128..191 (the state's, read out by then); O = P V into columns
 //      0..d_v.
-//   5. Right after the state MMA (before P): U_j is published (staged bf16 in the K
-//      buffer, stored coalesced); for odd j the CTA then forms the block state of slot
-//      j+1 (below) and publishes it.  Q stays in shared memory for step 6.
+//   5. Right after the state MMA (before P): U_j is staged bf16 in the K buffer; for even
+//      j it is published (stored coalesced), for odd j the CTA forms the block state of
+//      slot j+1 from it (below) and publishes that.  Q stays in shared memory for step 6.
 //   6. For every set bit m-1 of j, in increasing m: the block state of slot c_m by TMA
 //      into shared memory (K's tile holds one state of d_v = 128 or two of d_v = 64 and
 //      is free before P is built: the lowest levels load then if their flags are up;
@@ -372,8 +372,8 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
 
-  // ---- publish U_j (staged bf16 in Kb, which the state MMA no longer reads, then stored
-  // coalesced) and, for odd j, form the block state of slot j+1 and publish it.  Q stays
+  // ---- stage U_j (bf16 in Kb, which the state MMA no longer reads); publish it (stored
+  // coalesced) for even j; for odd j form the block state of slot j+1 and publish it.  Q stays
   // in Qb for the level MMAs.  Published states are row-major [d_k][d_v] bf16; thread tid
   // moves the 16-byte pieces q = it * 256 + tid.  This runs even after an error, so that
   // no reader waits for a flag that is never raised.
@@ -390,12 +390,16 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   }
   __syncthreads();
   const bool forms = (j & 1) && j + 1 < N;  // odd j forms the block state of slot j+1
+  // Only U of even tiles is read by other tiles (slot j+1, odd, is U_j; an even slot's
+  // parts are U_{c-2} and U_{c-1}, and U_{c-1} is summed by its own CTA), by the backward
+  // and by the prefill: odd tiles keep theirs on chip.
+  const bool pub_u = !(j & 1);
   float acc[8 * kStatePieces];              // that sum, fp32, in this thread's pieces
 #pragma unroll
   for (int it = 0; it < kStatePieces; ++it) {
     const int q = it * kThreadsF + tid;
     const uint4 w = *reinterpret_cast<const uint4*>(Kb + piece_offset<DV>(q));
-    reinterpret_cast<uint4*>(const_cast<uint8_t*>(Ug) + (int64_t)j * G::kStateBytes)[q] = w;
+    if (pub_u) reinterpret_cast<uint4*>(const_cast<uint8_t*>(Ug) + (int64_t)j * G::kStateBytes)[q] = w;
     const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -405,8 +409,10 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     }
   }
   if (tid == 0) p.lgu[bh * N + j] = lg;
-  __syncthreads();
-  if (tid == 0) st_release_gpu(&rdy_u[j], decay_flag(lg));
+  if (pub_u) {
+    __syncthreads();
+    if (tid == 0) st_release_gpu(&rdy_u[j], decay_flag(lg));
+  }
   if (forms) {
     // Slot c = j+1 holds [c - 2^z, c), z = ctz(c): the block states of slots c - 2^(k-1)
     // (k = z..2), then U_{j-1}, then U_j; summed right to left, each weighted by the

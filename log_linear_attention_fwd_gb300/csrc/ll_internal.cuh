@@ -65,7 +65,8 @@ struct FwdArgs {
   // feature dimension is contiguous); dense: {T*Hx*w, Hx*w, w}
   int64_t sq[3], sk[3], sv[3], so[3];
   // workspace
-  void* U;        // [B*H][N][dk][dv] chunk states (fp32 on CUDA cores, bf16 on tensor cores)
+  void* U;        // [B*H][N][dk][dv] chunk states (fp32 on CUDA cores; bf16 on tensor cores,
+                  // written for even tiles only: no reader takes an odd one)
   void* nodes;    // [B*H][N][dk*dv] Fenwick block states, slot c = first reader chunk
   float* lg;      // [B*H][N] log decay of each whole chunk
   // tensor cores only (block states published between CTAs of one launch):
