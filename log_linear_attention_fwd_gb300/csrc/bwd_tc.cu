@@ -743,19 +743,34 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (tid < kTile) colsum[tid] = 0.f;
   if (warp == 2) {  // the tile's levels: blocks of later tiles, with exp(E_m)
     int nl = 0;
+    int64_t cmax = i + 1;
     for (int m = 1; (int64_t(1) << (m - 1)) < p.N; ++m) {
       if ((i >> (m - 1)) & 1) continue;
       const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
       if (c1 >= p.N) continue;
-      float E = 0.f;
-      for (int64_t x = i + 1 + lane; x < c1; x += 32) E += p.lgu[bh * p.N + x];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) E += __shfl_xor_sync(0xffffffffu, E, o);
-      if (lane == 0) {
-        lv_c[nl] = (int)c1;
-        lv_w[nl] = __expf(E);
-      }
+      if (lane == 0) lv_c[nl] = (int)c1;
+      cmax = c1;  // c1 grows with m
       ++nl;
+    }
+    __syncwarp();
+    // E_m = the log decays of tiles [i+1, c1_m): running prefix sums over 32 tiles a step,
+    // read off at c1_m - 1 (one pass for all levels)
+    int k = 0;
+    for (; k < nl && lv_c[k] == i + 1; ++k)
+      if (lane == 0) lv_w[k] = 1.f;
+    float run = 0.f;
+    for (int64_t base = i + 1; base < cmax; base += 32) {
+      float x = base + lane < cmax ? p.lgu[bh * p.N + base + lane] : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      for (; k < nl && lv_c[k] - 1 < base + 32; ++k) {
+        const float E = run + __shfl_sync(0xffffffffu, x, (int)(lv_c[k] - 1 - base));
+        if (lane == 0) lv_w[k] = __expf(E);
+      }
+      run += __shfl_sync(0xffffffffu, x, 31);
     }
     if (lane == 0) *lv_n = nl;
   }
@@ -892,6 +907,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
   for (int it = 0; it < kIters; ++it) rt[it] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (all_ok) {
+#pragma unroll 2
     for (int l = 0; l < nl; ++l) {
       const float w = lv_w[l];
       const float* src = p.R + (bh * p.N + (int64_t)lv_c[l]) * elems + col;
@@ -1127,16 +1143,31 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   __syncwarp();
   // while the tiles load: every level's D and the inter-level lambdas
   if (warp == 2) {  // D of every level: log decay of the tiles [c, j)
-    int k = 0;
-    for (int m = 1; m < kMaxChunkLevels && k < nlev; ++m) {
-      if (!((j >> (m - 1)) & 1)) continue;
-      const int64_t c = ((int64_t)j >> (m - 1)) << (m - 1);
-      float x = 0.f;
-      for (int64_t i = c + lane; i < j; i += 32) x += p.lgu[bh * p.N + i];
+    // c falls as m grows: running suffix sums over 32 tiles a step, from j - 1 down, read
+    // off at each level's c (one pass for all levels)
+    int k = 0, m = 0;
+    do ++m;
+    while (!((j >> (m - 1)) & 1));  // nlev >= 1
+    int64_t c = ((int64_t)j >> (m - 1)) << (m - 1);  // block start of level k
+    float run = 0.f;
+    for (int64_t top = j; k < nlev; top -= 32) {  // tiles [top - 32, top)
+      const int64_t x_i = top - 1 - lane;
+      float x = x_i >= 0 ? p.lgu[bh * p.N + x_i] : 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      if (lane == 0) D_s[k] = x;
-      ++k;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;  // lane l: tiles [top - 1 - l, top)
+      }
+      while (k < nlev && c >= top - 32) {
+        const float D = run + (c < top ? __shfl_sync(0xffffffffu, x, (int)(top - 1 - c)) : 0.f);
+        if (lane == 0) D_s[k] = D;
+        if (++k < nlev) {
+          do ++m;
+          while (!((j >> (m - 1)) & 1));
+          c = ((int64_t)j >> (m - 1)) << (m - 1);
+        }
+      }
+      run += __shfl_sync(0xffffffffu, x, 31);
     }
   }
   {
