@@ -386,17 +386,42 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           sp[k] = x * wl;
         }
         bins[lvl] += ge * wsum;
-      } else {  // the diagonal chunk
-        const bool fact = cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f;
-        const float gt = __expf(cs - cs_s[c * 32 + 31]);
+      } else if (cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f) {
+        // the diagonal chunk with a decay range that keeps exp(cs_t - cs_e) <= e^80: the
+        // pair (r, s) has level bit_length(lane XOR k) <= 5 for column k <= lane, so the six
+        // lambdas and dlambda bins of the levels inside a 32-token chunk stay in registers
+        const int lane = tid & 31;
+        const float gt = row_live ? __expf(cs - cs_s[c * 32 + 31]) : 0.f;
+        const float l0 = lam_r[0], l1 = lam_r[1], l2 = lam_r[2], l3 = lam_r[3], l4 = lam_r[4],
+                    l5 = lam_r[5];
+        float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f, b4 = 0.f, b5 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int x = lane ^ k;
+          const float xv = k <= lane ? sp[k] * (gt * fcol[c * 32 + k]) : 0.f;
+          const float g = xv * sa[k];
+          b5 += x >= 16 ? g : 0.f;
+          b4 += (x >= 8 && x < 16) ? g : 0.f;
+          b3 += (x >= 4 && x < 8) ? g : 0.f;
+          b2 += (x >= 2 && x < 4) ? g : 0.f;
+          b1 += x == 1 ? g : 0.f;
+          b0 += x == 0 ? g : 0.f;
+          sp[k] = xv * (x >= 16 ? l5 : x >= 8 ? l4 : x >= 4 ? l3 : x >= 2 ? l2 : x >= 1 ? l1 : l0);
+        }
+        bins[0] += b0;
+        bins[1] += b1;
+        bins[2] += b2;
+        bins[3] += b3;
+        bins[4] += b4;
+        bins[5] += b5;
+      } else {  // the diagonal chunk, any decay
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int s = c * 32 + k;
           float pv = 0.f;
           if (s <= r && row_live) {
             const int lvl = fenwick_level((uint32_t)r, (uint32_t)s);
-            const float e = fact ? gt * fcol[s] : __expf(cs - cs_s[s]);
-            const float x = sp[k] * e;
+            const float x = sp[k] * __expf(cs - cs_s[s]);
             bins[lvl] += x * sa[k];
             pv = x * lam_r[lvl];
           }
@@ -850,19 +875,34 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         warp_column_sums(g);
         atomicAdd(&colsum[c * 32 + lane], g[0]);
       } else {
-        const bool fact = cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f;
-        const float gt = __expf(cs - cs_s[c * 32 + 31]);
         float g[32];
+        if (cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f) {
+          // the diagonal chunk with a decay range that keeps exp(cs_t - cs_e) <= e^80; the
+          // pair (r, s) has level bit_length(lane XOR k) <= 5 for column k <= lane: the six
+          // lambdas of the levels inside a 32-token chunk are picked from registers
+          const float gt = row_live ? __expf(cs - cs_s[c * 32 + 31]) : 0.f;
+          const float l0 = lam_r[0], l1 = lam_r[1], l2 = lam_r[2], l3 = lam_r[3],
+                      l4 = lam_r[4], l5 = lam_r[5];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int s = c * 32 + k;
-          float m = 0.f;
-          if (s <= r && row_live)
-            m = lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] *
-                (fact ? gt * fcol[s] : __expf(cs - cs_s[s]));
-          g[k] = m * sa[k] * sp[k];
-          sa[k] *= m;
-          sp[k] *= m;
+          for (int k = 0; k < 32; ++k) {
+            const int x = lane ^ k;
+            const float lv = x >= 16 ? l5 : x >= 8 ? l4 : x >= 4 ? l3 : x >= 2 ? l2 : x >= 1 ? l1 : l0;
+            const float m = k <= lane ? lv * (gt * fcol[c * 32 + k]) : 0.f;
+            g[k] = m * sa[k] * sp[k];
+            sa[k] *= m;
+            sp[k] *= m;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int s = c * 32 + k;
+            float m = 0.f;
+            if (s <= r && row_live)
+              m = lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * __expf(cs - cs_s[s]);
+            g[k] = m * sa[k] * sp[k];
+            sa[k] *= m;
+            sp[k] *= m;
+          }
         }
         warp_column_sums(g);
         atomicAdd(&colsum[c * 32 + lane], g[0]);
