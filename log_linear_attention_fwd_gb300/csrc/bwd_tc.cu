@@ -619,7 +619,6 @@ struct BkvParams {
                              // atomics by the hg heads that share it (zeroed before), or null
   const void* dk;            // non-null: dK in bf16 through the dK map (one q/k per head)
   float* dck;                // [B, T, H] k . dK, or null
-  int ahead;  // tiles between this one and the next on the same SM
 };
 
 struct KvSmem {
@@ -690,13 +689,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   uint8_t* Kb = smem + KvSmem::kK;
   uint8_t* Vb = smem + KvSmem::kV;
   uint8_t* Gb = smem + KvSmem::kG;
-  uint8_t* P1 = smem + KvSmem::kP1;
-  uint8_t* P0 = smem + KvSmem::kP0;
+  uint8_t* P1 = smem + KvSmem::kP1;  // P', then R_tot, then the bf16 dK tile
+  uint8_t* P0 = smem + KvSmem::kP0;  // P, then the bf16 dV tile
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + KvSmem::kBars);
-  uint64_t* bar_load = &bars[0];
-  uint64_t* bar_s = &bars[1];
-  uint64_t* bar_kv = &bars[2];
-  uint64_t* bar_inter = &bars[3];
+  uint64_t* bar_qg = &bars[0];       // Q and dO of a tile landed
+  uint64_t* bar_kv_in = &bars[1];    // K and V of a tile landed
+  uint64_t* bar_s = &bars[2];
+  uint64_t* bar_kv = &bars[3];
+  uint64_t* bar_inter = &bars[4];
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + KvSmem::kTslot);
   float* red = reinterpret_cast<float*>(smem + KvSmem::kRed);
   float* lg_s = reinterpret_cast<float*>(smem + KvSmem::kLg);
@@ -713,13 +713,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int qt = warp & 3, hh = warp >> 2;
   const int r = tid & (kTile - 1);
   const int BH = p.B * p.H;
-  const int i = blockIdx.x / BH, bhi = blockIdx.x - i * BH;
-  const int b = bhi / p.H, h = bhi - b * p.H, hq = h / p.hg;
-  const int64_t bh = bhi;
-  const int t0 = i * kTile;
-  const int n = min(kTile, p.T - t0);
-  const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;
-  const bool row_live = r < n;
+  const int64_t tiles = (int64_t)BH * p.N;
+  const int64_t elems = (int64_t)kD * DV;
 
   if (warp == 1) {
     tmem_alloc(tslot, 512);
@@ -730,7 +725,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmG);
-    for (int q = 0; q < 4; ++q) mbar_init(&bars[q], 1);
+    prefetch_tensormap(&tmDK);
+    prefetch_tensormap(&tmDV);
+    for (int q = 0; q < 5; ++q) mbar_init(&bars[q], 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -738,342 +735,398 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
-  bool landed = true;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_load, 2 * kOperand + 2 * kVBytes);
-    tma_load_4d(&tmQ, bar_load, Qb, 0, hq, t0, b);
-    tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, hq, t0, b);
-    tma_load_4d(&tmK, bar_load, Kb, 0, hq, t0, b);
-    tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, hq, t0, b);
+
+  // Thread 0 loads a tile's operands in two halves: Q and dO once dK's and dV's MMAs of the
+  // tile before are done with them, K and V once its inter MMAs are (both ahead of the
+  // epilogue, so the loads overlap it).
+  auto coords = [&](int64_t t, int* b, int* h, int* hq, int* t0) {
+    const int i = (int)(t / BH), bhi = (int)(t - (int64_t)i * BH);
+    *b = bhi / p.H;
+    *h = bhi - *b * p.H;
+    *hq = *h / p.hg;
+    *t0 = i * kTile;
+  };
+  auto load_qg = [&](int64_t t) {
+    int b, h, hq, t0;
+    coords(t, &b, &h, &hq, &t0);
+    mbar_arrive_expect_tx(bar_qg, kOperand + kVBytes);
+    tma_load_4d(&tmQ, bar_qg, Qb, 0, hq, t0, b);
+    tma_load_4d(&tmQ, bar_qg, Qb + kPanel, 64, hq, t0, b);
 #pragma unroll
-    for (int pv = 0; pv < kPanels; ++pv) {
-      tma_load_4d(&tmV, bar_load, Vb + pv * kPanel, 64 * pv, h, t0, b);
-      tma_load_4d(&tmG, bar_load, Gb + pv * kPanel, 64 * pv, h, t0, b);
+    for (int pv = 0; pv < kPanels; ++pv) tma_load_4d(&tmG, bar_qg, Gb + pv * kPanel, 64 * pv, h, t0, b);
+  };
+  auto load_kv = [&](int64_t t) {
+    int b, h, hq, t0;
+    coords(t, &b, &h, &hq, &t0);
+    mbar_arrive_expect_tx(bar_kv_in, kOperand + kVBytes);
+    tma_load_4d(&tmK, bar_kv_in, Kb, 0, hq, t0, b);
+    tma_load_4d(&tmK, bar_kv_in, Kb + kPanel, 64, hq, t0, b);
+#pragma unroll
+    for (int pv = 0; pv < kPanels; ++pv) tma_load_4d(&tmV, bar_kv_in, Vb + pv * kPanel, 64 * pv, h, t0, b);
+  };
+  int64_t tile = blockIdx.x;
+  // thread 0: loads issued and not yet waited for (bit 0: Q and dO, bit 1: K and V), and
+  // whether a TMA store may still be reading P0 / P1
+  uint32_t in_flight = 0, flight_ph = 0;  // flight_ph: the phase those loads complete
+  bool store_pending = false;
+  if (tid == 0 && tile < tiles) {
+    load_qg(tile);
+    load_kv(tile);
+    in_flight = 3;
+  }
+  uint32_t ph = 0;        // phase of every per-tile barrier: one completion per tile
+  uint32_t ph_inter = 0;  // bar_inter completes only for tiles with levels
+  bool all_ok = true;
+  for (; tile < tiles && all_ok; tile += gridDim.x, ph ^= 1) {
+    const int64_t next = tile + gridDim.x;
+    const int i = (int)(tile / BH), bhi = (int)(tile - (int64_t)i * BH);
+    const int b = bhi / p.H, h = bhi - b * p.H, hq = h / p.hg;
+    const int64_t bh = bhi;
+    const int t0 = i * kTile;
+    const int n = min(kTile, p.T - t0);
+    const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;
+    const bool row_live = r < n;
+
+    // ---- the tile's levels and their weights (while its operands land)
+    if (tid < kTile) colsum[tid] = 0.f;
+    if (warp == 2) {  // the tile's levels: blocks of later tiles, with exp(E_m)
+      int nl = 0;
+      int64_t cmax = i + 1;
+      for (int m = 1; (int64_t(1) << (m - 1)) < p.N; ++m) {
+        if ((i >> (m - 1)) & 1) continue;
+        const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
+        if (c1 >= p.N) continue;
+        if (lane == 0) lv_c[nl] = (int)c1;
+        cmax = c1;  // c1 grows with m
+        ++nl;
+      }
+      __syncwarp();
+      // E_m = the log decays of tiles [i+1, c1_m): running prefix sums over 32 tiles a step,
+      // read off at c1_m - 1 (one pass for all levels)
+      int k = 0;
+      for (; k < nl && lv_c[k] == i + 1; ++k)
+        if (lane == 0) lv_w[k] = 1.f;
+      float run = 0.f;
+      for (int64_t base = i + 1; base < cmax; base += 32) {
+        float x = base + lane < cmax ? p.lgu[bh * p.N + base + lane] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        for (; k < nl && lv_c[k] - 1 < base + 32; ++k) {
+          const float E = run + __shfl_sync(0xffffffffu, x, (int)(lv_c[k] - 1 - base));
+          if (lane == 0) lv_w[k] = __expf(E);
+        }
+        run += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) *lv_n = nl;
     }
-    TileAt nx;  // warm L2 with the next tile's operands
-    if (next_tile(p.ahead, p.B, p.T, p.H, p.hg, &nx)) {
-      tma_prefetch_4d(&tmQ, 0, nx.hq, nx.t0, nx.b);
-      tma_prefetch_4d(&tmQ, 64, nx.hq, nx.t0, nx.b);
-      tma_prefetch_4d(&tmK, 0, nx.hq, nx.t0, nx.b);
-      tma_prefetch_4d(&tmK, 64, nx.hq, nx.t0, nx.b);
+    __syncthreads();
+    const int nl = *lv_n;
+    if (tid >= 32 && tid < 32 + nl)  // warm L2 with the mirrored states summed below
+      prefetch_l2_bulk(p.R + (bh * p.N + lv_c[tid - 32]) * elems, (uint32_t)(elems * 4));
+    const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
+    float lam_in[kIntra / 2];
 #pragma unroll
-      for (int pv = 0; pv < kPanels; ++pv) {
-        tma_prefetch_4d(&tmV, 64 * pv, nx.h, nx.t0, nx.b);
-        tma_prefetch_4d(&tmG, 64 * pv, nx.h, nx.t0, nx.b);
+    for (int q = 0; q < kIntra / 2; ++q) {
+      const int l = hh * (kIntra / 2) + q;
+      lam_in[q] = (row_live && l < p.L) ? p.lam[row * p.L + l] : 0.f;
+    }
+    bool landed = true;
+    if (tid == 0) {  // S = Q K^T, S' = dO V^T
+      landed = mbar_wait(bar_qg, ph);
+      if (landed) in_flight &= ~1u;
+      landed = landed && mbar_wait(bar_kv_in, ph);
+      if (landed) in_flight &= ~2u;
+      if (landed) {
+        tc_fence_after();
+        constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+        const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb), ga = smem_u32(Gb), va = smem_u32(Vb);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+          mma_bf16(tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                   idesc, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+          mma_bf16(tmem + 128, smem_desc_sw128(ga + off, 16, 1024),
+                   smem_desc_sw128(va + off, 16, 1024), idesc, kk > 0);
+        }
+        mma_commit(bar_s);
+      }
+      // the previous tile's dK and dV stores read P0 and P1, which P and P' overwrite below
+      if (store_pending) tma_store_wait_read();
+      store_pending = false;
+    }
+    const float cs_scan = block_scan256(la, red);
+    if (hh == 0) cs_s[r] = cs_scan;
+    if (tid == kTile - 1) lg_s[0] = cs_scan;
+#pragma unroll
+    for (int q = 0; q < kIntra / 2; ++q) lam_s[r * kLamStride + hh * (kIntra / 2) + q] = lam_in[q];
+    __syncthreads();
+    const float cs = cs_s[r];
+    const float lg = lg_s[0];
+    if (hh == 1) fcol[r] = __expf(cs_s[r | 31] - cs);
+
+    all_ok = __syncthreads_and(landed);
+    bool ok = all_ok && mbar_wait(bar_s, ph);
+    tc_fence_after();
+    all_ok = __syncthreads_and(ok);
+
+    // ---- P (into P0) and P' (into P1) for row r's chunks, the column sums of G; and the
+    // rows of K and V scaled by g_r = exp(lg - cs_r) for the inter-tile MMAs (S and S' are
+    // done with K and V)
+    if (all_ok) {
+      const float* lam_r = lam_s + r * kLamStride;
+      for (int c = hh; c < kTile / 32; c += 2) {
+        if (c > qt) {
+          put_row32_zero(P0, r, c);
+          put_row32_zero(P1, r, c);
+          continue;
+        }
+        float sa[32], sp[32];
+        tmem_ld32(tmem + lane_base + c * 32, sa);
+        tmem_ld32(tmem + lane_base + 128 + c * 32, sp);
+        if (c < qt) {
+          const int lvl = 5 + (32 - __clz((unsigned)(qt ^ c)));
+          const float wl = lam_r[lvl] * __expf(cs - cs_s[c * 32 + 31]);
+          float g[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float m = wl * fcol[c * 32 + k];
+            g[k] = m * sa[k] * sp[k];
+            sa[k] *= m;
+            sp[k] *= m;
+          }
+          warp_column_sums(g);
+          atomicAdd(&colsum[c * 32 + lane], g[0]);
+        } else {
+          float g[32];
+          if (cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f) {
+            // the diagonal chunk with a decay range that keeps exp(cs_t - cs_e) <= e^80; the
+            // pair (r, s) has level bit_length(lane XOR k) <= 5 for column k <= lane: the six
+            // lambdas of the levels inside a 32-token chunk are picked from registers
+            const float gt = row_live ? __expf(cs - cs_s[c * 32 + 31]) : 0.f;
+            const float l0 = lam_r[0], l1 = lam_r[1], l2 = lam_r[2], l3 = lam_r[3],
+                        l4 = lam_r[4], l5 = lam_r[5];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int x = lane ^ k;
+              const float lv = x >= 16 ? l5 : x >= 8 ? l4 : x >= 4 ? l3 : x >= 2 ? l2 : x >= 1 ? l1 : l0;
+              const float m = k <= lane ? lv * (gt * fcol[c * 32 + k]) : 0.f;
+              g[k] = m * sa[k] * sp[k];
+              sa[k] *= m;
+              sp[k] *= m;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int s = c * 32 + k;
+              float m = 0.f;
+              if (s <= r && row_live)
+                m = lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * __expf(cs - cs_s[s]);
+              g[k] = m * sa[k] * sp[k];
+              sa[k] *= m;
+              sp[k] *= m;
+            }
+          }
+          warp_column_sums(g);
+          atomicAdd(&colsum[c * 32 + lane], g[0]);
+        }
+        put_row32_bf16(P0, r, c, sa);
+        put_row32_bf16(P1, r, c, sp);
+      }
+      if (nl > 0) {  // g_r = exp(lg - cs_r): decay from row r to the tile's end
+        const float g = row_live ? __expf(lg - cs) : 0.f;
+        scale_row_chunks(Kb, r, 8 * hh, 8, g);
+        scale_row_chunks(Vb, r, (DV / 16) * hh, DV / 16, g);
       }
     }
-  }
-  __syncwarp();
-  // while the tiles load: the tile's levels and their weights
-  if (tid < kTile) colsum[tid] = 0.f;
-  if (warp == 2) {  // the tile's levels: blocks of later tiles, with exp(E_m)
-    int nl = 0;
-    int64_t cmax = i + 1;
-    for (int m = 1; (int64_t(1) << (m - 1)) < p.N; ++m) {
-      if ((i >> (m - 1)) & 1) continue;
-      const int64_t c1 = (((int64_t)i >> (m - 1)) | 1) << (m - 1);
-      if (c1 >= p.N) continue;
-      if (lane == 0) lv_c[nl] = (int)c1;
-      cmax = c1;  // c1 grows with m
-      ++nl;
+    tc_fence_after();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    all_ok = __syncthreads_and(all_ok);
+    // ---- dK = P'^T Q into TMEM 256..383, dV = P^T dO into 384..384+DV (A MN-major)
+    if (all_ok && tid == 0) {
+      tc_fence_after();
+      constexpr uint32_t idk = idesc_bf16(128, 128, 1, 1);
+      constexpr uint32_t idv = idesc_bf16(128, DV, 1, 1);
+      const uint32_t p1 = smem_u32(P1), p0 = smem_u32(P0), qa = smem_u32(Qb), ga = smem_u32(Gb);
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        mma_bf16(tmem + 256, smem_desc_sw128(p1 + kk * 2048, kPanel, 1024),
+                 smem_desc_sw128(qa + kk * 2048, kPanel, 1024), idk, kk > 0);
+        mma_bf16(tmem + 384, smem_desc_sw128(p0 + kk * 2048, kPanel, 1024),
+                 smem_desc_sw128(ga + kk * 2048, kPanel, 1024), idv, kk > 0);
+      }
+      mma_commit(bar_kv);
     }
     __syncwarp();
-    // E_m = the log decays of tiles [i+1, c1_m): running prefix sums over 32 tiles a step,
-    // read off at c1_m - 1 (one pass for all levels)
-    int k = 0;
-    for (; k < nl && lv_c[k] == i + 1; ++k)
-      if (lane == 0) lv_w[k] = 1.f;
-    float run = 0.f;
-    for (int64_t base = i + 1; base < cmax; base += 32) {
-      float x = base + lane < cmax ? p.lgu[bh * p.N + base + lane] : 0.f;
+    // ---- R_tot summed over the levels while the MMAs run (fp32 loads, a warp reads whole
+    // rows: lane owns 4 consecutive columns, warp w rows w, w+8, ...), then written in bf16
+    // over P' once dK's MMA is done with it
+    constexpr int kLanesPerRow = DV / 4;             // 32 or 16
+    constexpr int kRowsPerIter = 32 / kLanesPerRow;  // 1 or 2
+    constexpr int kIters = kTile / 8 / kRowsPerIter; // 16 or 8
+    const int lrow = lane / kLanesPerRow, col = 4 * (lane % kLanesPerRow);
+    float4 rt[kIters];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      for (; k < nl && lv_c[k] - 1 < base + 32; ++k) {
-        const float E = run + __shfl_sync(0xffffffffu, x, (int)(lv_c[k] - 1 - base));
-        if (lane == 0) lv_w[k] = __expf(E);
-      }
-      run += __shfl_sync(0xffffffffu, x, 31);
-    }
-    if (lane == 0) *lv_n = nl;
-  }
-  __syncthreads();
-  const int nl = *lv_n;
-  const int64_t elems = (int64_t)kD * DV;
-  if (tid >= 32 && tid < 32 + nl)  // warm L2 with the mirrored states summed below
-    prefetch_l2_bulk(p.R + (bh * p.N + lv_c[tid - 32]) * elems, (uint32_t)(elems * 4));
-  const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
-  float lam_in[kIntra / 2];
-#pragma unroll
-  for (int q = 0; q < kIntra / 2; ++q) {
-    const int l = hh * (kIntra / 2) + q;
-    lam_in[q] = (row_live && l < p.L) ? p.lam[row * p.L + l] : 0.f;
-  }
-  if (tid == 0) {  // S = Q K^T, S' = dO V^T
-    landed = mbar_wait(bar_load, 0);
-    if (landed) {
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
-      const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb), ga = smem_u32(Gb), va = smem_u32(Vb);
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-        mma_bf16(tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                 idesc, kk > 0);
-      }
-#pragma unroll
-      for (int kk = 0; kk < DV / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-        mma_bf16(tmem + 128, smem_desc_sw128(ga + off, 16, 1024),
-                 smem_desc_sw128(va + off, 16, 1024), idesc, kk > 0);
-      }
-      mma_commit(bar_s);
-    }
-  }
-  const float cs_scan = block_scan256(la, red);
-  if (hh == 0) cs_s[r] = cs_scan;
-  if (tid == kTile - 1) lg_s[0] = cs_scan;
-#pragma unroll
-  for (int q = 0; q < kIntra / 2; ++q) lam_s[r * kLamStride + hh * (kIntra / 2) + q] = lam_in[q];
-  __syncthreads();
-  const float cs = cs_s[r];
-  const float lg = lg_s[0];
-  if (hh == 1) fcol[r] = __expf(cs_s[r | 31] - cs);
-
-  bool all_ok = __syncthreads_and(landed);
-  bool ok = all_ok && mbar_wait(bar_s, 0);
-  tc_fence_after();
-  all_ok = __syncthreads_and(ok);
-
-  // ---- P (into P0) and P' (into P1) for row r's chunks, the column sums of G; and the
-  // rows of K and V scaled by g_r = exp(lg - cs_r) for the inter-tile MMAs (S and S' are
-  // done with K and V)
-  if (all_ok) {
-    const float* lam_r = lam_s + r * kLamStride;
-    for (int c = hh; c < kTile / 32; c += 2) {
-      if (c > qt) {
-        put_row32_zero(P0, r, c);
-        put_row32_zero(P1, r, c);
-        continue;
-      }
-      float sa[32], sp[32];
-      tmem_ld32(tmem + lane_base + c * 32, sa);
-      tmem_ld32(tmem + lane_base + 128 + c * 32, sp);
-      if (c < qt) {
-        const int lvl = 5 + (32 - __clz((unsigned)(qt ^ c)));
-        const float wl = lam_r[lvl] * __expf(cs - cs_s[c * 32 + 31]);
-        float g[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float m = wl * fcol[c * 32 + k];
-          g[k] = m * sa[k] * sp[k];
-          sa[k] *= m;
-          sp[k] *= m;
-        }
-        warp_column_sums(g);
-        atomicAdd(&colsum[c * 32 + lane], g[0]);
-      } else {
-        float g[32];
-        if (cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f) {
-          // the diagonal chunk with a decay range that keeps exp(cs_t - cs_e) <= e^80; the
-          // pair (r, s) has level bit_length(lane XOR k) <= 5 for column k <= lane: the six
-          // lambdas of the levels inside a 32-token chunk are picked from registers
-          const float gt = row_live ? __expf(cs - cs_s[c * 32 + 31]) : 0.f;
-          const float l0 = lam_r[0], l1 = lam_r[1], l2 = lam_r[2], l3 = lam_r[3],
-                      l4 = lam_r[4], l5 = lam_r[5];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int x = lane ^ k;
-            const float lv = x >= 16 ? l5 : x >= 8 ? l4 : x >= 4 ? l3 : x >= 2 ? l2 : x >= 1 ? l1 : l0;
-            const float m = k <= lane ? lv * (gt * fcol[c * 32 + k]) : 0.f;
-            g[k] = m * sa[k] * sp[k];
-            sa[k] *= m;
-            sp[k] *= m;
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int s = c * 32 + k;
-            float m = 0.f;
-            if (s <= r && row_live)
-              m = lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * __expf(cs - cs_s[s]);
-            g[k] = m * sa[k] * sp[k];
-            sa[k] *= m;
-            sp[k] *= m;
-          }
-        }
-        warp_column_sums(g);
-        atomicAdd(&colsum[c * 32 + lane], g[0]);
-      }
-      put_row32_bf16(P0, r, c, sa);
-      put_row32_bf16(P1, r, c, sp);
-    }
-    if (nl > 0) {  // g_r = exp(lg - cs_r): decay from row r to the tile's end
-      const float g = row_live ? __expf(lg - cs) : 0.f;
-      scale_row_chunks(Kb, r, 8 * hh, 8, g);
-      scale_row_chunks(Vb, r, (DV / 16) * hh, DV / 16, g);
-    }
-  }
-  tc_fence_after();
-  fence_proxy_async_smem();
-  tc_fence_before();
-  all_ok = __syncthreads_and(all_ok);
-  // ---- dK = P'^T Q into TMEM 256..383, dV = P^T dO into 384..384+DV (A MN-major)
-  if (all_ok && tid == 0) {
-    tc_fence_after();
-    constexpr uint32_t idk = idesc_bf16(128, 128, 1, 1);
-    constexpr uint32_t idv = idesc_bf16(128, DV, 1, 1);
-    const uint32_t p1 = smem_u32(P1), p0 = smem_u32(P0), qa = smem_u32(Qb), ga = smem_u32(Gb);
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk) {
-      mma_bf16(tmem + 256, smem_desc_sw128(p1 + kk * 2048, kPanel, 1024),
-               smem_desc_sw128(qa + kk * 2048, kPanel, 1024), idk, kk > 0);
-      mma_bf16(tmem + 384, smem_desc_sw128(p0 + kk * 2048, kPanel, 1024),
-               smem_desc_sw128(ga + kk * 2048, kPanel, 1024), idv, kk > 0);
-    }
-    mma_commit(bar_kv);
-  }
-  __syncwarp();
-  // ---- R_tot summed over the levels while the MMAs run (fp32 loads, a warp reads whole
-  // rows: lane owns 4 consecutive columns, warp w rows w, w+8, ...), then written in bf16
-  // over P' once dK's MMA is done with it
-  constexpr int kLanesPerRow = DV / 4;             // 32 or 16
-  constexpr int kRowsPerIter = 32 / kLanesPerRow;  // 1 or 2
-  constexpr int kIters = kTile / 8 / kRowsPerIter; // 16 or 8
-  const int lrow = lane / kLanesPerRow, col = 4 * (lane % kLanesPerRow);
-  float4 rt[kIters];
-#pragma unroll
-  for (int it = 0; it < kIters; ++it) rt[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (all_ok) {
+    for (int it = 0; it < kIters; ++it) rt[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (all_ok) {
 #pragma unroll 2
-    for (int l = 0; l < nl; ++l) {
-      const float w = lv_w[l];
-      const float* src = p.R + (bh * p.N + (int64_t)lv_c[l]) * elems + col;
+      for (int l = 0; l < nl; ++l) {
+        const float w = lv_w[l];
+        const float* src = p.R + (bh * p.N + (int64_t)lv_c[l]) * elems + col;
+#pragma unroll
+        for (int it = 0; it < kIters; ++it) {
+          const int d = (it * kRowsPerIter + lrow) * 8 + warp;
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)d * DV));
+          rt[it].x = fmaf(w, x.x, rt[it].x);
+          rt[it].y = fmaf(w, x.y, rt[it].y);
+          rt[it].z = fmaf(w, x.z, rt[it].z);
+          rt[it].w = fmaf(w, x.w, rt[it].w);
+        }
+      }
+    }
+    ok = all_ok && mbar_wait(bar_kv, ph);
+    tc_fence_after();
+    all_ok = __syncthreads_and(ok);
+    // Q and dO are free (the MMAs above were their last readers): the next tile's load now
+    if (all_ok && tid == 0 && next < tiles) {
+      load_qg(next);
+      in_flight |= 1u;
+      flight_ph = ph ^ 1;
+    }
+    if (all_ok && nl > 0) {
 #pragma unroll
       for (int it = 0; it < kIters; ++it) {
         const int d = (it * kRowsPerIter + lrow) * 8 + warp;
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)d * DV));
-        rt[it].x = fmaf(w, x.x, rt[it].x);
-        rt[it].y = fmaf(w, x.y, rt[it].y);
-        rt[it].z = fmaf(w, x.z, rt[it].z);
-        rt[it].w = fmaf(w, x.w, rt[it].w);
+        uint8_t* dst = P1 + (col >> 6) * kPanel + sw128_offset(d, (col & 63) >> 3) + (col & 7) * 2;
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(pack_bf16(rt[it].x, rt[it].y), pack_bf16(rt[it].z, rt[it].w));
       }
     }
-  }
-  ok = all_ok && mbar_wait(bar_kv, 0);
-  tc_fence_after();
-  all_ok = __syncthreads_and(ok);
-  if (all_ok && nl > 0) {
-#pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-      const int d = (it * kRowsPerIter + lrow) * 8 + warp;
-      uint8_t* dst = P1 + (col >> 6) * kPanel + sw128_offset(d, (col & 63) >> 3) + (col & 7) * 2;
-      *reinterpret_cast<uint2*>(dst) =
-          make_uint2(pack_bf16(rt[it].x, rt[it].y), pack_bf16(rt[it].z, rt[it].w));
-    }
-  }
-  tc_fence_after();
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  // ---- dK += (g V) R_tot^T (B K-major: N = d_k), dV_inter = (g K) R_tot (B MN-major: N = d_v)
-  if (all_ok && nl > 0 && tid == 0) {
     tc_fence_after();
-    constexpr uint32_t idk = idesc_bf16(128, 128, 0, 0);
-    constexpr uint32_t idv = idesc_bf16(128, DV, 0, 1);
-    const uint32_t ra = smem_u32(P1), va = smem_u32(Vb), ka = smem_u32(Kb);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- dK += (g V) R_tot^T (B K-major: N = d_k), dV_inter = (g K) R_tot (B MN-major: N = d_v)
+    if (all_ok && nl > 0 && tid == 0) {
+      tc_fence_after();
+      constexpr uint32_t idk = idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idv = idesc_bf16(128, DV, 0, 1);
+      const uint32_t ra = smem_u32(P1), va = smem_u32(Vb), ka = smem_u32(Kb);
 #pragma unroll
-    for (int kk = 0; kk < DV / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-      mma_bf16(tmem + 256, smem_desc_sw128(va + off, 16, 1024), smem_desc_sw128(ra + off, 16, 1024),
-               idk, 1);
-    }
-#pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-      mma_bf16(tmem, smem_desc_sw128(ka + off, 16, 1024),
-               smem_desc_sw128(ra + kk * 2048, kPanel, 1024), idv, kk > 0);
-    }
-    mma_commit(bar_inter);
-  }
-  __syncwarp();
-  if (nl > 0) {
-    ok = all_ok && mbar_wait(bar_inter, 0);
-    tc_fence_after();
-    all_ok = __syncthreads_and(ok);
-  }
-  // ---- epilogue: dK (bf16, or fp32 per head), dV = intra + inter (bf16), k . dK.  No MMA
-  // reads Q or dO any more: the bf16 dK and dV tiles are staged there and stored by TMA.
-  if (all_ok) {
-    uint4 vrow[kHalf / 8];  // this row's half of v, loaded first so its latency overlaps
-    if (row_live) {
-      const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + row * DV + kHalf * hh);
-#pragma unroll
-      for (int q = 0; q < kHalf / 8; ++q) vrow[q] = vsrc[q];
-    }
-    float vd = 0.f;
-    {
-      float v0[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld32(tmem + lane_base + 256 + 64 * hh + 32 * c, v0);
-        if (p.dk) {
-          put_row32_bf16(Qb, r, 2 * hh + c, v0);
-        } else if (row_live) {  // shared q/k: this head's part of its group's dK
-          float4* dst = reinterpret_cast<float4*>(
-              p.dkh + (((int64_t)b * p.T + t0 + r) * (p.H / p.hg) + hq) * kD + 64 * hh + 32 * c);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            atomicAdd(dst + q, make_float4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]));
-        }
+      for (int kk = 0; kk < DV / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+        mma_bf16(tmem + 256, smem_desc_sw128(va + off, 16, 1024), smem_desc_sw128(ra + off, 16, 1024),
+                 idk, 1);
       }
-    }
 #pragma unroll
-    for (int c = 0; c < kPanels; ++c) {
-      float a[32], x[32];
-      tmem_ld32(tmem + lane_base + 384 + kHalf * hh + 32 * c, a);
-      if (nl > 0) {
-        tmem_ld32(tmem + lane_base + kHalf * hh + 32 * c, x);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 32; ++q) x[q] = 0.f;
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+        mma_bf16(tmem, smem_desc_sw128(ka + off, 16, 1024),
+                 smem_desc_sw128(ra + kk * 2048, kPanel, 1024), idv, kk > 0);
       }
+      mma_commit(bar_inter);
+    }
+    __syncwarp();
+    if (nl > 0) {
+      ok = all_ok && mbar_wait(bar_inter, ph_inter);
+      ph_inter ^= 1;
+      tc_fence_after();
+      all_ok = __syncthreads_and(ok);
+    }
+    // K and V are free (and P1 holds no operand any more): the next tile's K and V now
+    if (all_ok && tid == 0 && next < tiles) {
+      load_kv(next);
+      in_flight |= 2u;
+      flight_ph = ph ^ 1;
+    }
+    // ---- epilogue: dK (bf16, or fp32 per head), dV = intra + inter (bf16), k . dK.  The
+    // bf16 dK and dV tiles are staged in P1 and P0, which no MMA reads any more, and stored
+    // by TMA; the next tile's Q, dO, K and V load meanwhile.
+    if (all_ok) {
+      uint4 vrow[kHalf / 8];  // this row's half of v, loaded first so its latency overlaps
       if (row_live) {
+        const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + row * DV + kHalf * hh);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 w = vrow[4 * c + q];
-          const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+        for (int q = 0; q < kHalf / 8; ++q) vrow[q] = vsrc[q];
+      }
+      float vd = 0.f;
+      {
+        float v0[32];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
-            vd = fmaf(f.x, x[8 * q + 2 * e], vd);
-            vd = fmaf(f.y, x[8 * q + 2 * e + 1], vd);
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(tmem + lane_base + 256 + 64 * hh + 32 * c, v0);
+          if (p.dk) {
+            put_row32_bf16(P1, r, 2 * hh + c, v0);
+          } else if (row_live) {  // shared q/k: this head's part of its group's dK
+            float4* dst = reinterpret_cast<float4*>(
+                p.dkh + (((int64_t)b * p.T + t0 + r) * (p.H / p.hg) + hq) * kD + 64 * hh + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              atomicAdd(dst + q, make_float4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]));
           }
         }
       }
 #pragma unroll
-      for (int q = 0; q < 32; ++q) a[q] += x[q];
-      put_row32_bf16(Gb, r, kPanels * hh + c, a);
-    }
-    vd_s[hh * kTile + r] = vd;
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {  // rows past T are clipped by the maps
-      if (p.dk) {
-        tma_store_4d(&tmDK, Qb, 0, h, t0, b);
-        tma_store_4d(&tmDK, Qb + kPanel, 64, h, t0, b);
-      }
+      for (int c = 0; c < kPanels; ++c) {
+        float a[32], x[32];
+        tmem_ld32(tmem + lane_base + 384 + kHalf * hh + 32 * c, a);
+        if (nl > 0) {
+          tmem_ld32(tmem + lane_base + kHalf * hh + 32 * c, x);
+        } else {
 #pragma unroll
-      for (int pv = 0; pv < kPanels; ++pv) tma_store_4d(&tmDV, Gb + pv * kPanel, 64 * pv, h, t0, b);
-      tma_store_commit();
+          for (int q = 0; q < 32; ++q) x[q] = 0.f;
+        }
+        if (row_live) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = vrow[4 * c + q];
+            const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+              vd = fmaf(f.x, x[8 * q + 2 * e], vd);
+              vd = fmaf(f.y, x[8 * q + 2 * e + 1], vd);
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 32; ++q) a[q] += x[q];
+        put_row32_bf16(P0, r, kPanels * hh + c, a);
+      }
+      vd_s[hh * kTile + r] = vd;
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {  // rows past T are clipped by the maps
+        if (p.dk) {
+          tma_store_4d(&tmDK, P1, 0, h, t0, b);
+          tma_store_4d(&tmDK, P1 + kPanel, 64, h, t0, b);
+        }
+#pragma unroll
+        for (int pv = 0; pv < kPanels; ++pv) tma_store_4d(&tmDV, P0 + pv * kPanel, 64 * pv, h, t0, b);
+        tma_store_commit();
+        store_pending = true;
+      }
+      if (hh == 0 && row_live && p.dck)
+        p.dck[row] = colsum[r] + vd_s[r] + vd_s[kTile + r];
+    } else if (tid == 0) {
+      atomicOr(&g_tcb_error, 1u);
     }
-    if (hh == 0 && row_live && p.dck)
-      p.dck[row] = colsum[r] + vd_s[r] + vd_s[kTile + r];
-    if (tid == 0) tma_store_wait_read();  // the stage must outlive the stores' reads
-  } else if (tid == 0) {
-    atomicOr(&g_tcb_error, 1u);
+    tc_fence_before();
+    __syncthreads();  // TMEM, colsum and vd_s are read: the next tile may overwrite them
+  }
+  if (tid == 0) {
+    // the stores must finish reading shared memory, and after an error the loads still in
+    // flight into it must land (bounded waits), before it is handed to another CTA
+    if (store_pending) tma_store_wait_read();
+    if (in_flight & 1u) mbar_wait(bar_qg, flight_ph);
+    if (in_flight & 2u) mbar_wait(bar_kv_in, flight_ph);
   }
   tc_fence_before();
   __syncthreads();
@@ -1417,7 +1470,6 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
   p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.R = R;
   p.v = static_cast<const __nv_bfloat16*>(f.v);
   p.dkh = dkh; p.dk = dk_bf16; p.dck = dck;
-  p.ahead = sm_count();
   // The shared-memory limit is an attribute of the function on each device: set it
   // on every launch (a host-side call), so that every device the library runs on has it.
   const cudaError_t attr_err =
@@ -1426,13 +1478,16 @@ cudaError_t launch_tc_bwd_dkv(const FwdArgs& f, const void* dout, const float* R
                 : cudaFuncSetAttribute(tc_bwd_dkv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem_bwd_dkv());
   if (attr_err != cudaSuccess) return attr_err;
-  const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
+  // one persistent CTA per SM, taking tiles SM-count apart
+  const int64_t tiles = (int64_t)f.B * f.H * f.N;
+  const int sms = sm_count();
+  const unsigned grid = (unsigned)(sms > 0 && sms < tiles ? sms : tiles);
   if (dvw == 128)
-    tc_bwd_dkv_kernel<128><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, tmDK,
-                                                                    tmDV, p);
-  else
-    tc_bwd_dkv_kernel<64><<<tiles, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, tmDK,
+    tc_bwd_dkv_kernel<128><<<grid, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, tmDK,
                                                                    tmDV, p);
+  else
+    tc_bwd_dkv_kernel<64><<<grid, kThreadsB, smem_bwd_dkv(), s>>>(tmQ, tmK, tmV, tmG, tmDK,
+                                                                  tmDV, p);
   return cudaGetLastError();
 }
 
