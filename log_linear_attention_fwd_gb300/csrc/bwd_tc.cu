@@ -605,8 +605,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // summed over the tile's levels into R_tot = sum_m exp(E_m) R_{c_m} (E_m: log decay of the tiles strictly
 // between i and c_m):
 //   dK_s += g_s R_tot v_s,  dV_s += g_s R_tot^T k_s,  g_s = exp(lg_i - cs_s),
-// taken as MMAs with the rows of V and K scaled by g in place.  k_s . dK_s, which d log a
-// needs, is the column sum of G = M ⊙ S ⊙ S' (from the fp32 S and S') plus v_s . dV_inter.
+// taken as MMAs V R_tot^T and K R_tot whose row s the epilogue scales by g_s (in fp32).
+// k_s . dK_s, which d log a needs, is the column sum of G = M ⊙ S ⊙ S' (from the fp32 S
+// and S') plus v_s . dV_inter.
 
 struct BkvParams {
   int B, T, H, hg, L, N;
@@ -641,22 +642,6 @@ struct KvSmem {
 };
 
 size_t smem_bwd_dkv() { return (size_t)KvSmem::kEnd + 1024; }
-
-// Multiplies the 16-byte chunks [g0, g0 + cnt) of row r of a swizzled tile by s (chunk g
-// is columns 8g..8g+7: panel g / 8).
-__device__ __forceinline__ void scale_row_chunks(uint8_t* buf, int r, int g0, int cnt, float sc) {
-  for (int g = g0; g < g0 + cnt; ++g) {
-    uint4* ptr = reinterpret_cast<uint4*>(buf + (g >> 3) * kPanel + sw128_offset(r, g & 7));
-    uint4 u = *ptr;
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[k]));
-      w[k] = pack_bf16(f.x * sc, f.y * sc);
-    }
-    *ptr = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
 
 // Column sums of a 32 x 32 block held one row per lane: a transpose-reduce butterfly
 // (31 shuffles); on return a[0] of lane k is the sum of column k over the warp's rows.
@@ -939,11 +924,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         put_row32_bf16(P0, r, c, sa);
         put_row32_bf16(P1, r, c, sp);
       }
-      if (nl > 0) {  // g_r = exp(lg - cs_r): decay from row r to the tile's end
-        const float g = row_live ? __expf(lg - cs) : 0.f;
-        scale_row_chunks(Kb, r, 8 * hh, 8, g);
-        scale_row_chunks(Vb, r, (DV / 16) * hh, DV / 16, g);
-      }
     }
     tc_fence_after();
     fence_proxy_async_smem();
@@ -1013,7 +993,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // ---- dK += (g V) R_tot^T (B K-major: N = d_k), dV_inter = (g K) R_tot (B MN-major: N = d_v)
+    // ---- dK_inter = V R_tot^T into TMEM 128..255 (B K-major: N = d_k) and dV_inter = K R_tot
+    // into 0..DV (B MN-major: N = d_v), both freed by the P build; the epilogue scales row s
+    // of both by g_s
     if (all_ok && nl > 0 && tid == 0) {
       tc_fence_after();
       constexpr uint32_t idk = idesc_bf16(128, 128, 0, 0);
@@ -1022,8 +1004,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
       for (int kk = 0; kk < DV / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-        mma_bf16(tmem + 256, smem_desc_sw128(va + off, 16, 1024), smem_desc_sw128(ra + off, 16, 1024),
-                 idk, 1);
+        mma_bf16(tmem + 128, smem_desc_sw128(va + off, 16, 1024), smem_desc_sw128(ra + off, 16, 1024),
+                 idk, kk > 0);
       }
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
@@ -1057,11 +1039,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         for (int q = 0; q < kHalf / 8; ++q) vrow[q] = vsrc[q];
       }
       float vd = 0.f;
+      const float g = row_live && nl > 0 ? __expf(lg - cs) : 0.f;  // decay from row r to the end
       {
         float v0[32];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           tmem_ld32(tmem + lane_base + 256 + 64 * hh + 32 * c, v0);
+          if (nl > 0) {
+            float v1[32];
+            tmem_ld32(tmem + lane_base + 128 + 64 * hh + 32 * c, v1);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v0[q] = fmaf(g, v1[q], v0[q]);
+          }
           if (p.dk) {
             put_row32_bf16(P1, r, 2 * hh + c, v0);
           } else if (row_live) {  // shared q/k: this head's part of its group's dK
@@ -1079,6 +1068,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tmem_ld32(tmem + lane_base + 384 + kHalf * hh + 32 * c, a);
         if (nl > 0) {
           tmem_ld32(tmem + lane_base + kHalf * hh + 32 * c, x);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) x[q] *= g;
         } else {
 #pragma unroll
           for (int q = 0; q < 32; ++q) x[q] = 0.f;
