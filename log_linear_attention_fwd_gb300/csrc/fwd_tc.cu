@@ -132,6 +132,9 @@ __device__ __forceinline__ void put_row32_bf16(uint8_t* buf, int r, int c, const
 // itself after a global proxy fence.
 
 constexpr int kThreadsF = 256;
+// Stores an even tile's state and raises its flag: lane 0 of warp 4, whose rows (0..31)
+// have no P chunk above the diagonal to compute, so its wait costs the P build nothing.
+constexpr int kPubThread = 128;
 
 // Inclusive prefix sum over the 256 threads of the CTA; red holds 8 floats and must not
 // be reused before the next __syncthreads.
@@ -388,32 +391,36 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     tmem_ld32(tmem + lane_base + 128 + G::kHalf * hh + 32 * c, v);
     put_row32_bf16(Kb, r, G::kPanels * hh + c, v);
   }
-  __syncthreads();
-  const bool forms = (j & 1) && j + 1 < N;  // odd j forms the block state of slot j+1
   // Only U of even tiles is read by other tiles (slot j+1, odd, is U_j; an even slot's
   // parts are U_{c-2} and U_{c-1}, and U_{c-1} is summed by its own CTA), by the backward
-  // and by the prefill: odd tiles keep theirs on chip.
+  // and by the prefill: odd tiles keep theirs on chip.  Even tiles store the staged tile
+  // with TMA (thread kPubThread), which raises the ready flag once the store is complete:
+  // only that thread's warp waits for the store.
   const bool pub_u = !(j & 1);
-  float acc[8 * kStatePieces];              // that sum, fp32, in this thread's pieces
-#pragma unroll
-  for (int it = 0; it < kStatePieces; ++it) {
-    const int q = it * kThreadsF + tid;
-    const uint4 w = *reinterpret_cast<const uint4*>(Kb + piece_offset<DV>(q));
-    if (pub_u) reinterpret_cast<uint4*>(const_cast<uint8_t*>(Ug) + (int64_t)j * G::kStateBytes)[q] = w;
-    const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
-      acc[8 * it + 2 * e] = f.x;
-      acc[8 * it + 2 * e + 1] = f.y;
-    }
-  }
+  fence_proxy_async_smem();
+  __syncthreads();
   if (tid == 0) p.lgu[bh * N + j] = lg;
-  if (pub_u) {
-    __syncthreads();
-    if (tid == 0) st_release_gpu(&rdy_u[j], decay_flag(lg));
+  if (pub_u && tid == kPubThread) {
+    const int row0 = (int)((bh * N + j) * kD);
+#pragma unroll
+    for (int pv = 0; pv < G::kPanels; ++pv) tma_store_2d(&tmU, Kb + pv * kPanel, 64 * pv, row0);
+    tma_store_commit();
+    tma_store_wait_read();  // Kb is refilled below
   }
+  const bool forms = (j & 1) && j + 1 < N;  // odd j forms the block state of slot j+1
   if (forms) {
+    float acc[8 * kStatePieces];  // the block state of slot j+1, fp32, in this thread's pieces
+#pragma unroll
+    for (int it = 0; it < kStatePieces; ++it) {
+      const uint4 w = *reinterpret_cast<const uint4*>(Kb + piece_offset<DV>(it * kThreadsF + tid));
+      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+        acc[8 * it + 2 * e] = f.x;
+        acc[8 * it + 2 * e + 1] = f.y;
+      }
+    }
     // Slot c = j+1 holds [c - 2^z, c), z = ctz(c): the block states of slots c - 2^(k-1)
     // (k = z..2), then U_{j-1}, then U_j; summed right to left, each weighted by the
     // decay across what lies to its right, in fp32, rounded once to bf16.
@@ -460,6 +467,11 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   }
 
   __syncthreads();  // the staged U in Kb is no longer read
+  if (pub_u && tid == kPubThread) {  // once U_j is in memory, raise its flag
+    tma_store_wait_all();
+    fence_proxy_async_global();
+    st_release_gpu(&rdy_u[j], decay_flag(lg));
+  }
 
   // ---- the levels' block states.  Level k (the k-th set bit of j, from the lowest) is
   // owned by thread 32+k: it finds its slot c, acquires the slot's ready flag (which

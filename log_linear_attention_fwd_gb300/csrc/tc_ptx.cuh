@@ -143,6 +143,11 @@ __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Waits until every committed bulk store is complete (its writes performed).
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Warms L2 with `bytes` (a multiple of 16) of global memory from p (16-byte aligned); no
 // shared memory, no completion signal.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
