@@ -375,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(GdnChunkArg
   float* Qb = Pb + 2 * kD * kLdp;           // [2][kC][kLdp]
   float* Zs = Qb + 2 * kC * kLdp;           // [kD][kCols]: one level's column block
   float* Lb = Zs + kD * kCols;              // [2][kC][kMaxLv]: lambda of the chunk levels
+  float* Zs2 = Lb + 2 * kC * kMaxLv;        // [kD][kCols]: a second level's column block
   const int tid = threadIdx.x;
   const int slices = (a.dv + kCols - 1) / kCols;
   const int64_t bh = blockIdx.x / slices;
@@ -431,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(GdnChunkArg
   float u_next[8];    // U_{j} rows 8 rg.., column col: merged at the start of chunk j+1
   // the copies fill columns [0, dk) of each row; the padding up to a multiple of 4, read
   // by the float4 loop (times zero rows of Z), stays zero
-  for (int i = tid; i < 2 * kD * kLdp + 2 * kC * kLdp + kD * kCols + 2 * kC * kMaxLv; i += kThreads)
+  for (int i = tid; i < 2 * kD * kLdp + 2 * kC * kLdp + 2 * kD * kCols + 2 * kC * kMaxLv; i += kThreads)
     Pb[i] = 0.f;
   __syncthreads();
   issue(0);
@@ -486,39 +487,87 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(GdnChunkArg
     const float* Ps = Pb + (j & 1) * kD * kLdp;
     const float* Qs = Qb + (j & 1) * kC * kLdp;
     const float* Ls = Lb + (j & 1) * kC * kMaxLv;
-    // ---- per live level: readout of four tokens (t = rg + 16 i) and the carry of 8 rows
+    // ---- the live levels two at a time: readout of four tokens (t = rg + 16 i) and the
+    // carry of 8 rows for each, every row of P and Qt read once for both
     float o[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t todo = live & ~1u & (levels < 32 ? (1u << levels) - 1u : ~0u);
+    while (todo) {
+      const int m1 = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int m2 = todo ? __ffs(todo) - 1 : 0;  // 0: m1 is the last one
+      todo &= todo - 1;
 #pragma unroll
-    for (int m = 1; m < kLv; ++m) {
-      if (m >= levels) break;
-      if (!((live >> m) & 1)) continue;
+      for (int m = 1; m < kLv; ++m) {
+        if (m == m1) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) Zs[(8 * rg + i) * kCols + col] = z[m][i];
+          for (int i = 0; i < 8; ++i) Zs[(8 * rg + i) * kCols + col] = z[m][i];
+        }
+        if (m == m2) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) Zs2[(8 * rg + i) * kCols + col] = z[m][i];
+        }
+      }
       __syncthreads();
-      float rd[4] = {0.f, 0.f, 0.f, 0.f};
-      float cr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float rd0[4] = {0.f, 0.f, 0.f, 0.f}, rd1[4] = {0.f, 0.f, 0.f, 0.f};
+      float cr0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float cr1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       // four d at a time: rows of P and Qt as float4 (padded to a multiple of 4 with the
       // zero rows of Z beyond d_k)
-      for (int d = 0; d < dk; d += 4) {
-        float zd[4];
+      if (m2) {
+        for (int d = 0; d < dk; d += 4) {
+          float zd[4], ze[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) zd[e] = Zs[(d + e) * kCols + col];
+          for (int e = 0; e < 4; ++e) {
+            zd[e] = Zs[(d + e) * kCols + col];
+            ze[e] = Zs2[(d + e) * kCols + col];
+          }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 q4 = *reinterpret_cast<const float4*>(Qs + (rg + 16 * i) * kLdp + d);
-          rd[i] = fmaf(q4.x, zd[0], fmaf(q4.y, zd[1], fmaf(q4.z, zd[2], fmaf(q4.w, zd[3], rd[i]))));
+          for (int i = 0; i < 4; ++i) {
+            const float4 q4 = *reinterpret_cast<const float4*>(Qs + (rg + 16 * i) * kLdp + d);
+            rd0[i] = fmaf(q4.x, zd[0], fmaf(q4.y, zd[1], fmaf(q4.z, zd[2], fmaf(q4.w, zd[3], rd0[i]))));
+            rd1[i] = fmaf(q4.x, ze[0], fmaf(q4.y, ze[1], fmaf(q4.z, ze[2], fmaf(q4.w, ze[3], rd1[i]))));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 p4 = *reinterpret_cast<const float4*>(Ps + (8 * rg + i) * kLdp + d);
+            cr0[i] = fmaf(p4.x, zd[0], fmaf(p4.y, zd[1], fmaf(p4.z, zd[2], fmaf(p4.w, zd[3], cr0[i]))));
+            cr1[i] = fmaf(p4.x, ze[0], fmaf(p4.y, ze[1], fmaf(p4.z, ze[2], fmaf(p4.w, ze[3], cr1[i]))));
+          }
         }
+      } else {
+        for (int d = 0; d < dk; d += 4) {
+          float zd[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 p4 = *reinterpret_cast<const float4*>(Ps + (8 * rg + i) * kLdp + d);
-          cr[i] = fmaf(p4.x, zd[0], fmaf(p4.y, zd[1], fmaf(p4.z, zd[2], fmaf(p4.w, zd[3], cr[i]))));
+          for (int e = 0; e < 4; ++e) zd[e] = Zs[(d + e) * kCols + col];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 q4 = *reinterpret_cast<const float4*>(Qs + (rg + 16 * i) * kLdp + d);
+            rd0[i] = fmaf(q4.x, zd[0], fmaf(q4.y, zd[1], fmaf(q4.z, zd[2], fmaf(q4.w, zd[3], rd0[i]))));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 p4 = *reinterpret_cast<const float4*>(Ps + (8 * rg + i) * kLdp + d);
+            cr0[i] = fmaf(p4.x, zd[0], fmaf(p4.y, zd[1], fmaf(p4.z, zd[2], fmaf(p4.w, zd[3], cr0[i]))));
+          }
         }
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = fmaf(Ls[(rg + 16 * i) * kMaxLv + m], rd[i], o[i]);
+      for (int i = 0; i < 4; ++i) {
+        o[i] = fmaf(Ls[(rg + 16 * i) * kMaxLv + m1], rd0[i], o[i]);
+        if (m2) o[i] = fmaf(Ls[(rg + 16 * i) * kMaxLv + m2], rd1[i], o[i]);
+      }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) z[m][i] = 8 * rg + i < dk ? cr[i] : 0.f;
-      __syncthreads();  // Zs is rewritten by the next level
+      for (int m = 1; m < kLv; ++m) {
+        if (m == m1) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) z[m][i] = 8 * rg + i < dk ? cr0[i] : 0.f;
+        }
+        if (m == m2) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) z[m][i] = 8 * rg + i < dk ? cr1[i] : 0.f;
+        }
+      }
+      __syncthreads();  // Zs and Zs2 are rewritten by the next pair
     }
     // ---- the chunk's output rows: O_intra + readout
 #pragma unroll
@@ -612,7 +661,7 @@ cudaError_t launch_gdn_chunked(const void* q, const void* k, const void* v, cons
   while ((1 << (levels - 1)) < a.N) ++levels;
   if (levels > kMaxLv) return cudaErrorInvalidValue;
   const size_t smem2 =
-      sizeof(float) * ((size_t)2 * kD * kLdp + 2 * kC * kLdp + kD * kCols + 2 * kC * kMaxLv);
+      sizeof(float) * ((size_t)2 * kD * kLdp + 2 * kC * kLdp + 2 * kD * kCols + 2 * kC * kMaxLv);
   const unsigned grid2 = (unsigned)((int64_t)B * H * ((dv + kCols - 1) / kCols));
   if (out_dtype == LL_BF16)
     e = levels <= 12 ? launch_scan<__nv_bfloat16, 12>(a, levels, grid2, smem2, s)
