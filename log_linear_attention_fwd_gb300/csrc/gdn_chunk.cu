@@ -663,12 +663,15 @@ cudaError_t launch_gdn_chunked(const void* q, const void* k, const void* v, cons
   const size_t smem2 =
       sizeof(float) * ((size_t)2 * kD * kLdp + 2 * kC * kLdp + 2 * kD * kCols + 2 * kC * kMaxLv);
   const unsigned grid2 = (unsigned)((int64_t)B * H * ((dv + kCols - 1) / kCols));
+  // the chunk-level states live in registers: the smallest instance that holds them
   if (out_dtype == LL_BF16)
-    e = levels <= 12 ? launch_scan<__nv_bfloat16, 12>(a, levels, grid2, smem2, s)
-                     : launch_scan<__nv_bfloat16, kMaxLv>(a, levels, grid2, smem2, s);
+    e = levels <= 10   ? launch_scan<__nv_bfloat16, 10>(a, levels, grid2, smem2, s)
+        : levels <= 12 ? launch_scan<__nv_bfloat16, 12>(a, levels, grid2, smem2, s)
+                       : launch_scan<__nv_bfloat16, kMaxLv>(a, levels, grid2, smem2, s);
   else
-    e = levels <= 12 ? launch_scan<float, 12>(a, levels, grid2, smem2, s)
-                     : launch_scan<float, kMaxLv>(a, levels, grid2, smem2, s);
+    e = levels <= 10   ? launch_scan<float, 10>(a, levels, grid2, smem2, s)
+        : levels <= 12 ? launch_scan<float, 12>(a, levels, grid2, smem2, s)
+                       : launch_scan<float, kMaxLv>(a, levels, grid2, smem2, s);
   if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (!state) return cudaSuccess;
