@@ -1126,81 +1126,118 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 // ------------------------------------------------------------------ mirrored states
 //
-// Tile j adds, for every set bit m-1 of j, its part of the mirrored state of the block
-// starting at c = j with its low m-1 bits cleared (the block that the sources of tiles
-// [c - 2^(m-1), c) meet at level 7+m):
-//   R_c += sum_{t in j} w_t q_t dO_t^T,  w_t = exp(cs_t + D) lambda[t, 7+m],
-// D = log decay of the tiles [c, j).  Per level the rows of Q are scaled by w and split
-// into a bf16 high part and a bf16 residual (w q to about 16 bits; dO is exact in bf16),
-// and (w Q)^T dO = hi^T dO + lo^T dO (A and B MN-major) goes into one of two TMEM buffers;
-// the previous level's product is added to R_c (fp32, float4 atomics; a level-1 block is
-// the tile itself, so it is stored) meanwhile.  The
-// states feed k . dK, and with it d log a, a sum whose terms cancel, which is why w q is
-// not rounded to bf16 alone.
+// The sources of tiles [c - 2^z, c) (z = ctz(c)) meet the queries of tiles [c, c + 2^z)
+// at chunk level m = z + 1 (Fenwick level 7 + m).  Their mirrored state is
+//   R_c = sum_{j in [c, c + 2^z)} sum_{t in j} w_t q_t dO_t^T,
+//   w_t = exp(cs_t + D_j) lambda[t, 7+m],  D_j = log decay of the tiles [c, j).
+// One CTA takes one slot c and a run of at most 2^kRunLog of its reader tiles and sums
+// the run's products in one TMEM accumulator: per reader tile, Q and dO by TMA, the rows
+// of Q scaled by w in place and split into a bf16 high part and a bf16 residual (w q to
+// about 16 bits; dO is exact in bf16), and (w Q)^T dO = hi^T dO + lo^T dO (A and B
+// MN-major).  The states feed k . dK, and with it d log a, a sum whose terms cancel,
+// which is why w q is not rounded to bf16 alone.  The accumulator is staged in shared
+// memory and goes to R_c with coalesced stores when the run is the slot's only one
+// (z <= kRunLog), else with float4 atomics into the slot, zeroed before.  Two CTAs fit
+// per SM, so one run's loads overlap the other's products.
+//
+// Runs: those of level z cover the reader tiles j with bit z set, in aligned runs of
+// g = 2^min(z, kRunLog) tiles.  Their starts are s = q g for the q in [0, ceil(N / g))
+// whose bit z - log2(g) is set.  The grid takes the runs level by level from the highest
+// (the longest runs first), the (b, h) innermost.
+
+constexpr int kRunLog = 3;
+
+// How many q in [0, M) have bit b set.
+__host__ __device__ inline int64_t count_with_bit(int64_t M, int b) {
+  const int64_t full = (M >> (b + 1)) << b;
+  const int64_t rem = (M & ((int64_t(2) << b) - 1)) - (int64_t(1) << b);
+  return full + (rem > 0 ? rem : 0);
+}
+
+// Runs of level z for N tiles.
+__host__ __device__ inline int64_t runs_at_level(int64_t N, int z) {
+  const int lg = z < kRunLog ? z : kRunLog;
+  return count_with_bit((N + (int64_t(1) << lg) - 1) >> lg, z - lg);
+}
 
 struct BrParams {
   int B, T, H, hg, L, N;
+  int levels;          // chunk levels holding slots: the bit length of N - 1
   const float* log_a;
   const float* lam;
-  const float* lgu;   // [B*H][N] the tiles' log decays (forward workspace)
-  float* R;           // [B*H][N][d_k][d_v] mirrored states (even slots zeroed before)
-  int ahead;  // tiles between this one and the next on the same SM
+  const float* lgu;    // [B*H][N] the tiles' log decays (forward workspace)
+  float* R;            // [B*H][N][d_k][d_v] mirrored states (slots with z > kRunLog zeroed before)
 };
 
 struct RsSmem {
-  static constexpr int kQ = 0, kG = kOperand, kW = 2 * kOperand;  // W: [2 levels][hi, lo]
-  static constexpr int kBars = 6 * kOperand;  // load, r[2]
-  static constexpr int kTslot = kBars + 4 * 8;
-  static constexpr int kRed = kTslot + 16;
-  static constexpr int kCs = kRed + 32;                        // 128 floats
-  static constexpr int kD = kCs + 4 * kTile;                   // kMaxChunkLevels floats
-  static constexpr int kLamX = kD + 4 * kMaxChunkLevels;       // [levels][128] floats
+  // Q (then its scaled high part), the residual, dO; the accumulator is staged over Q and
+  // the residual at the end
+  static constexpr int kQ = 0, kLo = kOperand, kG = 2 * kOperand;
+  static constexpr int kBars = 3 * kOperand;  // load, mma
+  static constexpr int kTslot = kBars + 2 * 8;
+  static constexpr int kRed = kTslot + 16;    // 8 floats
+  static constexpr int kD0 = kRed + 32;       // 4 floats
+  static constexpr int kCs = kD0 + 16;        // 128 floats
+  static constexpr int kEnd = kCs + 4 * kTile;
 };
 
-size_t smem_bwd_rstate(int levels) { return (size_t)RsSmem::kLamX + 4 * (size_t)kTile * levels + 1024; }
+size_t smem_bwd_rstate() { return (size_t)RsSmem::kEnd + 1024; }
 
 template <int DV>
-__global__ void __launch_bounds__(kThreadsB, 1)
+__global__ void __launch_bounds__(kThreadsB, 2)
     tc_bwd_rstate_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmG, BrParams p) {
   constexpr int kPanels = DV / 64;
   constexpr int kVBytes = kTile * DV * 2;
   constexpr int kHalf = DV / 2;
   const int BH = p.B * p.H;
-  const int j = blockIdx.x / BH, bhi = blockIdx.x - j * BH;
-  const int nlev = __popc((unsigned)j);
-  if (nlev == 0) return;  // tile 0 of each (b, h) belongs to no mirrored block
+
+  // ---- the run
+  int64_t e = (int64_t)blockIdx.x / BH;
+  const int bhi = (int)((int64_t)blockIdx.x - e * BH);
+  int z = p.levels - 1;
+  for (; z > 0; --z) {
+    const int64_t cnt = runs_at_level(p.N, z);
+    if (e < cnt) break;
+    e -= cnt;
+  }
+  const int lgr = z < kRunLog ? z : kRunLog;
+  const int bq = z - lgr;
+  const int64_t q = ((e >> bq) << (bq + 1)) | (int64_t(1) << bq) | (e & ((int64_t(1) << bq) - 1));
+  const int s0 = (int)(q << lgr);               // the run's first reader tile
+  const int c = (s0 >> z) << z;                 // its slot
+  const int s1 = min(s0 + (1 << lgr), p.N);     // one past its last reader tile
+  const bool whole = z <= kRunLog;              // the run is the slot's only one
+  const int lam_l = kTileLc + z + 1;            // the Fenwick level of the run's pairs
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* Qb = smem + RsSmem::kQ;
+  uint8_t* Lb = smem + RsSmem::kLo;
   uint8_t* Gb = smem + RsSmem::kG;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RsSmem::kBars);
   uint64_t* bar_load = &bars[0];
-  uint64_t* bar_r = &bars[1];  // [2]
+  uint64_t* bar_mma = &bars[1];
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + RsSmem::kTslot);
   float* red = reinterpret_cast<float*>(smem + RsSmem::kRed);
+  float* d0_s = reinterpret_cast<float*>(smem + RsSmem::kD0);
   float* cs_s = reinterpret_cast<float*>(smem + RsSmem::kCs);
-  float* D_s = reinterpret_cast<float*>(smem + RsSmem::kD);
-  float* lamx = reinterpret_cast<float*>(smem + RsSmem::kLamX);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qt = warp & 3, hh = warp >> 2;
   const int r = tid & (kTile - 1);
   const int b = bhi / p.H, h = bhi - b * p.H, hq = h / p.hg;
   const int64_t bh = bhi;
-  const int t0 = j * kTile;
-  const int n = min(kTile, p.T - t0);
-  const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;
-  const bool row_live = r < n;
 
   if (warp == 1) {
-    tmem_alloc(tslot, 256);
+    tmem_alloc(tslot, 128);
     tmem_relinquish();
   }
   if (tid == 64) {
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmG);
-    for (int q = 0; q < 3; ++q) mbar_init(&bars[q], 1);
+    mbar_init(bar_load, 1);
+    mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -1208,174 +1245,146 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
-  bool landed = true;
-  if (tid == 0) {
+
+  // thread 0: Q and dO of reader tile j by TMA, and the next reader's boxes into L2
+  auto issue_loads = [&](int j) {
+    const int t0 = j * kTile;
     mbar_arrive_expect_tx(bar_load, kOperand + kVBytes);
     tma_load_4d(&tmQ, bar_load, Qb, 0, hq, t0, b);
     tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, hq, t0, b);
 #pragma unroll
     for (int pv = 0; pv < kPanels; ++pv)
       tma_load_4d(&tmG, bar_load, Gb + pv * kPanel, 64 * pv, h, t0, b);
-    TileAt nx;
-    if (next_tile(p.ahead, p.B, p.T, p.H, p.hg, &nx)) {
-      tma_prefetch_4d(&tmQ, 0, nx.hq, nx.t0, nx.b);
-      tma_prefetch_4d(&tmQ, 64, nx.hq, nx.t0, nx.b);
+    if (j + 1 < s1) {
+      tma_prefetch_4d(&tmQ, 0, hq, t0 + kTile, b);
+      tma_prefetch_4d(&tmQ, 64, hq, t0 + kTile, b);
 #pragma unroll
-      for (int pv = 0; pv < kPanels; ++pv) tma_prefetch_4d(&tmG, 64 * pv, nx.h, nx.t0, nx.b);
+      for (int pv = 0; pv < kPanels; ++pv) tma_prefetch_4d(&tmG, 64 * pv, h, t0 + kTile, b);
     }
+  };
+  bool pending = false;  // thread 0: a load was issued and not yet waited for
+  if (tid == 0) {
+    issue_loads(s0);
+    pending = true;
   }
   __syncwarp();
-  // while the tiles load: every level's D and the inter-level lambdas
-  if (warp == 2) {  // D of every level: log decay of the tiles [c, j)
-    // c falls as m grows: running suffix sums over 32 tiles a step, from j - 1 down, read
-    // off at each level's c (one pass for all levels)
-    int k = 0, m = 0;
-    do ++m;
-    while (!((j >> (m - 1)) & 1));  // nlev >= 1
-    int64_t c = ((int64_t)j >> (m - 1)) << (m - 1);  // block start of level k
-    float run = 0.f;
-    for (int64_t top = j; k < nlev; top -= 32) {  // tiles [top - 32, top)
-      const int64_t x_i = top - 1 - lane;
-      float x = x_i >= 0 ? p.lgu[bh * p.N + x_i] : 0.f;
+  if (warp == 2) {  // D of the first reader: the log decays of the tiles [c, s0)
+    float x = 0.f;
+    for (int i = c + lane; i < s0; i += 32) x += p.lgu[bh * p.N + i];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;  // lane l: tiles [top - 1 - l, top)
-      }
-      while (k < nlev && c >= top - 32) {
-        const float D = run + (c < top ? __shfl_sync(0xffffffffu, x, (int)(top - 1 - c)) : 0.f);
-        if (lane == 0) D_s[k] = D;
-        if (++k < nlev) {
-          do ++m;
-          while (!((j >> (m - 1)) & 1));
-          c = ((int64_t)j >> (m - 1)) << (m - 1);
-        }
-      }
-      run += __shfl_sync(0xffffffffu, x, 31);
-    }
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) d0_s[0] = x;
   }
-  {
-    int k = 0;
-    for (int m = 1; m < kMaxChunkLevels && k < nlev; ++m) {
-      if (!((j >> (m - 1)) & 1)) continue;
-      if ((k & 1) == hh)  // copied in the background: read after the barrier below
-        cp_async4(&lamx[k * kTile + r], row_live ? p.lam + row * p.L + kTileLc + m : p.lam,
-                  row_live ? 4u : 0u);
-      ++k;
-    }
-  }
-  const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
-  const float cs_scan = block_scan256(la, red);
-  if (hh == 0) cs_s[r] = cs_scan;
-  cp_async_wait_all();
-  if (tid == 0) landed = mbar_wait(bar_load, 0);
-  bool all_ok = __syncthreads_and(landed);
-  tc_fence_after();
-  const float cs = cs_s[r];
 
-  uint32_t ph[2] = {0, 0};
-  int c_prev = 0;  // block start of the level being drained
-  for (int k = 0; k <= nlev && all_ok; ++k) {
-    int c_k = 0;
-    if (k < nlev) {
-      int m = 0;
-      for (int seen = -1; seen < k;) {
-        ++m;
-        if ((j >> (m - 1)) & 1) ++seen;
-      }
-      c_k = (j >> (m - 1)) << (m - 1);
-      // rows of Q scaled by w_t, high part and residual, into buffer pair k & 1 (its
-      // previous MMA was drained before)
-      uint8_t* Wh = smem + RsSmem::kW + (k & 1) * 2 * kOperand;
-      uint8_t* Wl = Wh + kOperand;
-      const float w = row_live ? __expf(cs + D_s[k]) * lamx[k * kTile + r] : 0.f;
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const int off = hh * kPanel + sw128_offset(r, g);
-        const uint4 u = *reinterpret_cast<const uint4*>(Qb + off);
-        uint32_t x4[4] = {u.x, u.y, u.z, u.w}, y4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x4[e]));
-          const float a0 = f.x * w, a1 = f.y * w;
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(a0, a1);
-          const float2 hf = __bfloat1622float2(hi);
-          x4[e] = *reinterpret_cast<const uint32_t*>(&hi);
-          y4[e] = pack_bf16(a0 - hf.x, a1 - hf.y);
-        }
-        *reinterpret_cast<uint4*>(Wh + off) = make_uint4(x4[0], x4[1], x4[2], x4[3]);
-        *reinterpret_cast<uint4*>(Wl + off) = make_uint4(y4[0], y4[1], y4[2], y4[3]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        tc_fence_after();
-        constexpr uint32_t idesc = idesc_bf16(128, DV, 1, 1);
-        const uint32_t wh = smem_u32(Wh), wl = smem_u32(Wl), ga = smem_u32(Gb);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16(tmem + (k & 1) * 128, smem_desc_sw128(wh + kk * 2048, kPanel, 1024),
-                   smem_desc_sw128(ga + kk * 2048, kPanel, 1024), idesc, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16(tmem + (k & 1) * 128, smem_desc_sw128(wl + kk * 2048, kPanel, 1024),
-                   smem_desc_sw128(ga + kk * 2048, kPanel, 1024), idesc, 1);
-        mma_commit(&bar_r[k & 1]);
-      }
-      __syncwarp();
+  bool ok = true;
+  float D = 0.f;
+  uint32_t ph = 0;
+  for (int j = s0; j < s1; ++j, ph ^= 1) {
+    const int t0 = j * kTile;
+    const int n = min(kTile, p.T - t0);
+    const bool row_live = r < n;
+    const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;
+    const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
+    const float lam = row_live ? p.lam[row * p.L + lam_l] : 0.f;
+    const float cs_scan = block_scan256(la, red);  // threads 0..127 hold row prefixes
+    if (hh == 0) cs_s[r] = cs_scan;
+    bool landed = true;
+    if (tid == 0) {
+      landed = ok && mbar_wait(bar_load, ph);
+      if (landed) pending = false;
     }
-    if (k >= 1) {  // level k-1 into its block's d_k x d_v part
-      const int bf = (k - 1) & 1;
-      const bool got = __syncthreads_and(mbar_wait(&bar_r[bf], ph[bf]));
-      ph[bf] ^= 1;
-      if (!got) {
-        all_ok = false;
-        break;
+    ok = __syncthreads_and(ok && landed);
+    if (!ok) break;
+    if (j == s0) D = d0_s[0];
+    const float w = row_live ? __expf(cs_s[r] + D) * lam : 0.f;
+    // rows of Q scaled by w: the high part in place, the residual into Lb
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const int off = hh * kPanel + sw128_offset(r, g);
+      const uint4 u = *reinterpret_cast<const uint4*>(Qb + off);
+      uint32_t x4[4] = {u.x, u.y, u.z, u.w}, y4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x4[k]));
+        const float a0 = f.x * w, a1 = f.y * w;
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(a0, a1);
+        const float2 hf = __bfloat1622float2(hi);
+        x4[k] = *reinterpret_cast<const uint32_t*>(&hi);
+        y4[k] = pack_bf16(a0 - hf.x, a1 - hf.y);
       }
+      *reinterpret_cast<uint4*>(Qb + off) = make_uint4(x4[0], x4[1], x4[2], x4[3]);
+      *reinterpret_cast<uint4*>(Lb + off) = make_uint4(y4[0], y4[1], y4[2], y4[3]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
       tc_fence_after();
-      // Row d = r, this thread's half of d_v, staged in the W pair level k-1 read (its MMAs
-      // are done) as 16-byte chunks, chunk x of row d at x ^ (d & 7): the stores of 8
-      // consecutive rows and the reads of one row are free of bank conflicts.
-      float4* stage = reinterpret_cast<float4*>(smem + RsSmem::kW + bf * 2 * kOperand);
-      constexpr int kRowChunks = DV / 4;
+      constexpr uint32_t idesc = idesc_bf16(128, DV, 1, 1);
+      const uint32_t wh = smem_u32(Qb), wl = smem_u32(Lb), ga = smem_u32(Gb);
 #pragma unroll
-      for (int c = 0; c < kPanels; ++c) {
-        float v[32];
-        tmem_ld32(tmem + lane_base + bf * 128 + kHalf * hh + 32 * c, v);
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_bf16(tmem, smem_desc_sw128(wh + kk * 2048, kPanel, 1024),
+                 smem_desc_sw128(ga + kk * 2048, kPanel, 1024), idesc, (j > s0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int x = (kHalf * hh + 32 * c) / 4 + q;
-          stage[r * kRowChunks + (x ^ (r & 7))] =
-              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_bf16(tmem, smem_desc_sw128(wl + kk * 2048, kPanel, 1024),
+                 smem_desc_sw128(ga + kk * 2048, kPanel, 1024), idesc, 1u);
+      mma_commit(bar_mma);
+      // the buffers are free once the products are done: then the next reader's loads
+      ok = mbar_wait(bar_mma, ph);
+      if (ok && j + 1 < s1) {
+        issue_loads(j + 1);
+        pending = true;
       }
-      tc_fence_before();
-      __syncthreads();
-      // the block's part is contiguous in R: one warp's accesses cover 512 bytes.  A
-      // level-1 block (odd start) is this tile alone: stored, the others added.
-      float4* dst = reinterpret_cast<float4*>(p.R + (bh * p.N + c_prev) * kD * DV);
-      if (c_prev & 1) {
-#pragma unroll 4
-        for (int i = tid; i < kD * kRowChunks; i += kThreadsB) {
-          const int d = i / kRowChunks, x = i - d * kRowChunks;
-          dst[i] = stage[d * kRowChunks + (x ^ (d & 7))];
-        }
-      } else {
-#pragma unroll 4
-        for (int i = tid; i < kD * kRowChunks; i += kThreadsB) {
-          const int d = i / kRowChunks, x = i - d * kRowChunks;
-          atomicAdd(dst + i, stage[d * kRowChunks + (x ^ (d & 7))]);
-        }
-      }
-      __syncthreads();  // the stage is the W pair the next level writes
     }
-    c_prev = c_k;
+    __syncwarp();
+    D += p.lgu[bh * p.N + j];
   }
-  if (!all_ok && tid == 0) atomicOr(&g_tcb_error, 1u);
+  ok = __syncthreads_and(ok);
+  tc_fence_after();
+
+  if (ok) {
+    // Row d = r, this thread's half of d_v, staged over Q and the residual as 16-byte
+    // chunks, chunk x of row d at x ^ (d & 7): the stores of 8 consecutive rows and the
+    // reads of one row are free of bank conflicts.
+    float4* stage = reinterpret_cast<float4*>(smem + RsSmem::kQ);
+    constexpr int kRowChunks = DV / 4;
+#pragma unroll
+    for (int cc = 0; cc < kPanels; ++cc) {
+      float v[32];
+      tmem_ld32(tmem + lane_base + kHalf * hh + 32 * cc, v);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int x = (kHalf * hh + 32 * cc) / 4 + u;
+        stage[r * kRowChunks + (x ^ (r & 7))] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+      }
+    }
+    __syncthreads();
+    // the slot is contiguous in R: one warp's accesses cover 512 bytes
+    float4* dst = reinterpret_cast<float4*>(p.R + (bh * p.N + c) * kD * DV);
+    if (whole) {
+#pragma unroll 4
+      for (int i = tid; i < kD * kRowChunks; i += kThreadsB) {
+        const int d = i / kRowChunks, x = i - d * kRowChunks;
+        dst[i] = stage[d * kRowChunks + (x ^ (d & 7))];
+      }
+    } else {
+#pragma unroll 4
+      for (int i = tid; i < kD * kRowChunks; i += kThreadsB) {
+        const int d = i / kRowChunks, x = i - d * kRowChunks;
+        atomicAdd(dst + i, stage[d * kRowChunks + (x ^ (d & 7))]);
+      }
+    }
+  } else if (tid == 0) {
+    atomicOr(&g_tcb_error, 1u);
+    // wait (bounded) for a load still in flight into this CTA's shared memory before it
+    // is handed to another CTA
+    if (pending) mbar_wait(bar_load, ph);
+  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, 128);
 }
 
 }  // namespace
@@ -1491,30 +1500,38 @@ cudaError_t launch_tc_bwd_rstate(const FwdArgs& f, const void* dout, float* R, c
   BrParams p;
   p.B = f.B; p.T = f.T; p.H = f.H; p.hg = f.hg; p.L = f.L; p.N = f.N;
   p.log_a = f.log_a; p.lam = f.lam; p.lgu = f.lg; p.R = R;
-  p.ahead = sm_count();
-  int levels = 0;
+  int levels = 0;  // slots c < N: levels z = ctz(c) < bit length of N - 1
   while ((int64_t(1) << levels) < f.N) ++levels;
+  p.levels = levels;
+  int64_t runs = 0;
+  for (int z = 0; z < levels; ++z) runs += runs_at_level(f.N, z);
+  const int64_t grid = runs * f.B * f.H;
+  if (grid == 0) return cudaSuccess;
+  if (grid > INT32_MAX) return cudaErrorInvalidValue;
   // The shared-memory limit is an attribute of the function on each device: set it
   // on every launch (a host-side call), so that every device the library runs on has it.
   const cudaError_t attr_err =
       f.dv == 128 ? cudaFuncSetAttribute(tc_bwd_rstate_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_bwd_rstate(kMaxChunkLevels - 1))
-                : cudaFuncSetAttribute(tc_bwd_rstate_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_bwd_rstate(kMaxChunkLevels - 1));
+                                         (int)smem_bwd_rstate())
+                  : cudaFuncSetAttribute(tc_bwd_rstate_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_bwd_rstate());
   if (attr_err != cudaSuccess) return attr_err;
-  // Only blocks with an even start are sums over several tiles; the odd ones (level 1) are
-  // stored whole by their one tile.  With N even the even slots are every other one.
-  const size_t slot = sizeof(float) * (size_t)kD * f.dv;
-  const size_t slots = (size_t)f.B * f.H * f.N;
-  cudaError_t e = (f.N % 2 == 0)
-                      ? cudaMemset2DAsync(R, 2 * slot, 0, slot, slots / 2, s)
-                      : cudaMemsetAsync(R, 0, slot * slots, s);
-  if (e != cudaSuccess) return e;
-  const unsigned tiles = (unsigned)((int64_t)f.B * f.H * f.N);
+  // Slots with more readers than one run (z > kRunLog: c a multiple of 2^(kRunLog+1)) are
+  // sums of several runs' atomics: zeroed first.  With N a multiple of that period they are
+  // every period-th slot of the flat [B*H][N] array.
+  const int64_t period = int64_t(2) << kRunLog;
+  if (levels > kRunLog + 1) {
+    const size_t slot = sizeof(float) * (size_t)kD * f.dv;
+    const size_t slots = (size_t)f.B * f.H * f.N;
+    cudaError_t e = (f.N % period == 0)
+                        ? cudaMemset2DAsync(R, period * slot, 0, slot, slots / period, s)
+                        : cudaMemsetAsync(R, 0, slot * slots, s);
+    if (e != cudaSuccess) return e;
+  }
   if (f.dv == 128)
-    tc_bwd_rstate_kernel<128><<<tiles, kThreadsB, smem_bwd_rstate(levels), s>>>(tmQ, tmG, p);
+    tc_bwd_rstate_kernel<128><<<(unsigned)grid, kThreadsB, smem_bwd_rstate(), s>>>(tmQ, tmG, p);
   else
-    tc_bwd_rstate_kernel<64><<<tiles, kThreadsB, smem_bwd_rstate(levels), s>>>(tmQ, tmG, p);
+    tc_bwd_rstate_kernel<64><<<(unsigned)grid, kThreadsB, smem_bwd_rstate(), s>>>(tmQ, tmG, p);
   return cudaGetLastError();
 }
 
