@@ -1145,7 +1145,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // whose bit z - log2(g) is set.  The grid takes the runs level by level from the highest
 // (the longest runs first), the (b, h) innermost.
 
-constexpr int kRunLog = 3;
+constexpr int kRunLog = 4;
 
 // How many q in [0, M) have bit b set.
 __host__ __device__ inline int64_t count_with_bit(int64_t M, int b) {

@@ -152,10 +152,13 @@ __device__ __forceinline__ float block_scan256(float x, float* red) {
   return x + pre;
 }
 
+// kOut: the whole forward; else only the tile states and block states (the backward's
+// recompute, which needs no output): no Q, and K and V move to the front.
+template <bool kOut>
 struct FSmem {
   // byte offsets from the 1024-aligned base
-  static constexpr int kQ = 0, kK = kOperand, kV = 2 * kOperand;
-  static constexpr int kBars = 3 * kOperand;                   // 11 mbarriers (12 slots)
+  static constexpr int kQ = 0, kK = kOut ? kOperand : 0, kV = kK + kOperand;
+  static constexpr int kBars = kV + kOperand;                  // 11 mbarriers (12 slots)
   static constexpr int kTslot = kBars + 12 * 8;
   static constexpr int kInt = kTslot + 16;                     // ticket, loads per buffer
   static constexpr int kRed = kInt + 16;                       // 8 floats
@@ -167,7 +170,11 @@ struct FSmem {
   static constexpr int kLamX = kLam + 4 * kTile * kLamStride;  // [levels][128] floats
 };
 
-size_t smem_fused(int levels) { return (size_t)FSmem::kLamX + 4 * kTile * levels + 1024; }
+template <bool kOut>
+size_t smem_fused(int levels) {
+  return kOut ? (size_t)FSmem<true>::kLamX + 4 * kTile * levels + 1024
+              : (size_t)FSmem<false>::kLam + 1024;  // no lambdas
+}
 
 // Multiplies columns [64 half, 64 half + 64) of row r of a swizzled bf16 tile by s.
 __device__ __forceinline__ void scale_half_row_inplace(uint8_t* buf, int r, int half, float s) {
@@ -208,8 +215,8 @@ __device__ __forceinline__ uint32_t piece_offset(uint32_t q) {
   return (c16 >> 3) * kPanel + sw128_offset(row, c16 & 7);
 }
 
-template <int DV>
-__global__ void __launch_bounds__(kThreadsF, 2)
+template <int DV, bool kOut>
+__global__ void __launch_bounds__(kThreadsF, kOut ? 2 : 3)
     tc_forward_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV,
@@ -218,12 +225,15 @@ __global__ void __launch_bounds__(kThreadsF, 2)
                       const __grid_constant__ CUtensorMap tmNode, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* Qb = smem + FSmem::kQ;    // Q (kept for the level MMAs), then the output
-  uint8_t* Kb = smem + FSmem::kK;    // K, then w ⊙ K, then U in bf16, then P, then block states
-  uint8_t* Vb = smem + FSmem::kV;    // V, then block states
+  using FS = FSmem<kOut>;
+  constexpr uint32_t kTmemCols = kOut ? 256 : 128;  // states only: U in columns 0..d_v
+  constexpr uint32_t kUcol = kOut ? 128 : 0;
+  uint8_t* Qb = smem + FS::kQ;    // Q (kept for the level MMAs), then the output
+  uint8_t* Kb = smem + FS::kK;    // K, then w ⊙ K, then U in bf16, then P, then block states
+  uint8_t* Vb = smem + FS::kV;    // V, then block states
   using G = Dv<DV>;
   constexpr int kStatePieces = G::kStatePieces;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FSmem::kBars);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FS::kBars);
   uint64_t* bar_load = &bars[0];
   uint64_t* bar_s = &bars[1];
   uint64_t* bar_u = &bars[2];
@@ -231,15 +241,15 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   uint64_t* bar_lvl = &bars[4];      // [2]: level MMAs
   uint64_t* bar_node = &bars[6];     // [3]: block-state loads, one per shared buffer
   uint64_t* bar_free = &bars[9];     // [2]: every warp has read a level's TMEM buffer
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + FSmem::kTslot);
-  uint32_t* ints = reinterpret_cast<uint32_t*>(smem + FSmem::kInt);  // ticket, loads[3]
-  float* red = reinterpret_cast<float*>(smem + FSmem::kRed);
-  float* lg_s = reinterpret_cast<float*>(smem + FSmem::kLg);
-  float* nl_s = reinterpret_cast<float*>(smem + FSmem::kNl);
-  float* cs_s = reinterpret_cast<float*>(smem + FSmem::kCs);
-  float* fcol = reinterpret_cast<float*>(smem + FSmem::kFcol);  // exp(cs_e - cs_s), e = s | 31
-  float* lam_s = reinterpret_cast<float*>(smem + FSmem::kLam);
-  float* lamx = reinterpret_cast<float*>(smem + FSmem::kLamX);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + FS::kTslot);
+  uint32_t* ints = reinterpret_cast<uint32_t*>(smem + FS::kInt);  // ticket, loads[3]
+  float* red = reinterpret_cast<float*>(smem + FS::kRed);
+  float* lg_s = reinterpret_cast<float*>(smem + FS::kLg);
+  float* nl_s = reinterpret_cast<float*>(smem + FS::kNl);
+  float* cs_s = reinterpret_cast<float*>(smem + FS::kCs);
+  float* fcol = reinterpret_cast<float*>(smem + FS::kFcol);  // exp(cs_e - cs_s), e = s | 31
+  float* lam_s = reinterpret_cast<float*>(smem + FS::kLam);
+  float* lamx = reinterpret_cast<float*>(smem + FS::kLamX);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int qt = warp & 3;           // row quarter (TMEM lane quarter) of this warp
@@ -249,11 +259,11 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   // ---- the tile: by ticket
   if (tid == 0) ints[0] = atomicAdd(p.tick, 1u);
   if (warp == 1) {
-    tmem_alloc(tslot, 256);
+    tmem_alloc(tslot, kTmemCols);
     tmem_relinquish();
   }
   if (tid == 64) {
-    prefetch_tensormap(&tmQ);
+    if (kOut) prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmOut);
@@ -285,16 +295,18 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   const bool row_live = r < n;
   bool landed = true;  // thread 0: Q, K and V arrived
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar_load, 2 * kOperand + G::kVBytes);
-    tma_load_4d(&tmQ, bar_load, Qb, 0, hq, t0, b);
-    tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, hq, t0, b);
+    mbar_arrive_expect_tx(bar_load, (kOut ? 2 : 1) * kOperand + G::kVBytes);
+    if (kOut) {
+      tma_load_4d(&tmQ, bar_load, Qb, 0, hq, t0, b);
+      tma_load_4d(&tmQ, bar_load, Qb + kPanel, 64, hq, t0, b);
+    }
     tma_load_4d(&tmK, bar_load, Kb, 0, hq, t0, b);
     tma_load_4d(&tmK, bar_load, Kb + kPanel, 64, hq, t0, b);
 #pragma unroll
     for (int pv = 0; pv < G::kPanels; ++pv)
       tma_load_4d(&tmV, bar_load, Vb + pv * kPanel, 64 * pv, h, t0, b);
   }
-  if (tid == 64 && h == 0 && j + 2 < N) {  // warm L2 with tile j+2's log a and lambda (all heads)
+  if (kOut && tid == 64 && h == 0 && j + 2 < N) {  // warm L2 with tile j+2's log a and lambda (all heads)
     const int64_t tok0 = (int64_t)b * p.T + (int64_t)(j + 2) * kTile;
     const int64_t ntok = min(kTile, p.T - (j + 2) * kTile);
     prefetch_l2_range(p.lam + tok0 * p.H * p.L, ntok * p.H * p.L * 4);
@@ -309,9 +321,9 @@ __global__ void __launch_bounds__(kThreadsF, 2)
 #pragma unroll
   for (int i = 0; i < kIntraLevels / 2; ++i) {
     const int l = hh * (kIntraLevels / 2) + i;
-    lam_in[i] = (row_live && l < p.L) ? p.lam[row * p.L + l] : 0.f;
+    lam_in[i] = (kOut && row_live && l < p.L) ? p.lam[row * p.L + l] : 0.f;
   }
-  {
+  if (kOut) {
     int k = 0;
 #pragma unroll 4
     for (int m = 1; m < kMaxChunkLevels; ++m) {
@@ -324,7 +336,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   }
   if (tid == 0) {  // S = Q K^T as soon as the tiles land, before the scan needs log a
     landed = mbar_wait(bar_load, 0);
-    if (landed) {
+    if (kOut && landed) {
       tc_fence_after();
       constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
       const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb);
@@ -340,17 +352,19 @@ __global__ void __launch_bounds__(kThreadsF, 2)
   const float cs_scan = block_scan256(la, red);  // threads 0..127 hold row prefixes
   if (hh == 0) cs_s[r] = cs_scan;
   if (tid == kTile - 1) lg_s[0] = cs_scan;       // padding rows add 0: the tile's log decay
+  if (kOut) {
 #pragma unroll
-  for (int i = 0; i < kIntraLevels / 2; ++i)
-    lam_s[r * kLamStride + hh * (kIntraLevels / 2) + i] = lam_in[i];
+    for (int i = 0; i < kIntraLevels / 2; ++i)
+      lam_s[r * kLamStride + hh * (kIntraLevels / 2) + i] = lam_in[i];
+  }
   __syncthreads();
   const float cs = cs_s[r];
   const float lg = lg_s[0];
-  if (hh == 1) fcol[r] = __expf(cs_s[r | 31] - cs);  // <= 1: cs does not increase
+  if (kOut && hh == 1) fcol[r] = __expf(cs_s[r | 31] - cs);  // <= 1: cs does not increase
 
   // ---- S = Q K^T (issued by thread 0 above)
   bool all_ok = __syncthreads_and(landed);
-  bool ok = all_ok && mbar_wait(bar_s, 0);
+  bool ok = all_ok && (!kOut || mbar_wait(bar_s, 0));
   tc_fence_after();
   all_ok = __syncthreads_and(ok);
 
@@ -365,7 +379,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     const uint32_t va = smem_u32(Vb), ka = smem_u32(Kb);
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk)
-      mma_bf16(tmem + 128, smem_desc_sw128(ka + kk * 2048, kPanel, 1024),
+      mma_bf16(tmem + kUcol, smem_desc_sw128(ka + kk * 2048, kPanel, 1024),
                smem_desc_sw128(va + kk * 2048, kPanel, 1024), idesc, kk > 0);
     mma_commit(bar_u);
   }
@@ -388,7 +402,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
 #pragma unroll
   for (int c = 0; c < G::kPanels; ++c) {  // U row r (d_k), this thread's half of d_v -> Kb
     float v[32];
-    tmem_ld32(tmem + lane_base + 128 + G::kHalf * hh + 32 * c, v);
+    tmem_ld32(tmem + lane_base + kUcol + G::kHalf * hh + 32 * c, v);
     put_row32_bf16(Kb, r, G::kPanels * hh + c, v);
   }
   // Only U of even tiles is read by other tiles (slot j+1, odd, is U_j; an even slot's
@@ -473,251 +487,255 @@ __global__ void __launch_bounds__(kThreadsF, 2)
     st_release_gpu(&rdy_u[j], decay_flag(lg));
   }
 
-  // ---- the levels' block states.  Level k (the k-th set bit of j, from the lowest) is
-  // owned by thread 32+k: it finds its slot c, acquires the slot's ready flag (which
-  // carries the block's log decay) and issues the TMA load itself, after a proxy fence,
-  // so the acquire and the async-proxy read are ordered in one thread.  Level k goes to
-  // shared buffer k mod kNodeBufs: K's tile (free now; one buffer for d_v = 128, two for
-  // d_v = 64), then V's (free once P V is done).  The block state of slot c is U_{c-1}
-  // for odd c.
-  int my_c = 0;         // thread 32+k, k < nlev: the slot of level k
-  bool acquired = false;
-  {
-    const int k = tid - 32;
-    if (k >= 0 && k < nlev) {
-      int m = 0;
-      for (int seen = -1; seen < k;) {
-        ++m;
-        if ((j >> (m - 1)) & 1) ++seen;
+  uint32_t consumed = 0;  // thread 0: block-state loads waited for, 8 bits per buffer
+  if constexpr (kOut) {
+    // ---- the levels' block states.  Level k (the k-th set bit of j, from the lowest) is
+    // owned by thread 32+k: it finds its slot c, acquires the slot's ready flag (which
+    // carries the block's log decay) and issues the TMA load itself, after a proxy fence,
+    // so the acquire and the async-proxy read are ordered in one thread.  Level k goes to
+    // shared buffer k mod kNodeBufs: K's tile (free now; one buffer for d_v = 128, two for
+    // d_v = 64), then V's (free once P V is done).  The block state of slot c is U_{c-1}
+    // for odd c.
+    int my_c = 0;         // thread 32+k, k < nlev: the slot of level k
+    bool acquired = false;
+    {
+      const int k = tid - 32;
+      if (k >= 0 && k < nlev) {
+        int m = 0;
+        for (int seen = -1; seen < k;) {
+          ++m;
+          if ((j >> (m - 1)) & 1) ++seen;
+        }
+        my_c = (j >> (m - 1)) << (m - 1);
       }
-      my_c = (j >> (m - 1)) << (m - 1);
     }
-  }
-  auto node_buf = [&](int b) -> uint8_t* {
-    return b == G::kNodeBufs - 1 ? Vb : Kb + b * G::kStateBytes;
-  };
-  auto fetch = [&](int k) {  // thread 32+k: TMA of level k's block state
-    if (tid == 32 + k) {
-      const int b = k % G::kNodeBufs;
-      uint8_t* dst = node_buf(b);
-      const bool is_u = (my_c & 1) != 0;
-      const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
-      atomicAdd(&ints[1 + b], 1u);
-      mbar_arrive_expect_tx(&bar_node[b], G::kStateBytes);
+    auto node_buf = [&](int b) -> uint8_t* {
+      return b == G::kNodeBufs - 1 ? Vb : Kb + b * G::kStateBytes;
+    };
+    auto fetch = [&](int k) {  // thread 32+k: TMA of level k's block state
+      if (tid == 32 + k) {
+        const int b = k % G::kNodeBufs;
+        uint8_t* dst = node_buf(b);
+        const bool is_u = (my_c & 1) != 0;
+        const int row0 = (int)((bh * N + (is_u ? my_c - 1 : my_c)) * kD);
+        atomicAdd(&ints[1 + b], 1u);
+        mbar_arrive_expect_tx(&bar_node[b], G::kStateBytes);
 #pragma unroll
-      for (int pv = 0; pv < G::kPanels; ++pv)
-        tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[b], dst + pv * kPanel, 64 * pv, row0);
+        for (int pv = 0; pv < G::kPanels; ++pv)
+          tma_load_2d(is_u ? &tmU : &tmNode, &bar_node[b], dst + pv * kPanel, 64 * pv, row0);
+      }
+    };
+    // levels whose buffer lies in K's tile: load now if the flag is already up (one poll)
+    if (all_ok && tid >= 32 && tid - 32 < nlev && tid - 32 < G::kNodeBufs - 1) {
+      const uint32_t fv = ld_acquire_gpu(my_c & 1 ? &rdy_u[my_c - 1] : &rdy_n[my_c]);
+      if (fv != 0) {
+        acquired = true;
+        nl_s[tid - 32] = flag_decay(fv);
+        fence_proxy_async_global();
+        fetch(tid - 32);
+      }
     }
-  };
-  // levels whose buffer lies in K's tile: load now if the flag is already up (one poll)
-  if (all_ok && tid >= 32 && tid - 32 < nlev && tid - 32 < G::kNodeBufs - 1) {
-    const uint32_t fv = ld_acquire_gpu(my_c & 1 ? &rdy_u[my_c - 1] : &rdy_n[my_c]);
-    if (fv != 0) {
-      acquired = true;
-      nl_s[tid - 32] = flag_decay(fv);
-      fence_proxy_async_global();
-      fetch(tid - 32);
-    }
-  }
-  __syncwarp();
+    __syncwarp();
 
-  // ---- P, bf16 (two per column) into TMEM columns 128..191: the state's columns, read
-  // out above.  The two warps of quarter qt take the 32-column chunks of their parity;
-  // chunk c of row r goes to columns [128 + 16c, +16).  Chunks c > qt lie above the
-  // diagonal (zero), chunks c < qt below it (level 5 + bit_length(qt XOR c) for every
-  // pair), chunk qt holds the diagonal.
-  if (all_ok) {
-    const float* lam_r = lam_s + r * kLamStride;
-    for (int c = hh; c < kTile / 32; c += 2) {
-      float sv[32];
-      if (c <= qt) {
-        tmem_ld32(tmem + lane_base + c * 32, sv);
-        if (c < qt) {  // exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s), both <= 1
-          const float wl = lam_r[5 + (32 - __clz((unsigned)(qt ^ c)))] *
-                           __expf(cs - cs_s[c * 32 + 31]);
+    // ---- P, bf16 (two per column) into TMEM columns 128..191: the state's columns, read
+    // out above.  The two warps of quarter qt take the 32-column chunks of their parity;
+    // chunk c of row r goes to columns [128 + 16c, +16).  Chunks c > qt lie above the
+    // diagonal (zero), chunks c < qt below it (level 5 + bit_length(qt XOR c) for every
+    // pair), chunk qt holds the diagonal.
+    if (all_ok) {
+      const float* lam_r = lam_s + r * kLamStride;
+      for (int c = hh; c < kTile / 32; c += 2) {
+        float sv[32];
+        if (c <= qt) {
+          tmem_ld32(tmem + lane_base + c * 32, sv);
+          if (c < qt) {  // exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s), both <= 1
+            const float wl = lam_r[5 + (32 - __clz((unsigned)(qt ^ c)))] *
+                             __expf(cs - cs_s[c * 32 + 31]);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) sv[k] *= wl * fcol[c * 32 + k];
-        } else if (cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f) {
-          // the diagonal chunk with a decay range that keeps exp(cs_t - cs_e) <= e^80:
-          // exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s).  The pair (r, s) has level
-          // bit_length(lane XOR k) <= 5 for column k <= lane: the six lambdas of the levels
-          // inside a 32-token chunk are held in registers and picked by select.
-          const float gt = row_live ? __expf(cs - cs_s[c * 32 + 31]) : 0.f;
-          const int lane = tid & 31;
-          const float l0 = lam_r[0], l1 = lam_r[1], l2 = lam_r[2], l3 = lam_r[3],
-                      l4 = lam_r[4], l5 = lam_r[5];
+            for (int k = 0; k < 32; ++k) sv[k] *= wl * fcol[c * 32 + k];
+          } else if (cs_s[c * 32] - cs_s[c * 32 + 31] < 80.f) {
+            // the diagonal chunk with a decay range that keeps exp(cs_t - cs_e) <= e^80:
+            // exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s).  The pair (r, s) has level
+            // bit_length(lane XOR k) <= 5 for column k <= lane: the six lambdas of the levels
+            // inside a 32-token chunk are held in registers and picked by select.
+            const float gt = row_live ? __expf(cs - cs_s[c * 32 + 31]) : 0.f;
+            const int lane = tid & 31;
+            const float l0 = lam_r[0], l1 = lam_r[1], l2 = lam_r[2], l3 = lam_r[3],
+                        l4 = lam_r[4], l5 = lam_r[5];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int x = lane ^ k;
-            const float lv = x >= 16 ? l5 : x >= 8 ? l4 : x >= 4 ? l3 : x >= 2 ? l2 : x >= 1 ? l1 : l0;
-            const float v = sv[k] * lv * (gt * fcol[c * 32 + k]);
-            sv[k] = k <= lane ? v : 0.f;
+            for (int k = 0; k < 32; ++k) {
+              const int x = lane ^ k;
+              const float lv = x >= 16 ? l5 : x >= 8 ? l4 : x >= 4 ? l3 : x >= 2 ? l2 : x >= 1 ? l1 : l0;
+              const float v = sv[k] * lv * (gt * fcol[c * 32 + k]);
+              sv[k] = k <= lane ? v : 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int s = c * 32 + k;
+              float v = 0.f;
+              if (s <= r && row_live)
+                v = sv[k] * lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * __expf(cs - cs_s[s]);
+              sv[k] = v;
+            }
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int s = c * 32 + k;
-            float v = 0.f;
-            if (s <= r && row_live)
-              v = sv[k] * lam_r[fenwick_level((uint32_t)r, (uint32_t)s)] * __expf(cs - cs_s[s]);
-            sv[k] = v;
-          }
+          for (int k = 0; k < 32; ++k) sv[k] = 0.f;
         }
-      } else {
+        uint32_t pw[16];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) sv[k] = 0.f;
+        for (int e = 0; e < 16; ++e) pw[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
+        tmem_st16(tmem + lane_base + 128 + 16 * c, pw);
       }
-      uint32_t pw[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) pw[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
-      tmem_st16(tmem + lane_base + 128 + 16 * c, pw);
+      tmem_wait_st();
     }
-    tmem_wait_st();
-  }
-  tc_fence_before();
-  all_ok = __syncthreads_and(ok);
-  // ---- O = P V into columns 0..DV (P from TMEM, V MN-major as B)
-  if (all_ok && tid == 0) {
-    tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16(128, DV, 0, 1);
-    const uint32_t va = smem_u32(Vb);
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk)
-      mma_bf16_ts(tmem, tmem + 128 + 8 * kk, smem_desc_sw128(va + kk * 2048, kPanel, 1024), idesc,
-                  kk > 0);
-    mma_commit(bar_o);
-  }
-  __syncwarp();
-
-  // ---- while P V runs, the remaining levels' flags (waited for, bounded)
-  {
-    bool fl = true;
-    const int k = tid - 32;
-    if (k >= 0 && k < nlev && !acquired) {
-      uint32_t fv;
-      fl = wait_flag_acquire_value(my_c & 1 ? &rdy_u[my_c - 1] : &rdy_n[my_c], &fv);
-      nl_s[k] = fl ? flag_decay(fv) : 0.f;
-      fence_proxy_async_global();
-    }
-    if (!__syncthreads_and(fl) && tid == 0) atomicOr(&g_tc_error, 2u);
-  }
-  // ---- O = P V is done: V's tile is free
-  ok = all_ok && mbar_wait(bar_o, 0);
-  tc_fence_after();
-  all_ok = __syncthreads_and(ok);
-  if (all_ok && tid >= 32 && tid - 32 < nlev && tid - 32 < G::kNodeBufs && !acquired)
-    fetch(tid - 32);
-  __syncwarp();
-
-  // ---- O from TMEM into registers: this thread's half row, columns [DV/2 hh, +DV/2)
-  float o[G::kHalf];
-#pragma unroll
-  for (int q = 0; q < G::kHalf; ++q) o[q] = 0.f;
-  const uint32_t col0 = (uint32_t)G::kHalf * hh;
-  if (all_ok) {
-#pragma unroll
-    for (int c = 0; c < G::kPanels; ++c) {
-      float v[32];
-      tmem_ld32(tmem + lane_base + col0 + c * 32, v);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) o[c * 32 + q] = v[q];
-    }
-  }
-  cp_async_wait_all();  // the inter-level lambdas
-  tc_fence_before();
-  __syncthreads();  // TMEM is free
-
-  // ---- inter-chunk levels, without block barriers.  Level k uses shared buffer
-  // k mod kNodeBufs and TMEM columns [128 (k&1), +DV).  Thread 0 issues MMA k once its
-  // block state has landed and every warp has added level k-2 to O (bar_free[k&1]); each
-  // warp adds level k-1 to O once MMA k-1 is done (bar_lvl), then releases that TMEM
-  // buffer.  The load of level k-1+kNodeBufs starts as soon as MMA k-1 is done with its
-  // shared buffer.
-  const int lane = tid & 31;
-  uint32_t lvl_ph = 0, node_ph = 0, free_ph = 0;  // phase bits per buffer
-  uint32_t consumed = 0;  // thread 0: block-state loads waited for, 8 bits per buffer
-  float D = 0.f;  // log decay from block k's end to the tile's start
-  bool lv_ok = all_ok;
-  int nb = 0;  // k mod kNodeBufs
-  for (int k = 0; k <= nlev && all_ok; ++k) {
-    if (tid == 0 && k < nlev) {  // issue level k
-      bool go = lv_ok && mbar_wait(&bar_node[nb], (node_ph >> nb) & 1);
-      node_ph ^= 1u << nb;
-      if (go) consumed += 1u << (8 * nb);
-      if (k >= 2) {
-        go = go && mbar_wait(&bar_free[k & 1], (free_ph >> (k & 1)) & 1);
-        free_ph ^= 1u << (k & 1);
-      }
-      if (go) {
-        tc_fence_after();
-        // A = Q (K-major), B = the block state [d_k][d_v] (MN-major, like V in P V)
-        constexpr uint32_t idesc = idesc_bf16(128, DV, 0, 1);
-        const uint32_t qa = smem_u32(Qb), sa = smem_u32(node_buf(nb));
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-          mma_bf16(tmem + (k & 1) * 128, smem_desc_sw128(qa + off, 16, 1024),
-                   smem_desc_sw128(sa + kk * 2048, kPanel, 1024), idesc, kk > 0);
-        }
-        mma_commit(&bar_lvl[k & 1]);
-      }
-      lv_ok = go;
-    }
-    nb = nb + 1 == G::kNodeBufs ? 0 : nb + 1;
-    __syncwarp();
-    if (k >= 1) {  // level k-1 into O
-      const int bf = (k - 1) & 1;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_lvl[bf], (lvl_ph >> bf) & 1));
-      lvl_ph ^= 1u << bf;
-      if (!got) {
-        lv_ok = false;
-        break;
-      }
+    tc_fence_before();
+    all_ok = __syncthreads_and(ok);
+    // ---- O = P V into columns 0..DV (P from TMEM, V MN-major as B)
+    if (all_ok && tid == 0) {
       tc_fence_after();
-      if (k - 1 + G::kNodeBufs < nlev) fetch(k - 1 + G::kNodeBufs);  // into MMA k-1's buffer
-      const float wr = lamx[(k - 1) * kTile + r] * __expf(cs + D);
-      D += nl_s[k - 1];
+      constexpr uint32_t idesc = idesc_bf16(128, DV, 0, 1);
+      const uint32_t va = smem_u32(Vb);
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_bf16_ts(tmem, tmem + 128 + 8 * kk, smem_desc_sw128(va + kk * 2048, kPanel, 1024), idesc,
+                    kk > 0);
+      mma_commit(bar_o);
+    }
+    __syncwarp();
+
+    // ---- while P V runs, the remaining levels' flags (waited for, bounded)
+    {
+      bool fl = true;
+      const int k = tid - 32;
+      if (k >= 0 && k < nlev && !acquired) {
+        uint32_t fv;
+        fl = wait_flag_acquire_value(my_c & 1 ? &rdy_u[my_c - 1] : &rdy_n[my_c], &fv);
+        nl_s[k] = fl ? flag_decay(fv) : 0.f;
+        fence_proxy_async_global();
+      }
+      if (!__syncthreads_and(fl) && tid == 0) atomicOr(&g_tc_error, 2u);
+    }
+    // ---- O = P V is done: V's tile is free
+    ok = all_ok && mbar_wait(bar_o, 0);
+    tc_fence_after();
+    all_ok = __syncthreads_and(ok);
+    if (all_ok && tid >= 32 && tid - 32 < nlev && tid - 32 < G::kNodeBufs && !acquired)
+      fetch(tid - 32);
+    __syncwarp();
+
+    // ---- O from TMEM into registers: this thread's half row, columns [DV/2 hh, +DV/2)
+    float o[G::kHalf];
+#pragma unroll
+    for (int q = 0; q < G::kHalf; ++q) o[q] = 0.f;
+    const uint32_t col0 = (uint32_t)G::kHalf * hh;
+    if (all_ok) {
 #pragma unroll
       for (int c = 0; c < G::kPanels; ++c) {
         float v[32];
-        tmem_ld32(tmem + lane_base + bf * 128 + col0 + c * 32, v);
+        tmem_ld32(tmem + lane_base + col0 + c * 32, v);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) o[c * 32 + q] = fmaf(wr, v[q], o[c * 32 + q]);
+        for (int q = 0; q < 32; ++q) o[c * 32 + q] = v[q];
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_free[bf]);
     }
-  }
-  all_ok = __syncthreads_and(all_ok && lv_ok);
+    cp_async_wait_all();  // the inter-level lambdas
+    tc_fence_before();
+    __syncthreads();  // TMEM is free
 
-  // ---- epilogue
-  if (all_ok) {
-    if (p.out_f32) {
-      if (row_live) {
-        float4* dst = reinterpret_cast<float4*>(
-            reinterpret_cast<float*>(p.out) + (int64_t)b * p.so_b + (int64_t)(t0 + r) * p.so_t +
-            (int64_t)h * p.so_h + col0);
+    // ---- inter-chunk levels, without block barriers.  Level k uses shared buffer
+    // k mod kNodeBufs and TMEM columns [128 (k&1), +DV).  Thread 0 issues MMA k once its
+    // block state has landed and every warp has added level k-2 to O (bar_free[k&1]); each
+    // warp adds level k-1 to O once MMA k-1 is done (bar_lvl), then releases that TMEM
+    // buffer.  The load of level k-1+kNodeBufs starts as soon as MMA k-1 is done with its
+    // shared buffer.
+    const int lane = tid & 31;
+    uint32_t lvl_ph = 0, node_ph = 0, free_ph = 0;  // phase bits per buffer
+    float D = 0.f;  // log decay from block k's end to the tile's start
+    bool lv_ok = all_ok;
+    int nb = 0;  // k mod kNodeBufs
+    for (int k = 0; k <= nlev && all_ok; ++k) {
+      if (tid == 0 && k < nlev) {  // issue level k
+        bool go = lv_ok && mbar_wait(&bar_node[nb], (node_ph >> nb) & 1);
+        node_ph ^= 1u << nb;
+        if (go) consumed += 1u << (8 * nb);
+        if (k >= 2) {
+          go = go && mbar_wait(&bar_free[k & 1], (free_ph >> (k & 1)) & 1);
+          free_ph ^= 1u << (k & 1);
+        }
+        if (go) {
+          tc_fence_after();
+          // A = Q (K-major), B = the block state [d_k][d_v] (MN-major, like V in P V)
+          constexpr uint32_t idesc = idesc_bf16(128, DV, 0, 1);
+          const uint32_t qa = smem_u32(Qb), sa = smem_u32(node_buf(nb));
 #pragma unroll
-        for (int q = 0; q < G::kHalf / 4; ++q)
-          dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+            mma_bf16(tmem + (k & 1) * 128, smem_desc_sw128(qa + off, 16, 1024),
+                     smem_desc_sw128(sa + kk * 2048, kPanel, 1024), idesc, kk > 0);
+          }
+          mma_commit(&bar_lvl[k & 1]);
+        }
+        lv_ok = go;
       }
-    } else {
-      // no MMA reads Q any more: stage the bf16 tile there and store it with TMA
-#pragma unroll
-      for (int c = 0; c < G::kPanels; ++c) put_row32_bf16(Qb, r, G::kPanels * hh + c, o + c * 32);
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-#pragma unroll
-        for (int pv = 0; pv < G::kPanels; ++pv)
-          tma_store_4d(&tmOut, Qb + pv * kPanel, 64 * pv, h, t0, b);
-        tma_store_commit();
-        tma_store_wait_read();
-      }
+      nb = nb + 1 == G::kNodeBufs ? 0 : nb + 1;
       __syncwarp();
+      if (k >= 1) {  // level k-1 into O
+        const int bf = (k - 1) & 1;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_lvl[bf], (lvl_ph >> bf) & 1));
+        lvl_ph ^= 1u << bf;
+        if (!got) {
+          lv_ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (k - 1 + G::kNodeBufs < nlev) fetch(k - 1 + G::kNodeBufs);  // into MMA k-1's buffer
+        const float wr = lamx[(k - 1) * kTile + r] * __expf(cs + D);
+        D += nl_s[k - 1];
+#pragma unroll
+        for (int c = 0; c < G::kPanels; ++c) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + bf * 128 + col0 + c * 32, v);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) o[c * 32 + q] = fmaf(wr, v[q], o[c * 32 + q]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_free[bf]);
+      }
     }
-  } else if (tid == 0) {
+    all_ok = __syncthreads_and(all_ok && lv_ok);
+
+    // ---- epilogue
+    if (all_ok) {
+      if (p.out_f32) {
+        if (row_live) {
+          float4* dst = reinterpret_cast<float4*>(
+              reinterpret_cast<float*>(p.out) + (int64_t)b * p.so_b + (int64_t)(t0 + r) * p.so_t +
+              (int64_t)h * p.so_h + col0);
+#pragma unroll
+          for (int q = 0; q < G::kHalf / 4; ++q)
+            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      } else {
+        // no MMA reads Q any more: stage the bf16 tile there and store it with TMA
+#pragma unroll
+        for (int c = 0; c < G::kPanels; ++c) put_row32_bf16(Qb, r, G::kPanels * hh + c, o + c * 32);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+          for (int pv = 0; pv < G::kPanels; ++pv)
+            tma_store_4d(&tmOut, Qb + pv * kPanel, 64 * pv, h, t0, b);
+          tma_store_commit();
+          tma_store_wait_read();
+        }
+        __syncwarp();
+      }
+    } else if (tid == 0) {
+      atomicOr(&g_tc_error, 1u);
+    }
+  } else if (!all_ok && tid == 0) {  // states only
     atomicOr(&g_tc_error, 1u);
   }
   tc_fence_before();
@@ -730,7 +748,7 @@ __global__ void __launch_bounds__(kThreadsF, 2)
       for (uint32_t c = (consumed >> (8 * b)) & 255u; c < ints[1 + b]; ++c)
         mbar_wait(&bar_node[b], c & 1);
   }
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -790,7 +808,8 @@ bool tc_forward_supported(int64_t dk, int64_t dv, int in_dtype, int /*chunk*/) {
   return in_dtype == LL_BF16 && dk == kD && (dv == 64 || dv == 128);
 }
 
-cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev) {
+cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev,
+                              bool states_only) {
   const int64_t rows = (int64_t)a.B * a.H * a.N * kD;  // TMA row coordinates are int32
   if (rows > INT32_MAX) return cudaErrorInvalidValue;
   if (a.dk != kD || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
@@ -821,11 +840,12 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   while ((int64_t(1) << levels) < a.N) ++levels;
   // The shared-memory limit is an attribute of the function on each device: set it
   // on every launch (a host-side call), so that every device the library runs on has it.
-  const cudaError_t attr_err =
-      dv == 128 ? cudaFuncSetAttribute(tc_forward_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_fused(kMaxChunkLevels - 1))
-                : cudaFuncSetAttribute(tc_forward_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_fused(kMaxChunkLevels - 1));
+  auto kernel = dv == 128 ? (states_only ? tc_forward_kernel<128, false> : tc_forward_kernel<128, true>)
+                          : (states_only ? tc_forward_kernel<64, false> : tc_forward_kernel<64, true>);
+  const size_t smem = states_only ? smem_fused<false>(levels) : smem_fused<true>(levels);
+  const cudaError_t attr_err = cudaFuncSetAttribute(
+      kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)(states_only ? smem_fused<false>(0) : smem_fused<true>(kMaxChunkLevels - 1)));
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles = (int64_t)a.B * a.H * a.N;
   cudaError_t e;
@@ -834,12 +854,7 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   if ((e = cudaMemsetAsync(a.rdy_u, 0, sizeof(uint32_t) * (size_t)(2 * tiles + 1), s)) !=
       cudaSuccess)
     return e;
-  if (dv == 128)
-    tc_forward_kernel<128><<<dim3((unsigned)tiles), kThreadsF, smem_fused(levels), s>>>(
-        tmQ, tmK, tmV, tmOut, tmU, tmNode, p);
-  else
-    tc_forward_kernel<64><<<dim3((unsigned)tiles), kThreadsF, smem_fused(levels), s>>>(
-        tmQ, tmK, tmV, tmOut, tmU, tmNode, p);
+  kernel<<<dim3((unsigned)tiles), kThreadsF, smem, s>>>(tmQ, tmK, tmV, tmOut, tmU, tmNode, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = ev->record(s)) != cudaSuccess) return e;
   return ev ? ev->finish(s) : cudaSuccess;

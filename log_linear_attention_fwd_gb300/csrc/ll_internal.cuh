@@ -131,7 +131,10 @@ struct StageEvents {
 // Launchers (return cudaError_t of the launches).
 cudaError_t launch_simt_forward(const FwdArgs& a, int in_dtype, int out_dtype, cudaStream_t s,
                                 StageEvents* ev);
-cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev);
+// states_only: the tile states, block states and log decays (all a backward reads), no
+// output; Q is not read.
+cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, StageEvents* ev,
+                              bool states_only = false);
 cudaError_t launch_level_scan(const FwdArgs& a, cudaStream_t s);
 // The CUDA-core path's chunk states U and fp32 block states of every slot (K1 and K2 of
 // the forward, without the readout).

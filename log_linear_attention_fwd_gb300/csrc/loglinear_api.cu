@@ -580,8 +580,8 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (n_tc > 0) {
-    // dQ and dlambda on the tensor cores: a tensor-core forward publishes the block states
-    // (its output goes to scratch), then the dQ kernel reads them
+    // dQ and dlambda on the tensor cores: a tensor-core forward in its states-only form
+    // publishes the block states (no output), then the dQ kernel reads them
     FwdArgs f = a;
     f.C = kTcTile;
     f.lc = log2_exact(kTcTile);
@@ -610,7 +610,7 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
         e = cudaMemsetAsync(A.dkh, 0, qk_bytes, s);
       if (e != cudaSuccess) return cuda_fail(e);
     }
-    if (!fwd_workspace) e = launch_tc_forward(f, LL_BF16, s, nullptr);
+    if (!fwd_workspace) e = launch_tc_forward(f, LL_BF16, s, nullptr, /*states_only=*/true);
     if (e == cudaSuccess)
       e = launch_tc_bwd_dq(f, dout, A.dqh, own_qk ? dq : nullptr, A.dcq, dlambda, s);
     if (e == cudaSuccess && f.N > 1) e = launch_tc_bwd_rstate(f, dout, R, s);
