@@ -184,6 +184,34 @@ def test_bwd_tc_full_size_sampled(LL):
         assert all(e <= TOL_BF16 for e in errs.values()), errs
 
 
+@pytest.mark.parametrize("T,dv", [(5125, 64), (8269, 128)])
+def test_bwd_tc_long_mirrored_runs_no_decay(LL, T, dv):
+    """Without decay every level carries full weight into dk and dv.  41 and 65 tiles of
+    128 tokens: the top slots (32, and 64) have more reader tiles than one run takes, so
+    their mirrored states are sums of several runs added with atomics, and the tile counts
+    are not multiples of 16 (the whole mirrored-state buffer is zeroed first).  dq, dlambda
+    of sampled query rows and dk, dv of sampled source positions against the oracle."""
+    L = (T - 1).bit_length() + 1
+    cfg = W.FwdConfig("bwd_runs", 1, 2, T, 128, dv, 64, L, "bf16", False, "softplus", seed=T)
+    x = W.make_fwd_inputs(cfg)
+    dout = _dout(cfg, 7)
+    d = cuda(x)
+    got = LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout.cuda(), path="tc")
+    torch.cuda.synchronize()
+    assert LL.device_error() == 0
+    rows, cols = _positions(T, 16, 3), _positions(T, 16, 4)
+    heads = [(0, 0), (0, 1)]
+    want = oracle.backward_sampled(x["q"], x["k"], x["v"], x["log_a"], x["lam"], dout, rows,
+                                   cols, heads)
+    for i, (b, h) in enumerate(heads):
+        errs = {"q": rel_l2(got[0][b, rows, h].cpu(), want["q"][i]),
+                "lam": rel_l2(got[4][b, rows, h].cpu(), want["lam"][i]),
+                "k": rel_l2(got[1][b, cols, h].cpu(), want["k"][i]),
+                "v": rel_l2(got[2][b, cols, h].cpu(), want["v"][i])}
+        print(f"bwd tc runs T={T} dv={dv} head {h}: " + " ".join(f"{k}={e:.2e}" for k, e in errs.items()))
+        assert all(e <= TOL_BF16 for e in errs.values()), errs
+
+
 @pytest.mark.parametrize("dv,Hqk", [(128, 0), (64, 1)])
 def test_bwd_reads_forward_workspace(LL, dv, Hqk):
     """The backward given a tensor-core forward's workspace (its block states kept) equals
