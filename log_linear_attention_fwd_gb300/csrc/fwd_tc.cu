@@ -216,7 +216,7 @@ __device__ __forceinline__ uint32_t piece_offset(uint32_t q) {
 }
 
 template <int DV, bool kOut>
-__global__ void __launch_bounds__(kThreadsF, kOut ? 2 : 3)
+__global__ void __launch_bounds__(kThreadsF, 2)
     tc_forward_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV,
