@@ -184,13 +184,14 @@ def test_bwd_tc_full_size_sampled(LL):
         assert all(e <= TOL_BF16 for e in errs.values()), errs
 
 
-@pytest.mark.parametrize("T,dv", [(5125, 64), (8269, 128)])
+@pytest.mark.parametrize("T,dv", [(5125, 64), (8269, 128), (70000, 64)])
 def test_bwd_tc_long_mirrored_runs_no_decay(LL, T, dv):
-    """Without decay every level carries full weight into dk and dv.  41 and 65 tiles of
-    128 tokens: the top slots (32, and 64) have more reader tiles than one run takes, so
-    their mirrored states are sums of several runs added with atomics, and the tile counts
-    are not multiples of 16 (the whole mirrored-state buffer is zeroed first).  dq, dlambda
-    of sampled query rows and dk, dv of sampled source positions against the oracle."""
+    """Without decay every level carries full weight into dk and dv.  41, 65 and 547 tiles
+    of 128 tokens: the top slots (32; 64; 512 with 35 reader tiles) have more reader tiles
+    than one run takes, so their mirrored states are sums of several runs added with
+    atomics, and the tile counts are not multiples of 16 (the whole mirrored-state buffer
+    is zeroed first).  dq, dlambda of sampled query rows and dk, dv of sampled source
+    positions against the oracle."""
     L = (T - 1).bit_length() + 1
     cfg = W.FwdConfig("bwd_runs", 1, 2, T, 128, dv, 64, L, "bf16", False, "softplus", seed=T)
     x = W.make_fwd_inputs(cfg)
