@@ -58,6 +58,10 @@ def parse():
                         "on the decode workload, or on --decode-batch rows of it")
     p.add_argument("--decode-batch", type=int, default=None,
                    help="batch of --decode-only (default: the decode workload's 128)")
+    p.add_argument("--sweep-t", action="store_true",
+                   help="profiling aid: the pages' benchmark shape (B2, 48 heads sharing one "
+                        "q/k, d_v 64, d_k 128, C64) over T = 1K..128K: forward, backward and "
+                        "training step, one JSON line")
     return p.parse_args()
 
 
@@ -809,6 +813,30 @@ def measure_benchmark_shape(LL, cfg, dev, flush, peaks, reps=10):
                          "algorithmic_flops": fflops}}
 
 
+def run_sweep():
+    """The benchmark shape's forward, backward (with its recompute) and training step
+    (forward keeping its workspace, then the backward reading it) over the sequence lengths
+    of the pages' kernel benchmark, L = bit_length(T - 1) + 1; medians of a few calls, L2
+    flushed before each."""
+    import log_linear_attention_fwd_gb300 as LL
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+    base = W.FWD_CONFIGS["mva_B2H48_T16384"]
+    rows = []
+    for T in (1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072):
+        cfg = base.with_(name=f"mva_B2H48_T{T}", T=T, L=(T - 1).bit_length() + 1)
+        r = measure_benchmark_shape(LL, cfg, dev, flush, peaks, reps=5)
+        rows.append({"T": T, "L": cfg.L, "fwd_us": r["fwd_us"], "bwd_us": r["backward"]["bwd_us"],
+                     "fwd_bwd_us": r["fwd_bwd_us"], "fwd_hbm_frac": r["roofline"]["frac"],
+                     "fwd_tensor_frac": r["roofline"]["tensor_frac"],
+                     "bwd_tensor_frac": r["backward"]["roofline"]["tensor_frac"]})
+        torch.cuda.empty_cache()
+    print(json.dumps({"mode": "sweep-t", "workload": "B2 H48 (q/k heads 1) dk=128 dv=64 C64 bf16, "
+                      "Mamba-2 decay, synthetic", "peak_source": peaks["src"], "rows": rows}))
+
+
 def measure_e2e(LL, cfg, x, dev, ws, args):
     """Forward through the public API with inputs in pinned host memory: every step copies
     its inputs to the device, runs loglinear_fwd and copies the output back.
@@ -972,6 +1000,9 @@ def run_decode_only(args):
 
 def main():
     args = parse()
+    if args.sweep_t:
+        run_sweep()
+        return
     if args.fwd_only or args.bwd_only:
         run_one_pass(args, backward=args.bwd_only)
         return
