@@ -822,14 +822,13 @@ BwdWorkspace bwd_workspace_layout(int64_t B, int64_t T, int64_t H, int64_t Hqk, 
   w.off_dcq = up(w.off_dkh + qk_rows * dk * sizeof(float));
   w.off_dck = up(w.off_dcq + rows * sizeof(float));
   w.off_scan = up(w.off_dck + rows * sizeof(float));
-  w.off_fwd = w.off_out = 0;
+  w.off_fwd = 0;
   w.fwd = FwdWorkspace{};
   w.total = up(w.off_scan + (size_t)(B * H) * (size_t)((T + 1023) / 1024 + 1) * sizeof(float));
-  if (n_tc > 0) {
+  if (n_tc > 0) {  // the states-only forward's workspace (it writes no output)
     w.fwd = fwd_workspace_layout(B, H, n_tc, dk, dv, 2);
     w.off_fwd = w.total;
-    w.off_out = up(w.off_fwd + w.fwd.total);
-    w.total = up(w.off_out + rows * dv * 2);
+    w.total = up(w.off_fwd + w.fwd.total);
   }
   return w;
 }

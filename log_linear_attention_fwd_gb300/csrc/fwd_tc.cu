@@ -818,9 +818,12 @@ cudaError_t launch_tc_forward(const FwdArgs& a, int out_dtype, cudaStream_t s, S
   if (!make_tokens_map_strided(&tmQ, a.q, a.B, a.T, a.Hqk, kD, a.sq) ||
       !make_tokens_map_strided(&tmK, a.k, a.B, a.T, a.Hqk, kD, a.sk) ||
       !make_tokens_map_strided(&tmV, a.v, a.B, a.T, a.H, dv, a.sv) ||
-      !make_tokens_map_strided(&tmOut, a.out, a.B, a.T, a.H, dv, a.so) ||
       !make_rows_map(&tmU, a.U, rows, dv) ||
       !make_rows_map(&tmNode, a.nodes, rows, dv))
+    return cudaErrorInvalidValue;
+  if (states_only)
+    tmOut = tmV;  // not used: the states-only form writes no output (a.out may be null)
+  else if (!make_tokens_map_strided(&tmOut, a.out, a.B, a.T, a.H, dv, a.so))
     return cudaErrorInvalidValue;
   TcParams p;
   p.B = a.B; p.T = a.T; p.H = a.H; p.L = a.L; p.N = a.N; p.hg = a.hg;

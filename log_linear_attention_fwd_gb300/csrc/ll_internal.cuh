@@ -159,7 +159,7 @@ struct BwdArgs {
 };
 struct BwdWorkspace {
   size_t off_U, off_nodes, off_lg, off_dqh, off_dkh, off_dcq, off_dck, off_scan;
-  size_t off_fwd, off_out;  // tensor-core dQ only: a forward's workspace and its output
+  size_t off_fwd;  // tensor cores only: the workspace of the states-only forward
   FwdWorkspace fwd;         // that forward workspace's own layout (offsets from off_fwd)
   size_t total;
 };

@@ -589,7 +589,7 @@ int loglinear_bwd(const void* q, const void* k, const void* v, const float* log_
     // the states: those a forward call left in its own workspace, else a forward here
     char* fw = fwd_workspace ? static_cast<char*>(const_cast<void*>(fwd_workspace))
                              : ws + w.off_fwd;
-    f.out = ws + w.off_out;
+    f.out = nullptr;  // the states-only forward writes no output
     f.U = fw + w.fwd.off_U;
     f.nodes = fw + w.fwd.off_nodes;
     f.lg = reinterpret_cast<float*>(fw + w.fwd.off_lg);

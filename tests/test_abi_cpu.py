@@ -264,10 +264,11 @@ def test_bwd_validation_codes(L):
     sz = L.bwd_workspace_size(1, 64, 2, 2, 16, 16, 7, L.LL_F32, L.LL_F32)
     assert sz >= 2 * (1 * 2 * 2 * 16 * 16 * 4) + 2 * 64 * 2 * 16 * 4   # states + per-head dq, dk
     # the tensor-core path: fp32 mirrored states and a forward's bf16 states on the eight
-    # 128-token tiles, an output scratch, and with shared q/k one fp32 dq and dk per q/k head
+    # 128-token tiles (its states-only form writes no output, so there is no output
+    # scratch), and with shared q/k one fp32 dq and dk per q/k head
     tc = L.bwd_workspace_size(1, 1000, 2, 2, 128, 64, 11, L.LL_BF16, L.LL_BF16, "tc")
     st = 2 * 8 * 128 * 64
-    assert tc >= st * 4 + 2 * st * 2 + 1000 * 2 * 64 * 2
+    assert st * 4 + 2 * st * 2 <= tc < st * 4 + 2 * st * 2 + 1000 * 2 * 64 * 2
     tc1 = L.bwd_workspace_size(1, 1000, 2, 1, 128, 64, 11, L.LL_BF16, L.LL_BF16, "tc")
     assert tc1 >= tc + 2 * 1000 * 1 * 128 * 4
     assert L.bwd_workspace_size(1, 1000, 2, 2, 128, 64, 11, L.LL_BF16, L.LL_BF16) == tc
