@@ -1145,7 +1145,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // whose bit z - log2(g) is set.  The grid takes the runs level by level from the highest
 // (the longest runs first), the (b, h) innermost.
 
-constexpr int kRunLog = 4;
+constexpr int kRunLog = 5;
 
 // How many q in [0, M) have bit b set.
 __host__ __device__ inline int64_t count_with_bit(int64_t M, int b) {
@@ -1279,13 +1279,19 @@ __global__ void __launch_bounds__(kThreadsB, 2)
   bool ok = true;
   float D = 0.f;
   uint32_t ph = 0;
+  // row r's log a and lambda of a reader tile (loaded one reader ahead)
+  auto row_in = [&](int jj, float& la_o, float& lam_o, float& lg_o) {
+    const int tt0 = jj * kTile;
+    const bool live = r < min(kTile, p.T - tt0);
+    const int64_t rw = ((int64_t)b * p.T + tt0 + r) * p.H + h;
+    la_o = (hh == 0 && p.log_a && live) ? p.log_a[rw] : 0.f;
+    lam_o = live ? p.lam[rw * p.L + lam_l] : 0.f;
+    lg_o = p.lgu[bh * p.N + jj];
+  };
+  float la_n, lam_n, lg_n;
+  row_in(s0, la_n, lam_n, lg_n);
   for (int j = s0; j < s1; ++j, ph ^= 1) {
-    const int t0 = j * kTile;
-    const int n = min(kTile, p.T - t0);
-    const bool row_live = r < n;
-    const int64_t row = ((int64_t)b * p.T + t0 + r) * p.H + h;
-    const float la = (hh == 0 && p.log_a && row_live) ? p.log_a[row] : 0.f;
-    const float lam = row_live ? p.lam[row * p.L + lam_l] : 0.f;
+    const float la = la_n, lam = lam_n, lgj = lg_n;
     const float cs_scan = block_scan256(la, red);  // threads 0..127 hold row prefixes
     if (hh == 0) cs_s[r] = cs_scan;
     bool landed = true;
@@ -1296,7 +1302,8 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     ok = __syncthreads_and(ok && landed);
     if (!ok) break;
     if (j == s0) D = d0_s[0];
-    const float w = row_live ? __expf(cs_s[r] + D) * lam : 0.f;
+    const float w = __expf(cs_s[r] + D) * lam;  // lam = 0 on rows past T
+    if (j + 1 < s1) row_in(j + 1, la_n, lam_n, lg_n);
     // rows of Q scaled by w: the high part in place, the residual into Lb
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
@@ -1339,7 +1346,7 @@ __global__ void __launch_bounds__(kThreadsB, 2)
       }
     }
     __syncwarp();
-    D += p.lgu[bh * p.N + j];
+    D += lgj;
   }
   ok = __syncthreads_and(ok);
   tc_fence_after();

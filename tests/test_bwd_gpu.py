@@ -187,11 +187,12 @@ def test_bwd_tc_full_size_sampled(LL):
 @pytest.mark.parametrize("T,dv", [(5125, 64), (8269, 128), (70000, 64)])
 def test_bwd_tc_long_mirrored_runs_no_decay(LL, T, dv):
     """Without decay every level carries full weight into dk and dv.  41, 65 and 547 tiles
-    of 128 tokens: the top slots (32; 64; 512 with 35 reader tiles) have more reader tiles
-    than one run takes, so their mirrored states are sums of several runs added with
-    atomics, and the tile counts are not multiples of 16 (the whole mirrored-state buffer
-    is zeroed first).  dq, dlambda of sampled query rows and dk, dv of sampled source
-    positions against the oracle."""
+    of 128 tokens: the top slots (32 with 9 reader tiles, one run, stored; 64 and 512,
+    levels whose slots can have more readers than one run takes, added with atomics into
+    slots zeroed first; 512 has 35 readers, two runs) at tile counts that are not
+    multiples of the zeroing period (the whole mirrored-state buffer is zeroed).  dq,
+    dlambda of sampled query rows and dk, dv of sampled source positions against the
+    oracle."""
     L = (T - 1).bit_length() + 1
     cfg = W.FwdConfig("bwd_runs", 1, 2, T, 128, dv, 64, L, "bf16", False, "softplus", seed=T)
     x = W.make_fwd_inputs(cfg)
