@@ -321,12 +321,14 @@ LL_API int loglinear_gdn_fwd_chunked(const void* q, const void* k, const void* v
  * argument: the gradients do not depend on it.  1 <= dk, dv <= 128, L <= 64.  All
  * outputs are fully overwritten.
  * path: LL_PATH_TC computes dq, dk, dv and dlambda on the tensor cores (bf16 inputs and
- *   gradients, dk = 128, dv in {64, 128}; q, k, v, dout, dq, dk, dv 16-byte aligned): a tensor-core
- *   forward over the same inputs publishes its block states into the workspace, then
- *   128-token tiles take dQ and dlambda from them with tcgen05; the mirrored states of
- *   later tiles that dk and dv read are accumulated in fp32 on CUDA cores, then dK and dV
- *   are formed per 128-token tile with tcgen05.  These carry the bf16 roundings of P, P'
- *   and of the states.  LL_PATH_SIMT computes everything on CUDA cores in fp32.
+ *   gradients, dk = 128, dv in {64, 128}; q, k, v, dout, dq, dk, dv 16-byte aligned): the
+ *   tensor-core forward, in a form that writes no output, publishes its block states into
+ *   the workspace; 128-token tiles take dQ and dlambda from them with tcgen05; the
+ *   mirrored states of later tiles that dk and dv read are summed per Fenwick slot with
+ *   tcgen05 (fp32 accumulation, the scaled q split into a bf16 high part and residual),
+ *   then dK and dV are formed per 128-token tile with tcgen05.  These carry the bf16
+ *   roundings of P, P' and of the states.  LL_PATH_SIMT computes everything on CUDA cores
+ *   in fp32.
  *   LL_PATH_AUTO takes the tensor cores when they apply.  The workspace size depends on
  *   the path.
  * fwd_workspace: NULL, or, on the tensor-core path, the workspace of a loglinear_fwd call
