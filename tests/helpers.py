@@ -42,3 +42,12 @@ def per_head_qk(x):
     for n in ("q", "k"):
         y[n] = x[n].repeat_interleave(H // G, dim=2).contiguous()
     return y
+
+
+def one_head(x, b, h):
+    """The inputs of value head h of batch b alone (B = H = 1), with the q/k of its group:
+    input marshalling for the oracle, one head at a time."""
+    hq = h // (x["v"].shape[2] // x["q"].shape[2])
+    sl = lambda t, j: None if t is None else t[b:b + 1, :, j:j + 1].contiguous()
+    return {"q": sl(x["q"], hq), "k": sl(x["k"], hq), "v": sl(x["v"], h),
+            "log_a": sl(x["log_a"], h), "lam": sl(x["lam"], h)}

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.helpers import TOL_BF16, cuda, per_head_qk, rel_l2
+from tests.helpers import TOL_BF16, cuda, one_head, per_head_qk, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -212,6 +212,37 @@ def test_bwd_tc_long_mirrored_runs_no_decay(LL, T, dv):
                 "v": rel_l2(got[2][b, cols, h].cpu(), want["v"][i])}
         print(f"bwd tc runs T={T} dv={dv} head {h}: " + " ".join(f"{k}={e:.2e}" for k, e in errs.items()))
         assert all(e <= TOL_BF16 for e in errs.values()), errs
+
+
+def test_bwd_tc_benchmark_shape_sampled(LL):
+    """The pages' benchmark shape as the bench times it (B2, 48 heads sharing one q/k,
+    d_k 128, d_v 64, T 16384, bf16) on the tensor-core path.  dq and dk of the shared q/k
+    head are sums over the 48 heads: the oracle evaluates each head alone at sampled rows
+    and columns of batch 0 and adds them up; dv and dlambda on three of the heads."""
+    cfg = W.FWD_CONFIGS["mva_B2H48_T16384"]
+    x = W.make_fwd_inputs(cfg)
+    dout = _dout(cfg, 11)
+    d = cuda(x)
+    got = LL.loglinear_bwd(d["q"], d["k"], d["v"], d["log_a"], d["lam"], dout.cuda(), path="tc")
+    torch.cuda.synchronize()
+    assert LL.device_error() == 0
+    rows, cols = _positions(cfg.T, 8, 5), _positions(cfg.T, 8, 6)
+    dq = np.zeros((len(rows), cfg.dk))
+    dk = np.zeros((len(cols), cfg.dk))
+    errs = {}
+    for h in range(cfg.H):
+        one = one_head(x, 0, h)
+        w = oracle.backward_sampled(one["q"], one["k"], one["v"], one["log_a"], one["lam"],
+                                    dout[0:1, :, h:h + 1].contiguous(), rows, cols, [(0, 0)])
+        dq += w["q"][0]
+        dk += w["k"][0]
+        if h in (0, 23, 47):
+            errs[f"v{h}"] = rel_l2(got[2][0, cols, h].cpu(), w["v"][0])
+            errs[f"lam{h}"] = rel_l2(got[4][0, rows, h].cpu(), w["lam"][0])
+    errs["q"] = rel_l2(got[0][0, rows, 0].cpu(), dq)
+    errs["k"] = rel_l2(got[1][0, cols, 0].cpu(), dk)
+    print("bwd tc benchmark shape: " + " ".join(f"{k}={e:.2e}" for k, e in errs.items()))
+    assert all(e <= TOL_BF16 for e in errs.values()), errs
 
 
 @pytest.mark.parametrize("dv,Hqk", [(128, 0), (64, 1)])

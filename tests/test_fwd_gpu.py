@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.helpers import TOL_BF16, TOL_F32, cuda, max_abs, per_head_qk, rel_l2, tol_for
+from tests.helpers import TOL_BF16, TOL_F32, cuda, max_abs, one_head, per_head_qk, rel_l2, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -290,6 +290,22 @@ def test_tc_repeated_calls_same_workspace(LL):
 
 
 # ------------------------------------------------------------------ shared q/k heads
+
+
+def test_benchmark_shape_full_size_sampled(LL):
+    """The pages' benchmark shape as the bench times it (B2, 48 heads sharing one q/k,
+    d_k 128, d_v 64, T 16384, bf16) on the tensor-core path: sampled rows of six heads
+    against the oracle's per-head definition."""
+    cfg = W.FWD_CONFIGS["mva_B2H48_T16384"]
+    x = W.make_fwd_inputs(cfg)
+    got = run(LL, x, cfg.C, path="tc")
+    assert LL.device_error() == 0
+    rows = _sample_rows(cfg.T, 48, 5)
+    for b, h in [(0, 0), (0, 17), (0, 47), (1, 5), (1, 30), (1, 47)]:
+        want = oracle_fwd(one_head(x, b, h), rows=rows, heads=[(0, 0)])
+        err = rel_l2(got[b, rows, h], want[0, rows, 0])
+        print(f"benchmark shape b={b} h={h}: rel_l2(sampled rows)={err:.3e}")
+        assert err <= TOL_BF16
 
 
 @pytest.mark.parametrize("path,H,Hqk,dk,dv,T,dtype", [
