@@ -74,6 +74,37 @@ def test_prefill_state_tc(LL, T, dv, Hqk):
     print(f"tc T={T}: state rel_l2={err:.2e}")
 
 
+@pytest.mark.parametrize("decay", [True, False])
+def test_prefill_state_tc_headline_shape(LL, decay):
+    """The headline prompt (B1 H16 T16384 dk=dv=128 bf16) on the tensor-core path: at
+    t = 16383 every one of the 15 levels holds a bucket (levels 8-14 are the forward's
+    block states decayed to t).  Two heads against the bucket definition, level by level;
+    without decay the top levels carry full weight."""
+    cfg = W.FWD_CONFIGS["mamba2_T16384"].with_(decay=decay, seed=31)
+    x = W.make_fwd_inputs(cfg)
+    d = cuda(x)
+    out, state = LL.loglinear_prefill(d["q"], d["k"], d["v"], d["log_a"], d["lam"], cfg.C,
+                                      path="tc")
+    torch.cuda.synchronize()
+    assert LL.device_error() == 0
+    T = cfg.T
+    for h in (0, cfg.H - 1):
+        la = None if x["log_a"] is None else x["log_a"][0, :, h]
+        want = oracle.states_from_buckets(x["k"][0, :, h], x["v"][0, :, h], la, T - 1, cfg.L)
+        got = state[0, h].cpu()
+        errs = []
+        for lv in range(cfg.L):
+            if np.linalg.norm(want[lv]) > 1e-30:
+                errs.append(rel_l2(got[lv], want[lv]))
+                assert errs[-1] <= TOL_BF16, (h, lv, errs[-1])
+            else:  # decayed below fp32's range: the state rounds to zero there too
+                assert decay and float(got[lv].abs().max()) <= 1e-30, (h, lv)
+        if not decay:
+            assert len(errs) == cfg.L
+        print(f"tc prefill T={T} decay={decay} head {h}: per-level rel_l2 " +
+              " ".join(f"{e:.1e}" for e in errs))
+
+
 @pytest.mark.parametrize("path,T,dk,dv,dtype,H,Hqk", [("simt", 300, 16, 16, "f32", 2, 2),
                                                       ("tc", 1151, 128, 128, "bf16", 2, 2),
                                                       ("tc", 1151, 128, 64, "bf16", 2, 2),
