@@ -123,6 +123,32 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
   const int dk = a.dk, dv = a.dv;
 
   // ---- the chunk's q, k, v (fp32, zero past n rows and past dk / dv columns), gates
+  if (sizeof(InT) == 2 && dk == kD && dv == kD &&
+      ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
+        reinterpret_cast<uintptr_t>(a.v)) & 15u) == 0) {  // aligned bf16 rows of 128: 8 values per load
+#pragma unroll 4
+    for (int i = tid; i < kC * (kD / 8); i += kThreads) {
+      const int t = i / (kD / 8), d8 = 8 * (i - t * (kD / 8));
+      const bool live = t < n;
+      const int64_t tq = ((int64_t)b * a.T + t0 + t) * Hqk + hq;
+      const int64_t tv = ((int64_t)b * a.T + t0 + t) * a.H + h;
+      const uint4 z4 = make_uint4(0, 0, 0, 0);
+      const uint4 uq = live ? *reinterpret_cast<const uint4*>(static_cast<const InT*>(a.q) + tq * dk + d8) : z4;
+      const uint4 uk = live ? *reinterpret_cast<const uint4*>(static_cast<const InT*>(a.k) + tq * dk + d8) : z4;
+      const uint4 uv = live ? *reinterpret_cast<const uint4*>(static_cast<const InT*>(a.v) + tv * dv + d8) : z4;
+      const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wk[4] = {uk.x, uk.y, uk.z, uk.w},
+                     wv[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[e]));
+        const float2 fk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wk[e]));
+        const float2 fv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
+        Qs[t * kLd + d8 + 2 * e] = fq.x; Qs[t * kLd + d8 + 2 * e + 1] = fq.y;
+        Ks[t * kLd + d8 + 2 * e] = fk.x; Ks[t * kLd + d8 + 2 * e + 1] = fk.y;
+        Vs[t * kLd + d8 + 2 * e] = fv.x; Vs[t * kLd + d8 + 2 * e + 1] = fv.y;
+      }
+    }
+  } else
 #pragma unroll 8
   for (int i = tid; i < kC * kD; i += kThreads) {
     const int t = i / kD, d = i - t * kD;

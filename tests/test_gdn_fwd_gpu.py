@@ -151,6 +151,7 @@ def _run_chunked(LL, x, out_dtype=torch.float32):
     (2, 3, 0, 37, 32, 16, "f32", True),       # one ragged chunk
     (1, 4, 1, 130, 64, 24, "f32", False),     # three chunks, the last ragged; shared q/k
     (1, 2, 2, 300, 128, 64, "bf16", True),
+    (1, 3, 1, 600, 128, 128, "bf16", True),   # bf16 rows of 128: 16-byte loads
     (1, 1, 1, 1000, 128, 128, "f32", True),   # 16 chunks: chunk levels 1..4
     (2, 2, 0, 77, 7, 3, "f32", True),         # odd d_k, d_v
     (1, 2, 0, 2100, 32, 32, "f32", False),    # 33 chunks without decay: every level weighs
@@ -167,6 +168,25 @@ def test_gdn_fwd_chunked_matches_recurrence(LL, B, H, Hqk, T, dk, dv, dtype, dec
     err = rel_l2(got, want)
     print(f"gdn chunked B{B} H{H} Hqk{Hqk} T{T} dk{dk} dv{dv} {dtype}: rel_l2={err:.2e}")
     assert err <= TOL_F32
+
+
+def test_gdn_fwd_chunked_unaligned_inputs(LL):
+    """q, k, v whose base addresses are 2 bytes off a 16-byte boundary take the kernel's
+    element-wise loads instead of its 16-byte ones; the output is the same."""
+    cfg = W.FwdConfig("gdn_chunk_u", 1, 2, 300, 128, 128, 64, 10, "bf16", True, "softplus", seed=9)
+    x = W.make_gdn_inputs(cfg)
+    want = _run_chunked(LL, x)
+    d = _dev(x)
+    off = {}
+    for n in ("q", "k", "v"):
+        buf = torch.empty(d[n].numel() + 1, dtype=d[n].dtype, device="cuda")
+        off[n] = buf[1:].view(d[n].shape)
+        off[n].copy_(d[n])
+        assert off[n].data_ptr() % 16 == 2
+    got = LL.loglinear_gdn_fwd_chunked(off["q"], off["k"], off["v"], d["log_a"], d["beta"],
+                                       d["lam"], out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(got.cpu(), want)
 
 
 def test_gdn_fwd_chunked_bf16_out_and_constant_lambda(LL):
