@@ -201,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
   __syncthreads();
   // ---- T = (I + A)^-1 (unit lower triangular) by forward substitution, one row at a time:
   // T[i][c] = [i == c] - sum_{k = c}^{i-1} A[i][k] T[k][c]; thread (c, part) sums a quarter
-  // of k for column c.
+  // of k for column c.  A column depends only on its own earlier rows, and its four
+  // threads are in one warp: a warp barrier orders each row before the next.
   {
     const int c = tid >> 2, part = tid & 3;
     for (int i = 0; i < kC; ++i) {
@@ -211,9 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(GdnChunkArgs a) 
       x += __shfl_xor_sync(0xffffffffu, x, 1);
       x += __shfl_xor_sync(0xffffffffu, x, 2);
       if (part == 0) Ts[i * kLdc + c] = c < i ? -x : (c == i ? 1.f : 0.f);
-      __syncthreads();
+      __syncwarp();
     }
   }
+  __syncthreads();
   // ---- W = Aqk T diag(beta), masked by lambda[t, level(t, s)] (s <= t) into W
   {
     float w[4][4];
