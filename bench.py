@@ -219,8 +219,8 @@ class NvmlClocks:
 class ClockSampler:
     """SM clocks and throttle reasons sampled during the run, with a marked window.
 
-    With NVML a background thread reads the clock every millisecond, so that a timed region
-    of 10-30 ms holds a few dozen samples; without it, nvidia-smi samples every 20 ms.
+    With NVML a background thread reads the clock every half millisecond, so that a timed
+    region of 10-30 ms holds a few dozen samples; without it, nvidia-smi samples every 20 ms.
     mark_start()/mark_end() bracket the timed region; stop() reports the median SM clock
     and the reasons seen over the samples inside it (and the sample counts)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -240,7 +240,7 @@ class ClockSampler:
     def start(self):
         try:
             self.nvml = NvmlClocks(self.idx)
-            self.source = "nvml, every 1 ms"
+            self.source = "nvml, every 0.5 ms"
             import threading
             self.stop_flag = threading.Event()
 
@@ -249,7 +249,7 @@ class ClockSampler:
                     mhz, w, rs = self.nvml.read()
                     names = [n for bit, n in NvmlClocks.REASONS.items() if rs & bit]
                     self.samples.append((time.perf_counter(), mhz, w, names))
-                    time.sleep(0.001)
+                    time.sleep(0.0005)
 
             self.thread = threading.Thread(target=loop, daemon=True)
             self.thread.start()
